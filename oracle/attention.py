@@ -1,0 +1,84 @@
+"""Decode attention over the compressed cache (test infrastructure only).
+
+* Inner-product estimate, 甲子光年 article §2 第二階段 (the stage-1 inner
+  product is biased, the 1-bit QJL sketch of the residual makes the sum
+  unbiased) and intelliparadigm.com §2.1.2 / §2.2 theorem 2 (the estimate's
+  expectation equals the true inner product).  Reading: the asymmetric QJL
+  estimator -- the query is projected but not quantized --
+
+      <q, k> ~= <q, k_mse> + gamma * sqrt(pi/2) / m * <S q, 2 bits - 1>,
+
+  exactly unbiased because E[<g, q> sign(<g, r>)] = sqrt(2/pi) <q, r> / ||r||
+  for g ~ N(0, I).  The symmetric "C sign(Aq) sign(Ae)" form printed on the
+  intelliparadigm page cannot be unbiased (its mean is not linear in <q, e>)
+  and is not used.
+* Attention: scaled dot-product softmax over every cached token of the
+  sequence (a decode step sees its whole context), scale 1/sqrt(d) unless
+  given; values are the stage-1 reconstructions n_v R^T c_v[code].  The query
+  is not compressed (seo-farm page §4).  This oracle works in the original
+  space; rotation invariance (seo-farm §2, R^T R = I) is what lets a kernel
+  work in the rotated space instead.
+"""
+import math
+
+import numpy as np
+
+from . import packing
+from .quantize import reconstruct_mse
+
+
+def qjl_estimate(query, gamma32, signs, proj):
+    """gamma * sqrt(pi/2) / m * <S q, 2 s - 1> for every cached token."""
+    proj = np.asarray(proj, dtype=np.float64)
+    m = proj.shape[0]
+    sq = proj @ np.asarray(query, dtype=np.float64)
+    pm = 2.0 * np.asarray(signs, dtype=np.float64) - 1.0
+    return gamma32.astype(np.float64) * math.sqrt(math.pi / 2.0) / m * (pm @ sq)
+
+
+def attend(query, khat, qjl_term, vhat, scale):
+    """softmax(scale * (khat q + qjl_term)) @ vhat, all fp64."""
+    logits = scale * (np.asarray(khat) @ np.asarray(query, dtype=np.float64) + qjl_term)
+    logits = logits - np.max(logits)
+    weights = np.exp(logits)
+    weights /= np.sum(weights)
+    return weights @ np.asarray(vhat)
+
+
+def read_sequence(cache, table_row, length, head, block_size):
+    """Rows of every cache field for tokens 0..length-1 of one sequence/head."""
+    n_kv = cache["k_norm"].shape[1]
+    slots = np.arange(length, dtype=np.int64)
+    blocks = np.asarray(table_row, dtype=np.int64)[slots // block_size]
+    rows = (blocks * n_kv + head) * block_size + slots % block_size
+    out = {}
+    for name, arr in cache.items():
+        flat = arr.reshape(arr.shape[0] * arr.shape[1] * arr.shape[2], -1)
+        out[name] = flat[rows]
+    return out
+
+
+def decode_attention(query, cache, table_row, length, kv_head, book, scale=None):
+    """Output of one query head of one sequence, from the packed cache.
+
+    ``book`` holds the oracle's own R, S, levels and bit widths:
+    keys ``rot``, ``proj``, ``k_levels``, ``v_levels``, ``k_bits``, ``v_bits``.
+    ``cache`` maps field names to arrays [num_blocks][n_kv][block_size][...]:
+    ``k_codes``, ``k_qjl`` (may be absent when QJL is off), ``k_norm``,
+    ``k_rnorm``, ``v_codes``, ``v_norm``.
+    """
+    d = book["rot"].shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    block_size = cache["k_norm"].shape[2]
+    rows = read_sequence(cache, table_row, length, kv_head, block_size)
+    k_codes = packing.unpack_planes(rows["k_codes"], book["k_bits"], d)
+    khat = reconstruct_mse(rows["k_norm"].reshape(-1), k_codes, book["rot"], book["k_levels"])
+    if "k_qjl" in rows and book["proj"].shape[0] > 0:
+        signs = packing.unpack_signs(rows["k_qjl"], book["proj"].shape[0])
+        corr = qjl_estimate(query, rows["k_rnorm"].reshape(-1), signs, book["proj"])
+    else:
+        corr = np.zeros(length)
+    v_codes = packing.unpack_planes(rows["v_codes"], book["v_bits"], d)
+    vhat = reconstruct_mse(rows["v_norm"].reshape(-1), v_codes, book["rot"], book["v_levels"])
+    return attend(query, khat, corr, vhat, scale), float(np.max(np.linalg.norm(vhat, axis=1)))

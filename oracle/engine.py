@@ -1,0 +1,113 @@
+"""Whole-path oracle: codebook build, quantize-append into a paged cache, and
+decode attention (test infrastructure only).
+
+Bit split, 甲子光年 article §2 第二階段: a key budget of b bits per
+coordinate is b-1 MSE bits plus the 1-bit QJL sketch; values use all their
+bits for the MSE code and carry no sketch.  One R and one S serve keys,
+values and every head (a reading; the pages draw one rotation per quantizer).
+"""
+import functools
+
+import numpy as np
+
+from . import attention, codebook, packing, quantize, rotation
+
+
+@functools.lru_cache(maxsize=None)
+def _levels(d, bits):
+    return codebook.lloyd_max(d, bits)
+
+
+@functools.lru_cache(maxsize=None)
+def _matrices(d, m, seed):
+    return rotation.rotation_and_projection(d, m, seed)
+
+
+def build(d=128, k_bits=3, v_bits=3, qjl_m=128, seed=0):
+    """The oracle's own R, S and codebooks for one configuration."""
+    k_mse_bits = k_bits - 1 if qjl_m else k_bits
+    rot, proj = _matrices(d, qjl_m, seed)
+    k_levels, k_bounds = _levels(d, k_mse_bits)
+    v_levels, v_bounds = _levels(d, v_bits)
+    return {
+        "d": d, "qjl_m": qjl_m, "rot": rot, "proj": proj,
+        "k_bits": k_mse_bits, "v_bits": v_bits,
+        "k_levels": k_levels, "k_bounds": k_bounds,
+        "v_levels": v_levels, "v_bounds": v_bounds,
+    }
+
+
+def encode_keys(x, book):
+    """Key rows: dict of packed codes, sign bits, norm, residual norm, plus the
+    fp64 intermediates (unit rotated y, projected residual z) for acceptance."""
+    norm, y, codes = quantize.encode_mse(x, book["rot"], book["k_bounds"])
+    out = {"k_codes": packing.pack_planes(codes, book["k_bits"]), "k_norm": norm,
+           "codes": codes, "y": y}
+    if book["qjl_m"]:
+        gamma, signs, z = quantize.encode_qjl(x, norm, codes, book["rot"], book["k_levels"], book["proj"])
+        out.update({"k_qjl": packing.pack_signs(signs), "k_rnorm": gamma, "signs": signs, "z": z})
+    return out
+
+
+def encode_values(x, book):
+    """Value rows: packed codes and norm (plus fp64 intermediates)."""
+    norm, y, codes = quantize.encode_mse(x, book["rot"], book["v_bounds"])
+    return {"v_codes": packing.pack_planes(codes, book["v_bits"]), "v_norm": norm,
+            "codes": codes, "y": y}
+
+
+def field_bytes(book):
+    """Bytes per (token, head) of each cache field."""
+    d = book["d"]
+    out = {"k_codes": book["k_bits"] * d // 8, "k_norm": 4,
+           "v_codes": book["v_bits"] * d // 8, "v_norm": 4}
+    if book["qjl_m"]:
+        out["k_qjl"] = book["qjl_m"] // 8
+        out["k_rnorm"] = 4
+    return out
+
+
+def empty_cache(book, num_blocks, n_kv_heads, block_size):
+    cache = {}
+    for name, nbytes in field_bytes(book).items():
+        if name.endswith("norm"):
+            cache[name] = np.zeros((num_blocks, n_kv_heads, block_size), dtype=np.float32)
+        else:
+            cache[name] = np.zeros((num_blocks, n_kv_heads, block_size, nbytes), dtype=np.uint8)
+    return cache
+
+
+def append(cache, book, k, v, slots):
+    """Quantize k, v [n_tokens][n_kv][d] and write them at ``slots`` (one slot
+    per token; negative slots are skipped)."""
+    num_blocks, n_kv, block_size = cache["k_norm"].shape
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n_tok = k.shape[0]
+    keys = encode_keys(k.reshape(n_tok * n_kv, -1), book)
+    vals = encode_values(v.reshape(n_tok * n_kv, -1), book)
+    for name in field_bytes(book):
+        src = (keys if name.startswith("k_") else vals)[name]
+        src = src.reshape(n_tok, n_kv, *src.shape[1:])
+        flat = cache[name].reshape(num_blocks * n_kv * block_size, *cache[name].shape[3:])
+        for t in range(n_tok):
+            if slots[t] < 0:
+                continue
+            for h in range(n_kv):
+                flat[packing.slot_index(slots[t], h, n_kv, block_size)] = src[t, h]
+    return keys, vals
+
+
+def decode(query, cache, block_table, context_lens, book, scale=None):
+    """out [B][Hq][d] (fp64) and the per-(seq, head) normaliser max_t ||v_hat_t||."""
+    query = np.asarray(query, dtype=np.float64)
+    batch, n_q, d = query.shape
+    n_kv = cache["k_norm"].shape[1]
+    group = n_q // n_kv
+    out = np.zeros((batch, n_q, d))
+    vmax = np.zeros((batch, n_q))
+    for b in range(batch):
+        for h in range(n_q):
+            out[b, h], vmax[b, h] = attention.decode_attention(
+                query[b, h], cache, block_table[b], int(context_lens[b]), h // group, book, scale)
+    return out, vmax
