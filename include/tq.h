@@ -1,0 +1,159 @@
+/*
+ * tq.h -- C ABI of the TurboQuant KV-cache engine (sm_103a).
+ *
+ * The method (TurboQuant, "Online Vector Quantization with Near-optimal
+ * Distortion Rate", as described by the 甲子光年 article on admirer.cn, §2):
+ *   stage 1 (§2 第一階段): keep the vector norm, rotate the unit vector with a
+ *     random orthogonal R, replace every rotated coordinate by the nearest level
+ *     of a Lloyd-Max codebook built once for the rotated-coordinate Beta law;
+ *   stage 2 (§2 第二階段): for keys, spend b-1 bits on stage 1 and one bit per
+ *     projected coordinate on QJL, sign(S * residual), plus the residual norm,
+ *     which makes the inner-product estimate unbiased.
+ * Decode attention runs directly on the packed cache (seo-farm page §4: the
+ * query is not compressed; attention reads the de-quantized cache), in the
+ * rotated space, with one back-rotation by R^T at the end (seo-farm page §2:
+ * R^T R = I leaves attention unchanged).
+ *
+ * Conventions shared by every entry point
+ * - All functions return tq_status; TQ_OK is 0.  Argument checks run on the
+ *   host before anything is launched; a rejected call launches nothing and
+ *   leaves every buffer untouched.
+ * - Device pointers are plain CUDA device addresses on the handle's device and
+ *   are owned by the caller (the library never frees them).  The only memory
+ *   the library owns is the handle's (R, S' = S R^T, codebooks, an error word).
+ * - Launches are asynchronous on the caller's stream (cudaStream_t passed as
+ *   void*; NULL is the legacy default stream).  No entry point synchronises
+ *   except tq_codebook_build, tq_codebook_destroy and tq_get_last_device_error.
+ * - Launch failures map to TQ_ERR_CUDA.  Bad indices met on the device (a slot
+ *   or block id outside the cache) never trap: the kernel skips that item and
+ *   records an error code readable with tq_get_last_device_error.
+ * - A handle is immutable after build and may be used from several streams.
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1, /* null pointer, bad size, inconsistent shapes      */
+  TQ_ERR_UNSUPPORTED = 2, /* valid but not built: d != 128, bits outside 1..4 */
+  TQ_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed             */
+  TQ_ERR_OOM = 4,         /* host or device allocation failed (build only)    */
+  TQ_ERR_WORKSPACE = 5,   /* decode workspace null or smaller than required   */
+  TQ_ERR_DEVICE = 6       /* a kernel met an invalid slot/block id (see below) */
+} tq_status;
+
+typedef enum { TQ_BF16 = 0, TQ_FP32 = 1 } tq_dtype;
+
+/* Configuration.  d: head dimension (128 only).  k_bits: total key bits per
+ * coordinate; with QJL on (qjl_m > 0) keys use k_bits-1 MSE bits + the 1-bit
+ * sketch, so k_bits is 2..5; with QJL off keys use k_bits MSE bits (1..4).
+ * v_bits: value MSE bits (1..4).  qjl_m: QJL projection rows (0 = off, or
+ * 128).  seed: seeds the SplitMix64 stream that draws R (Haar, via QR of a
+ * Gaussian matrix) and S.  block_size: tokens per cache block (> 0). */
+typedef struct {
+  int d;
+  int k_bits;
+  int v_bits;
+  int qjl_m;
+  uint64_t seed;
+  int block_size;
+} tq_config;
+
+typedef struct tq_codebook tq_codebook; /* opaque, library-owned */
+
+/* The compressed cache: caller-owned device arrays, each laid out as
+ * [num_blocks][n_kv_heads][block_size][item], item sizes from
+ * tq_cache_field_bytes.  Codes are bit-planes: plane p holds bit p of every
+ * code, coordinate j at bit j%8 of byte j/8 of the plane.  QJL bit k is bit
+ * k%8 of byte k/8, set when the k-th projected residual is > 0.  Norms are
+ * float32.  Every pointer must be 16-byte aligned; k_qjl/k_rnorm may be NULL
+ * when qjl_m == 0. */
+typedef struct {
+  void* k_codes;
+  void* k_qjl;
+  float* k_norm;
+  float* k_rnorm;
+  void* v_codes;
+  float* v_norm;
+  int num_blocks;
+  int n_kv_heads;
+  int block_size;
+} tq_cache_view;
+
+/* Build a handle: draws R and S, computes S' = S R^T and the Lloyd-Max
+ * codebooks in fp64 on the host, then uploads float32 copies (and bf16 hi/lo
+ * splits for the tensor-core rotation) to `device`.  device < 0 builds a
+ * host-only handle whose tables can be inspected but which the kernels
+ * reject.  Synchronous.  Ownership of *out passes to the caller, who frees it
+ * with tq_codebook_destroy. */
+tq_status tq_codebook_build(const tq_config* cfg, int device, tq_codebook** out);
+tq_status tq_codebook_destroy(tq_codebook* book);
+
+/* fp64 copies of the codebook: which = 0 keys, 1 values.  levels gets
+ * 2^bits ascending values, bounds the 2^bits - 1 midpoints (either may be
+ * NULL).  *bits (may be NULL) receives the MSE bit width of that codebook. */
+tq_status tq_codebook_levels(const tq_codebook* book, int which, double* levels, double* bounds,
+                             int* bits);
+
+/* fp64 copies of R (d x d, row-major, y = R x) and S (qjl_m x d, row-major);
+ * either may be NULL. */
+tq_status tq_codebook_matrices(const tq_codebook* book, double* R, double* S);
+
+/* Bytes per (token, head) item of the six cache fields, in the order
+ * k_codes, k_qjl, k_norm, k_rnorm, v_codes, v_norm (0 for absent fields). */
+tq_status tq_cache_field_bytes(const tq_codebook* book, size_t bytes_per_item[6]);
+
+/* Quantize-append (the write path).  k, v: device [n_tokens][n_kv_heads][d]
+ * in `dtype`, contiguous, 16-byte aligned; either may be NULL to skip that
+ * tensor.  slot_mapping: device int64 [n_tokens]; token t goes to slot
+ * slot_mapping[t] (block = slot / block_size, offset = slot % block_size);
+ * a negative slot skips the token; a slot >= num_blocks*block_size is skipped
+ * and recorded as a device error.  Writes every field of every (token, head).
+ * Asynchronous on `stream`. */
+tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void* v, tq_dtype dtype,
+                             int n_tokens, int n_kv_heads, const int64_t* slot_mapping,
+                             const tq_cache_view* cache, void* stream);
+
+/* Workspace bytes tq_decode_attention needs for this batch shape (the
+ * split-K partials and the rotated/projected queries).  max_context bounds
+ * every context_lens[b]. */
+size_t tq_decode_workspace_bytes(const tq_codebook* book, int batch, int n_q_heads, int max_context);
+
+/* Decode attention (the read path) for one new query token per sequence.
+ * q: device [batch][n_q_heads][d] in `dtype`.  Query head h reads KV head
+ * h / (n_q_heads / n_kv_heads).  block_table: device int32 [batch][max_blocks]
+ * of physical block ids, or NULL for the identity layout (sequence b owns
+ * blocks b*max_blocks .. b*max_blocks + max_blocks - 1).  context_lens: device
+ * int32 [batch], each in [0, max_context] and <= max_blocks*block_size; a
+ * zero-length sequence yields a zero output row.  scale: softmax scale, 0
+ * selects 1/sqrt(d).  out: device float32 [batch][n_q_heads][d].  workspace:
+ * device scratch of at least tq_decode_workspace_bytes(book, batch,
+ * n_q_heads, max_context) bytes, 256-byte aligned, not used by any concurrent
+ * call.  Asynchronous on `stream`. */
+tq_status tq_decode_attention(const tq_codebook* book, const void* q, tq_dtype dtype, int batch,
+                              int n_q_heads, int n_kv_heads, const tq_cache_view* cache,
+                              const int32_t* block_table, int max_blocks,
+                              const int32_t* context_lens, int max_context, float scale, float* out,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream`, then return (and clear) the first device-side error
+ * code recorded since the last call: 0 none, 1 slot out of range in
+ * quantize-append, 2 block id out of range in decode, 3 context length out of
+ * range in decode.  Returns TQ_ERR_DEVICE when *code != 0. */
+tq_status tq_get_last_device_error(const tq_codebook* book, void* stream, int* code);
+
+/* Static description of a status code. */
+const char* tq_status_string(tq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

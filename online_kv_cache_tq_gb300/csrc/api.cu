@@ -1,0 +1,358 @@
+// C ABI of the engine: handle lifetime, host-side argument checks, launches.
+#include <cmath>
+#include <cstddef>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "tq.h"
+#include "tq_internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (dev >= 0 && dev != prev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+void free_device(tq_codebook* b) {
+  cudaFree(b->d_R);
+  cudaFree(b->d_Rt);
+  cudaFree(b->d_Spt);
+  cudaFree(b->d_rot_tc);
+  cudaFree(b->d_tables);
+  cudaFree(b->d_error);
+  b->d_R = b->d_Rt = b->d_Spt = nullptr;
+  b->d_rot_tc = nullptr;
+  b->d_tables = nullptr;
+  b->d_error = nullptr;
+}
+
+template <typename T>
+cudaError_t upload(T** dst, const std::vector<T>& src) {
+  cudaError_t err = cudaMalloc(reinterpret_cast<void**>(dst), src.size() * sizeof(T));
+  if (err != cudaSuccess) return err;
+  return cudaMemcpy(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice);
+}
+
+uint16_t bf16_bits(float x) {
+  __nv_bfloat16 h = __float2bfloat16_rn(x);
+  uint16_t out;
+  std::memcpy(&out, &h, sizeof(out));
+  return out;
+}
+
+float bf16_value(uint16_t bits) {
+  uint32_t w = static_cast<uint32_t>(bits) << 16;
+  float out;
+  std::memcpy(&out, &w, sizeof(out));
+  return out;
+}
+
+tq_status upload_tables(tq_codebook* b) {
+  const int d = b->cfg.d;
+  const int m = b->cfg.qjl_m;
+  const tq::HostTables& h = b->host;
+  std::vector<float> R(d * d), Rt(d * d), Spt(d * d, 0.f);
+  for (int i = 0; i < d; ++i) {
+    for (int j = 0; j < d; ++j) {
+      R[i * d + j] = static_cast<float>(h.R[i * d + j]);
+      Rt[j * d + i] = static_cast<float>(h.R[i * d + j]);
+    }
+  }
+  for (int k = 0; k < m; ++k)
+    for (int j = 0; j < d; ++j) Spt[j * d + k] = static_cast<float>(h.Sp[k * d + j]);
+  // bf16 hi/lo images of R and S' (row-major, [out][in]) for the tensor-core
+  // quantizer: W = hi + lo with hi = bf16(W), lo = bf16(W - hi).
+  std::vector<uint16_t> tc(4 * d * d, 0);
+  for (int i = 0; i < d * d; ++i) {
+    const float r = static_cast<float>(h.R[i]);
+    tc[i] = bf16_bits(r);
+    tc[d * d + i] = bf16_bits(r - bf16_value(tc[i]));
+    const float s = i < m * d ? static_cast<float>(h.Sp[i]) : 0.f;
+    tc[2 * d * d + i] = bf16_bits(s);
+    tc[3 * d * d + i] = bf16_bits(s - bf16_value(tc[2 * d * d + i]));
+  }
+  tq::DeviceTables t;
+  for (int i = 0; i < tq::kMaxLevels; ++i) {
+    t.k_levels[i] = i < static_cast<int>(h.k_levels.size()) ? static_cast<float>(h.k_levels[i]) : 0.f;
+    t.v_levels[i] = i < static_cast<int>(h.v_levels.size()) ? static_cast<float>(h.v_levels[i]) : 0.f;
+    t.k_bounds[i] = i < static_cast<int>(h.k_bounds.size()) ? static_cast<float>(h.k_bounds[i]) : INFINITY;
+    t.v_bounds[i] = i < static_cast<int>(h.v_bounds.size()) ? static_cast<float>(h.v_bounds[i]) : INFINITY;
+  }
+  std::vector<tq::DeviceTables> tv(1, t);
+  std::vector<int> zero(1, 0);
+  cudaError_t err = upload(&b->d_R, R);
+  if (err == cudaSuccess) err = upload(&b->d_Rt, Rt);
+  if (err == cudaSuccess) err = upload(&b->d_Spt, Spt);
+  if (err == cudaSuccess) err = upload(&b->d_rot_tc, tc);
+  if (err == cudaSuccess) err = upload(&b->d_tables, tv);
+  if (err == cudaSuccess) err = upload(&b->d_error, zero);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&b->num_sms, cudaDevAttrMultiProcessorCount, b->device);
+  if (err != cudaSuccess) {
+    free_device(b);
+    return err == cudaErrorMemoryAllocation ? TQ_ERR_OOM : TQ_ERR_CUDA;
+  }
+  return TQ_OK;
+}
+
+bool valid_device_handle(const tq_codebook* b) { return b != nullptr && b->device >= 0 && b->d_tables != nullptr; }
+
+bool valid_cache(const tq_codebook* b, const tq_cache_view* c) {
+  if (c == nullptr || c->num_blocks <= 0 || c->n_kv_heads <= 0 || c->block_size != b->cfg.block_size) return false;
+  if (!c->k_codes || !c->k_norm || !c->v_codes || !c->v_norm) return false;
+  if (!aligned16(c->k_codes) || !aligned16(c->k_norm) || !aligned16(c->v_codes) || !aligned16(c->v_norm)) return false;
+  if (b->cfg.qjl_m > 0) {
+    if (!c->k_qjl || !c->k_rnorm || !aligned16(c->k_qjl) || !aligned16(c->k_rnorm)) return false;
+  }
+  return true;
+}
+
+// Device address of one array inside the handle's DeviceTables.
+const float* table_field(const tq_codebook* b, size_t offset) {
+  return reinterpret_cast<const float*>(reinterpret_cast<const char*>(b->d_tables) + offset);
+}
+
+constexpr size_t kWsAlign = 256;
+size_t round_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+int max_chunks_for(int max_context) { return (max_context + tq::kChunk - 1) / tq::kChunk; }
+
+}  // namespace
+
+extern "C" {
+
+tq_status tq_codebook_build(const tq_config* cfg, int device, tq_codebook** out) {
+  if (cfg == nullptr || out == nullptr) return TQ_ERR_INVALID_ARG;
+  *out = nullptr;
+  const bool host_only = device < 0;
+  if (cfg->d <= 0 || cfg->d % 8 != 0 || cfg->d > 1024 || cfg->block_size <= 0) return TQ_ERR_INVALID_ARG;
+  if (cfg->qjl_m < 0 || cfg->qjl_m % 8 != 0 || cfg->qjl_m > 1024) return TQ_ERR_INVALID_ARG;
+  const int k_mse = cfg->qjl_m > 0 ? cfg->k_bits - 1 : cfg->k_bits;
+  if (k_mse < 1 || k_mse > 4 || cfg->v_bits < 1 || cfg->v_bits > 4) return TQ_ERR_UNSUPPORTED;
+  if (!host_only && (cfg->d != tq::kDim || (cfg->qjl_m != 0 && cfg->qjl_m != tq::kDim))) return TQ_ERR_UNSUPPORTED;
+  tq_codebook* b = new (std::nothrow) tq_codebook();
+  if (b == nullptr) return TQ_ERR_OOM;
+  b->cfg = *cfg;
+  b->device = host_only ? -1 : device;
+  b->k_mse_bits = k_mse;
+  b->v_bits = cfg->v_bits;
+  try {
+    tq::build_host_tables(cfg->d, cfg->qjl_m, cfg->seed, k_mse, cfg->v_bits, &b->host);
+  } catch (const std::bad_alloc&) {
+    delete b;
+    return TQ_ERR_OOM;
+  }
+  if (!host_only) {
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || device >= count) {
+      delete b;
+      return TQ_ERR_CUDA;
+    }
+    DeviceGuard guard(device);
+    tq_status st = upload_tables(b);
+    if (st != TQ_OK) {
+      delete b;
+      return st;
+    }
+  }
+  *out = b;
+  return TQ_OK;
+}
+
+tq_status tq_codebook_destroy(tq_codebook* book) {
+  if (book == nullptr) return TQ_ERR_INVALID_ARG;
+  if (book->device >= 0) {
+    DeviceGuard guard(book->device);
+    cudaDeviceSynchronize();
+    free_device(book);
+  }
+  delete book;
+  return TQ_OK;
+}
+
+tq_status tq_codebook_levels(const tq_codebook* book, int which, double* levels, double* bounds, int* bits) {
+  if (book == nullptr || (which != 0 && which != 1)) return TQ_ERR_INVALID_ARG;
+  const std::vector<double>& lv = which == 0 ? book->host.k_levels : book->host.v_levels;
+  const std::vector<double>& bd = which == 0 ? book->host.k_bounds : book->host.v_bounds;
+  if (levels) std::memcpy(levels, lv.data(), lv.size() * sizeof(double));
+  if (bounds) std::memcpy(bounds, bd.data(), bd.size() * sizeof(double));
+  if (bits) *bits = which == 0 ? book->k_mse_bits : book->v_bits;
+  return TQ_OK;
+}
+
+tq_status tq_codebook_matrices(const tq_codebook* book, double* R, double* S) {
+  if (book == nullptr) return TQ_ERR_INVALID_ARG;
+  if (R) std::memcpy(R, book->host.R.data(), book->host.R.size() * sizeof(double));
+  if (S) std::memcpy(S, book->host.S.data(), book->host.S.size() * sizeof(double));
+  return TQ_OK;
+}
+
+tq_status tq_cache_field_bytes(const tq_codebook* book, size_t bytes_per_item[6]) {
+  if (book == nullptr || bytes_per_item == nullptr) return TQ_ERR_INVALID_ARG;
+  const size_t d = static_cast<size_t>(book->cfg.d);
+  const bool qjl = book->cfg.qjl_m > 0;
+  bytes_per_item[0] = book->k_mse_bits * d / 8;
+  bytes_per_item[1] = qjl ? static_cast<size_t>(book->cfg.qjl_m) / 8 : 0;
+  bytes_per_item[2] = 4;
+  bytes_per_item[3] = qjl ? 4 : 0;
+  bytes_per_item[4] = book->v_bits * d / 8;
+  bytes_per_item[5] = 4;
+  return TQ_OK;
+}
+
+tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void* v, tq_dtype dtype,
+                             int n_tokens, int n_kv_heads, const int64_t* slot_mapping,
+                             const tq_cache_view* cache, void* stream) {
+  if (!valid_device_handle(book)) return TQ_ERR_INVALID_ARG;
+  if (dtype != TQ_BF16 && dtype != TQ_FP32) return TQ_ERR_INVALID_ARG;
+  if (n_tokens < 0 || n_kv_heads <= 0 || !valid_cache(book, cache) || cache->n_kv_heads != n_kv_heads) {
+    return TQ_ERR_INVALID_ARG;
+  }
+  if (n_tokens == 0) return TQ_OK;
+  if (slot_mapping == nullptr || (k == nullptr && v == nullptr)) return TQ_ERR_INVALID_ARG;
+  if ((k && !aligned16(k)) || (v && !aligned16(v))) return TQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(n_tokens) * n_kv_heads > (1ll << 31) - 1) return TQ_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool bf16 = dtype == TQ_BF16;
+  tq::QuantizeArgs a{};
+  a.n_vec = n_tokens * n_kv_heads;
+  a.n_kv = n_kv_heads;
+  a.slots = slot_mapping;
+  a.num_blocks = cache->num_blocks;
+  a.block_size = cache->block_size;
+  a.Rt = book->d_Rt;
+  a.Spt = book->d_Spt;
+  a.error = book->d_error;
+  if (k) {
+    a.x = k;
+    a.codes = static_cast<uint8_t*>(cache->k_codes);
+    a.qjl = book->cfg.qjl_m > 0 ? static_cast<uint8_t*>(cache->k_qjl) : nullptr;
+    a.norm = cache->k_norm;
+    a.rnorm = book->cfg.qjl_m > 0 ? cache->k_rnorm : nullptr;
+    a.bits = book->k_mse_bits;
+    a.levels = table_field(book, offsetof(tq::DeviceTables, k_levels));
+    a.bounds = table_field(book, offsetof(tq::DeviceTables, k_bounds));
+    if (tq::launch_quantize_simt(a, bf16, book->num_sms, s) != cudaSuccess) return TQ_ERR_CUDA;
+  }
+  if (v) {
+    a.x = v;
+    a.codes = static_cast<uint8_t*>(cache->v_codes);
+    a.qjl = nullptr;
+    a.norm = cache->v_norm;
+    a.rnorm = nullptr;
+    a.bits = book->v_bits;
+    a.levels = table_field(book, offsetof(tq::DeviceTables, v_levels));
+    a.bounds = table_field(book, offsetof(tq::DeviceTables, v_bounds));
+    if (tq::launch_quantize_simt(a, bf16, book->num_sms, s) != cudaSuccess) return TQ_ERR_CUDA;
+  }
+  return TQ_OK;
+}
+
+size_t tq_decode_workspace_bytes(const tq_codebook* book, int batch, int n_q_heads, int max_context) {
+  if (book == nullptr || batch <= 0 || n_q_heads <= 0 || max_context < 0) return 0;
+  const size_t vecs = static_cast<size_t>(batch) * n_q_heads;
+  const size_t q_bytes = round_up(vecs * 2 * tq::kDim * sizeof(float));
+  const size_t part_bytes =
+      round_up(vecs * static_cast<size_t>(max_chunks_for(max_context)) * tq::kPartStride * sizeof(float));
+  return q_bytes + part_bytes;
+}
+
+tq_status tq_decode_attention(const tq_codebook* book, const void* q, tq_dtype dtype, int batch,
+                              int n_q_heads, int n_kv_heads, const tq_cache_view* cache,
+                              const int32_t* block_table, int max_blocks, const int32_t* context_lens,
+                              int max_context, float scale, float* out, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!valid_device_handle(book)) return TQ_ERR_INVALID_ARG;
+  if (dtype != TQ_BF16 && dtype != TQ_FP32) return TQ_ERR_INVALID_ARG;
+  if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return TQ_ERR_INVALID_ARG;
+  if (!valid_cache(book, cache) || cache->n_kv_heads != n_kv_heads) return TQ_ERR_INVALID_ARG;
+  if (max_blocks <= 0 || max_context < 0 || !(scale >= 0.f) || !std::isfinite(scale)) return TQ_ERR_INVALID_ARG;
+  if (batch == 0) return TQ_OK;
+  if (q == nullptr || out == nullptr || context_lens == nullptr) return TQ_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return TQ_ERR_INVALID_ARG;
+  const int group = n_q_heads / n_kv_heads;
+  if (group != 1 && group != 2 && group != 4 && group != 8) return TQ_ERR_UNSUPPORTED;
+  if (block_table == nullptr && static_cast<long long>(batch) * max_blocks > cache->num_blocks) {
+    return TQ_ERR_INVALID_ARG;
+  }
+  const size_t need = tq_decode_workspace_bytes(book, batch, n_q_heads, max_context);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) {
+    return TQ_ERR_WORKSPACE;
+  }
+  tq::DecodeArgs a{};
+  a.q = q;
+  a.batch = batch;
+  a.n_q = n_q_heads;
+  a.n_kv = n_kv_heads;
+  a.group = group;
+  a.k_codes = static_cast<const uint8_t*>(cache->k_codes);
+  a.k_qjl = book->cfg.qjl_m > 0 ? static_cast<const uint8_t*>(cache->k_qjl) : nullptr;
+  a.k_norm = cache->k_norm;
+  a.k_rnorm = book->cfg.qjl_m > 0 ? cache->k_rnorm : nullptr;
+  a.v_codes = static_cast<const uint8_t*>(cache->v_codes);
+  a.v_norm = cache->v_norm;
+  a.num_blocks = cache->num_blocks;
+  a.block_size = cache->block_size;
+  a.k_bits = book->k_mse_bits;
+  a.v_bits = book->v_bits;
+  a.qjl_m = book->cfg.qjl_m;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.context_lens = context_lens;
+  a.max_context = max_context;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(book->cfg.d));
+  a.qjl_coef = book->cfg.qjl_m > 0 ? static_cast<float>(std::sqrt(M_PI / 2.0) / book->cfg.qjl_m) : 0.f;
+  a.out = out;
+  const size_t vecs = static_cast<size_t>(batch) * n_q_heads;
+  a.ws_q = static_cast<float*>(workspace);
+  a.ws_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(vecs * 2 * tq::kDim * sizeof(float)));
+  a.max_chunks = max_chunks_for(max_context);
+  a.R = book->d_R;
+  a.Rt = book->d_Rt;
+  a.Spt = book->d_Spt;
+  a.tables = book->d_tables;
+  a.error = book->d_error;
+  if (tq::launch_decode(a, dtype == TQ_BF16, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    return TQ_ERR_CUDA;
+  }
+  return TQ_OK;
+}
+
+tq_status tq_get_last_device_error(const tq_codebook* book, void* stream, int* code) {
+  if (!valid_device_handle(book) || code == nullptr) return TQ_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return TQ_ERR_CUDA;
+  int value = 0;
+  if (cudaMemcpy(&value, book->d_error, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TQ_ERR_CUDA;
+  if (cudaMemset(book->d_error, 0, sizeof(int)) != cudaSuccess) return TQ_ERR_CUDA;
+  *code = value;
+  return value == 0 ? TQ_OK : TQ_ERR_DEVICE;
+}
+
+const char* tq_status_string(tq_status status) {
+  switch (status) {
+    case TQ_OK: return "ok";
+    case TQ_ERR_INVALID_ARG: return "invalid argument";
+    case TQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case TQ_ERR_CUDA: return "CUDA error";
+    case TQ_ERR_OOM: return "out of memory";
+    case TQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case TQ_ERR_DEVICE: return "device-side error recorded";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// Kernel launchers (CUDA translation units) called by the C ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "tq_internal.h"
+
+namespace tq {
+
+// Error codes a kernel records in the handle's error word.
+enum DeviceError : int { kErrSlot = 1, kErrBlock = 2, kErrContext = 3 };
+
+struct QuantizeArgs {
+  const void* x;          // [n_vec][128], bf16 or fp32
+  int n_vec;              // n_tokens * n_kv_heads
+  int n_kv;
+  const int64_t* slots;   // [n_tokens]
+  uint8_t* codes;         // field base, bits * 16 bytes per item
+  uint8_t* qjl;           // field base, 16 bytes per item (null: no QJL)
+  float* norm;
+  float* rnorm;           // null when no QJL
+  int num_blocks;
+  int block_size;
+  int bits;               // MSE bits of this tensor
+  const float* levels;    // 2^bits device floats
+  const float* bounds;    // 15 device floats, +inf padded
+  const float* Rt;        // [128][128], Rt[i][o] = R[o][i]
+  const float* Spt;       // [128][128], Spt[j][k] = S'[k][j]
+  int* error;
+};
+
+cudaError_t launch_quantize_simt(const QuantizeArgs& args, bool bf16, int num_sms, cudaStream_t stream);
+
+struct DecodeArgs {
+  const void* q;            // [batch][n_q][128]
+  int batch, n_q, n_kv, group;
+  const uint8_t* k_codes;
+  const uint8_t* k_qjl;     // null: no QJL
+  const float* k_norm;
+  const float* k_rnorm;
+  const uint8_t* v_codes;
+  const float* v_norm;
+  int num_blocks, block_size;
+  int k_bits, v_bits, qjl_m;
+  const int32_t* block_table;  // null: identity
+  int max_blocks;
+  const int32_t* context_lens;
+  int max_context;
+  float scale;
+  float qjl_coef;           // sqrt(pi/2) / m
+  float* out;               // [batch][n_q][128]
+  float* ws_q;              // [batch*n_q][256]: rotated query, projected query
+  float* ws_part;           // [batch*n_q][max_chunks][kPartStride]
+  int max_chunks;
+  const float* R;           // [128][128] row-major
+  const float* Rt;
+  const float* Spt;
+  const DeviceTables* tables;
+  int* error;
+};
+
+constexpr int kChunk = 512;       // context tokens per split-K work item
+constexpr int kPartStride = 132;  // m, l, 2 pad, acc[128]
+
+cudaError_t launch_decode(const DecodeArgs& args, bool bf16, cudaStream_t stream);
+
+}  // namespace tq

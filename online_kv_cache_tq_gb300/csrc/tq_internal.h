@@ -1,0 +1,55 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "tq.h"
+
+namespace tq {
+
+constexpr int kDim = 128;       // head dimension supported by the kernels
+constexpr int kMaxLevels = 16;  // 4-bit codebooks at most
+
+// Codebook tables as the kernels read them (float32, one struct in device
+// memory).  Boundaries are padded with +inf so a kernel may compare against
+// all 15 entries whatever the bit width.
+struct DeviceTables {
+  float k_levels[kMaxLevels];
+  float k_bounds[kMaxLevels];
+  float v_levels[kMaxLevels];
+  float v_bounds[kMaxLevels];
+};
+
+// Host-side construction products (fp64), independent of any device.
+struct HostTables {
+  std::vector<double> R;         // d x d, y = R x
+  std::vector<double> S;         // m x d
+  std::vector<double> Sp;        // m x d, S' = S R^T (acts on rotated residuals)
+  std::vector<double> k_levels;  // 2^k_mse_bits
+  std::vector<double> k_bounds;
+  std::vector<double> v_levels;  // 2^v_bits
+  std::vector<double> v_bounds;
+};
+
+// Build R, S, S' and the codebooks on the host (host_builder.cpp).
+void build_host_tables(int d, int qjl_m, uint64_t seed, int k_mse_bits, int v_bits, HostTables* out);
+
+}  // namespace tq
+
+struct tq_codebook {
+  tq_config cfg;
+  int device;         // -1: host-only handle
+  int k_mse_bits;
+  int v_bits;
+  tq::HostTables host;
+  // Device copies (float32 unless noted), owned by the handle.
+  float* d_R;         // [d][d] row-major R
+  float* d_Rt;        // [d][d] R transposed
+  float* d_Spt;       // [d][m] S' transposed (column k of S' is row k)
+  uint16_t* d_rot_tc; // bf16 hi/lo operand images for the tensor-core quantizer
+  tq::DeviceTables* d_tables;
+  int* d_error;       // first device-side error code, 0 when none
+  int num_sms;
+};
