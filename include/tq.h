@@ -143,10 +143,34 @@ tq_status tq_decode_attention(const tq_codebook* book, const void* q, tq_dtype d
                               const int32_t* context_lens, int max_context, float scale, float* out,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/* The three stages tq_decode_attention runs, callable one at a time on the
+ * same stream with the same arguments and workspace (e.g. to overlap query
+ * preparation with other work, or to time the stages):
+ *   tq_decode_prepare  -- rotated query R q and projected query S' R q into
+ *                         the workspace (seo-farm page §4: the query is rotated,
+ *                         not quantized);
+ *   tq_decode_partials -- per context chunk and KV head: scores from the packed
+ *                         codes plus the QJL correction (甲子光年 §2 第二階段),
+ *                         chunk max/sum and the value sum in the rotated space;
+ *   tq_decode_finish   -- merge the chunk partials, divide by the softmax sum
+ *                         and back-rotate by R^T into `out`.
+ * Argument meaning, checks and errors are those of tq_decode_attention. */
+tq_status tq_decode_prepare(const tq_codebook* book, const void* q, tq_dtype dtype, int batch,
+                            int n_q_heads, int max_context, void* workspace, size_t workspace_bytes,
+                            void* stream);
+tq_status tq_decode_partials(const tq_codebook* book, int batch, int n_q_heads, int n_kv_heads,
+                             const tq_cache_view* cache, const int32_t* block_table, int max_blocks,
+                             const int32_t* context_lens, int max_context, float scale,
+                             void* workspace, size_t workspace_bytes, void* stream);
+tq_status tq_decode_finish(const tq_codebook* book, int batch, int n_q_heads,
+                           const int32_t* context_lens, int max_context, int max_blocks, float* out,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronise `stream`, then return (and clear) the first device-side error
  * code recorded since the last call: 0 none, 1 slot out of range in
  * quantize-append, 2 block id out of range in decode, 3 context length out of
- * range in decode.  Returns TQ_ERR_DEVICE when *code != 0. */
+ * range in decode, 4 a kernel's internal wait timed out (the kernel stopped
+ * early; its outputs are incomplete).  Returns TQ_ERR_DEVICE when *code != 0. */
 tq_status tq_get_last_device_error(const tq_codebook* book, void* stream, int* code);
 
 /* Static description of a status code. */

@@ -22,7 +22,8 @@ FIELDS = ("k_codes", "k_qjl", "k_norm", "k_rnorm", "v_codes", "v_norm")
 # Entry points declared in include/tq.h, checked by the ABI test.
 EXPORTED = ("tq_codebook_build", "tq_codebook_destroy", "tq_codebook_levels", "tq_codebook_matrices",
             "tq_cache_field_bytes", "tq_quantize_append", "tq_decode_workspace_bytes",
-            "tq_decode_attention", "tq_get_last_device_error", "tq_status_string")
+            "tq_decode_attention", "tq_decode_prepare", "tq_decode_partials", "tq_decode_finish",
+            "tq_get_last_device_error", "tq_status_string")
 
 
 class TQError(RuntimeError):
@@ -69,6 +70,10 @@ def load():
     lib.tq_decode_workspace_bytes.restype = sz
     lib.tq_decode_attention.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.POINTER(tq_cache_view), vp, i32,
                                         vp, i32, ctypes.c_float, vp, vp, sz, vp]
+    lib.tq_decode_prepare.argtypes = [vp, vp, i32, i32, i32, i32, vp, sz, vp]
+    lib.tq_decode_partials.argtypes = [vp, i32, i32, i32, ctypes.POINTER(tq_cache_view), vp, i32, vp, i32,
+                                       ctypes.c_float, vp, sz, vp]
+    lib.tq_decode_finish.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, sz, vp]
     lib.tq_get_last_device_error.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.tq_status_string.argtypes = [i32]
     lib.tq_status_string.restype = ctypes.c_char_p
@@ -192,6 +197,25 @@ def tq_decode_attention(book, q, dtype, batch, n_q_heads, n_kv_heads, view, bloc
                                       max_context, scale, _ptr(out), _ptr(workspace), workspace_bytes,
                                       _stream(stream)),
            "tq_decode_attention")
+
+
+def tq_decode_prepare(book, q, dtype, batch, n_q_heads, max_context, workspace, workspace_bytes, stream=None):
+    _check(load().tq_decode_prepare(book.handle, _ptr(q), dtype, batch, n_q_heads, max_context, _ptr(workspace),
+                                    workspace_bytes, _stream(stream)), "tq_decode_prepare")
+
+
+def tq_decode_partials(book, batch, n_q_heads, n_kv_heads, view, block_table, max_blocks, context_lens,
+                       max_context, scale, workspace, workspace_bytes, stream=None):
+    _check(load().tq_decode_partials(book.handle, batch, n_q_heads, n_kv_heads, ctypes.byref(view),
+                                     _ptr(block_table), max_blocks, _ptr(context_lens), max_context, scale,
+                                     _ptr(workspace), workspace_bytes, _stream(stream)), "tq_decode_partials")
+
+
+def tq_decode_finish(book, batch, n_q_heads, context_lens, max_context, max_blocks, out, workspace,
+                     workspace_bytes, stream=None):
+    _check(load().tq_decode_finish(book.handle, batch, n_q_heads, _ptr(context_lens), max_context, max_blocks,
+                                   _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)),
+           "tq_decode_finish")
 
 
 def tq_get_last_device_error(book, stream=None):

@@ -5,8 +5,10 @@
 #include <new>
 #include <vector>
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "kernels.h"
 #include "tq.h"
@@ -15,6 +17,35 @@
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult res;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &res) !=
+            cudaSuccess ||
+        res != cudaDriverEntryPointSuccess) {
+      ptr = nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
+// 2-D map over a row-major [rows][128] bf16 array, 64 x 128 boxes, 128-byte
+// swizzle (the K-major operand layout of the tensor-core quantizer).
+bool encode_rows_bf16(CUtensorMap* map, const void* base, uint64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr || rows == 0) return false;
+  cuuint64_t dims[2] = {128, rows};
+  cuuint64_t strides[1] = {128 * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t elem[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 struct DeviceGuard {
   int prev = -1;
@@ -101,6 +132,9 @@ tq_status upload_tables(tq_codebook* b) {
   if (err == cudaSuccess) err = upload(&b->d_tables, tv);
   if (err == cudaSuccess) err = upload(&b->d_error, zero);
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&b->num_sms, cudaDevAttrMultiProcessorCount, b->device);
+  if (err == cudaSuccess && !encode_rows_bf16(&b->w_map, b->d_rot_tc, 4 * static_cast<uint64_t>(d))) {
+    err = cudaErrorInvalidValue;
+  }
   if (err != cudaSuccess) {
     free_device(b);
     return err == cudaErrorMemoryAllocation ? TQ_ERR_OOM : TQ_ERR_CUDA;
@@ -123,6 +157,14 @@ bool valid_cache(const tq_codebook* b, const tq_cache_view* c) {
 // Device address of one array inside the handle's DeviceTables.
 const float* table_field(const tq_codebook* b, size_t offset) {
   return reinterpret_cast<const float*>(reinterpret_cast<const char*>(b->d_tables) + offset);
+}
+
+// bf16 inputs go to the tensor-core quantizer, fp32 inputs to the SIMT one.
+cudaError_t launch_quantize(const tq_codebook* b, const tq::QuantizeArgs& a, bool bf16, cudaStream_t s) {
+  if (!bf16) return tq::launch_quantize_simt(a, false, b->num_sms, s);
+  CUtensorMap x_map;
+  if (!encode_rows_bf16(&x_map, a.x, static_cast<uint64_t>(a.n_vec))) return cudaErrorInvalidValue;
+  return tq::launch_quantize_tc(a, x_map, b->w_map, b->num_sms, s);
 }
 
 constexpr size_t kWsAlign = 256;
@@ -245,7 +287,7 @@ tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void*
     a.bits = book->k_mse_bits;
     a.levels = table_field(book, offsetof(tq::DeviceTables, k_levels));
     a.bounds = table_field(book, offsetof(tq::DeviceTables, k_bounds));
-    if (tq::launch_quantize_simt(a, bf16, book->num_sms, s) != cudaSuccess) return TQ_ERR_CUDA;
+    if (launch_quantize(book, a, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;
   }
   if (v) {
     a.x = v;
@@ -256,7 +298,7 @@ tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void*
     a.bits = book->v_bits;
     a.levels = table_field(book, offsetof(tq::DeviceTables, v_levels));
     a.bounds = table_field(book, offsetof(tq::DeviceTables, v_bounds));
-    if (tq::launch_quantize_simt(a, bf16, book->num_sms, s) != cudaSuccess) return TQ_ERR_CUDA;
+    if (launch_quantize(book, a, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;
   }
   return TQ_OK;
 }
@@ -270,65 +312,132 @@ size_t tq_decode_workspace_bytes(const tq_codebook* book, int batch, int n_q_hea
   return q_bytes + part_bytes;
 }
 
+}  // extern "C"
+
+namespace {
+
+enum Stage { kPrepare = 1, kPartials = 2, kFinish = 4 };
+
+// Validate the arguments a decode stage uses and fill the launch arguments.
+tq_status decode_args(const tq_codebook* book, int stages, const void* q, tq_dtype dtype, int batch,
+                      int n_q_heads, int n_kv_heads, const tq_cache_view* cache, const int32_t* block_table,
+                      int max_blocks, const int32_t* context_lens, int max_context, float scale, float* out,
+                      void* workspace, size_t workspace_bytes, tq::DecodeArgs* a) {
+  if (!valid_device_handle(book)) return TQ_ERR_INVALID_ARG;
+  if (batch < 0 || n_q_heads <= 0 || max_context < 0) return TQ_ERR_INVALID_ARG;
+  *a = tq::DecodeArgs{};
+  if (stages & kPrepare) {
+    if (dtype != TQ_BF16 && dtype != TQ_FP32) return TQ_ERR_INVALID_ARG;
+    if (batch > 0 && (q == nullptr || !aligned16(q))) return TQ_ERR_INVALID_ARG;
+  }
+  if (stages & kPartials) {
+    if (n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return TQ_ERR_INVALID_ARG;
+    if (!valid_cache(book, cache) || cache->n_kv_heads != n_kv_heads) return TQ_ERR_INVALID_ARG;
+    if (!(scale >= 0.f) || !std::isfinite(scale)) return TQ_ERR_INVALID_ARG;
+    const int group = n_q_heads / n_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return TQ_ERR_UNSUPPORTED;
+    if (block_table == nullptr && static_cast<long long>(batch) * max_blocks > cache->num_blocks) {
+      return TQ_ERR_INVALID_ARG;
+    }
+  }
+  if (stages & (kPartials | kFinish)) {
+    if (max_blocks <= 0) return TQ_ERR_INVALID_ARG;
+    if (batch > 0 && context_lens == nullptr) return TQ_ERR_INVALID_ARG;
+  }
+  if ((stages & kFinish) && batch > 0 && (out == nullptr || !aligned16(out))) return TQ_ERR_INVALID_ARG;
+  if (batch == 0) return TQ_OK;
+  const size_t need = tq_decode_workspace_bytes(book, batch, n_q_heads, max_context);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) {
+    return TQ_ERR_WORKSPACE;
+  }
+  a->q = q;
+  a->batch = batch;
+  a->n_q = n_q_heads;
+  if (stages & kPartials) {
+    a->n_kv = n_kv_heads;
+    a->group = n_q_heads / n_kv_heads;
+    a->k_codes = static_cast<const uint8_t*>(cache->k_codes);
+    a->k_qjl = book->cfg.qjl_m > 0 ? static_cast<const uint8_t*>(cache->k_qjl) : nullptr;
+    a->k_norm = cache->k_norm;
+    a->k_rnorm = book->cfg.qjl_m > 0 ? cache->k_rnorm : nullptr;
+    a->v_codes = static_cast<const uint8_t*>(cache->v_codes);
+    a->v_norm = cache->v_norm;
+    a->num_blocks = cache->num_blocks;
+  }
+  a->block_size = book->cfg.block_size;
+  a->k_bits = book->k_mse_bits;
+  a->v_bits = book->v_bits;
+  a->qjl_m = book->cfg.qjl_m;
+  a->block_table = block_table;
+  a->max_blocks = max_blocks;
+  a->context_lens = context_lens;
+  a->max_context = max_context;
+  a->scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(book->cfg.d));
+  a->qjl_coef = book->cfg.qjl_m > 0 ? static_cast<float>(std::sqrt(M_PI / 2.0) / book->cfg.qjl_m) : 0.f;
+  a->out = out;
+  const size_t vecs = static_cast<size_t>(batch) * n_q_heads;
+  a->ws_q = static_cast<float*>(workspace);
+  a->ws_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(vecs * 2 * tq::kDim * sizeof(float)));
+  a->max_chunks = max_chunks_for(max_context);
+  a->R = book->d_R;
+  a->Rt = book->d_Rt;
+  a->Spt = book->d_Spt;
+  a->tables = book->d_tables;
+  a->error = book->d_error;
+  return TQ_OK;
+}
+
+tq_status launched(cudaError_t err) { return err == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
 tq_status tq_decode_attention(const tq_codebook* book, const void* q, tq_dtype dtype, int batch,
                               int n_q_heads, int n_kv_heads, const tq_cache_view* cache,
                               const int32_t* block_table, int max_blocks, const int32_t* context_lens,
                               int max_context, float scale, float* out, void* workspace,
                               size_t workspace_bytes, void* stream) {
-  if (!valid_device_handle(book)) return TQ_ERR_INVALID_ARG;
-  if (dtype != TQ_BF16 && dtype != TQ_FP32) return TQ_ERR_INVALID_ARG;
-  if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return TQ_ERR_INVALID_ARG;
-  if (!valid_cache(book, cache) || cache->n_kv_heads != n_kv_heads) return TQ_ERR_INVALID_ARG;
-  if (max_blocks <= 0 || max_context < 0 || !(scale >= 0.f) || !std::isfinite(scale)) return TQ_ERR_INVALID_ARG;
-  if (batch == 0) return TQ_OK;
-  if (q == nullptr || out == nullptr || context_lens == nullptr) return TQ_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(out)) return TQ_ERR_INVALID_ARG;
-  const int group = n_q_heads / n_kv_heads;
-  if (group != 1 && group != 2 && group != 4 && group != 8) return TQ_ERR_UNSUPPORTED;
-  if (block_table == nullptr && static_cast<long long>(batch) * max_blocks > cache->num_blocks) {
-    return TQ_ERR_INVALID_ARG;
-  }
-  const size_t need = tq_decode_workspace_bytes(book, batch, n_q_heads, max_context);
-  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) {
-    return TQ_ERR_WORKSPACE;
-  }
-  tq::DecodeArgs a{};
-  a.q = q;
-  a.batch = batch;
-  a.n_q = n_q_heads;
-  a.n_kv = n_kv_heads;
-  a.group = group;
-  a.k_codes = static_cast<const uint8_t*>(cache->k_codes);
-  a.k_qjl = book->cfg.qjl_m > 0 ? static_cast<const uint8_t*>(cache->k_qjl) : nullptr;
-  a.k_norm = cache->k_norm;
-  a.k_rnorm = book->cfg.qjl_m > 0 ? cache->k_rnorm : nullptr;
-  a.v_codes = static_cast<const uint8_t*>(cache->v_codes);
-  a.v_norm = cache->v_norm;
-  a.num_blocks = cache->num_blocks;
-  a.block_size = cache->block_size;
-  a.k_bits = book->k_mse_bits;
-  a.v_bits = book->v_bits;
-  a.qjl_m = book->cfg.qjl_m;
-  a.block_table = block_table;
-  a.max_blocks = max_blocks;
-  a.context_lens = context_lens;
-  a.max_context = max_context;
-  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(book->cfg.d));
-  a.qjl_coef = book->cfg.qjl_m > 0 ? static_cast<float>(std::sqrt(M_PI / 2.0) / book->cfg.qjl_m) : 0.f;
-  a.out = out;
-  const size_t vecs = static_cast<size_t>(batch) * n_q_heads;
-  a.ws_q = static_cast<float*>(workspace);
-  a.ws_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(vecs * 2 * tq::kDim * sizeof(float)));
-  a.max_chunks = max_chunks_for(max_context);
-  a.R = book->d_R;
-  a.Rt = book->d_Rt;
-  a.Spt = book->d_Spt;
-  a.tables = book->d_tables;
-  a.error = book->d_error;
-  if (tq::launch_decode(a, dtype == TQ_BF16, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
-    return TQ_ERR_CUDA;
-  }
-  return TQ_OK;
+  tq::DecodeArgs a;
+  tq_status st = decode_args(book, kPrepare | kPartials | kFinish, q, dtype, batch, n_q_heads, n_kv_heads, cache,
+                             block_table, max_blocks, context_lens, max_context, scale, out, workspace,
+                             workspace_bytes, &a);
+  if (st != TQ_OK || batch == 0) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = launched(tq::launch_decode_prepare(a, dtype == TQ_BF16, s));
+  if (st == TQ_OK) st = launched(tq::launch_decode_partials(a, s));
+  if (st == TQ_OK) st = launched(tq::launch_decode_finish(a, s));
+  return st;
+}
+
+tq_status tq_decode_prepare(const tq_codebook* book, const void* q, tq_dtype dtype, int batch, int n_q_heads,
+                            int max_context, void* workspace, size_t workspace_bytes, void* stream) {
+  tq::DecodeArgs a;
+  tq_status st = decode_args(book, kPrepare, q, dtype, batch, n_q_heads, 0, nullptr, nullptr, 1, nullptr,
+                             max_context, 0.f, nullptr, workspace, workspace_bytes, &a);
+  if (st != TQ_OK || batch == 0) return st;
+  return launched(tq::launch_decode_prepare(a, dtype == TQ_BF16, static_cast<cudaStream_t>(stream)));
+}
+
+tq_status tq_decode_partials(const tq_codebook* book, int batch, int n_q_heads, int n_kv_heads,
+                             const tq_cache_view* cache, const int32_t* block_table, int max_blocks,
+                             const int32_t* context_lens, int max_context, float scale, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  tq::DecodeArgs a;
+  tq_status st = decode_args(book, kPartials, nullptr, TQ_FP32, batch, n_q_heads, n_kv_heads, cache, block_table,
+                             max_blocks, context_lens, max_context, scale, nullptr, workspace, workspace_bytes, &a);
+  if (st != TQ_OK || batch == 0) return st;
+  return launched(tq::launch_decode_partials(a, static_cast<cudaStream_t>(stream)));
+}
+
+tq_status tq_decode_finish(const tq_codebook* book, int batch, int n_q_heads, const int32_t* context_lens,
+                           int max_context, int max_blocks, float* out, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  tq::DecodeArgs a;
+  tq_status st = decode_args(book, kFinish, nullptr, TQ_FP32, batch, n_q_heads, 0, nullptr, nullptr, max_blocks,
+                             context_lens, max_context, 0.f, out, workspace, workspace_bytes, &a);
+  if (st != TQ_OK || batch == 0) return st;
+  return launched(tq::launch_decode_finish(a, static_cast<cudaStream_t>(stream)));
 }
 
 tq_status tq_get_last_device_error(const tq_codebook* book, void* stream, int* code) {

@@ -293,20 +293,29 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(DecodeArgs a) {
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs& args, bool bf16, cudaStream_t stream) {
+cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_t stream) {
   const int n_vec = args.batch * args.n_q;
   if (n_vec <= 0) return cudaSuccess;
   qprep_kernel<<<n_vec, kThreads, 0, stream>>>(args, bf16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_partials(const DecodeArgs& args, cudaStream_t stream) {
+  if (args.batch <= 0 || args.max_chunks <= 0) return cudaSuccess;
   dim3 grid(args.max_chunks, args.n_kv, args.batch);
-  if (args.max_chunks > 0) {
-    switch (args.group) {
-      case 1: attention_kernel<1><<<grid, kThreads, 0, stream>>>(args); break;
-      case 2: attention_kernel<2><<<grid, kThreads, 0, stream>>>(args); break;
-      case 4: attention_kernel<4><<<grid, kThreads, 0, stream>>>(args); break;
-      case 8: attention_kernel<8><<<grid, kThreads, 0, stream>>>(args); break;
-      default: return cudaErrorInvalidValue;
-    }
+  switch (args.group) {
+    case 1: attention_kernel<1><<<grid, kThreads, 0, stream>>>(args); break;
+    case 2: attention_kernel<2><<<grid, kThreads, 0, stream>>>(args); break;
+    case 4: attention_kernel<4><<<grid, kThreads, 0, stream>>>(args); break;
+    case 8: attention_kernel<8><<<grid, kThreads, 0, stream>>>(args); break;
+    default: return cudaErrorInvalidValue;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream) {
+  const int n_vec = args.batch * args.n_q;
+  if (n_vec <= 0) return cudaSuccess;
   combine_kernel<<<n_vec, kThreads, 0, stream>>>(args);
   return cudaGetLastError();
 }

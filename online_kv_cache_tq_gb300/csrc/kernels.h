@@ -1,6 +1,7 @@
 // Kernel launchers (CUDA translation units) called by the C ABI layer.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "tq_internal.h"
@@ -8,7 +9,7 @@
 namespace tq {
 
 // Error codes a kernel records in the handle's error word.
-enum DeviceError : int { kErrSlot = 1, kErrBlock = 2, kErrContext = 3 };
+enum DeviceError : int { kErrSlot = 1, kErrBlock = 2, kErrContext = 3, kErrTimeout = 4 };
 
 struct QuantizeArgs {
   const void* x;          // [n_vec][128], bf16 or fp32
@@ -30,6 +31,12 @@ struct QuantizeArgs {
 };
 
 cudaError_t launch_quantize_simt(const QuantizeArgs& args, bool bf16, int num_sms, cudaStream_t stream);
+
+// bf16 inputs on the tensor cores; x_map tiles x as [n_vec][128] bf16 in
+// 64 x 128 boxes (128-byte swizzle), w_map tiles the handle's bf16 hi/lo
+// images of R and S' as [512][128].
+cudaError_t launch_quantize_tc(const QuantizeArgs& args, const CUtensorMap& x_map, const CUtensorMap& w_map,
+                               int num_sms, cudaStream_t stream);
 
 struct DecodeArgs {
   const void* q;            // [batch][n_q][128]
@@ -62,6 +69,8 @@ struct DecodeArgs {
 constexpr int kChunk = 512;       // context tokens per split-K work item
 constexpr int kPartStride = 132;  // m, l, 2 pad, acc[128]
 
-cudaError_t launch_decode(const DecodeArgs& args, bool bf16, cudaStream_t stream);
+cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_t stream);
+cudaError_t launch_decode_partials(const DecodeArgs& args, cudaStream_t stream);
+cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream);
 
 }  // namespace tq

@@ -7,6 +7,8 @@
 
 #include "tq.h"
 
+#include <cuda.h>
+
 namespace tq {
 
 constexpr int kDim = 128;       // head dimension supported by the kernels
@@ -52,4 +54,5 @@ struct tq_codebook {
   tq::DeviceTables* d_tables;
   int* d_error;       // first device-side error code, 0 when none
   int num_sms;
+  CUtensorMap w_map;  // TMA map of d_rot_tc as [512][128] bf16
 };

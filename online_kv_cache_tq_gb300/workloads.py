@@ -112,3 +112,11 @@ def slots_for(block_table_row, positions, block_size):
     """Cache slots (physical block * block_size + offset) of token positions."""
     positions = np.asarray(positions, dtype=np.int64)
     return block_table_row[positions // block_size].astype(np.int64) * block_size + positions % block_size
+
+
+def bf16_round_numpy(x):
+    """float64 array rounded to the nearest bfloat16 (ties to even), as float64:
+    the values a bf16 input tensor holds, for host-side (oracle) workloads."""
+    bits = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).view(np.uint32).astype(np.uint64)
+    bits = (bits + 0x7FFF + ((bits >> 16) & 1)) & 0xFFFF0000
+    return bits.astype(np.uint32).view(np.float32).astype(np.float64)
