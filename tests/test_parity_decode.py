@@ -1,0 +1,153 @@
+"""GPU decode attention vs the fp64 oracle, through the C ABI.
+
+The oracle decodes the GPU's own packed cache (identical codes), so these
+tests isolate the read path: scores, QJL correction, softmax, split-K merge
+and back-rotation."""
+import numpy as np
+import pytest
+import torch
+
+from online_kv_cache_tq_gb300 import binding as B
+from online_kv_cache_tq_gb300 import cache as C
+from online_kv_cache_tq_gb300 import workloads as W
+
+from parity_helpers import (attn_pairs, books, check_decode, decode, fill_cache, generator, host_cache,
+                            identity_table)
+
+pytestmark = pytest.mark.gpu
+
+
+def test_single_head_fp32_every_output():
+    cfg = W.CONFIGS["c1_single_head_parity"]
+    book, ref = books(cfg["k_bits"], cfg["v_bits"], cfg["qjl_m"], cfg["seed"])
+    g = generator(0)
+    ctx = np.array([4096], dtype=np.int32)
+    table = identity_table(1, 64)
+    cache = fill_cache(book, cfg, ctx, table, g)
+    q = W.queries(1, 1, torch.float32, "cuda", g)
+    out = decode(book, cache, q, None, ctx, 4096)
+    worst = check_decode(out, host_cache(cache), q, table, ctx, ref, [(0, 0)])
+    print("c1 worst normalised error %.3g" % worst)
+    assert B.tq_get_last_device_error(book) == 0
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_gqa_ragged_contexts_shuffled_blocks(group):
+    # contexts spanning 0, 1, partial and several 512-token chunks; shuffled pages
+    n_kv = 2
+    cfg = dict(n_kv=n_kv, block_size=64, dtype="bf16", seed=group, log_uniform=(0.1, 10.0), outliers=3,
+               outlier_scale=30.0)
+    book, ref = books(3, 3, 128, seed=1)
+    ctx = np.array([0, 1, 77, 512, 513, 1500, 2100], dtype=np.int32)
+    table, _ = W.block_layout(ctx, 64, True, seed=group)
+    g = generator(group)
+    cache = fill_cache(book, cfg, ctx, table, g, chunk_tokens=1000)
+    q = W.queries(len(ctx), n_kv * group, torch.bfloat16, "cuda", g)
+    out = decode(book, cache, q, table, ctx, 2100)
+    pairs = [(b, h) for b in range(len(ctx)) for h in range(n_kv * group)]
+    check_decode(out, host_cache(cache), q, table, ctx, ref, pairs)
+    assert B.tq_get_last_device_error(book) == 0
+
+
+@pytest.mark.parametrize("k_bits,v_bits,qjl", [(2, 1, 128), (5, 4, 128), (4, 2, 128), (2, 3, 0)])
+def test_bit_width_variants(k_bits, v_bits, qjl):
+    cfg = dict(n_kv=1, block_size=64, dtype="bf16", seed=5, log_uniform=None, outliers=2, outlier_scale=20.0)
+    book, ref = books(k_bits, v_bits, qjl, seed=2)
+    ctx = np.array([1100, 300], dtype=np.int32)
+    table, _ = W.block_layout(ctx, 64, False, seed=0)
+    g = generator(k_bits)
+    cache = fill_cache(book, cfg, ctx, table, g)
+    q = W.queries(2, 4, torch.float32, "cuda", g)
+    out = decode(book, cache, q, table, ctx, 1100)
+    check_decode(out, host_cache(cache), q, table, ctx, ref, [(b, h) for b in range(2) for h in range(4)])
+
+
+def test_staged_calls_match_the_one_call():
+    cfg = dict(n_kv=2, block_size=64, dtype="bf16", seed=8, log_uniform=(0.1, 10.0), outliers=0,
+               outlier_scale=1.0)
+    book, _ = books(3, 3, 128, seed=5)
+    ctx = np.array([700, 1300], dtype=np.int32)
+    table, _ = W.block_layout(ctx, 64, True, seed=3)
+    g = generator(11)
+    cache = fill_cache(book, cfg, ctx, table, g)
+    q = W.queries(2, 8, torch.bfloat16, "cuda", g)
+    whole = decode(book, cache, q, table, ctx, 1300)
+    ws, nbytes = C.allocate_workspace(book, 2, 8, 1300)
+    out = torch.zeros((2, 8, 128), device="cuda")
+    table_t = torch.as_tensor(table, device="cuda")
+    ctx_t = torch.as_tensor(ctx, device="cuda")
+    view = C.cache_view(book, cache)
+    B.tq_decode_prepare(book, q, B.TQ_BF16, 2, 8, 1300, ws, nbytes)
+    B.tq_decode_partials(book, 2, 8, 2, view, table_t, table.shape[1], ctx_t, 1300, 0.0, ws, nbytes)
+    B.tq_decode_finish(book, 2, 8, ctx_t, 1300, table.shape[1], out, ws, nbytes)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), whole)
+
+
+def test_custom_scale_and_device_errors():
+    cfg = dict(n_kv=1, block_size=64, dtype="fp32", seed=3, log_uniform=None, outliers=0, outlier_scale=1.0)
+    book, ref = books(3, 3, 128, seed=4)
+    ctx = np.array([200], dtype=np.int32)
+    table, _ = W.block_layout(ctx, 64, False, seed=0)
+    g = generator(9)
+    cache = fill_cache(book, cfg, ctx, table, g)
+    q = W.queries(1, 1, torch.float32, "cuda", g)
+    out = decode(book, cache, q, table, ctx, 200, scale=0.05)
+    check_decode(out, host_cache(cache), q, table, ctx, ref, [(0, 0)], scale=0.05)
+    # a block id outside the cache is skipped and recorded (code 2)
+    bad = table.copy()
+    bad[0, 1] = 1000
+    decode(book, cache, q, bad, ctx, 200)
+    assert B.tq_get_last_device_error(book) == 2
+    # a context longer than max_context is clamped and recorded (code 3)
+    decode(book, cache, q, table, np.array([300], dtype=np.int32), 200)
+    assert B.tq_get_last_device_error(book) == 3
+    assert B.tq_get_last_device_error(book) == 0
+
+
+def test_workspace_and_argument_checks():
+    book, _ = books()
+    cache = C.allocate_cache(book, 4, 1)
+    view = C.cache_view(book, cache)
+    q = torch.zeros((1, 1, 128), device="cuda")
+    out = torch.zeros((1, 1, 128), device="cuda")
+    ctx = torch.ones(1, dtype=torch.int32, device="cuda")
+    need = B.tq_decode_workspace_bytes(book, 1, 1, 256)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    with pytest.raises(B.TQError) as err:
+        B.tq_decode_attention(book, q, B.TQ_FP32, 1, 1, 1, view, None, 4, ctx, 256, 0.0, out, ws, need - 256)
+    assert err.value.status == 5
+    with pytest.raises(B.TQError) as err:
+        B.tq_decode_attention(book, q, B.TQ_FP32, 1, 3, 1, view, None, 4, ctx, 256, 0.0, out, ws, need)
+    assert err.value.status == 2                     # group of 3 is not built
+    with pytest.raises(B.TQError) as err:
+        B.tq_decode_attention(book, q, B.TQ_FP32, 1, 1, 2, view, None, 4, ctx, 256, 0.0, out, ws, need)
+    assert err.value.status == 1                     # n_kv differs from the cache
+
+
+def _full_size(name, n_pairs, seed):
+    cfg = W.CONFIGS[name]
+    book, ref = books(cfg["k_bits"], cfg["v_bits"], cfg["qjl_m"], cfg["seed"])
+    ctx = W.context_lengths(cfg, cfg["seed"])
+    table, _ = W.block_layout(ctx, cfg["block_size"], cfg.get("shuffled_table", False), cfg["seed"])
+    g = generator(seed)
+    cache = fill_cache(book, cfg, ctx, table, g, chunk_tokens=8192)
+    q = W.queries(cfg["batch"], cfg["n_q"], W.torch_dtype(cfg["dtype"]), "cuda", g)
+    out = decode(book, cache, q, table, ctx, int(ctx.max()))
+    assert np.all(np.isfinite(out))
+    pairs = attn_pairs(cfg["batch"], cfg["n_q"], n_pairs, seed)
+    worst = check_decode(out, host_cache(cache), q, table, ctx, ref, pairs)
+    print("%s worst normalised error %.3g over %d sampled heads" % (name, worst, len(pairs)))
+    assert B.tq_get_last_device_error(book) == 0
+
+
+def test_llama3_8b_decode_full_size_sampled():
+    _full_size("c2_llama3_8b_decode", 6, 21)
+
+
+def test_long_context_full_size_sampled():
+    _full_size("c4_long_context", 3, 22)
+
+
+def test_llama3_70b_paged_full_size_sampled():
+    _full_size("c5_llama3_70b_paged", 3, 23)

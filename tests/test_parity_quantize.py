@@ -1,0 +1,110 @@
+"""GPU quantize-append vs the fp64 oracle, through the C ABI.
+
+fp32 inputs run the SIMT quantizer, bf16 inputs the tcgen05 one."""
+import numpy as np
+import pytest
+import torch
+
+from online_kv_cache_tq_gb300 import binding as B
+from online_kv_cache_tq_gb300 import cache as C
+from online_kv_cache_tq_gb300 import workloads as W
+
+from parity_helpers import books, check_append, generator, quantize_into
+
+pytestmark = pytest.mark.gpu
+
+
+def test_single_head_fp32_outliers_every_vector():
+    # 4096 fp32 keys/values, 4 channels x20 (seeded separately), b = 3
+    cfg = W.CONFIGS["c1_single_head_parity"]
+    book, ref = books(cfg["k_bits"], cfg["v_bits"], cfg["qjl_m"], cfg["seed"])
+    g = generator(0)
+    k = W.gaussian_tokens(4096, W.channel_scales(0, 1, None, 4, 20.0), torch.float32, "cuda", g)
+    v = W.gaussian_tokens(4096, W.channel_scales(1, 1, None, 4, 20.0), torch.float32, "cuda", g)
+    cache = C.allocate_cache(book, 4096 // 64, 1)
+    slots = np.arange(4096)
+    quantize_into(book, cache, k, v, slots)
+    rep = check_append(book, ref, cache, k, v, slots)
+    assert rep["vectors"] == 4096
+    assert B.tq_get_last_device_error(book) == 0
+
+
+@pytest.mark.parametrize("k_bits,v_bits", [(2, 2), (3, 3), (4, 4), (5, 1), (4, 2)])
+def test_bf16_gqa_ragged_shuffled_slots(k_bits, v_bits):
+    book, ref = books(k_bits, v_bits, 128, seed=3)
+    n_tok, n_kv = 1001, 3                 # 3003 vectors: 24 tiles of 128 and a ragged tail
+    g = generator(k_bits * 10 + v_bits)
+    scales = W.channel_scales(5, n_kv, (0.1, 10.0), 3, 30.0)
+    k = W.gaussian_tokens(n_tok, scales, torch.bfloat16, "cuda", g)
+    v = W.gaussian_tokens(n_tok, scales[::-1].copy(), torch.bfloat16, "cuda", g)
+    num_blocks = 20
+    slots = np.random.default_rng(1).permutation(num_blocks * 64)[:n_tok]
+    cache = C.allocate_cache(book, num_blocks, n_kv)
+    quantize_into(book, cache, k, v, slots)
+    print(check_append(book, ref, cache, k, v, slots))
+    assert B.tq_get_last_device_error(book) == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_qjl_off_and_separate_k_v_calls(dtype):
+    book, ref = books(3, 2, 0, seed=9)
+    g = generator(2)
+    k = W.gaussian_tokens(300, np.ones((2, 128)), dtype, "cuda", g)
+    v = W.gaussian_tokens(300, np.ones((2, 128)), dtype, "cuda", g)
+    cache = C.allocate_cache(book, 5, 2)
+    assert "k_qjl" not in cache
+    slots = np.arange(300)
+    quantize_into(book, cache, k, None, slots)
+    quantize_into(book, cache, None, v, slots)
+    check_append(book, ref, cache, k, v, slots)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_zero_vectors_negative_and_out_of_range_slots(dtype):
+    book, ref = books(3, 3, 128, seed=0)
+    g = generator(4)
+    k = W.gaussian_tokens(40, np.ones((2, 128)), dtype, "cuda", g)
+    v = W.gaussian_tokens(40, np.ones((2, 128)), dtype, "cuda", g)
+    k[5] = 0.0
+    v[6] = 0.0
+    cache = C.allocate_cache(book, 1, 2)
+    for name in cache:
+        cache[name].fill_(0xAB if cache[name].dtype == torch.uint8 else 7.0)
+    slots = np.full(40, -1)
+    slots[:10] = np.arange(10)
+    slots[3] = -1                         # skipped silently
+    slots[10] = 64 + 5                    # beyond the one-block cache: skipped and recorded
+    quantize_into(book, cache, k, v, slots)
+    assert B.tq_get_last_device_error(book) == 1
+    assert B.tq_get_last_device_error(book) == 0       # cleared by the read
+    valid = np.array([t for t in range(40) if 0 <= slots[t] < 64])
+    check_append(book, ref, cache, k, v, slots, sample=valid)
+    hc = {n: t.cpu() for n, t in cache.items()}
+    assert torch.all(hc["k_codes"][0, :, 3] == 0xAB) and torch.all(hc["v_norm"][0, :, 3] == 7.0)
+
+
+def test_empty_append_is_a_no_op():
+    book, _ = books()
+    cache = C.allocate_cache(book, 1, 1)
+    view = C.cache_view(book, cache)
+    B.tq_quantize_append(book, None, None, B.TQ_BF16, 0, 1, None, view)
+    with pytest.raises(B.TQError):
+        B.tq_quantize_append(book, None, None, B.TQ_BF16, 1, 1, None, view)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_prefill_full_size_sampled(bits):
+    # 32768 tokens x 8 KV heads, Student-t(3) channels, in the benchmark's launch shape
+    cfg = W.CONFIGS["c3_prefill_quantize"]
+    book, ref = books(bits, bits, 128, seed=0)
+    g = generator(bits)
+    k = W.student_t_tokens(cfg["tokens"], cfg["n_kv"], cfg["student_t_channels"], torch.bfloat16, "cuda", g, 0)
+    v = W.student_t_tokens(cfg["tokens"], cfg["n_kv"], cfg["student_t_channels"], torch.bfloat16, "cuda", g, 1)
+    cache = C.allocate_cache(book, cfg["tokens"] // 64, cfg["n_kv"])
+    slots = np.arange(cfg["tokens"])
+    quantize_into(book, cache, k, v, slots)
+    sample = np.random.default_rng(bits).choice(cfg["tokens"], size=400, replace=False)
+    sample = np.concatenate([sample, [0, cfg["tokens"] - 1]])
+    rep = check_append(book, ref, cache, k, v, slots, sample=sample)
+    print("prefill bits=%d" % bits, rep)
+    assert B.tq_get_last_device_error(book) == 0
