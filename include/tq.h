@@ -166,6 +166,35 @@ tq_status tq_decode_finish(const tq_codebook* book, int batch, int n_q_heads,
                            const int32_t* context_lens, int max_context, int max_blocks, float* out,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the scratch array compiled into the library for
+ * tq_decode_attention_static: 16 MiB per GPU that loads the library, held
+ * until the process exits. */
+#define TQ_STATIC_WORKSPACE_BYTES (16u << 20)
+
+/* tq_decode_attention for callers that cannot allocate device memory (for
+ * example a serving runtime whose memory pool owns the whole GPU, or a loop
+ * where a device allocation and the synchronisation it may cause are not
+ * allowed).  Same arguments, checks and results as tq_decode_attention, but
+ * the split-K scratch is a fixed array inside the library instead of a
+ * caller-supplied workspace; the call allocates nothing.  The paper has no
+ * counterpart: this is an interface convenience, not part of the method.
+ * - Returns TQ_ERR_WORKSPACE when tq_decode_workspace_bytes(book, batch,
+ *   n_q_heads, max_context) exceeds TQ_STATIC_WORKSPACE_BYTES (e.g. 512
+ *   query vectors at context 8192 need about 5 MiB).
+ * - The first call on a device looks up the array's device address once (with
+ *   the handle's device made current briefly); make that first call before
+ *   any stream capture.
+ * - Every call on a device shares the one array, and a call leaves its
+ *   contents behind; nothing in it has to start at zero, because each call
+ *   writes every scratch value it reads.  Calls that overlap on the GPU
+ *   (different streams, or different threads without ordering) race on the
+ *   array and give wrong results: serialise them. */
+tq_status tq_decode_attention_static(const tq_codebook* book, const void* q, tq_dtype dtype, int batch,
+                                     int n_q_heads, int n_kv_heads, const tq_cache_view* cache,
+                                     const int32_t* block_table, int max_blocks,
+                                     const int32_t* context_lens, int max_context, float scale, float* out,
+                                     void* stream);
+
 /* Synchronise `stream`, then return (and clear) the first device-side error
  * code recorded since the last call: 0 none, 1 slot out of range in
  * quantize-append, 2 block id out of range in decode, 3 context length out of

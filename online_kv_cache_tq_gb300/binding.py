@@ -23,7 +23,7 @@ FIELDS = ("k_codes", "k_qjl", "k_norm", "k_rnorm", "v_codes", "v_norm")
 EXPORTED = ("tq_codebook_build", "tq_codebook_destroy", "tq_codebook_levels", "tq_codebook_matrices",
             "tq_cache_field_bytes", "tq_quantize_append", "tq_decode_workspace_bytes",
             "tq_decode_attention", "tq_decode_prepare", "tq_decode_partials", "tq_decode_finish",
-            "tq_get_last_device_error", "tq_status_string")
+            "tq_decode_attention_static", "tq_get_last_device_error", "tq_status_string")
 
 
 class TQError(RuntimeError):
@@ -74,6 +74,8 @@ def load():
     lib.tq_decode_partials.argtypes = [vp, i32, i32, i32, ctypes.POINTER(tq_cache_view), vp, i32, vp, i32,
                                        ctypes.c_float, vp, sz, vp]
     lib.tq_decode_finish.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, sz, vp]
+    lib.tq_decode_attention_static.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.POINTER(tq_cache_view), vp,
+                                               i32, vp, i32, ctypes.c_float, vp, vp]
     lib.tq_get_last_device_error.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.tq_status_string.argtypes = [i32]
     lib.tq_status_string.restype = ctypes.c_char_p
@@ -216,6 +218,15 @@ def tq_decode_finish(book, batch, n_q_heads, context_lens, max_context, max_bloc
     _check(load().tq_decode_finish(book.handle, batch, n_q_heads, _ptr(context_lens), max_context, max_blocks,
                                    _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)),
            "tq_decode_finish")
+
+
+def tq_decode_attention_static(book, q, dtype, batch, n_q_heads, n_kv_heads, view, block_table, max_blocks,
+                               context_lens, max_context, scale, out, stream=None):
+    """Decode attention with the library's built-in scratch (no workspace argument)."""
+    _check(load().tq_decode_attention_static(book.handle, _ptr(q), dtype, batch, n_q_heads, n_kv_heads,
+                                             ctypes.byref(view), _ptr(block_table), max_blocks, _ptr(context_lens),
+                                             max_context, scale, _ptr(out), _stream(stream)),
+           "tq_decode_attention_static")
 
 
 def tq_get_last_device_error(book, stream=None):
