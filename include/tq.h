@@ -56,7 +56,8 @@ typedef enum { TQ_BF16 = 0, TQ_FP32 = 1 } tq_dtype;
  * sketch, so k_bits is 2..5; with QJL off keys use k_bits MSE bits (1..4).
  * v_bits: value MSE bits (1..4).  qjl_m: QJL projection rows (0 = off, or
  * 128).  seed: seeds the SplitMix64 stream that draws R (Haar, via QR of a
- * Gaussian matrix) and S.  block_size: tokens per cache block (> 0). */
+ * Gaussian matrix) and S.  block_size: tokens per cache block, a multiple of
+ * 32 for device handles. */
 typedef struct {
   int d;
   int k_bits;
@@ -70,11 +71,15 @@ typedef struct tq_codebook tq_codebook; /* opaque, library-owned */
 
 /* The compressed cache: caller-owned device arrays, each laid out as
  * [num_blocks][n_kv_heads][block_size][item], item sizes from
- * tq_cache_field_bytes.  Codes are bit-planes: plane p holds bit p of every
- * code, coordinate j at bit j%8 of byte j/8 of the plane.  QJL bit k is bit
- * k%8 of byte k/8, set when the k-th projected residual is > 0.  Norms are
- * float32.  Every pointer must be 16-byte aligned; k_qjl/k_rnorm may be NULL
- * when qjl_m == 0. */
+ * tq_cache_field_bytes.  Key codes are bit-planes per token: plane p holds
+ * bit p of every code, coordinate j at bit j%8 of byte j/8 of the plane.
+ * Value codes are stored token-transposed inside each block so that decode
+ * can contract over tokens: the value field of one (block, head) is
+ * [v_bits][d][block_size/8] bytes, and for plane p and coordinate j, bit t%8
+ * of byte t/8 holds bit p of the code of the token at offset t (the same
+ * bytes per token as the key layout).  QJL bit k is bit k%8 of byte k/8, set
+ * when the k-th projected residual is > 0.  Norms are float32.  Every pointer
+ * must be 16-byte aligned; k_qjl/k_rnorm may be NULL when qjl_m == 0. */
 typedef struct {
   void* k_codes;
   void* k_qjl;

@@ -33,6 +33,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// 3-D map over head vectors x [n_tokens][n_kv][128] bf16: boxes of 64
+// columns x 1 head x 128 tokens (128-byte swizzle), so one tile holds 128
+// consecutive tokens of one head.
+bool encode_tokens_bf16(CUtensorMap* map, const void* base, uint64_t n_tokens, uint64_t n_kv) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr || n_tokens == 0 || n_kv == 0) return false;
+  cuuint64_t dims[3] = {128, n_kv, n_tokens};
+  cuuint64_t strides[2] = {128 * 2, n_kv * 128 * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t elem[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D map over a row-major [rows][128] bf16 array, 64 x 128 boxes, 128-byte
 // swizzle (the K-major operand layout of the tensor-core quantizer).
 bool encode_rows_bf16(CUtensorMap* map, const void* base, uint64_t rows) {
@@ -163,7 +178,9 @@ const float* table_field(const tq_codebook* b, size_t offset) {
 cudaError_t launch_quantize(const tq_codebook* b, const tq::QuantizeArgs& a, bool bf16, cudaStream_t s) {
   if (!bf16) return tq::launch_quantize_simt(a, false, b->num_sms, s);
   CUtensorMap x_map;
-  if (!encode_rows_bf16(&x_map, a.x, static_cast<uint64_t>(a.n_vec))) return cudaErrorInvalidValue;
+  if (!encode_tokens_bf16(&x_map, a.x, static_cast<uint64_t>(a.n_tokens), static_cast<uint64_t>(a.n_kv))) {
+    return cudaErrorInvalidValue;
+  }
   return tq::launch_quantize_tc(a, x_map, b->w_map, b->num_sms, s);
 }
 
@@ -185,6 +202,7 @@ tq_status tq_codebook_build(const tq_config* cfg, int device, tq_codebook** out)
   const int k_mse = cfg->qjl_m > 0 ? cfg->k_bits - 1 : cfg->k_bits;
   if (k_mse < 1 || k_mse > 4 || cfg->v_bits < 1 || cfg->v_bits > 4) return TQ_ERR_UNSUPPORTED;
   if (!host_only && (cfg->d != tq::kDim || (cfg->qjl_m != 0 && cfg->qjl_m != tq::kDim))) return TQ_ERR_UNSUPPORTED;
+  if (!host_only && cfg->block_size % 32 != 0) return TQ_ERR_UNSUPPORTED;
   tq_codebook* b = new (std::nothrow) tq_codebook();
   if (b == nullptr) return TQ_ERR_OOM;
   b->cfg = *cfg;
@@ -271,6 +289,7 @@ tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void*
   const bool bf16 = dtype == TQ_BF16;
   tq::QuantizeArgs a{};
   a.n_vec = n_tokens * n_kv_heads;
+  a.n_tokens = n_tokens;
   a.n_kv = n_kv_heads;
   a.slots = slot_mapping;
   a.num_blocks = cache->num_blocks;
@@ -285,6 +304,7 @@ tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void*
     a.norm = cache->k_norm;
     a.rnorm = book->cfg.qjl_m > 0 ? cache->k_rnorm : nullptr;
     a.bits = book->k_mse_bits;
+    a.transposed = false;
     a.levels = table_field(book, offsetof(tq::DeviceTables, k_levels));
     a.bounds = table_field(book, offsetof(tq::DeviceTables, k_bounds));
     if (launch_quantize(book, a, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;
@@ -296,6 +316,7 @@ tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void*
     a.norm = cache->v_norm;
     a.rnorm = nullptr;
     a.bits = book->v_bits;
+    a.transposed = true;
     a.levels = table_field(book, offsetof(tq::DeviceTables, v_levels));
     a.bounds = table_field(book, offsetof(tq::DeviceTables, v_bounds));
     if (launch_quantize(book, a, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;

@@ -205,24 +205,23 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(DecodeArgs a) {
   for (int g = 0; g < G; ++g)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[g][i] = 0.f;
-  const int vbytes = a.v_bits * 16;
   for (int tl = warp; tl < n_local; tl += kWarps) {
     const long long row = row_s[tl];
     if (row < 0) continue;
-    uint4 vw[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      vw[p] = p < a.v_bits ? reinterpret_cast<const uint4*>(a.v_codes + row * vbytes)[p] : make_uint4(0, 0, 0, 0);
-    }
+    // token-transposed value codes: bit (off % 32) of the word of this
+    // token's 32-token group, per plane and coordinate
+    const long long bh = row / a.block_size;          // (block * n_kv + head)
+    const int off = static_cast<int>(row - bh * a.block_size);
+    const unsigned* words = reinterpret_cast<const unsigned*>(a.v_codes);
+    const long long base = (bh * a.v_bits * 128) * (a.block_size / 32) + off / 32;
     const float nv = a.v_norm[row];
     float val[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       int code = 0;
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const unsigned w = i == 0 ? vw[p].x : i == 1 ? vw[p].y : i == 2 ? vw[p].z : vw[p].w;
-        code |= ((w >> lane) & 1) << p;
+      for (int p = 0; p < a.v_bits; ++p) {
+        const unsigned w = words[base + static_cast<long long>(p * 128 + lane + 32 * i) * (a.block_size / 32)];
+        code |= ((w >> (off & 31)) & 1) << p;
       }
       val[i] = nv * lv_s[code];
     }

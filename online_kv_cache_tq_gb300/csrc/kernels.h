@@ -12,9 +12,11 @@ namespace tq {
 enum DeviceError : int { kErrSlot = 1, kErrBlock = 2, kErrContext = 3, kErrTimeout = 4 };
 
 struct QuantizeArgs {
-  const void* x;          // [n_vec][128], bf16 or fp32
+  const void* x;          // [n_tokens][n_kv][128], bf16 or fp32
   int n_vec;              // n_tokens * n_kv_heads
+  int n_tokens;
   int n_kv;
+  bool transposed;        // codes field stored token-transposed (values)
   const int64_t* slots;   // [n_tokens]
   uint8_t* codes;         // field base, bits * 16 bytes per item
   uint8_t* qjl;           // field base, 16 bytes per item (null: no QJL)
@@ -32,9 +34,9 @@ struct QuantizeArgs {
 
 cudaError_t launch_quantize_simt(const QuantizeArgs& args, bool bf16, int num_sms, cudaStream_t stream);
 
-// bf16 inputs on the tensor cores; x_map tiles x as [n_vec][128] bf16 in
-// 64 x 128 boxes (128-byte swizzle), w_map tiles the handle's bf16 hi/lo
-// images of R and S' as [512][128].
+// bf16 inputs on the tensor cores; x_map tiles x as [n_tokens][n_kv][128]
+// bf16 in boxes of 64 columns x 1 head x 128 tokens (128-byte swizzle), w_map
+// tiles the handle's bf16 hi/lo images of R and S' as [512][128].
 cudaError_t launch_quantize_tc(const QuantizeArgs& args, const CUtensorMap& x_map, const CUtensorMap& w_map,
                                int num_sms, cudaStream_t stream);
 
@@ -65,6 +67,13 @@ struct DecodeArgs {
   const DeviceTables* tables;
   int* error;
 };
+
+// Word (uint32 units) of a token-transposed codes field holding plane p,
+// coordinate `dim` of the 32-token group of slot offset `off` in block `blk`.
+__host__ __device__ inline long long transposed_word(long long blk, int head, int n_kv, int bits, int p, int dim,
+                                                     int block_size, int off) {
+  return (((blk * n_kv + head) * bits + p) * 128 + dim) * (block_size / 32) + off / 32;
+}
 
 constexpr int kChunk = 512;       // context tokens per split-K work item
 constexpr int kPartStride = 132;  // m, l, 2 pad, acc[128]

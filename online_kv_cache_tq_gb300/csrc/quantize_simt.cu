@@ -129,13 +129,31 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantizeArgs a,
         for (int t = 0; t + 1 < n_levels; ++t) c += (y > bnd_s[t]) ? 1 : 0;
         code[i] = c;
       }
-      // Bit-planes: ballot over lanes gives word i of plane p directly.
-      for (int p = 0; p < a.bits; ++p) {
+      if (a.transposed) {
+        // token-transposed field: one bit per (plane, coordinate) in the word
+        // of this token's 32-token group; other tokens' bits are left alone
+        if (row >= 0) {
+          const long long blk = slot / a.block_size;
+          const int off = static_cast<int>(slot - blk * a.block_size);
+          unsigned* words = reinterpret_cast<unsigned*>(a.codes);
+          const unsigned mask = 1u << (off & 31);
+          for (int p = 0; p < a.bits; ++p) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const unsigned word = __ballot_sync(0xffffffffu, (code[i] >> p) & 1);
-          if (row >= 0 && lane == p * 4 + i) {
-            reinterpret_cast<unsigned*>(a.codes + row * row_bytes)[p * 4 + i] = word;
+            for (int i = 0; i < 4; ++i) {
+              unsigned* w = words + transposed_word(blk, head, a.n_kv, a.bits, p, lane + 32 * i, a.block_size, off);
+              if ((code[i] >> p) & 1) atomicOr(w, mask); else atomicAnd(w, ~mask);
+            }
+          }
+        }
+      } else {
+        // Bit-planes: ballot over lanes gives word i of plane p directly.
+        for (int p = 0; p < a.bits; ++p) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const unsigned word = __ballot_sync(0xffffffffu, (code[i] >> p) & 1);
+            if (row >= 0 && lane == p * 4 + i) {
+              reinterpret_cast<unsigned*>(a.codes + row * row_bytes)[p * 4 + i] = word;
+            }
           }
         }
       }

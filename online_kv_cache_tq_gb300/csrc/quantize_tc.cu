@@ -12,8 +12,14 @@
 // passes), and the fp32 residual is split too: Z = r_hi S'_hi^T + r_hi S'_lo^T
 // + r_lo S'_hi^T (three passes).  The split leaves a relative error near 2^-17.
 //
+// A tile is 128 consecutive tokens of one KV head (a 3-D TMA box), so each
+// epilogue warp holds 32 consecutive tokens of one head: value codes, which
+// the cache stores token-transposed, are transposed 32 x 32 bits at a time
+// with warp shuffles and stored as whole words when the 32 slots are
+// contiguous and aligned (prefill), or set bit by bit with atomics otherwise.
+//
 // One persistent CTA per SM, 6 warps:
-//   warp 0      TMA producer: R/S' hi/lo once, then 128-vector tiles of X;
+//   warp 0      TMA producer: R/S' hi/lo once, then 128-token tiles of X;
 //   warp 1      tcgen05.mma issuer (and owner of the tensor-memory columns);
 //   warps 2..5  epilogue, one thread per vector (tensor-memory lane): norm from
 //               the X tile, codes and bit-planes from Y, residual hi/lo written
@@ -53,12 +59,26 @@ struct Layout {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Lane i holds row i of a 32 x 32 bit matrix (bit j = column j); afterwards
+// lane j holds column j (bit i = row i).  Five butterfly stages.
+__device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
+  const uint32_t masks[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    const int sh = 16 >> k;
+    const uint32_t m = masks[k];
+    const uint32_t o = __shfl_xor_sync(0xffffffffu, x, sh);
+    x = (lane & sh) ? ((x & ~m) | ((o & ~m) >> sh)) : ((x & m) | ((o & m) << sh));
+  }
+  return x;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <int BITS, bool QJL>
+template <int BITS, bool QJL, bool TRANS>
 __global__ void __launch_bounds__(kThreads, 1)
     quantize_tc_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map,
                        QuantizeArgs a) {
@@ -75,7 +95,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int n_tiles = (a.n_vec + kTileRows - 1) / kTileRows;
+  const int n_tt = (a.n_tokens + kTileRows - 1) / kTileRows;   // token tiles per head
+  const int n_tiles = n_tt * a.n_kv;
   volatile int* abort = &abort_s;
 
   if (tid == 0) {
@@ -119,8 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ptx::wait_bar(&x_empty[s], ph ^ 1, abort, a.error, kErrTimeout)) break;
         ptx::mbar_arrive_expect_tx(&x_full[s], kMatBytes);
         for (int kb = 0; kb < 2; ++kb)
-          ptx::tma_load_2d(smem + L::kX0 + s * kMatBytes + kb * kHalfBytes, &x_map, &x_full[s], kb * kKBlock,
-                           tile * kTileRows);
+          ptx::tma_load_3d(smem + L::kX0 + s * kMatBytes + kb * kHalfBytes, &x_map, &x_full[s], kb * kKBlock,
+                           tile / n_tt, (tile % n_tt) * kTileRows);
         last_stage = s;
         last_phase = ph;
       }
@@ -223,17 +244,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float n = sqrtf(ss);
       const float inv = n > 0.f ? 1.f / n : 0.f;
 
-      const int v = tile * kTileRows + row;
+      const int head = tile / n_tt;
+      const int token = (tile % n_tt) * kTileRows + row;
       long long dst = -1;
-      if (v < a.n_vec) {
-        const int token = v / a.n_kv;
-        const int head = v - token * a.n_kv;
-        const long long slot = a.slots[token];
+      long long slot = -1;
+      if (token < a.n_tokens) {
+        slot = a.slots[token];
         if (slot >= 0 && slot < cache_rows) {
           const long long blk = slot / a.block_size;
           dst = (blk * a.n_kv + head) * a.block_size + (slot - blk * a.block_size);
         } else if (slot >= cache_rows) {
           atomicCAS(a.error, 0, kErrSlot);
+          slot = -1;
         }
       }
 
@@ -283,12 +305,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(&y_empty);
-      if (dst >= 0) {
+      if (TRANS) {
+        // token-transposed codes: whole words when the warp's 32 slots are
+        // contiguous and start a 32-token group, single bits otherwise
+        const long long slot0 = __shfl_sync(0xffffffffu, slot, 0);
+        const bool aligned = __all_sync(0xffffffffu, dst >= 0 && slot == slot0 + lane && (slot0 & 31) == 0);
+        unsigned* words = reinterpret_cast<unsigned*>(a.codes);
+        if (aligned) {
+          const long long blk = slot0 / a.block_size;
+          const int off0 = static_cast<int>(slot0 - blk * a.block_size);
+#pragma unroll
+          for (int p = 0; p < BITS; ++p)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              words[transposed_word(blk, head, a.n_kv, BITS, p, 32 * c + lane, a.block_size, off0)] =
+                  transpose32(planes[p][c], lane);
+        } else if (dst >= 0) {
+          const long long blk = slot / a.block_size;
+          const int off = static_cast<int>(slot - blk * a.block_size);
+          const unsigned mask = 1u << (off & 31);
+          for (int p = 0; p < BITS; ++p)
+            for (int c = 0; c < 4; ++c)
+              for (int j = 0; j < 32; ++j) {
+                unsigned* w = words + transposed_word(blk, head, a.n_kv, BITS, p, 32 * c + j, a.block_size, off);
+                if ((planes[p][c] >> j) & 1) atomicOr(w, mask); else atomicAnd(w, ~mask);
+              }
+        }
+      } else if (dst >= 0) {
         uint4* out = reinterpret_cast<uint4*>(a.codes + dst * (BITS * 16));
 #pragma unroll
         for (int p = 0; p < BITS; ++p) out[p] = make_uint4(planes[p][0], planes[p][1], planes[p][2], planes[p][3]);
-        a.norm[dst] = n;
       }
+      if (dst >= 0) a.norm[dst] = n;
       if (QJL) {
         ptx::fence_async_shared();
         ptx::mbar_arrive(&res_full);
@@ -322,15 +370,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BITS, bool QJL>
+template <int BITS, bool QJL, bool TRANS>
 cudaError_t launch_bits(const CUtensorMap& x_map, const CUtensorMap& w_map, const QuantizeArgs& a, int grid,
                         cudaStream_t stream) {
   const int smem = Layout<QJL>::kBytes + 1024;
-  cudaError_t err = cudaFuncSetAttribute(quantize_tc_kernel<BITS, QJL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem);
+  cudaError_t err = cudaFuncSetAttribute(quantize_tc_kernel<BITS, QJL, TRANS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  quantize_tc_kernel<BITS, QJL><<<grid, kThreads, smem, stream>>>(x_map, w_map, a);
+  quantize_tc_kernel<BITS, QJL, TRANS><<<grid, kThreads, smem, stream>>>(x_map, w_map, a);
   return cudaGetLastError();
+}
+
+template <int BITS>
+cudaError_t launch_kind(const CUtensorMap& x_map, const CUtensorMap& w_map, const QuantizeArgs& a, int grid,
+                        cudaStream_t stream) {
+  if (a.qjl != nullptr) return launch_bits<BITS, true, false>(x_map, w_map, a, grid, stream);
+  if (a.transposed) return launch_bits<BITS, false, true>(x_map, w_map, a, grid, stream);
+  return launch_bits<BITS, false, false>(x_map, w_map, a, grid, stream);
 }
 
 }  // namespace
@@ -338,18 +394,14 @@ cudaError_t launch_bits(const CUtensorMap& x_map, const CUtensorMap& w_map, cons
 cudaError_t launch_quantize_tc(const QuantizeArgs& a, const CUtensorMap& x_map, const CUtensorMap& w_map,
                                int num_sms, cudaStream_t stream) {
   if (a.n_vec <= 0) return cudaSuccess;
-  const int n_tiles = (a.n_vec + kTileRows - 1) / kTileRows;
+  if (a.qjl != nullptr && a.transposed) return cudaErrorInvalidValue;
+  const int n_tiles = ((a.n_tokens + kTileRows - 1) / kTileRows) * a.n_kv;
   const int grid = n_tiles < num_sms ? n_tiles : num_sms;
-  const bool qjl = a.qjl != nullptr;
-  switch (a.bits * 2 + (qjl ? 1 : 0)) {
-    case 2: return launch_bits<1, false>(x_map, w_map, a, grid, stream);
-    case 3: return launch_bits<1, true>(x_map, w_map, a, grid, stream);
-    case 4: return launch_bits<2, false>(x_map, w_map, a, grid, stream);
-    case 5: return launch_bits<2, true>(x_map, w_map, a, grid, stream);
-    case 6: return launch_bits<3, false>(x_map, w_map, a, grid, stream);
-    case 7: return launch_bits<3, true>(x_map, w_map, a, grid, stream);
-    case 8: return launch_bits<4, false>(x_map, w_map, a, grid, stream);
-    case 9: return launch_bits<4, true>(x_map, w_map, a, grid, stream);
+  switch (a.bits) {
+    case 1: return launch_kind<1>(x_map, w_map, a, grid, stream);
+    case 2: return launch_kind<2>(x_map, w_map, a, grid, stream);
+    case 3: return launch_kind<3>(x_map, w_map, a, grid, stream);
+    case 4: return launch_kind<4>(x_map, w_map, a, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

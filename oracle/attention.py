@@ -46,13 +46,17 @@ def attend(query, khat, qjl_term, vhat, scale):
 
 
 def read_sequence(cache, table_row, length, head, block_size):
-    """Rows of every cache field for tokens 0..length-1 of one sequence/head."""
+    """Rows of every token-major cache field, and the value codes, for tokens
+    0..length-1 of one sequence/head (value codes as ``v_code_values``)."""
     n_kv = cache["k_norm"].shape[1]
-    slots = np.arange(length, dtype=np.int64)
-    blocks = np.asarray(table_row, dtype=np.int64)[slots // block_size]
-    rows = (blocks * n_kv + head) * block_size + slots % block_size
+    pos = np.arange(length, dtype=np.int64)
+    blocks = np.asarray(table_row, dtype=np.int64)[pos // block_size]
+    rows = (blocks * n_kv + head) * block_size + pos % block_size
     out = {}
     for name, arr in cache.items():
+        if name == "v_codes":
+            out["v_code_values"] = packing.read_value_codes(arr, blocks * block_size + pos % block_size, head)
+            continue
         flat = arr.reshape(arr.shape[0] * arr.shape[1] * arr.shape[2], -1)
         out[name] = flat[rows]
     return out
@@ -79,6 +83,6 @@ def decode_attention(query, cache, table_row, length, kv_head, book, scale=None)
         corr = qjl_estimate(query, rows["k_rnorm"].reshape(-1), signs, book["proj"])
     else:
         corr = np.zeros(length)
-    v_codes = packing.unpack_planes(rows["v_codes"], book["v_bits"], d)
+    v_codes = rows["v_code_values"]
     vhat = reconstruct_mse(rows["v_norm"].reshape(-1), v_codes, book["rot"], book["v_levels"])
     return attend(query, khat, corr, vhat, scale), float(np.max(np.linalg.norm(vhat, axis=1)))

@@ -70,7 +70,10 @@ def field_bytes(book):
 def empty_cache(book, num_blocks, n_kv_heads, block_size):
     cache = {}
     for name, nbytes in field_bytes(book).items():
-        if name.endswith("norm"):
+        if name == "v_codes":
+            cache[name] = np.zeros((num_blocks, n_kv_heads, book["v_bits"], book["d"], block_size // 8),
+                                   dtype=np.uint8)
+        elif name.endswith("norm"):
             cache[name] = np.zeros((num_blocks, n_kv_heads, block_size), dtype=np.float32)
         else:
             cache[name] = np.zeros((num_blocks, n_kv_heads, block_size, nbytes), dtype=np.uint8)
@@ -86,7 +89,13 @@ def append(cache, book, k, v, slots):
     n_tok = k.shape[0]
     keys = encode_keys(k.reshape(n_tok * n_kv, -1), book)
     vals = encode_values(v.reshape(n_tok * n_kv, -1), book)
+    live = [t for t in range(n_tok) if slots[t] >= 0]
+    for h in range(n_kv):
+        codes = vals["codes"].reshape(n_tok, n_kv, -1)[live, h]
+        packing.write_value_codes(cache["v_codes"], codes, np.asarray(slots)[live], h)
     for name in field_bytes(book):
+        if name == "v_codes":
+            continue
         src = (keys if name.startswith("k_") else vals)[name]
         src = src.reshape(n_tok, n_kv, *src.shape[1:])
         flat = cache[name].reshape(num_blocks * n_kv * block_size, *cache[name].shape[3:])

@@ -11,8 +11,15 @@ norm (§2 第二階段) -- but not the byte layout.  Readings taken:
 * QJL signs: bit k (LSB first in byte k div 8) is 1 exactly when the k-th
   projected residual is > 0 (intelliparadigm.com §2.1.2 keeps
   ``projected > 0``).
-* Paging: slot s lives in block s div block_size at offset s mod block_size;
-  every field is an array [num_blocks][n_kv_heads][block_size][bytes_per_item].
+* Paging: slot s lives in block s div block_size at offset s mod block_size.
+  Key fields and all norms are arrays [num_blocks][n_kv_heads][block_size][item]
+  (one row per token).
+* Value codes are stored token-transposed inside a block (a reading chosen so
+  that decode can contract over tokens): the value field is
+  [num_blocks][n_kv_heads][bits][d][block_size / 8]; for plane p and
+  coordinate j, bit (t mod 8) of byte (t div 8) holds bit p of the code of the
+  token at offset t.  Per block and head this is the same bits * d *
+  block_size / 8 bytes as the token-major form.
 """
 import numpy as np
 
@@ -56,3 +63,33 @@ def slot_index(slot, head, n_kv_heads, block_size):
     block = slot // block_size
     offset = slot % block_size
     return (block * n_kv_heads + head) * block_size + offset
+
+
+def write_value_codes(field, codes, slots, head):
+    """Store codes [N, d] of tokens at ``slots`` (one KV head) into a value
+    field [num_blocks][n_kv][bits][d][block_size / 8] (uint8, in place)."""
+    bits, d, nbytes = field.shape[2], field.shape[3], field.shape[4]
+    block_size = nbytes * 8
+    codes = np.asarray(codes, dtype=np.int64)
+    for n, slot in enumerate(np.asarray(slots, dtype=np.int64)):
+        block, off = int(slot) // block_size, int(slot) % block_size
+        for p in range(bits):
+            for j in range(d):
+                byte = field[block, head, p, j, off // 8]
+                bit = (int(codes[n, j]) >> p) & 1
+                byte = (int(byte) & ~(1 << (off % 8))) | (bit << (off % 8))
+                field[block, head, p, j, off // 8] = byte
+
+
+def read_value_codes(field, slots, head):
+    """Codes [N, d] of the tokens at ``slots`` (one KV head) from a value field."""
+    bits, d, nbytes = field.shape[2], field.shape[3], field.shape[4]
+    block_size = nbytes * 8
+    slots = np.asarray(slots, dtype=np.int64)
+    block, off = slots // block_size, slots % block_size
+    codes = np.zeros((len(slots), d), dtype=np.int64)
+    for p in range(bits):
+        for j in range(d):
+            byte = field[block, head, p, j, off // 8].astype(np.int64)
+            codes[:, j] |= ((byte >> (off % 8)) & 1) << p
+    return codes

@@ -62,12 +62,10 @@ def rows_at(hcache, name, slots, n_kv, block_size):
     return flat[idx]
 
 
-def check_mse_codes(x, packed, norm_gpu, ref, which):
-    """Compare GPU codes/norms with the oracle for vectors x [N][d] (fp64)."""
-    bits = ref[which + "_bits"]
+def check_mse_codes(x, got, norm_gpu, ref, which):
+    """Compare GPU codes [N][d] and norms with the oracle for vectors x [N][d] (fp64)."""
     bounds = ref[which + "_bounds"]
     norm, y, codes = quantize.encode_mse(x, ref["rot"], bounds)
-    got = packing.unpack_planes(packed, bits, x.shape[1])
     diff = got != codes
     exempt = quantize.boundary_distance(y, bounds) < CODE_EXEMPT
     bad = diff & ~exempt
@@ -103,9 +101,14 @@ def check_append(book, ref, cache, k, v, slots, sample=None):
         if x_t is None:
             continue
         x = x_t[torch.as_tensor(toks, device=x_t.device)].double().cpu().numpy().reshape(-1, 128)
-        packed = rows_at(hc, which + "_codes", slots[toks], n_kv, bs).reshape(len(x), -1)
+        if which == "k":
+            packed = rows_at(hc, "k_codes", slots[toks], n_kv, bs).reshape(len(x), -1)
+            got = packing.unpack_planes(packed, ref["k_bits"], 128)
+        else:
+            got = np.stack([packing.read_value_codes(hc["v_codes"], slots[toks], h) for h in range(n_kv)], axis=1)
+            got = got.reshape(len(x), -1)
         norm = rows_at(hc, which + "_norm", slots[toks], n_kv, bs).reshape(-1)
-        diffs, exempt, codes = check_mse_codes(x, packed, norm, ref, which)
+        diffs, exempt, codes = check_mse_codes(x, got, norm, ref, which)
         report[which + "_exempt_code_diffs"] = diffs
         report[which + "_near_boundary"] = exempt
         if which == "k" and ref["qjl_m"]:

@@ -227,6 +227,30 @@ def test_packing_round_trip(bits):
     assert np.array_equal(packing.unpack_planes(packed, bits, 128), codes)
 
 
+def test_value_packing_hand_worked_case():
+    field = np.zeros((1, 1, 2, 2, 1), dtype=np.uint8)
+    codes = np.array([[(t + j) % 4 for j in range(2)] for t in range(8)])
+    packing.write_value_codes(field, codes, np.arange(8), 0)
+    for line in _golden_lines("value_packing.txt"):
+        where, byte = line.split("|")
+        p, j = (int(v) for v in where.split())
+        assert field[0, 0, p, j, 0] == int(byte, 16)
+    assert np.array_equal(packing.read_value_codes(field, np.arange(8), 0), codes)
+
+
+def test_value_packing_round_trip_keeps_other_tokens_and_heads():
+    rng = np.random.default_rng(8)
+    field = rng.integers(0, 256, size=(3, 2, 3, 128, 8), dtype=np.uint8)
+    before = field.copy()
+    slots = np.array([5, 70, 191, 64])
+    codes = rng.integers(0, 8, size=(4, 128))
+    packing.write_value_codes(field, codes, slots, 1)
+    assert np.array_equal(packing.read_value_codes(field, slots, 1), codes)
+    assert np.array_equal(field[:, 0], before[:, 0])
+    others = np.setdiff1d(np.arange(192), slots)
+    assert np.array_equal(packing.read_value_codes(field, others, 1), packing.read_value_codes(before, others, 1))
+
+
 def test_slot_index_layout():
     # [num_blocks][n_kv][block_size] rows: slot 70, head 1, 3 heads, 64-token blocks
     assert packing.slot_index(70, 1, 3, 64) == (1 * 3 + 1) * 64 + 6

@@ -31,6 +31,7 @@ def test_single_head_fp32_outliers_every_vector():
 
 @pytest.mark.parametrize("k_bits,v_bits", [(2, 2), (3, 3), (4, 4), (5, 1), (4, 2)])
 def test_bf16_gqa_ragged_shuffled_slots(k_bits, v_bits):
+    # shuffled slots: value codes take the bit-by-bit path
     book, ref = books(k_bits, v_bits, 128, seed=3)
     n_tok, n_kv = 1001, 3                 # 3003 vectors: 24 tiles of 128 and a ragged tail
     g = generator(k_bits * 10 + v_bits)
@@ -81,6 +82,30 @@ def test_zero_vectors_negative_and_out_of_range_slots(dtype):
     check_append(book, ref, cache, k, v, slots, sample=valid)
     hc = {n: t.cpu() for n, t in cache.items()}
     assert torch.all(hc["k_codes"][0, :, 3] == 0xAB) and torch.all(hc["v_norm"][0, :, 3] == 7.0)
+    # untouched value-code bits (token offset 3, and offsets 10..63) keep their old contents
+    vbits = np.unpackbits(hc["v_codes"].numpy()[0], axis=-1, bitorder="little")   # [head][plane][dim][64]
+    assert np.all(vbits[..., 3] == 1) and np.all(vbits[..., 10:] == np.unpackbits(np.uint8(0xAB), bitorder="little")[
+        np.arange(10, 64) % 8])
+
+
+@pytest.mark.parametrize("n_tok", [64, 1000, 2048])
+def test_bf16_contiguous_prefill_and_partial_blocks(n_tok):
+    # contiguous slots from offset 0 (whole 32-token words) and an offset start
+    # (a partial first and last word): both value-code paths, then a second
+    # append that overwrites part of the first
+    book, ref = books(3, 3, 128, seed=7)
+    n_kv = 4
+    g = generator(n_tok)
+    scales = W.channel_scales(2, n_kv, (0.1, 10.0), 3, 30.0)
+    num_blocks = (n_tok + 100) // 64 + 2
+    cache = C.allocate_cache(book, num_blocks, n_kv)
+    for start in (0, 37):
+        k = W.gaussian_tokens(n_tok, scales, torch.bfloat16, "cuda", g)
+        v = W.gaussian_tokens(n_tok, scales, torch.bfloat16, "cuda", g)
+        slots = np.arange(start, start + n_tok)
+        quantize_into(book, cache, k, v, slots)
+        check_append(book, ref, cache, k, v, slots)
+    assert B.tq_get_last_device_error(book) == 0
 
 
 def test_empty_append_is_a_no_op():
