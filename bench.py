@@ -225,7 +225,8 @@ class DecodeWorkload:
         self.out = torch.empty((self.batch, self.n_q, 128), dtype=torch.float32, device="cuda")
         self.ws, self.ws_bytes = C.allocate_workspace(self.book, self.batch, self.n_q, self.max_ctx)
         torch.cuda.synchronize()
-        self.launches_per_step = 5      # quantize K, quantize V, prepare, partials, finish
+        # quantize (K and V share one launch up to 1024 head vectors per tensor), prepare, partials, finish
+        self.launches_per_step = (1 if self.batch * self.n_kv <= 1024 else 2) + 3
 
     def step(self, i, ev=None):
         B = self.B
@@ -433,7 +434,8 @@ def main(argv=None):
     ms_per_step = max_ms / args.steps
     peak, peak_src = hbm_peak()
     achieved = wl.cache_bytes / (attn_ms * 1e-3) / 1e9
-    kernel = "attention_kernel<%d>" % (wl.n_q // wl.n_kv)
+    tc = wl.B.tq_decode_kernel_kind(wl.book, wl.n_q, wl.n_kv)
+    kernel = ("attention_tc_kernel<%d>" if tc else "attention_kernel<%d>") % (wl.n_q // wl.n_kv)
     line = {
         "metric": METRIC, "value": world * wl.batch / (ms_per_step * 1e-3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,

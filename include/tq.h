@@ -200,6 +200,12 @@ tq_status tq_decode_attention_static(const tq_codebook* book, const void* q, tq_
                                      const int32_t* context_lens, int max_context, float scale, float* out,
                                      void* stream);
 
+/* Which decode-partials kernel tq_decode_attention / tq_decode_partials run
+ * for this shape: *tensor_cores = 1 for the tensor-core kernel (fp8 sign-plane
+ * GEMMs; shapes with n_q_heads / n_kv_heads in {1, 2, 4, 8} whose operands fit
+ * in tensor memory), 0 for the CUDA-core kernel.  Host only; launches nothing. */
+tq_status tq_decode_kernel_kind(const tq_codebook* book, int n_q_heads, int n_kv_heads, int* tensor_cores);
+
 /* Synchronise `stream`, then return (and clear) the first device-side error
  * code recorded since the last call: 0 none, 1 slot out of range in
  * quantize-append, 2 block id out of range in decode, 3 context length out of

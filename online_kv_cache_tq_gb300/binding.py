@@ -23,7 +23,8 @@ FIELDS = ("k_codes", "k_qjl", "k_norm", "k_rnorm", "v_codes", "v_norm")
 EXPORTED = ("tq_codebook_build", "tq_codebook_destroy", "tq_codebook_levels", "tq_codebook_matrices",
             "tq_cache_field_bytes", "tq_quantize_append", "tq_decode_workspace_bytes",
             "tq_decode_attention", "tq_decode_prepare", "tq_decode_partials", "tq_decode_finish",
-            "tq_decode_attention_static", "tq_get_last_device_error", "tq_status_string")
+            "tq_decode_attention_static", "tq_decode_kernel_kind", "tq_get_last_device_error",
+            "tq_status_string")
 
 
 class TQError(RuntimeError):
@@ -76,6 +77,7 @@ def load():
     lib.tq_decode_finish.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, sz, vp]
     lib.tq_decode_attention_static.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.POINTER(tq_cache_view), vp,
                                                i32, vp, i32, ctypes.c_float, vp, vp]
+    lib.tq_decode_kernel_kind.argtypes = [vp, i32, i32, ctypes.POINTER(i32)]
     lib.tq_get_last_device_error.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.tq_status_string.argtypes = [i32]
     lib.tq_status_string.restype = ctypes.c_char_p
@@ -227,6 +229,14 @@ def tq_decode_attention_static(book, q, dtype, batch, n_q_heads, n_kv_heads, vie
                                              ctypes.byref(view), _ptr(block_table), max_blocks, _ptr(context_lens),
                                              max_context, scale, _ptr(out), _stream(stream)),
            "tq_decode_attention_static")
+
+
+def tq_decode_kernel_kind(book, n_q_heads, n_kv_heads):
+    """1 when decode partials run on the tensor cores for this shape, else 0."""
+    flag = ctypes.c_int()
+    _check(load().tq_decode_kernel_kind(book.handle, n_q_heads, n_kv_heads, ctypes.byref(flag)),
+           "tq_decode_kernel_kind")
+    return flag.value
 
 
 def tq_get_last_device_error(book, stream=None):

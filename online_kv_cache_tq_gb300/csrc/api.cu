@@ -1,4 +1,5 @@
 // C ABI of the engine: handle lifetime, host-side argument checks, launches.
+#include <algorithm>
 #include <cmath>
 #include <cstddef>
 #include <cstring>
@@ -107,6 +108,40 @@ float bf16_value(uint16_t bits) {
   return out;
 }
 
+// Sign-plane coefficients of a codebook (see DeviceTables); returns whether
+// they reproduce every level to 1e-12 relative (an odd-symmetric codebook).
+bool walsh_coefficients(const std::vector<double>& levels, int bits, float* out) {
+  const int count = 1 << bits;
+  const int planes = 1 << (bits - 1);
+  std::vector<double> coef(planes, 0.0);
+  double scale = 0.0;
+  for (double c : levels) scale = std::max(scale, std::fabs(c));
+  for (int s = 0; s < planes; ++s) {
+    const int set = tq::kWalshSets[bits - 1][s];
+    for (int code = 0; code < count; ++code) {
+      double sign = 1.0;
+      for (int p = 0; p < bits; ++p)
+        if (set & (1 << p)) sign *= ((code >> p) & 1) ? 1.0 : -1.0;
+      coef[s] += levels[code] * sign;
+    }
+    coef[s] /= count;
+  }
+  bool ok = true;
+  for (int code = 0; code < count; ++code) {
+    double v = 0.0;
+    for (int s = 0; s < planes; ++s) {
+      const int set = tq::kWalshSets[bits - 1][s];
+      double sign = 1.0;
+      for (int p = 0; p < bits; ++p)
+        if (set & (1 << p)) sign *= ((code >> p) & 1) ? 1.0 : -1.0;
+      v += coef[s] * sign;
+    }
+    if (std::fabs(v - levels[code]) > 1e-12 * scale) ok = false;
+  }
+  for (int s = 0; s < 8; ++s) out[s] = s < planes ? static_cast<float>(coef[s]) : 0.f;
+  return ok;
+}
+
 tq_status upload_tables(tq_codebook* b) {
   const int d = b->cfg.d;
   const int m = b->cfg.qjl_m;
@@ -138,6 +173,8 @@ tq_status upload_tables(tq_codebook* b) {
     t.k_bounds[i] = i < static_cast<int>(h.k_bounds.size()) ? static_cast<float>(h.k_bounds[i]) : INFINITY;
     t.v_bounds[i] = i < static_cast<int>(h.v_bounds.size()) ? static_cast<float>(h.v_bounds[i]) : INFINITY;
   }
+  b->walsh_ok = walsh_coefficients(h.k_levels, b->k_mse_bits, t.k_walsh) &&
+                walsh_coefficients(h.v_levels, b->v_bits, t.v_walsh);
   std::vector<tq::DeviceTables> tv(1, t);
   std::vector<int> zero(1, 0);
   cudaError_t err = upload(&b->d_R, R);
@@ -174,7 +211,8 @@ const float* table_field(const tq_codebook* b, size_t offset) {
   return reinterpret_cast<const float*>(reinterpret_cast<const char*>(b->d_tables) + offset);
 }
 
-// bf16 inputs go to the tensor-core quantizer, fp32 inputs to the SIMT one.
+// Larger bf16 batches go to the tensor-core quantizer, larger fp32 batches to
+// the SIMT one (small batches are handled by tq_quantize_append directly).
 cudaError_t launch_quantize(const tq_codebook* b, const tq::QuantizeArgs& a, bool bf16, cudaStream_t s) {
   if (!bf16) return tq::launch_quantize_simt(a, false, b->num_sms, s);
   CUtensorMap x_map;
@@ -287,40 +325,42 @@ tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void*
   if (static_cast<long long>(n_tokens) * n_kv_heads > (1ll << 31) - 1) return TQ_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf16 = dtype == TQ_BF16;
-  tq::QuantizeArgs a{};
-  a.n_vec = n_tokens * n_kv_heads;
-  a.n_tokens = n_tokens;
-  a.n_kv = n_kv_heads;
-  a.slots = slot_mapping;
-  a.num_blocks = cache->num_blocks;
-  a.block_size = cache->block_size;
-  a.Rt = book->d_Rt;
-  a.Spt = book->d_Spt;
-  a.error = book->d_error;
-  if (k) {
-    a.x = k;
-    a.codes = static_cast<uint8_t*>(cache->k_codes);
-    a.qjl = book->cfg.qjl_m > 0 ? static_cast<uint8_t*>(cache->k_qjl) : nullptr;
-    a.norm = cache->k_norm;
-    a.rnorm = book->cfg.qjl_m > 0 ? cache->k_rnorm : nullptr;
-    a.bits = book->k_mse_bits;
-    a.transposed = false;
-    a.levels = table_field(book, offsetof(tq::DeviceTables, k_levels));
-    a.bounds = table_field(book, offsetof(tq::DeviceTables, k_bounds));
-    if (launch_quantize(book, a, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;
+  tq::QuantizeArgs base{};
+  base.n_vec = n_tokens * n_kv_heads;
+  base.n_tokens = n_tokens;
+  base.n_kv = n_kv_heads;
+  base.slots = slot_mapping;
+  base.num_blocks = cache->num_blocks;
+  base.block_size = cache->block_size;
+  base.Rt = book->d_Rt;
+  base.Spt = book->d_Spt;
+  base.error = book->d_error;
+  tq::QuantizeArgs ka = base, va = base;
+  ka.x = k;
+  ka.codes = static_cast<uint8_t*>(cache->k_codes);
+  ka.qjl = book->cfg.qjl_m > 0 ? static_cast<uint8_t*>(cache->k_qjl) : nullptr;
+  ka.norm = cache->k_norm;
+  ka.rnorm = book->cfg.qjl_m > 0 ? cache->k_rnorm : nullptr;
+  ka.bits = book->k_mse_bits;
+  ka.transposed = false;
+  ka.levels = table_field(book, offsetof(tq::DeviceTables, k_levels));
+  ka.bounds = table_field(book, offsetof(tq::DeviceTables, k_bounds));
+  va.x = v;
+  va.codes = static_cast<uint8_t*>(cache->v_codes);
+  va.qjl = nullptr;
+  va.norm = cache->v_norm;
+  va.rnorm = nullptr;
+  va.bits = book->v_bits;
+  va.transposed = true;
+  va.levels = table_field(book, offsetof(tq::DeviceTables, v_levels));
+  va.bounds = table_field(book, offsetof(tq::DeviceTables, v_bounds));
+  if (base.n_vec <= tq::kSmallQuantize) {
+    // a decode step: keys and values in one launch, one CTA per vector
+    return tq::launch_quantize_small(k ? &ka : nullptr, v ? &va : nullptr, bf16, s) == cudaSuccess ? TQ_OK
+                                                                                                    : TQ_ERR_CUDA;
   }
-  if (v) {
-    a.x = v;
-    a.codes = static_cast<uint8_t*>(cache->v_codes);
-    a.qjl = nullptr;
-    a.norm = cache->v_norm;
-    a.rnorm = nullptr;
-    a.bits = book->v_bits;
-    a.transposed = true;
-    a.levels = table_field(book, offsetof(tq::DeviceTables, v_levels));
-    a.bounds = table_field(book, offsetof(tq::DeviceTables, v_bounds));
-    if (launch_quantize(book, a, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;
-  }
+  if (k && launch_quantize(book, ka, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;
+  if (v && launch_quantize(book, va, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;
   return TQ_OK;
 }
 
@@ -410,6 +450,12 @@ tq_status decode_args(const tq_codebook* book, int stages, const void* q, tq_dty
 
 tq_status launched(cudaError_t err) { return err == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
 
+// Tensor-core partials where supported, SIMT otherwise.
+cudaError_t launch_partials(const tq_codebook* book, const tq::DecodeArgs& a, cudaStream_t s) {
+  if (tq::tc_decode_supported(a, book->walsh_ok)) return tq::launch_decode_partials_tc(a, s);
+  return tq::launch_decode_partials(a, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -426,7 +472,7 @@ tq_status tq_decode_attention(const tq_codebook* book, const void* q, tq_dtype d
   if (st != TQ_OK || batch == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = launched(tq::launch_decode_prepare(a, dtype == TQ_BF16, s));
-  if (st == TQ_OK) st = launched(tq::launch_decode_partials(a, s));
+  if (st == TQ_OK) st = launched(launch_partials(book, a, s));
   if (st == TQ_OK) st = launched(tq::launch_decode_finish(a, s));
   return st;
 }
@@ -448,7 +494,7 @@ tq_status tq_decode_partials(const tq_codebook* book, int batch, int n_q_heads, 
   tq_status st = decode_args(book, kPartials, nullptr, TQ_FP32, batch, n_q_heads, n_kv_heads, cache, block_table,
                              max_blocks, context_lens, max_context, scale, nullptr, workspace, workspace_bytes, &a);
   if (st != TQ_OK || batch == 0) return st;
-  return launched(tq::launch_decode_partials(a, static_cast<cudaStream_t>(stream)));
+  return launched(launch_partials(book, a, static_cast<cudaStream_t>(stream)));
 }
 
 tq_status tq_decode_finish(const tq_codebook* book, int batch, int n_q_heads, const int32_t* context_lens,
@@ -459,6 +505,21 @@ tq_status tq_decode_finish(const tq_codebook* book, int batch, int n_q_heads, co
                              context_lens, max_context, 0.f, out, workspace, workspace_bytes, &a);
   if (st != TQ_OK || batch == 0) return st;
   return launched(tq::launch_decode_finish(a, static_cast<cudaStream_t>(stream)));
+}
+
+tq_status tq_decode_kernel_kind(const tq_codebook* book, int n_q_heads, int n_kv_heads, int* tensor_cores) {
+  if (!valid_device_handle(book) || tensor_cores == nullptr || n_q_heads <= 0 || n_kv_heads <= 0 ||
+      n_q_heads % n_kv_heads != 0) {
+    return TQ_ERR_INVALID_ARG;
+  }
+  tq::DecodeArgs a{};
+  a.group = n_q_heads / n_kv_heads;
+  a.block_size = book->cfg.block_size;
+  a.k_bits = book->k_mse_bits;
+  a.v_bits = book->v_bits;
+  a.k_qjl = book->cfg.qjl_m > 0 ? reinterpret_cast<const uint8_t*>(1) : nullptr;
+  *tensor_cores = tq::tc_decode_supported(a, book->walsh_ok) ? 1 : 0;
+  return TQ_OK;
 }
 
 tq_status tq_get_last_device_error(const tq_codebook* book, void* stream, int* code) {

@@ -34,6 +34,12 @@ struct QuantizeArgs {
 
 cudaError_t launch_quantize_simt(const QuantizeArgs& args, bool bf16, int num_sms, cudaStream_t stream);
 
+// Small batches (up to kSmallQuantize vectors per tensor): one CTA per
+// vector; K and V (either may be null) share one launch.
+constexpr int kSmallQuantize = 1024;
+cudaError_t launch_quantize_small(const QuantizeArgs* first, const QuantizeArgs* second, bool bf16,
+                                  cudaStream_t stream);
+
 // bf16 inputs on the tensor cores; x_map tiles x as [n_tokens][n_kv][128]
 // bf16 in boxes of 64 columns x 1 head x 128 tokens (128-byte swizzle), w_map
 // tiles the handle's bf16 hi/lo images of R and S' as [512][128].
@@ -80,6 +86,12 @@ constexpr int kPartStride = 132;  // m, l, 2 pad, acc[128]
 
 cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_t stream);
 cudaError_t launch_decode_partials(const DecodeArgs& args, cudaStream_t stream);
+
+// Tensor-core partials (fp8 sign planes, decode_tc.cu) for the shapes it
+// supports: G in {1, 2, 4, 8}, tensor-memory columns within 512, and
+// odd-symmetric codebooks; the SIMT kernel serves every other shape.
+bool tc_decode_supported(const DecodeArgs& args, bool walsh_ok);
+cudaError_t launch_decode_partials_tc(const DecodeArgs& args, cudaStream_t stream);
 cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream);
 
 }  // namespace tq

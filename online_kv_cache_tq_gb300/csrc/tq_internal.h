@@ -22,7 +22,17 @@ struct DeviceTables {
   float k_bounds[kMaxLevels];
   float v_levels[kMaxLevels];
   float v_bounds[kMaxLevels];
+  // Coefficients of a codebook written in sign planes: with s_p = 2 bit_p - 1
+  // for the bits of a code, level(code) = sum_S walsh[S] * prod_{p in S} s_p
+  // over the odd subsets S (1 plane at 1 bit, 2 at 2 bits, 4 at 3 bits:
+  // {0},{1},{2},{0,1,2}; 8 at 4 bits: {0},{1},{2},{3},{0,1,2},{0,1,3},{0,2,3},
+  // {1,2,3}).  Exact for the symmetric Lloyd-Max codebooks.
+  float k_walsh[8];
+  float v_walsh[8];
 };
+
+// Odd sign-plane subsets, as bit masks over the code bits, in walsh[] order.
+constexpr int kWalshSets[4][8] = {{1}, {1, 2}, {1, 2, 4, 7}, {1, 2, 4, 8, 7, 11, 13, 14}};
 
 // Host-side construction products (fp64), independent of any device.
 struct HostTables {
@@ -55,4 +65,5 @@ struct tq_codebook {
   int* d_error;       // first device-side error code, 0 when none
   int num_sms;
   CUtensorMap w_map;  // TMA map of d_rot_tc as [512][128] bf16
+  bool walsh_ok;      // both codebooks are exactly odd-symmetric (sign-plane decode usable)
 };
