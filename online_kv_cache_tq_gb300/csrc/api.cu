@@ -364,13 +364,28 @@ tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void*
   return TQ_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Per query head: the tensor-core score operand pieces (only for codebooks
+// the tensor-core decode can take).
+size_t bk_bytes(const tq_codebook* book) {
+  if (!book->walsh_ok || book->k_mse_bits < 1 || book->k_mse_bits > 4) return 0;
+  return static_cast<size_t>(tq::bk_head_bytes(book->k_mse_bits, book->cfg.qjl_m > 0));
+}
+
+}  // namespace
+
+extern "C" {
+
 size_t tq_decode_workspace_bytes(const tq_codebook* book, int batch, int n_q_heads, int max_context) {
   if (book == nullptr || batch <= 0 || n_q_heads <= 0 || max_context < 0) return 0;
   const size_t vecs = static_cast<size_t>(batch) * n_q_heads;
   const size_t q_bytes = round_up(vecs * 2 * tq::kDim * sizeof(float));
   const size_t part_bytes =
       round_up(vecs * static_cast<size_t>(max_chunks_for(max_context)) * tq::kPartStride * sizeof(float));
-  return q_bytes + part_bytes;
+  return q_bytes + part_bytes + round_up(vecs * bk_bytes(book));
 }
 
 }  // extern "C"
@@ -440,6 +455,11 @@ tq_status decode_args(const tq_codebook* book, int stages, const void* q, tq_dty
   a->ws_q = static_cast<float*>(workspace);
   a->ws_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(vecs * 2 * tq::kDim * sizeof(float)));
   a->max_chunks = max_chunks_for(max_context);
+  const size_t bk = bk_bytes(book);
+  a->ws_bk = bk == 0 ? nullptr
+                     : reinterpret_cast<uint8_t*>(a->ws_part) +
+                           round_up(vecs * static_cast<size_t>(a->max_chunks) * tq::kPartStride * sizeof(float));
+  a->bk_stride = static_cast<int>(bk);
   a->R = book->d_R;
   a->Rt = book->d_Rt;
   a->Spt = book->d_Spt;
@@ -518,6 +538,7 @@ tq_status tq_decode_kernel_kind(const tq_codebook* book, int n_q_heads, int n_kv
   a.k_bits = book->k_mse_bits;
   a.v_bits = book->v_bits;
   a.k_qjl = book->cfg.qjl_m > 0 ? reinterpret_cast<const uint8_t*>(1) : nullptr;
+  a.ws_bk = bk_bytes(book) > 0 ? reinterpret_cast<uint8_t*>(1) : nullptr;   // null checks only
   *tensor_cores = tq::tc_decode_supported(a, book->walsh_ok) ? 1 : 0;
   return TQ_OK;
 }

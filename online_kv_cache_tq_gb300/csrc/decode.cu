@@ -15,6 +15,7 @@
 // (m, l, acc[128]) that the combine kernel merges.
 #include <cuda_bf16.h>
 
+#include "e4m3_pieces.cuh"
 #include "kernels.h"
 
 namespace tq {
@@ -31,10 +32,13 @@ __device__ __forceinline__ float load_elem(const void* base, long long idx, bool
 
 __device__ __forceinline__ void record(int* error, int code) { atomicCAS(error, 0, code); }
 
-// ws_q[vec] = (R q, S' R q).
+// ws_q[vec] = (R q, S' R q); with ws_bk, also the tensor-core score operand
+// of this query head: e4m3 pieces of sigma_0 a_S (R q) per key sign plane S
+// and of sigma_1 S' R q (sigma_0, sigma_1 powers of two that bound the pieces).
 __global__ void __launch_bounds__(kThreads) qprep_kernel(DecodeArgs a, bool bf16) {
   __shared__ float q_s[kDim];
   __shared__ float qr_s[kDim];
+  __shared__ float red_s[2][kWarps];
   const int vec = blockIdx.x;
   const int o = threadIdx.x;
   q_s[o] = load_elem(a.q, static_cast<long long>(vec) * kDim + o, bf16);
@@ -44,10 +48,42 @@ __global__ void __launch_bounds__(kThreads) qprep_kernel(DecodeArgs a, bool bf16
   qr_s[o] = acc;
   a.ws_q[static_cast<long long>(vec) * 2 * kDim + o] = acc;
   __syncthreads();
+  float z = 0.f;
   if (a.qjl_m > 0) {
-    float z = 0.f;
     for (int j = 0; j < kDim; ++j) z = fmaf(a.Spt[j * kDim + o], qr_s[j], z);
     a.ws_q[static_cast<long long>(vec) * 2 * kDim + kDim + o] = z;
+  }
+  if (a.ws_bk == nullptr) return;
+  const int planes = 1 << (a.k_bits - 1);
+  float amax = 0.f;
+  for (int s = 0; s < planes; ++s) amax = fmaxf(amax, fabsf(a.tables->k_walsh[s]));
+  float m0 = fabsf(acc) * amax, m1 = fabsf(z);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+  }
+  if ((o & 31) == 0) {
+    red_s[0][o >> 5] = m0;
+    red_s[1][o >> 5] = m1;
+  }
+  __syncthreads();
+  for (int w = 0; w < kWarps; ++w) {
+    m0 = fmaxf(m0, red_s[0][w]);
+    m1 = fmaxf(m1, red_s[1][w]);
+  }
+  const float sig0 = piece_scale(m0), sig1 = piece_scale(m1);
+  uint8_t* dst = a.ws_bk + static_cast<long long>(vec) * a.bk_stride;
+  const int kpos = k_position(o);
+  for (int s = 0; s < planes; ++s)
+    write_pieces_rows<kQPieces>(dst + s * kQPieces * 128, kpos, a.tables->k_walsh[s] * acc * sig0);
+  if (a.qjl_m > 0) write_pieces_rows<kQPieces>(dst + planes * kQPieces * 128, kpos, z * sig1);
+  if (o == 0) {
+    float* hdr = reinterpret_cast<float*>(dst + (planes + (a.qjl_m > 0 ? 1 : 0)) * kQPieces * 128);
+    hdr[0] = sig0;
+    hdr[1] = sig1;
+    hdr[2] = 1.f / sig0;      // exact: powers of two
+    hdr[3] = 1.f / sig1;
   }
 }
 

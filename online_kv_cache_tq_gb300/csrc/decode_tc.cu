@@ -29,14 +29,20 @@
 // kernel writes, merged by the same finish kernel.
 //
 // One CTA of 256 threads per (512-token chunk, KV head, sequence); threads t
-// and t + 128 share tensor-memory lane t and split its work (sign planes,
-// accumulator columns, softmax-weight pieces) between them.  At the start, thread 0 copies the chunk's packed
-// fields (whole cache blocks, contiguous per block and head) into shared
-// memory with bulk asynchronous copies while all threads build B_K.  Thread 0
-// issues the MMAs between barriers and alone waits on their completion (time-
-// bounded mbarrier waits, error code 4); the others wait at the barrier.
+// and t + 128 share tensor-memory lane t and split its work: each builds two
+// of the four 32-bit words of every sign plane, half of the accumulator
+// columns and half of the operand pieces.  Lane k of warp 0 copies block k
+// of the chunk's packed fields (contiguous per block and head) into shared
+// memory with bulk asynchronous copies while all threads move the query
+// pieces that the prepare step built (B_K) into the swizzled operand layout.
+// The sign planes go to two alternating tensor-memory slots, so the planes of
+// the next tile (or value-plane pair) are built while the MMAs of the previous
+// one run; an elected lane of warp 0 issues the MMAs after one barrier per
+// tile and every thread waits on the MMA mbarrier itself (time-bounded, error
+// code 4) before it reuses a slot or reads accumulators.
 #include <cuda_fp8.h>
 
+#include "e4m3_pieces.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
 
@@ -46,17 +52,11 @@ namespace {
 constexpr int kTile = 128;                  // tokens per tile = tensor-memory lanes
 constexpr int kTiles = kChunk / kTile;      // tiles per chunk
 constexpr int kThreads = 256;               // two threads per tensor-memory lane
-constexpr int kQPieces = 6;                 // e4m3 pieces of a query coefficient
 constexpr int kVPieces = 3;                 // e4m3 pieces of a softmax weight
 
 __host__ __device__ constexpr int round16(int x) { return (x + 15) / 16 * 16; }
 __host__ __device__ constexpr int score_cols(int g) { return round16(kQPieces * g); }   // per group
 __host__ __device__ constexpr int value_cols(int g) { return round16(kVPieces * g); }   // per value plane
-
-// Position along K of coordinate (or token) i inside a 128-element block: the
-// e4m3 operand byte built from bit i sits at 32 (i/32) + 4 (i%8) + (i%32)/8,
-// because one 32-bit register is built from bits i, i+8, i+16, i+24 of a word.
-__device__ __forceinline__ int k_position(int i) { return 32 * (i >> 5) + 4 * (i & 7) + ((i & 31) >> 3); }
 
 // Byte offset of (row n, K position k) in a K-major operand stored with the
 // 128-byte swizzle (rows of 128 bytes, 16-byte chunk c of row n at c ^ (n % 8)).
@@ -87,21 +87,6 @@ __device__ __forceinline__ uint32_t plane_word(uint32_t b0, uint32_t b1, uint32_
   return (b0 & m0) ^ (b1 & m1) ^ (b2 & m2) ^ (b3 & m3);
 }
 
-__device__ __forceinline__ uint8_t to_e4m3(float x) {
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
-}
-__device__ __forceinline__ float from_e4m3(uint8_t b) {
-  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b), __NV_E4M3);
-  return __half2float(__half(h));
-}
-
-// Power of two sigma with sigma * maxabs <= 200 (so every e4m3 piece stays
-// below the format's 448 limit), 1 when maxabs is 0.
-__device__ __forceinline__ float piece_scale(float maxabs) {
-  if (!(maxabs > 0.f)) return 1.f;
-  return exp2f(floorf(log2f(200.f / maxabs)));
-}
-
 // Write the e4m3 pieces of y (row `row0 + i` for piece i): each piece is the
 // e4m3 rounding of what the previous pieces left, times 16.
 template <int N>
@@ -114,12 +99,21 @@ __device__ __forceinline__ void write_pieces(uint8_t* b, int row0, int kpos, flo
   }
 }
 
-// 16^-i for the piece index i (an exact power of two built from its exponent
-// field, so no call is left for the compiler to make).
-__device__ __forceinline__ float inv16_pow(int i) { return __int_as_float((127 - 4 * i) << 23); }
+// Two values at once (one paired conversion each way): pieces of ya go to rows
+// row_a + i, of yb to rows row_b + i.
+template <int N>
+__device__ __forceinline__ void write_pieces2(uint8_t* b, int row_a, int row_b, int kpos, float ya, float yb) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(make_float2(ya, yb), __NV_SATFINITE, __NV_E4M3);
+    b[sw128(row_a + i, kpos)] = static_cast<uint8_t>(p & 0xFFu);
+    b[sw128(row_b + i, kpos)] = static_cast<uint8_t>(p >> 8);
+    const float2 back = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(p, __NV_E4M3)));
+    ya = (ya - back.x) * 16.f;
+    yb = (yb - back.y) * 16.f;
+  }
+}
 
-// Reduce N values per thread over warps [w0, w0 + nw) of the block at once
-// (one pair of barriers for all N); every thread gets the results of its range.
 template <int N, typename Op>
 __device__ __forceinline__ void block_reduce(float (&v)[N], float* red, int w0, int nw, Op op) {
 #pragma unroll
@@ -151,32 +145,26 @@ __device__ __forceinline__ int context_of(const DecodeArgs& a, int b) {
   return ctx;
 }
 
-// Build sign planes [s0, s1) of one tensor-memory row from bit-plane words
-// bw[p][c] and store plane s at column 32 s; with `last_is_sign` the last
-// plane is the QJL sign word sgn[c] instead.
-__device__ __forceinline__ void store_planes(uint32_t row_addr, const uint32_t (&bw)[4][4], int bits, int s0, int s1,
-                                             bool last_is_sign, const uint32_t (&sgn)[4]) {
-  for (int s = s0; s < s1; ++s) {
-    const bool sign = last_is_sign && s == s1 - 1;
-    const int set = walsh_set(bits, s);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t w = sign ? sgn[c] : plane_word(bw[0][c], bw[1][c], bw[2][c], bw[3][c], set);
-      store_signs(row_addr + 32 * s + 8 * c, w);
-    }
-  }
-}
-
 }  // namespace
 
 // Tensor-memory columns and dynamic shared memory the kernel needs.
+//
+// Key phase: k_slots slots of kp = 32 (pk + pq) columns (the sign planes of
+// one tile), then the score accumulators (n1 mse + n2 qjl columns).  Value
+// phase (after every score has been read, so it reuses the same columns): two
+// slots of 64 columns (two value sign planes each), then pv accumulator blocks
+// of no columns.  Two key slots are used when they fit beside the rest; the
+// allocation is a power of two of at least 32 columns.
 struct TcLayout {
   int pk, pq, pv;           // key sign planes, QJL plane (0/1), value sign planes
   int n1, n2, no;           // score columns (mse, qjl), value columns per plane
+  int kp, k_slots;          // columns per key slot, key slots (1 or 2)
   int col_s, col_o, cols, tmem;
   int kbytes, vblock;       // key code bytes per token; value code bytes per (block, head)
-  int off_bmse, off_bqjl, off_bv, off_scores, off_qjl, off_kc, off_kq, off_kn, off_kr, off_vn, off_vc, smem_bytes;
+  int off_bmse, off_bqjl, off_bv, off_s0, off_s1, off_kc, off_kq, off_kn, off_kr, off_vn, off_vc, smem_bytes;
 };
+
+constexpr int kValueSlot = 64;              // columns of one value slot (two sign planes)
 
 TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size) {
   TcLayout l{};
@@ -186,12 +174,17 @@ TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size) 
   l.n1 = score_cols(group);
   l.n2 = qjl ? l.n1 : 0;
   l.no = value_cols(group);
-  // The value phase starts after every score column has been read, so its
-  // sign planes and accumulators reuse the key phase's columns.
-  l.col_s = 32 * (l.pk + l.pq);
-  l.col_o = 32 * l.pv;
-  const int key_cols = l.col_s + l.n1 + l.n2, value_cols_total = l.col_o + l.pv * l.no;
-  l.cols = key_cols > value_cols_total ? key_cols : value_cols_total;
+  l.kp = 32 * (l.pk + l.pq);
+  const int vcols = 2 * kValueSlot + l.pv * l.no;
+  auto kcols = [&](int slots) { return slots * l.kp + l.n1 + l.n2; };
+  auto mx = [](int x, int y) { return x > y ? x : y; };
+  if (mx(kcols(2), vcols) <= 256) l.k_slots = 2;
+  else if (mx(kcols(1), vcols) <= 256) l.k_slots = 1;
+  else if (mx(kcols(2), vcols) <= 512) l.k_slots = 2;
+  else l.k_slots = 1;
+  l.col_s = l.k_slots * l.kp;
+  l.col_o = 2 * kValueSlot;
+  l.cols = mx(kcols(l.k_slots), vcols);
   l.tmem = 32;
   while (l.tmem < l.cols) l.tmem *= 2;
   l.kbytes = k_bits * 16;
@@ -200,8 +193,8 @@ TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size) 
   l.off_bmse = o; o += l.n1 * l.pk * 128;
   l.off_bqjl = o; o += l.n2 * 128;
   l.off_bv = o; o += kTiles * l.no * 128;
-  l.off_scores = o; o += group * kChunk * 4;
-  l.off_qjl = o; o += group * kTile * 4;
+  l.off_s0 = o; o += group * kChunk * 4;
+  l.off_s1 = o; o += group * kChunk * 4;
   l.off_kc = o; o += kChunk * l.kbytes;
   l.off_kq = o; o += kChunk * 16;
   l.off_kn = o; o += kChunk * 4;
@@ -209,8 +202,23 @@ TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size) 
   l.off_vn = o; o += kChunk * 4;
   l.off_vc = o; o += (kChunk / block_size) * l.vblock;
   l.smem_bytes = o + 1024;
+  // more than half of tensor memory: keep a second CTA off the SM instead of
+  // letting it wait in the allocator
+  if (l.tmem > 256 && l.smem_bytes < 120 * 1024) l.smem_bytes = 120 * 1024;
   return l;
 }
+
+namespace {
+
+// Time-bounded wait on an mbarrier phase by the calling thread (suspending
+// between polls); false after a timeout anywhere in the CTA.
+// The result is made warp-uniform, since tensor-memory loads and stores that
+// follow are warp-collective.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort, int* error) {
+  return __all_sync(0xffffffffu, ptx::wait_bar(bar, parity, abort, error, kErrTimeout));
+}
+
+}  // namespace
 
 template <int G>
 __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a, TcLayout L) {
@@ -231,38 +239,42 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   uint8_t* b_mse = smem + L.off_bmse;
   uint8_t* b_qjl = smem + L.off_bqjl;
   uint8_t* b_v = smem + L.off_bv;
-  float* scores = reinterpret_cast<float*>(smem + L.off_scores);   // [G][kChunk]
-  float* qjl_part = reinterpret_cast<float*>(smem + L.off_qjl);    // [G][kTile]
+  float* s0 = reinterpret_cast<float*>(smem + L.off_s0);           // [G][kChunk] mse part, then the weights
+  float* s1 = reinterpret_cast<float*>(smem + L.off_s1);           // [G][kChunk] qjl part, then output halves
   uint8_t* kc_s = smem + L.off_kc;                                  // [kChunk][kbytes]
   uint8_t* kq_s = smem + L.off_kq;                                  // [kChunk][16]
   float* kn_s = reinterpret_cast<float*>(smem + L.off_kn);
   float* kr_s = reinterpret_cast<float*>(smem + L.off_kr);
   float* vn_s = reinterpret_cast<float*>(smem + L.off_vn);
   uint32_t* vc_s = reinterpret_cast<uint32_t*>(smem + L.off_vc);   // [blk][plane][dim][bs/32]
-  __shared__ __align__(8) uint64_t bar_in, bar_s, bar_o;
+  __shared__ __align__(8) uint64_t bar_in, bar_s, bar_v[2], bar_d;
   __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_s, ok_s;
+  __shared__ int abort_s;
   __shared__ float red_s[(kThreads / 32) * (G + 1)];
-  __shared__ float sig_s[2][G];                 // piece scales of the mse / qjl columns
   __shared__ float stat_s[2][G];                // chunk max, chunk sum per head
   __shared__ int blk_ok_s[kChunk / 32];         // physical block of each block slot is valid
   __shared__ float sv_s;                        // piece scale of the softmax weights
+  __shared__ float vw_s[8];                     // odd Walsh coefficients of the value codebook
 
   const int t = threadIdx.x;
   const int lane = t & (kTile - 1);             // tensor-memory lane (token or coordinate)
   const int half = t >> 7;                      // which of the two threads of the lane
+  const int w0 = 2 * half;                      // this thread's words of every sign plane: w0, w0 + 1
   const uint32_t row_addr = static_cast<uint32_t>(((t >> 5) & 3) * 32) << 16;
   const bool qjl = a.k_qjl != nullptr;
   const int qbase = b * a.n_q + kvh * G;
   volatile int* abort = &abort_s;
 
   // zero the B operands (padding rows must be 0)
-  for (int i = t; i < L.off_scores / 16; i += kThreads) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = t; i < L.off_s0 / 16; i += kThreads) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  if (t < 8) vw_s[t] = a.tables->v_walsh[t];
   if (t == 0) {
     abort_s = 0;
     ptx::mbar_init(&bar_in, 1);
     ptx::mbar_init(&bar_s, 1);
-    ptx::mbar_init(&bar_o, 1);
+    ptx::mbar_init(&bar_v[0], 1);
+    ptx::mbar_init(&bar_v[1], 1);
+    ptx::mbar_init(&bar_d, 32);
     ptx::fence_mbar_init();
   }
   if (t < 32) {
@@ -273,32 +285,30 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
-  // ---- prefetch the chunk's packed fields into shared memory ----
-  if (t == 0) {
-    uint32_t total = 0;
-    for (int k = 0; k < n_blk; ++k) {
-      const int lblk = (start / bs) + k;
-      const int phys = a.block_table ? a.block_table[static_cast<long long>(b) * a.max_blocks + lblk]
-                                     : b * a.max_blocks + lblk;
-      const bool valid = phys >= 0 && phys < a.num_blocks;
-      blk_ok_s[k] = valid;
-      if (!valid) {
-        atomicCAS(a.error, 0, kErrBlock);
-        continue;
-      }
-      const int rows = min(bs, (n_local - k * bs + 31) / 32 * 32);
+  // ---- prefetch the chunk's packed fields into shared memory (lane k of warp 0: block k) ----
+  if (t < 32) {
+    bool valid = false;
+    long long phys = 0;
+    int rows = 0;
+    uint32_t bytes = 0;
+    if (t < n_blk) {
+      const int lblk = (start / bs) + t;
+      phys = a.block_table ? a.block_table[static_cast<long long>(b) * a.max_blocks + lblk]
+                           : static_cast<long long>(b) * a.max_blocks + lblk;
+      valid = phys >= 0 && phys < a.num_blocks;
+      blk_ok_s[t] = valid;
+      if (!valid) atomicCAS(a.error, 0, kErrBlock);
+      rows = min(bs, (n_local - t * bs + 31) / 32 * 32);
       // key codes, key norm, value norm (+ QJL signs and residual norm) per row, value block
-      total += rows * (L.kbytes + 4 + 4 + (qjl ? 16 + 4 : 0)) + L.vblock;
+      if (valid) bytes = rows * (L.kbytes + 4 + 4 + (qjl ? 16 + 4 : 0)) + L.vblock;
     }
-    ptx::mbar_arrive_expect_tx(&bar_in, total);
-    for (int k = 0; k < n_blk; ++k) {
-      if (!blk_ok_s[k]) continue;
-      const int lblk = (start / bs) + k;
-      const int phys = a.block_table ? a.block_table[static_cast<long long>(b) * a.max_blocks + lblk]
-                                     : b * a.max_blocks + lblk;
-      const int rows = min(bs, (n_local - k * bs + 31) / 32 * 32);
-      const long long r0 = (static_cast<long long>(phys) * a.n_kv + kvh) * bs;    // first row of this block
-      const int tl0 = k * bs;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, off);
+    if (t == 0) ptx::mbar_arrive_expect_tx(&bar_in, bytes);
+    __syncwarp();
+    if (valid) {
+      const long long r0 = (phys * a.n_kv + kvh) * bs;    // first row of this block
+      const int tl0 = t * bs;
       ptx::bulk_load(kc_s + tl0 * L.kbytes, a.k_codes + r0 * L.kbytes, rows * L.kbytes, &bar_in);
       if (qjl) {
         ptx::bulk_load(kq_s + tl0 * 16, a.k_qjl + r0 * 16, rows * 16, &bar_in);
@@ -306,142 +316,155 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       }
       ptx::bulk_load(kn_s + tl0, a.k_norm + r0, rows * 4, &bar_in);
       ptx::bulk_load(vn_s + tl0, a.v_norm + r0, rows * 4, &bar_in);
-      ptx::bulk_load(vc_s + k * (L.vblock / 4), a.v_codes + (static_cast<long long>(phys) * a.n_kv + kvh) * L.vblock,
-                     L.vblock, &bar_in);
+      ptx::bulk_load(vc_s + t * (L.vblock / 4), a.v_codes + (phys * a.n_kv + kvh) * L.vblock, L.vblock, &bar_in);
     }
   }
 
-  // ---- B_K: e4m3 pieces of a_S q_rot per key sign plane, and of q_s ----
-  // (overlaps the copies; half 0 writes the mse operand, half 1 the qjl one)
+  // ---- B_K: the group's prepared score operand pieces, into the swizzled layout ----
+  // (overlaps the copies) row n = h kQPieces + i of plane s; 16-byte chunk c
+  // of a row lands at c ^ (n % 8)
+  float inv_sig[G];                             // 1 / sigma of this thread's accumulator columns
   {
-    const int d = lane;
-    const int kpos = k_position(d);
-    float amax = 0.f;
-    for (int s = 0; s < L.pk; ++s) amax = fmaxf(amax, fabsf(a.tables->k_walsh[s]));
-    float m[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float* src = a.ws_q + static_cast<long long>(qbase + h) * 2 * kDim;
-      m[h] = fabsf(half == 0 ? src[d] * amax : (qjl ? src[kDim + d] : 0.f));
+    const int nk = L.pk + L.pq;
+    const int per_head = nk * kQPieces * 8;     // 16-byte chunks per head
+    for (int idx = t; idx < G * per_head; idx += kThreads) {
+      const int h = idx / per_head, r = idx - h * per_head;
+      const int s = r / (kQPieces * 8), i = (r / 8) % kQPieces, c = r % 8;
+      const uint4 v = reinterpret_cast<const uint4*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride)[r];
+      const int n = h * kQPieces + i;
+      uint8_t* dst = s < L.pk ? b_mse + s * L.n1 * 128 : b_qjl;
+      *reinterpret_cast<uint4*>(dst + n * 128 + ((c ^ (n & 7)) << 4)) = v;
     }
-    // max over this half's 128 values (warps 4 half .. 4 half + 3)
-    block_reduce(m, red_s, 4 * half, 4, MaxOp());
-    if (lane == 0)
 #pragma unroll
-      for (int h = 0; h < G; ++h) sig_s[half][h] = piece_scale(m[h]);
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float* src = a.ws_q + static_cast<long long>(qbase + h) * 2 * kDim;
-      if (half == 0) {
-        const float q = src[d] * sig_s[0][h];
-        for (int s = 0; s < L.pk; ++s)
-          write_pieces<kQPieces>(b_mse + s * L.n1 * 128, h * kQPieces, kpos, a.tables->k_walsh[s] * q);
-      } else if (qjl) {
-        write_pieces<kQPieces>(b_qjl, h * kQPieces, kpos, src[kDim + d] * sig_s[1][h]);
-      }
-    }
+    for (int h = 0; h < G; ++h)
+      inv_sig[h] = reinterpret_cast<const float*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride +
+                                                  nk * kQPieces * 128)[2 + half];
   }
   ptx::fence_async_shared();
-  if (t == 0) ok_s = ptx::wait_bar(&bar_in, 0, abort, a.error, kErrTimeout);
-  __syncthreads();
-  bool ok = ok_s;
+  bool ok = wait_phase(&bar_in, 0, abort, a.error);
+  ok = __syncthreads_and(ok);
 
   const uint32_t idesc_s = ptx::idesc_e4m3_f32(128, N1);
   const uint32_t idesc_o = ptx::idesc_e4m3_f32(128, NO);
-  uint32_t ph_s = 0, ph_o = 0;
+  // operand descriptors and accumulator addresses, ready before the issue points
+  // (the start-address field counts 16-byte units: +2 per 32-byte K step)
+  const uint64_t desc_mse = ptx::desc_k_sw128(ptx::smem_u32(b_mse));
+  const uint64_t desc_qjl = ptx::desc_k_sw128(ptx::smem_u32(b_qjl));
+  const uint64_t desc_v = ptx::desc_k_sw128(ptx::smem_u32(b_v));
+  const uint32_t mse_plane_step = (L.n1 * 128) >> 4, v_tile_step = (L.no * 128) >> 4;
+  const uint32_t d_mse = tmem + L.col_s;
   const int nk_planes = L.pk + L.pq;
-  const int k_split = (nk_planes + 1) / 2;        // half 0 builds planes [0, k_split), half 1 the rest
 
-  // ---- scores, one 128-token tile at a time ----
-  for (int tile = 0; tile < n_tiles && ok; ++tile) {
-    const int tl = tile * kTile + lane;
+  // accumulators of key tile i -> s0 (half 0: n_k <q_rot, k_mse> / sigma) and
+  // s1 (half 1: gamma coef <q_s, signs> / sigma)
+  auto read_scores = [&](int i) {
+    const int tl = i * kTile + lane;
     const bool valid = tl < n_local && blk_ok_s[tl / bs];
-    {
-      uint32_t bw[4][4] = {};
-      uint32_t sgn[4] = {};
-      if (valid) {
-        const uint4* kc = reinterpret_cast<const uint4*>(kc_s + tl * L.kbytes);
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          if (p < a.k_bits) {
-            const uint4 w = kc[p];
-            bw[p][0] = w.x; bw[p][1] = w.y; bw[p][2] = w.z; bw[p][3] = w.w;
-          }
-        }
-        if (qjl) {
-          const uint4 w = reinterpret_cast<const uint4*>(kq_s + tl * 16)[0];
-          sgn[0] = w.x; sgn[1] = w.y; sgn[2] = w.z; sgn[3] = w.w;
-        }
-      }
-      const int s0 = half == 0 ? 0 : k_split, s1 = half == 0 ? k_split : nk_planes;
-      store_planes(tmem + row_addr, bw, a.k_bits, s0, s1, qjl && s1 == nk_planes, sgn);
-    }
-    ptx::tmem_wait_st();
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (t == 0) {
-      ptx::tc_fence_after();
-      for (int s = 0; s < L.pk; ++s)
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_e4m3_tmem_a(tmem + L.col_s, tmem + 32 * s + 8 * kk,
-                               ptx::desc_k_sw128(ptx::smem_u32(b_mse + s * L.n1 * 128) + 32 * kk), idesc_s,
-                               (s | kk) != 0);
-      if (qjl)
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_e4m3_tmem_a(tmem + L.col_s + L.n1, tmem + 32 * L.pk + 8 * kk,
-                               ptx::desc_k_sw128(ptx::smem_u32(b_qjl) + 32 * kk), idesc_s, kk != 0);
-      ptx::mma_commit(&bar_s);
-      ok_s = ptx::wait_bar(&bar_s, ph_s, abort, a.error, kErrTimeout);
-    }
-    ph_s ^= 1;
-    __syncthreads();
-    ok = ok_s;
-    if (!ok) break;
-    ptx::tc_fence_after();
-    // half 0 combines the mse columns, half 1 the qjl columns of the lane's token
+    if (half == 1 && !qjl) return;
     float acc[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) acc[h] = 0.f;
-    if (half == 0 || qjl) {
 #pragma unroll
-      for (int c0 = 0; c0 < N1; c0 += 16) {
-        uint32_t v[16];
-        ptx::tmem_ld16(tmem + row_addr + L.col_s + half * N1 + c0, v);
+    for (int c0 = 0; c0 < N1; c0 += 16) {
+      uint32_t v[16];
+      ptx::tmem_ld16(tmem + row_addr + L.col_s + half * N1 + c0, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int h = (c0 + i) / kQPieces, piece = (c0 + i) % kQPieces;
-          if (h < G) acc[h] = fmaf(__uint_as_float(v[i]), inv16_pow(piece), acc[h]);
+      for (int j = 0; j < 16; ++j) {
+        const int h = (c0 + j) / kQPieces, piece = (c0 + j) % kQPieces;
+        if (h < G) acc[h] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), acc[h]);
+      }
+    }
+    const float f = valid ? (half == 0 ? kn_s[tl] : kr_s[tl] * a.qjl_coef) : 0.f;
+    float* dst = half == 0 ? s0 : s1;
+#pragma unroll
+    for (int h = 0; h < G; ++h) dst[h * kChunk + tl] = f * (acc[h] * inv_sig[h]);
+  };
+
+  // ---- scores: sign planes of tile i are built while the MMAs of tile i - 1 run ----
+  for (int i = 0; i < n_tiles && ok; ++i) {
+    const int slot = L.k_slots == 2 ? (i & 1) : 0;
+    if (L.k_slots == 1 && i > 0) {
+      ok = wait_phase(&bar_s, (i - 1) & 1, abort, a.error);
+      ptx::tc_fence_after();
+      if (ok) read_scores(i - 1);
+    }
+    if (ok) {
+      const int tl = i * kTile + lane;
+      const bool valid = tl < n_local && blk_ok_s[tl / bs];
+      uint32_t bw[4][2] = {};
+      uint32_t sg[2] = {};
+      if (valid) {
+        const uint2* kc = reinterpret_cast<const uint2*>(kc_s + tl * L.kbytes);
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+          if (p < a.k_bits) {
+            const uint2 w = kc[2 * p + half];
+            bw[p][0] = w.x;
+            bw[p][1] = w.y;
+          }
+        if (qjl) {
+          const uint2 w = reinterpret_cast<const uint2*>(kq_s + tl * 16)[half];
+          sg[0] = w.x;
+          sg[1] = w.y;
         }
       }
+      const uint32_t base = tmem + row_addr + slot * L.kp;
+      for (int s = 0; s < nk_planes; ++s) {
+        const bool sign = s == L.pk;
+        const int set = walsh_set(a.k_bits, s);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          store_signs(base + 32 * s + 8 * (w0 + c), sign ? sg[c] : plane_word(bw[0][c], bw[1][c], bw[2][c], bw[3][c], set));
+      }
+      ptx::tmem_wait_st();
+    }
+    if (L.k_slots == 2 && i > 0 && ok) {
+      ok = wait_phase(&bar_s, (i - 1) & 1, abort, a.error);
+      ptx::tc_fence_after();
+      if (ok) read_scores(i - 1);
     }
     ptx::tc_fence_before();
-    if (half == 1) {
-      const float gk = valid && qjl ? kr_s[tl] : 0.f;
+    ok = __syncthreads_and(ok);
+    if (ok && t < 32 && ptx::elect_one()) {
+      ptx::tc_fence_after();
+      uint32_t a_col = tmem + slot * L.kp;
+      uint64_t dsc = desc_mse;
+      for (int s = 0; s < L.pk; ++s) {
 #pragma unroll
-      for (int h = 0; h < G; ++h) qjl_part[h * kTile + lane] = gk * a.qjl_coef * (acc[h] / sig_s[1][h]);
-    }
-    __syncthreads();
-    if (half == 0) {
-      const float nk = valid ? kn_s[tl] : 0.f;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float s = a.scale * fmaf(nk, acc[h] / sig_s[0][h], qjl_part[h * kTile + lane]);
-        scores[h * kChunk + tl] = valid ? s : -INFINITY;
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_e4m3_tmem_a(d_mse, a_col + 8 * kk, dsc + 2 * kk, idesc_s, (s | kk) != 0);
+        a_col += 32;
+        dsc += mse_plane_step;
       }
+      if (qjl)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_e4m3_tmem_a(d_mse + N1, a_col + 8 * kk, desc_qjl + 2 * kk, idesc_s, kk != 0);
+      ptx::mma_commit(&bar_s);
     }
   }
-  __syncthreads();
+  if (ok) {
+    ok = wait_phase(&bar_s, (n_tiles - 1) & 1, abort, a.error);
+    ptx::tc_fence_after();
+    if (ok) read_scores(n_tiles - 1);
+  }
+  ptx::tc_fence_before();
+  ok = __syncthreads_and(ok);
 
   // ---- softmax statistics over the chunk; B_V pieces of exp(s - m) n_v ----
   if (ok) {
     float mx[G + 1];                      // per-head score max, then the value-norm max
 #pragma unroll
     for (int h = 0; h <= G; ++h) mx[h] = h < G ? -INFINITY : 0.f;
-    for (int i = t; i < n_local; i += kThreads) {
+    for (int i = t; i < n_tiles * kTile; i += kThreads) {
+      const bool valid = i < n_local && blk_ok_s[i / bs];
 #pragma unroll
-      for (int h = 0; h < G; ++h) mx[h] = fmaxf(mx[h], scores[h * kChunk + i]);
-      if (blk_ok_s[i / bs]) mx[G] = fmaxf(mx[G], vn_s[i]);
+      for (int h = 0; h < G; ++h) {
+        const float sc = valid ? a.scale * (s0[h * kChunk + i] + (qjl ? s1[h * kChunk + i] : 0.f)) : -INFINITY;
+        s0[h * kChunk + i] = sc;
+        mx[h] = fmaxf(mx[h], sc);
+      }
+      if (valid) mx[G] = fmaxf(mx[G], vn_s[i]);
     }
     block_reduce(mx, red_s, 0, kThreads / 32, MaxOp());
     float l[G];
@@ -450,8 +473,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     for (int i = t; i < n_tiles * kTile; i += kThreads) {
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float e = (i < n_local && mx[h] != -INFINITY) ? __expf(scores[h * kChunk + i] - mx[h]) : 0.f;
-        scores[h * kChunk + i] = e;
+        const float e = mx[h] != -INFINITY ? __expf(s0[h * kChunk + i] - mx[h]) : 0.f;
+        s0[h * kChunk + i] = e;
         l[h] += e;
       }
     }
@@ -462,101 +485,127 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         stat_s[0][h] = mx[h];
         stat_s[1][h] = l[h];
       }
-    const float vmax = mx[G];
-    const float sv = piece_scale(vmax);
-    // thread (lane, half) writes tile tiles [half, half + 2, ...] of its token slot
+    const float sv = piece_scale(mx[G]);
+    // thread (lane, half) writes the pieces of token slot `lane` in tiles half, half + 2
     const int kpos = k_position(lane);
     for (int tile = half; tile < n_tiles; tile += 2) {
       const int tl = tile * kTile + lane;
       const float nv = (tl < n_local && blk_ok_s[tl / bs]) ? vn_s[tl] * sv : 0.f;
+      uint8_t* dst = b_v + tile * L.no * 128;
 #pragma unroll
-      for (int h = 0; h < G; ++h)
-        write_pieces<kVPieces>(b_v + tile * L.no * 128, h * kVPieces, kpos, scores[h * kChunk + tl] * nv);
+      for (int h = 0; h < G; h += 2) {
+        if (h + 1 < G)
+          write_pieces2<kVPieces>(dst, h * kVPieces, (h + 1) * kVPieces, kpos, s0[h * kChunk + tl] * nv,
+                                  s0[(h + 1) * kChunk + tl] * nv);
+        else
+          write_pieces<kVPieces>(dst, h * kVPieces, kpos, s0[h * kChunk + tl] * nv);
+      }
     }
     if (t == 0) sv_s = sv;
     ptx::fence_async_shared();
-    __syncthreads();
   }
+  ok = __syncthreads_and(ok);
   const float sv = sv_s;
 
-  // ---- values: the two threads of lane d own coordinate d, splitting its sign planes ----
+  // ---- values: lane d owns coordinate d; units of two sign planes alternate slots ----
   const int words_per_dim = bs / 32;
-  const int v_split = (L.pv + 1) / 2;
+  const int n_pairs = (L.pv + 1) / 2;
+  const int n_units = n_tiles * n_pairs;
   for (int tile = 0; tile < n_tiles && ok; ++tile) {
-    {
-      uint32_t bw[4][4] = {};                          // [bit-plane][32-token group]
+    uint32_t bw[4][2] = {};                            // [bit-plane][this thread's 32-token groups]
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const int tl = tile * kTile + 32 * g;
-        if (tl < n_local && blk_ok_s[tl / bs]) {
-          const int k = tl / bs, grp = (tl % bs) / 32;
-          const uint32_t* base = vc_s + k * (L.vblock / 4) + grp;
+    for (int c = 0; c < 2; ++c) {
+      const int tl = tile * kTile + 32 * (w0 + c);
+      if (tl < n_local && blk_ok_s[tl / bs]) {
+        const int k = tl / bs, grp = (tl % bs) / 32;
+        const uint32_t* src = vc_s + k * (L.vblock / 4) + grp;
 #pragma unroll
-          for (int p = 0; p < 4; ++p)
-            if (p < a.v_bits) bw[p][g] = base[(p * 128 + lane) * words_per_dim];
-        }
+        for (int p = 0; p < 4; ++p)
+          if (p < a.v_bits) bw[p][c] = src[(p * 128 + lane) * words_per_dim];
       }
-      store_planes(tmem + row_addr, bw, a.v_bits, half == 0 ? 0 : v_split, half == 0 ? v_split : L.pv, false, bw[0]);
     }
-    ptx::tmem_wait_st();
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (t == 0) {
-      ptx::tc_fence_after();
-      for (int s = 0; s < L.pv; ++s)
+    for (int pair = 0; pair < n_pairs && ok; ++pair) {
+      const int u = tile * n_pairs + pair, slot = u & 1;
+      if (u >= 2) {
+        ok = wait_phase(&bar_v[slot], ((u - 2) >> 1) & 1, abort, a.error);
+        ptx::tc_fence_after();
+      }
+      if (ok) {
+        for (int s = 2 * pair; s < min(2 * pair + 2, L.pv); ++s) {
+          const int set = walsh_set(a.v_bits, s);
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            store_signs(tmem + row_addr + slot * kValueSlot + 32 * (s - 2 * pair) + 8 * (w0 + c),
+                        plane_word(bw[0][c], bw[1][c], bw[2][c], bw[3][c], set));
+        }
+        ptx::tmem_wait_st();
+      }
+      ptx::tc_fence_before();
+      ok = __syncthreads_and(ok);
+      if (ok && t < 32 && ptx::elect_one()) {
+        ptx::tc_fence_after();
+        const uint64_t dsc = desc_v + tile * v_tile_step;
+        const uint32_t a_col = tmem + slot * kValueSlot;
+        const uint32_t d_col = tmem + L.col_o + 2 * pair * L.no;
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_e4m3_tmem_a(tmem + L.col_o + s * L.no, tmem + 32 * s + 8 * kk,
-                               ptx::desc_k_sw128(ptx::smem_u32(b_v + tile * L.no * 128) + 32 * kk), idesc_o,
-                               (tile | kk) != 0);
-      ptx::mma_commit(&bar_o);
-      ok_s = ptx::wait_bar(&bar_o, ph_o, abort, a.error, kErrTimeout);
+          ptx::mma_e4m3_tmem_a(d_col, a_col + 8 * kk, dsc + 2 * kk, idesc_o, (tile | kk) != 0);
+        if (2 * pair + 1 < L.pv)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_e4m3_tmem_a(d_col + L.no, a_col + 32 + 8 * kk, dsc + 2 * kk, idesc_o, (tile | kk) != 0);
+        ptx::mma_commit(&bar_v[slot]);
+      }
     }
-    ph_o ^= 1;
-    __syncthreads();
-    ok = ok_s;
   }
+  // the last commit of each value slot (a commit covers every earlier MMA)
+  if (ok && n_units >= 2) ok = wait_phase(&bar_v[(n_units - 2) & 1], ((n_units - 2) >> 1) & 1, abort, a.error);
+  if (ok) ok = wait_phase(&bar_v[(n_units - 1) & 1], ((n_units - 1) >> 1) & 1, abort, a.error);
+  ptx::tc_fence_after();
 
-  // ---- partial output of this chunk: half h reads planes [h * v_split, ...) ----
+  // ---- partial output of this chunk: half h reads the planes s with s % 2 == h ----
   if (ok) {
-    ptx::tc_fence_after();
     float o[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) o[h] = 0.f;
-    for (int s = half == 0 ? 0 : v_split; s < (half == 0 ? v_split : L.pv); ++s) {
-      const float ws = a.tables->v_walsh[s];
+    for (int s = half; s < L.pv; s += 2) {
+      const float ws = vw_s[s];
 #pragma unroll
       for (int c0 = 0; c0 < NO; c0 += 16) {
         uint32_t v[16];
         ptx::tmem_ld16(tmem + row_addr + L.col_o + s * L.no + c0, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int h = (c0 + i) / kVPieces, piece = (c0 + i) % kVPieces;
-          if (h < G) o[h] = fmaf(ws * inv16_pow(piece), __uint_as_float(v[i]), o[h]);
+        for (int j = 0; j < 16; ++j) {
+          const int h = (c0 + j) / kVPieces, piece = (c0 + j) % kVPieces;
+          if (h < G) o[h] = fmaf(ws * inv16_pow(piece), __uint_as_float(v[j]), o[h]);
         }
       }
     }
-    ptx::tc_fence_before();
-    if (half == 1) {
+    if (half == 1)
 #pragma unroll
-      for (int h = 0; h < G; ++h) qjl_part[h * kTile + lane] = o[h];
-    }
+      for (int h = 0; h < G; ++h) s1[h * kTile + lane] = o[h];
     __syncthreads();
     if (half == 0) {
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float* part = a.ws_part + (static_cast<long long>(qbase + h) * a.max_chunks + chunk) * kPartStride;
-        part[4 + lane] = (o[h] + qjl_part[h * kTile + lane]) / sv;
+        part[4 + lane] = (o[h] + s1[h * kTile + lane]) * (1.f / sv);   // exact: sv is a power of two
         if (lane == 0) {
           part[0] = stat_s[0][h];
           part[1] = stat_s[1][h];
         }
       }
     }
-  } else if (t == 0) {
-    // a wait gave up: let every issued copy and MMA finish before the memory goes
-    ptx::drain_bar(&bar_in, 0);
-    ptx::mma_commit(&bar_s);
-    ptx::drain_bar(&bar_s, ph_s);
+  }
+  ok = __syncthreads_and(ok);
+  if (!ok && t < 32) {
+    // a wait gave up: let every issued copy and MMA finish before the memory
+    // goes (each lane of warp 0 commits, covering whichever lane issued)
+    ptx::mma_commit(&bar_d);
+    if (t == 0) {
+      ptx::drain_bar(&bar_in, 0);
+      ptx::drain_bar(&bar_d, 0);
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -567,7 +616,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
 }
 
 bool tc_decode_supported(const DecodeArgs& a, bool walsh_ok) {
-  if (!walsh_ok || a.block_size % 32 != 0 || kChunk % a.block_size != 0) return false;
+  if (!walsh_ok || a.ws_bk == nullptr || a.block_size % 32 != 0 || kChunk % a.block_size != 0) return false;
+  if (a.k_bits < 1 || a.k_bits > 4 || a.v_bits < 1 || a.v_bits > 4) return false;
   if (a.group != 1 && a.group != 2 && a.group != 4 && a.group != 8) return false;
   const TcLayout l = tc_layout(a.group, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size);
   return l.cols <= 512 && l.smem_bytes <= 200 * 1024;

@@ -66,6 +66,8 @@ struct DecodeArgs {
   float* out;               // [batch][n_q][128]
   float* ws_q;              // [batch*n_q][256]: rotated query, projected query
   float* ws_part;           // [batch*n_q][max_chunks][kPartStride]
+  uint8_t* ws_bk;           // [batch*n_q][bk_stride]: tensor-core score operand pieces (null: not built)
+  int bk_stride;
   int max_chunks;
   const float* R;           // [128][128] row-major
   const float* Rt;
@@ -82,6 +84,15 @@ __host__ __device__ inline long long transposed_word(long long blk, int head, in
 }
 
 constexpr int kChunk = 512;       // context tokens per split-K work item
+constexpr int kQPieces = 6;       // e4m3 pieces of a query coefficient (tensor-core decode)
+
+// Bytes of one query head's tensor-core score operand in the decode
+// workspace: for each key sign plane and the QJL plane, kQPieces rows of 128
+// e4m3 bytes (row i: piece i of a_S q_rot or of q_s, K order of k_position),
+// then sigma_mse, sigma_qjl and their inverses as floats.
+__host__ __device__ constexpr int bk_head_bytes(int k_mse_bits, bool qjl) {
+  return ((k_mse_bits >= 1 ? (1 << (k_mse_bits - 1)) : 0) + (qjl ? 1 : 0)) * kQPieces * 128 + 16;
+}
 constexpr int kPartStride = 132;  // m, l, 2 pad, acc[128]
 
 cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_t stream);

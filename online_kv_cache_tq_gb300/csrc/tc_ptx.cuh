@@ -52,6 +52,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended for up to `hint_ns`
+// nanoseconds while the phase is incomplete, so a waiting warp issues few
+// instructions.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr uint32_t kSuspendHintNs = 20000;
+
 // Wait for the phase of `bar` with the given parity.  Returns false when
 // another role raised `abort`, or after kWaitLimitNs (then it raises `abort`
 // and records `timeout_code` in the device error word).
@@ -60,7 +77,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint(bar, parity, kSuspendHintNs)) return true;
     if (*abort) return false;
     if (global_ns() - t0 > kWaitLimitNs) {
       *abort = 1;
@@ -73,7 +90,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 // Bounded wait that ignores `abort` (used to drain in-flight copies).
 __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity) && global_ns() - t0 < kWaitLimitNs) {
+  while (!mbar_try_wait_hint(bar, parity, kSuspendHintNs) && global_ns() - t0 < kWaitLimitNs) {
   }
 }
 
@@ -193,6 +210,19 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, uint32_t r0, uint32_t r
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// One lane of the (converged) warp returns true.  Issuing tcgen05.mma from an
+// elected lane keeps its operands in uniform registers, which a plain
+// `lane == 0` branch does not.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
 
 // ---- tcgen05.mma --------------------------------------------------------
 

@@ -38,6 +38,7 @@ def test_gqa_ragged_contexts_shuffled_blocks(group):
     cfg = dict(n_kv=n_kv, block_size=64, dtype="bf16", seed=group, log_uniform=(0.1, 10.0), outliers=3,
                outlier_scale=30.0)
     book, ref = books(3, 3, 128, seed=1)
+    assert B.tq_decode_kernel_kind(book, n_kv * group, n_kv) == 1      # tensor-core partials
     ctx = np.array([0, 1, 77, 512, 513, 1500, 2100], dtype=np.int32)
     table, _ = W.block_layout(ctx, 64, True, seed=group)
     g = generator(group)
@@ -60,6 +61,24 @@ def test_bit_width_variants(k_bits, v_bits, qjl):
     q = W.queries(2, 4, torch.float32, "cuda", g)
     out = decode(book, cache, q, table, ctx, 1100)
     check_decode(out, host_cache(cache), q, table, ctx, ref, [(b, h) for b in range(2) for h in range(4)])
+
+
+@pytest.mark.parametrize("block_size", [96, 1024])
+def test_blocks_not_dividing_the_chunk_take_the_simt_kernel(block_size):
+    # 512-token chunks cut through these blocks, which the tensor-core kernel
+    # does not take: the SIMT partials kernel serves them
+    cfg = dict(n_kv=2, block_size=block_size, dtype="bf16", seed=11, log_uniform=(0.1, 10.0), outliers=3,
+               outlier_scale=30.0)
+    book, ref = books(3, 3, 128, seed=4, block_size=block_size)
+    assert B.tq_decode_kernel_kind(book, 8, 2) == 0
+    ctx = np.array([1, 700, 1500], dtype=np.int32)
+    table, _ = W.block_layout(ctx, block_size, True, seed=3)
+    g = generator(block_size)
+    cache = fill_cache(book, cfg, ctx, table, g, chunk_tokens=1000)
+    q = W.queries(len(ctx), 8, torch.bfloat16, "cuda", g)
+    out = decode(book, cache, q, table, ctx, 1500)
+    check_decode(out, host_cache(cache), q, table, ctx, ref, [(b, h) for b in range(len(ctx)) for h in range(8)])
+    assert B.tq_get_last_device_error(book) == 0
 
 
 def test_staged_calls_match_the_one_call():
