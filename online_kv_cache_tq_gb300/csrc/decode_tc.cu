@@ -65,10 +65,23 @@ __device__ __forceinline__ int sw128(int n, int k) { return n * 128 + ((((k >> 4
 // Store the e4m3 +-1 image of one 32-bit word of bits (bit 1 -> +1.0 = 0x38,
 // bit 0 -> -1.0 = 0xB8) as eight columns: column j holds bits j, j+8, j+16,
 // j+24 of the word.
+// The bit arithmetic sits inside the asm block so that the compiler keeps
+// only the word, not eight operand registers per plane, live across planes.
 __device__ __forceinline__ void store_signs(uint32_t taddr, uint32_t w) {
-  const uint32_t inv = ~w;
-  auto col = [inv](int j) { return ((inv << (7 - j)) & 0x80808080u) | 0x38383838u; };
-  ptx::tmem_st8(taddr, col(0), col(1), col(2), col(3), col(4), col(5), col(6), col(7));
+  asm volatile(
+      "{\n\t.reg .b32 i, c0, c1, c2, c3, c4, c5, c6, c7;\n\t"
+      "not.b32 i, %1;\n\t"
+      "shl.b32 c0, i, 7;\n\tand.b32 c0, c0, 0x80808080;\n\tor.b32 c0, c0, 0x38383838;\n\t"
+      "shl.b32 c1, i, 6;\n\tand.b32 c1, c1, 0x80808080;\n\tor.b32 c1, c1, 0x38383838;\n\t"
+      "shl.b32 c2, i, 5;\n\tand.b32 c2, c2, 0x80808080;\n\tor.b32 c2, c2, 0x38383838;\n\t"
+      "shl.b32 c3, i, 4;\n\tand.b32 c3, c3, 0x80808080;\n\tor.b32 c3, c3, 0x38383838;\n\t"
+      "shl.b32 c4, i, 3;\n\tand.b32 c4, c4, 0x80808080;\n\tor.b32 c4, c4, 0x38383838;\n\t"
+      "shl.b32 c5, i, 2;\n\tand.b32 c5, c5, 0x80808080;\n\tor.b32 c5, c5, 0x38383838;\n\t"
+      "shl.b32 c6, i, 1;\n\tand.b32 c6, c6, 0x80808080;\n\tor.b32 c6, c6, 0x38383838;\n\t"
+      "and.b32 c7, i, 0x80808080;\n\tor.b32 c7, c7, 0x38383838;\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {c0, c1, c2, c3, c4, c5, c6, c7};\n\t}\n"
+      ::"r"(taddr), "r"(w)
+      : "memory");
 }
 
 // Code-bit subset of sign plane s (same order as kWalshSets): the single bits
@@ -85,6 +98,47 @@ __device__ __forceinline__ uint32_t plane_word(uint32_t b0, uint32_t b1, uint32_
   const uint32_t m0 = (set & 1) ? ~0u : 0u, m1 = (set & 2) ? ~0u : 0u;
   const uint32_t m2 = (set & 4) ? ~0u : 0u, m3 = (set & 8) ? ~0u : 0u;
   return (b0 & m0) ^ (b1 & m1) ^ (b2 & m2) ^ (b3 & m3);
+}
+
+// Sign planes of one key tile for BITS-bit codes (the Walsh sets fold to
+// constants), words w0 and w0 + 1 of each plane; the QJL plane follows.
+template <int BITS>
+__device__ __forceinline__ void key_planes(uint32_t base, const uint32_t (&bw)[4][2], const uint32_t (&sg)[2],
+                                           bool qjl, int w0) {
+  constexpr int P = 1 << (BITS - 1);
+#pragma unroll
+  for (int s = 0; s < P; ++s) {
+    const int set = walsh_set(BITS, s);
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      store_signs(base + 32 * s + 8 * (w0 + c), plane_word(bw[0][c], bw[1][c], bw[2][c], bw[3][c], set));
+  }
+  if (qjl)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) store_signs(base + 32 * P + 8 * (w0 + c), sg[c]);
+}
+
+// Value sign plane S of BITS-bit codes (compile-time Walsh set) at `col`.
+template <int BITS, int S>
+__device__ __forceinline__ void value_plane(uint32_t col, const uint32_t (&bw)[4][2], int w0) {
+  if constexpr (S < (1 << (BITS - 1))) {
+    constexpr int set = S < BITS ? 1 << S : (BITS == 3 ? 7 : 15 ^ (1 << (7 - S)));
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      store_signs(col + 8 * (w0 + c), plane_word(bw[0][c], bw[1][c], bw[2][c], bw[3][c], set));
+  }
+}
+
+// Value sign planes 2 pair and 2 pair + 1 (those that exist) into a slot;
+// one straight-line case per pair keeps only two planes' words live.
+template <int BITS>
+__device__ __forceinline__ void value_pair(uint32_t base, const uint32_t (&bw)[4][2], int pair, int w0) {
+  switch (pair) {
+    case 0: value_plane<BITS, 0>(base, bw, w0); value_plane<BITS, 1>(base + 32, bw, w0); break;
+    case 1: value_plane<BITS, 2>(base, bw, w0); value_plane<BITS, 3>(base + 32, bw, w0); break;
+    case 2: value_plane<BITS, 4>(base, bw, w0); value_plane<BITS, 5>(base + 32, bw, w0); break;
+    default: value_plane<BITS, 6>(base, bw, w0); value_plane<BITS, 7>(base + 32, bw, w0); break;
+  }
 }
 
 // Write the e4m3 pieces of y (row `row0 + i` for piece i): each piece is the
@@ -231,8 +285,9 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   if (start >= ctx) return;
   const int n_local = min(kChunk, ctx - start);
   const int n_tiles = (n_local + kTile - 1) / kTile;
-  const int bs = a.block_size;
-  const int n_blk = (n_local + bs - 1) / bs;          // blocks of this chunk (block_size divides kChunk)
+  const int bs = a.block_size;                        // a power of two that divides kChunk
+  const int bs_shift = 31 - __clz(bs);
+  const int n_blk = (n_local + bs - 1) >> bs_shift;   // blocks of this chunk
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -353,13 +408,12 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   const uint64_t desc_v = ptx::desc_k_sw128(ptx::smem_u32(b_v));
   const uint32_t mse_plane_step = (L.n1 * 128) >> 4, v_tile_step = (L.no * 128) >> 4;
   const uint32_t d_mse = tmem + L.col_s;
-  const int nk_planes = L.pk + L.pq;
 
   // accumulators of key tile i -> s0 (half 0: n_k <q_rot, k_mse> / sigma) and
   // s1 (half 1: gamma coef <q_s, signs> / sigma)
   auto read_scores = [&](int i) {
     const int tl = i * kTile + lane;
-    const bool valid = tl < n_local && blk_ok_s[tl / bs];
+    const bool valid = tl < n_local && blk_ok_s[tl >> bs_shift];
     if (half == 1 && !qjl) return;
     float acc[G];
 #pragma unroll
@@ -390,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     }
     if (ok) {
       const int tl = i * kTile + lane;
-      const bool valid = tl < n_local && blk_ok_s[tl / bs];
+      const bool valid = tl < n_local && blk_ok_s[tl >> bs_shift];
       uint32_t bw[4][2] = {};
       uint32_t sg[2] = {};
       if (valid) {
@@ -409,12 +463,11 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         }
       }
       const uint32_t base = tmem + row_addr + slot * L.kp;
-      for (int s = 0; s < nk_planes; ++s) {
-        const bool sign = s == L.pk;
-        const int set = walsh_set(a.k_bits, s);
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          store_signs(base + 32 * s + 8 * (w0 + c), sign ? sg[c] : plane_word(bw[0][c], bw[1][c], bw[2][c], bw[3][c], set));
+      switch (a.k_bits) {
+        case 1: key_planes<1>(base, bw, sg, qjl, w0); break;
+        case 2: key_planes<2>(base, bw, sg, qjl, w0); break;
+        case 3: key_planes<3>(base, bw, sg, qjl, w0); break;
+        default: key_planes<4>(base, bw, sg, qjl, w0); break;
       }
       ptx::tmem_wait_st();
     }
@@ -457,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
 #pragma unroll
     for (int h = 0; h <= G; ++h) mx[h] = h < G ? -INFINITY : 0.f;
     for (int i = t; i < n_tiles * kTile; i += kThreads) {
-      const bool valid = i < n_local && blk_ok_s[i / bs];
+      const bool valid = i < n_local && blk_ok_s[i >> bs_shift];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float sc = valid ? a.scale * (s0[h * kChunk + i] + (qjl ? s1[h * kChunk + i] : 0.f)) : -INFINITY;
@@ -490,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     const int kpos = k_position(lane);
     for (int tile = half; tile < n_tiles; tile += 2) {
       const int tl = tile * kTile + lane;
-      const float nv = (tl < n_local && blk_ok_s[tl / bs]) ? vn_s[tl] * sv : 0.f;
+      const float nv = (tl < n_local && blk_ok_s[tl >> bs_shift]) ? vn_s[tl] * sv : 0.f;
       uint8_t* dst = b_v + tile * L.no * 128;
 #pragma unroll
       for (int h = 0; h < G; h += 2) {
@@ -508,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   const float sv = sv_s;
 
   // ---- values: lane d owns coordinate d; units of two sign planes alternate slots ----
-  const int words_per_dim = bs / 32;
+  const int wpd_shift = bs_shift - 5;                 // log2 of the words per coordinate in a block
   const int n_pairs = (L.pv + 1) / 2;
   const int n_units = n_tiles * n_pairs;
   for (int tile = 0; tile < n_tiles && ok; ++tile) {
@@ -516,12 +569,11 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int tl = tile * kTile + 32 * (w0 + c);
-      if (tl < n_local && blk_ok_s[tl / bs]) {
-        const int k = tl / bs, grp = (tl % bs) / 32;
-        const uint32_t* src = vc_s + k * (L.vblock / 4) + grp;
+      if (tl < n_local && blk_ok_s[tl >> bs_shift]) {
+        const uint32_t* src = vc_s + (tl >> bs_shift) * (L.vblock / 4) + ((tl & (bs - 1)) >> 5) + (lane << wpd_shift);
 #pragma unroll
         for (int p = 0; p < 4; ++p)
-          if (p < a.v_bits) bw[p][c] = src[(p * 128 + lane) * words_per_dim];
+          if (p < a.v_bits) bw[p][c] = src[(p * 128) << wpd_shift];
       }
     }
     for (int pair = 0; pair < n_pairs && ok; ++pair) {
@@ -531,12 +583,12 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         ptx::tc_fence_after();
       }
       if (ok) {
-        for (int s = 2 * pair; s < min(2 * pair + 2, L.pv); ++s) {
-          const int set = walsh_set(a.v_bits, s);
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-            store_signs(tmem + row_addr + slot * kValueSlot + 32 * (s - 2 * pair) + 8 * (w0 + c),
-                        plane_word(bw[0][c], bw[1][c], bw[2][c], bw[3][c], set));
+        const uint32_t base = tmem + row_addr + slot * kValueSlot;
+        switch (a.v_bits) {
+          case 1: value_pair<1>(base, bw, pair, w0); break;
+          case 2: value_pair<2>(base, bw, pair, w0); break;
+          case 3: value_pair<3>(base, bw, pair, w0); break;
+          default: value_pair<4>(base, bw, pair, w0); break;
         }
         ptx::tmem_wait_st();
       }
