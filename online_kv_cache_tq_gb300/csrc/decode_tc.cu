@@ -28,18 +28,18 @@
 // The output of a CTA is the same split-K partial (m, l, acc[128]) the SIMT
 // kernel writes, merged by the same finish kernel.
 //
-// One CTA of 256 threads per (512-token chunk, KV head, sequence); threads t
-// and t + 128 share tensor-memory lane t and split its work: each builds two
-// of the four 32-bit words of every sign plane, half of the accumulator
-// columns and half of the operand pieces.  Lane k of warp 0 copies block k
-// of the chunk's packed fields (contiguous per block and head) into shared
-// memory with bulk asynchronous copies while all threads move the query
-// pieces that the prepare step built (B_K) into the swizzled operand layout.
-// The sign planes go to two alternating tensor-memory slots, so the planes of
-// the next tile (or value-plane pair) are built while the MMAs of the previous
-// one run; an elected lane of warp 0 issues the MMAs after one barrier per
-// tile and every thread waits on the MMA mbarrier itself (time-bounded, error
-// code 4) before it reuses a slot or reads accumulators.
+// One CTA of 288 threads per (512-token chunk, KV head, sequence).  Warps 0-7
+// build operands: threads t and t + 128 share tensor-memory lane t and split
+// its work (two of the four 32-bit words of every sign plane, half of the
+// accumulator columns, half of the operand pieces).  Warp 8 is the control
+// warp: lane k copies block k of the chunk's packed fields (contiguous per
+// block and head) into shared memory with bulk asynchronous copies, then an
+// elected lane issues every MMA.  The two sides meet only on mbarriers: the
+// builders store a tile's sign planes into one of two tensor-memory slots and
+// arrive; the control warp issues that tile's MMAs and commits; the builders
+// build the next tile meanwhile and wait on the commit only to read the
+// accumulators or to reuse the slot.  Every wait is time-bounded (error
+// code 4) and a failed wait makes every other wait give up.
 #include <cuda_fp8.h>
 
 #include "e4m3_pieces.cuh"
@@ -51,7 +51,8 @@ namespace {
 
 constexpr int kTile = 128;                  // tokens per tile = tensor-memory lanes
 constexpr int kTiles = kChunk / kTile;      // tiles per chunk
-constexpr int kThreads = 256;               // two threads per tensor-memory lane
+constexpr int kBuilders = 256;              // warps 0-7: two threads per tensor-memory lane
+constexpr int kThreads = kBuilders + 32;     // warp 8: copies and MMA issue
 constexpr int kVPieces = 3;                 // e4m3 pieces of a softmax weight
 
 __host__ __device__ constexpr int round16(int x) { return (x + 15) / 16 * 16; }
@@ -168,17 +169,22 @@ __device__ __forceinline__ void write_pieces2(uint8_t* b, int row_a, int row_b, 
   }
 }
 
+// Barrier of the 256 builder threads only (named barrier 1).
+__device__ __forceinline__ void builder_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Reduce N values per thread over warps [w0, w0 + nw) of the builders at once
+// (one pair of barriers for all N); every thread gets the results of its range.
 template <int N, typename Op>
 __device__ __forceinline__ void block_reduce(float (&v)[N], float* red, int w0, int nw, Op op) {
 #pragma unroll
   for (int j = 0; j < N; ++j)
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v[j] = op(v[j], __shfl_xor_sync(0xffffffffu, v[j], off));
-  __syncthreads();
+  builder_sync();
   if ((threadIdx.x & 31) == 0)
 #pragma unroll
     for (int j = 0; j < N; ++j) red[(threadIdx.x >> 5) * N + j] = v[j];
-  __syncthreads();
+  builder_sync();
 #pragma unroll
   for (int j = 0; j < N; ++j) {
     float r = red[w0 * N + j];
@@ -302,147 +308,212 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   float* kr_s = reinterpret_cast<float*>(smem + L.off_kr);
   float* vn_s = reinterpret_cast<float*>(smem + L.off_vn);
   uint32_t* vc_s = reinterpret_cast<uint32_t*>(smem + L.off_vc);   // [blk][plane][dim][bs/32]
-  __shared__ __align__(8) uint64_t bar_in, bar_s, bar_v[2], bar_d;
+  // bar_in: the chunk's fields landed; kfull / vfull: the builders stored a
+  // slot's planes (256 arrivals); kdone / vdone: the slot's MMAs completed
+  // (commit); sfree: the builders read the score accumulators (256 arrivals);
+  // bar_d: drain after a failed wait
+  __shared__ __align__(8) uint64_t bar_in, kfull[2], kdone, sfree, vfull[2], vdone[2], bar_d;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
-  __shared__ float red_s[(kThreads / 32) * (G + 1)];
+  __shared__ float red_s[(kBuilders / 32) * (G + 1)];
   __shared__ float stat_s[2][G];                // chunk max, chunk sum per head
   __shared__ int blk_ok_s[kChunk / 32];         // physical block of each block slot is valid
   __shared__ float sv_s;                        // piece scale of the softmax weights
   __shared__ float vw_s[8];                     // odd Walsh coefficients of the value codebook
 
   const int t = threadIdx.x;
+  const bool builder = t < kBuilders;
   const int lane = t & (kTile - 1);             // tensor-memory lane (token or coordinate)
-  const int half = t >> 7;                      // which of the two threads of the lane
+  const int half = (t >> 7) & 1;                // which of the two threads of the lane
   const int w0 = 2 * half;                      // this thread's words of every sign plane: w0, w0 + 1
   const uint32_t row_addr = static_cast<uint32_t>(((t >> 5) & 3) * 32) << 16;
   const bool qjl = a.k_qjl != nullptr;
   const int qbase = b * a.n_q + kvh * G;
   volatile int* abort = &abort_s;
+  const int n_pairs = (L.pv + 1) / 2;
+  const int n_units = n_tiles * n_pairs;
 
   // zero the B operands (padding rows must be 0)
   for (int i = t; i < L.off_s0 / 16; i += kThreads) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  ptx::fence_async_shared();                    // the MMAs read these bytes through the async proxy
   if (t < 8) vw_s[t] = a.tables->v_walsh[t];
-  if (t == 0) {
+  if (t == kBuilders) {
     abort_s = 0;
     ptx::mbar_init(&bar_in, 1);
-    ptx::mbar_init(&bar_s, 1);
-    ptx::mbar_init(&bar_v[0], 1);
-    ptx::mbar_init(&bar_v[1], 1);
+    ptx::mbar_init(&kfull[0], kBuilders);
+    ptx::mbar_init(&kfull[1], kBuilders);
+    ptx::mbar_init(&kdone, 1);
+    ptx::mbar_init(&sfree, kBuilders);
+    ptx::mbar_init(&vfull[0], kBuilders);
+    ptx::mbar_init(&vfull[1], kBuilders);
+    ptx::mbar_init(&vdone[0], 1);
+    ptx::mbar_init(&vdone[1], 1);
     ptx::mbar_init(&bar_d, 32);
     ptx::fence_mbar_init();
   }
-  if (t < 32) {
+  if (!builder) {
     ptx::tmem_alloc(&tmem_base_s, L.tmem);
     ptx::tmem_relinquish();
   }
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_base_s;
+  bool ok = true;
 
-  // ---- prefetch the chunk's packed fields into shared memory (lane k of warp 0: block k) ----
-  if (t < 32) {
-    bool valid = false;
-    long long phys = 0;
-    int rows = 0;
-    uint32_t bytes = 0;
-    if (t < n_blk) {
-      const int lblk = (start / bs) + t;
-      phys = a.block_table ? a.block_table[static_cast<long long>(b) * a.max_blocks + lblk]
-                           : static_cast<long long>(b) * a.max_blocks + lblk;
-      valid = phys >= 0 && phys < a.num_blocks;
-      blk_ok_s[t] = valid;
-      if (!valid) atomicCAS(a.error, 0, kErrBlock);
-      rows = min(bs, (n_local - t * bs + 31) / 32 * 32);
-      // key codes, key norm, value norm (+ QJL signs and residual norm) per row, value block
-      if (valid) bytes = rows * (L.kbytes + 4 + 4 + (qjl ? 16 + 4 : 0)) + L.vblock;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, off);
-    if (t == 0) ptx::mbar_arrive_expect_tx(&bar_in, bytes);
-    __syncwarp();
-    if (valid) {
-      const long long r0 = (phys * a.n_kv + kvh) * bs;    // first row of this block
-      const int tl0 = t * bs;
-      ptx::bulk_load(kc_s + tl0 * L.kbytes, a.k_codes + r0 * L.kbytes, rows * L.kbytes, &bar_in);
-      if (qjl) {
-        ptx::bulk_load(kq_s + tl0 * 16, a.k_qjl + r0 * 16, rows * 16, &bar_in);
-        ptx::bulk_load(kr_s + tl0, a.k_rnorm + r0, rows * 4, &bar_in);
+  if (!builder) {
+    // =================== control warp: copies, then every MMA ===================
+    const int ln = t - kBuilders;
+    {
+      // lane k copies block k of the chunk
+      bool valid = false;
+      long long phys = 0;
+      int rows = 0;
+      uint32_t bytes = 0;
+      if (ln < n_blk) {
+        const int lblk = (start >> bs_shift) + ln;
+        phys = a.block_table ? a.block_table[static_cast<long long>(b) * a.max_blocks + lblk]
+                             : static_cast<long long>(b) * a.max_blocks + lblk;
+        valid = phys >= 0 && phys < a.num_blocks;
+        blk_ok_s[ln] = valid;
+        if (!valid) atomicCAS(a.error, 0, kErrBlock);
+        rows = min(bs, (n_local - ln * bs + 31) / 32 * 32);
+        // key codes, key norm, value norm (+ QJL signs and residual norm) per row, value block
+        if (valid) bytes = rows * (L.kbytes + 4 + 4 + (qjl ? 16 + 4 : 0)) + L.vblock;
       }
-      ptx::bulk_load(kn_s + tl0, a.k_norm + r0, rows * 4, &bar_in);
-      ptx::bulk_load(vn_s + tl0, a.v_norm + r0, rows * 4, &bar_in);
-      ptx::bulk_load(vc_s + t * (L.vblock / 4), a.v_codes + (phys * a.n_kv + kvh) * L.vblock, L.vblock, &bar_in);
-    }
-  }
-
-  // ---- B_K: the group's prepared score operand pieces, into the swizzled layout ----
-  // (overlaps the copies) row n = h kQPieces + i of plane s; 16-byte chunk c
-  // of a row lands at c ^ (n % 8)
-  float inv_sig[G];                             // 1 / sigma of this thread's accumulator columns
-  {
-    const int nk = L.pk + L.pq;
-    const int per_head = nk * kQPieces * 8;     // 16-byte chunks per head
-    for (int idx = t; idx < G * per_head; idx += kThreads) {
-      const int h = idx / per_head, r = idx - h * per_head;
-      const int s = r / (kQPieces * 8), i = (r / 8) % kQPieces, c = r % 8;
-      const uint4 v = reinterpret_cast<const uint4*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride)[r];
-      const int n = h * kQPieces + i;
-      uint8_t* dst = s < L.pk ? b_mse + s * L.n1 * 128 : b_qjl;
-      *reinterpret_cast<uint4*>(dst + n * 128 + ((c ^ (n & 7)) << 4)) = v;
-    }
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-      inv_sig[h] = reinterpret_cast<const float*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride +
-                                                  nk * kQPieces * 128)[2 + half];
-  }
-  ptx::fence_async_shared();
-  bool ok = wait_phase(&bar_in, 0, abort, a.error);
-  ok = __syncthreads_and(ok);
-
-  const uint32_t idesc_s = ptx::idesc_e4m3_f32(128, N1);
-  const uint32_t idesc_o = ptx::idesc_e4m3_f32(128, NO);
-  // operand descriptors and accumulator addresses, ready before the issue points
-  // (the start-address field counts 16-byte units: +2 per 32-byte K step)
-  const uint64_t desc_mse = ptx::desc_k_sw128(ptx::smem_u32(b_mse));
-  const uint64_t desc_qjl = ptx::desc_k_sw128(ptx::smem_u32(b_qjl));
-  const uint64_t desc_v = ptx::desc_k_sw128(ptx::smem_u32(b_v));
-  const uint32_t mse_plane_step = (L.n1 * 128) >> 4, v_tile_step = (L.no * 128) >> 4;
-  const uint32_t d_mse = tmem + L.col_s;
-
-  // accumulators of key tile i -> s0 (half 0: n_k <q_rot, k_mse> / sigma) and
-  // s1 (half 1: gamma coef <q_s, signs> / sigma)
-  auto read_scores = [&](int i) {
-    const int tl = i * kTile + lane;
-    const bool valid = tl < n_local && blk_ok_s[tl >> bs_shift];
-    if (half == 1 && !qjl) return;
-    float acc[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = 0.f;
-#pragma unroll
-    for (int c0 = 0; c0 < N1; c0 += 16) {
-      uint32_t v[16];
-      ptx::tmem_ld16(tmem + row_addr + L.col_s + half * N1 + c0, v);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int h = (c0 + j) / kQPieces, piece = (c0 + j) % kQPieces;
-        if (h < G) acc[h] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), acc[h]);
+      for (int off = 16; off > 0; off >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, off);
+      __syncwarp();                             // blk_ok_s before the arrival the builders acquire
+      if (ln == 0) ptx::mbar_arrive_expect_tx(&bar_in, bytes);
+      __syncwarp();
+      if (valid) {
+        const long long r0 = (phys * a.n_kv + kvh) * bs;    // first row of this block
+        const int tl0 = ln * bs;
+        ptx::bulk_load(kc_s + tl0 * L.kbytes, a.k_codes + r0 * L.kbytes, rows * L.kbytes, &bar_in);
+        if (qjl) {
+          ptx::bulk_load(kq_s + tl0 * 16, a.k_qjl + r0 * 16, rows * 16, &bar_in);
+          ptx::bulk_load(kr_s + tl0, a.k_rnorm + r0, rows * 4, &bar_in);
+        }
+        ptx::bulk_load(kn_s + tl0, a.k_norm + r0, rows * 4, &bar_in);
+        ptx::bulk_load(vn_s + tl0, a.v_norm + r0, rows * 4, &bar_in);
+        ptx::bulk_load(vc_s + ln * (L.vblock / 4), a.v_codes + (phys * a.n_kv + kvh) * L.vblock, L.vblock, &bar_in);
       }
     }
-    const float f = valid ? (half == 0 ? kn_s[tl] : kr_s[tl] * a.qjl_coef) : 0.f;
-    float* dst = half == 0 ? s0 : s1;
+    const uint32_t idesc_s = ptx::idesc_e4m3_f32(128, N1);
+    const uint32_t idesc_o = ptx::idesc_e4m3_f32(128, NO);
+    // the start-address field of a descriptor counts 16-byte units: +2 per 32-byte K step
+    const uint64_t desc_mse = ptx::desc_k_sw128(ptx::smem_u32(b_mse));
+    const uint64_t desc_qjl = ptx::desc_k_sw128(ptx::smem_u32(b_qjl));
+    const uint64_t desc_v = ptx::desc_k_sw128(ptx::smem_u32(b_v));
+    const uint32_t mse_plane_step = (L.n1 * 128) >> 4, v_tile_step = (L.no * 128) >> 4;
+    const uint32_t d_mse = tmem + L.col_s;
+    // scores: tile i once its planes are stored and tile i - 1's accumulators were read
+    for (int i = 0; i < n_tiles && ok; ++i) {
+      const int slot = L.k_slots == 2 ? (i & 1) : 0;
+      ok = wait_phase(&kfull[slot], (i / L.k_slots) & 1, abort, a.error);
+      if (ok && i > 0) ok = wait_phase(&sfree, (i - 1) & 1, abort, a.error);
+      if (ok && ptx::elect_one()) {
+        ptx::tc_fence_after();
+        uint32_t a_col = tmem + slot * L.kp;
+        uint64_t dsc = desc_mse;
+        for (int s = 0; s < L.pk; ++s) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) dst[h * kChunk + tl] = f * (acc[h] * inv_sig[h]);
-  };
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_e4m3_tmem_a(d_mse, a_col + 8 * kk, dsc + 2 * kk, idesc_s, (s | kk) != 0);
+          a_col += 32;
+          dsc += mse_plane_step;
+        }
+        if (qjl)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_e4m3_tmem_a(d_mse + N1, a_col + 8 * kk, desc_qjl + 2 * kk, idesc_s, kk != 0);
+        ptx::mma_commit(&kdone);
+      }
+      __syncwarp();
+    }
+    // values: unit u (tile u / n_pairs, plane pair u % n_pairs) from slot u % 2
+    for (int u = 0; u < n_units && ok; ++u) {
+      const int tile = u / n_pairs, pair = u - tile * n_pairs, slot = u & 1;
+      ok = wait_phase(&vfull[slot], (u >> 1) & 1, abort, a.error);
+      if (ok && ptx::elect_one()) {
+        ptx::tc_fence_after();
+        const uint64_t dsc = desc_v + tile * v_tile_step;
+        const uint32_t a_col = tmem + slot * kValueSlot;
+        const uint32_t d_col = tmem + L.col_o + 2 * pair * L.no;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_e4m3_tmem_a(d_col, a_col + 8 * kk, dsc + 2 * kk, idesc_o, (tile | kk) != 0);
+        if (2 * pair + 1 < L.pv)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_e4m3_tmem_a(d_col + L.no, a_col + 32 + 8 * kk, dsc + 2 * kk, idesc_o, (tile | kk) != 0);
+        ptx::mma_commit(&vdone[slot]);
+      }
+      __syncwarp();
+    }
+  } else {
+    // =================== builders ===================
+    // B_K: the group's prepared score operand pieces into the swizzled layout
+    // (overlaps the copies); row n = h kQPieces + i of plane s, 16-byte chunk c
+    // of a row at c ^ (n % 8)
+    float inv_sig[G];                             // 1 / sigma of this thread's accumulator columns
+    {
+      const int nk = L.pk + L.pq;
+      const int per_head = nk * kQPieces * 8;     // 16-byte chunks per head
+      for (int idx = t; idx < G * per_head; idx += kBuilders) {
+        const int h = idx / per_head, r = idx - h * per_head;
+        const int s = r / (kQPieces * 8), i = (r / 8) % kQPieces, c = r % 8;
+        const uint4 v = reinterpret_cast<const uint4*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride)[r];
+        const int n = h * kQPieces + i;
+        uint8_t* dst = s < L.pk ? b_mse + s * L.n1 * 128 : b_qjl;
+        *reinterpret_cast<uint4*>(dst + n * 128 + ((c ^ (n & 7)) << 4)) = v;
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        inv_sig[h] = reinterpret_cast<const float*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride +
+                                                    nk * kQPieces * 128)[2 + half];
+    }
+    ptx::fence_async_shared();
+    ok = wait_phase(&bar_in, 0, abort, a.error);
+    builder_sync();                               // blk_ok_s was written by the control warp before its copies
 
-  // ---- scores: sign planes of tile i are built while the MMAs of tile i - 1 run ----
-  for (int i = 0; i < n_tiles && ok; ++i) {
-    const int slot = L.k_slots == 2 ? (i & 1) : 0;
-    if (L.k_slots == 1 && i > 0) {
-      ok = wait_phase(&bar_s, (i - 1) & 1, abort, a.error);
+    // accumulators of key tile i -> s0 (half 0: n_k <q_rot, k_mse> / sigma) and
+    // s1 (half 1: gamma coef <q_s, signs> / sigma)
+    auto read_scores = [&](int i) {
+      const int tl = i * kTile + lane;
+      const bool valid = tl < n_local && blk_ok_s[tl >> bs_shift];
+      if (half == 1 && !qjl) return;
+      float acc[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc[h] = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < N1; c0 += 16) {
+        uint32_t v[16];
+        ptx::tmem_ld16(tmem + row_addr + L.col_s + half * N1 + c0, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int h = (c0 + j) / kQPieces, piece = (c0 + j) % kQPieces;
+          if (h < G) acc[h] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), acc[h]);
+        }
+      }
+      const float f = valid ? (half == 0 ? kn_s[tl] : kr_s[tl] * a.qjl_coef) : 0.f;
+      float* dst = half == 0 ? s0 : s1;
+#pragma unroll
+      for (int h = 0; h < G; ++h) dst[h * kChunk + tl] = f * (acc[h] * inv_sig[h]);
+    };
+    // wait for the MMAs of tile i, read its accumulators, release them
+    auto take_scores = [&](int i, bool release) {
+      ok = ok && wait_phase(&kdone, i & 1, abort, a.error);
       ptx::tc_fence_after();
-      if (ok) read_scores(i - 1);
-    }
-    if (ok) {
+      if (ok) read_scores(i);
+      ptx::tc_fence_before();
+      if (release) ptx::mbar_arrive(&sfree);
+    };
+
+    // ---- scores: the planes of tile i are built while the MMAs of tile i - 1 run ----
+    for (int i = 0; i < n_tiles && ok; ++i) {
+      const int slot = L.k_slots == 2 ? (i & 1) : 0;
+      if (L.k_slots == 1 && i > 0) take_scores(i - 1, true);
+      if (!ok) break;
       const int tl = i * kTile + lane;
       const bool valid = tl < n_local && blk_ok_s[tl >> bs_shift];
       uint32_t bw[4][2] = {};
@@ -470,198 +541,159 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         default: key_planes<4>(base, bw, sg, qjl, w0); break;
       }
       ptx::tmem_wait_st();
-    }
-    if (L.k_slots == 2 && i > 0 && ok) {
-      ok = wait_phase(&bar_s, (i - 1) & 1, abort, a.error);
-      ptx::tc_fence_after();
-      if (ok) read_scores(i - 1);
-    }
-    ptx::tc_fence_before();
-    ok = __syncthreads_and(ok);
-    if (ok && t < 32 && ptx::elect_one()) {
-      ptx::tc_fence_after();
-      uint32_t a_col = tmem + slot * L.kp;
-      uint64_t dsc = desc_mse;
-      for (int s = 0; s < L.pk; ++s) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_e4m3_tmem_a(d_mse, a_col + 8 * kk, dsc + 2 * kk, idesc_s, (s | kk) != 0);
-        a_col += 32;
-        dsc += mse_plane_step;
-      }
-      if (qjl)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_e4m3_tmem_a(d_mse + N1, a_col + 8 * kk, desc_qjl + 2 * kk, idesc_s, kk != 0);
-      ptx::mma_commit(&bar_s);
-    }
-  }
-  if (ok) {
-    ok = wait_phase(&bar_s, (n_tiles - 1) & 1, abort, a.error);
-    ptx::tc_fence_after();
-    if (ok) read_scores(n_tiles - 1);
-  }
-  ptx::tc_fence_before();
-  ok = __syncthreads_and(ok);
-
-  // ---- softmax statistics over the chunk; B_V pieces of exp(s - m) n_v ----
-  if (ok) {
-    float mx[G + 1];                      // per-head score max, then the value-norm max
-#pragma unroll
-    for (int h = 0; h <= G; ++h) mx[h] = h < G ? -INFINITY : 0.f;
-    for (int i = t; i < n_tiles * kTile; i += kThreads) {
-      const bool valid = i < n_local && blk_ok_s[i >> bs_shift];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float sc = valid ? a.scale * (s0[h * kChunk + i] + (qjl ? s1[h * kChunk + i] : 0.f)) : -INFINITY;
-        s0[h * kChunk + i] = sc;
-        mx[h] = fmaxf(mx[h], sc);
-      }
-      if (valid) mx[G] = fmaxf(mx[G], vn_s[i]);
-    }
-    block_reduce(mx, red_s, 0, kThreads / 32, MaxOp());
-    float l[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) l[h] = 0.f;
-    for (int i = t; i < n_tiles * kTile; i += kThreads) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float e = mx[h] != -INFINITY ? __expf(s0[h * kChunk + i] - mx[h]) : 0.f;
-        s0[h * kChunk + i] = e;
-        l[h] += e;
-      }
-    }
-    block_reduce(l, red_s, 0, kThreads / 32, SumOp());
-    if (t == 0)
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        stat_s[0][h] = mx[h];
-        stat_s[1][h] = l[h];
-      }
-    const float sv = piece_scale(mx[G]);
-    // thread (lane, half) writes the pieces of token slot `lane` in tiles half, half + 2
-    const int kpos = k_position(lane);
-    for (int tile = half; tile < n_tiles; tile += 2) {
-      const int tl = tile * kTile + lane;
-      const float nv = (tl < n_local && blk_ok_s[tl >> bs_shift]) ? vn_s[tl] * sv : 0.f;
-      uint8_t* dst = b_v + tile * L.no * 128;
-#pragma unroll
-      for (int h = 0; h < G; h += 2) {
-        if (h + 1 < G)
-          write_pieces2<kVPieces>(dst, h * kVPieces, (h + 1) * kVPieces, kpos, s0[h * kChunk + tl] * nv,
-                                  s0[(h + 1) * kChunk + tl] * nv);
-        else
-          write_pieces<kVPieces>(dst, h * kVPieces, kpos, s0[h * kChunk + tl] * nv);
-      }
-    }
-    if (t == 0) sv_s = sv;
-    ptx::fence_async_shared();
-  }
-  ok = __syncthreads_and(ok);
-  const float sv = sv_s;
-
-  // ---- values: lane d owns coordinate d; units of two sign planes alternate slots ----
-  const int wpd_shift = bs_shift - 5;                 // log2 of the words per coordinate in a block
-  const int n_pairs = (L.pv + 1) / 2;
-  const int n_units = n_tiles * n_pairs;
-  for (int tile = 0; tile < n_tiles && ok; ++tile) {
-    uint32_t bw[4][2] = {};                            // [bit-plane][this thread's 32-token groups]
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int tl = tile * kTile + 32 * (w0 + c);
-      if (tl < n_local && blk_ok_s[tl >> bs_shift]) {
-        const uint32_t* src = vc_s + (tl >> bs_shift) * (L.vblock / 4) + ((tl & (bs - 1)) >> 5) + (lane << wpd_shift);
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-          if (p < a.v_bits) bw[p][c] = src[(p * 128) << wpd_shift];
-      }
-    }
-    for (int pair = 0; pair < n_pairs && ok; ++pair) {
-      const int u = tile * n_pairs + pair, slot = u & 1;
-      if (u >= 2) {
-        ok = wait_phase(&bar_v[slot], ((u - 2) >> 1) & 1, abort, a.error);
-        ptx::tc_fence_after();
-      }
-      if (ok) {
-        const uint32_t base = tmem + row_addr + slot * kValueSlot;
-        switch (a.v_bits) {
-          case 1: value_pair<1>(base, bw, pair, w0); break;
-          case 2: value_pair<2>(base, bw, pair, w0); break;
-          case 3: value_pair<3>(base, bw, pair, w0); break;
-          default: value_pair<4>(base, bw, pair, w0); break;
-        }
-        ptx::tmem_wait_st();
-      }
       ptx::tc_fence_before();
-      ok = __syncthreads_and(ok);
-      if (ok && t < 32 && ptx::elect_one()) {
-        ptx::tc_fence_after();
-        const uint64_t dsc = desc_v + tile * v_tile_step;
-        const uint32_t a_col = tmem + slot * kValueSlot;
-        const uint32_t d_col = tmem + L.col_o + 2 * pair * L.no;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_e4m3_tmem_a(d_col, a_col + 8 * kk, dsc + 2 * kk, idesc_o, (tile | kk) != 0);
-        if (2 * pair + 1 < L.pv)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_e4m3_tmem_a(d_col + L.no, a_col + 32 + 8 * kk, dsc + 2 * kk, idesc_o, (tile | kk) != 0);
-        ptx::mma_commit(&bar_v[slot]);
-      }
+      ptx::mbar_arrive(&kfull[slot]);
+      if (L.k_slots == 2 && i > 0) take_scores(i - 1, true);
     }
-  }
-  // the last commit of each value slot (a commit covers every earlier MMA)
-  if (ok && n_units >= 2) ok = wait_phase(&bar_v[(n_units - 2) & 1], ((n_units - 2) >> 1) & 1, abort, a.error);
-  if (ok) ok = wait_phase(&bar_v[(n_units - 1) & 1], ((n_units - 1) >> 1) & 1, abort, a.error);
-  ptx::tc_fence_after();
+    if (ok) take_scores(n_tiles - 1, false);
+    builder_sync();
+    ok = ok && *abort == 0;
 
-  // ---- partial output of this chunk: half h reads the planes s with s % 2 == h ----
-  if (ok) {
-    float o[G];
+    // ---- softmax statistics over the chunk; B_V pieces of exp(s - m) n_v ----
+    if (ok) {
+      float mx[G + 1];                      // per-head score max, then the value-norm max
 #pragma unroll
-    for (int h = 0; h < G; ++h) o[h] = 0.f;
-    for (int s = half; s < L.pv; s += 2) {
-      const float ws = vw_s[s];
+      for (int h = 0; h <= G; ++h) mx[h] = h < G ? -INFINITY : 0.f;
+      for (int i = t; i < n_tiles * kTile; i += kBuilders) {
+        const bool valid = i < n_local && blk_ok_s[i >> bs_shift];
 #pragma unroll
-      for (int c0 = 0; c0 < NO; c0 += 16) {
-        uint32_t v[16];
-        ptx::tmem_ld16(tmem + row_addr + L.col_o + s * L.no + c0, v);
+        for (int h = 0; h < G; ++h) {
+          const float sc = valid ? a.scale * (s0[h * kChunk + i] + (qjl ? s1[h * kChunk + i] : 0.f)) : -INFINITY;
+          s0[h * kChunk + i] = sc;
+          mx[h] = fmaxf(mx[h], sc);
+        }
+        if (valid) mx[G] = fmaxf(mx[G], vn_s[i]);
+      }
+      block_reduce(mx, red_s, 0, kBuilders / 32, MaxOp());
+      float l[G];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int h = (c0 + j) / kVPieces, piece = (c0 + j) % kVPieces;
-          if (h < G) o[h] = fmaf(ws * inv16_pow(piece), __uint_as_float(v[j]), o[h]);
+      for (int h = 0; h < G; ++h) l[h] = 0.f;
+      for (int i = t; i < n_tiles * kTile; i += kBuilders) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float e = mx[h] != -INFINITY ? __expf(s0[h * kChunk + i] - mx[h]) : 0.f;
+          s0[h * kChunk + i] = e;
+          l[h] += e;
         }
       }
-    }
-    if (half == 1)
+      block_reduce(l, red_s, 0, kBuilders / 32, SumOp());
+      if (t == 0)
 #pragma unroll
-      for (int h = 0; h < G; ++h) s1[h * kTile + lane] = o[h];
-    __syncthreads();
-    if (half == 0) {
+        for (int h = 0; h < G; ++h) {
+          stat_s[0][h] = mx[h];
+          stat_s[1][h] = l[h];
+        }
+      const float sv = piece_scale(mx[G]);
+      // thread (lane, half) writes the pieces of token slot `lane` in tiles half, half + 2
+      const int kpos = k_position(lane);
+      for (int tile = half; tile < n_tiles; tile += 2) {
+        const int tl = tile * kTile + lane;
+        const float nv = (tl < n_local && blk_ok_s[tl >> bs_shift]) ? vn_s[tl] * sv : 0.f;
+        uint8_t* dst = b_v + tile * L.no * 128;
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float* part = a.ws_part + (static_cast<long long>(qbase + h) * a.max_chunks + chunk) * kPartStride;
-        part[4 + lane] = (o[h] + s1[h * kTile + lane]) * (1.f / sv);   // exact: sv is a power of two
-        if (lane == 0) {
-          part[0] = stat_s[0][h];
-          part[1] = stat_s[1][h];
+        for (int h = 0; h < G; h += 2) {
+          if (h + 1 < G)
+            write_pieces2<kVPieces>(dst, h * kVPieces, (h + 1) * kVPieces, kpos, s0[h * kChunk + tl] * nv,
+                                    s0[(h + 1) * kChunk + tl] * nv);
+          else
+            write_pieces<kVPieces>(dst, h * kVPieces, kpos, s0[h * kChunk + tl] * nv);
+        }
+      }
+      if (t == 0) sv_s = sv;
+      ptx::fence_async_shared();
+      builder_sync();                       // every B_V piece is in place before the first value MMA
+
+      // ---- values: lane d owns coordinate d; units of two sign planes alternate slots ----
+      const int wpd_shift = bs_shift - 5;   // log2 of the words per coordinate in a block
+      for (int tile = 0; tile < n_tiles && ok; ++tile) {
+        uint32_t bw[4][2] = {};             // [bit-plane][this thread's 32-token groups]
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int tl = tile * kTile + 32 * (w0 + c);
+          if (tl < n_local && blk_ok_s[tl >> bs_shift]) {
+            const uint32_t* src =
+                vc_s + (tl >> bs_shift) * (L.vblock / 4) + ((tl & (bs - 1)) >> 5) + (lane << wpd_shift);
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+              if (p < a.v_bits) bw[p][c] = src[(p * 128) << wpd_shift];
+          }
+        }
+        for (int pair = 0; pair < n_pairs && ok; ++pair) {
+          const int u = tile * n_pairs + pair, slot = u & 1;
+          if (u >= 2) {
+            ok = wait_phase(&vdone[slot], ((u - 2) >> 1) & 1, abort, a.error);
+            ptx::tc_fence_after();
+            if (!ok) break;
+          }
+          const uint32_t base = tmem + row_addr + slot * kValueSlot;
+          switch (a.v_bits) {
+            case 1: value_pair<1>(base, bw, pair, w0); break;
+            case 2: value_pair<2>(base, bw, pair, w0); break;
+            case 3: value_pair<3>(base, bw, pair, w0); break;
+            default: value_pair<4>(base, bw, pair, w0); break;
+          }
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&vfull[slot]);
+        }
+      }
+      // the last commit of each value slot (a commit covers every earlier MMA)
+      if (ok && n_units >= 2) ok = wait_phase(&vdone[(n_units - 2) & 1], ((n_units - 2) >> 1) & 1, abort, a.error);
+      if (ok) ok = wait_phase(&vdone[(n_units - 1) & 1], ((n_units - 1) >> 1) & 1, abort, a.error);
+      ptx::tc_fence_after();
+
+      // ---- partial output of this chunk: half h reads the planes s with s % 2 == h ----
+      float o[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) o[h] = 0.f;
+      if (ok) {
+        for (int s = half; s < L.pv; s += 2) {
+          const float ws = vw_s[s];
+#pragma unroll
+          for (int c0 = 0; c0 < NO; c0 += 16) {
+            uint32_t v[16];
+            ptx::tmem_ld16(tmem + row_addr + L.col_o + s * L.no + c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int h = (c0 + j) / kVPieces, piece = (c0 + j) % kVPieces;
+              if (h < G) o[h] = fmaf(ws * inv16_pow(piece), __uint_as_float(v[j]), o[h]);
+            }
+          }
+        }
+      }
+      if (half == 1)
+#pragma unroll
+        for (int h = 0; h < G; ++h) s1[h * kTile + lane] = o[h];
+      builder_sync();
+      ok = ok && *abort == 0;
+      if (ok && half == 0) {
+        const float inv_sv = 1.f / sv_s;    // exact: sv is a power of two
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float* part = a.ws_part + (static_cast<long long>(qbase + h) * a.max_chunks + chunk) * kPartStride;
+          part[4 + lane] = (o[h] + s1[h * kTile + lane]) * inv_sv;
+          if (lane == 0) {
+            part[0] = stat_s[0][h];
+            part[1] = stat_s[1][h];
+          }
         }
       }
     }
   }
-  ok = __syncthreads_and(ok);
-  if (!ok && t < 32) {
-    // a wait gave up: let every issued copy and MMA finish before the memory
-    // goes (each lane of warp 0 commits, covering whichever lane issued)
-    ptx::mma_commit(&bar_d);
-    if (t == 0) {
-      ptx::drain_bar(&bar_in, 0);
-      ptx::drain_bar(&bar_d, 0);
-    }
-  }
+
   ptx::tc_fence_before();
   __syncthreads();
-  if (t < 32) {
+  if (!builder) {
+    if (*abort != 0) {
+      // a wait gave up: let every issued copy and MMA finish before the memory
+      // goes (each lane commits, covering whichever lane issued)
+      ptx::mma_commit(&bar_d);
+      if (t == kBuilders) {
+        ptx::drain_bar(&bar_in, 0);
+        ptx::drain_bar(&bar_d, 0);
+      }
+      __syncwarp();
+    }
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, L.tmem);
   }
