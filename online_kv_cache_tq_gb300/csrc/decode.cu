@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 
 #include "e4m3_pieces.cuh"
+#include "gemv512.cuh"
 #include "kernels.h"
 
 namespace tq {
@@ -33,57 +34,62 @@ __device__ __forceinline__ float load_elem(const void* base, long long idx, bool
 __device__ __forceinline__ void record(int* error, int code) { atomicCAS(error, 0, code); }
 
 // ws_q[vec] = (R q, S' R q); with ws_bk, also the tensor-core score operand
-// of this query head: e4m3 pieces of sigma_0 a_S (R q) per key sign plane S
-// and of sigma_1 S' R q (sigma_0, sigma_1 powers of two that bound the pieces).
-__global__ void __launch_bounds__(kThreads) qprep_kernel(DecodeArgs a, bool bf16) {
+// of this query head: e4m3 pieces of 2 sigma_0 a_S (R q)_j / beta_j per key
+// sign plane S and of 2 sigma_1 (S' R q)_j / beta_j (sigma_0, sigma_1 powers
+// of two that bound the pieces; beta_j the bit scale of coordinate j), and the
+// sums that turn the 0/1 bit products into +-1 sign products.  512 threads:
+// thread (o, q) works on coordinate o; the copies of o split the
+// matrix-vector products and the piece planes.
+__global__ void __launch_bounds__(kGemvThreads) qprep_kernel(DecodeArgs a, bool bf16) {
   __shared__ float q_s[kDim];
   __shared__ float qr_s[kDim];
-  __shared__ float red_s[2][kWarps];
+  __shared__ float red_s[4 * kDim];
+  __shared__ float part_s[4];
   const int vec = blockIdx.x;
-  const int o = threadIdx.x;
-  q_s[o] = load_elem(a.q, static_cast<long long>(vec) * kDim + o, bf16);
+  const int o = threadIdx.x & 127, qq = threadIdx.x >> 7;
+  const bool lead = qq == 0;
+  if (lead) q_s[o] = load_elem(a.q, static_cast<long long>(vec) * kDim + o, bf16);
   __syncthreads();
-  float acc = 0.f;
-  for (int i = 0; i < kDim; ++i) acc = fmaf(a.Rt[i * kDim + o], q_s[i], acc);
-  qr_s[o] = acc;
-  a.ws_q[static_cast<long long>(vec) * 2 * kDim + o] = acc;
+  const float acc = gemv512(a.Rt, q_s, red_s);
+  if (lead) {
+    qr_s[o] = acc;
+    a.ws_q[static_cast<long long>(vec) * 2 * kDim + o] = acc;
+  }
   __syncthreads();
   float z = 0.f;
   if (a.qjl_m > 0) {
-    for (int j = 0; j < kDim; ++j) z = fmaf(a.Spt[j * kDim + o], qr_s[j], z);
-    a.ws_q[static_cast<long long>(vec) * 2 * kDim + kDim + o] = z;
+    z = gemv512(a.Spt, qr_s, red_s);
+    if (lead) a.ws_q[static_cast<long long>(vec) * 2 * kDim + kDim + o] = z;
   }
   if (a.ws_bk == nullptr) return;
   const int planes = 1 << (a.k_bits - 1);
-  float amax = 0.f;
-  for (int s = 0; s < planes; ++s) amax = fmaxf(amax, fabsf(a.tables->k_walsh[s]));
-  float m0 = fabsf(acc) * amax, m1 = fabsf(z);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+  float amax = 0.f, asum = 0.f;
+  for (int s = 0; s < planes; ++s) {
+    amax = fmaxf(amax, fabsf(a.tables->k_walsh[s]));
+    asum += a.tables->k_walsh[s];
   }
-  if ((o & 31) == 0) {
-    red_s[0][o >> 5] = m0;
-    red_s[1][o >> 5] = m1;
-  }
-  __syncthreads();
-  for (int w = 0; w < kWarps; ++w) {
-    m0 = fmaxf(m0, red_s[0][w]);
-    m1 = fmaxf(m1, red_s[1][w]);
-  }
-  const float sig0 = piece_scale(m0), sig1 = piece_scale(m1);
+  const float ib = 2.f * bit_inv_scale(o);
+  const float sig0 = piece_scale(max128(fabsf(acc) * amax * ib, part_s));
+  const float sig1 = piece_scale(max128(fabsf(z) * ib, part_s));
+  const float sum_qr = sum128(acc, part_s), sum_qs = sum128(z, part_s);
   uint8_t* dst = a.ws_bk + static_cast<long long>(vec) * a.bk_stride;
   const int kpos = k_position(o);
-  for (int s = 0; s < planes; ++s)
-    write_pieces_rows<kQPieces>(dst + s * kQPieces * 128, kpos, a.tables->k_walsh[s] * acc * sig0);
-  if (a.qjl_m > 0) write_pieces_rows<kQPieces>(dst + planes * kQPieces * 128, kpos, z * sig1);
-  if (o == 0) {
-    float* hdr = reinterpret_cast<float*>(dst + (planes + (a.qjl_m > 0 ? 1 : 0)) * kQPieces * 128);
+  // plane s (s == planes: the QJL operand) by the copies qq == s % 4
+  const int items = planes + (a.qjl_m > 0 ? 1 : 0);
+  for (int s = qq; s < items; s += 4) {
+    const float y = s < planes ? a.tables->k_walsh[s] * acc * ib * sig0 : z * ib * sig1;
+    write_pieces_rows<kQPieces>(dst + s * kQPieces * 128, kpos, y);
+  }
+  if (threadIdx.x == 0) {
+    float* hdr = reinterpret_cast<float*>(dst + items * kQPieces * 128);
     hdr[0] = sig0;
     hdr[1] = sig1;
     hdr[2] = 1.f / sig0;      // exact: powers of two
     hdr[3] = 1.f / sig1;
+    hdr[4] = asum * sum_qr;   // sum_S a_S <q_rot, 1>: the -1 half of every sign
+    hdr[5] = sum_qs;
+    hdr[6] = 0.f;
+    hdr[7] = 0.f;
   }
 }
 
@@ -292,38 +298,55 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(DecodeArgs a) {
   }
 }
 
-// out[vec] = R^T (merged acc / merged l).
-__global__ void __launch_bounds__(kThreads) combine_kernel(DecodeArgs a) {
+// out[vec] = R^T (merged acc / merged l).  512 threads: thread (o, q) merges
+// coordinate o over the chunks c with c % 4 == q, then the copies of o add up
+// and split the back-rotation.
+__global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
   __shared__ float o_s[kDim];
+  __shared__ float red_s[4 * kDim];
+  __shared__ float lred_s[4];
   __shared__ float w_s[1024];
+  __shared__ float part_s[16];
   const int vec = blockIdx.x;
   const int b = vec / a.n_q;
-  const int i = threadIdx.x;
+  const int t = threadIdx.x;
+  const int o = t & 127, q = t >> 7;
   const int ctx = context_of(a, b);
   const int n_chunks = (ctx + kChunk - 1) / kChunk;
   const float* part = a.ws_part + static_cast<long long>(vec) * a.max_chunks * kPartStride;
   float mx = -INFINITY;
-  for (int c = 0; c < n_chunks; ++c) mx = fmaxf(mx, part[c * kPartStride]);
+  for (int c = t; c < n_chunks; c += kGemvThreads) mx = fmaxf(mx, part[c * kPartStride]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if ((t & 31) == 0) part_s[t >> 5] = mx;
+  __syncthreads();
+  mx = part_s[0];
+  for (int w = 1; w < kGemvThreads / 32; ++w) mx = fmaxf(mx, part_s[w]);
   float l = 0.f, acc = 0.f;
   for (int c0 = 0; c0 < n_chunks; c0 += 1024) {
     const int cn = min(1024, n_chunks - c0);
     __syncthreads();
-    for (int c = i; c < cn; c += kThreads) {
+    for (int c = t; c < cn; c += kGemvThreads) {
       const float m = part[(c0 + c) * kPartStride];
       w_s[c] = (m == -INFINITY) ? 0.f : __expf(m - mx);
     }
     __syncthreads();
-    for (int c = 0; c < cn; ++c) {
+    for (int c = q; c < cn; c += 4) {
       const float w = w_s[c];
       l = fmaf(w, part[(c0 + c) * kPartStride + 1], l);
-      acc = fmaf(w, part[(c0 + c) * kPartStride + 4 + i], acc);
+      acc = fmaf(w, part[(c0 + c) * kPartStride + 4 + o], acc);
     }
   }
-  o_s[i] = l > 0.f ? acc / l : 0.f;
+  red_s[q * kDim + o] = acc;
+  if (o == 0) lred_s[q] = l;
   __syncthreads();
-  float out = 0.f;
-  for (int j = 0; j < kDim; ++j) out = fmaf(a.R[j * kDim + i], o_s[j], out);
-  a.out[static_cast<long long>(vec) * kDim + i] = out;
+  const float lt = (lred_s[0] + lred_s[1]) + (lred_s[2] + lred_s[3]);
+  const float at = (red_s[o] + red_s[kDim + o]) + (red_s[2 * kDim + o] + red_s[3 * kDim + o]);
+  __syncthreads();
+  if (q == 0) o_s[o] = lt > 0.f ? at / lt : 0.f;
+  __syncthreads();
+  const float out = gemv512(a.R, o_s, red_s);
+  if (q == 0) a.out[static_cast<long long>(vec) * kDim + o] = out;
 }
 
 }  // namespace
@@ -331,7 +354,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(DecodeArgs a) {
 cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_t stream) {
   const int n_vec = args.batch * args.n_q;
   if (n_vec <= 0) return cudaSuccess;
-  qprep_kernel<<<n_vec, kThreads, 0, stream>>>(args, bf16);
+  qprep_kernel<<<n_vec, kGemvThreads, 0, stream>>>(args, bf16);
   return cudaGetLastError();
 }
 
@@ -351,7 +374,7 @@ cudaError_t launch_decode_partials(const DecodeArgs& args, cudaStream_t stream) 
 cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream) {
   const int n_vec = args.batch * args.n_q;
   if (n_vec <= 0) return cudaSuccess;
-  combine_kernel<<<n_vec, kThreads, 0, stream>>>(args);
+  combine_kernel<<<n_vec, kGemvThreads, 0, stream>>>(args);
   return cudaGetLastError();
 }
 

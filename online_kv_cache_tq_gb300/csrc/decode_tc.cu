@@ -53,7 +53,7 @@ constexpr int kTile = 128;                  // tokens per tile = tensor-memory l
 constexpr int kTiles = kChunk / kTile;      // tiles per chunk
 constexpr int kBuilders = 256;              // warps 0-7: two threads per tensor-memory lane
 constexpr int kThreads = kBuilders + 32;     // warp 8: copies and MMA issue
-constexpr int kVPieces = 3;                 // e4m3 pieces of a softmax weight
+constexpr int kVPieces = 4;                 // e4m3 pieces of a softmax weight
 
 __host__ __device__ constexpr int round16(int x) { return (x + 15) / 16 * 16; }
 __host__ __device__ constexpr int score_cols(int g) { return round16(kQPieces * g); }   // per group
@@ -63,23 +63,24 @@ __host__ __device__ constexpr int value_cols(int g) { return round16(kVPieces * 
 // 128-byte swizzle (rows of 128 bytes, 16-byte chunk c of row n at c ^ (n % 8)).
 __device__ __forceinline__ int sw128(int n, int k) { return n * 128 + ((((k >> 4) ^ (n & 7))) << 4) + (k & 15); }
 
-// Store the e4m3 +-1 image of one 32-bit word of bits (bit 1 -> +1.0 = 0x38,
-// bit 0 -> -1.0 = 0xB8) as eight columns: column j holds bits j, j+8, j+16,
-// j+24 of the word.
-// The bit arithmetic sits inside the asm block so that the compiler keeps
-// only the word, not eight operand registers per plane, live across planes.
-__device__ __forceinline__ void store_signs(uint32_t taddr, uint32_t w) {
+// Store the 0/beta_j e4m3 image of one 32-bit word of bits as eight columns:
+// column j holds bits j, j+8, j+16, j+24 of the word, each as 0 or the power
+// of two beta_j of bit_inv_scale (ten integer operations per word).  The
+// arithmetic sits inside the asm block so that the compiler keeps only the
+// word, not eight operand registers per plane, live across planes.
+__device__ __forceinline__ void store_bits(uint32_t taddr, uint32_t w) {
   asm volatile(
-      "{\n\t.reg .b32 i, c0, c1, c2, c3, c4, c5, c6, c7;\n\t"
-      "not.b32 i, %1;\n\t"
-      "shl.b32 c0, i, 7;\n\tand.b32 c0, c0, 0x80808080;\n\tor.b32 c0, c0, 0x38383838;\n\t"
-      "shl.b32 c1, i, 6;\n\tand.b32 c1, c1, 0x80808080;\n\tor.b32 c1, c1, 0x38383838;\n\t"
-      "shl.b32 c2, i, 5;\n\tand.b32 c2, c2, 0x80808080;\n\tor.b32 c2, c2, 0x38383838;\n\t"
-      "shl.b32 c3, i, 4;\n\tand.b32 c3, c3, 0x80808080;\n\tor.b32 c3, c3, 0x38383838;\n\t"
-      "shl.b32 c4, i, 3;\n\tand.b32 c4, c4, 0x80808080;\n\tor.b32 c4, c4, 0x38383838;\n\t"
-      "shl.b32 c5, i, 2;\n\tand.b32 c5, c5, 0x80808080;\n\tor.b32 c5, c5, 0x38383838;\n\t"
-      "shl.b32 c6, i, 1;\n\tand.b32 c6, c6, 0x80808080;\n\tor.b32 c6, c6, 0x38383838;\n\t"
-      "and.b32 c7, i, 0x80808080;\n\tor.b32 c7, c7, 0x38383838;\n\t"
+      "{\n\t.reg .b32 s, h, c0, c1, c2, c3, c4, c5, c6, c7;\n\t"
+      "shl.b32 s, %1, 3;\n\t"
+      "shr.b32 h, %1, 1;\n\t"
+      "and.b32 c0, s, 0x08080808;\n\t"
+      "and.b32 c1, s, 0x10101010;\n\t"
+      "and.b32 c2, s, 0x20202020;\n\t"
+      "and.b32 c3, %1, 0x08080808;\n\t"
+      "and.b32 c4, %1, 0x10101010;\n\t"
+      "and.b32 c5, %1, 0x20202020;\n\t"
+      "and.b32 c6, %1, 0x40404040;\n\t"
+      "and.b32 c7, h, 0x40404040;\n\t"
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {c0, c1, c2, c3, c4, c5, c6, c7};\n\t}\n"
       ::"r"(taddr), "r"(w)
       : "memory");
@@ -112,11 +113,11 @@ __device__ __forceinline__ void key_planes(uint32_t base, const uint32_t (&bw)[4
     const int set = walsh_set(BITS, s);
 #pragma unroll
     for (int c = 0; c < 2; ++c)
-      store_signs(base + 32 * s + 8 * (w0 + c), plane_word(bw[0][c], bw[1][c], bw[2][c], bw[3][c], set));
+      store_bits(base + 32 * s + 8 * (w0 + c), plane_word(bw[0][c], bw[1][c], bw[2][c], bw[3][c], set));
   }
   if (qjl)
 #pragma unroll
-    for (int c = 0; c < 2; ++c) store_signs(base + 32 * P + 8 * (w0 + c), sg[c]);
+    for (int c = 0; c < 2; ++c) store_bits(base + 32 * P + 8 * (w0 + c), sg[c]);
 }
 
 // Value sign plane S of BITS-bit codes (compile-time Walsh set) at `col`.
@@ -126,7 +127,7 @@ __device__ __forceinline__ void value_plane(uint32_t col, const uint32_t (&bw)[4
     constexpr int set = S < BITS ? 1 << S : (BITS == 3 ? 7 : 15 ^ (1 << (7 - S)));
 #pragma unroll
     for (int c = 0; c < 2; ++c)
-      store_signs(col + 8 * (w0 + c), plane_word(bw[0][c], bw[1][c], bw[2][c], bw[3][c], set));
+      store_bits(col + 8 * (w0 + c), plane_word(bw[0][c], bw[1][c], bw[2][c], bw[3][c], set));
   }
 }
 
@@ -315,10 +316,11 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   __shared__ __align__(8) uint64_t bar_in, kfull[2], kdone, sfree, vfull[2], vdone[2], bar_d;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
-  __shared__ float red_s[(kBuilders / 32) * (G + 1)];
+  __shared__ float red_s[(kBuilders / 32) * (2 * G + 1)];   // block_reduce of up to 2 G + 1 values
   __shared__ float stat_s[2][G];                // chunk max, chunk sum per head
   __shared__ int blk_ok_s[kChunk / 32];         // physical block of each block slot is valid
   __shared__ float sv_s;                        // piece scale of the softmax weights
+  __shared__ float wsum_s[G];                   // sum over the chunk of e n_v per head
   __shared__ float vw_s[8];                     // odd Walsh coefficients of the value codebook
 
   const int t = threadIdx.x;
@@ -456,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     // (overlaps the copies); row n = h kQPieces + i of plane s, 16-byte chunk c
     // of a row at c ^ (n % 8)
     float inv_sig[G];                             // 1 / sigma of this thread's accumulator columns
+    float ones[G];                                // the -1 half of the +-1 products of those columns
     {
       const int nk = L.pk + L.pq;
       const int per_head = nk * kQPieces * 8;     // 16-byte chunks per head
@@ -468,16 +471,20 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         *reinterpret_cast<uint4*>(dst + n * 128 + ((c ^ (n & 7)) << 4)) = v;
       }
 #pragma unroll
-      for (int h = 0; h < G; ++h)
-        inv_sig[h] = reinterpret_cast<const float*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride +
-                                                    nk * kQPieces * 128)[2 + half];
+      for (int h = 0; h < G; ++h) {
+        const float* hdr = reinterpret_cast<const float*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride +
+                                                          nk * kQPieces * 128);
+        inv_sig[h] = hdr[2 + half];
+        ones[h] = hdr[4 + half];
+      }
     }
     ptx::fence_async_shared();
     ok = wait_phase(&bar_in, 0, abort, a.error);
     builder_sync();                               // blk_ok_s was written by the control warp before its copies
 
-    // accumulators of key tile i -> s0 (half 0: n_k <q_rot, k_mse> / sigma) and
-    // s1 (half 1: gamma coef <q_s, signs> / sigma)
+    // accumulators of key tile i -> s0 (half 0: n_k <q_rot, k_mse>) and s1
+    // (half 1: gamma coef <q_s, signs>); an accumulator holds sigma times the
+    // 0/1-bit sum, so the +-1 sum is acc / sigma - ones
     auto read_scores = [&](int i) {
       const int tl = i * kTile + lane;
       const bool valid = tl < n_local && blk_ok_s[tl >> bs_shift];
@@ -498,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       const float f = valid ? (half == 0 ? kn_s[tl] : kr_s[tl] * a.qjl_coef) : 0.f;
       float* dst = half == 0 ? s0 : s1;
 #pragma unroll
-      for (int h = 0; h < G; ++h) dst[h * kChunk + tl] = f * (acc[h] * inv_sig[h]);
+      for (int h = 0; h < G; ++h) dst[h * kChunk + tl] = f * fmaf(acc[h], inv_sig[h], -ones[h]);
     };
     // wait for the MMAs of tile i, read its accumulators, release them
     auto take_scores = [&](int i, bool release) {
@@ -565,15 +572,17 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         if (valid) mx[G] = fmaxf(mx[G], vn_s[i]);
       }
       block_reduce(mx, red_s, 0, kBuilders / 32, MaxOp());
-      float l[G];
+      float l[2 * G];                       // sum of e, then sum of e n_v, per head
 #pragma unroll
-      for (int h = 0; h < G; ++h) l[h] = 0.f;
+      for (int h = 0; h < 2 * G; ++h) l[h] = 0.f;
       for (int i = t; i < n_tiles * kTile; i += kBuilders) {
+        const float nv = (i < n_local && blk_ok_s[i >> bs_shift]) ? vn_s[i] : 0.f;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const float e = mx[h] != -INFINITY ? __expf(s0[h * kChunk + i] - mx[h]) : 0.f;
           s0[h * kChunk + i] = e;
           l[h] += e;
+          l[G + h] = fmaf(e, nv, l[G + h]);
         }
       }
       block_reduce(l, red_s, 0, kBuilders / 32, SumOp());
@@ -582,13 +591,16 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         for (int h = 0; h < G; ++h) {
           stat_s[0][h] = mx[h];
           stat_s[1][h] = l[h];
+          wsum_s[h] = l[G + h];
         }
-      const float sv = piece_scale(mx[G]);
+      // the pieces carry 2 e n_v sv / beta_t, below 2 * 64 * max n_v * sv
+      const float sv = piece_scale(2.f * kMaxBitInvScale * mx[G]);
       // thread (lane, half) writes the pieces of token slot `lane` in tiles half, half + 2
       const int kpos = k_position(lane);
+      const float ib = 2.f * bit_inv_scale(lane);
       for (int tile = half; tile < n_tiles; tile += 2) {
         const int tl = tile * kTile + lane;
-        const float nv = (tl < n_local && blk_ok_s[tl >> bs_shift]) ? vn_s[tl] * sv : 0.f;
+        const float nv = (tl < n_local && blk_ok_s[tl >> bs_shift]) ? vn_s[tl] * sv * ib : 0.f;
         uint8_t* dst = b_v + tile * L.no * 128;
 #pragma unroll
         for (int h = 0; h < G; h += 2) {
@@ -668,10 +680,12 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       ok = ok && *abort == 0;
       if (ok && half == 0) {
         const float inv_sv = 1.f / sv_s;    // exact: sv is a power of two
+        float a_sum = 0.f;                  // sum_S a_S: the -1 half of every sign product
+        for (int s = 0; s < L.pv; ++s) a_sum += vw_s[s];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           float* part = a.ws_part + (static_cast<long long>(qbase + h) * a.max_chunks + chunk) * kPartStride;
-          part[4 + lane] = (o[h] + s1[h * kTile + lane]) * inv_sv;
+          part[4 + lane] = fmaf(o[h] + s1[h * kTile + lane], inv_sv, -a_sum * wsum_s[h]);
           if (lane == 0) {
             part[0] = stat_s[0][h];
             part[1] = stat_s[1][h];

@@ -1,0 +1,58 @@
+// 128 x 128 matrix-vector products for the per-vector kernels of one decode
+// step (append, query preparation, combine), by a CTA of 512 threads.
+#pragma once
+
+namespace tq {
+
+constexpr int kGemvThreads = 512;
+
+// out[o] = sum_i w[i * 128 + o] * in_s[i] for o = threadIdx.x % 128.  Thread
+// (o, q = threadIdx.x / 128) sums the 32 terms i in [32 q, 32 q + 32) with all
+// 32 loads in flight at once, and the four partial sums meet in red_s
+// ([4][128] floats).  Every thread returns out[o]; in_s must be visible to
+// all threads before the call, and red_s is free again on return.
+__device__ __forceinline__ float gemv512(const float* __restrict__ w, const float* in_s, float* red_s) {
+  const int o = threadIdx.x & 127, q = threadIdx.x >> 7;
+  const float* wp = w + (32 * q) * 128 + o;
+  float v[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) v[k] = __ldg(wp + k * 128);
+  float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+  for (int k = 0; k < 32; k += 4) {
+    acc0 = fmaf(v[k + 0], in_s[32 * q + k + 0], acc0);
+    acc1 = fmaf(v[k + 1], in_s[32 * q + k + 1], acc1);
+    acc2 = fmaf(v[k + 2], in_s[32 * q + k + 2], acc2);
+    acc3 = fmaf(v[k + 3], in_s[32 * q + k + 3], acc3);
+  }
+  red_s[q * 128 + o] = (acc0 + acc1) + (acc2 + acc3);
+  __syncthreads();
+  const float r = (red_s[o] + red_s[128 + o]) + (red_s[256 + o] + red_s[384 + o]);
+  __syncthreads();
+  return r;
+}
+
+// Sum of v over the 128 values o (each held by threads o, o + 128, ...): the
+// first four warps reduce into part_s ([4] floats); every thread gets the sum.
+__device__ __forceinline__ float sum128(float v, float* part_s) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  if (threadIdx.x < 128 && (threadIdx.x & 31) == 0) part_s[threadIdx.x >> 5] = v;
+  __syncthreads();
+  const float s = (part_s[0] + part_s[1]) + (part_s[2] + part_s[3]);
+  __syncthreads();
+  return s;
+}
+
+// Maximum of v over the 128 values o, as sum128.
+__device__ __forceinline__ float max128(float v, float* part_s) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  if (threadIdx.x < 128 && (threadIdx.x & 31) == 0) part_s[threadIdx.x >> 5] = v;
+  __syncthreads();
+  const float s = fmaxf(fmaxf(part_s[0], part_s[1]), fmaxf(part_s[2], part_s[3]));
+  __syncthreads();
+  return s;
+}
+
+}  // namespace tq

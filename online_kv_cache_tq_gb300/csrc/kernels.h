@@ -88,10 +88,12 @@ constexpr int kQPieces = 6;       // e4m3 pieces of a query coefficient (tensor-
 
 // Bytes of one query head's tensor-core score operand in the decode
 // workspace: for each key sign plane and the QJL plane, kQPieces rows of 128
-// e4m3 bytes (row i: piece i of a_S q_rot or of q_s, K order of k_position),
-// then sigma_mse, sigma_qjl and their inverses as floats.
+// e4m3 bytes (row i: piece i of 2 a_S q_rot / beta or of 2 q_s / beta, in the
+// K order of k_position), then 8 floats: sigma_mse, sigma_qjl, their
+// inverses, (sum_S a_S) (sum_j q_rot_j), sum_k q_s_k, and two unused.
+constexpr int kBkHeader = 32;
 __host__ __device__ constexpr int bk_head_bytes(int k_mse_bits, bool qjl) {
-  return ((k_mse_bits >= 1 ? (1 << (k_mse_bits - 1)) : 0) + (qjl ? 1 : 0)) * kQPieces * 128 + 16;
+  return ((k_mse_bits >= 1 ? (1 << (k_mse_bits - 1)) : 0) + (qjl ? 1 : 0)) * kQPieces * 128 + kBkHeader;
 }
 constexpr int kPartStride = 132;  // m, l, 2 pad, acc[128]
 
