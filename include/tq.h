@@ -148,6 +148,35 @@ tq_status tq_decode_attention(const tq_codebook* book, const void* q, tq_dtype d
                               const int32_t* context_lens, int max_context, float scale, float* out,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/* One decode step in one call: append one new key and value per sequence at
+ * position context_lens[b] - 1 of sequence b (the slot follows from
+ * block_table exactly as decode reads it), then decode attention for one
+ * query per sequence over the cache that now holds them.  k_new, v_new:
+ * device [batch][n_kv_heads][d] in kv_dtype (both required when batch > 0);
+ * every other argument as in tq_decode_attention, and context_lens already
+ * counts the appended token (a sequence with context 0 appends nothing).
+ * Equivalent to tq_quantize_append with those slots followed by
+ * tq_decode_attention.  When batch * n_kv_heads <= 1024 the append and the
+ * query preparation share one launch, and the partials kernel starts while
+ * it runs (a programmatic dependent launch that waits for it only where it
+ * reads the query operands and the chunk holding the appended token).
+ * Asynchronous on `stream`. */
+tq_status tq_decode_step(const tq_codebook* book, const void* k_new, const void* v_new, tq_dtype kv_dtype,
+                         const void* q, tq_dtype q_dtype, int batch, int n_q_heads, int n_kv_heads,
+                         const tq_cache_view* cache, const int32_t* block_table, int max_blocks,
+                         const int32_t* context_lens, int max_context, float scale, float* out,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* The first stage of tq_decode_step, for callers that run the stages one at a
+ * time (then tq_decode_partials and tq_decode_finish with the step's
+ * arguments): the append of k_new / v_new and the query preparation, in one
+ * launch when batch * n_kv_heads <= 1024.  Arguments as tq_decode_step. */
+tq_status tq_decode_step_prepare(const tq_codebook* book, const void* k_new, const void* v_new,
+                                 tq_dtype kv_dtype, const void* q, tq_dtype q_dtype, int batch,
+                                 int n_q_heads, int n_kv_heads, const tq_cache_view* cache,
+                                 const int32_t* block_table, int max_blocks, const int32_t* context_lens,
+                                 int max_context, void* workspace, size_t workspace_bytes, void* stream);
+
 /* The three stages tq_decode_attention runs, callable one at a time on the
  * same stream with the same arguments and workspace (e.g. to overlap query
  * preparation with other work, or to time the stages):

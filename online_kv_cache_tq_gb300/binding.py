@@ -22,7 +22,7 @@ FIELDS = ("k_codes", "k_qjl", "k_norm", "k_rnorm", "v_codes", "v_norm")
 # Entry points declared in include/tq.h, checked by the ABI test.
 EXPORTED = ("tq_codebook_build", "tq_codebook_destroy", "tq_codebook_levels", "tq_codebook_matrices",
             "tq_cache_field_bytes", "tq_quantize_append", "tq_decode_workspace_bytes",
-            "tq_decode_attention", "tq_decode_prepare", "tq_decode_partials", "tq_decode_finish",
+            "tq_decode_attention", "tq_decode_step", "tq_decode_step_prepare", "tq_decode_prepare", "tq_decode_partials", "tq_decode_finish",
             "tq_decode_attention_static", "tq_decode_kernel_kind", "tq_get_last_device_error",
             "tq_status_string")
 
@@ -71,6 +71,10 @@ def load():
     lib.tq_decode_workspace_bytes.restype = sz
     lib.tq_decode_attention.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.POINTER(tq_cache_view), vp, i32,
                                         vp, i32, ctypes.c_float, vp, vp, sz, vp]
+    lib.tq_decode_step.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32, ctypes.POINTER(tq_cache_view), vp,
+                                   i32, vp, i32, ctypes.c_float, vp, vp, sz, vp]
+    lib.tq_decode_step_prepare.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                           ctypes.POINTER(tq_cache_view), vp, i32, vp, i32, vp, sz, vp]
     lib.tq_decode_prepare.argtypes = [vp, vp, i32, i32, i32, i32, vp, sz, vp]
     lib.tq_decode_partials.argtypes = [vp, i32, i32, i32, ctypes.POINTER(tq_cache_view), vp, i32, vp, i32,
                                        ctypes.c_float, vp, sz, vp]
@@ -201,6 +205,25 @@ def tq_decode_attention(book, q, dtype, batch, n_q_heads, n_kv_heads, view, bloc
                                       max_context, scale, _ptr(out), _ptr(workspace), workspace_bytes,
                                       _stream(stream)),
            "tq_decode_attention")
+
+
+def tq_decode_step(book, k_new, v_new, kv_dtype, q, q_dtype, batch, n_q_heads, n_kv_heads, view, block_table,
+                   max_blocks, context_lens, max_context, scale, out, workspace, workspace_bytes, stream=None):
+    _check(load().tq_decode_step(book.handle, _ptr(k_new), _ptr(v_new), kv_dtype, _ptr(q), q_dtype, batch,
+                                 n_q_heads, n_kv_heads, ctypes.byref(view), _ptr(block_table), max_blocks,
+                                 _ptr(context_lens), max_context, scale, _ptr(out), _ptr(workspace),
+                                 workspace_bytes, _stream(stream)),
+           "tq_decode_step")
+
+
+def tq_decode_step_prepare(book, k_new, v_new, kv_dtype, q, q_dtype, batch, n_q_heads, n_kv_heads, view,
+                           block_table, max_blocks, context_lens, max_context, workspace, workspace_bytes,
+                           stream=None):
+    _check(load().tq_decode_step_prepare(book.handle, _ptr(k_new), _ptr(v_new), kv_dtype, _ptr(q), q_dtype, batch,
+                                         n_q_heads, n_kv_heads, ctypes.byref(view), _ptr(block_table),
+                                         max_blocks, _ptr(context_lens), max_context, _ptr(workspace),
+                                         workspace_bytes, _stream(stream)),
+           "tq_decode_step_prepare")
 
 
 def tq_decode_prepare(book, q, dtype, batch, n_q_heads, max_context, workspace, workspace_bytes, stream=None):

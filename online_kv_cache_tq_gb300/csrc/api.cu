@@ -311,20 +311,23 @@ tq_status tq_cache_field_bytes(const tq_codebook* book, size_t bytes_per_item[6]
   return TQ_OK;
 }
 
-tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void* v, tq_dtype dtype,
-                             int n_tokens, int n_kv_heads, const int64_t* slot_mapping,
-                             const tq_cache_view* cache, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Validate an append and fill the launch arguments of its keys and values.
+tq_status append_args(const tq_codebook* book, const void* k, const void* v, tq_dtype dtype, int n_tokens,
+                      int n_kv_heads, const int64_t* slot_mapping, const tq_cache_view* cache, tq::QuantizeArgs* ka,
+                      tq::QuantizeArgs* va) {
   if (!valid_device_handle(book)) return TQ_ERR_INVALID_ARG;
   if (dtype != TQ_BF16 && dtype != TQ_FP32) return TQ_ERR_INVALID_ARG;
   if (n_tokens < 0 || n_kv_heads <= 0 || !valid_cache(book, cache) || cache->n_kv_heads != n_kv_heads) {
     return TQ_ERR_INVALID_ARG;
   }
   if (n_tokens == 0) return TQ_OK;
-  if (slot_mapping == nullptr || (k == nullptr && v == nullptr)) return TQ_ERR_INVALID_ARG;
+  if (k == nullptr && v == nullptr) return TQ_ERR_INVALID_ARG;
   if ((k && !aligned16(k)) || (v && !aligned16(v))) return TQ_ERR_INVALID_ARG;
   if (static_cast<long long>(n_tokens) * n_kv_heads > (1ll << 31) - 1) return TQ_ERR_INVALID_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool bf16 = dtype == TQ_BF16;
   tq::QuantizeArgs base{};
   base.n_vec = n_tokens * n_kv_heads;
   base.n_tokens = n_tokens;
@@ -335,26 +338,33 @@ tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void*
   base.Rt = book->d_Rt;
   base.Spt = book->d_Spt;
   base.error = book->d_error;
-  tq::QuantizeArgs ka = base, va = base;
-  ka.x = k;
-  ka.codes = static_cast<uint8_t*>(cache->k_codes);
-  ka.qjl = book->cfg.qjl_m > 0 ? static_cast<uint8_t*>(cache->k_qjl) : nullptr;
-  ka.norm = cache->k_norm;
-  ka.rnorm = book->cfg.qjl_m > 0 ? cache->k_rnorm : nullptr;
-  ka.bits = book->k_mse_bits;
-  ka.transposed = false;
-  ka.levels = table_field(book, offsetof(tq::DeviceTables, k_levels));
-  ka.bounds = table_field(book, offsetof(tq::DeviceTables, k_bounds));
-  va.x = v;
-  va.codes = static_cast<uint8_t*>(cache->v_codes);
-  va.qjl = nullptr;
-  va.norm = cache->v_norm;
-  va.rnorm = nullptr;
-  va.bits = book->v_bits;
-  va.transposed = true;
-  va.levels = table_field(book, offsetof(tq::DeviceTables, v_levels));
-  va.bounds = table_field(book, offsetof(tq::DeviceTables, v_bounds));
-  if (base.n_vec <= tq::kSmallQuantize) {
+  *ka = base;
+  *va = base;
+  ka->x = k;
+  ka->codes = static_cast<uint8_t*>(cache->k_codes);
+  ka->qjl = book->cfg.qjl_m > 0 ? static_cast<uint8_t*>(cache->k_qjl) : nullptr;
+  ka->norm = cache->k_norm;
+  ka->rnorm = book->cfg.qjl_m > 0 ? cache->k_rnorm : nullptr;
+  ka->bits = book->k_mse_bits;
+  ka->transposed = false;
+  ka->levels = table_field(book, offsetof(tq::DeviceTables, k_levels));
+  ka->bounds = table_field(book, offsetof(tq::DeviceTables, k_bounds));
+  va->x = v;
+  va->codes = static_cast<uint8_t*>(cache->v_codes);
+  va->qjl = nullptr;
+  va->norm = cache->v_norm;
+  va->rnorm = nullptr;
+  va->bits = book->v_bits;
+  va->transposed = true;
+  va->levels = table_field(book, offsetof(tq::DeviceTables, v_levels));
+  va->bounds = table_field(book, offsetof(tq::DeviceTables, v_bounds));
+  return TQ_OK;
+}
+
+// Launch a validated append (either tensor may be absent).
+tq_status run_append(const tq_codebook* book, const void* k, const void* v, const tq::QuantizeArgs& ka,
+                     const tq::QuantizeArgs& va, bool bf16, cudaStream_t s) {
+  if (ka.n_vec <= tq::kSmallQuantize) {
     // a decode step: keys and values in one launch, one CTA per vector
     return tq::launch_quantize_small(k ? &ka : nullptr, v ? &va : nullptr, bf16, s) == cudaSuccess ? TQ_OK
                                                                                                     : TQ_ERR_CUDA;
@@ -362,6 +372,20 @@ tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void*
   if (k && launch_quantize(book, ka, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;
   if (v && launch_quantize(book, va, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;
   return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void* v, tq_dtype dtype,
+                             int n_tokens, int n_kv_heads, const int64_t* slot_mapping,
+                             const tq_cache_view* cache, void* stream) {
+  if (n_tokens > 0 && slot_mapping == nullptr) return TQ_ERR_INVALID_ARG;
+  tq::QuantizeArgs ka{}, va{};
+  const tq_status st = append_args(book, k, v, dtype, n_tokens, n_kv_heads, slot_mapping, cache, &ka, &va);
+  if (st != TQ_OK || n_tokens == 0) return st;
+  return run_append(book, k, v, ka, va, dtype == TQ_BF16, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
@@ -470,9 +494,11 @@ tq_status decode_args(const tq_codebook* book, int stages, const void* q, tq_dty
 
 tq_status launched(cudaError_t err) { return err == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
 
-// Tensor-core partials where supported, SIMT otherwise.
-cudaError_t launch_partials(const tq_codebook* book, const tq::DecodeArgs& a, cudaStream_t s) {
-  if (tq::tc_decode_supported(a, book->walsh_ok)) return tq::launch_decode_partials_tc(a, s);
+// Tensor-core partials where supported, SIMT otherwise.  early: the previous
+// launch on the stream is a decode step's fused append + query preparation
+// and the tensor-core kernel may overlap it (programmatic dependent launch).
+cudaError_t launch_partials(const tq_codebook* book, const tq::DecodeArgs& a, cudaStream_t s, bool early = false) {
+  if (tq::tc_decode_supported(a, book->walsh_ok)) return tq::launch_decode_partials_tc(a, s, early);
   return tq::launch_decode_partials(a, s);
 }
 
@@ -493,6 +519,85 @@ tq_status tq_decode_attention(const tq_codebook* book, const void* q, tq_dtype d
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = launched(tq::launch_decode_prepare(a, dtype == TQ_BF16, s));
   if (st == TQ_OK) st = launched(launch_partials(book, a, s));
+  if (st == TQ_OK) st = launched(tq::launch_decode_finish(a, s));
+  return st;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Arguments of a decode step: the append of one key and value per sequence
+// at position context_lens[b] - 1 (slots derived on the device from the
+// block table) and the decode stages.
+tq_status step_args(const tq_codebook* book, const void* k_new, const void* v_new, tq_dtype kv_dtype, const void* q,
+                    tq_dtype q_dtype, int batch, int n_q_heads, int n_kv_heads, const tq_cache_view* cache,
+                    const int32_t* block_table, int max_blocks, const int32_t* context_lens, int max_context,
+                    float scale, float* out, void* workspace, size_t workspace_bytes, int stages,
+                    tq::QuantizeArgs* ka, tq::QuantizeArgs* va, tq::DecodeArgs* a) {
+  if (batch > 0 && (k_new == nullptr || v_new == nullptr)) return TQ_ERR_INVALID_ARG;
+  tq_status st = append_args(book, k_new, v_new, kv_dtype, batch, n_kv_heads, nullptr, cache, ka, va);
+  if (st != TQ_OK) return st;
+  st = decode_args(book, stages, q, q_dtype, batch, n_q_heads, n_kv_heads, cache, block_table, max_blocks,
+                   context_lens, max_context, scale, out, workspace, workspace_bytes, a);
+  if (st != TQ_OK) return st;
+  if (batch > 0 && (max_blocks <= 0 || context_lens == nullptr)) return TQ_ERR_INVALID_ARG;
+  for (tq::QuantizeArgs* x : {ka, va}) {
+    x->step_block_table = block_table;
+    x->step_context_lens = context_lens;
+    x->step_max_blocks = max_blocks;
+  }
+  return TQ_OK;
+}
+
+// Launch the append and query preparation of a validated step.
+tq_status run_step_prepare(const tq_codebook* book, const void* k_new, const void* v_new, bool kv_bf16,
+                           const tq::QuantizeArgs& ka, const tq::QuantizeArgs& va, const tq::DecodeArgs& a,
+                           bool q_bf16, cudaStream_t s, bool* fused) {
+  *fused = ka.n_vec <= tq::kSmallQuantize;
+  if (*fused) return launched(tq::launch_step_prep(ka, va, kv_bf16, a, q_bf16, s));
+  tq_status st = run_append(book, k_new, v_new, ka, va, kv_bf16, s);
+  if (st == TQ_OK) st = launched(tq::launch_decode_prepare(a, q_bf16, s));
+  return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+tq_status tq_decode_step_prepare(const tq_codebook* book, const void* k_new, const void* v_new,
+                                 tq_dtype kv_dtype, const void* q, tq_dtype q_dtype, int batch, int n_q_heads,
+                                 int n_kv_heads, const tq_cache_view* cache, const int32_t* block_table,
+                                 int max_blocks, const int32_t* context_lens, int max_context, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  tq::QuantizeArgs ka{}, va{};
+  tq::DecodeArgs a;
+  tq_status st = step_args(book, k_new, v_new, kv_dtype, q, q_dtype, batch, n_q_heads, n_kv_heads, cache,
+                           block_table, max_blocks, context_lens, max_context, 0.f, nullptr, workspace,
+                           workspace_bytes, kPrepare | kPartials, &ka, &va, &a);
+  if (st != TQ_OK || batch == 0) return st;
+  bool fused;
+  return run_step_prepare(book, k_new, v_new, kv_dtype == TQ_BF16, ka, va, a, q_dtype == TQ_BF16,
+                          static_cast<cudaStream_t>(stream), &fused);
+}
+
+tq_status tq_decode_step(const tq_codebook* book, const void* k_new, const void* v_new, tq_dtype kv_dtype,
+                         const void* q, tq_dtype q_dtype, int batch, int n_q_heads, int n_kv_heads,
+                         const tq_cache_view* cache, const int32_t* block_table, int max_blocks,
+                         const int32_t* context_lens, int max_context, float scale, float* out, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  tq::QuantizeArgs ka{}, va{};
+  tq::DecodeArgs a;
+  tq_status st = step_args(book, k_new, v_new, kv_dtype, q, q_dtype, batch, n_q_heads, n_kv_heads, cache,
+                           block_table, max_blocks, context_lens, max_context, scale, out, workspace,
+                           workspace_bytes, kPrepare | kPartials | kFinish, &ka, &va, &a);
+  if (st != TQ_OK || batch == 0) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool fused;
+  st = run_step_prepare(book, k_new, v_new, kv_dtype == TQ_BF16, ka, va, a, q_dtype == TQ_BF16, s, &fused);
+  // after the fused launch, the partials kernel starts early: only the chunk
+  // holding the appended token, and the query operands, wait for it
+  if (st == TQ_OK) st = launched(launch_partials(book, a, s, fused));
   if (st == TQ_OK) st = launched(tq::launch_decode_finish(a, s));
   return st;
 }

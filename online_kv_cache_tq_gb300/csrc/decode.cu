@@ -1,5 +1,6 @@
-// Decode attention over the packed cache: query prep, split-K attention and
-// the combine/back-rotation, all in the rotated space.
+// Decode attention over the packed cache: the SIMT split-K partials kernel,
+// in the rotated space (the query preparation and the combine/back-rotation
+// are in vector_kernels.cu).
 //
 // Estimator (甲子光年 article §2 第二階段; intelliparadigm.com §2.1.2, §2.2):
 //   <q, k> ~= n_k <R q, c_K[code]> + gamma sqrt(pi/2)/m <S' R q, 2 bits - 1>
@@ -15,8 +16,6 @@
 // (m, l, acc[128]) that the combine kernel merges.
 #include <cuda_bf16.h>
 
-#include "e4m3_pieces.cuh"
-#include "gemv512.cuh"
 #include "kernels.h"
 
 namespace tq {
@@ -26,72 +25,7 @@ constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTokPerThread = kChunk / kThreads;
 
-__device__ __forceinline__ float load_elem(const void* base, long long idx, bool bf16) {
-  if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
-  return reinterpret_cast<const float*>(base)[idx];
-}
-
 __device__ __forceinline__ void record(int* error, int code) { atomicCAS(error, 0, code); }
-
-// ws_q[vec] = (R q, S' R q); with ws_bk, also the tensor-core score operand
-// of this query head: e4m3 pieces of 2 sigma_0 a_S (R q)_j / beta_j per key
-// sign plane S and of 2 sigma_1 (S' R q)_j / beta_j (sigma_0, sigma_1 powers
-// of two that bound the pieces; beta_j the bit scale of coordinate j), and the
-// sums that turn the 0/1 bit products into +-1 sign products.  512 threads:
-// thread (o, q) works on coordinate o; the copies of o split the
-// matrix-vector products and the piece planes.
-__global__ void __launch_bounds__(kGemvThreads) qprep_kernel(DecodeArgs a, bool bf16) {
-  __shared__ float q_s[kDim];
-  __shared__ float qr_s[kDim];
-  __shared__ float red_s[4 * kDim];
-  __shared__ float part_s[4];
-  const int vec = blockIdx.x;
-  const int o = threadIdx.x & 127, qq = threadIdx.x >> 7;
-  const bool lead = qq == 0;
-  if (lead) q_s[o] = load_elem(a.q, static_cast<long long>(vec) * kDim + o, bf16);
-  __syncthreads();
-  const float acc = gemv512(a.Rt, q_s, red_s);
-  if (lead) {
-    qr_s[o] = acc;
-    a.ws_q[static_cast<long long>(vec) * 2 * kDim + o] = acc;
-  }
-  __syncthreads();
-  float z = 0.f;
-  if (a.qjl_m > 0) {
-    z = gemv512(a.Spt, qr_s, red_s);
-    if (lead) a.ws_q[static_cast<long long>(vec) * 2 * kDim + kDim + o] = z;
-  }
-  if (a.ws_bk == nullptr) return;
-  const int planes = 1 << (a.k_bits - 1);
-  float amax = 0.f, asum = 0.f;
-  for (int s = 0; s < planes; ++s) {
-    amax = fmaxf(amax, fabsf(a.tables->k_walsh[s]));
-    asum += a.tables->k_walsh[s];
-  }
-  const float ib = 2.f * bit_inv_scale(o);
-  const float sig0 = piece_scale(max128(fabsf(acc) * amax * ib, part_s));
-  const float sig1 = piece_scale(max128(fabsf(z) * ib, part_s));
-  const float sum_qr = sum128(acc, part_s), sum_qs = sum128(z, part_s);
-  uint8_t* dst = a.ws_bk + static_cast<long long>(vec) * a.bk_stride;
-  const int kpos = k_position(o);
-  // plane s (s == planes: the QJL operand) by the copies qq == s % 4
-  const int items = planes + (a.qjl_m > 0 ? 1 : 0);
-  for (int s = qq; s < items; s += 4) {
-    const float y = s < planes ? a.tables->k_walsh[s] * acc * ib * sig0 : z * ib * sig1;
-    write_pieces_rows<kQPieces>(dst + s * kQPieces * 128, kpos, y);
-  }
-  if (threadIdx.x == 0) {
-    float* hdr = reinterpret_cast<float*>(dst + items * kQPieces * 128);
-    hdr[0] = sig0;
-    hdr[1] = sig1;
-    hdr[2] = 1.f / sig0;      // exact: powers of two
-    hdr[3] = 1.f / sig1;
-    hdr[4] = asum * sum_qr;   // sum_S a_S <q_rot, 1>: the -1 half of every sign
-    hdr[5] = sum_qs;
-    hdr[6] = 0.f;
-    hdr[7] = 0.f;
-  }
-}
 
 __device__ __forceinline__ int context_of(const DecodeArgs& a, int b) {
   int ctx = a.context_lens[b];
@@ -298,65 +232,7 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(DecodeArgs a) {
   }
 }
 
-// out[vec] = R^T (merged acc / merged l).  512 threads: thread (o, q) merges
-// coordinate o over the chunks c with c % 4 == q, then the copies of o add up
-// and split the back-rotation.
-__global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
-  __shared__ float o_s[kDim];
-  __shared__ float red_s[4 * kDim];
-  __shared__ float lred_s[4];
-  __shared__ float w_s[1024];
-  __shared__ float part_s[16];
-  const int vec = blockIdx.x;
-  const int b = vec / a.n_q;
-  const int t = threadIdx.x;
-  const int o = t & 127, q = t >> 7;
-  const int ctx = context_of(a, b);
-  const int n_chunks = (ctx + kChunk - 1) / kChunk;
-  const float* part = a.ws_part + static_cast<long long>(vec) * a.max_chunks * kPartStride;
-  float mx = -INFINITY;
-  for (int c = t; c < n_chunks; c += kGemvThreads) mx = fmaxf(mx, part[c * kPartStride]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  if ((t & 31) == 0) part_s[t >> 5] = mx;
-  __syncthreads();
-  mx = part_s[0];
-  for (int w = 1; w < kGemvThreads / 32; ++w) mx = fmaxf(mx, part_s[w]);
-  float l = 0.f, acc = 0.f;
-  for (int c0 = 0; c0 < n_chunks; c0 += 1024) {
-    const int cn = min(1024, n_chunks - c0);
-    __syncthreads();
-    for (int c = t; c < cn; c += kGemvThreads) {
-      const float m = part[(c0 + c) * kPartStride];
-      w_s[c] = (m == -INFINITY) ? 0.f : __expf(m - mx);
-    }
-    __syncthreads();
-    for (int c = q; c < cn; c += 4) {
-      const float w = w_s[c];
-      l = fmaf(w, part[(c0 + c) * kPartStride + 1], l);
-      acc = fmaf(w, part[(c0 + c) * kPartStride + 4 + o], acc);
-    }
-  }
-  red_s[q * kDim + o] = acc;
-  if (o == 0) lred_s[q] = l;
-  __syncthreads();
-  const float lt = (lred_s[0] + lred_s[1]) + (lred_s[2] + lred_s[3]);
-  const float at = (red_s[o] + red_s[kDim + o]) + (red_s[2 * kDim + o] + red_s[3 * kDim + o]);
-  __syncthreads();
-  if (q == 0) o_s[o] = lt > 0.f ? at / lt : 0.f;
-  __syncthreads();
-  const float out = gemv512(a.R, o_s, red_s);
-  if (q == 0) a.out[static_cast<long long>(vec) * kDim + o] = out;
-}
-
 }  // namespace
-
-cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_t stream) {
-  const int n_vec = args.batch * args.n_q;
-  if (n_vec <= 0) return cudaSuccess;
-  qprep_kernel<<<n_vec, kGemvThreads, 0, stream>>>(args, bf16);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_decode_partials(const DecodeArgs& args, cudaStream_t stream) {
   if (args.batch <= 0 || args.max_chunks <= 0) return cudaSuccess;
@@ -371,11 +247,5 @@ cudaError_t launch_decode_partials(const DecodeArgs& args, cudaStream_t stream) 
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream) {
-  const int n_vec = args.batch * args.n_q;
-  if (n_vec <= 0) return cudaSuccess;
-  combine_kernel<<<n_vec, kGemvThreads, 0, stream>>>(args);
-  return cudaGetLastError();
-}
 
 }  // namespace tq

@@ -387,6 +387,9 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       __syncwarp();                             // blk_ok_s before the arrival the builders acquire
       if (ln == 0) ptx::mbar_arrive_expect_tx(&bar_in, bytes);
       __syncwarp();
+      // the chunk holding position ctx - 1 may hold the token a decode step's
+      // append (the grid this one may overlap) is writing: wait for that grid
+      if (start + n_local == ctx) asm volatile("griddepcontrol.wait;" ::: "memory");
       if (valid) {
         const long long r0 = (phys * a.n_kv + kvh) * bs;    // first row of this block
         const int tl0 = ln * bs;
@@ -459,6 +462,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     // of a row at c ^ (n % 8)
     float inv_sig[G];                             // 1 / sigma of this thread's accumulator columns
     float ones[G];                                // the -1 half of the +-1 products of those columns
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the query operands come from the previous grid
     {
       const int nk = L.pk + L.pq;
       const int per_head = nk * kQPieces * 8;     // 16-byte chunks per head
@@ -722,23 +726,31 @@ bool tc_decode_supported(const DecodeArgs& a, bool walsh_ok) {
 }
 
 template <int G>
-cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, bool early) {
   const TcLayout l = tc_layout(G, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size);
   cudaError_t err = cudaFuncSetAttribute(attention_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          l.smem_bytes);
   if (err != cudaSuccess) return err;
-  dim3 grid(a.max_chunks, a.n_kv, a.batch);
-  attention_tc_kernel<G><<<grid, kThreads, l.smem_bytes, stream>>>(a, l);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.max_chunks, a.n_kv, a.batch);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = l.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = early ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attention_tc_kernel<G>, a, l);
 }
 
-cudaError_t launch_decode_partials_tc(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_decode_partials_tc(const DecodeArgs& a, cudaStream_t stream, bool early) {
   if (a.batch <= 0 || a.max_chunks <= 0) return cudaSuccess;
   switch (a.group) {
-    case 1: return launch_g<1>(a, stream);
-    case 2: return launch_g<2>(a, stream);
-    case 4: return launch_g<4>(a, stream);
-    case 8: return launch_g<8>(a, stream);
+    case 1: return launch_g<1>(a, stream, early);
+    case 2: return launch_g<2>(a, stream, early);
+    case 4: return launch_g<4>(a, stream, early);
+    case 8: return launch_g<8>(a, stream, early);
     default: return cudaErrorInvalidValue;
   }
 }

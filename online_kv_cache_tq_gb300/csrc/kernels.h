@@ -17,7 +17,10 @@ struct QuantizeArgs {
   int n_tokens;
   int n_kv;
   bool transposed;        // codes field stored token-transposed (values)
-  const int64_t* slots;   // [n_tokens]
+  const int64_t* slots;   // [n_tokens]; null: a decode step, slot derived below
+  const int32_t* step_block_table;   // decode step: [n_tokens][step_max_blocks] (null: identity)
+  const int32_t* step_context_lens;  // decode step: token b is position context_lens[b] - 1 of sequence b
+  int step_max_blocks;
   uint8_t* codes;         // field base, bits * 16 bytes per item
   uint8_t* qjl;           // field base, 16 bytes per item (null: no QJL)
   float* norm;
@@ -31,6 +34,22 @@ struct QuantizeArgs {
   const float* Spt;       // [128][128], Spt[j][k] = S'[k][j]
   int* error;
 };
+
+// Cache slot of token `token` of an append: slot_mapping[token], or for a
+// decode step (one token per sequence, slots == null) the slot of position
+// context_lens[token] - 1 of that sequence under its block table (-1, i.e.
+// skipped, for an empty context).
+__device__ __forceinline__ long long slot_of(const QuantizeArgs& a, int token) {
+  if (a.slots != nullptr) return a.slots[token];
+  const int pos = a.step_context_lens[token] - 1;
+  if (pos < 0) return -1;
+  const int lblk = pos / a.block_size;
+  if (lblk >= a.step_max_blocks) return static_cast<long long>(a.num_blocks) * a.block_size;   // out of range
+  const long long phys = a.step_block_table ? a.step_block_table[static_cast<long long>(token) * a.step_max_blocks + lblk]
+                                            : static_cast<long long>(token) * a.step_max_blocks + lblk;
+  if (phys < 0) return static_cast<long long>(a.num_blocks) * a.block_size;
+  return phys * a.block_size + pos % a.block_size;
+}
 
 cudaError_t launch_quantize_simt(const QuantizeArgs& args, bool bf16, int num_sms, cudaStream_t stream);
 
@@ -98,13 +117,22 @@ __host__ __device__ constexpr int bk_head_bytes(int k_mse_bits, bool qjl) {
 constexpr int kPartStride = 132;  // m, l, 2 pad, acc[128]
 
 cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_t stream);
+
+// Quantize-append of one new key and value per sequence (ka and va share the
+// shape, at most kSmallQuantize vectors each) and the query preparation of
+// the same decode step, in one launch.
+cudaError_t launch_step_prep(const QuantizeArgs& ka, const QuantizeArgs& va, bool kv_bf16, const DecodeArgs& da,
+                             bool q_bf16, cudaStream_t stream);
 cudaError_t launch_decode_partials(const DecodeArgs& args, cudaStream_t stream);
 
 // Tensor-core partials (fp8 sign planes, decode_tc.cu) for the shapes it
 // supports: G in {1, 2, 4, 8}, tensor-memory columns within 512, and
 // odd-symmetric codebooks; the SIMT kernel serves every other shape.
 bool tc_decode_supported(const DecodeArgs& args, bool walsh_ok);
-cudaError_t launch_decode_partials_tc(const DecodeArgs& args, cudaStream_t stream);
+// early: launched as a programmatic dependent of the decode step's fused
+// append + query preparation; the kernel waits for that grid only before it
+// reads the query operands and the chunk that holds the appended token.
+cudaError_t launch_decode_partials_tc(const DecodeArgs& args, cudaStream_t stream, bool early);
 cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream);
 
 }  // namespace tq

@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantizeArgs a,
       if (gv >= a.n_vec) break;
       const int token = gv / a.n_kv;
       const int head = gv - token * a.n_kv;
-      const long long slot = a.slots[token];
+      const long long slot = slot_of(a, token);
       long long row = -1;
       if (slot >= 0 && slot < cache_rows) {
         const long long blk = slot / a.block_size;
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantizeArgs a,
         if (gv >= a.n_vec) break;
         const int token = gv / a.n_kv;
         const int head = gv - token * a.n_kv;
-        const long long slot = a.slots[token];
+        const long long slot = slot_of(a, token);
         if (slot < 0 || slot >= cache_rows) continue;
         const long long blk = slot / a.block_size;
         const long long row = (blk * a.n_kv + head) * a.block_size + (slot - blk * a.block_size);

@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long dst = -1;
       long long slot = -1;
       if (token < a.n_tokens) {
-        slot = a.slots[token];
+        slot = slot_of(a, token);
         if (slot >= 0 && slot < cache_rows) {
           const long long blk = slot / a.block_size;
           dst = (blk * a.n_kv + head) * a.block_size + (slot - blk * a.block_size);

@@ -1,0 +1,269 @@
+// Per-vector kernels of a decode step, one CTA of 512 threads per head
+// vector: quantize-append of the step's new keys and values, the query
+// preparation of decode attention (a fused launch runs both for a step), and
+// the merge of the split-K partials with the back-rotation.
+//
+// Same arithmetic as the tile quantizers (甲子光年 article §2 第一階段 /
+// 第二階段) and the decode estimator (§2 第二階段: <q, k> ~= n <R q, c[code]>
+// + gamma sqrt(pi/2)/m <S' R q, 2 bits - 1>; out = R^T acc / l, seo-farm page
+// §4).  R^T, S'^T and R are read from global memory (L2-resident after first
+// use), so a launch costs a few microseconds instead of staging 128 KB of
+// constants per CTA.
+#include <cuda_bf16.h>
+
+#include "e4m3_pieces.cuh"
+#include "gemv512.cuh"
+#include "kernels.h"
+
+namespace tq {
+namespace {
+
+__device__ __forceinline__ float load_elem(const void* base, long long idx, bool bf16) {
+  if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
+  return reinterpret_cast<const float*>(base)[idx];
+}
+
+
+// Quantize head vector v of `a` (n = ||x||, y = R x / n, nearest level, and
+// for keys the rotated residual r' = R x - n c[code], its norm and the signs
+// of S' r').  Thread (o, q) of the 512 works on rotated coordinate o; the
+// four copies of o split the matrix-vector products and threads q == 0
+// (warps 0-3) write the results.
+__device__ __forceinline__ void quantize_vector(const QuantizeArgs& a, int v, bool bf16) {
+  __shared__ float x_s[kDim];
+  __shared__ float r_s[kDim];
+  __shared__ float red_s[4 * kDim];
+  __shared__ float part_s[4];
+  const int o = threadIdx.x & 127;
+  const bool lead = threadIdx.x < 128;
+  const int lane = o & 31;
+  const int warp = o >> 5;
+  const int token = v / a.n_kv;
+  const int head = v - token * a.n_kv;
+
+  const long long idx = static_cast<long long>(v) * kDim + o;
+  const float x = bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.x)[idx])
+                       : reinterpret_cast<const float*>(a.x)[idx];
+  if (lead) x_s[o] = x;
+  const float n = sqrtf(sum128(x * x, part_s));          // its barriers also publish x_s
+  const float yv = gemv512(a.Rt, x_s, red_s);           // (R x)_o
+  const float y = n > 0.f ? yv / n : 0.f;
+  int code = 0;
+  for (int t = 0; t + 1 < (1 << a.bits); ++t) code += (y > a.bounds[t]) ? 1 : 0;
+
+  const long long cache_rows = static_cast<long long>(a.num_blocks) * a.block_size;
+  const long long slot = slot_of(a, token);
+  const bool ok = slot >= 0 && slot < cache_rows;
+  if (slot >= cache_rows && threadIdx.x == 0) atomicCAS(a.error, 0, kErrSlot);
+  const long long blk = ok ? slot / a.block_size : 0;
+  const int off = ok ? static_cast<int>(slot - blk * a.block_size) : 0;
+  const long long row = (blk * a.n_kv + head) * a.block_size + off;
+
+  if (a.transposed) {
+    if (ok && lead) {
+      unsigned* words = reinterpret_cast<unsigned*>(a.codes);
+      const unsigned mask = 1u << (off & 31);
+      for (int p = 0; p < a.bits; ++p) {
+        unsigned* w = words + transposed_word(blk, head, a.n_kv, a.bits, p, o, a.block_size, off);
+        if ((code >> p) & 1) atomicOr(w, mask); else atomicAnd(w, ~mask);
+      }
+    }
+  } else {
+    for (int p = 0; p < a.bits; ++p) {
+      const unsigned word = __ballot_sync(0xffffffffu, (code >> p) & 1);
+      if (ok && lead && lane == 0) reinterpret_cast<unsigned*>(a.codes + row * (a.bits * 16))[p * 4 + warp] = word;
+    }
+  }
+  if (ok && threadIdx.x == 0) a.norm[row] = n;
+
+  if (a.qjl != nullptr) {
+    const float r = fmaf(-n, a.levels[code], yv);
+    if (lead) r_s[o] = r;
+    const float gamma = sqrtf(sum128(r * r, part_s));    // its barriers also publish r_s
+    const float z = gemv512(a.Spt, r_s, red_s);
+    const unsigned word = __ballot_sync(0xffffffffu, z > 0.f);
+    if (ok && lead && lane == 0) reinterpret_cast<unsigned*>(a.qjl + row * 16)[warp] = word;
+    if (ok && threadIdx.x == 0) a.rnorm[row] = gamma;
+  }
+}
+
+
+// Query head vec: ws_q[vec] = (R q, S' R q); with ws_bk, also the tensor-core score operand
+// of this query head: e4m3 pieces of 2 sigma_0 a_S (R q)_j / beta_j per key
+// sign plane S and of 2 sigma_1 (S' R q)_j / beta_j (sigma_0, sigma_1 powers
+// of two that bound the pieces; beta_j the bit scale of coordinate j), and the
+// sums that turn the 0/1 bit products into +-1 sign products.  512 threads:
+// thread (o, q) works on coordinate o; the copies of o split the
+// matrix-vector products and the piece planes.
+__device__ __forceinline__ void prepare_query(const DecodeArgs& a, int vec, bool bf16) {
+  __shared__ float q_s[kDim];
+  __shared__ float qr_s[kDim];
+  __shared__ float red_s[4 * kDim];
+  __shared__ float part_s[4];
+  const int o = threadIdx.x & 127, qq = threadIdx.x >> 7;
+  const bool lead = qq == 0;
+  if (lead) q_s[o] = load_elem(a.q, static_cast<long long>(vec) * kDim + o, bf16);
+  __syncthreads();
+  const float acc = gemv512(a.Rt, q_s, red_s);
+  if (lead) {
+    qr_s[o] = acc;
+    a.ws_q[static_cast<long long>(vec) * 2 * kDim + o] = acc;
+  }
+  __syncthreads();
+  float z = 0.f;
+  if (a.qjl_m > 0) {
+    z = gemv512(a.Spt, qr_s, red_s);
+    if (lead) a.ws_q[static_cast<long long>(vec) * 2 * kDim + kDim + o] = z;
+  }
+  if (a.ws_bk == nullptr) return;
+  const int planes = 1 << (a.k_bits - 1);
+  float amax = 0.f, asum = 0.f;
+  for (int s = 0; s < planes; ++s) {
+    amax = fmaxf(amax, fabsf(a.tables->k_walsh[s]));
+    asum += a.tables->k_walsh[s];
+  }
+  const float ib = 2.f * bit_inv_scale(o);
+  const float sig0 = piece_scale(max128(fabsf(acc) * amax * ib, part_s));
+  const float sig1 = piece_scale(max128(fabsf(z) * ib, part_s));
+  const float sum_qr = sum128(acc, part_s), sum_qs = sum128(z, part_s);
+  uint8_t* dst = a.ws_bk + static_cast<long long>(vec) * a.bk_stride;
+  const int kpos = k_position(o);
+  // plane s (s == planes: the QJL operand) by the copies qq == s % 4
+  const int items = planes + (a.qjl_m > 0 ? 1 : 0);
+  for (int s = qq; s < items; s += 4) {
+    const float y = s < planes ? a.tables->k_walsh[s] * acc * ib * sig0 : z * ib * sig1;
+    write_pieces_rows<kQPieces>(dst + s * kQPieces * 128, kpos, y);
+  }
+  if (threadIdx.x == 0) {
+    float* hdr = reinterpret_cast<float*>(dst + items * kQPieces * 128);
+    hdr[0] = sig0;
+    hdr[1] = sig1;
+    hdr[2] = 1.f / sig0;      // exact: powers of two
+    hdr[3] = 1.f / sig1;
+    hdr[4] = asum * sum_qr;   // sum_S a_S <q_rot, 1>: the -1 half of every sign
+    hdr[5] = sum_qs;
+    hdr[6] = 0.f;
+    hdr[7] = 0.f;
+  }
+}
+
+__device__ __forceinline__ int context_of(const DecodeArgs& a, int b) {
+  int ctx = a.context_lens[b];
+  const int cap = min(a.max_context, a.max_blocks * a.block_size);
+  if (ctx < 0 || ctx > cap) {
+    atomicCAS(a.error, 0, kErrContext);
+    ctx = ctx < 0 ? 0 : cap;
+  }
+  return ctx;
+}
+
+// out[vec] = R^T (merged acc / merged l).  512 threads: thread (o, q) merges
+// coordinate o over the chunks c with c % 4 == q, then the copies of o add up
+// and split the back-rotation.
+__global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
+  __shared__ float o_s[kDim];
+  __shared__ float red_s[4 * kDim];
+  __shared__ float lred_s[4];
+  __shared__ float w_s[1024];
+  __shared__ float part_s[16];
+  const int vec = blockIdx.x;
+  const int b = vec / a.n_q;
+  const int t = threadIdx.x;
+  const int o = t & 127, q = t >> 7;
+  const int ctx = context_of(a, b);
+  const int n_chunks = (ctx + kChunk - 1) / kChunk;
+  const float* part = a.ws_part + static_cast<long long>(vec) * a.max_chunks * kPartStride;
+  float mx = -INFINITY;
+  for (int c = t; c < n_chunks; c += kGemvThreads) mx = fmaxf(mx, part[c * kPartStride]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if ((t & 31) == 0) part_s[t >> 5] = mx;
+  __syncthreads();
+  mx = part_s[0];
+  for (int w = 1; w < kGemvThreads / 32; ++w) mx = fmaxf(mx, part_s[w]);
+  float l = 0.f, acc = 0.f;
+  for (int c0 = 0; c0 < n_chunks; c0 += 1024) {
+    const int cn = min(1024, n_chunks - c0);
+    __syncthreads();
+    for (int c = t; c < cn; c += kGemvThreads) {
+      const float m = part[(c0 + c) * kPartStride];
+      w_s[c] = (m == -INFINITY) ? 0.f : __expf(m - mx);
+    }
+    __syncthreads();
+    for (int c = q; c < cn; c += 4) {
+      const float w = w_s[c];
+      l = fmaf(w, part[(c0 + c) * kPartStride + 1], l);
+      acc = fmaf(w, part[(c0 + c) * kPartStride + 4 + o], acc);
+    }
+  }
+  red_s[q * kDim + o] = acc;
+  if (o == 0) lred_s[q] = l;
+  __syncthreads();
+  const float lt = (lred_s[0] + lred_s[1]) + (lred_s[2] + lred_s[3]);
+  const float at = (red_s[o] + red_s[kDim + o]) + (red_s[2 * kDim + o] + red_s[3 * kDim + o]);
+  __syncthreads();
+  if (q == 0) o_s[o] = lt > 0.f ? at / lt : 0.f;
+  __syncthreads();
+  const float out = gemv512(a.R, o_s, red_s);
+  if (q == 0) a.out[static_cast<long long>(vec) * kDim + o] = out;
+}
+
+// Blocks [0, first.n_vec) quantize `first`, the rest `second` (K and V of one
+// append in a single launch).
+__global__ void __launch_bounds__(kGemvThreads) quantize_small_kernel(QuantizeArgs first, QuantizeArgs second,
+                                                                      bool bf16) {
+  const bool in_first = static_cast<int>(blockIdx.x) < first.n_vec;
+  quantize_vector(in_first ? first : second, in_first ? blockIdx.x : blockIdx.x - first.n_vec, bf16);
+}
+
+__global__ void __launch_bounds__(kGemvThreads) qprep_kernel(DecodeArgs a, bool bf16) {
+  prepare_query(a, blockIdx.x, bf16);
+}
+
+// One decode step's per-vector work: blocks [0, n_k) quantize the new keys,
+// [n_k, 2 n_k) the new values, the rest prepare the queries.  The decode
+// partials kernel that follows may start as soon as these blocks run (it
+// waits for their results where it reads them).
+__global__ void __launch_bounds__(kGemvThreads) step_prep_kernel(QuantizeArgs ka, QuantizeArgs va, bool kv_bf16,
+                                                                 DecodeArgs da, bool q_bf16) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int blk = blockIdx.x;
+  if (blk < ka.n_vec) quantize_vector(ka, blk, kv_bf16);
+  else if (blk < 2 * ka.n_vec) quantize_vector(va, blk - ka.n_vec, kv_bf16);
+  else prepare_query(da, blk - 2 * ka.n_vec, q_bf16);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_small(const QuantizeArgs* first, const QuantizeArgs* second, bool bf16,
+                                  cudaStream_t stream) {
+  const int n = (first ? first->n_vec : 0) + (second ? second->n_vec : 0);
+  if (n <= 0) return cudaSuccess;
+  QuantizeArgs none{};
+  quantize_small_kernel<<<n, kGemvThreads, 0, stream>>>(first ? *first : none, second ? *second : none, bf16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_t stream) {
+  const int n_vec = args.batch * args.n_q;
+  if (n_vec <= 0) return cudaSuccess;
+  qprep_kernel<<<n_vec, kGemvThreads, 0, stream>>>(args, bf16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream) {
+  const int n_vec = args.batch * args.n_q;
+  if (n_vec <= 0) return cudaSuccess;
+  combine_kernel<<<n_vec, kGemvThreads, 0, stream>>>(args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_step_prep(const QuantizeArgs& ka, const QuantizeArgs& va, bool kv_bf16, const DecodeArgs& da,
+                             bool q_bf16, cudaStream_t stream) {
+  const int n = 2 * ka.n_vec + da.batch * da.n_q;
+  if (n <= 0) return cudaSuccess;
+  step_prep_kernel<<<n, kGemvThreads, 0, stream>>>(ka, va, kv_bf16, da, q_bf16);
+  return cudaGetLastError();
+}
+
+}  // namespace tq

@@ -170,3 +170,51 @@ def test_long_context_full_size_sampled():
 
 def test_llama3_70b_paged_full_size_sampled():
     _full_size("c5_llama3_70b_paged", 3, 23)
+
+
+@pytest.mark.parametrize("batch,n_kv,group", [(5, 2, 4), (130, 8, 1)])
+def test_decode_step_equals_append_then_attention(batch, n_kv, group):
+    # one call (fused append + query preparation and an early-started partials
+    # kernel when batch * n_kv <= 1024, the tile quantizer otherwise) against
+    # the two calls it stands for: identical caches and outputs, and the output
+    # within tolerance of the oracle; sequence 0 has an empty context
+    cfg = dict(n_kv=n_kv, block_size=64, dtype="bf16", seed=21, log_uniform=(0.1, 10.0), outliers=3,
+               outlier_scale=30.0)
+    book, ref = books(3, 3, 128, seed=6)
+    rng = np.random.default_rng(batch)
+    ctx = rng.integers(1, 1500, size=batch).astype(np.int32)
+    ctx[0] = 0
+    table, _ = W.block_layout(ctx, 64, True, seed=batch)
+    g = generator(batch)
+    cache = fill_cache(book, cfg, np.maximum(ctx - 1, 0), table, g, chunk_tokens=1000)
+    n_q = n_kv * group
+    k_new = W.gaussian_tokens(batch, W.channel_scales(3, n_kv, (0.1, 10.0), 3, 30.0), torch.bfloat16, "cuda", g)
+    v_new = W.gaussian_tokens(batch, W.channel_scales(4, n_kv, (0.1, 10.0), 3, 30.0), torch.bfloat16, "cuda", g)
+    q = W.queries(batch, n_q, torch.bfloat16, "cuda", g)
+    slots = torch.as_tensor(np.array([W.slots_for(table[b], [int(ctx[b]) - 1], 64)[0] if ctx[b] > 0 else -1
+                                      for b in range(batch)]), device="cuda")
+    table_d = torch.as_tensor(table, device="cuda")
+    ctx_d = torch.as_tensor(ctx, device="cuda")
+    max_ctx = int(ctx.max())
+    ws, nbytes = C.allocate_workspace(book, batch, n_q, max_ctx)
+    outs, caches = [], []
+    for fused in (False, True):
+        c = {name: t.clone() for name, t in cache.items()}
+        view = C.cache_view(book, c)
+        out = torch.full((batch, n_q, 128), float("nan"), device="cuda", dtype=torch.float32)
+        if fused:
+            B.tq_decode_step(book, k_new, v_new, B.TQ_BF16, q, B.TQ_BF16, batch, n_q, n_kv, view, table_d,
+                             table.shape[1], ctx_d, max_ctx, 0.0, out, ws, nbytes)
+        else:
+            B.tq_quantize_append(book, k_new, v_new, B.TQ_BF16, batch, n_kv, slots, view)
+            B.tq_decode_attention(book, q, B.TQ_BF16, batch, n_q, n_kv, view, table_d, table.shape[1], ctx_d,
+                                  max_ctx, 0.0, out, ws, nbytes)
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy())
+        caches.append({name: t.cpu() for name, t in c.items()})
+    for name in caches[0]:
+        assert torch.equal(caches[0][name], caches[1][name]), name
+    assert np.array_equal(outs[0], outs[1])
+    pairs = [(0, 0)] + attn_pairs(batch, n_q, 12, seed=batch)
+    check_decode(outs[1], host_cache(caches[1]), q, table, ctx, ref, pairs)
+    assert B.tq_get_last_device_error(book) == 0
