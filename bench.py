@@ -223,7 +223,7 @@ class DecodeWorkload:
         self.ws, self.ws_bytes = C.allocate_workspace(self.book, self.batch, self.n_q, self.max_ctx)
         torch.cuda.synchronize()
         # tq_decode_step: append + query preparation (one launch up to 1024 head vectors, else
-        # quantize K, quantize V, prepare), partials, finish
+        # quantize K, quantize V, prepare), partials, merge
         self.launches_per_step = (1 if self.batch * self.n_kv <= 1024 else 3) + 2
 
     def step(self, i):

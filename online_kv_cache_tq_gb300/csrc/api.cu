@@ -502,6 +502,15 @@ cudaError_t launch_partials(const tq_codebook* book, const tq::DecodeArgs& a, cu
   return tq::launch_decode_partials(a, s);
 }
 
+// Partials, then the merge into `out`; after the tensor-core kernel the merge
+// is a programmatic dependent launch (it starts as the last partials CTAs end).
+cudaError_t launch_partials_and_merge(const tq_codebook* book, const tq::DecodeArgs& a, cudaStream_t s,
+                                      bool early = false) {
+  const bool tc = tq::tc_decode_supported(a, book->walsh_ok);
+  const cudaError_t err = tc ? tq::launch_decode_partials_tc(a, s, early) : tq::launch_decode_partials(a, s);
+  return err == cudaSuccess ? tq::launch_decode_finish(a, s, tc) : err;
+}
+
 }  // namespace
 
 extern "C" {
@@ -518,8 +527,7 @@ tq_status tq_decode_attention(const tq_codebook* book, const void* q, tq_dtype d
   if (st != TQ_OK || batch == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = launched(tq::launch_decode_prepare(a, dtype == TQ_BF16, s));
-  if (st == TQ_OK) st = launched(launch_partials(book, a, s));
-  if (st == TQ_OK) st = launched(tq::launch_decode_finish(a, s));
+  if (st == TQ_OK) st = launched(launch_partials_and_merge(book, a, s));
   return st;
 }
 
@@ -597,8 +605,7 @@ tq_status tq_decode_step(const tq_codebook* book, const void* k_new, const void*
   st = run_step_prepare(book, k_new, v_new, kv_dtype == TQ_BF16, ka, va, a, q_dtype == TQ_BF16, s, &fused);
   // after the fused launch, the partials kernel starts early: only the chunk
   // holding the appended token, and the query operands, wait for it
-  if (st == TQ_OK) st = launched(launch_partials(book, a, s, fused));
-  if (st == TQ_OK) st = launched(tq::launch_decode_finish(a, s));
+  if (st == TQ_OK) st = launched(launch_partials_and_merge(book, a, s, fused));
   return st;
 }
 

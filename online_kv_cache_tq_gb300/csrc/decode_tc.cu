@@ -289,7 +289,10 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   const int b = blockIdx.z;
   const int ctx = context_of(a, b);
   const int start = chunk * kChunk;
-  if (start >= ctx) return;
+  if (start >= ctx) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    return;
+  }
   const int n_local = min(kChunk, ctx - start);
   const int n_tiles = (n_local + kTile - 1) / kTile;
   const int bs = a.block_size;                        // a power of two that divides kChunk
@@ -697,8 +700,12 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         }
       }
     }
+
   }
 
+  // the merge kernel that follows may launch once every CTA got here (it
+  // waits for this grid to finish before it reads the partials)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   ptx::tc_fence_before();
   __syncthreads();
   if (!builder) {

@@ -133,6 +133,8 @@ bool tc_decode_supported(const DecodeArgs& args, bool walsh_ok);
 // append + query preparation; the kernel waits for that grid only before it
 // reads the query operands and the chunk that holds the appended token.
 cudaError_t launch_decode_partials_tc(const DecodeArgs& args, cudaStream_t stream, bool early);
-cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream);
+// early: launched as a programmatic dependent of the tensor-core partials
+// kernel (the merge waits for it before reading the partials).
+cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream, bool early = false);
 
 }  // namespace tq

@@ -161,6 +161,7 @@ __device__ __forceinline__ int context_of(const DecodeArgs& a, int b) {
 // coordinate o over the chunks c with c % 4 == q, then the copies of o add up
 // and split the back-rotation.
 __global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the partials (no-op unless launched early)
   __shared__ float o_s[kDim];
   __shared__ float red_s[4 * kDim];
   __shared__ float lred_s[4];
@@ -251,11 +252,19 @@ cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream) {
+cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream, bool early) {
   const int n_vec = args.batch * args.n_q;
   if (n_vec <= 0) return cudaSuccess;
-  combine_kernel<<<n_vec, kGemvThreads, 0, stream>>>(args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_vec);
+  cfg.blockDim = dim3(kGemvThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = early ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, args);
 }
 
 cudaError_t launch_step_prep(const QuantizeArgs& ka, const QuantizeArgs& va, bool kv_bf16, const DecodeArgs& da,
