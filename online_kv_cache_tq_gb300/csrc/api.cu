@@ -489,6 +489,7 @@ tq_status decode_args(const tq_codebook* book, int stages, const void* q, tq_dty
   a->Spt = book->d_Spt;
   a->tables = book->d_tables;
   a->error = book->d_error;
+  a->num_sms = book->num_sms;
   return TQ_OK;
 }
 

@@ -56,7 +56,16 @@ constexpr int kThreads = kBuilders + 32;     // warp 8: copies and MMA issue
 constexpr int kVPieces = 4;                 // e4m3 pieces of a softmax weight
 
 __host__ __device__ constexpr int round16(int x) { return (x + 15) / 16 * 16; }
-__host__ __device__ constexpr int score_cols(int g) { return round16(kQPieces * g); }   // per group
+// Score accumulator columns: the query heads of a group are split into two
+// halves (threads t < 128 read the first, t >= 128 the second); head h's
+// pieces sit at column score_half(g) * (h / half_heads(g)) + kQPieces * (h %
+// half_heads(g)), so each thread reads 16-column groups of its own heads only.
+__host__ __device__ constexpr int half_heads(int g) { return g >= 2 ? g / 2 : 1; }
+__host__ __device__ constexpr int score_half(int g) { return round16(kQPieces * half_heads(g)); }
+__host__ __device__ constexpr int score_cols(int g) { return g >= 2 ? 2 * score_half(g) : score_half(g); }
+__host__ __device__ constexpr int score_row(int g, int h, int piece) {
+  return score_half(g) * (h / half_heads(g)) + kQPieces * (h % half_heads(g)) + piece;
+}
 __host__ __device__ constexpr int value_cols(int g) { return round16(kVPieces * g); }   // per value plane
 
 // Byte offset of (row n, K position k) in a K-major operand stored with the
@@ -281,49 +290,69 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
 
 }  // namespace
 
-template <int G>
-__global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a, TcLayout L) {
-  constexpr int N1 = score_cols(G), NO = value_cols(G);
-  const int chunk = blockIdx.x;
-  const int kvh = blockIdx.y;
-  const int b = blockIdx.z;
-  const int ctx = context_of(a, b);
-  const int start = chunk * kChunk;
-  if (start >= ctx) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    return;
+// One work item: (sequence b, KV head kvh, chunk) in the order of the item
+// index ((b * n_kv) + kvh) * max_chunks + chunk.  Items whose chunk starts at
+// or beyond the sequence's context are empty and skipped by every role.
+struct Item {
+  int b, kvh, chunk, ctx, start, n_local, n_tiles, n_blk;
+};
+
+__device__ __forceinline__ bool next_item(const DecodeArgs& a, int& it, int last, int bs_shift, Item& x) {
+  for (; it < last; ++it) {
+    const int chunk = it % a.max_chunks, g = it / a.max_chunks;
+    const int b = g / a.n_kv;
+    const int ctx = context_of(a, b);
+    if (chunk * kChunk >= ctx) continue;
+    x.b = b;
+    x.kvh = g - b * a.n_kv;
+    x.chunk = chunk;
+    x.ctx = ctx;
+    x.start = chunk * kChunk;
+    x.n_local = min(kChunk, ctx - x.start);
+    x.n_tiles = (x.n_local + kTile - 1) / kTile;
+    x.n_blk = (x.n_local + (1 << bs_shift) - 1) >> bs_shift;
+    ++it;
+    return true;
   }
-  const int n_local = min(kChunk, ctx - start);
-  const int n_tiles = (n_local + kTile - 1) / kTile;
+  return false;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a, TcLayout L, int items_per_cta) {
+  constexpr int N1 = score_cols(G), NO = value_cols(G);
+  const int total = a.batch * a.n_kv * a.max_chunks;
+  const int first = blockIdx.x * items_per_cta;
+  const int last = min(total, first + items_per_cta);
   const int bs = a.block_size;                        // a power of two that divides kChunk
   const int bs_shift = 31 - __clz(bs);
-  const int n_blk = (n_local + bs - 1) >> bs_shift;   // blocks of this chunk
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* b_mse = smem + L.off_bmse;
   uint8_t* b_qjl = smem + L.off_bqjl;
   uint8_t* b_v = smem + L.off_bv;
-  float* s0 = reinterpret_cast<float*>(smem + L.off_s0);           // [G][kChunk] mse part, then the weights
-  float* s1 = reinterpret_cast<float*>(smem + L.off_s1);           // [G][kChunk] qjl part, then output halves
+  float* s0 = reinterpret_cast<float*>(smem + L.off_s0);           // [G][kChunk] scores, then weights
+  float* s1 = reinterpret_cast<float*>(smem + L.off_s1);           // output halves
   uint8_t* kc_s = smem + L.off_kc;                                  // [kChunk][kbytes]
   uint8_t* kq_s = smem + L.off_kq;                                  // [kChunk][16]
   float* kn_s = reinterpret_cast<float*>(smem + L.off_kn);
   float* kr_s = reinterpret_cast<float*>(smem + L.off_kr);
   float* vn_s = reinterpret_cast<float*>(smem + L.off_vn);
   uint32_t* vc_s = reinterpret_cast<uint32_t*>(smem + L.off_vc);   // [blk][plane][dim][bs/32]
-  // bar_in: the chunk's fields landed; kfull / vfull: the builders stored a
-  // slot's planes (256 arrivals); kdone / vdone: the slot's MMAs completed
-  // (commit); sfree: the builders read the score accumulators (256 arrivals);
-  // bar_d: drain after a failed wait
-  __shared__ __align__(8) uint64_t bar_in, kfull[2], kdone, sfree, vfull[2], vdone[2], bar_d;
+  // kin / vin: an item's key / value fields landed (one phase per item);
+  // kfree / vfree: the builders are done with the key / value fields of an
+  // item (256 arrivals); kfull / vfull: the builders stored a slot's planes
+  // (256 arrivals); kdone / vdone: the slot's MMAs completed (commit); sfree:
+  // the builders read the score accumulators (256 arrivals); bar_d: drain
+  __shared__ __align__(8) uint64_t kin, vin, kfree, vfree, kfull[2], kdone, sfree, vfull[2], vdone[2], bar_d;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
   __shared__ float red_s[(kBuilders / 32) * (2 * G + 1)];   // block_reduce of up to 2 G + 1 values
   __shared__ float stat_s[2][G];                // chunk max, chunk sum per head
-  __shared__ int blk_ok_s[kChunk / 32];         // physical block of each block slot is valid
+  __shared__ int blk_ok_s[2][kChunk / 32];      // per item parity: physical block of each block slot is valid
   __shared__ float sv_s;                        // piece scale of the softmax weights
   __shared__ float wsum_s[G];                   // sum over the chunk of e n_v per head
+  __shared__ float cst_s[4][G];                 // per head: 1/sigma_mse, 1/sigma_qjl, ones_mse, ones_qjl
   __shared__ float vw_s[8];                     // odd Walsh coefficients of the value codebook
 
   const int t = threadIdx.x;
@@ -333,18 +362,19 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   const int w0 = 2 * half;                      // this thread's words of every sign plane: w0, w0 + 1
   const uint32_t row_addr = static_cast<uint32_t>(((t >> 5) & 3) * 32) << 16;
   const bool qjl = a.k_qjl != nullptr;
-  const int qbase = b * a.n_q + kvh * G;
   volatile int* abort = &abort_s;
   const int n_pairs = (L.pv + 1) / 2;
-  const int n_units = n_tiles * n_pairs;
 
-  // zero the B operands (padding rows must be 0)
+  // zero the B operands once (their padding rows stay 0)
   for (int i = t; i < L.off_s0 / 16; i += kThreads) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
   ptx::fence_async_shared();                    // the MMAs read these bytes through the async proxy
   if (t < 8) vw_s[t] = a.tables->v_walsh[t];
   if (t == kBuilders) {
     abort_s = 0;
-    ptx::mbar_init(&bar_in, 1);
+    ptx::mbar_init(&kin, 1);
+    ptx::mbar_init(&vin, 1);
+    ptx::mbar_init(&kfree, kBuilders);
+    ptx::mbar_init(&vfree, kBuilders);
     ptx::mbar_init(&kfull[0], kBuilders);
     ptx::mbar_init(&kfull[1], kBuilders);
     ptx::mbar_init(&kdone, 1);
@@ -364,48 +394,56 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   bool ok = true;
+  int drain_k = 0, drain_v = 0;                 // control warp: copy rounds to drain after a failure
 
   if (!builder) {
-    // =================== control warp: copies, then every MMA ===================
+    // =================== control warp: copies one item ahead, every MMA ===================
     const int ln = t - kBuilders;
-    {
-      // lane k copies block k of the chunk
+    // lane k copies block k of an item: the key fields (keys = true) or the value fields
+    int kin_issued = 0, vin_issued = 0;         // copy rounds issued on kin / vin (one phase each)
+    auto copy_fields = [&](const Item& x, int seq, bool keys) {
+      ++(keys ? kin_issued : vin_issued);
       bool valid = false;
       long long phys = 0;
       int rows = 0;
       uint32_t bytes = 0;
-      if (ln < n_blk) {
-        const int lblk = (start >> bs_shift) + ln;
-        phys = a.block_table ? a.block_table[static_cast<long long>(b) * a.max_blocks + lblk]
-                             : static_cast<long long>(b) * a.max_blocks + lblk;
+      if (ln < x.n_blk) {
+        const int lblk = (x.start >> bs_shift) + ln;
+        phys = a.block_table ? a.block_table[static_cast<long long>(x.b) * a.max_blocks + lblk]
+                             : static_cast<long long>(x.b) * a.max_blocks + lblk;
         valid = phys >= 0 && phys < a.num_blocks;
-        blk_ok_s[ln] = valid;
-        if (!valid) atomicCAS(a.error, 0, kErrBlock);
-        rows = min(bs, (n_local - ln * bs + 31) / 32 * 32);
-        // key codes, key norm, value norm (+ QJL signs and residual norm) per row, value block
-        if (valid) bytes = rows * (L.kbytes + 4 + 4 + (qjl ? 16 + 4 : 0)) + L.vblock;
+        if (keys) {
+          blk_ok_s[seq & 1][ln] = valid;
+          if (!valid) atomicCAS(a.error, 0, kErrBlock);
+        }
+        rows = min(bs, (x.n_local - ln * bs + 31) / 32 * 32);
+        if (valid) bytes = keys ? rows * (L.kbytes + 4 + (qjl ? 16 + 4 : 0)) : rows * 4 + L.vblock;
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, off);
       __syncwarp();                             // blk_ok_s before the arrival the builders acquire
-      if (ln == 0) ptx::mbar_arrive_expect_tx(&bar_in, bytes);
+      if (ln == 0) ptx::mbar_arrive_expect_tx(keys ? &kin : &vin, bytes);
       __syncwarp();
       // the chunk holding position ctx - 1 may hold the token a decode step's
       // append (the grid this one may overlap) is writing: wait for that grid
-      if (start + n_local == ctx) asm volatile("griddepcontrol.wait;" ::: "memory");
+      if (x.start + x.n_local == x.ctx) asm volatile("griddepcontrol.wait;" ::: "memory");
       if (valid) {
-        const long long r0 = (phys * a.n_kv + kvh) * bs;    // first row of this block
+        const long long r0 = (phys * a.n_kv + x.kvh) * bs;    // first row of this block
         const int tl0 = ln * bs;
-        ptx::bulk_load(kc_s + tl0 * L.kbytes, a.k_codes + r0 * L.kbytes, rows * L.kbytes, &bar_in);
-        if (qjl) {
-          ptx::bulk_load(kq_s + tl0 * 16, a.k_qjl + r0 * 16, rows * 16, &bar_in);
-          ptx::bulk_load(kr_s + tl0, a.k_rnorm + r0, rows * 4, &bar_in);
+        if (keys) {
+          ptx::bulk_load(kc_s + tl0 * L.kbytes, a.k_codes + r0 * L.kbytes, rows * L.kbytes, &kin);
+          if (qjl) {
+            ptx::bulk_load(kq_s + tl0 * 16, a.k_qjl + r0 * 16, rows * 16, &kin);
+            ptx::bulk_load(kr_s + tl0, a.k_rnorm + r0, rows * 4, &kin);
+          }
+          ptx::bulk_load(kn_s + tl0, a.k_norm + r0, rows * 4, &kin);
+        } else {
+          ptx::bulk_load(vn_s + tl0, a.v_norm + r0, rows * 4, &vin);
+          ptx::bulk_load(vc_s + ln * (L.vblock / 4), a.v_codes + (phys * a.n_kv + x.kvh) * L.vblock, L.vblock,
+                         &vin);
         }
-        ptx::bulk_load(kn_s + tl0, a.k_norm + r0, rows * 4, &bar_in);
-        ptx::bulk_load(vn_s + tl0, a.v_norm + r0, rows * 4, &bar_in);
-        ptx::bulk_load(vc_s + ln * (L.vblock / 4), a.v_codes + (phys * a.n_kv + kvh) * L.vblock, L.vblock, &bar_in);
       }
-    }
+    };
     const uint32_t idesc_s = ptx::idesc_e4m3_f32(128, N1);
     const uint32_t idesc_o = ptx::idesc_e4m3_f32(128, NO);
     // the start-address field of a descriptor counts 16-byte units: +2 per 32-byte K step
@@ -414,222 +452,273 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     const uint64_t desc_v = ptx::desc_k_sw128(ptx::smem_u32(b_v));
     const uint32_t mse_plane_step = (L.n1 * 128) >> 4, v_tile_step = (L.no * 128) >> 4;
     const uint32_t d_mse = tmem + L.col_s;
-    // scores: tile i once its planes are stored and tile i - 1's accumulators were read
-    for (int i = 0; i < n_tiles && ok; ++i) {
-      const int slot = L.k_slots == 2 ? (i & 1) : 0;
-      ok = wait_phase(&kfull[slot], (i / L.k_slots) & 1, abort, a.error);
-      if (ok && i > 0) ok = wait_phase(&sfree, (i - 1) & 1, abort, a.error);
-      if (ok && ptx::elect_one()) {
-        ptx::tc_fence_after();
-        uint32_t a_col = tmem + slot * L.kp;
-        uint64_t dsc = desc_mse;
-        for (int s = 0; s < L.pk; ++s) {
+    int it = first, seq = 0, ktile = 0, vunit = 0;
+    Item cur, nxt;
+    bool have = next_item(a, it, last, bs_shift, cur);
+    if (have) {
+      copy_fields(cur, 0, true);
+      copy_fields(cur, 0, false);
+    }
+    while (have && ok) {
+      const bool more = next_item(a, it, last, bs_shift, nxt);
+      // scores: tile i once its planes are stored and the previous tile's accumulators were read
+      for (int i = 0; i < cur.n_tiles && ok; ++i, ++ktile) {
+        const int slot = L.k_slots == 2 ? (ktile & 1) : 0;
+        ok = wait_phase(&kfull[slot], (L.k_slots == 2 ? ktile >> 1 : ktile) & 1, abort, a.error);
+        if (ok && ktile > 0) ok = wait_phase(&sfree, (ktile - 1) & 1, abort, a.error);
+        if (ok && ptx::elect_one()) {
+          ptx::tc_fence_after();
+          uint32_t a_col = tmem + slot * L.kp;
+          uint64_t dsc = desc_mse;
+          for (int s = 0; s < L.pk; ++s) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_e4m3_tmem_a(d_mse, a_col + 8 * kk, dsc + 2 * kk, idesc_s, (s | kk) != 0);
-          a_col += 32;
-          dsc += mse_plane_step;
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::mma_e4m3_tmem_a(d_mse, a_col + 8 * kk, dsc + 2 * kk, idesc_s, (s | kk) != 0);
+            a_col += 32;
+            dsc += mse_plane_step;
+          }
+          if (qjl)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::mma_e4m3_tmem_a(d_mse + N1, a_col + 8 * kk, desc_qjl + 2 * kk, idesc_s, kk != 0);
+          ptx::mma_commit(&kdone);
         }
-        if (qjl)
+        __syncwarp();
+      }
+      // the next item's key fields, once the builders are done with this item's
+      if (ok && more) {
+        ok = wait_phase(&kfree, seq & 1, abort, a.error);
+        if (ok) copy_fields(nxt, seq + 1, true);
+      }
+      // values: unit u (tile u / n_pairs, plane pair u % n_pairs) from slot u % 2
+      const int n_units = cur.n_tiles * n_pairs;
+      for (int u = 0; u < n_units && ok; ++u, ++vunit) {
+        const int tile = u / n_pairs, pair = u - tile * n_pairs, slot = vunit & 1;
+        ok = wait_phase(&vfull[slot], (vunit >> 1) & 1, abort, a.error);
+        if (ok && ptx::elect_one()) {
+          ptx::tc_fence_after();
+          const uint64_t dsc = desc_v + tile * v_tile_step;
+          const uint32_t a_col = tmem + slot * kValueSlot;
+          const uint32_t d_col = tmem + L.col_o + 2 * pair * L.no;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_e4m3_tmem_a(d_mse + N1, a_col + 8 * kk, desc_qjl + 2 * kk, idesc_s, kk != 0);
-        ptx::mma_commit(&kdone);
-      }
-      __syncwarp();
-    }
-    // values: unit u (tile u / n_pairs, plane pair u % n_pairs) from slot u % 2
-    for (int u = 0; u < n_units && ok; ++u) {
-      const int tile = u / n_pairs, pair = u - tile * n_pairs, slot = u & 1;
-      ok = wait_phase(&vfull[slot], (u >> 1) & 1, abort, a.error);
-      if (ok && ptx::elect_one()) {
-        ptx::tc_fence_after();
-        const uint64_t dsc = desc_v + tile * v_tile_step;
-        const uint32_t a_col = tmem + slot * kValueSlot;
-        const uint32_t d_col = tmem + L.col_o + 2 * pair * L.no;
+            ptx::mma_e4m3_tmem_a(d_col, a_col + 8 * kk, dsc + 2 * kk, idesc_o, (tile | kk) != 0);
+          if (2 * pair + 1 < L.pv)
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_e4m3_tmem_a(d_col, a_col + 8 * kk, dsc + 2 * kk, idesc_o, (tile | kk) != 0);
-        if (2 * pair + 1 < L.pv)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_e4m3_tmem_a(d_col + L.no, a_col + 32 + 8 * kk, dsc + 2 * kk, idesc_o, (tile | kk) != 0);
-        ptx::mma_commit(&vdone[slot]);
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::mma_e4m3_tmem_a(d_col + L.no, a_col + 32 + 8 * kk, dsc + 2 * kk, idesc_o, (tile | kk) != 0);
+          ptx::mma_commit(&vdone[slot]);
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      // the next item's value fields, once the builders loaded this item's value words
+      if (ok && more) {
+        ok = wait_phase(&vfree, seq & 1, abort, a.error);
+        if (ok) copy_fields(nxt, seq + 1, false);
+      }
+      cur = nxt;
+      have = more;
+      ++seq;
     }
+    drain_k = kin_issued;
+    drain_v = vin_issued;
   } else {
     // =================== builders ===================
-    // B_K: the group's prepared score operand pieces into the swizzled layout
-    // (overlaps the copies); row n = h kQPieces + i of plane s, 16-byte chunk c
-    // of a row at c ^ (n % 8)
-    float inv_sig[G];                             // 1 / sigma of this thread's accumulator columns
-    float ones[G];                                // the -1 half of the +-1 products of those columns
-    asm volatile("griddepcontrol.wait;" ::: "memory");   // the query operands come from the previous grid
-    {
-      const int nk = L.pk + L.pq;
-      const int per_head = nk * kQPieces * 8;     // 16-byte chunks per head
-      for (int idx = t; idx < G * per_head; idx += kBuilders) {
-        const int h = idx / per_head, r = idx - h * per_head;
-        const int s = r / (kQPieces * 8), i = (r / 8) % kQPieces, c = r % 8;
-        const uint4 v = reinterpret_cast<const uint4*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride)[r];
-        const int n = h * kQPieces + i;
-        uint8_t* dst = s < L.pk ? b_mse + s * L.n1 * 128 : b_qjl;
-        *reinterpret_cast<uint4*>(dst + n * 128 + ((c ^ (n & 7)) << 4)) = v;
-      }
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float* hdr = reinterpret_cast<const float*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride +
-                                                          nk * kQPieces * 128);
-        inv_sig[h] = hdr[2 + half];
-        ones[h] = hdr[4 + half];
-      }
-    }
-    ptx::fence_async_shared();
-    ok = wait_phase(&bar_in, 0, abort, a.error);
-    builder_sync();                               // blk_ok_s was written by the control warp before its copies
-
-    // accumulators of key tile i -> s0 (half 0: n_k <q_rot, k_mse>) and s1
-    // (half 1: gamma coef <q_s, signs>); an accumulator holds sigma times the
-    // 0/1-bit sum, so the +-1 sum is acc / sigma - ones
-    auto read_scores = [&](int i) {
-      const int tl = i * kTile + lane;
-      const bool valid = tl < n_local && blk_ok_s[tl >> bs_shift];
-      if (half == 1 && !qjl) return;
-      float acc[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = 0.f;
-#pragma unroll
-      for (int c0 = 0; c0 < N1; c0 += 16) {
-        uint32_t v[16];
-        ptx::tmem_ld16(tmem + row_addr + L.col_s + half * N1 + c0, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int h = (c0 + j) / kQPieces, piece = (c0 + j) % kQPieces;
-          if (h < G) acc[h] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), acc[h]);
+    constexpr int HG = half_heads(G), HC = score_half(G);
+    const bool owner = half * HG < G;             // thread (lane, half) owns heads h / HG == half
+    int it = first, seq = 0, ktile = 0, vunit = 0, cur_group = -1;
+    Item x;
+    const int wpd_shift = bs_shift - 5;         // log2 of the words per coordinate in a block
+    while (ok && next_item(a, it, last, bs_shift, x)) {
+      const int group = x.b * a.n_kv + x.kvh;
+      const int qbase = x.b * a.n_q + x.kvh * G;
+      const int* blk_ok = blk_ok_s[seq & 1];
+      // B_K: the group's prepared score operand pieces into the swizzled layout
+      // (the previous item's score MMAs have completed: its last kdone was
+      // waited for); row n = score_row(G, h, i) of plane s, 16-byte chunk c of
+      // a row at c ^ (n % 8)
+      if (group != cur_group) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // the query operands come from the previous grid
+        const int nk = L.pk + L.pq;
+        const int per_head = nk * kQPieces * 8;     // 16-byte chunks per head
+        for (int idx = t; idx < G * per_head; idx += kBuilders) {
+          const int h = idx / per_head, r = idx - h * per_head;
+          const int s = r / (kQPieces * 8), i = (r / 8) % kQPieces, c = r % 8;
+          const uint4 v = reinterpret_cast<const uint4*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride)[r];
+          const int n = score_row(G, h, i);
+          uint8_t* dst = s < L.pk ? b_mse + s * L.n1 * 128 : b_qjl;
+          *reinterpret_cast<uint4*>(dst + n * 128 + ((c ^ (n & 7)) << 4)) = v;
         }
-      }
-      const float f = valid ? (half == 0 ? kn_s[tl] : kr_s[tl] * a.qjl_coef) : 0.f;
-      float* dst = half == 0 ? s0 : s1;
-#pragma unroll
-      for (int h = 0; h < G; ++h) dst[h * kChunk + tl] = f * fmaf(acc[h], inv_sig[h], -ones[h]);
-    };
-    // wait for the MMAs of tile i, read its accumulators, release them
-    auto take_scores = [&](int i, bool release) {
-      ok = ok && wait_phase(&kdone, i & 1, abort, a.error);
-      ptx::tc_fence_after();
-      if (ok) read_scores(i);
-      ptx::tc_fence_before();
-      if (release) ptx::mbar_arrive(&sfree);
-    };
-
-    // ---- scores: the planes of tile i are built while the MMAs of tile i - 1 run ----
-    for (int i = 0; i < n_tiles && ok; ++i) {
-      const int slot = L.k_slots == 2 ? (i & 1) : 0;
-      if (L.k_slots == 1 && i > 0) take_scores(i - 1, true);
-      if (!ok) break;
-      const int tl = i * kTile + lane;
-      const bool valid = tl < n_local && blk_ok_s[tl >> bs_shift];
-      uint32_t bw[4][2] = {};
-      uint32_t sg[2] = {};
-      if (valid) {
-        const uint2* kc = reinterpret_cast<const uint2*>(kc_s + tl * L.kbytes);
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-          if (p < a.k_bits) {
-            const uint2 w = kc[2 * p + half];
-            bw[p][0] = w.x;
-            bw[p][1] = w.y;
-          }
-        if (qjl) {
-          const uint2 w = reinterpret_cast<const uint2*>(kq_s + tl * 16)[half];
-          sg[0] = w.x;
-          sg[1] = w.y;
+        // per head: 1 / sigma_mse, 1 / sigma_qjl, and the -1 halves of the +-1 sums
+        if (t < 4 * G) {
+          const int h = t >> 2, k = t & 3;
+          const float* hdr = reinterpret_cast<const float*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride +
+                                                            nk * kQPieces * 128);
+          cst_s[k][h] = hdr[k < 2 ? 2 + k : 4 + (k - 2)];
         }
+        ptx::fence_async_shared();
+        builder_sync();
+        cur_group = group;
       }
-      const uint32_t base = tmem + row_addr + slot * L.kp;
-      switch (a.k_bits) {
-        case 1: key_planes<1>(base, bw, sg, qjl, w0); break;
-        case 2: key_planes<2>(base, bw, sg, qjl, w0); break;
-        case 3: key_planes<3>(base, bw, sg, qjl, w0); break;
-        default: key_planes<4>(base, bw, sg, qjl, w0); break;
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&kfull[slot]);
-      if (L.k_slots == 2 && i > 0) take_scores(i - 1, true);
-    }
-    if (ok) take_scores(n_tiles - 1, false);
-    builder_sync();
-    ok = ok && *abort == 0;
+      ok = wait_phase(&kin, seq & 1, abort, a.error);
 
-    // ---- softmax statistics over the chunk; B_V pieces of exp(s - m) n_v ----
-    if (ok) {
-      float mx[G + 1];                      // per-head score max, then the value-norm max
+      // thread (lane, half) owns the query heads h with h / HG == half: it turns
+      // their accumulators of a key tile into the scaled scores of token lane,
+      // s = scale (n_k <q_rot, k_mse> + gamma coef <q_s, signs>), into s0, and
+      // keeps their running max (an accumulator holds sigma times the 0/1-bit
+      // sum, so the +-1 sum is acc / sigma - ones)
+      float mx[G + 1];                            // owned heads' score max, then the value-norm max
 #pragma unroll
       for (int h = 0; h <= G; ++h) mx[h] = h < G ? -INFINITY : 0.f;
-      for (int i = t; i < n_tiles * kTile; i += kBuilders) {
-        const bool valid = i < n_local && blk_ok_s[i >> bs_shift];
+      auto read_scores = [&](int i) {
+        if (!owner) return;
+        const int tl = i * kTile + lane;
+        const bool valid = tl < x.n_local && blk_ok[tl >> bs_shift];
+        float am[HG], aq[HG];
+#pragma unroll
+        for (int j = 0; j < HG; ++j) am[j] = aq[j] = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < HC; c0 += 16) {
+          uint32_t v[16];
+          ptx::tmem_ld16(tmem + row_addr + L.col_s + half * HC + c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int hj = (c0 + j) / kQPieces, piece = (c0 + j) % kQPieces;
+            if (hj < HG) am[hj] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), am[hj]);
+          }
+          if (qjl) {
+            ptx::tmem_ld16(tmem + row_addr + L.col_s + N1 + half * HC + c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int hj = (c0 + j) / kQPieces, piece = (c0 + j) % kQPieces;
+              if (hj < HG) aq[hj] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), aq[hj]);
+            }
+          }
+        }
+        const float nk = valid ? kn_s[tl] : 0.f;
+        const float gk = valid && qjl ? kr_s[tl] * a.qjl_coef : 0.f;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float sc = valid ? a.scale * (s0[h * kChunk + i] + (qjl ? s1[h * kChunk + i] : 0.f)) : -INFINITY;
-          s0[h * kChunk + i] = sc;
+          if (h / HG != half) continue;             // compile-time index, warp-uniform test
+          const int j = h % HG;
+          const float mse = fmaf(am[j], cst_s[0][h], -cst_s[2][h]);
+          const float qv = qjl ? fmaf(aq[j], cst_s[1][h], -cst_s[3][h]) : 0.f;
+          const float sc = valid ? a.scale * fmaf(nk, mse, gk * qv) : -INFINITY;
+          s0[h * kChunk + tl] = sc;
           mx[h] = fmaxf(mx[h], sc);
         }
-        if (valid) mx[G] = fmaxf(mx[G], vn_s[i]);
-      }
-      block_reduce(mx, red_s, 0, kBuilders / 32, MaxOp());
-      float l[2 * G];                       // sum of e, then sum of e n_v, per head
+      };
+      // wait for the MMAs of key tile i (global index g), read its accumulators, release them
+      auto take_scores = [&](int i, int g) {
+        ok = ok && wait_phase(&kdone, g & 1, abort, a.error);
+        ptx::tc_fence_after();
+        if (ok) read_scores(i);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&sfree);
+      };
+
+      // ---- scores: the planes of tile i are built while the MMAs of tile i - 1 run ----
+      const int k0 = ktile;
+      for (int i = 0; i < x.n_tiles && ok; ++i, ++ktile) {
+        const int slot = L.k_slots == 2 ? (ktile & 1) : 0;
+        if (L.k_slots == 1 && i > 0) take_scores(i - 1, ktile - 1);
+        if (!ok) break;
+        const int tl = i * kTile + lane;
+        const bool valid = tl < x.n_local && blk_ok[tl >> bs_shift];
+        uint32_t bw[4][2] = {};
+        uint32_t sg[2] = {};
+        if (valid) {
+          const uint2* kc = reinterpret_cast<const uint2*>(kc_s + tl * L.kbytes);
 #pragma unroll
-      for (int h = 0; h < 2 * G; ++h) l[h] = 0.f;
-      for (int i = t; i < n_tiles * kTile; i += kBuilders) {
-        const float nv = (i < n_local && blk_ok_s[i >> bs_shift]) ? vn_s[i] : 0.f;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float e = mx[h] != -INFINITY ? __expf(s0[h * kChunk + i] - mx[h]) : 0.f;
-          s0[h * kChunk + i] = e;
-          l[h] += e;
-          l[G + h] = fmaf(e, nv, l[G + h]);
+          for (int p = 0; p < 4; ++p)
+            if (p < a.k_bits) {
+              const uint2 w = kc[2 * p + half];
+              bw[p][0] = w.x;
+              bw[p][1] = w.y;
+            }
+          if (qjl) {
+            const uint2 w = reinterpret_cast<const uint2*>(kq_s + tl * 16)[half];
+            sg[0] = w.x;
+            sg[1] = w.y;
+          }
         }
+        const uint32_t base = tmem + row_addr + slot * L.kp;
+        switch (a.k_bits) {
+          case 1: key_planes<1>(base, bw, sg, qjl, w0); break;
+          case 2: key_planes<2>(base, bw, sg, qjl, w0); break;
+          case 3: key_planes<3>(base, bw, sg, qjl, w0); break;
+          default: key_planes<4>(base, bw, sg, qjl, w0); break;
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&kfull[slot]);
+        if (L.k_slots == 2 && i > 0) take_scores(i - 1, ktile - 1);
       }
-      block_reduce(l, red_s, 0, kBuilders / 32, SumOp());
+      if (ok) take_scores(x.n_tiles - 1, k0 + x.n_tiles - 1);
+      ptx::mbar_arrive(&kfree);                   // this item's key fields are no longer read
+      ok = ok && wait_phase(&vin, seq & 1, abort, a.error);
+      builder_sync();
+      ok = ok && *abort == 0;
+      if (!ok) break;
+
+      // ---- softmax max over the chunk; B_V pieces of exp(s - m) n_v ----
+      for (int i = t; i < x.n_tiles * kTile; i += kBuilders)
+        if (i < x.n_local && blk_ok[i >> bs_shift]) mx[G] = fmaxf(mx[G], vn_s[i]);
+      float lw[2 * G];                            // owned heads: sum of e, then sum of e n_v
+#pragma unroll
+      for (int h = 0; h < 2 * G; ++h) lw[h] = 0.f;
+      block_reduce(mx, red_s, 0, kBuilders / 32, MaxOp());
       if (t == 0)
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          stat_s[0][h] = mx[h];
-          stat_s[1][h] = l[h];
-          wsum_s[h] = l[G + h];
-        }
+        for (int h = 0; h < G; ++h) stat_s[0][h] = mx[h];
       // the pieces carry 2 e n_v sv / beta_t, below 2 * 64 * max n_v * sv
       const float sv = piece_scale(2.f * kMaxBitInvScale * mx[G]);
-      // thread (lane, half) writes the pieces of token slot `lane` in tiles half, half + 2
-      const int kpos = k_position(lane);
-      const float ib = 2.f * bit_inv_scale(lane);
-      for (int tile = half; tile < n_tiles; tile += 2) {
-        const int tl = tile * kTile + lane;
-        const float nv = (tl < n_local && blk_ok_s[tl >> bs_shift]) ? vn_s[tl] * sv * ib : 0.f;
-        uint8_t* dst = b_v + tile * L.no * 128;
+      {
+        // thread (lane, half): token slot `lane` of every tile, its own heads
+        const int kpos = k_position(lane);
+        const float ib = 2.f * bit_inv_scale(lane) * sv;
+        for (int tile = 0; tile < x.n_tiles && owner; ++tile) {
+          const int tl = tile * kTile + lane;
+          const bool valid = tl < x.n_local && blk_ok[tl >> bs_shift];
+          const float nv = valid ? vn_s[tl] : 0.f;
+          uint8_t* dst = b_v + tile * L.no * 128;
+          float e[G];
 #pragma unroll
-        for (int h = 0; h < G; h += 2) {
-          if (h + 1 < G)
-            write_pieces2<kVPieces>(dst, h * kVPieces, (h + 1) * kVPieces, kpos, s0[h * kChunk + tl] * nv,
-                                    s0[(h + 1) * kChunk + tl] * nv);
-          else
-            write_pieces<kVPieces>(dst, h * kVPieces, kpos, s0[h * kChunk + tl] * nv);
+          for (int h = 0; h < G; ++h) {
+            e[h] = 0.f;
+            if (h / HG != half) continue;
+            if (valid && mx[h] != -INFINITY) e[h] = __expf(s0[h * kChunk + tl] - mx[h]);
+            lw[h] += e[h];
+            lw[G + h] = fmaf(e[h], nv, lw[G + h]);
+          }
+          // owned heads, two at a time where both of a pair (h, h + 1), h even, are owned
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            if (h / HG != half) continue;
+            const bool with_next = h % 2 == 0 && h + 1 < G && (h + 1) / HG == half;
+            const bool with_prev = h % 2 == 1 && (h - 1) / HG == half;
+            if (with_prev) continue;                // written with h - 1
+            if (with_next)
+              write_pieces2<kVPieces>(dst, h * kVPieces, (h + 1) * kVPieces, kpos, e[h] * nv * ib,
+                                      e[h + 1] * nv * ib);
+            else
+              write_pieces<kVPieces>(dst, h * kVPieces, kpos, e[h] * nv * ib);
+          }
         }
       }
       if (t == 0) sv_s = sv;
       ptx::fence_async_shared();
-      builder_sync();                       // every B_V piece is in place before the first value MMA
+      builder_sync();                             // every B_V piece is in place before the first value MMA
 
       // ---- values: lane d owns coordinate d; units of two sign planes alternate slots ----
-      const int wpd_shift = bs_shift - 5;   // log2 of the words per coordinate in a block
-      for (int tile = 0; tile < n_tiles && ok; ++tile) {
-        uint32_t bw[4][2] = {};             // [bit-plane][this thread's 32-token groups]
+      const int n_units = x.n_tiles * n_pairs;
+      const int v0 = vunit;
+      for (int tile = 0; tile < x.n_tiles && ok; ++tile) {
+        uint32_t bw[4][2] = {};                   // [bit-plane][this thread's 32-token groups]
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int tl = tile * kTile + 32 * (w0 + c);
-          if (tl < n_local && blk_ok_s[tl >> bs_shift]) {
+          if (tl < x.n_local && blk_ok[tl >> bs_shift]) {
             const uint32_t* src =
                 vc_s + (tl >> bs_shift) * (L.vblock / 4) + ((tl & (bs - 1)) >> 5) + (lane << wpd_shift);
 #pragma unroll
@@ -637,10 +726,11 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
               if (p < a.v_bits) bw[p][c] = src[(p * 128) << wpd_shift];
           }
         }
-        for (int pair = 0; pair < n_pairs && ok; ++pair) {
-          const int u = tile * n_pairs + pair, slot = u & 1;
-          if (u >= 2) {
-            ok = wait_phase(&vdone[slot], ((u - 2) >> 1) & 1, abort, a.error);
+        if (tile == x.n_tiles - 1) ptx::mbar_arrive(&vfree);   // the value fields are no longer read
+        for (int pair = 0; pair < n_pairs && ok; ++pair, ++vunit) {
+          const int slot = vunit & 1;
+          if (vunit >= 2) {
+            ok = wait_phase(&vdone[slot], ((vunit - 2) >> 1) & 1, abort, a.error);
             ptx::tc_fence_after();
             if (!ok) break;
           }
@@ -657,9 +747,18 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         }
       }
       // the last commit of each value slot (a commit covers every earlier MMA)
-      if (ok && n_units >= 2) ok = wait_phase(&vdone[(n_units - 2) & 1], ((n_units - 2) >> 1) & 1, abort, a.error);
-      if (ok) ok = wait_phase(&vdone[(n_units - 1) & 1], ((n_units - 1) >> 1) & 1, abort, a.error);
+      const int vl = v0 + n_units - 1;
+      if (ok && vl >= 1) ok = wait_phase(&vdone[(vl - 1) & 1], ((vl - 1) >> 1) & 1, abort, a.error);
+      if (ok) ok = wait_phase(&vdone[vl & 1], (vl >> 1) & 1, abort, a.error);
       ptx::tc_fence_after();
+
+      block_reduce(lw, red_s, 0, kBuilders / 32, SumOp());
+      if (t == 0)
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          stat_s[1][h] = lw[h];
+          wsum_s[h] = lw[G + h];
+        }
 
       // ---- partial output of this chunk: half h reads the planes s with s % 2 == h ----
       float o[G];
@@ -680,18 +779,19 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           }
         }
       }
+      ptx::tc_fence_before();
       if (half == 1)
 #pragma unroll
         for (int h = 0; h < G; ++h) s1[h * kTile + lane] = o[h];
       builder_sync();
       ok = ok && *abort == 0;
       if (ok && half == 0) {
-        const float inv_sv = 1.f / sv_s;    // exact: sv is a power of two
-        float a_sum = 0.f;                  // sum_S a_S: the -1 half of every sign product
+        const float inv_sv = 1.f / sv_s;          // exact: sv is a power of two
+        float a_sum = 0.f;                        // sum_S a_S: the -1 half of every sign product
         for (int s = 0; s < L.pv; ++s) a_sum += vw_s[s];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          float* part = a.ws_part + (static_cast<long long>(qbase + h) * a.max_chunks + chunk) * kPartStride;
+          float* part = a.ws_part + (static_cast<long long>(qbase + h) * a.max_chunks + x.chunk) * kPartStride;
           part[4 + lane] = fmaf(o[h] + s1[h * kTile + lane], inv_sv, -a_sum * wsum_s[h]);
           if (lane == 0) {
             part[0] = stat_s[0][h];
@@ -699,8 +799,9 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           }
         }
       }
+      builder_sync();                             // s1, stat_s and wsum_s are free for the next item
+      ++seq;
     }
-
   }
 
   // the merge kernel that follows may launch once every CTA got here (it
@@ -714,7 +815,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       // goes (each lane commits, covering whichever lane issued)
       ptx::mma_commit(&bar_d);
       if (t == kBuilders) {
-        ptx::drain_bar(&bar_in, 0);
+        if (drain_k > 0) ptx::drain_bar(&kin, (drain_k - 1) & 1);
+        if (drain_v > 0) ptx::drain_bar(&vin, (drain_v - 1) & 1);
         ptx::drain_bar(&bar_d, 0);
       }
       __syncwarp();
@@ -738,8 +840,17 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, bool early) {
   cudaError_t err = cudaFuncSetAttribute(attention_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          l.smem_bytes);
   if (err != cudaSuccess) return err;
+  // a persistent grid: two CTAs per SM (one when the tensor memory or shared
+  // memory of a CTA leaves room for one), each taking a contiguous run of
+  // (sequence, KV head, chunk) items so that consecutive items share the query
+  // operands and the next item's fields load while the current one computes
+  const long long total = static_cast<long long>(a.batch) * a.n_kv * a.max_chunks;
+  const int per_sm = (l.tmem <= 256 && l.smem_bytes <= 113 * 1024) ? 2 : 1;
+  const long long slots = static_cast<long long>(per_sm) * (a.num_sms > 0 ? a.num_sms : 148);
+  const int per_cta = static_cast<int>((total + slots - 1) / slots);
+  const int n_ctas = static_cast<int>((total + per_cta - 1) / per_cta);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.max_chunks, a.n_kv, a.batch);
+  cfg.gridDim = dim3(n_ctas);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = l.smem_bytes;
   cfg.stream = stream;
@@ -748,7 +859,7 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, bool early) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = early ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attention_tc_kernel<G>, a, l);
+  return cudaLaunchKernelEx(&cfg, attention_tc_kernel<G>, a, l, per_cta);
 }
 
 cudaError_t launch_decode_partials_tc(const DecodeArgs& a, cudaStream_t stream, bool early) {

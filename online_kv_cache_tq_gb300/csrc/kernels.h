@@ -93,6 +93,7 @@ struct DecodeArgs {
   const float* Spt;
   const DeviceTables* tables;
   int* error;
+  int num_sms;              // of the handle's device
 };
 
 // Word (uint32 units) of a token-transposed codes field holding plane p,
