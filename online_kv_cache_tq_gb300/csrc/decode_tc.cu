@@ -42,6 +42,8 @@
 // code 4) and a failed wait makes every other wait give up.
 #include <cuda_fp8.h>
 
+#include <type_traits>
+
 #include "e4m3_pieces.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
@@ -229,12 +231,14 @@ struct TcLayout {
   int pk, pq, pv;           // key sign planes, QJL plane (0/1), value sign planes
   int n1, n2, no;           // score columns (mse, qjl), value columns per plane
   int kp, k_slots;          // columns per key slot, key slots (1 or 2)
+  int v_slots;              // value slots of kValueSlot columns (2 to kMaxValueSlots)
   int col_s, col_o, cols, tmem;
   int kbytes, vblock;       // key code bytes per token; value code bytes per (block, head)
   int off_bmse, off_bqjl, off_bv, off_s0, off_s1, off_kc, off_kq, off_kn, off_kr, off_vn, off_vc, smem_bytes;
 };
 
 constexpr int kValueSlot = 64;              // columns of one value slot (two sign planes)
+constexpr int kMaxValueSlots = 4;
 
 TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size) {
   TcLayout l{};
@@ -245,7 +249,10 @@ TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size) 
   l.n2 = qjl ? l.n1 : 0;
   l.no = value_cols(group);
   l.kp = 32 * (l.pk + l.pq);
-  const int vcols = 2 * kValueSlot + l.pv * l.no;
+  // value slots: as many as fit beside the accumulators in the allocation the
+  // key phase needs (at least two), so the builders run further ahead of the MMAs
+  const int vacc = l.pv * l.no;
+  const int vcols = 2 * kValueSlot + vacc;
   auto kcols = [&](int slots) { return slots * l.kp + l.n1 + l.n2; };
   auto mx = [](int x, int y) { return x > y ? x : y; };
   if (mx(kcols(2), vcols) <= 256) l.k_slots = 2;
@@ -253,10 +260,12 @@ TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size) 
   else if (mx(kcols(2), vcols) <= 512) l.k_slots = 2;
   else l.k_slots = 1;
   l.col_s = l.k_slots * l.kp;
-  l.col_o = 2 * kValueSlot;
   l.cols = mx(kcols(l.k_slots), vcols);
   l.tmem = 32;
   while (l.tmem < l.cols) l.tmem *= 2;
+  l.v_slots = 2;
+  while (l.v_slots < kMaxValueSlots && (l.v_slots + 1) * kValueSlot + vacc <= l.tmem) ++l.v_slots;
+  l.col_o = l.v_slots * kValueSlot;
   l.kbytes = k_bits * 16;
   l.vblock = v_bits * 128 * block_size / 8;
   int o = 0;
@@ -344,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   // item (256 arrivals); kfull / vfull: the builders stored a slot's planes
   // (256 arrivals); kdone / vdone: the slot's MMAs completed (commit); sfree:
   // the builders read the score accumulators (256 arrivals); bar_d: drain
-  __shared__ __align__(8) uint64_t kin, vin, kfree, vfree, kfull[2], kdone, sfree, vfull[2], vdone[2], bar_d;
+  __shared__ __align__(8) uint64_t kin, vin, kfree, vfree, kfull[2], kdone, sfree, vfull[kMaxValueSlots],
+      vdone[kMaxValueSlots], bar_d;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
   __shared__ float red_s[(kBuilders / 32) * (2 * G + 1)];   // block_reduce of up to 2 G + 1 values
@@ -379,10 +389,10 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     ptx::mbar_init(&kfull[1], kBuilders);
     ptx::mbar_init(&kdone, 1);
     ptx::mbar_init(&sfree, kBuilders);
-    ptx::mbar_init(&vfull[0], kBuilders);
-    ptx::mbar_init(&vfull[1], kBuilders);
-    ptx::mbar_init(&vdone[0], 1);
-    ptx::mbar_init(&vdone[1], 1);
+    for (int i = 0; i < kMaxValueSlots; ++i) {
+      ptx::mbar_init(&vfull[i], kBuilders);
+      ptx::mbar_init(&vdone[i], 1);
+    }
     ptx::mbar_init(&bar_d, 32);
     ptx::fence_mbar_init();
   }
@@ -452,7 +462,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     const uint64_t desc_v = ptx::desc_k_sw128(ptx::smem_u32(b_v));
     const uint32_t mse_plane_step = (L.n1 * 128) >> 4, v_tile_step = (L.no * 128) >> 4;
     const uint32_t d_mse = tmem + L.col_s;
-    int it = first, seq = 0, ktile = 0, vunit = 0;
+    int it = first, seq = 0, ktile = 0;
+    int vslot = 0, vwrap = 0;                   // value unit counter as (slot, times round the slots)
     Item cur, nxt;
     bool have = next_item(a, it, last, bs_shift, cur);
     if (have) {
@@ -490,11 +501,11 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         ok = wait_phase(&kfree, seq & 1, abort, a.error);
         if (ok) copy_fields(nxt, seq + 1, true);
       }
-      // values: unit u (tile u / n_pairs, plane pair u % n_pairs) from slot u % 2
+      // values: unit u (tile u / n_pairs, plane pair u % n_pairs) from slot u % v_slots
       const int n_units = cur.n_tiles * n_pairs;
-      for (int u = 0; u < n_units && ok; ++u, ++vunit) {
-        const int tile = u / n_pairs, pair = u - tile * n_pairs, slot = vunit & 1;
-        ok = wait_phase(&vfull[slot], (vunit >> 1) & 1, abort, a.error);
+      for (int u = 0, tile = 0, pair = 0; u < n_units && ok; ++u) {
+        const int slot = vslot;
+        ok = wait_phase(&vfull[slot], vwrap & 1, abort, a.error);
         if (ok && ptx::elect_one()) {
           ptx::tc_fence_after();
           const uint64_t dsc = desc_v + tile * v_tile_step;
@@ -510,6 +521,14 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           ptx::mma_commit(&vdone[slot]);
         }
         __syncwarp();
+        if (++pair == n_pairs) {
+          pair = 0;
+          ++tile;
+        }
+        if (++vslot == L.v_slots) {
+          vslot = 0;
+          ++vwrap;
+        }
       }
       // the next item's value fields, once the builders loaded this item's value words
       if (ok && more) {
@@ -525,8 +544,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   } else {
     // =================== builders ===================
     constexpr int HG = half_heads(G), HC = score_half(G);
-    const bool owner = half * HG < G;             // thread (lane, half) owns heads h / HG == half
-    int it = first, seq = 0, ktile = 0, vunit = 0, cur_group = -1;
+    int it = first, seq = 0, ktile = 0, cur_group = -1;
+    int vslot = 0, vwrap = 0;                     // value unit counter as (slot, times round the slots)
     Item x;
     const int wpd_shift = bs_shift - 5;         // log2 of the words per coordinate in a block
     while (ok && next_item(a, it, last, bs_shift, x)) {
@@ -570,43 +589,50 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       float mx[G + 1];                            // owned heads' score max, then the value-norm max
 #pragma unroll
       for (int h = 0; h <= G; ++h) mx[h] = h < G ? -INFINITY : 0.f;
-      auto read_scores = [&](int i) {
-        if (!owner) return;
-        const int tl = i * kTile + lane;
-        const bool valid = tl < x.n_local && blk_ok[tl >> bs_shift];
-        float am[HG], aq[HG];
+      // (templated on the half, so that the owned heads are compile-time indices)
+      auto read_scores_half = [&](int i, auto half_c) {
+        constexpr int H0 = decltype(half_c)::value * HG;
+        if constexpr (H0 < G) {
+          const int tl = i * kTile + lane;
+          const bool valid = tl < x.n_local && blk_ok[tl >> bs_shift];
+          float am[HG], aq[HG];
 #pragma unroll
-        for (int j = 0; j < HG; ++j) am[j] = aq[j] = 0.f;
+          for (int j = 0; j < HG; ++j) am[j] = aq[j] = 0.f;
 #pragma unroll
-        for (int c0 = 0; c0 < HC; c0 += 16) {
-          uint32_t v[16];
-          ptx::tmem_ld16(tmem + row_addr + L.col_s + half * HC + c0, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int hj = (c0 + j) / kQPieces, piece = (c0 + j) % kQPieces;
-            if (hj < HG) am[hj] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), am[hj]);
-          }
-          if (qjl) {
-            ptx::tmem_ld16(tmem + row_addr + L.col_s + N1 + half * HC + c0, v);
+          for (int c0 = 0; c0 < HC; c0 += 16) {
+            uint32_t v[16];
+            ptx::tmem_ld16(tmem + row_addr + L.col_s + (H0 / HG) * HC + c0, v);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int hj = (c0 + j) / kQPieces, piece = (c0 + j) % kQPieces;
-              if (hj < HG) aq[hj] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), aq[hj]);
+              if (hj < HG) am[hj] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), am[hj]);
+            }
+            if (qjl) {
+              ptx::tmem_ld16(tmem + row_addr + L.col_s + N1 + (H0 / HG) * HC + c0, v);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int hj = (c0 + j) / kQPieces, piece = (c0 + j) % kQPieces;
+                if (hj < HG) aq[hj] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), aq[hj]);
+              }
             }
           }
-        }
-        const float nk = valid ? kn_s[tl] : 0.f;
-        const float gk = valid && qjl ? kr_s[tl] * a.qjl_coef : 0.f;
+          const float nk = valid ? kn_s[tl] : 0.f;
+          const float gk = valid && qjl ? kr_s[tl] * a.qjl_coef : 0.f;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          if (h / HG != half) continue;             // compile-time index, warp-uniform test
-          const int j = h % HG;
-          const float mse = fmaf(am[j], cst_s[0][h], -cst_s[2][h]);
-          const float qv = qjl ? fmaf(aq[j], cst_s[1][h], -cst_s[3][h]) : 0.f;
-          const float sc = valid ? a.scale * fmaf(nk, mse, gk * qv) : -INFINITY;
-          s0[h * kChunk + tl] = sc;
-          mx[h] = fmaxf(mx[h], sc);
+          for (int j = 0; j < HG; ++j) {
+            const int h = H0 + j;
+            if (h >= G) break;
+            const float mse = fmaf(am[j], cst_s[0][h], -cst_s[2][h]);
+            const float qv = qjl ? fmaf(aq[j], cst_s[1][h], -cst_s[3][h]) : 0.f;
+            const float sc = valid ? a.scale * fmaf(nk, mse, gk * qv) : -INFINITY;
+            s0[h * kChunk + tl] = sc;
+            mx[h] = fmaxf(mx[h], sc);
+          }
         }
+      };
+      auto read_scores = [&](int i) {
+        if (half == 0) read_scores_half(i, std::integral_constant<int, 0>{});
+        else read_scores_half(i, std::integral_constant<int, 1>{});
       };
       // wait for the MMAs of key tile i (global index g), read its accumulators, release them
       auto take_scores = [&](int i, int g) {
@@ -675,44 +701,50 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       const float sv = piece_scale(2.f * kMaxBitInvScale * mx[G]);
       {
         // thread (lane, half): token slot `lane` of every tile, its own heads
+        // (templated on the half, so that the owned heads are compile-time indices)
         const int kpos = k_position(lane);
         const float ib = 2.f * bit_inv_scale(lane) * sv;
-        for (int tile = 0; tile < x.n_tiles && owner; ++tile) {
-          const int tl = tile * kTile + lane;
-          const bool valid = tl < x.n_local && blk_ok[tl >> bs_shift];
-          const float nv = valid ? vn_s[tl] : 0.f;
-          uint8_t* dst = b_v + tile * L.no * 128;
-          float e[G];
+        auto weights_half = [&](auto half_c) {
+          constexpr int H0 = decltype(half_c)::value * HG;
+          if constexpr (H0 < G) {
+            for (int tile = 0; tile < x.n_tiles; ++tile) {
+              const int tl = tile * kTile + lane;
+              const bool valid = tl < x.n_local && blk_ok[tl >> bs_shift];
+              const float nv = valid ? vn_s[tl] : 0.f;
+              uint8_t* dst = b_v + tile * L.no * 128;
+              float e[HG];
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            e[h] = 0.f;
-            if (h / HG != half) continue;
-            if (valid && mx[h] != -INFINITY) e[h] = __expf(s0[h * kChunk + tl] - mx[h]);
-            lw[h] += e[h];
-            lw[G + h] = fmaf(e[h], nv, lw[G + h]);
-          }
-          // owned heads, two at a time where both of a pair (h, h + 1), h even, are owned
+              for (int j = 0; j < HG; ++j) {
+                const int h = H0 + j;
+                e[j] = 0.f;
+                if (h >= G) continue;
+                if (valid && mx[h] != -INFINITY) e[j] = __expf(s0[h * kChunk + tl] - mx[h]);
+                lw[h] += e[j];
+                lw[G + h] = fmaf(e[j], nv, lw[G + h]);
+              }
+              // the owned heads two at a time (one when the half owns one head)
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            if (h / HG != half) continue;
-            const bool with_next = h % 2 == 0 && h + 1 < G && (h + 1) / HG == half;
-            const bool with_prev = h % 2 == 1 && (h - 1) / HG == half;
-            if (with_prev) continue;                // written with h - 1
-            if (with_next)
-              write_pieces2<kVPieces>(dst, h * kVPieces, (h + 1) * kVPieces, kpos, e[h] * nv * ib,
-                                      e[h + 1] * nv * ib);
-            else
-              write_pieces<kVPieces>(dst, h * kVPieces, kpos, e[h] * nv * ib);
+              for (int j = 0; j < HG; j += 2) {
+                const int h = H0 + j;
+                if (h >= G) continue;
+                if (j + 1 < HG && h + 1 < G)
+                  write_pieces2<kVPieces>(dst, h * kVPieces, (h + 1) * kVPieces, kpos, e[j] * nv * ib,
+                                          e[j + 1] * nv * ib);
+                else
+                  write_pieces<kVPieces>(dst, h * kVPieces, kpos, e[j] * nv * ib);
+              }
+            }
           }
-        }
+        };
+        if (half == 0) weights_half(std::integral_constant<int, 0>{});
+        else weights_half(std::integral_constant<int, 1>{});
       }
       if (t == 0) sv_s = sv;
       ptx::fence_async_shared();
       builder_sync();                             // every B_V piece is in place before the first value MMA
 
-      // ---- values: lane d owns coordinate d; units of two sign planes alternate slots ----
-      const int n_units = x.n_tiles * n_pairs;
-      const int v0 = vunit;
+      // ---- values: lane d owns coordinate d; units of two sign planes rotate through the slots ----
+      int last_slot = 0, last_wrap = 0;
       for (int tile = 0; tile < x.n_tiles && ok; ++tile) {
         uint32_t bw[4][2] = {};                   // [bit-plane][this thread's 32-token groups]
 #pragma unroll
@@ -727,10 +759,16 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           }
         }
         if (tile == x.n_tiles - 1) ptx::mbar_arrive(&vfree);   // the value fields are no longer read
-        for (int pair = 0; pair < n_pairs && ok; ++pair, ++vunit) {
-          const int slot = vunit & 1;
-          if (vunit >= 2) {
-            ok = wait_phase(&vdone[slot], ((vunit - 2) >> 1) & 1, abort, a.error);
+        for (int pair = 0; pair < n_pairs && ok; ++pair) {
+          const int slot = vslot;
+          last_slot = vslot;
+          last_wrap = vwrap;
+          if (++vslot == L.v_slots) {
+            vslot = 0;
+            ++vwrap;
+          }
+          if (last_wrap > 0) {                    // the slot's previous unit has completed
+            ok = wait_phase(&vdone[slot], (last_wrap - 1) & 1, abort, a.error);
             ptx::tc_fence_after();
             if (!ok) break;
           }
@@ -746,10 +784,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           ptx::mbar_arrive(&vfull[slot]);
         }
       }
-      // the last commit of each value slot (a commit covers every earlier MMA)
-      const int vl = v0 + n_units - 1;
-      if (ok && vl >= 1) ok = wait_phase(&vdone[(vl - 1) & 1], ((vl - 1) >> 1) & 1, abort, a.error);
-      if (ok) ok = wait_phase(&vdone[vl & 1], (vl >> 1) & 1, abort, a.error);
+      // the item's last commit (a commit covers every earlier MMA)
+      if (ok) ok = wait_phase(&vdone[last_slot], last_wrap & 1, abort, a.error);
       ptx::tc_fence_after();
 
       block_reduce(lw, red_s, 0, kBuilders / 32, SumOp());
