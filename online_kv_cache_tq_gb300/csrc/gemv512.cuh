@@ -1,33 +1,43 @@
 // 128 x 128 matrix-vector products for the per-vector kernels of one decode
-// step (append, query preparation, combine), by a CTA of 512 threads.
+// step (append, query preparation, combine): one CTA per vector, THREADS =
+// 128 * copies threads, thread (o, q = threadIdx.x / 128) working on output o.
 #pragma once
 
 namespace tq {
 
-constexpr int kGemvThreads = 512;
+constexpr int kGemvThreads = 512;   // combine: four copies of every coordinate
+constexpr int kVecThreads = 256;    // append and query preparation: two copies
 
 // out[o] = sum_i w[i * 128 + o] * in_s[i] for o = threadIdx.x % 128.  Thread
-// (o, q = threadIdx.x / 128) sums the 32 terms i in [32 q, 32 q + 32) with all
-// 32 loads in flight at once, and the four partial sums meet in red_s
-// ([4][128] floats).  Every thread returns out[o]; in_s must be visible to
-// all threads before the call, and red_s is free again on return.
-__device__ __forceinline__ float gemv512(const float* __restrict__ w, const float* in_s, float* red_s) {
+// (o, q) sums the 128 / copies terms i in [q * 128 / copies, ...) in batches of
+// 32 loads in flight at once, and the partial sums meet in red_s ([copies][128]
+// floats).  Every thread returns out[o]; in_s must be visible to all threads
+// before the call, and red_s is free again on return.
+template <int THREADS>
+__device__ __forceinline__ float gemv(const float* __restrict__ w, const float* in_s, float* red_s) {
+  constexpr int kCopies = THREADS / 128, kTerms = 128 / kCopies;
   const int o = threadIdx.x & 127, q = threadIdx.x >> 7;
-  const float* wp = w + (32 * q) * 128 + o;
-  float v[32];
-#pragma unroll
-  for (int k = 0; k < 32; ++k) v[k] = __ldg(wp + k * 128);
   float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
-  for (int k = 0; k < 32; k += 4) {
-    acc0 = fmaf(v[k + 0], in_s[32 * q + k + 0], acc0);
-    acc1 = fmaf(v[k + 1], in_s[32 * q + k + 1], acc1);
-    acc2 = fmaf(v[k + 2], in_s[32 * q + k + 2], acc2);
-    acc3 = fmaf(v[k + 3], in_s[32 * q + k + 3], acc3);
+  for (int k0 = 0; k0 < kTerms; k0 += 32) {
+    const float* wp = w + (kTerms * q + k0) * 128 + o;
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = __ldg(wp + k * 128);
+    const float* x = in_s + kTerms * q + k0;
+#pragma unroll
+    for (int k = 0; k < 32; k += 4) {
+      acc0 = fmaf(v[k + 0], x[k + 0], acc0);
+      acc1 = fmaf(v[k + 1], x[k + 1], acc1);
+      acc2 = fmaf(v[k + 2], x[k + 2], acc2);
+      acc3 = fmaf(v[k + 3], x[k + 3], acc3);
+    }
   }
   red_s[q * 128 + o] = (acc0 + acc1) + (acc2 + acc3);
   __syncthreads();
-  const float r = (red_s[o] + red_s[128 + o]) + (red_s[256 + o] + red_s[384 + o]);
+  float r = red_s[o];
+#pragma unroll
+  for (int c = 1; c < kCopies; ++c) r += red_s[c * 128 + o];
   __syncthreads();
   return r;
 }

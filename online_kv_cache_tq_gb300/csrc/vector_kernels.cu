@@ -1,5 +1,5 @@
-// Per-vector kernels of a decode step, one CTA of 512 threads per head
-// vector: quantize-append of the step's new keys and values, the query
+// Per-vector kernels of a decode step, one CTA per head vector (256 threads
+// for the append and the query preparation, 512 for the merge): quantize-append of the step's new keys and values, the query
 // preparation of decode attention (a fused launch runs both for a step), and
 // the merge of the split-K partials with the back-rotation.
 //
@@ -26,8 +26,8 @@ __device__ __forceinline__ float load_elem(const void* base, long long idx, bool
 
 // Quantize head vector v of `a` (n = ||x||, y = R x / n, nearest level, and
 // for keys the rotated residual r' = R x - n c[code], its norm and the signs
-// of S' r').  Thread (o, q) of the 512 works on rotated coordinate o; the
-// four copies of o split the matrix-vector products and threads q == 0
+// of S' r').  Thread (o, q) of the 256 works on rotated coordinate o; the
+// two copies of o split the matrix-vector products and threads q == 0
 // (warps 0-3) write the results.
 __device__ __forceinline__ void quantize_vector(const QuantizeArgs& a, int v, bool bf16) {
   __shared__ float x_s[kDim];
@@ -46,7 +46,7 @@ __device__ __forceinline__ void quantize_vector(const QuantizeArgs& a, int v, bo
                        : reinterpret_cast<const float*>(a.x)[idx];
   if (lead) x_s[o] = x;
   const float n = sqrtf(sum128(x * x, part_s));          // its barriers also publish x_s
-  const float yv = gemv512(a.Rt, x_s, red_s);           // (R x)_o
+  const float yv = gemv<kVecThreads>(a.Rt, x_s, red_s);           // (R x)_o
   const float y = n > 0.f ? yv / n : 0.f;
   int code = 0;
   for (int t = 0; t + 1 < (1 << a.bits); ++t) code += (y > a.bounds[t]) ? 1 : 0;
@@ -80,7 +80,7 @@ __device__ __forceinline__ void quantize_vector(const QuantizeArgs& a, int v, bo
     const float r = fmaf(-n, a.levels[code], yv);
     if (lead) r_s[o] = r;
     const float gamma = sqrtf(sum128(r * r, part_s));    // its barriers also publish r_s
-    const float z = gemv512(a.Spt, r_s, red_s);
+    const float z = gemv<kVecThreads>(a.Spt, r_s, red_s);
     const unsigned word = __ballot_sync(0xffffffffu, z > 0.f);
     if (ok && lead && lane == 0) reinterpret_cast<unsigned*>(a.qjl + row * 16)[warp] = word;
     if (ok && threadIdx.x == 0) a.rnorm[row] = gamma;
@@ -92,8 +92,8 @@ __device__ __forceinline__ void quantize_vector(const QuantizeArgs& a, int v, bo
 // of this query head: e4m3 pieces of 2 sigma_0 a_S (R q)_j / beta_j per key
 // sign plane S and of 2 sigma_1 (S' R q)_j / beta_j (sigma_0, sigma_1 powers
 // of two that bound the pieces; beta_j the bit scale of coordinate j), and the
-// sums that turn the 0/1 bit products into +-1 sign products.  512 threads:
-// thread (o, q) works on coordinate o; the copies of o split the
+// sums that turn the 0/1 bit products into +-1 sign products.  256 threads:
+// thread (o, q) works on coordinate o; the two copies of o split the
 // matrix-vector products and the piece planes.
 __device__ __forceinline__ void prepare_query(const DecodeArgs& a, int vec, bool bf16) {
   __shared__ float q_s[kDim];
@@ -104,7 +104,7 @@ __device__ __forceinline__ void prepare_query(const DecodeArgs& a, int vec, bool
   const bool lead = qq == 0;
   if (lead) q_s[o] = load_elem(a.q, static_cast<long long>(vec) * kDim + o, bf16);
   __syncthreads();
-  const float acc = gemv512(a.Rt, q_s, red_s);
+  const float acc = gemv<kVecThreads>(a.Rt, q_s, red_s);
   if (lead) {
     qr_s[o] = acc;
     a.ws_q[static_cast<long long>(vec) * 2 * kDim + o] = acc;
@@ -112,7 +112,7 @@ __device__ __forceinline__ void prepare_query(const DecodeArgs& a, int vec, bool
   __syncthreads();
   float z = 0.f;
   if (a.qjl_m > 0) {
-    z = gemv512(a.Spt, qr_s, red_s);
+    z = gemv<kVecThreads>(a.Spt, qr_s, red_s);
     if (lead) a.ws_q[static_cast<long long>(vec) * 2 * kDim + kDim + o] = z;
   }
   if (a.ws_bk == nullptr) return;
@@ -128,9 +128,9 @@ __device__ __forceinline__ void prepare_query(const DecodeArgs& a, int vec, bool
   const float sum_qr = sum128(acc, part_s), sum_qs = sum128(z, part_s);
   uint8_t* dst = a.ws_bk + static_cast<long long>(vec) * a.bk_stride;
   const int kpos = k_position(o);
-  // plane s (s == planes: the QJL operand) by the copies qq == s % 4
+  // plane s (s == planes: the QJL operand) by the copy qq == s % copies
   const int items = planes + (a.qjl_m > 0 ? 1 : 0);
-  for (int s = qq; s < items; s += 4) {
+  for (int s = qq; s < items; s += kVecThreads / 128) {
     const float y = s < planes ? a.tables->k_walsh[s] * acc * ib * sig0 : z * ib * sig1;
     write_pieces_rows<kQPieces>(dst + s * kQPieces * 128, kpos, y);
   }
@@ -205,19 +205,19 @@ __global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
   __syncthreads();
   if (q == 0) o_s[o] = lt > 0.f ? at / lt : 0.f;
   __syncthreads();
-  const float out = gemv512(a.R, o_s, red_s);
+  const float out = gemv<kGemvThreads>(a.R, o_s, red_s);
   if (q == 0) a.out[static_cast<long long>(vec) * kDim + o] = out;
 }
 
 // Blocks [0, first.n_vec) quantize `first`, the rest `second` (K and V of one
 // append in a single launch).
-__global__ void __launch_bounds__(kGemvThreads) quantize_small_kernel(QuantizeArgs first, QuantizeArgs second,
+__global__ void __launch_bounds__(kVecThreads) quantize_small_kernel(QuantizeArgs first, QuantizeArgs second,
                                                                       bool bf16) {
   const bool in_first = static_cast<int>(blockIdx.x) < first.n_vec;
   quantize_vector(in_first ? first : second, in_first ? blockIdx.x : blockIdx.x - first.n_vec, bf16);
 }
 
-__global__ void __launch_bounds__(kGemvThreads) qprep_kernel(DecodeArgs a, bool bf16) {
+__global__ void __launch_bounds__(kVecThreads) qprep_kernel(DecodeArgs a, bool bf16) {
   prepare_query(a, blockIdx.x, bf16);
 }
 
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kGemvThreads) qprep_kernel(DecodeArgs a, bool 
 // [n_k, 2 n_k) the new values, the rest prepare the queries.  The decode
 // partials kernel that follows may start as soon as these blocks run (it
 // waits for their results where it reads them).
-__global__ void __launch_bounds__(kGemvThreads) step_prep_kernel(QuantizeArgs ka, QuantizeArgs va, bool kv_bf16,
+__global__ void __launch_bounds__(kVecThreads) step_prep_kernel(QuantizeArgs ka, QuantizeArgs va, bool kv_bf16,
                                                                  DecodeArgs da, bool q_bf16) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int blk = blockIdx.x;
@@ -241,14 +241,14 @@ cudaError_t launch_quantize_small(const QuantizeArgs* first, const QuantizeArgs*
   const int n = (first ? first->n_vec : 0) + (second ? second->n_vec : 0);
   if (n <= 0) return cudaSuccess;
   QuantizeArgs none{};
-  quantize_small_kernel<<<n, kGemvThreads, 0, stream>>>(first ? *first : none, second ? *second : none, bf16);
+  quantize_small_kernel<<<n, kVecThreads, 0, stream>>>(first ? *first : none, second ? *second : none, bf16);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_t stream) {
   const int n_vec = args.batch * args.n_q;
   if (n_vec <= 0) return cudaSuccess;
-  qprep_kernel<<<n_vec, kGemvThreads, 0, stream>>>(args, bf16);
+  qprep_kernel<<<n_vec, kVecThreads, 0, stream>>>(args, bf16);
   return cudaGetLastError();
 }
 
@@ -271,7 +271,7 @@ cudaError_t launch_step_prep(const QuantizeArgs& ka, const QuantizeArgs& va, boo
                              bool q_bf16, cudaStream_t stream) {
   const int n = 2 * ka.n_vec + da.batch * da.n_q;
   if (n <= 0) return cudaSuccess;
-  step_prep_kernel<<<n, kGemvThreads, 0, stream>>>(ka, va, kv_bf16, da, q_bf16);
+  step_prep_kernel<<<n, kVecThreads, 0, stream>>>(ka, va, kv_bf16, da, q_bf16);
   return cudaGetLastError();
 }
 
