@@ -158,52 +158,61 @@ __device__ __forceinline__ int context_of(const DecodeArgs& a, int b) {
 }
 
 // out[vec] = R^T (merged acc / merged l).  512 threads: thread (o, q) merges
-// coordinate o over the chunks c with c % 4 == q, then the copies of o add up
-// and split the back-rotation.
+// coordinate o over the chunks c with c % 4 == q as a running (m, l, acc), the
+// four copies of o merge theirs, and the copies split the back-rotation.
+// Every thread's chunk loads are independent, so a launch is a few memory
+// round trips long.
 __global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // the partials (no-op unless launched early)
   __shared__ float o_s[kDim];
   __shared__ float red_s[4 * kDim];
-  __shared__ float lred_s[4];
-  __shared__ float w_s[1024];
-  __shared__ float part_s[16];
+  __shared__ float ml_s[2][4];
   const int vec = blockIdx.x;
   const int b = vec / a.n_q;
   const int t = threadIdx.x;
   const int o = t & 127, q = t >> 7;
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the partials (no-op unless launched early)
   const int ctx = context_of(a, b);
   const int n_chunks = (ctx + kChunk - 1) / kChunk;
   const float* part = a.ws_part + static_cast<long long>(vec) * a.max_chunks * kPartStride;
-  float mx = -INFINITY;
-  for (int c = t; c < n_chunks; c += kGemvThreads) mx = fmaxf(mx, part[c * kPartStride]);
+  float m = -INFINITY, l = 0.f, acc = 0.f;
+  for (int c0 = q; c0 < n_chunks; c0 += 4 * 4) {
+    float mc[4], lc[4], ac[4];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  if ((t & 31) == 0) part_s[t >> 5] = mx;
-  __syncthreads();
-  mx = part_s[0];
-  for (int w = 1; w < kGemvThreads / 32; ++w) mx = fmaxf(mx, part_s[w]);
-  float l = 0.f, acc = 0.f;
-  for (int c0 = 0; c0 < n_chunks; c0 += 1024) {
-    const int cn = min(1024, n_chunks - c0);
-    __syncthreads();
-    for (int c = t; c < cn; c += kGemvThreads) {
-      const float m = part[(c0 + c) * kPartStride];
-      w_s[c] = (m == -INFINITY) ? 0.f : __expf(m - mx);
+    for (int j = 0; j < 4; ++j) {
+      const int c = c0 + 4 * j;
+      mc[j] = c < n_chunks ? part[c * kPartStride] : -INFINITY;
+      lc[j] = c < n_chunks ? part[c * kPartStride + 1] : 0.f;
+      ac[j] = c < n_chunks ? part[c * kPartStride + 4 + o] : 0.f;
     }
-    __syncthreads();
-    for (int c = q; c < cn; c += 4) {
-      const float w = w_s[c];
-      l = fmaf(w, part[(c0 + c) * kPartStride + 1], l);
-      acc = fmaf(w, part[(c0 + c) * kPartStride + 4 + o], acc);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (mc[j] == -INFINITY) continue;
+      const float mn = fmaxf(m, mc[j]);
+      const float so = m == -INFINITY ? 0.f : __expf(m - mn), sn = __expf(mc[j] - mn);
+      l = fmaf(l, so, lc[j] * sn);
+      acc = fmaf(acc, so, ac[j] * sn);
+      m = mn;
     }
   }
   red_s[q * kDim + o] = acc;
-  if (o == 0) lred_s[q] = l;
+  if (o == 0) {
+    ml_s[0][q] = m;
+    ml_s[1][q] = l;
+  }
   __syncthreads();
-  const float lt = (lred_s[0] + lred_s[1]) + (lred_s[2] + lred_s[3]);
-  const float at = (red_s[o] + red_s[kDim + o]) + (red_s[2 * kDim + o] + red_s[3 * kDim + o]);
-  __syncthreads();
-  if (q == 0) o_s[o] = lt > 0.f ? at / lt : 0.f;
+  if (q == 0) {
+    float mt = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) mt = fmaxf(mt, ml_s[0][c]);
+    float lt = 0.f, at = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float w = ml_s[0][c] == -INFINITY ? 0.f : __expf(ml_s[0][c] - mt);
+      lt = fmaf(w, ml_s[1][c], lt);
+      at = fmaf(w, red_s[c * kDim + o], at);
+    }
+    o_s[o] = lt > 0.f ? at / lt : 0.f;
+  }
   __syncthreads();
   const float out = gemv<kGemvThreads>(a.R, o_s, red_s);
   if (q == 0) a.out[static_cast<long long>(vec) * kDim + o] = out;
