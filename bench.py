@@ -32,6 +32,7 @@ if ROOT not in sys.path:
 
 L2_BYTES = 129 * 10 ** 6
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 METRIC = "decode attention tokens/s over the packed 3-bit KV cache"
 
 
@@ -146,6 +147,69 @@ def hbm_peak():
             return float(json.load(fh)["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def bf16_peak():
+    """Burst bf16 dense tensor TFLOP/s (a kernel timed alone), measured or fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def measure_prefill_quantize(steps, warmup):
+    """Secondary figure: quantize-append throughput of a prefill of 32768 tokens
+    x 8 KV heads (bf16, 3-bit keys = 2 MSE bits + QJL, 3-bit values), two
+    input copies rotated so the 128 MB of inputs are read from HBM."""
+    import numpy as np
+    import torch
+
+    from online_kv_cache_tq_gb300 import binding as B
+    from online_kv_cache_tq_gb300 import cache as C
+    from online_kv_cache_tq_gb300 import workloads as W
+    cfg = W.CONFIGS["c3_prefill_quantize"]
+    n_tok, n_kv = cfg["tokens"], cfg["n_kv"]
+    book = B.Codebook(k_bits=3, v_bits=3, qjl_m=cfg["qjl_m"], seed=cfg["seed"], block_size=cfg["block_size"],
+                      device=torch.cuda.current_device())
+    g = torch.Generator(device="cuda")
+    g.manual_seed(cfg["seed"])
+    inputs = [(W.student_t_tokens(n_tok, n_kv, cfg["student_t_channels"], torch.bfloat16, "cuda", g, 2 * i),
+               W.student_t_tokens(n_tok, n_kv, cfg["student_t_channels"], torch.bfloat16, "cuda", g, 2 * i + 1))
+              for i in range(2)]
+    cache = C.allocate_cache(book, n_tok // cfg["block_size"], n_kv)
+    view = C.cache_view(book, cache)
+    slots = torch.arange(n_tok, device="cuda", dtype=torch.int64)
+
+    def append(i):
+        k, v = inputs[i % 2]
+        B.tq_quantize_append(book, k, v, B.TQ_BF16, n_tok, n_kv, slots, view)
+
+    for i in range(warmup):
+        append(i)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(steps):
+        append(i)
+    end.record()
+    torch.cuda.synchronize()
+    if B.tq_get_last_device_error(book):
+        raise RuntimeError("device error during the prefill quantize measurement")
+    secs = start.elapsed_time(end) * 1e-3 / steps
+    vectors = 2 * n_tok * n_kv
+    field = C.cache_bytes_per_token_head(book)
+    nbytes = vectors * 256 + n_tok * n_kv * field            # bf16 reads + packed writes
+    flops = n_tok * n_kv * (2 * 32768) + n_tok * n_kv * 32768  # K: rotation + QJL, V: rotation
+    hbm, _ = hbm_peak()
+    tensor, tensor_src = bf16_peak()
+    return {"workload": "c3_prefill_quantize", "tokens": n_tok, "n_kv_heads": n_kv, "k_bits": 3, "v_bits": 3,
+            "ms_per_append": secs * 1e3, "vectors_per_s": vectors / secs,
+            "hbm_gbs": nbytes / secs / 1e9, "hbm_frac": nbytes / secs / 1e9 / hbm,
+            "algorithmic_tflops": flops / secs / 1e12, "tensor_frac": flops / secs / 1e12 / tensor,
+            "tensor_peak": tensor, "tensor_peak_source": tensor_src + " bf16_tflops",
+            "note": "algorithmic flops; the bf16 hi/lo splitting runs 2 (rotation) and 3 (QJL) tensor passes"}
 
 
 def source_digest(rel):
@@ -315,13 +379,14 @@ def run_ours(args, rank, world, local_rank):
     dev = "cuda" if world > 1 else "cpu"
     max_ms = max_over_ranks(total_ms, dev)
     max_attn = max_over_ranks(attn_ms, dev)
+    quant = measure_prefill_quantize(20, 3)
     e2e = None
     if not args.no_e2e:
         secs, h2d, d2h = wl.e2e(args.steps, min(args.warmup, 5))
         secs = max_over_ranks(secs, dev)
         e2e = {"value": world * wl.batch * args.steps / secs, "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-    return wl, max_ms, max_attn, clock_info, e2e
+    return wl, max_ms, max_attn, clock_info, e2e, quant
 
 
 # ----------------------------------------------------- oracle (reference) --
@@ -437,7 +502,7 @@ def main(argv=None):
     if rank == 0 and not args.no_cpu_baseline:
         pool, procs = oracle_pool()         # spawned before any GPU work
     init_ranks("nccl" if world > 1 else "gloo")
-    wl, max_ms, attn_ms, clock_info, e2e = run_ours(args, rank, world, local_rank)
+    wl, max_ms, attn_ms, clock_info, e2e, quant = run_ours(args, rank, world, local_rank)
     if rank != 0:
         return 0
     ms_per_step = max_ms / args.steps
@@ -459,6 +524,7 @@ def main(argv=None):
         "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clock_info,
         "e2e": e2e,
+        "prefill_quantize": quant,
     }
     if pool is not None:
         value, groups = oracle_throughput(args.workload, args.cpu_groups, 7, pool, procs)
