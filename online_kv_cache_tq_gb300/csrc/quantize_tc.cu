@@ -18,13 +18,18 @@
 // with warp shuffles and stored as whole words when the 32 slots are
 // contiguous and aligned (prefill), or set bit by bit with atomics otherwise.
 //
-// One persistent CTA per SM, 6 warps:
+// One persistent CTA per SM, 18 warps:
 //   warp 0      TMA producer: R/S' hi/lo once, then 128-token tiles of X;
 //   warp 1      tcgen05.mma issuer (and owner of the tensor-memory columns);
-//   warps 2..5  epilogue, one thread per vector (tensor-memory lane): norm from
-//               the X tile, codes and bit-planes from Y, residual hi/lo written
-//               back to shared memory as the A operand of the second product,
-//               then the QJL signs from Z.
+//   warps 2..17 epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. +31
+//               (one vector per lane) and the 32 columns 32 g .. 32 g + 31,
+//               g = (w - 2) / 4, so four threads share a vector and each
+//               takes 32 of its coordinates: the norm and the residual norm
+//               are summed over the four in shared memory; codes, bit-plane
+//               words, residual hi/lo for the second product and QJL sign
+//               words are per 32 coordinates.
+// The accumulators are double-buffered in tensor memory, so the products of
+// the next tile run while the epilogue works on the current one.
 // Operands sit in shared memory in the 128-byte swizzled K-major layout that
 // TMA writes and tcgen05 descriptors read (two 64-column K blocks per matrix).
 // Every mbarrier wait is bounded in time; on a timeout the CTA records an
@@ -42,7 +47,9 @@ constexpr int kTileRows = 128;
 constexpr int kKBlock = 64;                       // bf16 columns per 128-byte swizzle row
 constexpr int kHalfBytes = kTileRows * 128;       // one K block of a 128-row operand: 16 KB
 constexpr int kMatBytes = 2 * kHalfBytes;         // one 128 x 128 bf16 operand: 32 KB
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 16;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 64 + kEpiThreads;
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, 128);
 
 template <bool QJL>
@@ -53,7 +60,8 @@ struct Layout {
   static constexpr int kX0 = kW * kMatBytes;
   static constexpr int kRes0 = kX0 + kStages * kMatBytes;
   static constexpr int kBytes = kRes0 + (QJL ? 2 * kMatBytes : 0);
-  static constexpr uint32_t kTmemCols = QJL ? 256 : 128;
+  static constexpr uint32_t kBufCols = QJL ? 256 : 128;     // Y (+ Z) of one tile
+  static constexpr uint32_t kTmemCols = 2 * kBufCols;        // two tiles in flight
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -78,6 +86,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// Barrier of the epilogue warps only (named barrier 1) that also ORs a flag
+// over them, so that every epilogue thread takes the same exit decision.
+__device__ __forceinline__ bool epi_sync_any(bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(flag)), "n"(kEpiThreads)
+      : "memory");
+  return r != 0;
+}
+
+// Byte offset, within an X tile, of the first 16-byte chunk that the thread of
+// coordinate group g reads from row `row` (K block g / 2, chunk (g % 2) * 4,
+// 128-byte swizzle).
+__device__ __forceinline__ int x_partial_offset(int g, int row) {
+  return (g >> 1) * kHalfBytes + row * 128 + ((((g & 1) * 4) ^ (row & 7)) << 4);
+}
+
 template <int BITS, bool QJL, bool TRANS>
 __global__ void __launch_bounds__(kThreads, 1)
     quantize_tc_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map,
@@ -85,8 +112,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Layout<QJL>;
   constexpr int kLevels = 1 << BITS;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t w_full, x_full[L::kStages], x_empty[L::kStages], y_full, y_empty, res_full,
-      z_full, drain;
+  // y_full / z_full: the products of a tile's buffer are in tensor memory;
+  // y_empty: the epilogue read that buffer (its second product, if any, too)
+  __shared__ __align__(8) uint64_t w_full, x_full[L::kStages], x_empty[L::kStages], y_full[2], y_empty[2],
+      res_full, z_full[2], drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
   __shared__ float lev_s[kMaxLevels];
@@ -104,12 +133,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(&w_full, 1);
     for (int s = 0; s < L::kStages; ++s) {
       ptx::mbar_init(&x_full[s], 1);
-      ptx::mbar_init(&x_empty[s], 128);
+      ptx::mbar_init(&x_empty[s], kEpiThreads);
     }
-    ptx::mbar_init(&y_full, 1);
-    ptx::mbar_init(&y_empty, 128);
-    ptx::mbar_init(&res_full, 128);
-    ptx::mbar_init(&z_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&y_full[b], 1);
+      ptx::mbar_init(&y_empty[b], kEpiThreads);
+      ptx::mbar_init(&z_full[b], 1);
+    }
+    ptx::mbar_init(&res_full, kEpiThreads);
     ptx::mbar_init(&drain, 1);
     ptx::fence_mbar_init();
   }
@@ -159,8 +190,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++it) {
         const int s = it % L::kStages;
         const uint32_t ph = (it / L::kStages) & 1;
+        const int buf = it & 1;
+        const uint32_t yb = tmem + buf * L::kBufCols;
         if (!ptx::wait_bar(&x_full[s], ph, abort, a.error, kErrTimeout)) break;
-        if (!ptx::wait_bar(&y_empty, (it & 1) ^ 1, abort, a.error, kErrTimeout)) break;
+        // the buffer's previous tile (it - 2) has been read by the epilogue
+        if (!ptx::wait_bar(&y_empty[buf], ((it >> 1) & 1) ^ 1, abort, a.error, kErrTimeout)) break;
         ptx::tc_fence_after();
         const uint32_t x_base = ptx::smem_u32(smem + L::kX0 + s * kMatBytes);
         uint32_t acc = 0;
@@ -171,13 +205,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               const uint32_t off = kb * kHalfBytes + ks * 32;
-              ptx::mma_bf16(tmem, ptx::desc_k_sw128(x_base + off),
+              ptx::mma_bf16(yb, ptx::desc_k_sw128(x_base + off),
                             ptx::desc_k_sw128(w_base + pass * kMatBytes + off), kIdesc, acc);
               acc = 1;
             }
           }
         }
-        ptx::mma_commit(&y_full);
+        ptx::mma_commit(&y_full[buf]);
         if (QJL) {
           if (!ptx::wait_bar(&res_full, it & 1, abort, a.error, kErrTimeout)) break;
           ptx::tc_fence_after();
@@ -193,13 +227,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks) {
                 const uint32_t off = kb * kHalfBytes + ks * 32;
-                ptx::mma_bf16(tmem + 128, ptx::desc_k_sw128(res_base + a_sel * kMatBytes + off),
+                ptx::mma_bf16(yb + 128, ptx::desc_k_sw128(res_base + a_sel * kMatBytes + off),
                               ptx::desc_k_sw128(w_base + b_sel * kMatBytes + off), kIdesc, acc);
                 acc = 1;
               }
             }
           }
-          ptx::mma_commit(&z_full);
+          ptx::mma_commit(&z_full[buf]);
         }
       }
       if (*abort) {
@@ -208,8 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue: one thread per vector ----------------
+    // ---------------- epilogue: four threads per vector, 32 coordinates each ----------------
     const int quarter = warp & 3;                 // tensor-memory lanes this warp may access
+    const int g = (warp - 2) >> 2;                // its coordinate group: 32 g .. 32 g + 31
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     float bnd[kLevels - 1];
@@ -220,18 +255,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
       const int s = it % L::kStages;
       const uint32_t ph = (it / L::kStages) & 1;
+      const int buf = it & 1;
+      const uint32_t yb = lane_addr + buf * L::kBufCols;
       bool ok = ptx::wait_bar(&x_full[s], ph, abort, a.error, kErrTimeout);
-      ok = ok && ptx::wait_bar(&y_full, it & 1, abort, a.error, kErrTimeout);
-      if (!__all_sync(0xffffffffu, ok)) break;    // tcgen05.ld below needs the whole warp
-      // norm from the bf16 X row (swizzled: 16-byte chunk c of a row sits at c ^ (row % 8))
-      const uint8_t* xrow = smem + L::kX0 + s * kMatBytes + row * 128;
+      // the partial norm from this group's 32 bf16 coordinates of the X row
+      // (K block g / 2, 16-byte chunks (g % 2) * 4 .. + 3, chunk c of a row at c ^ (row % 8))
+      uint8_t* const x_tile = smem + L::kX0 + s * kMatBytes;
+      const uint8_t* xrow = x_tile + (g >> 1) * kHalfBytes + row * 128;
       float ss = 0.f;
+      if (ok) {
 #pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 q = *reinterpret_cast<const uint4*>(xrow + kb * kHalfBytes + ((c ^ (row & 7)) << 4));
-          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        for (int q = 0; q < 4; ++q) {
+          const int c = (g & 1) * 4 + q;
+          const uint4 v = *reinterpret_cast<const uint4*>(xrow + ((c ^ (row & 7)) << 4));
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float lo = bf16_lo(w[e]), hi = bf16_hi(w[e]);
@@ -240,8 +277,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      ok = ok && ptx::wait_bar(&y_full[buf], (it >> 1) & 1, abort, a.error, kErrTimeout);
+      // Once the products have read X, the first 4 bytes this thread read carry
+      // its partial sum to the other three threads of the row (no other thread
+      // reads those bytes, and the stage is refilled only after all have read).
+      if (ok) *reinterpret_cast<float*>(x_tile + x_partial_offset(g, row)) = ss;
+      // a failed wait anywhere ends every epilogue warp (the tcgen05.ld below
+      // needs whole warps, the barriers below all 16)
+      if (epi_sync_any(!ok || *abort)) break;
+      const float n = sqrtf((*reinterpret_cast<const float*>(x_tile + x_partial_offset(0, row)) +
+                             *reinterpret_cast<const float*>(x_tile + x_partial_offset(1, row))) +
+                            (*reinterpret_cast<const float*>(x_tile + x_partial_offset(2, row)) +
+                             *reinterpret_cast<const float*>(x_tile + x_partial_offset(3, row))));
+      ptx::fence_async_shared();                  // the generic write above, before TMA refills the stage
       ptx::mbar_arrive(&x_empty[s]);
-      const float n = sqrtf(ss);
       const float inv = n > 0.f ? 1.f / n : 0.f;
 
       const int head = tile / n_tt;
@@ -254,22 +303,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const long long blk = slot / a.block_size;
           dst = (blk * a.n_kv + head) * a.block_size + (slot - blk * a.block_size);
         } else if (slot >= cache_rows) {
-          atomicCAS(a.error, 0, kErrSlot);
+          if (g == 0) atomicCAS(a.error, 0, kErrSlot);
           slot = -1;
         }
       }
 
       ptx::tc_fence_after();
-      uint32_t planes[BITS][4];
+      uint32_t planes[BITS];
       float rs = 0.f;
-      uint8_t* res_hi = smem + L::kRes0 + row * 128;
-      uint8_t* res_lo = res_hi + kMatBytes;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      {
         uint32_t yr[32];
-        ptx::tmem_ld32(lane_addr + c * 32, yr);
+        ptx::tmem_ld32(yb + 32 * g, yr);
 #pragma unroll
-        for (int p = 0; p < BITS; ++p) planes[p][c] = 0;
+        for (int p = 0; p < BITS; ++p) planes[p] = 0;
         float r[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -279,18 +325,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < kLevels - 1; ++i) code += (y > bnd[i]) ? 1 : 0;
 #pragma unroll
-          for (int p = 0; p < BITS; ++p) planes[p][c] |= static_cast<uint32_t>((code >> p) & 1) << j;
+          for (int p = 0; p < BITS; ++p) planes[p] |= static_cast<uint32_t>((code >> p) & 1) << j;
           if (QJL) {
             r[j] = fmaf(-n, lev_s[code], yv);
             rs = fmaf(r[j], r[j], rs);
           }
         }
         if (QJL) {
-          // 32 coordinates = 4 chunks of 8 in K block c/2, chunks (c%2)*4 .. +3
+          // 32 coordinates = 4 chunks of 8 in K block g / 2, chunks (g % 2) * 4 .. + 3
+          uint8_t* res_hi = smem + L::kRes0 + (g >> 1) * kHalfBytes + row * 128;
+          uint8_t* res_lo = res_hi + kMatBytes;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int chunk = (c & 1) * 4 + q;
-            const int off = (c >> 1) * kHalfBytes + ((chunk ^ (row & 7)) << 4);
+            const int chunk = (g & 1) * 4 + q;
+            const int off = (chunk ^ (row & 7)) << 4;
             uint32_t hw[4], lw[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -303,8 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&y_empty);
+      if (!QJL) {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&y_empty[buf]);          // this buffer may take the tile after next
+      }
       if (TRANS) {
         // token-transposed codes: whole words when the warp's 32 slots are
         // contiguous and start a 32-token group, single bits otherwise
@@ -316,49 +366,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int off0 = static_cast<int>(slot0 - blk * a.block_size);
 #pragma unroll
           for (int p = 0; p < BITS; ++p)
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              words[transposed_word(blk, head, a.n_kv, BITS, p, 32 * c + lane, a.block_size, off0)] =
-                  transpose32(planes[p][c], lane);
+            words[transposed_word(blk, head, a.n_kv, BITS, p, 32 * g + lane, a.block_size, off0)] =
+                transpose32(planes[p], lane);
         } else if (dst >= 0) {
           const long long blk = slot / a.block_size;
           const int off = static_cast<int>(slot - blk * a.block_size);
           const unsigned mask = 1u << (off & 31);
           for (int p = 0; p < BITS; ++p)
-            for (int c = 0; c < 4; ++c)
-              for (int j = 0; j < 32; ++j) {
-                unsigned* w = words + transposed_word(blk, head, a.n_kv, BITS, p, 32 * c + j, a.block_size, off);
-                if ((planes[p][c] >> j) & 1) atomicOr(w, mask); else atomicAnd(w, ~mask);
-              }
+            for (int j = 0; j < 32; ++j) {
+              unsigned* w = words + transposed_word(blk, head, a.n_kv, BITS, p, 32 * g + j, a.block_size, off);
+              if ((planes[p] >> j) & 1) atomicOr(w, mask); else atomicAnd(w, ~mask);
+            }
         }
       } else if (dst >= 0) {
-        uint4* out = reinterpret_cast<uint4*>(a.codes + dst * (BITS * 16));
+        uint32_t* out = reinterpret_cast<uint32_t*>(a.codes + dst * (BITS * 16));
 #pragma unroll
-        for (int p = 0; p < BITS; ++p) out[p] = make_uint4(planes[p][0], planes[p][1], planes[p][2], planes[p][3]);
+        for (int p = 0; p < BITS; ++p) out[p * 4 + g] = planes[p];
       }
-      if (dst >= 0) a.norm[dst] = n;
+      if (dst >= 0 && g == 0) a.norm[dst] = n;
       if (QJL) {
         ptx::fence_async_shared();
         ptx::mbar_arrive(&res_full);
-        const bool zok = ptx::wait_bar(&z_full, it & 1, abort, a.error, kErrTimeout);
-        if (!__all_sync(0xffffffffu, zok)) break;
+        const bool zok = ptx::wait_bar(&z_full[buf], (it >> 1) & 1, abort, a.error, kErrTimeout);
+        // the second products are done with the residual tile: its first 2 KB
+        // carry the partial residual norms until the next tile's first barrier
+        float* const rs_x = reinterpret_cast<float*>(smem + L::kRes0);
+        if (zok) rs_x[g * kTileRows + row] = rs;
+        if (epi_sync_any(!zok)) break;
         ptx::tc_fence_after();
-        uint32_t sw[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t zr[32];
-          ptx::tmem_ld32(lane_addr + 128 + c * 32, zr);
-          uint32_t word = 0;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) word |= (__uint_as_float(zr[j]) > 0.f ? 1u : 0u) << j;
-          sw[c] = word;
-        }
+        uint32_t zr[32];
+        ptx::tmem_ld32(yb + 128 + 32 * g, zr);
         ptx::tc_fence_before();
+        ptx::mbar_arrive(&y_empty[buf]);          // this buffer (Y and Z) may take the tile after next
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) word |= (__uint_as_float(zr[j]) > 0.f ? 1u : 0u) << j;
         if (dst >= 0) {
-          *reinterpret_cast<uint4*>(a.qjl + dst * 16) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
-          a.rnorm[dst] = sqrtf(rs);
+          reinterpret_cast<uint32_t*>(a.qjl + dst * 16)[g] = word;
+          if (g == 0)
+            a.rnorm[dst] = sqrtf((rs_x[row] + rs_x[kTileRows + row]) + (rs_x[2 * kTileRows + row] + rs_x[3 * kTileRows + row]));
         }
       }
+      // No barrier closes the tile: the residual tile is rewritten only after
+      // the next tile's first barrier, which a thread passes once every thread
+      // has read this tile's partial residual norms.
     }
   }
 
