@@ -98,6 +98,39 @@ __device__ __forceinline__ bool epi_sync_any(bool flag) {
   return r != 0;
 }
 
+// The bits of code = #{i : t_i < y} for non-decreasing boundaries t (the
+// Lloyd-Max midpoints are), found by binary search from the top bit: with the
+// bits above p forming the prefix k, code >= c holds exactly when y > t[c - 1],
+// so bit p is y > t[k 2^(p+1) + 2^p - 1]. The candidates of each level are
+// narrowed by the bits already found, lowest first, with selects only.
+template <int BITS>
+__device__ __forceinline__ void code_bits(float y, const float (&t)[(1 << BITS) - 1], bool (&b)[BITS]) {
+#pragma unroll
+  for (int p = BITS - 1; p >= 0; --p) {
+    float cand[1 << (BITS - 1)];
+#pragma unroll
+    for (int k = 0; k < (1 << (BITS - 1 - p)); ++k) cand[k] = t[(2 * k + 1) * (1 << p) - 1];
+#pragma unroll
+    for (int q = p + 1; q < BITS; ++q)
+#pragma unroll
+      for (int k = 0; k < (1 << (BITS - 1 - q)); ++k) cand[k] = b[q] ? cand[2 * k + 1] : cand[2 * k];
+    b[p] = y > cand[0];
+  }
+}
+
+// levels[code] for the code whose bits are b, by selects (lowest bit first).
+template <int BITS>
+__device__ __forceinline__ float level_of(const float (&levels)[1 << BITS], const bool (&b)[BITS]) {
+  float cand[1 << BITS];
+#pragma unroll
+  for (int k = 0; k < (1 << BITS); ++k) cand[k] = levels[k];
+#pragma unroll
+  for (int q = 0; q < BITS; ++q)
+#pragma unroll
+    for (int k = 0; k < (1 << (BITS - 1 - q)); ++k) cand[k] = b[q] ? cand[2 * k + 1] : cand[2 * k];
+  return cand[0];
+}
+
 // Byte offset, within an X tile, of the first 16-byte chunk that the thread of
 // coordinate group g reads from row `row` (K block g / 2, chunk (g % 2) * 4,
 // 128-byte swizzle).
@@ -118,7 +151,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       res_full, z_full[2], drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
-  __shared__ float lev_s[kMaxLevels];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x;
@@ -144,7 +176,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(&drain, 1);
     ptx::fence_mbar_init();
   }
-  if (tid < kMaxLevels) lev_s[tid] = tid < kLevels ? a.levels[tid] : 0.f;
   if (warp == 1) {
     ptx::tmem_alloc(&tmem_base_s, L::kTmemCols);
     ptx::tmem_relinquish();
@@ -250,13 +281,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     float bnd[kLevels - 1];
 #pragma unroll
     for (int i = 0; i < kLevels - 1; ++i) bnd[i] = a.bounds[i];
+    float lev[kLevels];                           // read only by the QJL residual
+#pragma unroll
+    for (int i = 0; i < kLevels; ++i) lev[i] = QJL ? a.levels[i] : 0.f;
     const long long cache_rows = static_cast<long long>(a.num_blocks) * a.block_size;
+    const bool bs_pow2 = (a.block_size & (a.block_size - 1)) == 0;
+    const int bs_shift = __ffs(a.block_size) - 1;
     int it = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
       const int s = it % L::kStages;
       const uint32_t ph = (it / L::kStages) & 1;
       const int buf = it & 1;
       const uint32_t yb = lane_addr + buf * L::kBufCols;
+
+      // destination row first: its global loads overlap the waits below
+      const int head = tile / n_tt;
+      const int token = (tile % n_tt) * kTileRows + row;
+      long long dst = -1;
+      long long slot = -1;
+      long long blk = 0;
+      if (token < a.n_tokens) {
+        slot = slot_of(a, token);
+        if (slot >= 0 && slot < cache_rows) {
+          blk = bs_pow2 ? (slot >> bs_shift) : slot / a.block_size;
+          dst = (blk * a.n_kv + head) * a.block_size + (slot - blk * a.block_size);
+        } else if (slot >= cache_rows) {
+          if (g == 0) atomicCAS(a.error, 0, kErrSlot);
+          slot = -1;
+        }
+      }
+
       bool ok = ptx::wait_bar(&x_full[s], ph, abort, a.error, kErrTimeout);
       // the partial norm from this group's 32 bf16 coordinates of the X row
       // (K block g / 2, 16-byte chunks (g % 2) * 4 .. + 3, chunk c of a row at c ^ (row % 8))
@@ -293,21 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(&x_empty[s]);
       const float inv = n > 0.f ? 1.f / n : 0.f;
 
-      const int head = tile / n_tt;
-      const int token = (tile % n_tt) * kTileRows + row;
-      long long dst = -1;
-      long long slot = -1;
-      if (token < a.n_tokens) {
-        slot = slot_of(a, token);
-        if (slot >= 0 && slot < cache_rows) {
-          const long long blk = slot / a.block_size;
-          dst = (blk * a.n_kv + head) * a.block_size + (slot - blk * a.block_size);
-        } else if (slot >= cache_rows) {
-          if (g == 0) atomicCAS(a.error, 0, kErrSlot);
-          slot = -1;
-        }
-      }
-
       ptx::tc_fence_after();
       uint32_t planes[BITS];
       float rs = 0.f;
@@ -321,13 +360,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 32; ++j) {
           const float yv = __uint_as_float(yr[j]);
           const float y = yv * inv;
-          int code = 0;
+          bool b[BITS];
+          code_bits<BITS>(y, bnd, b);
 #pragma unroll
-          for (int i = 0; i < kLevels - 1; ++i) code += (y > bnd[i]) ? 1 : 0;
-#pragma unroll
-          for (int p = 0; p < BITS; ++p) planes[p] |= static_cast<uint32_t>((code >> p) & 1) << j;
+          for (int p = 0; p < BITS; ++p) planes[p] |= b[p] ? (1u << j) : 0u;
           if (QJL) {
-            r[j] = fmaf(-n, lev_s[code], yv);
+            r[j] = fmaf(-n, level_of<BITS>(lev, b), yv);
             rs = fmaf(r[j], r[j], rs);
           }
         }
@@ -362,14 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool aligned = __all_sync(0xffffffffu, dst >= 0 && slot == slot0 + lane && (slot0 & 31) == 0);
         unsigned* words = reinterpret_cast<unsigned*>(a.codes);
         if (aligned) {
-          const long long blk = slot0 / a.block_size;
-          const int off0 = static_cast<int>(slot0 - blk * a.block_size);
+          const long long blk0 = __shfl_sync(0xffffffffu, blk, 0);
+          const int off0 = static_cast<int>(slot0 - blk0 * a.block_size);
 #pragma unroll
           for (int p = 0; p < BITS; ++p)
-            words[transposed_word(blk, head, a.n_kv, BITS, p, 32 * g + lane, a.block_size, off0)] =
+            words[transposed_word(blk0, head, a.n_kv, BITS, p, 32 * g + lane, a.block_size, off0)] =
                 transpose32(planes[p], lane);
         } else if (dst >= 0) {
-          const long long blk = slot / a.block_size;
           const int off = static_cast<int>(slot - blk * a.block_size);
           const unsigned mask = 1u << (off & 31);
           for (int p = 0; p < BITS; ++p)
