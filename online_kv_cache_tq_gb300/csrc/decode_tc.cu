@@ -326,7 +326,9 @@ __device__ __forceinline__ bool next_item(const DecodeArgs& a, int& it, int last
   return false;
 }
 
-template <int G>
+// KB, VB, QJ: key MSE bits, value bits and QJL plane (0/1) fixed at compile
+// time, or 0, 0, -1 to take them from the arguments.
+template <int G, int KB, int VB, int QJ>
 __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a, TcLayout L, int items_per_cta) {
   constexpr int N1 = score_cols(G), NO = value_cols(G);
   const int total = a.batch * a.n_kv * a.max_chunks;
@@ -335,8 +337,18 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   const int bs = a.block_size;                        // a power of two that divides kChunk
   const int bs_shift = 31 - __clz(bs);
 
+  const int k_bits = KB > 0 ? KB : a.k_bits;
+  const int v_bits = VB > 0 ? VB : a.v_bits;
+  const int pk = KB > 0 ? 1 << (KB - 1) : L.pk;     // key sign planes
+  const int pq = QJ >= 0 ? QJ : L.pq;                // QJL plane
+  const int pv = VB > 0 ? 1 << (VB - 1) : L.pv;     // value sign planes
+  const int kp = 32 * (pk + pq);                     // columns per key slot
+  const int kbytes = 16 * k_bits;                    // key code bytes per token
+  const int vblock = v_bits * 16 * bs;               // value code bytes per (block, head)
+
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned, as an offset from smem_raw so that accesses stay shared-space
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* b_mse = smem + L.off_bmse;
   uint8_t* b_qjl = smem + L.off_bqjl;
   uint8_t* b_v = smem + L.off_bv;
@@ -371,9 +383,9 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   const int half = (t >> 7) & 1;                // which of the two threads of the lane
   const int w0 = 2 * half;                      // this thread's words of every sign plane: w0, w0 + 1
   const uint32_t row_addr = static_cast<uint32_t>(((t >> 5) & 3) * 32) << 16;
-  const bool qjl = a.k_qjl != nullptr;
+  const bool qjl = QJ >= 0 ? QJ == 1 : a.k_qjl != nullptr;
   volatile int* abort = &abort_s;
-  const int n_pairs = (L.pv + 1) / 2;
+  const int n_pairs = (pv + 1) / 2;
 
   // zero the B operands once (their padding rows stay 0)
   for (int i = t; i < L.off_s0 / 16; i += kThreads) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
@@ -427,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           if (!valid) atomicCAS(a.error, 0, kErrBlock);
         }
         rows = min(bs, (x.n_local - ln * bs + 31) / 32 * 32);
-        if (valid) bytes = keys ? rows * (L.kbytes + 4 + (qjl ? 16 + 4 : 0)) : rows * 4 + L.vblock;
+        if (valid) bytes = keys ? rows * (kbytes + 4 + (qjl ? 16 + 4 : 0)) : rows * 4 + vblock;
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, off);
@@ -441,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         const long long r0 = (phys * a.n_kv + x.kvh) * bs;    // first row of this block
         const int tl0 = ln * bs;
         if (keys) {
-          ptx::bulk_load(kc_s + tl0 * L.kbytes, a.k_codes + r0 * L.kbytes, rows * L.kbytes, &kin);
+          ptx::bulk_load(kc_s + tl0 * kbytes, a.k_codes + r0 * kbytes, rows * kbytes, &kin);
           if (qjl) {
             ptx::bulk_load(kq_s + tl0 * 16, a.k_qjl + r0 * 16, rows * 16, &kin);
             ptx::bulk_load(kr_s + tl0, a.k_rnorm + r0, rows * 4, &kin);
@@ -449,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           ptx::bulk_load(kn_s + tl0, a.k_norm + r0, rows * 4, &kin);
         } else {
           ptx::bulk_load(vn_s + tl0, a.v_norm + r0, rows * 4, &vin);
-          ptx::bulk_load(vc_s + ln * (L.vblock / 4), a.v_codes + (phys * a.n_kv + x.kvh) * L.vblock, L.vblock,
+          ptx::bulk_load(vc_s + ln * (vblock / 4), a.v_codes + (phys * a.n_kv + x.kvh) * vblock, vblock,
                          &vin);
         }
       }
@@ -479,9 +491,9 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         if (ok && ktile > 0) ok = wait_phase(&sfree, (ktile - 1) & 1, abort, a.error);
         if (ok && ptx::elect_one()) {
           ptx::tc_fence_after();
-          uint32_t a_col = tmem + slot * L.kp;
+          uint32_t a_col = tmem + slot * kp;
           uint64_t dsc = desc_mse;
-          for (int s = 0; s < L.pk; ++s) {
+          for (int s = 0; s < pk; ++s) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               ptx::mma_e4m3_tmem_a(d_mse, a_col + 8 * kk, dsc + 2 * kk, idesc_s, (s | kk) != 0);
@@ -514,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             ptx::mma_e4m3_tmem_a(d_col, a_col + 8 * kk, dsc + 2 * kk, idesc_o, (tile | kk) != 0);
-          if (2 * pair + 1 < L.pv)
+          if (2 * pair + 1 < pv)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               ptx::mma_e4m3_tmem_a(d_col + L.no, a_col + 32 + 8 * kk, dsc + 2 * kk, idesc_o, (tile | kk) != 0);
@@ -558,14 +570,14 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       // a row at c ^ (n % 8)
       if (group != cur_group) {
         asm volatile("griddepcontrol.wait;" ::: "memory");   // the query operands come from the previous grid
-        const int nk = L.pk + L.pq;
+        const int nk = pk + pq;
         const int per_head = nk * kQPieces * 8;     // 16-byte chunks per head
         for (int idx = t; idx < G * per_head; idx += kBuilders) {
           const int h = idx / per_head, r = idx - h * per_head;
           const int s = r / (kQPieces * 8), i = (r / 8) % kQPieces, c = r % 8;
           const uint4 v = reinterpret_cast<const uint4*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride)[r];
           const int n = score_row(G, h, i);
-          uint8_t* dst = s < L.pk ? b_mse + s * L.n1 * 128 : b_qjl;
+          uint8_t* dst = s < pk ? b_mse + s * L.n1 * 128 : b_qjl;
           *reinterpret_cast<uint4*>(dst + n * 128 + ((c ^ (n & 7)) << 4)) = v;
         }
         // per head: 1 / sigma_mse, 1 / sigma_qjl, and the -1 halves of the +-1 sums
@@ -654,10 +666,10 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         uint32_t bw[4][2] = {};
         uint32_t sg[2] = {};
         if (valid) {
-          const uint2* kc = reinterpret_cast<const uint2*>(kc_s + tl * L.kbytes);
+          const uint2* kc = reinterpret_cast<const uint2*>(kc_s + tl * kbytes);
 #pragma unroll
           for (int p = 0; p < 4; ++p)
-            if (p < a.k_bits) {
+            if (p < k_bits) {
               const uint2 w = kc[2 * p + half];
               bw[p][0] = w.x;
               bw[p][1] = w.y;
@@ -668,8 +680,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             sg[1] = w.y;
           }
         }
-        const uint32_t base = tmem + row_addr + slot * L.kp;
-        switch (a.k_bits) {
+        const uint32_t base = tmem + row_addr + slot * kp;
+        switch (k_bits) {
           case 1: key_planes<1>(base, bw, sg, qjl, w0); break;
           case 2: key_planes<2>(base, bw, sg, qjl, w0); break;
           case 3: key_planes<3>(base, bw, sg, qjl, w0); break;
@@ -752,10 +764,10 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           const int tl = tile * kTile + 32 * (w0 + c);
           if (tl < x.n_local && blk_ok[tl >> bs_shift]) {
             const uint32_t* src =
-                vc_s + (tl >> bs_shift) * (L.vblock / 4) + ((tl & (bs - 1)) >> 5) + (lane << wpd_shift);
+                vc_s + (tl >> bs_shift) * (vblock / 4) + ((tl & (bs - 1)) >> 5) + (lane << wpd_shift);
 #pragma unroll
             for (int p = 0; p < 4; ++p)
-              if (p < a.v_bits) bw[p][c] = src[(p * 128) << wpd_shift];
+              if (p < v_bits) bw[p][c] = src[(p * 128) << wpd_shift];
           }
         }
         if (tile == x.n_tiles - 1) ptx::mbar_arrive(&vfree);   // the value fields are no longer read
@@ -773,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             if (!ok) break;
           }
           const uint32_t base = tmem + row_addr + slot * kValueSlot;
-          switch (a.v_bits) {
+          switch (v_bits) {
             case 1: value_pair<1>(base, bw, pair, w0); break;
             case 2: value_pair<2>(base, bw, pair, w0); break;
             case 3: value_pair<3>(base, bw, pair, w0); break;
@@ -801,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
 #pragma unroll
       for (int h = 0; h < G; ++h) o[h] = 0.f;
       if (ok) {
-        for (int s = half; s < L.pv; s += 2) {
+        for (int s = half; s < pv; s += 2) {
           const float ws = vw_s[s];
 #pragma unroll
           for (int c0 = 0; c0 < NO; c0 += 16) {
@@ -824,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       if (ok && half == 0) {
         const float inv_sv = 1.f / sv_s;          // exact: sv is a power of two
         float a_sum = 0.f;                        // sum_S a_S: the -1 half of every sign product
-        for (int s = 0; s < L.pv; ++s) a_sum += vw_s[s];
+        for (int s = 0; s < pv; ++s) a_sum += vw_s[s];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           float* part = a.ws_part + (static_cast<long long>(qbase + h) * a.max_chunks + x.chunk) * kPartStride;
@@ -873,8 +885,11 @@ bool tc_decode_supported(const DecodeArgs& a, bool walsh_ok) {
 template <int G>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, bool early) {
   const TcLayout l = tc_layout(G, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size);
-  cudaError_t err = cudaFuncSetAttribute(attention_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         l.smem_bytes);
+  // 3-bit keys (2 MSE bits + the QJL bit) with 3-bit values have their own
+  // build with the widths folded in; other widths are read at run time
+  const bool fixed = a.k_bits == 2 && a.v_bits == 3 && a.k_qjl != nullptr;
+  auto kernel = fixed ? attention_tc_kernel<G, 2, 3, 1> : attention_tc_kernel<G, 0, 0, -1>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem_bytes);
   if (err != cudaSuccess) return err;
   // a persistent grid: two CTAs per SM (one when the tensor memory or shared
   // memory of a CTA leaves room for one), each taking a contiguous run of
@@ -895,7 +910,7 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, bool early) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = early ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attention_tc_kernel<G>, a, l, per_cta);
+  return cudaLaunchKernelEx(&cfg, kernel, a, l, per_cta);
 }
 
 cudaError_t launch_decode_partials_tc(const DecodeArgs& a, cudaStream_t stream, bool early) {
