@@ -78,10 +78,11 @@ void free_device(tq_codebook* b) {
   cudaFree(b->d_R);
   cudaFree(b->d_Rt);
   cudaFree(b->d_Spt);
+  cudaFree(b->d_St);
   cudaFree(b->d_rot_tc);
   cudaFree(b->d_tables);
   cudaFree(b->d_error);
-  b->d_R = b->d_Rt = b->d_Spt = nullptr;
+  b->d_R = b->d_Rt = b->d_Spt = b->d_St = nullptr;
   b->d_rot_tc = nullptr;
   b->d_tables = nullptr;
   b->d_error = nullptr;
@@ -146,7 +147,7 @@ tq_status upload_tables(tq_codebook* b) {
   const int d = b->cfg.d;
   const int m = b->cfg.qjl_m;
   const tq::HostTables& h = b->host;
-  std::vector<float> R(d * d), Rt(d * d), Spt(d * d, 0.f);
+  std::vector<float> R(d * d), Rt(d * d), Spt(d * d, 0.f), St(d * d, 0.f);
   for (int i = 0; i < d; ++i) {
     for (int j = 0; j < d; ++j) {
       R[i * d + j] = static_cast<float>(h.R[i * d + j]);
@@ -154,7 +155,10 @@ tq_status upload_tables(tq_codebook* b) {
     }
   }
   for (int k = 0; k < m; ++k)
-    for (int j = 0; j < d; ++j) Spt[j * d + k] = static_cast<float>(h.Sp[k * d + j]);
+    for (int j = 0; j < d; ++j) {
+      Spt[j * d + k] = static_cast<float>(h.Sp[k * d + j]);
+      St[j * d + k] = static_cast<float>(h.S[k * d + j]);
+    }
   // bf16 hi/lo images of R and S' (row-major, [out][in]) for the tensor-core
   // quantizer: W = hi + lo with hi = bf16(W), lo = bf16(W - hi).
   std::vector<uint16_t> tc(4 * d * d, 0);
@@ -180,6 +184,7 @@ tq_status upload_tables(tq_codebook* b) {
   cudaError_t err = upload(&b->d_R, R);
   if (err == cudaSuccess) err = upload(&b->d_Rt, Rt);
   if (err == cudaSuccess) err = upload(&b->d_Spt, Spt);
+  if (err == cudaSuccess) err = upload(&b->d_St, St);
   if (err == cudaSuccess) err = upload(&b->d_rot_tc, tc);
   if (err == cudaSuccess) err = upload(&b->d_tables, tv);
   if (err == cudaSuccess) err = upload(&b->d_error, zero);
@@ -487,6 +492,7 @@ tq_status decode_args(const tq_codebook* book, int stages, const void* q, tq_dty
   a->R = book->d_R;
   a->Rt = book->d_Rt;
   a->Spt = book->d_Spt;
+  a->St = book->d_St;
   a->tables = book->d_tables;
   a->error = book->d_error;
   a->num_sms = book->num_sms;

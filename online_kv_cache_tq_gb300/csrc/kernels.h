@@ -91,6 +91,7 @@ struct DecodeArgs {
   const float* R;           // [128][128] row-major
   const float* Rt;
   const float* Spt;
+  const float* St;          // [128][128], St[i][k] = S[k][i]: the projected query S' R q = S q
   const DeviceTables* tables;
   int* error;
   int num_sms;              // of the handle's device

@@ -60,6 +60,7 @@ struct tq_codebook {
   float* d_R;         // [d][d] row-major R
   float* d_Rt;        // [d][d] R transposed
   float* d_Spt;       // [d][m] S' transposed (column k of S' is row k)
+  float* d_St;        // [d][m] S transposed: S q = S' R q for a query q
   uint16_t* d_rot_tc; // bf16 hi/lo operand images for the tensor-core quantizer
   tq::DeviceTables* d_tables;
   int* d_error;       // first device-side error code, 0 when none

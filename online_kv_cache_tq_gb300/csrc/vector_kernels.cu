@@ -18,6 +18,8 @@
 namespace tq {
 namespace {
 
+constexpr int kQueriesPerCta = 2;   // query heads prepared by one block
+
 __device__ __forceinline__ float load_elem(const void* base, long long idx, bool bf16) {
   if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
   return reinterpret_cast<const float*>(base)[idx];
@@ -88,32 +90,52 @@ __device__ __forceinline__ void quantize_vector(const QuantizeArgs& a, int v, bo
 }
 
 
-// Query head vec: ws_q[vec] = (R q, S' R q); with ws_bk, also the tensor-core score operand
-// of this query head: e4m3 pieces of 2 sigma_0 a_S (R q)_j / beta_j per key
-// sign plane S and of 2 sigma_1 (S' R q)_j / beta_j (sigma_0, sigma_1 powers
-// of two that bound the pieces; beta_j the bit scale of coordinate j), and the
-// sums that turn the 0/1 bit products into +-1 sign products.  256 threads:
-// thread (o, q) works on coordinate o; the two copies of o split the
-// matrix-vector products and the piece planes.
-__device__ __forceinline__ void prepare_query(const DecodeArgs& a, int vec, bool bf16) {
-  __shared__ float q_s[kDim];
-  __shared__ float qr_s[kDim];
-  __shared__ float red_s[4 * kDim];
-  __shared__ float part_s[4];
-  const int o = threadIdx.x & 127, qq = threadIdx.x >> 7;
-  const bool lead = qq == 0;
-  if (lead) q_s[o] = load_elem(a.q, static_cast<long long>(vec) * kDim + o, bf16);
-  __syncthreads();
-  const float acc = gemv<kVecThreads>(a.Rt, q_s, red_s);
-  if (lead) {
-    qr_s[o] = acc;
-    a.ws_q[static_cast<long long>(vec) * 2 * kDim + o] = acc;
+// Query heads v0 .. v0 + nv - 1 (nv <= kQueriesPerCta; consecutive heads
+// share every matrix load): ws_q[v] = (R q, S' R q), the projection taken as
+// S q since S' = S R^T; with ws_bk, also each head's tensor-core score
+// operand: e4m3 pieces of 2 sigma_0 a_S (R q)_j / beta_j per key sign plane S
+// and of 2 sigma_1 (S q)_j / beta_j (sigma_0, sigma_1 powers of two that bound
+// the pieces; beta_j the bit scale of coordinate j), and the sums that turn
+// the 0/1 bit products into +-1 sign products.  256 threads: thread (o, m)
+// computes coordinate o of R q (m = 0) or of S q (m = 1) for every head, so
+// the two products run side by side.
+__device__ __forceinline__ void prepare_queries(const DecodeArgs& a, int v0, int nv, bool bf16) {
+  constexpr int QN = kQueriesPerCta;
+  __shared__ __align__(16) float q_s[QN][kDim];
+  __shared__ float stat_s[2][4][2 * QN];        // [m][warp]: max, then sum, per head
+  const int o = threadIdx.x & 127, m = threadIdx.x >> 7;
+  const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) & 3;
+  for (int i = threadIdx.x; i < QN * kDim; i += kVecThreads) {
+    const int j = i >> 7;
+    q_s[j][i & 127] = j < nv ? load_elem(a.q, static_cast<long long>(v0) * kDim + i, bf16) : 0.f;
   }
   __syncthreads();
-  float z = 0.f;
-  if (a.qjl_m > 0) {
-    z = gemv<kVecThreads>(a.Spt, qr_s, red_s);
-    if (lead) a.ws_q[static_cast<long long>(vec) * 2 * kDim + kDim + o] = z;
+  const bool proj = m == 1;
+  const bool active = !proj || a.qjl_m > 0;
+  float acc[QN];
+#pragma unroll
+  for (int j = 0; j < QN; ++j) acc[j] = 0.f;
+  if (active) {
+    const float* w = (proj ? a.St : a.Rt) + o;
+#pragma unroll
+    for (int k0 = 0; k0 < kDim; k0 += 32) {
+      float v[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = __ldg(w + (k0 + k) * kDim);
+#pragma unroll
+      for (int k = 0; k < 32; k += 4)
+#pragma unroll
+        for (int j = 0; j < QN; ++j) {
+          const float4 x = *reinterpret_cast<const float4*>(&q_s[j][k0 + k]);
+          acc[j] = fmaf(v[k], x.x, acc[j]);
+          acc[j] = fmaf(v[k + 1], x.y, acc[j]);
+          acc[j] = fmaf(v[k + 2], x.z, acc[j]);
+          acc[j] = fmaf(v[k + 3], x.w, acc[j]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < QN; ++j)
+      if (j < nv) a.ws_q[static_cast<long long>(v0 + j) * 2 * kDim + m * kDim + o] = acc[j];
   }
   if (a.ws_bk == nullptr) return;
   const int planes = 1 << (a.k_bits - 1);
@@ -123,27 +145,51 @@ __device__ __forceinline__ void prepare_query(const DecodeArgs& a, int vec, bool
     asum += a.tables->k_walsh[s];
   }
   const float ib = 2.f * bit_inv_scale(o);
-  const float sig0 = piece_scale(max128(fabsf(acc) * amax * ib, part_s));
-  const float sig1 = piece_scale(max128(fabsf(z) * ib, part_s));
-  const float sum_qr = sum128(acc, part_s), sum_qs = sum128(z, part_s);
-  uint8_t* dst = a.ws_bk + static_cast<long long>(vec) * a.bk_stride;
-  const int kpos = k_position(o);
-  // plane s (s == planes: the QJL operand) by the copy qq == s % copies
-  const int items = planes + (a.qjl_m > 0 ? 1 : 0);
-  for (int s = qq; s < items; s += kVecThreads / 128) {
-    const float y = s < planes ? a.tables->k_walsh[s] * acc * ib * sig0 : z * ib * sig1;
-    write_pieces_rows<kQPieces>(dst + s * kQPieces * 128, kpos, y);
+  // per head: max of the scaled magnitudes (sigma) and sum of the coordinates
+  float red[2 * QN];
+#pragma unroll
+  for (int j = 0; j < QN; ++j) {
+    red[j] = fabsf(acc[j]) * (proj ? ib : amax * ib);
+    red[QN + j] = acc[j];
   }
-  if (threadIdx.x == 0) {
-    float* hdr = reinterpret_cast<float*>(dst + items * kQPieces * 128);
-    hdr[0] = sig0;
-    hdr[1] = sig1;
-    hdr[2] = 1.f / sig0;      // exact: powers of two
-    hdr[3] = 1.f / sig1;
-    hdr[4] = asum * sum_qr;   // sum_S a_S <q_rot, 1>: the -1 half of every sign
-    hdr[5] = sum_qs;
-    hdr[6] = 0.f;
-    hdr[7] = 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+    for (int j = 0; j < 2 * QN; ++j) {
+      const float u = __shfl_xor_sync(0xffffffffu, red[j], off);
+      red[j] = j < QN ? fmaxf(red[j], u) : red[j] + u;
+    }
+  if (lane == 0)
+#pragma unroll
+    for (int j = 0; j < 2 * QN; ++j) stat_s[m][warp][j] = red[j];
+  __syncthreads();
+  const int kpos = k_position(o);
+  const int items = planes + (a.qjl_m > 0 ? 1 : 0);
+#pragma unroll
+  for (int j = 0; j < QN; ++j) {
+    if (j >= nv) break;
+    const float sig0 = piece_scale(fmaxf(fmaxf(stat_s[0][0][j], stat_s[0][1][j]), fmaxf(stat_s[0][2][j], stat_s[0][3][j])));
+    const float sig1 = piece_scale(fmaxf(fmaxf(stat_s[1][0][j], stat_s[1][1][j]), fmaxf(stat_s[1][2][j], stat_s[1][3][j])));
+    uint8_t* dst = a.ws_bk + static_cast<long long>(v0 + j) * a.bk_stride;
+    if (!proj) {
+      for (int s = 0; s < planes; ++s)
+        write_pieces_rows<kQPieces>(dst + s * kQPieces * 128, kpos, a.tables->k_walsh[s] * acc[j] * ib * sig0);
+    } else if (a.qjl_m > 0) {
+      write_pieces_rows<kQPieces>(dst + planes * kQPieces * 128, kpos, acc[j] * ib * sig1);
+    }
+    if (threadIdx.x == 0) {
+      const float sum_qr = (stat_s[0][0][QN + j] + stat_s[0][1][QN + j]) + (stat_s[0][2][QN + j] + stat_s[0][3][QN + j]);
+      const float sum_qs = (stat_s[1][0][QN + j] + stat_s[1][1][QN + j]) + (stat_s[1][2][QN + j] + stat_s[1][3][QN + j]);
+      float* hdr = reinterpret_cast<float*>(dst + items * kQPieces * 128);
+      hdr[0] = sig0;
+      hdr[1] = sig1;
+      hdr[2] = 1.f / sig0;      // exact: powers of two
+      hdr[3] = 1.f / sig1;
+      hdr[4] = asum * sum_qr;   // sum_S a_S <q_rot, 1>: the -1 half of every sign
+      hdr[5] = sum_qs;
+      hdr[6] = 0.f;
+      hdr[7] = 0.f;
+    }
   }
 }
 
@@ -227,11 +273,13 @@ __global__ void __launch_bounds__(kVecThreads) quantize_small_kernel(QuantizeArg
 }
 
 __global__ void __launch_bounds__(kVecThreads) qprep_kernel(DecodeArgs a, bool bf16) {
-  prepare_query(a, blockIdx.x, bf16);
+  const int v0 = blockIdx.x * kQueriesPerCta;
+  prepare_queries(a, v0, min(kQueriesPerCta, a.batch * a.n_q - v0), bf16);
 }
 
 // One decode step's per-vector work: blocks [0, n_k) quantize the new keys,
-// [n_k, 2 n_k) the new values, the rest prepare the queries.  The decode
+// [n_k, 2 n_k) the new values, the rest prepare the queries, kQueriesPerCta
+// heads per block.  The decode
 // partials kernel that follows may start as soon as these blocks run (it
 // waits for their results where it reads them).
 __global__ void __launch_bounds__(kVecThreads) step_prep_kernel(QuantizeArgs ka, QuantizeArgs va, bool kv_bf16,
@@ -240,7 +288,10 @@ __global__ void __launch_bounds__(kVecThreads) step_prep_kernel(QuantizeArgs ka,
   const int blk = blockIdx.x;
   if (blk < ka.n_vec) quantize_vector(ka, blk, kv_bf16);
   else if (blk < 2 * ka.n_vec) quantize_vector(va, blk - ka.n_vec, kv_bf16);
-  else prepare_query(da, blk - 2 * ka.n_vec, q_bf16);
+  else {
+    const int v0 = (blk - 2 * ka.n_vec) * kQueriesPerCta;
+    prepare_queries(da, v0, min(kQueriesPerCta, da.batch * da.n_q - v0), q_bf16);
+  }
 }
 
 }  // namespace
@@ -257,7 +308,7 @@ cudaError_t launch_quantize_small(const QuantizeArgs* first, const QuantizeArgs*
 cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_t stream) {
   const int n_vec = args.batch * args.n_q;
   if (n_vec <= 0) return cudaSuccess;
-  qprep_kernel<<<n_vec, kVecThreads, 0, stream>>>(args, bf16);
+  qprep_kernel<<<(n_vec + kQueriesPerCta - 1) / kQueriesPerCta, kVecThreads, 0, stream>>>(args, bf16);
   return cudaGetLastError();
 }
 
@@ -278,7 +329,7 @@ cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream, bo
 
 cudaError_t launch_step_prep(const QuantizeArgs& ka, const QuantizeArgs& va, bool kv_bf16, const DecodeArgs& da,
                              bool q_bf16, cudaStream_t stream) {
-  const int n = 2 * ka.n_vec + da.batch * da.n_q;
+  const int n = 2 * ka.n_vec + (da.batch * da.n_q + kQueriesPerCta - 1) / kQueriesPerCta;
   if (n <= 0) return cudaSuccess;
   step_prep_kernel<<<n, kVecThreads, 0, stream>>>(ka, va, kv_bf16, da, q_bf16);
   return cudaGetLastError();
