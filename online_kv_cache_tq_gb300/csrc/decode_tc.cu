@@ -592,6 +592,12 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         cur_group = group;
       }
       ok = wait_phase(&kin, seq & 1, abort, a.error);
+      // this thread's heads: 1/sigma_mse, 1/sigma_qjl, ones_mse, ones_qjl
+      float cst_r[4][HG];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int j = 0; j < HG; ++j) cst_r[k][j] = half * HG + j < G ? cst_s[k][half * HG + j] : 0.f;
 
       // thread (lane, half) owns the query heads h with h / HG == half: it turns
       // their accumulators of a key tile into the scaled scores of token lane,
@@ -634,8 +640,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           for (int j = 0; j < HG; ++j) {
             const int h = H0 + j;
             if (h >= G) break;
-            const float mse = fmaf(am[j], cst_s[0][h], -cst_s[2][h]);
-            const float qv = qjl ? fmaf(aq[j], cst_s[1][h], -cst_s[3][h]) : 0.f;
+            const float mse = fmaf(am[j], cst_r[0][j], -cst_r[2][j]);
+            const float qv = qjl ? fmaf(aq[j], cst_r[1][j], -cst_r[3][j]) : 0.f;
             const float sc = valid ? a.scale * fmaf(nk, mse, gk * qv) : -INFINITY;
             s0[h * kChunk + tl] = sc;
             mx[h] = fmaxf(mx[h], sc);
@@ -771,7 +777,12 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           }
         }
         if (tile == x.n_tiles - 1) ptx::mbar_arrive(&vfree);   // the value fields are no longer read
-        for (int pair = 0; pair < n_pairs && ok; ++pair) {
+        // (a compile-time trip count when the value width is fixed, so the
+        // plane pair of every unit folds)
+        constexpr int kMaxPairs = VB > 0 ? ((1 << (VB - 1)) + 1) / 2 : 4;
+#pragma unroll
+        for (int pair = 0; pair < kMaxPairs; ++pair) {
+          if (pair >= n_pairs || !ok) break;
           const int slot = vslot;
           last_slot = vslot;
           last_wrap = vwrap;
