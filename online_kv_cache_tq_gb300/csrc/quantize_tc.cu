@@ -52,16 +52,22 @@ constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, 128);
 
+// Shared memory: the bf16 hi/lo images of R (and S'), X stages and, with the
+// QJL bit, the partial residual norms of two tiles.  Tensor memory: Y buffers
+// of 128 columns (with the QJL bit each turns into the residual, hi and lo
+// bf16, once its Y is read, and serves as the A operand of the second
+// product) and, with the QJL bit, one Z buffer.
 template <bool QJL>
 struct Layout {
   static constexpr int kW = QJL ? 4 : 2;          // R_hi, R_lo (, S'_hi, S'_lo)
-  static constexpr int kStages = QJL ? 1 : 3;     // X tiles in flight
+  static constexpr int kStages = QJL ? 2 : 3;     // X tiles in flight
   static constexpr int kW0 = 0;
   static constexpr int kX0 = kW * kMatBytes;
-  static constexpr int kRes0 = kX0 + kStages * kMatBytes;
-  static constexpr int kBytes = kRes0 + (QJL ? 2 * kMatBytes : 0);
-  static constexpr uint32_t kBufCols = QJL ? 256 : 128;     // Y (+ Z) of one tile
-  static constexpr uint32_t kTmemCols = 2 * kBufCols;        // two tiles in flight
+  static constexpr int kRs0 = kX0 + kStages * kMatBytes;   // [2][4][128] floats
+  static constexpr int kBytes = kRs0 + (QJL ? 2 * 4 * kTileRows * 4 : 0);
+  static constexpr int kYBufs = QJL ? 3 : 2;
+  static constexpr uint32_t kZCol = 3 * 128;
+  static constexpr uint32_t kTmemCols = QJL ? 512 : 256;
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -145,10 +151,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Layout<QJL>;
   constexpr int kLevels = 1 << BITS;
   extern __shared__ uint8_t smem_raw[];
-  // y_full / z_full: the products of a tile's buffer are in tensor memory;
-  // y_empty: the epilogue read that buffer (its second product, if any, too)
-  __shared__ __align__(8) uint64_t w_full, x_full[L::kStages], x_empty[L::kStages], y_full[2], y_empty[2],
-      res_full, z_full[2], drain;
+  // y_full[b]: the first products of Y buffer b are in tensor memory;
+  // y_empty[b]: the epilogue is done with buffer b (Y read, and with the QJL
+  // bit its residual consumed by the second products); res_full[b]: the
+  // residual of buffer b is stored; z_full / z_empty: the second products are
+  // in the Z buffer / were read.
+  __shared__ __align__(8) uint64_t w_full, x_full[L::kStages], x_empty[L::kStages], y_full[3], y_empty[3],
+      res_full[3], z_full, z_empty, drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
 
@@ -168,12 +177,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&x_full[s], 1);
       ptx::mbar_init(&x_empty[s], kEpiThreads);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 3; ++b) {
       ptx::mbar_init(&y_full[b], 1);
       ptx::mbar_init(&y_empty[b], kEpiThreads);
-      ptx::mbar_init(&z_full[b], 1);
+      ptx::mbar_init(&res_full[b], kEpiThreads);
     }
-    ptx::mbar_init(&res_full, kEpiThreads);
+    ptx::mbar_init(&z_full, 1);
+    ptx::mbar_init(&z_empty, kEpiThreads);
     ptx::mbar_init(&drain, 1);
     ptx::fence_mbar_init();
   }
@@ -215,18 +225,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // Y of tile i goes to buffer i % kYBufs; with the QJL bit the second
+    // products of tile i - 1 follow those of tile i, so that they run while
+    // the epilogue works on the first half of tile i.
     if (lane == 0) {
       bool ok = ptx::wait_bar(&w_full, 0, abort, a.error, kErrTimeout);
       const uint32_t w_base = ptx::smem_u32(smem + L::kW0);
+      // second products of tile j: Z = r_hi S'_hi + r_hi S'_lo + r_lo S'_hi,
+      // the residual read from tensor memory (thread group g stored
+      // coordinates 32 g .. 32 g + 31 as 16 hi columns, then 16 lo columns)
+      auto issue_z = [&](int j) -> bool {
+        const int b = j % 3;
+        if (!ptx::wait_bar(&res_full[b], (j / 3) & 1, abort, a.error, kErrTimeout)) return false;
+        if (j > 0 && !ptx::wait_bar(&z_empty, (j - 1) & 1, abort, a.error, kErrTimeout)) return false;
+        ptx::tc_fence_after();
+        const uint32_t r_base = tmem + b * 128;
+        uint32_t acc = 0;
+#pragma unroll
+        for (int pass = 0; pass < 3; ++pass) {
+          const uint32_t lo = pass == 2 ? 16 : 0;
+          const int b_sel = pass == 1 ? 3 : 2;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {          // 16 coordinates per step
+            const uint32_t a_col = r_base + 32 * (ks >> 1) + 8 * (ks & 1) + lo;
+            const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+            ptx::mma_bf16_tmem_a(tmem + L::kZCol, a_col, ptx::desc_k_sw128(w_base + b_sel * kMatBytes + off), kIdesc,
+                                 acc);
+            acc = 1;
+          }
+        }
+        ptx::mma_commit(&z_full);
+        return true;
+      };
       int it = 0;
       for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++it) {
         const int s = it % L::kStages;
         const uint32_t ph = (it / L::kStages) & 1;
-        const int buf = it & 1;
-        const uint32_t yb = tmem + buf * L::kBufCols;
-        if (!ptx::wait_bar(&x_full[s], ph, abort, a.error, kErrTimeout)) break;
-        // the buffer's previous tile (it - 2) has been read by the epilogue
-        if (!ptx::wait_bar(&y_empty[buf], ((it >> 1) & 1) ^ 1, abort, a.error, kErrTimeout)) break;
+        const int b = it % L::kYBufs;
+        const uint32_t yb = tmem + b * 128;
+        ok = ptx::wait_bar(&x_full[s], ph, abort, a.error, kErrTimeout);
+        // the buffer's previous tile (it - kYBufs) is done with
+        ok = ok && ptx::wait_bar(&y_empty[b], ((it / L::kYBufs) & 1) ^ 1, abort, a.error, kErrTimeout);
+        if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t x_base = ptx::smem_u32(smem + L::kX0 + s * kMatBytes);
         uint32_t acc = 0;
@@ -243,31 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        ptx::mma_commit(&y_full[buf]);
-        if (QJL) {
-          if (!ptx::wait_bar(&res_full, it & 1, abort, a.error, kErrTimeout)) break;
-          ptx::tc_fence_after();
-          const uint32_t res_base = ptx::smem_u32(smem + L::kRes0);
-          // (r_hi, S'_hi), (r_hi, S'_lo), (r_lo, S'_hi)
-          acc = 0;
-#pragma unroll
-          for (int pass = 0; pass < 3; ++pass) {
-            const int a_sel = pass == 2 ? 1 : 0;
-            const int b_sel = pass == 1 ? 3 : 2;
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
-#pragma unroll
-              for (int ks = 0; ks < 4; ++ks) {
-                const uint32_t off = kb * kHalfBytes + ks * 32;
-                ptx::mma_bf16(yb + 128, ptx::desc_k_sw128(res_base + a_sel * kMatBytes + off),
-                              ptx::desc_k_sw128(w_base + b_sel * kMatBytes + off), kIdesc, acc);
-                acc = 1;
-              }
-            }
-          }
-          ptx::mma_commit(&z_full[buf]);
-        }
+        ptx::mma_commit(&y_full[b]);
+        if (QJL && it > 0) ok = issue_z(it - 1);
       }
+      if (QJL && ok && it > 0) ok = issue_z(it - 1);
       if (*abort) {
         ptx::mma_commit(&drain);
         ptx::drain_bar(&drain, 0);
@@ -288,12 +307,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long cache_rows = static_cast<long long>(a.num_blocks) * a.block_size;
     const bool bs_pow2 = (a.block_size & (a.block_size - 1)) == 0;
     const int bs_shift = __ffs(a.block_size) - 1;
+    float* const rs_s = reinterpret_cast<float*>(smem + L::kRs0);   // [tile parity][g][row]
+
+    // the QJL signs and the residual norm of tile j (second half of its epilogue)
+    auto finish_qjl = [&](int j, long long dstp) {
+      const bool zok = __all_sync(0xffffffffu, ptx::wait_bar(&z_full, j & 1, abort, a.error, kErrTimeout));
+      if (!zok) return;                           // the next barrier ends every epilogue warp
+      ptx::tc_fence_after();
+      uint32_t zr[32];
+      ptx::tmem_ld32(lane_addr + L::kZCol + 32 * g, zr);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&z_empty);
+      ptx::mbar_arrive(&y_empty[j % 3]);          // its residual has been consumed too
+      uint32_t word = 0;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) word |= (__uint_as_float(zr[k]) > 0.f ? 1u : 0u) << k;
+      if (dstp >= 0) {
+        reinterpret_cast<uint32_t*>(a.qjl + dstp * 16)[g] = word;
+        const float* r4 = rs_s + (j & 1) * 4 * kTileRows + row;
+        if (g == 0) a.rnorm[dstp] = sqrtf((r4[0] + r4[kTileRows]) + (r4[2 * kTileRows] + r4[3 * kTileRows]));
+      }
+    };
+
     int it = 0;
+    bool alive = true;
+    long long dst_prev = -1;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
       const int s = it % L::kStages;
       const uint32_t ph = (it / L::kStages) & 1;
-      const int buf = it & 1;
-      const uint32_t yb = lane_addr + buf * L::kBufCols;
+      const int b = it % L::kYBufs;
+      const uint32_t yb = lane_addr + b * 128;
 
       // destination row first: its global loads overlap the waits below
       const int head = tile / n_tt;
@@ -332,14 +375,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      ok = ok && ptx::wait_bar(&y_full[buf], (it >> 1) & 1, abort, a.error, kErrTimeout);
+      ok = ok && ptx::wait_bar(&y_full[b], (it / L::kYBufs) & 1, abort, a.error, kErrTimeout);
       // Once the products have read X, the first 4 bytes this thread read carry
       // its partial sum to the other three threads of the row (no other thread
       // reads those bytes, and the stage is refilled only after all have read).
       if (ok) *reinterpret_cast<float*>(x_tile + x_partial_offset(g, row)) = ss;
       // a failed wait anywhere ends every epilogue warp (the tcgen05.ld below
-      // needs whole warps, the barriers below all 16)
-      if (epi_sync_any(!ok || *abort)) break;
+      // needs whole warps, the barriers below all 16); this barrier also
+      // publishes the previous tile's partial residual norms
+      if (epi_sync_any(!ok || *abort)) {
+        alive = false;
+        break;
+      }
       const float n = sqrtf((*reinterpret_cast<const float*>(x_tile + x_partial_offset(0, row)) +
                              *reinterpret_cast<const float*>(x_tile + x_partial_offset(1, row))) +
                             (*reinterpret_cast<const float*>(x_tile + x_partial_offset(2, row)) +
@@ -361,38 +408,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 32; ++j) {
           const float yv = __uint_as_float(yr[j]);
           const float y = yv * inv;
-          bool b[BITS];
-          code_bits<BITS>(y, bnd, b);
+          bool bits[BITS];
+          code_bits<BITS>(y, bnd, bits);
 #pragma unroll
-          for (int p = 0; p < BITS; ++p) planes[p] |= b[p] ? (1u << j) : 0u;
+          for (int p = 0; p < BITS; ++p) planes[p] |= bits[p] ? (1u << j) : 0u;
           if (QJL) {
-            r[j] = fmaf(-n, level_of<BITS>(lev, b), yv);
+            r[j] = fmaf(-n, level_of<BITS>(lev, bits), yv);
             rs = fmaf(r[j], r[j], rs);
           }
         }
         if (QJL) {
-          // 32 coordinates = 4 chunks of 8 in K block g / 2, chunks (g % 2) * 4 .. + 3
-          uint8_t* res_hi = smem + L::kRes0 + (g >> 1) * kHalfBytes + row * 128;
-          uint8_t* res_lo = res_hi + kMatBytes;
+          // the residual over this thread's (already read) Y columns: hi
+          // bf16 pairs in the first 16, lo pairs in the last 16
+          uint32_t rw[32];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int chunk = (g & 1) * 4 + q;
-            const int off = (chunk ^ (row & 7)) << 4;
-            uint32_t hw[4], lw[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float r0 = r[q * 8 + 2 * e], r1 = r[q * 8 + 2 * e + 1];
-              hw[e] = pack_bf16x2(r0, r1);
-              lw[e] = pack_bf16x2(r0 - bf16_lo(hw[e]), r1 - bf16_hi(hw[e]));
-            }
-            *reinterpret_cast<uint4*>(res_hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(res_lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          for (int e = 0; e < 16; ++e) {
+            const float r0 = r[2 * e], r1 = r[2 * e + 1];
+            rw[e] = pack_bf16x2(r0, r1);
+            rw[16 + e] = pack_bf16x2(r0 - bf16_lo(rw[e]), r1 - bf16_hi(rw[e]));
           }
+          ptx::tmem_st32(yb + 32 * g, rw);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&res_full[b]);
+        } else {
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&y_empty[b]);          // this buffer may take the tile after next
         }
-      }
-      if (!QJL) {
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&y_empty[buf]);          // this buffer may take the tile after next
       }
       if (TRANS) {
         // token-transposed codes: whole words when the warp's 32 slots are
@@ -423,32 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (dst >= 0 && g == 0) a.norm[dst] = n;
       if (QJL) {
-        ptx::fence_async_shared();
-        ptx::mbar_arrive(&res_full);
-        const bool zok = ptx::wait_bar(&z_full[buf], (it >> 1) & 1, abort, a.error, kErrTimeout);
-        // the second products are done with the residual tile: its first 2 KB
-        // carry the partial residual norms until the next tile's first barrier
-        float* const rs_x = reinterpret_cast<float*>(smem + L::kRes0);
-        if (zok) rs_x[g * kTileRows + row] = rs;
-        if (epi_sync_any(!zok)) break;
-        ptx::tc_fence_after();
-        uint32_t zr[32];
-        ptx::tmem_ld32(yb + 128 + 32 * g, zr);
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&y_empty[buf]);          // this buffer (Y and Z) may take the tile after next
-        uint32_t word = 0;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) word |= (__uint_as_float(zr[j]) > 0.f ? 1u : 0u) << j;
-        if (dst >= 0) {
-          reinterpret_cast<uint32_t*>(a.qjl + dst * 16)[g] = word;
-          if (g == 0)
-            a.rnorm[dst] = sqrtf((rs_x[row] + rs_x[kTileRows + row]) + (rs_x[2 * kTileRows + row] + rs_x[3 * kTileRows + row]));
-        }
+        // rs_s[it & 1] is read after the next tile's first barrier and written
+        // again two tiles later, after every thread has passed that barrier
+        rs_s[(it & 1) * 4 * kTileRows + g * kTileRows + row] = rs;
+        if (it > 0) finish_qjl(it - 1, dst_prev);
+        dst_prev = dst;
       }
-      // No barrier closes the tile: the residual tile is rewritten only after
-      // the next tile's first barrier, which a thread passes once every thread
-      // has read this tile's partial residual norms.
     }
+    if (QJL && alive && it > 0 && !epi_sync_any(*abort)) finish_qjl(it - 1, dst_prev);
   }
 
   __syncthreads();
