@@ -393,7 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                              *reinterpret_cast<const float*>(x_tile + x_partial_offset(3, row))));
       ptx::fence_async_shared();                  // the generic write above, before TMA refills the stage
       ptx::mbar_arrive(&x_empty[s]);
-      const float inv = n > 0.f ? 1.f / n : 0.f;
+      // y = Y / n against t is taken as Y against n t (a zero vector compares
+      // y = 0 against t): one product per boundary instead of one per coordinate
+      const float n_eff = n > 0.f ? n : 1.f;
+      float tn[kLevels - 1];
+#pragma unroll
+      for (int i = 0; i < kLevels - 1; ++i) tn[i] = bnd[i] * n_eff;
 
       ptx::tc_fence_after();
       uint32_t planes[BITS];
@@ -407,9 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float yv = __uint_as_float(yr[j]);
-          const float y = yv * inv;
           bool bits[BITS];
-          code_bits<BITS>(y, bnd, bits);
+          code_bits<BITS>(yv, tn, bits);
 #pragma unroll
           for (int p = 0; p < BITS; ++p) planes[p] |= bits[p] ? (1u << j) : 0u;
           if (QJL) {
