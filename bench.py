@@ -204,11 +204,14 @@ def measure_prefill_quantize(steps, warmup):
     flops = n_tok * n_kv * (2 * 32768) + n_tok * n_kv * 32768  # K: rotation + QJL, V: rotation
     hbm, _ = hbm_peak()
     tensor, tensor_src = bf16_peak()
+    rec = [recorded_traffic(k, "c3_prefill_quantize") for k in ("quantize_tc_kernel<2,1,0>", "quantize_tc_kernel<3,0,1>")]
+    traffic = sum(rec) if all(r is not None for r in rec) else None
     return {"workload": "c3_prefill_quantize", "tokens": n_tok, "n_kv_heads": n_kv, "k_bits": 3, "v_bits": 3,
             "ms_per_append": secs * 1e3, "vectors_per_s": vectors / secs,
             "hbm_gbs": nbytes / secs / 1e9, "hbm_frac": nbytes / secs / 1e9 / hbm,
             "algorithmic_tflops": flops / secs / 1e12, "tensor_frac": flops / secs / 1e12 / tensor,
             "tensor_peak": tensor, "tensor_peak_source": tensor_src + " bf16_tflops",
+            "algorithmic_bytes_per_append": nbytes, "traffic_bytes_per_append": traffic,
             "note": "algorithmic flops; the bf16 hi/lo splitting runs 2 (rotation) and 3 (QJL) tensor passes"}
 
 
