@@ -186,16 +186,34 @@ __device__ __forceinline__ void builder_sync() { asm volatile("bar.sync 1, 256;"
 
 // Reduce N values per thread over warps [w0, w0 + nw) of the builders at once
 // (one pair of barriers for all N); every thread gets the results of its range.
+// Within a warp the value set halves at every shuffle step (lanes with bit
+// `off` set keep the upper half and send the lower): P = N rounded up to a
+// power of two takes P - 1 + log2(32 / P) shuffles instead of 5 N, after
+// which lane l holds value idx(l) reduced over the warp.
 template <int N, typename Op>
 __device__ __forceinline__ void block_reduce(float (&v)[N], float* red, int w0, int nw, Op op) {
+  constexpr int P = N <= 1 ? 1 : N <= 2 ? 2 : N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : 32;
+  static_assert(N <= 32, "at most 32 values");
+  const int lane = threadIdx.x & 31;
+  float cur[P];
 #pragma unroll
-  for (int j = 0; j < N; ++j)
+  for (int j = 0; j < P; ++j) cur[j] = j < N ? v[j] : op.identity();
+  int idx = 0;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v[j] = op(v[j], __shfl_xor_sync(0xffffffffu, v[j], off));
+  for (int n = P, off = 16; n > 1; n >>= 1, off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? cur[i] : cur[i + n / 2];
+      const float keep = upper ? cur[i + n / 2] : cur[i];
+      cur[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, off));
+    }
+    if (upper) idx += n / 2;
+  }
+#pragma unroll
+  for (int off = 16 / P; off > 0; off >>= 1) cur[0] = op(cur[0], __shfl_xor_sync(0xffffffffu, cur[0], off));
   builder_sync();
-  if ((threadIdx.x & 31) == 0)
-#pragma unroll
-    for (int j = 0; j < N; ++j) red[(threadIdx.x >> 5) * N + j] = v[j];
+  if ((lane & (32 / P - 1)) == 0 && idx < N) red[(threadIdx.x >> 5) * N + idx] = cur[0];
   builder_sync();
 #pragma unroll
   for (int j = 0; j < N; ++j) {
@@ -204,8 +222,14 @@ __device__ __forceinline__ void block_reduce(float (&v)[N], float* red, int w0, 
     v[j] = r;
   }
 }
-struct MaxOp { __device__ float operator()(float a, float b) const { return fmaxf(a, b); } };
-struct SumOp { __device__ float operator()(float a, float b) const { return a + b; } };
+struct MaxOp {
+  __device__ float operator()(float a, float b) const { return fmaxf(a, b); }
+  __device__ float identity() const { return -INFINITY; }
+};
+struct SumOp {
+  __device__ float operator()(float a, float b) const { return a + b; }
+  __device__ float identity() const { return 0.f; }
+};
 
 __device__ __forceinline__ int context_of(const DecodeArgs& a, int b) {
   int ctx = a.context_lens[b];
@@ -345,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   const int kp = 32 * (pk + pq);                     // columns per key slot
   const int kbytes = 16 * k_bits;                    // key code bytes per token
   const int vblock = v_bits * 16 * bs;               // value code bytes per (block, head)
+  const int k_slots = KB > 0 ? 2 : L.k_slots;        // the fixed build is launched with two key slots
 
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned, as an offset from smem_raw so that accesses stay shared-space
@@ -486,8 +511,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       const bool more = next_item(a, it, last, bs_shift, nxt);
       // scores: tile i once its planes are stored and the previous tile's accumulators were read
       for (int i = 0; i < cur.n_tiles && ok; ++i, ++ktile) {
-        const int slot = L.k_slots == 2 ? (ktile & 1) : 0;
-        ok = wait_phase(&kfull[slot], (L.k_slots == 2 ? ktile >> 1 : ktile) & 1, abort, a.error);
+        const int slot = k_slots == 2 ? (ktile & 1) : 0;
+        ok = wait_phase(&kfull[slot], (k_slots == 2 ? ktile >> 1 : ktile) & 1, abort, a.error);
         if (ok && ktile > 0) ok = wait_phase(&sfree, (ktile - 1) & 1, abort, a.error);
         if (ok && ptx::elect_one()) {
           ptx::tc_fence_after();
@@ -664,14 +689,16 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       // ---- scores: the planes of tile i are built while the MMAs of tile i - 1 run ----
       const int k0 = ktile;
       for (int i = 0; i < x.n_tiles && ok; ++i, ++ktile) {
-        const int slot = L.k_slots == 2 ? (ktile & 1) : 0;
-        if (L.k_slots == 1 && i > 0) take_scores(i - 1, ktile - 1);
+        const int slot = k_slots == 2 ? (ktile & 1) : 0;
+        if (k_slots == 1 && i > 0) take_scores(i - 1, ktile - 1);
         if (!ok) break;
         const int tl = i * kTile + lane;
-        const bool valid = tl < x.n_local && blk_ok[tl >> bs_shift];
+        // loaded for every token slot of the tile (tl < kChunk, inside the
+        // copied fields): a slot past the context or in a skipped block holds
+        // stale but finite operand bytes, and its score is set to -inf
         uint32_t bw[4][2] = {};
         uint32_t sg[2] = {};
-        if (valid) {
+        {
           const uint2* kc = reinterpret_cast<const uint2*>(kc_s + tl * kbytes);
 #pragma unroll
           for (int p = 0; p < 4; ++p)
@@ -696,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(&kfull[slot]);
-        if (L.k_slots == 2 && i > 0) take_scores(i - 1, ktile - 1);
+        if (k_slots == 2 && i > 0) take_scores(i - 1, ktile - 1);
       }
       if (ok) take_scores(x.n_tiles - 1, k0 + x.n_tiles - 1);
       ptx::mbar_arrive(&kfree);                   // this item's key fields are no longer read
@@ -767,8 +794,10 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         uint32_t bw[4][2] = {};                   // [bit-plane][this thread's 32-token groups]
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
+          // every 32-token group of the tile (inside the copied fields): a group
+          // past the context or in a skipped block gets weight 0
           const int tl = tile * kTile + 32 * (w0 + c);
-          if (tl < x.n_local && blk_ok[tl >> bs_shift]) {
+          {
             const uint32_t* src =
                 vc_s + (tl >> bs_shift) * (vblock / 4) + ((tl & (bs - 1)) >> 5) + (lane << wpd_shift);
 #pragma unroll
@@ -898,7 +927,7 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, bool early) {
   const TcLayout l = tc_layout(G, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size);
   // 3-bit keys (2 MSE bits + the QJL bit) with 3-bit values have their own
   // build with the widths folded in; other widths are read at run time
-  const bool fixed = a.k_bits == 2 && a.v_bits == 3 && a.k_qjl != nullptr;
+  const bool fixed = a.k_bits == 2 && a.v_bits == 3 && a.k_qjl != nullptr && l.k_slots == 2;
   auto kernel = fixed ? attention_tc_kernel<G, 2, 3, 1> : attention_tc_kernel<G, 0, 0, -1>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem_bytes);
   if (err != cudaSuccess) return err;
