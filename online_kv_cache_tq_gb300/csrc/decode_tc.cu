@@ -659,8 +659,9 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
               }
             }
           }
-          const float nk = valid ? kn_s[tl] : 0.f;
-          const float gk = valid && qjl ? kr_s[tl] * a.qjl_coef : 0.f;
+          const float kn = kn_s[tl], kr = kr_s[tl];     // (tl < kChunk: in bounds; selected below)
+          const float nk = valid ? kn : 0.f;
+          const float gk = valid && qjl ? kr * a.qjl_coef : 0.f;
 #pragma unroll
           for (int j = 0; j < HG; ++j) {
             const int h = H0 + j;
@@ -734,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
 
       // ---- softmax max over the chunk; B_V pieces of exp(s - m) n_v ----
       for (int i = t; i < x.n_tiles * kTile; i += kBuilders)
-        if (i < x.n_local && blk_ok[i >> bs_shift]) mx[G] = fmaxf(mx[G], vn_s[i]);
+        mx[G] = fmaxf(mx[G], i < x.n_local && blk_ok[i >> bs_shift] ? vn_s[i] : 0.f);
       float lw[2 * G];                            // owned heads: sum of e, then sum of e n_v
 #pragma unroll
       for (int h = 0; h < 2 * G; ++h) lw[h] = 0.f;
@@ -755,7 +756,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             for (int tile = 0; tile < x.n_tiles; ++tile) {
               const int tl = tile * kTile + lane;
               const bool valid = tl < x.n_local && blk_ok[tl >> bs_shift];
-              const float nv = valid ? vn_s[tl] : 0.f;
+              const float vn = vn_s[tl];                // (tl < kChunk: in bounds; selected below)
+              const float nv = valid ? vn : 0.f;
               uint8_t* dst = b_v + tile * L.no * 128;
               float e[HG];
 #pragma unroll
@@ -763,7 +765,9 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
                 const int h = H0 + j;
                 e[j] = 0.f;
                 if (h >= G) continue;
-                if (valid && mx[h] != -INFINITY) e[j] = __expf(s0[h * kChunk + tl] - mx[h]);
+                // (a select, not a branch: the exponent of an invalid slot may be nan)
+                const float ex = __expf(s0[h * kChunk + tl] - mx[h]);
+                e[j] = valid && mx[h] != -INFINITY ? ex : 0.f;
                 lw[h] += e[j];
                 lw[G + h] = fmaf(e[j], nv, lw[G + h]);
               }
