@@ -318,25 +318,26 @@ class DecodeWorkload:
                            self.ws, self.ws_bytes)
 
     def e2e(self, steps, warmup):
-        """Same step through the one-call public API with pinned host buffers:
-        H2D of the step's inputs, tq_decode_step, D2H of the output."""
+        """Same step through the one-call C entry point for host buffers
+        (tq_decode_step_host): per step the H2D copies of the step's inputs
+        from pinned host memory, the step, the D2H copy of the output, and a
+        synchronisation before the host reads it."""
         torch, B = self.torch, self.B
         host = {name: t.cpu().pin_memory() for name, t in
                 (("q", self.q), ("k", self.k_new), ("v", self.v_new), ("ctx", self.ctx_d))}
-        dev = {name: torch.empty_like(t, device="cuda") for name, t in host.items()}
         out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        ws_bytes = B.tq_decode_step_host_workspace_bytes(self.book, self.batch, self.n_q, self.n_kv, self.max_ctx,
+                                                         self.dtype_code, self.dtype_code)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = out_h.numel() * out_h.element_size()
         stream = torch.cuda.current_stream()
 
         def one(i):
-            for name in host:
-                dev[name].copy_(host[name], non_blocking=True)
             view = self.views[i % len(self.views)]
-            B.tq_decode_step(self.book, dev["k"], dev["v"], self.dtype_code, dev["q"], self.dtype_code, self.batch,
-                             self.n_q, self.n_kv, view, self.table_d, self.max_blocks, dev["ctx"], self.max_ctx,
-                             0.0, self.out, self.ws, self.ws_bytes)
-            out_h.copy_(self.out, non_blocking=True)
+            B.tq_decode_step_host(self.book, host["k"], host["v"], self.dtype_code, host["q"], self.dtype_code,
+                                  self.batch, self.n_q, self.n_kv, view, self.table_d, self.max_blocks, host["ctx"],
+                                  self.max_ctx, 0.0, out_h, ws, ws_bytes, stream)
             stream.synchronize()
 
         for i in range(warmup):

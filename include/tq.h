@@ -167,6 +167,34 @@ tq_status tq_decode_step(const tq_codebook* book, const void* k_new, const void*
                          const int32_t* context_lens, int max_context, float scale, float* out,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/* Device workspace bytes tq_decode_step_host needs: the decode workspace of
+ * (batch, n_q_heads, max_context) after a staging area for one step's inputs
+ * (k_new, v_new, q, context_lens) and output. 0 for invalid arguments. */
+size_t tq_decode_step_host_workspace_bytes(const tq_codebook* book, int batch, int n_q_heads, int n_kv_heads,
+                                           int max_context, tq_dtype kv_dtype, tq_dtype q_dtype);
+
+/* tq_decode_step with the step's inputs and output in HOST memory, for a
+ * caller whose tokens arrive from and leave to the host: k_new_h, v_new_h
+ * [batch][n_kv_heads][128] (kv_dtype), q_h [batch][n_q_heads][128] (q_dtype),
+ * context_lens_h [batch] int32 (each sequence's length including the new
+ * token) and out_h [batch][n_q_heads][128] fp32 are host addresses; they
+ * should be page-locked (cudaHostAlloc / pinned) so that the copies overlap
+ * the host, pageable memory works but its copies block the calling thread.
+ * The call copies the inputs into the staging area at the start of
+ * `workspace` (one cudaMemcpyAsync each), runs tq_decode_step on those device
+ * copies with the rest of the workspace, and copies the output back, all in
+ * order on `stream`: out_h holds the result once the caller synchronises the
+ * stream, and the host inputs may be reused only then. block_table stays a
+ * device array (it belongs to the cache, not to the step). Argument meaning,
+ * checks and errors are those of tq_decode_step, plus TQ_ERR_WORKSPACE when
+ * workspace_bytes is below tq_decode_step_host_workspace_bytes, and
+ * TQ_ERR_CUDA when a copy cannot be queued. */
+tq_status tq_decode_step_host(const tq_codebook* book, const void* k_new_h, const void* v_new_h,
+                              tq_dtype kv_dtype, const void* q_h, tq_dtype q_dtype, int batch, int n_q_heads,
+                              int n_kv_heads, const tq_cache_view* cache, const int32_t* block_table,
+                              int max_blocks, const int32_t* context_lens_h, int max_context, float scale,
+                              float* out_h, void* workspace, size_t workspace_bytes, void* stream);
+
 /* The first stage of tq_decode_step, for callers that run the stages one at a
  * time (then tq_decode_partials and tq_decode_finish with the step's
  * arguments): the append of k_new / v_new and the query preparation, in one

@@ -22,7 +22,8 @@ FIELDS = ("k_codes", "k_qjl", "k_norm", "k_rnorm", "v_codes", "v_norm")
 # Entry points declared in include/tq.h, checked by the ABI test.
 EXPORTED = ("tq_codebook_build", "tq_codebook_destroy", "tq_codebook_levels", "tq_codebook_matrices",
             "tq_cache_field_bytes", "tq_quantize_append", "tq_decode_workspace_bytes",
-            "tq_decode_attention", "tq_decode_step", "tq_decode_step_prepare", "tq_decode_prepare", "tq_decode_partials", "tq_decode_finish",
+            "tq_decode_attention", "tq_decode_step", "tq_decode_step_host", "tq_decode_step_host_workspace_bytes",
+            "tq_decode_step_prepare", "tq_decode_prepare", "tq_decode_partials", "tq_decode_finish",
             "tq_decode_attention_static", "tq_decode_kernel_kind", "tq_get_last_device_error",
             "tq_status_string")
 
@@ -73,6 +74,10 @@ def load():
                                         vp, i32, ctypes.c_float, vp, vp, sz, vp]
     lib.tq_decode_step.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32, ctypes.POINTER(tq_cache_view), vp,
                                    i32, vp, i32, ctypes.c_float, vp, vp, sz, vp]
+    lib.tq_decode_step_host.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32, ctypes.POINTER(tq_cache_view),
+                                        vp, i32, vp, i32, ctypes.c_float, vp, vp, sz, vp]
+    lib.tq_decode_step_host_workspace_bytes.argtypes = [vp, i32, i32, i32, i32, i32, i32]
+    lib.tq_decode_step_host_workspace_bytes.restype = sz
     lib.tq_decode_step_prepare.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32,
                                            ctypes.POINTER(tq_cache_view), vp, i32, vp, i32, vp, sz, vp]
     lib.tq_decode_prepare.argtypes = [vp, vp, i32, i32, i32, i32, vp, sz, vp]
@@ -86,7 +91,7 @@ def load():
     lib.tq_status_string.argtypes = [i32]
     lib.tq_status_string.restype = ctypes.c_char_p
     for name in EXPORTED:
-        if name not in ("tq_decode_workspace_bytes", "tq_status_string"):
+        if name not in ("tq_decode_workspace_bytes", "tq_decode_step_host_workspace_bytes", "tq_status_string"):
             getattr(lib, name).restype = i32
     _LIB = lib
     return lib
@@ -214,6 +219,22 @@ def tq_decode_step(book, k_new, v_new, kv_dtype, q, q_dtype, batch, n_q_heads, n
                                  _ptr(context_lens), max_context, scale, _ptr(out), _ptr(workspace),
                                  workspace_bytes, _stream(stream)),
            "tq_decode_step")
+
+
+def tq_decode_step_host_workspace_bytes(book, batch, n_q_heads, n_kv_heads, max_context, kv_dtype, q_dtype):
+    return load().tq_decode_step_host_workspace_bytes(book.handle, batch, n_q_heads, n_kv_heads, max_context,
+                                                      kv_dtype, q_dtype)
+
+
+def tq_decode_step_host(book, k_new, v_new, kv_dtype, q, q_dtype, batch, n_q_heads, n_kv_heads, view, block_table,
+                        max_blocks, context_lens, max_context, scale, out, workspace, workspace_bytes, stream=None):
+    """tq_decode_step with k_new, v_new, q, context_lens and out in host memory
+    (tensors on the CPU, preferably pinned, or int addresses)."""
+    _check(load().tq_decode_step_host(book.handle, _ptr(k_new), _ptr(v_new), kv_dtype, _ptr(q), q_dtype, batch,
+                                      n_q_heads, n_kv_heads, ctypes.byref(view), _ptr(block_table), max_blocks,
+                                      _ptr(context_lens), max_context, scale, _ptr(out), _ptr(workspace),
+                                      workspace_bytes, _stream(stream)),
+           "tq_decode_step_host")
 
 
 def tq_decode_step_prepare(book, k_new, v_new, kv_dtype, q, q_dtype, batch, n_q_heads, n_kv_heads, view,

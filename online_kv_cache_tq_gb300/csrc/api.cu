@@ -616,6 +616,72 @@ tq_status tq_decode_step(const tq_codebook* book, const void* k_new, const void*
   return st;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Staging layout of tq_decode_step_host: k_new, v_new, q, context_lens, out.
+struct HostStaging {
+  size_t k, v, q, ctx, out, total;
+};
+
+bool host_staging(int batch, int n_q_heads, int n_kv_heads, tq_dtype kv_dtype, tq_dtype q_dtype, HostStaging* h) {
+  if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0) return false;
+  if ((kv_dtype != TQ_BF16 && kv_dtype != TQ_FP32) || (q_dtype != TQ_BF16 && q_dtype != TQ_FP32)) return false;
+  const size_t kv_elem = kv_dtype == TQ_BF16 ? 2 : 4, q_elem = q_dtype == TQ_BF16 ? 2 : 4;
+  h->k = h->v = static_cast<size_t>(batch) * n_kv_heads * tq::kDim * kv_elem;
+  h->q = static_cast<size_t>(batch) * n_q_heads * tq::kDim * q_elem;
+  h->ctx = static_cast<size_t>(batch) * sizeof(int32_t);
+  h->out = static_cast<size_t>(batch) * n_q_heads * tq::kDim * sizeof(float);
+  h->total = round_up(h->k) + round_up(h->v) + round_up(h->q) + round_up(h->ctx) + round_up(h->out);
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tq_decode_step_host_workspace_bytes(const tq_codebook* book, int batch, int n_q_heads, int n_kv_heads,
+                                           int max_context, tq_dtype kv_dtype, tq_dtype q_dtype) {
+  HostStaging h;
+  if (!host_staging(batch, n_q_heads, n_kv_heads, kv_dtype, q_dtype, &h)) return 0;
+  const size_t ws = tq_decode_workspace_bytes(book, batch, n_q_heads, max_context);
+  return ws == 0 ? 0 : h.total + ws;
+}
+
+tq_status tq_decode_step_host(const tq_codebook* book, const void* k_new_h, const void* v_new_h,
+                              tq_dtype kv_dtype, const void* q_h, tq_dtype q_dtype, int batch, int n_q_heads,
+                              int n_kv_heads, const tq_cache_view* cache, const int32_t* block_table,
+                              int max_blocks, const int32_t* context_lens_h, int max_context, float scale,
+                              float* out_h, void* workspace, size_t workspace_bytes, void* stream) {
+  HostStaging h;
+  if (book == nullptr || !host_staging(batch, n_q_heads, n_kv_heads, kv_dtype, q_dtype, &h)) {
+    return TQ_ERR_INVALID_ARG;
+  }
+  if (batch == 0) return TQ_OK;
+  if (k_new_h == nullptr || v_new_h == nullptr || q_h == nullptr || context_lens_h == nullptr || out_h == nullptr) {
+    return TQ_ERR_INVALID_ARG;
+  }
+  if (workspace == nullptr || workspace_bytes < h.total) return TQ_ERR_WORKSPACE;
+  char* base = static_cast<char*>(workspace);
+  void* k_d = base;
+  void* v_d = base + round_up(h.k);
+  void* q_d = base + round_up(h.k) + round_up(h.v);
+  int32_t* ctx_d = reinterpret_cast<int32_t*>(base + round_up(h.k) + round_up(h.v) + round_up(h.q));
+  float* out_d = reinterpret_cast<float*>(base + round_up(h.k) + round_up(h.v) + round_up(h.q) + round_up(h.ctx));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaMemcpyAsync(k_d, k_new_h, h.k, cudaMemcpyHostToDevice, s);
+  if (err == cudaSuccess) err = cudaMemcpyAsync(v_d, v_new_h, h.v, cudaMemcpyHostToDevice, s);
+  if (err == cudaSuccess) err = cudaMemcpyAsync(q_d, q_h, h.q, cudaMemcpyHostToDevice, s);
+  if (err == cudaSuccess) err = cudaMemcpyAsync(ctx_d, context_lens_h, h.ctx, cudaMemcpyHostToDevice, s);
+  if (err != cudaSuccess) return TQ_ERR_CUDA;
+  const tq_status st = tq_decode_step(book, k_d, v_d, kv_dtype, q_d, q_dtype, batch, n_q_heads, n_kv_heads, cache,
+                                      block_table, max_blocks, ctx_d, max_context, scale, out_d, base + h.total,
+                                      workspace_bytes - h.total, stream);
+  if (st != TQ_OK) return st;
+  return cudaMemcpyAsync(out_h, out_d, h.out, cudaMemcpyDeviceToHost, s) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
 tq_status tq_decode_prepare(const tq_codebook* book, const void* q, tq_dtype dtype, int batch, int n_q_heads,
                             int max_context, void* workspace, size_t workspace_bytes, void* stream) {
   tq::DecodeArgs a;

@@ -175,7 +175,8 @@ def test_llama3_70b_paged_full_size_sampled():
 @pytest.mark.parametrize("batch,n_kv,group", [(5, 2, 4), (130, 8, 1)])
 def test_decode_step_equals_append_then_attention(batch, n_kv, group):
     # one call (fused append + query preparation and an early-started partials
-    # kernel when batch * n_kv <= 1024, the tile quantizer otherwise) against
+    # kernel when batch * n_kv <= 1024, the tile quantizer otherwise), and the
+    # same call with the step's inputs and output in pinned host memory, against
     # the two calls it stands for: identical caches and outputs, and the output
     # within tolerance of the oracle; sequence 0 has an empty context
     cfg = dict(n_kv=n_kv, block_size=64, dtype="bf16", seed=21, log_uniform=(0.1, 10.0), outliers=3,
@@ -198,13 +199,27 @@ def test_decode_step_equals_append_then_attention(batch, n_kv, group):
     max_ctx = int(ctx.max())
     ws, nbytes = C.allocate_workspace(book, batch, n_q, max_ctx)
     outs, caches = [], []
-    for fused in (False, True):
+    for mode in ("two_calls", "step", "host"):
         c = {name: t.clone() for name, t in cache.items()}
         view = C.cache_view(book, c)
         out = torch.full((batch, n_q, 128), float("nan"), device="cuda", dtype=torch.float32)
-        if fused:
+        if mode == "step":
             B.tq_decode_step(book, k_new, v_new, B.TQ_BF16, q, B.TQ_BF16, batch, n_q, n_kv, view, table_d,
                              table.shape[1], ctx_d, max_ctx, 0.0, out, ws, nbytes)
+        elif mode == "host":
+            hk, hv, hq = (t.cpu().pin_memory() for t in (k_new, v_new, q))
+            hctx = torch.as_tensor(ctx).pin_memory()
+            hout = torch.full((batch, n_q, 128), float("nan"), dtype=torch.float32).pin_memory()
+            hbytes = B.tq_decode_step_host_workspace_bytes(book, batch, n_q, n_kv, max_ctx, B.TQ_BF16, B.TQ_BF16)
+            assert hbytes > nbytes
+            hws = torch.empty(hbytes, dtype=torch.uint8, device="cuda")
+            with pytest.raises(B.TQError):       # a workspace without room for the staging area
+                B.tq_decode_step_host(book, hk, hv, B.TQ_BF16, hq, B.TQ_BF16, batch, n_q, n_kv, view, table_d,
+                                      table.shape[1], hctx, max_ctx, 0.0, hout, hws, 1024)
+            B.tq_decode_step_host(book, hk, hv, B.TQ_BF16, hq, B.TQ_BF16, batch, n_q, n_kv, view, table_d,
+                                  table.shape[1], hctx, max_ctx, 0.0, hout, hws, hbytes)
+            torch.cuda.synchronize()
+            out.copy_(hout)
         else:
             B.tq_quantize_append(book, k_new, v_new, B.TQ_BF16, batch, n_kv, slots, view)
             B.tq_decode_attention(book, q, B.TQ_BF16, batch, n_q, n_kv, view, table_d, table.shape[1], ctx_d,
@@ -212,9 +227,10 @@ def test_decode_step_equals_append_then_attention(batch, n_kv, group):
         torch.cuda.synchronize()
         outs.append(out.cpu().numpy())
         caches.append({name: t.cpu() for name, t in c.items()})
-    for name in caches[0]:
-        assert torch.equal(caches[0][name], caches[1][name]), name
-    assert np.array_equal(outs[0], outs[1])
+    for other in (1, 2):
+        for name in caches[0]:
+            assert torch.equal(caches[0][name], caches[other][name]), name
+        assert np.array_equal(outs[0], outs[other])
     pairs = [(0, 0)] + attn_pairs(batch, n_q, 12, seed=batch)
     check_decode(outs[1], host_cache(caches[1]), q, table, ctx, ref, pairs)
     assert B.tq_get_last_device_error(book) == 0
