@@ -184,15 +184,17 @@ __device__ __forceinline__ void write_pieces2(uint8_t* b, int row_a, int row_b, 
 // Barrier of the 256 builder threads only (named barrier 1).
 __device__ __forceinline__ void builder_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// Reduce N values per thread over warps [w0, w0 + nw) of the builders at once
-// (one pair of barriers for all N); every thread gets the results of its range.
-// Within a warp the value set halves at every shuffle step (lanes with bit
-// `off` set keep the upper half and send the lower): P = N rounded up to a
-// power of two takes P - 1 + log2(32 / P) shuffles instead of 5 N, after
-// which lane l holds value idx(l) reduced over the warp.
+// Reduce N values per thread over the eight builder warps at once (one pair
+// of barriers for all N); on return lane j < N of every warp holds the total
+// of value j (the other lanes the identity).  Within a warp the value set
+// halves at every shuffle step (lanes with bit `off` set keep the upper half
+// and send the lower): P = N rounded up to a power of two takes
+// P - 1 + log2(32 / P) shuffles instead of 5 N.  Across warps lane j sums
+// warp 0's partial first, then warps 1..7 in order.
 template <int N, typename Op>
-__device__ __forceinline__ void block_reduce(float (&v)[N], float* red, int w0, int nw, Op op) {
+__device__ __forceinline__ float block_reduce(const float (&v)[N], float* red, Op op) {
   constexpr int P = N <= 1 ? 1 : N <= 2 ? 2 : N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : 32;
+  constexpr int kWarps = kBuilders / 32;
   static_assert(N <= 32, "at most 32 values");
   const int lane = threadIdx.x & 31;
   float cur[P];
@@ -215,12 +217,13 @@ __device__ __forceinline__ void block_reduce(float (&v)[N], float* red, int w0, 
   builder_sync();
   if ((lane & (32 / P - 1)) == 0 && idx < N) red[(threadIdx.x >> 5) * N + idx] = cur[0];
   builder_sync();
+  float r = op.identity();
+  if (lane < N) {
+    r = red[lane];
 #pragma unroll
-  for (int j = 0; j < N; ++j) {
-    float r = red[w0 * N + j];
-    for (int w = 1; w < nw; ++w) r = op(r, red[(w0 + w) * N + j]);
-    v[j] = r;
+    for (int w = 1; w < kWarps; ++w) r = op(r, red[w * N + lane]);
   }
+  return r;
 }
 struct MaxOp {
   __device__ float operator()(float a, float b) const { return fmaxf(a, b); }
@@ -330,28 +333,52 @@ struct Item {
   int b, kvh, chunk, ctx, start, n_local, n_tiles, n_blk;
 };
 
-__device__ __forceinline__ bool next_item(const DecodeArgs& a, int& it, int last, int bs_shift, Item& x) {
-  for (; it < last; ++it) {
-    const int chunk = it % a.max_chunks, g = it / a.max_chunks;
-    const int b = g / a.n_kv;
-    const int ctx = context_of(a, b);
-    if (chunk * kChunk >= ctx) continue;
-    x.b = b;
-    x.kvh = g - b * a.n_kv;
-    x.chunk = chunk;
-    x.ctx = ctx;
-    x.start = chunk * kChunk;
-    x.n_local = min(kChunk, ctx - x.start);
-    x.n_tiles = (x.n_local + kTile - 1) / kTile;
-    x.n_blk = (x.n_local + (1 << bs_shift) - 1) >> bs_shift;
-    ++it;
-    return true;
+// Walks the item indices [first, last) of a CTA: the index is split into
+// (b, kvh, chunk) once, then carried forward one item at a time, and a
+// sequence's context length is read when the walk enters the sequence.
+struct ItemCursor {
+  int it, last, chunk, kvh, b, ctx;
+  __device__ ItemCursor(const DecodeArgs& a, int first, int last_) : it(first), last(last_) {
+    const int g = first / a.max_chunks;
+    chunk = first - g * a.max_chunks;
+    b = g / a.n_kv;
+    kvh = g - b * a.n_kv;
+    ctx = first < last ? context_of(a, b) : 0;
   }
-  return false;
-}
+  __device__ __forceinline__ void advance(const DecodeArgs& a) {
+    ++it;
+    if (++chunk == a.max_chunks) {
+      chunk = 0;
+      if (++kvh == a.n_kv) {
+        kvh = 0;
+        ++b;
+        ctx = it < last ? context_of(a, b) : 0;
+      }
+    }
+  }
+  // the next non-empty item, if any
+  __device__ __forceinline__ bool next(const DecodeArgs& a, int bs_shift, Item& x) {
+    for (; it < last; advance(a)) {
+      if (chunk * kChunk >= ctx) continue;
+      x.b = b;
+      x.kvh = kvh;
+      x.chunk = chunk;
+      x.ctx = ctx;
+      x.start = chunk * kChunk;
+      x.n_local = min(kChunk, ctx - x.start);
+      x.n_tiles = (x.n_local + kTile - 1) / kTile;
+      x.n_blk = (x.n_local + (1 << bs_shift) - 1) >> bs_shift;
+      advance(a);
+      return true;
+    }
+    return false;
+  }
+};
 
 // KB, VB, QJ: key MSE bits, value bits and QJL plane (0/1) fixed at compile
-// time, or 0, 0, -1 to take them from the arguments.
+// time, or 0, 0, -1 to take them from the arguments.  Two CTAs per SM cap a
+// thread at 96 registers (the register file is split over four sub-partitions
+// of 16384, and one of them holds five of the two CTAs' eighteen warps).
 template <int G, int KB, int VB, int QJ>
 __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a, TcLayout L, int items_per_cta) {
   constexpr int N1 = score_cols(G), NO = value_cols(G);
@@ -499,16 +526,17 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     const uint64_t desc_v = ptx::desc_k_sw128(ptx::smem_u32(b_v));
     const uint32_t mse_plane_step = (L.n1 * 128) >> 4, v_tile_step = (L.no * 128) >> 4;
     const uint32_t d_mse = tmem + L.col_s;
-    int it = first, seq = 0, ktile = 0;
+    ItemCursor cursor(a, first, last);
+    int seq = 0, ktile = 0;
     int vslot = 0, vwrap = 0;                   // value unit counter as (slot, times round the slots)
     Item cur, nxt;
-    bool have = next_item(a, it, last, bs_shift, cur);
+    bool have = cursor.next(a, bs_shift, cur);
     if (have) {
       copy_fields(cur, 0, true);
       copy_fields(cur, 0, false);
     }
     while (have && ok) {
-      const bool more = next_item(a, it, last, bs_shift, nxt);
+      const bool more = cursor.next(a, bs_shift, nxt);
       // scores: tile i once its planes are stored and the previous tile's accumulators were read
       for (int i = 0; i < cur.n_tiles && ok; ++i, ++ktile) {
         const int slot = k_slots == 2 ? (ktile & 1) : 0;
@@ -581,11 +609,12 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   } else {
     // =================== builders ===================
     constexpr int HG = half_heads(G), HC = score_half(G);
-    int it = first, seq = 0, ktile = 0, cur_group = -1;
+    ItemCursor cursor(a, first, last);
+    int seq = 0, ktile = 0, cur_group = -1;
     int vslot = 0, vwrap = 0;                     // value unit counter as (slot, times round the slots)
     Item x;
     const int wpd_shift = bs_shift - 5;         // log2 of the words per coordinate in a block
-    while (ok && next_item(a, it, last, bs_shift, x)) {
+    while (ok && cursor.next(a, bs_shift, x)) {
       const int group = x.b * a.n_kv + x.kvh;
       const int qbase = x.b * a.n_q + x.kvh * G;
       const int* blk_ok = blk_ok_s[seq & 1];
@@ -739,10 +768,12 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       float lw[2 * G];                            // owned heads: sum of e, then sum of e n_v
 #pragma unroll
       for (int h = 0; h < 2 * G; ++h) lw[h] = 0.f;
-      block_reduce(mx, red_s, 0, kBuilders / 32, MaxOp());
-      if (t == 0)
+      {
+        const float tot = block_reduce(mx, red_s, MaxOp());
+        if (t < G) stat_s[0][t] = tot;
 #pragma unroll
-        for (int h = 0; h < G; ++h) stat_s[0][h] = mx[h];
+        for (int h = 0; h <= G; ++h) mx[h] = __shfl_sync(0xffffffffu, tot, h);
+      }
       // the pieces carry 2 e n_v sv / beta_t, below 2 * 64 * max n_v * sv
       const float sv = piece_scale(2.f * kMaxBitInvScale * mx[G]);
       {
@@ -844,13 +875,13 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       if (ok) ok = wait_phase(&vdone[last_slot], last_wrap & 1, abort, a.error);
       ptx::tc_fence_after();
 
-      block_reduce(lw, red_s, 0, kBuilders / 32, SumOp());
-      if (t == 0)
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          stat_s[1][h] = lw[h];
-          wsum_s[h] = lw[G + h];
-        }
+      {
+        // (only thread 0's warp keeps the sums: lanes 0..G-1 the sums of e,
+        // lanes G..2G-1 those of e n_v)
+        const float tot = block_reduce(lw, red_s, SumOp());
+        if (t < G) stat_s[1][t] = tot;
+        else if (t < 2 * G) wsum_s[t - G] = tot;
+      }
 
       // ---- partial output of this chunk: half h reads the planes s with s % 2 == h ----
       float o[G];
