@@ -37,6 +37,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <utility>
+
 #include "kernels.h"
 #include "tc_ptx.cuh"
 
@@ -135,6 +137,54 @@ __device__ __forceinline__ float level_of(const float (&levels)[1 << BITS], cons
 #pragma unroll
     for (int k = 0; k < (1 << (BITS - 1 - q)); ++k) cand[k] = b[q] ? cand[2 * k + 1] : cand[2 * k];
   return cand[0];
+}
+
+// The same search for 2- and 3-bit codes in one block of predicated PTX:
+// each compare feeds the next level's boundary select and a predicated OR of
+// bit j into its plane word (one logic instruction per plane bit where a
+// select and an OR would be two).  With LEV it also returns levels[code].
+template <int BITS, bool LEV, int J>
+__device__ __forceinline__ float decide(float y, const float (&t)[(1 << BITS) - 1], const float (&l)[1 << BITS],
+                                        uint32_t (&pl)[BITS]) {
+  static_assert(BITS == 2 || BITS == 3, "2- or 3-bit codes");
+  float lev = 0.f;
+  if constexpr (BITS == 3) {
+    asm("{\n\t.reg .pred q2, q1, q0;\n\t.reg .f32 ta, tb, tc, td;\n\t"
+        "setp.gt.f32 q2, %3, %4;\n\t@q2 or.b32 %0, %0, %11;\n\t"
+        "selp.f32 ta, %6, %5, q2;\n\t"
+        "setp.gt.f32 q1, %3, ta;\n\t@q1 or.b32 %1, %1, %11;\n\t"
+        "selp.f32 tb, %10, %9, q1;\n\tselp.f32 tc, %8, %7, q1;\n\tselp.f32 td, tb, tc, q2;\n\t"
+        "setp.gt.f32 q0, %3, td;\n\t@q0 or.b32 %2, %2, %11;\n\t}"
+        : "+r"(pl[2]), "+r"(pl[1]), "+r"(pl[0])
+        : "f"(y), "f"(t[3]), "f"(t[1]), "f"(t[5]), "f"(t[0]), "f"(t[2]), "f"(t[4]), "f"(t[6]), "n"(1u << J));
+    if constexpr (LEV) {
+      // (only with 3 MSE bits and the QJL bit: the level by the generic selects)
+      const bool b[3] = {((pl[0] >> J) & 1u) != 0, ((pl[1] >> J) & 1u) != 0, ((pl[2] >> J) & 1u) != 0};
+      lev = level_of<3>(l, b);
+    }
+  } else if constexpr (LEV) {
+    asm("{\n\t.reg .pred q1, q0;\n\t.reg .f32 ta, la, lb;\n\t"
+        "setp.gt.f32 q1, %3, %4;\n\t@q1 or.b32 %0, %0, %11;\n\t"
+        "selp.f32 ta, %6, %5, q1;\n\t"
+        "setp.gt.f32 q0, %3, ta;\n\t@q0 or.b32 %1, %1, %11;\n\t"
+        "selp.f32 la, %10, %9, q0;\n\tselp.f32 lb, %8, %7, q0;\n\tselp.f32 %2, la, lb, q1;\n\t}"
+        : "+r"(pl[1]), "+r"(pl[0]), "=f"(lev)
+        : "f"(y), "f"(t[1]), "f"(t[0]), "f"(t[2]), "f"(l[0]), "f"(l[1]), "f"(l[2]), "f"(l[3]), "n"(1u << J));
+  } else {
+    asm("{\n\t.reg .pred q1, q0;\n\t.reg .f32 ta;\n\t"
+        "setp.gt.f32 q1, %2, %3;\n\t@q1 or.b32 %0, %0, %6;\n\t"
+        "selp.f32 ta, %5, %4, q1;\n\t"
+        "setp.gt.f32 q0, %2, ta;\n\t@q0 or.b32 %1, %1, %6;\n\t}"
+        : "+r"(pl[1]), "+r"(pl[0])
+        : "f"(y), "f"(t[1]), "f"(t[0]), "f"(t[2]), "n"(1u << J));
+  }
+  return lev;
+}
+
+// f(integral_constant<int, J>) for J = 0 .. N-1 (compile-time bit positions).
+template <typename F, int... Js>
+__device__ __forceinline__ void for_each_index(F&& f, std::integer_sequence<int, Js...>) {
+  (f(std::integral_constant<int, Js>{}), ...);
 }
 
 // Byte offset, within an X tile, of the first 16-byte chunk that the thread of
@@ -409,16 +459,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int p = 0; p < BITS; ++p) planes[p] = 0;
         float r[32];
+        if constexpr (BITS == 2 || BITS == 3) {
+          for_each_index(
+              [&](auto jc) {
+                constexpr int j = decltype(jc)::value;
+                const float yv = __uint_as_float(yr[j]);
+                const float lv = decide<BITS, QJL, j>(yv, tn, lev, planes);
+                if (QJL) {
+                  r[j] = fmaf(-n, lv, yv);
+                  rs = fmaf(r[j], r[j], rs);
+                }
+              },
+              std::make_integer_sequence<int, 32>{});
+        } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float yv = __uint_as_float(yr[j]);
-          bool bits[BITS];
-          code_bits<BITS>(yv, tn, bits);
+          for (int j = 0; j < 32; ++j) {
+            const float yv = __uint_as_float(yr[j]);
+            bool bits[BITS];
+            code_bits<BITS>(yv, tn, bits);
 #pragma unroll
-          for (int p = 0; p < BITS; ++p) planes[p] |= bits[p] ? (1u << j) : 0u;
-          if (QJL) {
-            r[j] = fmaf(-n, level_of<BITS>(lev, bits), yv);
-            rs = fmaf(r[j], r[j], rs);
+            for (int p = 0; p < BITS; ++p) planes[p] |= bits[p] ? (1u << j) : 0u;
+            if (QJL) {
+              r[j] = fmaf(-n, level_of<BITS>(lev, bits), yv);
+              rs = fmaf(r[j], r[j], rs);
+            }
           }
         }
         if (QJL) {
