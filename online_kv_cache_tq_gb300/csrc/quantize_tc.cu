@@ -370,8 +370,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(&z_empty);
       ptx::mbar_arrive(&y_empty[j % 3]);          // its residual has been consumed too
       uint32_t word = 0;
-#pragma unroll
-      for (int k = 0; k < 32; ++k) word |= (__uint_as_float(zr[k]) > 0.f ? 1u : 0u) << k;
+      for_each_index(
+          [&](auto kc) {
+            constexpr int k = decltype(kc)::value;
+            // bit k = (z_k > 0), as a predicated OR
+            asm("{\n\t.reg .pred q;\n\tsetp.gt.f32 q, %1, 0f00000000;\n\t@q or.b32 %0, %0, %2;\n\t}"
+                : "+r"(word)
+                : "f"(__uint_as_float(zr[k])), "n"(1u << k));
+          },
+          std::make_integer_sequence<int, 32>{});
       if (dstp >= 0) {
         reinterpret_cast<uint32_t*>(a.qjl + dstp * 16)[g] = word;
         const float* r4 = rs_s + (j & 1) * 4 * kTileRows + row;
