@@ -669,6 +669,15 @@ tq_status tq_decode_step_host(const tq_codebook* book, const void* k_new_h, cons
   void* q_d = base + round_up(h.k) + round_up(h.v);
   int32_t* ctx_d = reinterpret_cast<int32_t*>(base + round_up(h.k) + round_up(h.v) + round_up(h.q));
   float* out_d = reinterpret_cast<float*>(base + round_up(h.k) + round_up(h.v) + round_up(h.q) + round_up(h.ctx));
+  // every check of the step (handle, shapes, cache, workspace) before a copy is queued
+  {
+    tq::QuantizeArgs ka{}, va{};
+    tq::DecodeArgs a;
+    const tq_status chk = step_args(book, k_d, v_d, kv_dtype, q_d, q_dtype, batch, n_q_heads, n_kv_heads, cache,
+                                    block_table, max_blocks, ctx_d, max_context, scale, out_d, base + h.total,
+                                    workspace_bytes - h.total, kPrepare | kPartials | kFinish, &ka, &va, &a);
+    if (chk != TQ_OK) return chk;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err = cudaMemcpyAsync(k_d, k_new_h, h.k, cudaMemcpyHostToDevice, s);
   if (err == cudaSuccess) err = cudaMemcpyAsync(v_d, v_new_h, h.v, cudaMemcpyHostToDevice, s);

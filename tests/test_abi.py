@@ -81,6 +81,14 @@ def test_host_only_handle_rejected_by_kernels(lib):
     assert lib.tq_quantize_append(book.handle, 16, 16, 0, 1, 1, 16, ctypes.byref(view), None) == 1
     assert lib.tq_decode_attention(book.handle, 16, 0, 1, 1, 1, ctypes.byref(view), None, 1, 16, 64, 0.0,
                                    16, 256, 1 << 20, None) == 1
+    # the host-buffer step validates the whole step before it queues a copy
+    ws_bytes = lib.tq_decode_step_host_workspace_bytes(book.handle, 1, 1, 1, 64, 0, 0)
+    assert ws_bytes > 0
+    assert lib.tq_decode_step_host(book.handle, 16, 16, 0, 16, 0, 1, 1, 1, ctypes.byref(view), 16, 1, 16, 64,
+                                   0.0, 16, 256, ws_bytes, None) == 1
+    assert lib.tq_decode_step_host(None, 16, 16, 0, 16, 0, 1, 1, 1, ctypes.byref(view), 16, 1, 16, 64, 0.0,
+                                   16, 256, ws_bytes, None) == 1
+    assert lib.tq_decode_step_host_workspace_bytes(book.handle, 1, 1, 1, 64, 7, 0) == 0
     code = ctypes.c_int()
     assert lib.tq_get_last_device_error(book.handle, None, ctypes.byref(code)) == 1
     assert lib.tq_codebook_destroy(None) == 1
