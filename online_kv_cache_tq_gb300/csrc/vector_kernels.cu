@@ -203,65 +203,89 @@ __device__ __forceinline__ int context_of(const DecodeArgs& a, int b) {
   return ctx;
 }
 
-// out[vec] = R^T (merged acc / merged l).  512 threads: thread (o, q) merges
-// coordinate o over the chunks c with c % 4 == q as a running (m, l, acc), the
-// four copies of o merge theirs, and the copies split the back-rotation.
-// Every thread's chunk loads are independent, so a launch is a few memory
-// round trips long.
+// out[v] = R^T (merged acc / merged l) for the query heads v = 2 blockIdx.x
+// and 2 blockIdx.x + 1 (one head when the count is odd).  512 threads:
+// thread (o, q) merges coordinate o of head q / 2 over the chunks c with
+// c % 2 == q % 2 as a running (m, l, acc); the two copies of a head merge
+// theirs; then thread (o, q) sums the terms [32 q, 32 q + 32) of both heads'
+// back-rotations from one set of loads of R.  Every thread's chunk loads are
+// independent, so a launch is a few memory round trips long.
 __global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
-  __shared__ float o_s[kDim];
-  __shared__ float red_s[4 * kDim];
+  constexpr int kHeads = 2;
+  __shared__ float o_s[kHeads][kDim];
+  __shared__ float red_s[4][kHeads][kDim];
   __shared__ float ml_s[2][4];
-  const int vec = blockIdx.x;
-  const int b = vec / a.n_q;
   const int t = threadIdx.x;
   const int o = t & 127, q = t >> 7;
+  const int n_vec = a.batch * a.n_q;
+  const int vec = kHeads * blockIdx.x + (q >> 1);           // this thread's head in the merge
+  const bool live = vec < n_vec;
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the partials (no-op unless launched early)
-  const int ctx = context_of(a, b);
-  const int n_chunks = (ctx + kChunk - 1) / kChunk;
-  const float* part = a.ws_part + static_cast<long long>(vec) * a.max_chunks * kPartStride;
   float m = -INFINITY, l = 0.f, acc = 0.f;
-  for (int c0 = q; c0 < n_chunks; c0 += 4 * 4) {
-    float mc[4], lc[4], ac[4];
+  if (live) {
+    const int ctx = context_of(a, vec / a.n_q);
+    const int n_chunks = (ctx + kChunk - 1) / kChunk;
+    const float* part = a.ws_part + static_cast<long long>(vec) * a.max_chunks * kPartStride;
+    for (int c0 = q & 1; c0 < n_chunks; c0 += 2 * 4) {
+      float mc[4], lc[4], ac[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = c0 + 4 * j;
-      mc[j] = c < n_chunks ? part[c * kPartStride] : -INFINITY;
-      lc[j] = c < n_chunks ? part[c * kPartStride + 1] : 0.f;
-      ac[j] = c < n_chunks ? part[c * kPartStride + 4 + o] : 0.f;
-    }
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + 2 * j;
+        mc[j] = c < n_chunks ? part[c * kPartStride] : -INFINITY;
+        lc[j] = c < n_chunks ? part[c * kPartStride + 1] : 0.f;
+        ac[j] = c < n_chunks ? part[c * kPartStride + 4 + o] : 0.f;
+      }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (mc[j] == -INFINITY) continue;
-      const float mn = fmaxf(m, mc[j]);
-      const float so = m == -INFINITY ? 0.f : __expf(m - mn), sn = __expf(mc[j] - mn);
-      l = fmaf(l, so, lc[j] * sn);
-      acc = fmaf(acc, so, ac[j] * sn);
-      m = mn;
+      for (int j = 0; j < 4; ++j) {
+        if (mc[j] == -INFINITY) continue;
+        const float mn = fmaxf(m, mc[j]);
+        const float so = m == -INFINITY ? 0.f : __expf(m - mn), sn = __expf(mc[j] - mn);
+        l = fmaf(l, so, lc[j] * sn);
+        acc = fmaf(acc, so, ac[j] * sn);
+        m = mn;
+      }
     }
   }
-  red_s[q * kDim + o] = acc;
+  red_s[q][0][o] = acc;
   if (o == 0) {
     ml_s[0][q] = m;
     ml_s[1][q] = l;
   }
   __syncthreads();
-  if (q == 0) {
-    float mt = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) mt = fmaxf(mt, ml_s[0][c]);
+  if ((q & 1) == 0) {                             // copies q and q + 1 of head q / 2
+    const float mt = fmaxf(ml_s[0][q], ml_s[0][q + 1]);
     float lt = 0.f, at = 0.f;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float w = ml_s[0][c] == -INFINITY ? 0.f : __expf(ml_s[0][c] - mt);
-      lt = fmaf(w, ml_s[1][c], lt);
-      at = fmaf(w, red_s[c * kDim + o], at);
+    for (int c = 0; c < 2; ++c) {
+      const float w = ml_s[0][q + c] == -INFINITY ? 0.f : __expf(ml_s[0][q + c] - mt);
+      lt = fmaf(w, ml_s[1][q + c], lt);
+      at = fmaf(w, red_s[q + c][0][o], at);
     }
-    o_s[o] = lt > 0.f ? at / lt : 0.f;
+    o_s[q >> 1][o] = lt > 0.f ? at / lt : 0.f;
   }
   __syncthreads();
-  const float out = gemv<kGemvThreads>(a.R, o_s, red_s);
-  if (q == 0) a.out[static_cast<long long>(vec) * kDim + o] = out;
+  // out[h][o] = sum_i R[o][i] o_s[h][i]: R stored as w[i * 128 + o]; thread q takes i in [32 q, 32 q + 32)
+  float s0 = 0.f, s1 = 0.f;
+  {
+    const float* wp = a.R + (32 * q) * kDim + o;
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = __ldg(wp + k * kDim);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      s0 = fmaf(v[k], o_s[0][32 * q + k], s0);
+      s1 = fmaf(v[k], o_s[1][32 * q + k], s1);
+    }
+  }
+  red_s[q][0][o] = s0;
+  red_s[q][1][o] = s1;
+  __syncthreads();
+  if (q < kHeads) {
+    const int v = kHeads * blockIdx.x + q;
+    if (v < n_vec)
+      a.out[static_cast<long long>(v) * kDim + o] =
+          (red_s[0][q][o] + red_s[1][q][o]) + (red_s[2][q][o] + red_s[3][q][o]);
+  }
 }
 
 // Blocks [0, first.n_vec) quantize `first`, the rest `second` (K and V of one
@@ -316,7 +340,7 @@ cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream, bo
   const int n_vec = args.batch * args.n_q;
   if (n_vec <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_vec);
+  cfg.gridDim = dim3((n_vec + 1) / 2);             // two query heads per block
   cfg.blockDim = dim3(kGemvThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
