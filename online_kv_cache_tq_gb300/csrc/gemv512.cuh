@@ -1,12 +1,12 @@
-// 128 x 128 matrix-vector products for the per-vector kernels of one decode
-// step (append, query preparation, combine): one CTA per vector, THREADS =
-// 128 * copies threads, thread (o, q = threadIdx.x / 128) working on output o.
+// 128 x 128 matrix-vector product and reductions for the per-vector kernels
+// of one decode step: THREADS = 128 * copies threads, thread (o, q =
+// threadIdx.x / 128) working on output o.
 #pragma once
 
 namespace tq {
 
-constexpr int kGemvThreads = 512;   // combine: four copies of every coordinate
-constexpr int kVecThreads = 256;    // append and query preparation: two copies
+constexpr int kGemvThreads = 512;   // merge: four threads per coordinate
+constexpr int kVecThreads = 256;    // append and query preparation: two threads per coordinate
 
 // out[o] = sum_i w[i * 128 + o] * in_s[i] for o = threadIdx.x % 128.  Thread
 // (o, q) sums the 128 / copies terms i in [q * 128 / copies, ...) in batches of
@@ -50,17 +50,6 @@ __device__ __forceinline__ float sum128(float v, float* part_s) {
   if (threadIdx.x < 128 && (threadIdx.x & 31) == 0) part_s[threadIdx.x >> 5] = v;
   __syncthreads();
   const float s = (part_s[0] + part_s[1]) + (part_s[2] + part_s[3]);
-  __syncthreads();
-  return s;
-}
-
-// Maximum of v over the 128 values o, as sum128.
-__device__ __forceinline__ float max128(float v, float* part_s) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-  if (threadIdx.x < 128 && (threadIdx.x & 31) == 0) part_s[threadIdx.x >> 5] = v;
-  __syncthreads();
-  const float s = fmaxf(fmaxf(part_s[0], part_s[1]), fmaxf(part_s[2], part_s[3]));
   __syncthreads();
   return s;
 }

@@ -1,7 +1,8 @@
-// Per-vector kernels of a decode step, one CTA per head vector (256 threads
-// for the append and the query preparation, 512 for the merge): quantize-append of the step's new keys and values, the query
-// preparation of decode attention (a fused launch runs both for a step), and
-// the merge of the split-K partials with the back-rotation.
+// Per-vector kernels of a decode step: quantize-append of the step's new keys
+// and values (one vector per 256-thread CTA), the query preparation of decode
+// attention (two query heads per 256-thread CTA; a fused launch runs both for
+// a step), and the merge of the split-K partials with the back-rotation (two
+// query heads per 512-thread CTA).
 //
 // Same arithmetic as the tile quantizers (甲子光年 article §2 第一階段 /
 // 第二階段) and the decode estimator (§2 第二階段: <q, k> ~= n <R q, c[code]>
@@ -204,7 +205,7 @@ __device__ __forceinline__ int context_of(const DecodeArgs& a, int b) {
 }
 
 // out[v] = R^T (merged acc / merged l) for the query heads v = 2 blockIdx.x
-// and 2 blockIdx.x + 1 (one head when the count is odd).  512 threads:
+// and 2 blockIdx.x + 1 (one head when the count is odd).  kGemvThreads = 512:
 // thread (o, q) merges coordinate o of head q / 2 over the chunks c with
 // c % 2 == q % 2 as a running (m, l, acc); the two copies of a head merge
 // theirs; then thread (o, q) sums the terms [32 q, 32 q + 32) of both heads'
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
   __shared__ float ml_s[2][4];
   const int t = threadIdx.x;
   const int o = t & 127, q = t >> 7;
+  static_assert(kGemvThreads == 512, "threads (o, q) with q = 0..3");
   const int n_vec = a.batch * a.n_q;
   const int vec = kHeads * blockIdx.x + (q >> 1);           // this thread's head in the merge
   const bool live = vec < n_vec;
