@@ -2,18 +2,26 @@
 """Benchmark of the TurboQuant KV-cache hot path on GB300.
 
 One step = the whole per-layer decode path for one batch: quantize-append of
-each sequence's new K/V token into the packed 3-bit cache, then decode
-attention of every query head over the full packed context (query prep,
-split-K attention, merge + back-rotation).  Default workload: Llama-3-8B-shaped
-decode layer (batch 16, 32 query heads, 8 KV heads, d 128, context 8192,
-3-bit K = 2-bit MSE + 1-bit QJL, 3-bit V), synthetic bf16 K/V with
-log-uniform per-channel scales and 2% outlier channels.
+each sequence's new K/V token into the packed cache, then decode attention of
+every query head over the full packed context (query preparation, split-K
+attention with the merge and back-rotation in the same kernel).
+
+Headline workload (the largest single-GPU configuration): a Llama-3-70B-shaped
+paged decode layer -- batch 64, 64 query heads, 8 KV heads, d 128, context
+lengths drawn uniformly from [1024, 32768], 64-token blocks under a shuffled
+block table, 3-bit K (2-bit MSE + 1-bit QJL) and 3-bit V, synthetic bf16 K/V
+with log-uniform per-channel scales.  The same JSON line carries secondary
+figures for the other workloads: the Llama-3-8B decode layer, the 128 K-token
+long-context case, the fp32 single-head case and the prefill quantize-append
+at 2, 3 and 4 bits.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
-oracle on the host cores on the same workload (bounded sample per step).
+oracle on the host cores on the headline workload (bounded sample per step).
 Multi-GPU: one process per GPU under torchrun; every rank runs its own
 replica (different seeds: weak scaling, no data-path collective); the step
-time is the max over ranks.
+time is the max over ranks.  The oracle runs only in the CPU leg: the timed
+oracle sample (cpu_baseline) and, on the same host pass, the parity figures
+(the GPU's codes and outputs against the oracle on sampled inputs).
 """
 import argparse
 import hashlib
@@ -33,19 +41,24 @@ if ROOT not in sys.path:
 L2_BYTES = 129 * 10 ** 6
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-METRIC = "decode attention tokens/s over the packed 3-bit KV cache"
+METRIC = "decode attn tokens/s & HBM GB/s (% of peak) over 3-bit KV; quantize vectors/s"
+HEADLINE = "c5_llama3_70b_paged"
+SECONDARY_DECODE = ("c2_llama3_8b_decode", "c4_long_context")
+CODE_EXEMPT = 1e-5          # codes within this distance of a boundary (unit-vector units) may differ
+ATTN_TOL = 1e-3             # max |o_gpu - o_oracle| / max_t ||v_hat_t||
 
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="c2_llama3_8b_decode")
-    p.add_argument("--cpu-groups", type=int, default=48, help="oracle (sequence, KV head) groups timed")
-    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--workload", default=HEADLINE)
+    p.add_argument("--cpu-groups", type=int, default=32, help="oracle (sequence, KV head) groups timed")
+    p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle leg (timing and parity)")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-secondary", action="store_true", help="headline workload only")
     return p.parse_args(argv)
 
 
@@ -140,79 +153,29 @@ class ClockSampler:
 
 # ------------------------------------------------------- roofline inputs --
 
-def hbm_peak():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def _peaks():
     try:
-        with open(path) as fh:
-            return float(json.load(fh)["hbm_gbs"]), "measured"
-    except (OSError, KeyError, ValueError):
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh)
+    except (OSError, ValueError):
+        return None
+
+
+def hbm_peak():
+    p = _peaks()
+    try:
+        return float(p["hbm_gbs"]), "measured"
+    except (TypeError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
 
 
 def bf16_peak():
     """Burst bf16 dense tensor TFLOP/s (a kernel timed alone), measured or fallback."""
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    p = _peaks()
     try:
-        with open(path) as fh:
-            return float(json.load(fh)["bf16_tflops"]), "measured"
-    except (OSError, KeyError, ValueError):
+        return float(p["bf16_tflops"]), "measured"
+    except (TypeError, KeyError, ValueError):
         return FALLBACK_BF16_TFLOPS, "fallback"
-
-
-def measure_prefill_quantize(steps, warmup):
-    """Secondary figure: quantize-append throughput of a prefill of 32768 tokens
-    x 8 KV heads (bf16, 3-bit keys = 2 MSE bits + QJL, 3-bit values), two
-    input copies rotated so the 128 MB of inputs are read from HBM."""
-    import numpy as np
-    import torch
-
-    from online_kv_cache_tq_gb300 import binding as B
-    from online_kv_cache_tq_gb300 import cache as C
-    from online_kv_cache_tq_gb300 import workloads as W
-    cfg = W.CONFIGS["c3_prefill_quantize"]
-    n_tok, n_kv = cfg["tokens"], cfg["n_kv"]
-    book = B.Codebook(k_bits=3, v_bits=3, qjl_m=cfg["qjl_m"], seed=cfg["seed"], block_size=cfg["block_size"],
-                      device=torch.cuda.current_device())
-    g = torch.Generator(device="cuda")
-    g.manual_seed(cfg["seed"])
-    inputs = [(W.student_t_tokens(n_tok, n_kv, cfg["student_t_channels"], torch.bfloat16, "cuda", g, 2 * i),
-               W.student_t_tokens(n_tok, n_kv, cfg["student_t_channels"], torch.bfloat16, "cuda", g, 2 * i + 1))
-              for i in range(2)]
-    cache = C.allocate_cache(book, n_tok // cfg["block_size"], n_kv)
-    view = C.cache_view(book, cache)
-    slots = torch.arange(n_tok, device="cuda", dtype=torch.int64)
-
-    def append(i):
-        k, v = inputs[i % 2]
-        B.tq_quantize_append(book, k, v, B.TQ_BF16, n_tok, n_kv, slots, view)
-
-    for i in range(warmup):
-        append(i)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    start.record()
-    for i in range(steps):
-        append(i)
-    end.record()
-    torch.cuda.synchronize()
-    if B.tq_get_last_device_error(book):
-        raise RuntimeError("device error during the prefill quantize measurement")
-    secs = start.elapsed_time(end) * 1e-3 / steps
-    vectors = 2 * n_tok * n_kv
-    field = C.cache_bytes_per_token_head(book)
-    nbytes = vectors * 256 + n_tok * n_kv * field            # bf16 reads + packed writes
-    flops = n_tok * n_kv * (2 * 32768) + n_tok * n_kv * 32768  # K: rotation + QJL, V: rotation
-    hbm, _ = hbm_peak()
-    tensor, tensor_src = bf16_peak()
-    rec = [recorded_traffic(k, "c3_prefill_quantize") for k in ("quantize_tc_kernel<2,1,0>", "quantize_tc_kernel<3,0,1>")]
-    traffic = sum(rec) if all(r is not None for r in rec) else None
-    return {"workload": "c3_prefill_quantize", "tokens": n_tok, "n_kv_heads": n_kv, "k_bits": 3, "v_bits": 3,
-            "ms_per_append": secs * 1e3, "vectors_per_s": vectors / secs,
-            "hbm_gbs": nbytes / secs / 1e9, "hbm_frac": nbytes / secs / 1e9 / hbm,
-            "algorithmic_tflops": flops / secs / 1e12, "tensor_frac": flops / secs / 1e12 / tensor,
-            "tensor_peak": tensor, "tensor_peak_source": tensor_src + " bf16_tflops",
-            "algorithmic_bytes_per_append": nbytes, "traffic_bytes_per_append": traffic,
-            "note": "algorithmic flops; the bf16 hi/lo splitting runs 2 (rotation) and 3 (QJL) tensor passes"}
 
 
 def source_digest(rel):
@@ -234,6 +197,11 @@ def recorded_traffic(kernel, workload):
     return rec.get("dram_bytes_per_launch")
 
 
+def events(n):
+    import torch
+    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+
+
 # --------------------------------------------------------- decode (ours) --
 
 class DecodeWorkload:
@@ -251,6 +219,7 @@ class DecodeWorkload:
         cfg = W.CONFIGS[name]
         self.cfg = cfg
         self.name = name
+        self.seed = seed
         self.batch, self.n_q, self.n_kv = cfg["batch"], cfg["n_q"], cfg["n_kv"]
         self.book = B.Codebook(k_bits=cfg["k_bits"], v_bits=cfg["v_bits"], qjl_m=cfg["qjl_m"], seed=cfg["seed"],
                                block_size=cfg["block_size"], device=device)
@@ -290,8 +259,10 @@ class DecodeWorkload:
         self.ws, self.ws_bytes = C.allocate_workspace(self.book, self.batch, self.n_q, self.max_ctx)
         torch.cuda.synchronize()
         # tq_decode_step: append + query preparation (one launch up to 1024 head vectors, else
-        # quantize K, quantize V, prepare), partials, merge
-        self.launches_per_step = (1 if self.batch * self.n_kv <= 1024 else 3) + 2
+        # quantize K, quantize V, prepare), then the partials kernel that also merges (tensor
+        # cores) or partials + merge (CUDA cores)
+        self.tc = B.tq_decode_kernel_kind(self.book, self.n_q, self.n_kv) == 1
+        self.launches_per_step = (1 if self.batch * self.n_kv <= 1024 else 3) + (1 if self.tc else 2)
 
     def step(self, i):
         """One decode step: tq_decode_step (append the new K/V token of every
@@ -301,21 +272,18 @@ class DecodeWorkload:
                               self.max_blocks, self.ctx_d, self.max_ctx, 0.0, self.out, self.ws, self.ws_bytes)
 
     def staged_step(self, i, ev):
-        """The same step through the staged calls (same kernels, without the
-        early start of the partials kernel), with events around the partials."""
+        """The same step through the staged calls: the append + query
+        preparation, then (between the events) the partials kernel exactly as
+        the step runs it -- it merges and writes the output itself."""
         B = self.B
         view = self.views[i % len(self.views)]
         B.tq_decode_step_prepare(self.book, self.k_new, self.v_new, self.dtype_code, self.q, self.dtype_code,
                                  self.batch, self.n_q, self.n_kv, view, self.table_d, self.max_blocks, self.ctx_d,
                                  self.max_ctx, self.ws, self.ws_bytes)
-        if ev is not None:
-            ev[0].record()
+        ev[0].record()
         B.tq_decode_partials(self.book, self.batch, self.n_q, self.n_kv, view, self.table_d, self.max_blocks,
-                             self.ctx_d, self.max_ctx, 0.0, self.ws, self.ws_bytes)
-        if ev is not None:
-            ev[1].record()
-        B.tq_decode_finish(self.book, self.batch, self.n_q, self.ctx_d, self.max_ctx, self.max_blocks, self.out,
-                           self.ws, self.ws_bytes)
+                             self.ctx_d, self.max_ctx, 0.0, self.ws, self.ws_bytes, out=self.out)
+        ev[1].record()
 
     def e2e(self, steps, warmup):
         """Same step through the one-call C entry point for host buffers
@@ -347,53 +315,249 @@ class DecodeWorkload:
             one(i)
         return time.perf_counter() - t0, h2d, d2h
 
+    def kernel_name(self):
+        return ("attention_tc_kernel<%d>" if self.tc else "attention_kernel<%d>") % (self.n_q // self.n_kv)
+
+    def parity_sample(self, n_groups, seed):
+        """Host copies for the oracle check of ``n_groups`` sampled (sequence,
+        KV head) groups: each group's sequence blocks of every cache field (the
+        state the last step decoded), the group's queries and GPU outputs."""
+        np, torch = self.np, self.torch
+        rng = np.random.default_rng(seed)
+        groups = sorted({(int(rng.integers(self.batch)), int(rng.integers(self.n_kv))) for _ in range(n_groups)})
+        out_h = self.out.cpu().numpy()
+        q_h = self.q.double().cpu().numpy()
+        bs = self.cfg["block_size"]
+        items = []
+        for b, kvh in groups:
+            n_blk = (int(self.ctx[b]) + bs - 1) // bs
+            idx = torch.as_tensor(self.table[b, :n_blk].astype(np.int64), device="cuda")
+            fields = {name: t.index_select(0, idx).cpu().numpy() for name, t in self.caches[0].items()}
+            g = self.n_q // self.n_kv
+            items.append({"b": b, "kvh": kvh, "ctx": int(self.ctx[b]), "cache": fields,
+                          "q": q_h[b, kvh * g:(kvh + 1) * g], "out": out_h[b, kvh * g:(kvh + 1) * g]})
+        return {"workload": self.name, "k_bits": self.cfg["k_bits"], "v_bits": self.cfg["v_bits"],
+                "qjl_m": self.cfg["qjl_m"], "seed": self.cfg["seed"], "groups": items}
+
+
+def measure_decode(name, steps, warmup, seed, clocks=None, with_e2e=False, parity_groups=0):
+    """Decode step time and the partials kernel's time for one workload."""
+    import torch
+    wl = DecodeWorkload(name, torch.cuda.current_device(), seed)
+    for i in range(warmup):
+        wl.step(i)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clocks is not None:
+        clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(steps):
+        wl.step(warmup + i)
+    end.record()
+    torch.cuda.synchronize()
+    barrier()
+    # the dominant kernel's duration: the same steps through the staged calls,
+    # with events around each partials launch on the launching stream
+    ev = events(steps)
+    for i in range(steps):
+        wl.staged_step(warmup + steps + i, ev[i])
+    torch.cuda.synchronize()
+    clock_info = clocks.stop() if clocks is not None else None
+    if wl.B.tq_get_last_device_error(wl.book):
+        raise RuntimeError("device error during the %s benchmark" % name)
+    # one more step, so that the output and cache match for the parity sample
+    wl.step(0)
+    torch.cuda.synchronize()
+    step_ms = start.elapsed_time(end) / steps
+    part_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    res = {"wl": wl, "step_ms": step_ms, "partials_ms": part_ms, "clocks": clock_info}
+    if with_e2e:
+        res["e2e"] = wl.e2e(steps, min(warmup, 5))
+    if parity_groups:
+        res["parity_sample"] = wl.parity_sample(parity_groups, seed + 5)
+    return res
+
+
+def decode_summary(res, world, dev):
+    """Secondary-line figures of one decode workload (max over ranks)."""
+    wl = res["wl"]
+    step_ms = max_over_ranks(res["step_ms"], dev)
+    part_ms = max_over_ranks(res["partials_ms"], dev)
+    peak, src = hbm_peak()
+    achieved = wl.cache_bytes / (part_ms * 1e-3) / 1e9
+    return {
+        "workload": wl.name, "ms_per_step": step_ms, "tokens_per_s": world * wl.batch / (step_ms * 1e-3),
+        "kv_token_heads_per_s": world * float(wl.ctx.sum()) * wl.n_kv / (step_ms * 1e-3),
+        "hbm_gbs_step": wl.cache_bytes / (step_ms * 1e-3) / 1e9,
+        "bytes_per_token_head": wl.bytes_per_token_head,
+        "compression_vs_bf16": 4.0 * 128 / wl.bytes_per_token_head,
+        "partials": {"kernel": wl.kernel_name(), "launch_ms": part_ms, "achieved_gbs": achieved,
+                     "frac": achieved / peak, "peak_source": src + " hbm_gbs",
+                     "algorithmic_bytes_per_launch": wl.cache_bytes},
+        "context_tokens": int(wl.ctx.sum()), "l2": l2_note(len(wl.caches)),
+    }
+
+
+def l2_note(copies):
+    return ("inputs larger than L2: steps rotate over %d cache copies" % copies if copies > 1
+            else "inputs larger than L2: one cache larger than 2x L2")
+
+
+# ------------------------------------------------------ quantize (ours) --
+
+def measure_quantize(bits, steps, warmup, sample_tokens=0):
+    """Prefill quantize-append of 32768 tokens x 8 KV heads (bf16, Student-t
+    outlier channels) at ``bits`` per K (bits - 1 MSE + QJL) and V; two input
+    copies rotated so the 128 MB of inputs are read from HBM."""
+    import numpy as np
+    import torch
+
+    from online_kv_cache_tq_gb300 import binding as B
+    from online_kv_cache_tq_gb300 import cache as C
+    from online_kv_cache_tq_gb300 import workloads as W
+    cfg = W.CONFIGS["c3_prefill_quantize"]
+    n_tok, n_kv = cfg["tokens"], cfg["n_kv"]
+    book = B.Codebook(k_bits=bits, v_bits=bits, qjl_m=cfg["qjl_m"], seed=cfg["seed"], block_size=cfg["block_size"],
+                      device=torch.cuda.current_device())
+    g = torch.Generator(device="cuda")
+    g.manual_seed(cfg["seed"] + bits)
+    inputs = [(W.student_t_tokens(n_tok, n_kv, cfg["student_t_channels"], torch.bfloat16, "cuda", g, 2 * i),
+               W.student_t_tokens(n_tok, n_kv, cfg["student_t_channels"], torch.bfloat16, "cuda", g, 2 * i + 1))
+              for i in range(2)]
+    cache = C.allocate_cache(book, n_tok // cfg["block_size"], n_kv)
+    view = C.cache_view(book, cache)
+    slots = torch.arange(n_tok, device="cuda", dtype=torch.int64)
+
+    def append(i):
+        k, v = inputs[i % 2]
+        B.tq_quantize_append(book, k, v, B.TQ_BF16, n_tok, n_kv, slots, view)
+
+    for i in range(warmup):
+        append(i)
+    ev = events(steps)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        ev[i][0].record()
+        append(i)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    if B.tq_get_last_device_error(book):
+        raise RuntimeError("device error during the quantize measurement")
+    secs = sum(a.elapsed_time(b) for a, b in ev) * 1e-3 / steps
+    vectors = 2 * n_tok * n_kv
+    field = C.cache_bytes_per_token_head(book)
+    nbytes = vectors * 256 + n_tok * n_kv * field            # bf16 reads + packed writes
+    flops = n_tok * n_kv * (2 * 32768) + n_tok * n_kv * 32768  # K: rotation + QJL, V: rotation
+    hbm, _ = hbm_peak()
+    tensor, tensor_src = bf16_peak()
+    kb = bits - 1
+    rec = [recorded_traffic(k, "c3_prefill_quantize") for k in
+           ("quantize_tc_kernel<%d,1,0>" % kb, "quantize_tc_kernel<%d,0,1>" % bits)]
+    traffic = sum(rec) if all(r is not None for r in rec) else None
+    res = {"workload": "c3_prefill_quantize", "tokens": n_tok, "n_kv_heads": n_kv, "k_bits": bits, "v_bits": bits,
+           "ms_per_append": secs * 1e3, "vectors_per_s": vectors / secs,
+           "hbm_gbs": nbytes / secs / 1e9, "hbm_frac": nbytes / secs / 1e9 / hbm,
+           "algorithmic_tflops": flops / secs / 1e12, "tensor_frac": flops / secs / 1e12 / tensor,
+           "tensor_peak_source": tensor_src + " bf16_tflops",
+           "algorithmic_bytes_per_append": nbytes, "traffic_bytes_per_append": traffic,
+           "note": "algorithmic flops; the bf16 hi/lo splitting runs 2 (rotation) and 3 (QJL) tensor passes"}
+    sample = None
+    if sample_tokens:
+        # the last append wrote inputs[(steps - 1) % 2]: sampled tokens and their cache rows on the host
+        k, v = inputs[(steps - 1) % 2]
+        toks = np.sort(np.random.default_rng(bits).choice(n_tok, size=sample_tokens, replace=False))
+        idx = torch.as_tensor(toks, device="cuda")
+        sample = {"bits": bits, "qjl_m": cfg["qjl_m"], "seed": cfg["seed"], "block_size": cfg["block_size"],
+                  "slots": toks, "k": k.index_select(0, idx).double().cpu().numpy(),
+                  "v": v.index_select(0, idx).double().cpu().numpy(),
+                  "cache": {name: t.cpu().numpy() for name, t in cache.items()}}
+    return res, sample
+
+
+def measure_single_head_fp32(steps, warmup):
+    """The fp32 single-head workload: quantize-append of 4096 keys and 4096
+    values (4 outlier channels x20) and decode of one query over them."""
+    import numpy as np
+    import torch
+
+    from online_kv_cache_tq_gb300 import binding as B
+    from online_kv_cache_tq_gb300 import cache as C
+    from online_kv_cache_tq_gb300 import workloads as W
+    cfg = W.CONFIGS["c1_single_head_parity"]
+    n = cfg["context"]
+    book = B.Codebook(k_bits=cfg["k_bits"], v_bits=cfg["v_bits"], qjl_m=cfg["qjl_m"], seed=cfg["seed"],
+                      block_size=cfg["block_size"], device=torch.cuda.current_device())
+    g = torch.Generator(device="cuda")
+    g.manual_seed(cfg["seed"])
+    k = W.gaussian_tokens(n, W.channel_scales(0, 1, None, 4, 20.0), torch.float32, "cuda", g)
+    v = W.gaussian_tokens(n, W.channel_scales(1, 1, None, 4, 20.0), torch.float32, "cuda", g)
+    cache = C.allocate_cache(book, n // cfg["block_size"], 1)
+    view = C.cache_view(book, cache)
+    slots = torch.arange(n, device="cuda", dtype=torch.int64)
+    q = W.queries(1, 1, torch.float32, "cuda", g)
+    ctx = torch.full((1,), n, dtype=torch.int32, device="cuda")
+    ws, nbytes = C.allocate_workspace(book, 1, 1, n)
+    out = torch.empty((1, 1, 128), device="cuda")
+    for _ in range(warmup):
+        B.tq_quantize_append(book, k, v, B.TQ_FP32, n, 1, slots, view)
+        B.tq_decode_attention(book, q, B.TQ_FP32, 1, 1, 1, view, None, n // cfg["block_size"], ctx, n, 0.0, out,
+                              ws, nbytes)
+    eq, ed = events(steps), events(steps)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        eq[i][0].record()
+        B.tq_quantize_append(book, k, v, B.TQ_FP32, n, 1, slots, view)
+        eq[i][1].record()
+        ed[i][0].record()
+        B.tq_decode_attention(book, q, B.TQ_FP32, 1, 1, 1, view, None, n // cfg["block_size"], ctx, n, 0.0, out,
+                              ws, nbytes)
+        ed[i][1].record()
+    torch.cuda.synchronize()
+    if B.tq_get_last_device_error(book):
+        raise RuntimeError("device error during the fp32 single-head measurement")
+    tq_ms = sum(a.elapsed_time(b) for a, b in eq) / steps
+    td_ms = sum(a.elapsed_time(b) for a, b in ed) / steps
+    return {"workload": "c1_single_head_parity", "input_dtype": "fp32", "vectors": 2 * n,
+            "quantize_ms": tq_ms, "quantize_vectors_per_s": 2 * n / (tq_ms * 1e-3),
+            "decode_ms": td_ms, "decode_tokens_per_s": 1.0 / (td_ms * 1e-3),
+            "decode_kv_token_heads_per_s": n / (td_ms * 1e-3),
+            "note": "latency-bound sizes: one head, 4096 tokens"}
+
 
 def run_ours(args, rank, world, local_rank):
     import torch
     torch.cuda.set_device(local_rank)
     import __graft_entry__
     __graft_entry__.build()
-    wl = DecodeWorkload(args.workload, local_rank, rank_seed(0, rank))
-    for i in range(args.warmup):
-        wl.step(i)
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    barrier()
-    torch.cuda.synchronize()
-    start.record()
-    for i in range(args.steps):
-        wl.step(args.warmup + i)
-    end.record()
-    torch.cuda.synchronize()
-    barrier()
-    # the dominant kernel's duration: the same steps through the staged calls,
-    # with events around each partials launch on the launching stream
-    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps):
-        wl.staged_step(args.warmup + args.steps + i, events[i])
-    torch.cuda.synchronize()
-    clock_info = clocks.stop()
-    total_ms = start.elapsed_time(end)
-    attn_ms = sum(a.elapsed_time(b) for a, b in events) / args.steps
-    err = wl.B.tq_get_last_device_error(wl.book)
-    if err:
-        raise RuntimeError("device error %d during the benchmark" % err)
     dev = "cuda" if world > 1 else "cpu"
-    max_ms = max_over_ranks(total_ms, dev)
-    max_attn = max_over_ranks(attn_ms, dev)
-    quant = measure_prefill_quantize(20, 3)
-    e2e = None
-    if not args.no_e2e:
-        secs, h2d, d2h = wl.e2e(args.steps, min(args.warmup, 5))
-        secs = max_over_ranks(secs, dev)
-        e2e = {"value": world * wl.batch * args.steps / secs, "unit": "tokens/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-    return wl, max_ms, max_attn, clock_info, e2e, quant
+    want_parity = rank == 0 and not args.no_cpu_baseline
+    head = measure_decode(args.workload, args.steps, args.warmup, rank_seed(0, rank), ClockSampler(local_rank),
+                          with_e2e=not args.no_e2e, parity_groups=6 if want_parity else 0)
+    out = {"head": head, "secondary": {}, "quant_samples": [], "decode_samples": []}
+    if want_parity:
+        out["decode_samples"].append(head.pop("parity_sample"))
+    if not args.no_secondary:
+        steps = max(20, min(args.steps, 100))
+        for name in SECONDARY_DECODE:
+            if name == args.workload:
+                continue
+            res = measure_decode(name, steps, args.warmup, rank_seed(0, rank), parity_groups=4 if want_parity else 0)
+            out["secondary"][name] = decode_summary(res, world, dev)
+            if want_parity:
+                out["decode_samples"].append(res.pop("parity_sample"))
+            del res
+        for bits in (2, 3, 4):
+            res, sample = measure_quantize(bits, 20, 3, sample_tokens=256 if want_parity else 0)
+            out["secondary"]["c3_prefill_quantize_b%d" % bits] = res
+            if sample is not None:
+                out["quant_samples"].append(sample)
+        out["secondary"]["c1_single_head_parity"] = measure_single_head_fp32(20, 3)
+    return out
 
 
-# ----------------------------------------------------- oracle (reference) --
+# ----------------------------------------------------- oracle (CPU leg) --
 
 def _oracle_group(task):
     """Oracle time for one (sequence, KV head) of a decode step: quantize the
@@ -433,7 +597,8 @@ def _pool_init():
 
 def oracle_throughput(name, n_groups, seed, pool, processes):
     """Decode tokens/s of the oracle on ``processes`` host cores, measured on
-    ``n_groups`` sampled (sequence, KV head) groups of the workload."""
+    ``n_groups`` sampled (sequence, KV head) groups of the workload: the mean
+    group time, scaled to the batch's mean context, times the groups of a step."""
     import numpy as np
 
     from online_kv_cache_tq_gb300 import workloads as W
@@ -444,7 +609,8 @@ def oracle_throughput(name, n_groups, seed, pool, processes):
              for i in range(n_groups)]
     times = pool.map(_oracle_group, tasks)
     per_group = float(np.mean(times)) * float(np.mean(ctx)) / float(np.mean([t[2] for t in tasks]))
-    return processes / (cfg["n_kv"] * per_group), n_groups
+    step_s = cfg["batch"] * cfg["n_kv"] * per_group / processes
+    return cfg["batch"] / step_s, n_groups
 
 
 def oracle_pool():
@@ -453,15 +619,94 @@ def oracle_pool():
     return mp.get_context("spawn").Pool(procs, initializer=_pool_init), procs
 
 
+def _decode_parity_group(task):
+    """Worst normalised attention error of one sampled group's G heads: the
+    oracle decodes the GPU's own packed cache (identical codes)."""
+    import numpy as np
+
+    from oracle import attention, engine
+    cfg, item = task
+    book = engine.build(k_bits=cfg["k_bits"], v_bits=cfg["v_bits"], qjl_m=cfg["qjl_m"], seed=cfg["seed"])
+    table = np.arange(item["cache"]["k_norm"].shape[0])
+    worst = 0.0
+    for h in range(item["q"].shape[0]):
+        expect, vmax = attention.decode_attention(item["q"][h], item["cache"], table, item["ctx"], item["kvh"],
+                                                  book)
+        worst = max(worst, float(np.max(np.abs(item["out"][h] - expect)) / vmax))
+    return worst
+
+
+def _quant_parity(sample):
+    """Exempt and non-exempt code / sign disagreements of sampled vectors (the
+    GPU's cache rows against the oracle's encoding of the same inputs)."""
+    import numpy as np
+
+    from oracle import engine, packing, quantize
+    bits = sample["bits"]
+    ref = engine.build(k_bits=bits, v_bits=bits, qjl_m=sample["qjl_m"], seed=sample["seed"])
+    cache, slots, bs = sample["cache"], sample["slots"], sample["block_size"]
+    n_kv = cache["k_norm"].shape[1]
+    rep = {"bits": bits, "vectors": 0, "exempt_codes": 0, "near_boundary": 0, "non_exempt_codes": 0,
+           "exempt_signs": 0, "non_exempt_signs": 0}
+    for which in ("k", "v"):
+        x = sample[which].reshape(-1, 128)
+        rows = np.stack([packing.slot_index(slots, h, n_kv, bs) for h in range(n_kv)], axis=1).reshape(-1)
+        if which == "k":
+            flat = cache["k_codes"].reshape(-1, cache["k_codes"].shape[-1])
+            got = packing.unpack_planes(flat[rows], ref["k_bits"], 128)
+        else:
+            got = np.stack([packing.read_value_codes(cache["v_codes"], slots, h) for h in range(n_kv)], axis=1)
+            got = got.reshape(-1, 128)
+        norm = cache[which + "_norm"].reshape(-1)[rows]
+        bounds = ref[which + "_bounds"]
+        _, y, codes = quantize.encode_mse(x, ref["rot"], bounds)
+        diff = got != codes
+        exempt = quantize.boundary_distance(y, bounds) < CODE_EXEMPT
+        rep["vectors"] += len(x)
+        rep["exempt_codes"] += int((diff & exempt).sum())
+        rep["near_boundary"] += int(exempt.sum())
+        rep["non_exempt_codes"] += int((diff & ~exempt).sum())
+        if which == "k" and ref["qjl_m"]:
+            _, signs, z = quantize.encode_qjl(x, norm, got, ref["rot"], ref["k_levels"], ref["proj"])
+            flat = cache["k_qjl"].reshape(-1, cache["k_qjl"].shape[-1])
+            gs = packing.unpack_signs(flat[rows], ref["proj"].shape[0])
+            xn = np.linalg.norm(x, axis=1)
+            ex = np.abs(z) < CODE_EXEMPT * xn[:, None] * np.linalg.norm(ref["proj"], axis=1)[None, :]
+            d = gs != signs
+            rep["exempt_signs"] += int((d & ex).sum())
+            rep["non_exempt_signs"] += int((d & ~ex).sum())
+    return rep
+
+
+def cpu_leg(name, n_groups, pool, procs, decode_samples, quant_samples):
+    """The oracle on the host cores: its timed decode throughput on a bounded
+    sample of the workload (cpu_baseline), then the parity figures of the GPU
+    outputs and codes sampled by the GPU runs."""
+    value, groups = oracle_throughput(name, n_groups, 7, pool, procs)
+    base = {"value": value, "unit": "tokens/s", "cores": procs, "kind": "oracle",
+            "sample": "%d sampled (sequence, KV head) groups: quantize the new token + decode the group's "
+                      "query heads over its context, scaled to the batch" % groups}
+    parity = {"attention_tolerance": ATTN_TOL, "code_exempt_band": CODE_EXEMPT, "decode": {}, "quantize": {}}
+    for s in decode_samples:
+        cfg = {k: s[k] for k in ("k_bits", "v_bits", "qjl_m", "seed")}
+        worst = pool.map(_decode_parity_group, [(cfg, it) for it in s["groups"]])
+        parity["decode"][s["workload"]] = {
+            "groups": len(worst), "heads": int(sum(it["q"].shape[0] for it in s["groups"])),
+            "worst_normalised_error": max(worst), "within_tolerance": max(worst) <= ATTN_TOL}
+    for rep in pool.map(_quant_parity, quant_samples):
+        parity["quantize"]["c3_prefill_quantize_b%d" % rep["bits"]] = rep
+    return base, parity
+
+
 def workload_config(name, cfg, copies):
     ctx = cfg["context"]
     out = {"workload": name, "batch": cfg["batch"], "n_q_heads": cfg["n_q"], "n_kv_heads": cfg["n_kv"],
            "head_dim": 128, "context": list(ctx) if isinstance(ctx, tuple) else ctx,
            "k_bits": cfg["k_bits"], "v_bits": cfg["v_bits"], "qjl_m": cfg["qjl_m"],
-           "block_size": cfg["block_size"], "input_dtype": cfg["dtype"], "parallelism": "replicas"}
+           "block_size": cfg["block_size"], "input_dtype": cfg["dtype"],
+           "shuffled_block_table": bool(cfg.get("shuffled_table", False)), "parallelism": "replicas"}
     if copies is not None:
-        out["l2"] = ("inputs larger than L2: steps rotate over %d cache copies" % copies if copies > 1
-                     else "inputs larger than L2: one cache larger than 2x L2")
+        out["l2"] = l2_note(copies)
     return out
 
 
@@ -486,7 +731,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wall / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(args.workload, cfg, None),
+        "config": workload_config(args.workload, cfg, 1),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": procs, "kind": "oracle",
                          "sample": "%d (sequence, KV head) groups per step, each: quantize the new token + decode "
                                    "%d query heads over its context; scaled to the full batch" %
@@ -506,36 +751,47 @@ def main(argv=None):
     if rank == 0 and not args.no_cpu_baseline:
         pool, procs = oracle_pool()         # spawned before any GPU work
     init_ranks("nccl" if world > 1 else "gloo")
-    wl, max_ms, attn_ms, clock_info, e2e, quant = run_ours(args, rank, world, local_rank)
+    res = run_ours(args, rank, world, local_rank)
+    head = res["head"]
+    wl = head["wl"]
+    dev = "cuda" if world > 1 else "cpu"
+    step_ms = max_over_ranks(head["step_ms"], dev)
+    part_ms = max_over_ranks(head["partials_ms"], dev)
+    e2e = None
+    if "e2e" in head:
+        secs, h2d, d2h = head["e2e"]
+        secs = max_over_ranks(secs, dev)
+        e2e = {"value": world * wl.batch * args.steps / secs, "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if rank != 0:
         return 0
-    ms_per_step = max_ms / args.steps
     peak, peak_src = hbm_peak()
-    achieved = wl.cache_bytes / (attn_ms * 1e-3) / 1e9
-    tc = wl.B.tq_decode_kernel_kind(wl.book, wl.n_q, wl.n_kv)
-    kernel = ("attention_tc_kernel<%d>" if tc else "attention_kernel<%d>") % (wl.n_q // wl.n_kv)
+    achieved = wl.cache_bytes / (part_ms * 1e-3) / 1e9
+    kernel = wl.kernel_name()
     line = {
-        "metric": METRIC, "value": world * wl.batch / (ms_per_step * 1e-3), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "metric": METRIC, "value": world * wl.batch / (step_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(args.workload, wl.cfg, len(wl.caches)),
-        "hbm_gbs_step": wl.cache_bytes / (ms_per_step * 1e-3) / 1e9,
-        "kv_token_heads_per_s": world * float(wl.ctx.sum()) * wl.n_kv / (ms_per_step * 1e-3),
+        "hbm_gbs_step": wl.cache_bytes / (step_ms * 1e-3) / 1e9,
+        "kv_token_heads_per_s": world * float(wl.ctx.sum()) * wl.n_kv / (step_ms * 1e-3),
+        "bytes_per_token_head": wl.bytes_per_token_head,
+        "compression_vs_bf16": 4.0 * 128 / wl.bytes_per_token_head,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": recorded_traffic(kernel, args.workload), "kernel": kernel,
                      "peak_source": peak_src + " hbm_gbs", "algorithmic_bytes_per_launch": wl.cache_bytes,
-                     "launch_ms": attn_ms},
+                     "launch_ms": part_ms},
         "gpu_launches": wl.launches_per_step * args.steps,
-        "clocks": clock_info,
+        "clocks": head["clocks"],
         "e2e": e2e,
-        "prefill_quantize": quant,
+        "secondary": res["secondary"],
     }
     if pool is not None:
-        value, groups = oracle_throughput(args.workload, args.cpu_groups, 7, pool, procs)
+        base, parity = cpu_leg(args.workload, args.cpu_groups, pool, procs, res["decode_samples"],
+                               res["quant_samples"])
         pool.close()
-        line["cpu_baseline"] = {"value": value, "unit": "tokens/s", "cores": procs, "kind": "oracle",
-                                "sample": "%d sampled (sequence, KV head) groups: quantize the new token + decode "
-                                          "the group's query heads over its context, scaled to the batch" % groups}
+        line["cpu_baseline"] = base
+        line["parity"] = parity
     print(json.dumps(line))
     return 0
 

@@ -115,7 +115,9 @@ tq_status tq_codebook_matrices(const tq_codebook* book, double* R, double* S);
  * k_codes, k_qjl, k_norm, k_rnorm, v_codes, v_norm (0 for absent fields). */
 tq_status tq_cache_field_bytes(const tq_codebook* book, size_t bytes_per_item[6]);
 
-/* Quantize-append (the write path).  k, v: device [n_tokens][n_kv_heads][d]
+/* Quantize-append (the write path; 甲子光年 article §2 第一階段 for the
+ * norm, rotation, Lloyd-Max code and bit packing of every vector, §2 第二階段
+ * for the keys' QJL sign bits and residual norm).  k, v: device [n_tokens][n_kv_heads][d]
  * in `dtype`, contiguous, 16-byte aligned; either may be NULL to skip that
  * tensor.  slot_mapping: device int64 [n_tokens]; token t goes to slot
  * slot_mapping[t] (block = slot / block_size, offset = slot % block_size);
@@ -131,7 +133,11 @@ tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void*
  * every context_lens[b]. */
 size_t tq_decode_workspace_bytes(const tq_codebook* book, int batch, int n_q_heads, int max_context);
 
-/* Decode attention (the read path) for one new query token per sequence.
+/* Decode attention (the read path; 甲子光年 article §2 第二階段 for the score
+ * estimate n <R q, c[code]> + gamma sqrt(pi/2)/m <S q, 2 bits - 1>, seo-farm
+ * page §4 for attention over the de-quantized cache with the query left
+ * uncompressed, §2 for working in the rotated space and back-rotating once)
+ * for one new query token per sequence.
  * q: device [batch][n_q_heads][d] in `dtype`.  Query head h reads KV head
  * h / (n_q_heads / n_kv_heads).  block_table: device int32 [batch][max_blocks]
  * of physical block ids, or NULL for the identity layout (sequence b owns
@@ -213,16 +219,24 @@ tq_status tq_decode_step_prepare(const tq_codebook* book, const void* k_new, con
  *                         not quantized);
  *   tq_decode_partials -- per context chunk and KV head: scores from the packed
  *                         codes plus the QJL correction (甲子光年 §2 第二階段),
- *                         chunk max/sum and the value sum in the rotated space;
- *   tq_decode_finish   -- merge the chunk partials, divide by the softmax sum
- *                         and back-rotate by R^T into `out`.
+ *                         chunk max/sum and the value sum in the rotated space.
+ *                         With out == NULL it leaves split-K partials in the
+ *                         workspace for tq_decode_finish.  With an `out`
+ *                         (device float32 [batch][n_q_heads][d]) it leaves the
+ *                         final output there instead, as tq_decode_attention's
+ *                         last two stages do (the tensor-core kernel merges
+ *                         each (sequence, KV head) in place; after the CUDA-core
+ *                         kernel the merge runs as a second launch); calling
+ *                         tq_decode_finish afterwards is allowed and redundant;
+ *   tq_decode_finish   -- merge the partials, divide by the softmax sum and
+ *                         back-rotate by R^T into `out`.
  * Argument meaning, checks and errors are those of tq_decode_attention. */
 tq_status tq_decode_prepare(const tq_codebook* book, const void* q, tq_dtype dtype, int batch,
                             int n_q_heads, int max_context, void* workspace, size_t workspace_bytes,
                             void* stream);
 tq_status tq_decode_partials(const tq_codebook* book, int batch, int n_q_heads, int n_kv_heads,
                              const tq_cache_view* cache, const int32_t* block_table, int max_blocks,
-                             const int32_t* context_lens, int max_context, float scale,
+                             const int32_t* context_lens, int max_context, float scale, float* out,
                              void* workspace, size_t workspace_bytes, void* stream);
 tq_status tq_decode_finish(const tq_codebook* book, int batch, int n_q_heads,
                            const int32_t* context_lens, int max_context, int max_blocks, float* out,
@@ -243,9 +257,14 @@ tq_status tq_decode_finish(const tq_codebook* book, int batch, int n_q_heads,
  * - Returns TQ_ERR_WORKSPACE when tq_decode_workspace_bytes(book, batch,
  *   n_q_heads, max_context) exceeds TQ_STATIC_WORKSPACE_BYTES (e.g. 512
  *   query vectors at context 8192 need about 5 MiB).
- * - The first call on a device looks up the array's device address once (with
- *   the handle's device made current briefly); make that first call before
- *   any stream capture.
+ * - The first call on a device looks up the array's device address (with the
+ *   handle's device made current briefly, a host-side query that allocates
+ *   nothing); make that first call before any stream capture.  The address is
+ *   kept per device and looked up again when the device's current context is
+ *   a new one (after cudaDeviceReset, which also invalidates every handle:
+ *   rebuild the handles, then make the first call again before any capture).
+ * - Arguments are checked (TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED,
+ *   TQ_ERR_WORKSPACE) before the look-up, and nothing is launched on an error.
  * - Every call on a device shares the one array, and a call leaves its
  *   contents behind; nothing in it has to start at zero, because each call
  *   writes every scratch value it reads.  Calls that overlap on the GPU

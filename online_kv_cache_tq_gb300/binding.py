@@ -82,7 +82,7 @@ def load():
                                            ctypes.POINTER(tq_cache_view), vp, i32, vp, i32, vp, sz, vp]
     lib.tq_decode_prepare.argtypes = [vp, vp, i32, i32, i32, i32, vp, sz, vp]
     lib.tq_decode_partials.argtypes = [vp, i32, i32, i32, ctypes.POINTER(tq_cache_view), vp, i32, vp, i32,
-                                       ctypes.c_float, vp, sz, vp]
+                                       ctypes.c_float, vp, vp, sz, vp]
     lib.tq_decode_finish.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, sz, vp]
     lib.tq_decode_attention_static.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.POINTER(tq_cache_view), vp,
                                                i32, vp, i32, ctypes.c_float, vp, vp]
@@ -253,10 +253,13 @@ def tq_decode_prepare(book, q, dtype, batch, n_q_heads, max_context, workspace, 
 
 
 def tq_decode_partials(book, batch, n_q_heads, n_kv_heads, view, block_table, max_blocks, context_lens,
-                       max_context, scale, workspace, workspace_bytes, stream=None):
+                       max_context, scale, workspace, workspace_bytes, stream=None, out=None):
+    """``out`` None: leave split-K partials for tq_decode_finish; a float32
+    [batch][n_q_heads][128] device tensor: leave the final output there."""
     _check(load().tq_decode_partials(book.handle, batch, n_q_heads, n_kv_heads, ctypes.byref(view),
                                      _ptr(block_table), max_blocks, _ptr(context_lens), max_context, scale,
-                                     _ptr(workspace), workspace_bytes, _stream(stream)), "tq_decode_partials")
+                                     _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)),
+           "tq_decode_partials")
 
 
 def tq_decode_finish(book, batch, n_q_heads, context_lens, max_context, max_blocks, out, workspace,

@@ -404,17 +404,35 @@ size_t bk_bytes(const tq_codebook* book) {
   return static_cast<size_t>(tq::bk_head_bytes(book->k_mse_bits, book->cfg.qjl_m > 0));
 }
 
+// Decode workspace regions (byte offsets, each 256-byte aligned): rotated and
+// projected queries, split-K partial entries, tensor-core score operands,
+// per-group segment tickets and per-query-head segment records.
+struct DecodeLayout {
+  size_t q, part, bk, ticket, seg, total;
+};
+
+DecodeLayout decode_layout(const tq_codebook* book, int batch, int n_q_heads, int max_context) {
+  const size_t vecs = static_cast<size_t>(batch) * n_q_heads;
+  DecodeLayout l;
+  l.q = 0;
+  l.part = l.q + round_up(vecs * 2 * tq::kDim * sizeof(float));
+  const long long entries = tq::partial_entries(static_cast<long long>(vecs), max_chunks_for(max_context),
+                                                book->num_sms > 0 ? book->num_sms : 160);
+  l.bk = l.part + round_up(static_cast<size_t>(entries) * tq::kPartStride * sizeof(float));
+  l.ticket = l.bk + round_up(vecs * bk_bytes(book));
+  l.seg = l.ticket + round_up(vecs * sizeof(int));
+  l.total = l.seg + round_up(vecs * sizeof(tq::SegInfo));
+  return l;
+}
+
 }  // namespace
 
 extern "C" {
 
 size_t tq_decode_workspace_bytes(const tq_codebook* book, int batch, int n_q_heads, int max_context) {
   if (book == nullptr || batch <= 0 || n_q_heads <= 0 || max_context < 0) return 0;
-  const size_t vecs = static_cast<size_t>(batch) * n_q_heads;
-  const size_t q_bytes = round_up(vecs * 2 * tq::kDim * sizeof(float));
-  const size_t part_bytes =
-      round_up(vecs * static_cast<size_t>(max_chunks_for(max_context)) * tq::kPartStride * sizeof(float));
-  return q_bytes + part_bytes + round_up(vecs * bk_bytes(book));
+  const DecodeLayout l = decode_layout(book, batch, n_q_heads, max_context);
+  return l.total;
 }
 
 }  // extern "C"
@@ -442,6 +460,10 @@ tq_status decode_args(const tq_codebook* book, int stages, const void* q, tq_dty
     const int group = n_q_heads / n_kv_heads;
     if (group != 1 && group != 2 && group != 4 && group != 8) return TQ_ERR_UNSUPPORTED;
     if (block_table == nullptr && static_cast<long long>(batch) * max_blocks > cache->num_blocks) {
+      return TQ_ERR_INVALID_ARG;
+    }
+    // work items (sequence, KV head, chunk) are numbered in int
+    if (static_cast<long long>(batch) * n_kv_heads * max_chunks_for(max_context) >= (1ll << 31)) {
       return TQ_ERR_INVALID_ARG;
     }
   }
@@ -480,14 +502,15 @@ tq_status decode_args(const tq_codebook* book, int stages, const void* q, tq_dty
   a->scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(book->cfg.d));
   a->qjl_coef = book->cfg.qjl_m > 0 ? static_cast<float>(std::sqrt(M_PI / 2.0) / book->cfg.qjl_m) : 0.f;
   a->out = out;
-  const size_t vecs = static_cast<size_t>(batch) * n_q_heads;
-  a->ws_q = static_cast<float*>(workspace);
-  a->ws_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(vecs * 2 * tq::kDim * sizeof(float)));
+  const DecodeLayout l = decode_layout(book, batch, n_q_heads, max_context);
+  char* ws = static_cast<char*>(workspace);
+  a->ws_q = reinterpret_cast<float*>(ws + l.q);
+  a->ws_part = reinterpret_cast<float*>(ws + l.part);
   a->max_chunks = max_chunks_for(max_context);
   const size_t bk = bk_bytes(book);
-  a->ws_bk = bk == 0 ? nullptr
-                     : reinterpret_cast<uint8_t*>(a->ws_part) +
-                           round_up(vecs * static_cast<size_t>(a->max_chunks) * tq::kPartStride * sizeof(float));
+  a->ws_bk = bk == 0 ? nullptr : reinterpret_cast<uint8_t*>(ws + l.bk);
+  a->ws_ticket = reinterpret_cast<int*>(ws + l.ticket);
+  a->ws_seg = reinterpret_cast<tq::SegInfo*>(ws + l.seg);
   a->bk_stride = static_cast<int>(bk);
   a->R = book->d_R;
   a->Rt = book->d_Rt;
@@ -496,26 +519,52 @@ tq_status decode_args(const tq_codebook* book, int stages, const void* q, tq_dty
   a->tables = book->d_tables;
   a->error = book->d_error;
   a->num_sms = book->num_sms;
+  // the tensor-core partials kernel merges a group's segments and writes `out`
+  // itself when the call goes all the way to the output
+  a->merge_in_partials = (stages & kPartials) && out != nullptr && tq::tc_decode_supported(*a, book->walsh_ok);
   return TQ_OK;
 }
 
 tq_status launched(cudaError_t err) { return err == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
 
-// Tensor-core partials where supported, SIMT otherwise.  early: the previous
-// launch on the stream is a decode step's fused append + query preparation
-// and the tensor-core kernel may overlap it (programmatic dependent launch).
-cudaError_t launch_partials(const tq_codebook* book, const tq::DecodeArgs& a, cudaStream_t s, bool early = false) {
-  if (tq::tc_decode_supported(a, book->walsh_ok)) return tq::launch_decode_partials_tc(a, s, early);
-  return tq::launch_decode_partials(a, s);
+}  // namespace
+
+namespace tq {
+
+tq_status check_decode_call(const tq_codebook* book, const void* q, tq_dtype dtype, int batch, int n_q_heads,
+                            int n_kv_heads, const tq_cache_view* cache, const int32_t* block_table, int max_blocks,
+                            const int32_t* context_lens, int max_context, float scale, float* out,
+                            size_t workspace_bytes) {
+  DecodeArgs a;
+  // any non-null 256-byte aligned address stands for the workspace: only its
+  // size and alignment are checked
+  return decode_args(book, kPrepare | kPartials | kFinish, q, dtype, batch, n_q_heads, n_kv_heads, cache,
+                     block_table, max_blocks, context_lens, max_context, scale, out, reinterpret_cast<void*>(256),
+                     workspace_bytes, &a);
 }
 
-// Partials, then the merge into `out`; after the tensor-core kernel the merge
-// is a programmatic dependent launch (it starts as the last partials CTAs end).
+}  // namespace tq
+
+namespace {
+
+// Partials and the merge into `out`: the tensor-core kernel merges in place
+// (the CTA that finishes a (sequence, KV head) group's last segment merges
+// it); after the SIMT kernel the merge kernel runs.  early: the previous
+// launch on the stream is a decode step's fused append + query preparation
+// and the tensor-core kernel may overlap it (programmatic dependent launch).
 cudaError_t launch_partials_and_merge(const tq_codebook* book, const tq::DecodeArgs& a, cudaStream_t s,
                                       bool early = false) {
+  if (a.merge_in_partials) return tq::launch_decode_partials_tc(a, s, early);
   const bool tc = tq::tc_decode_supported(a, book->walsh_ok);
   const cudaError_t err = tc ? tq::launch_decode_partials_tc(a, s, early) : tq::launch_decode_partials(a, s);
-  return err == cudaSuccess ? tq::launch_decode_finish(a, s, tc) : err;
+  return err == cudaSuccess ? tq::launch_decode_finish(a, s) : err;
+}
+
+// Partials only (the staged call without an output): tensor-core kernel where
+// supported, SIMT otherwise.
+cudaError_t launch_partials(const tq_codebook* book, const tq::DecodeArgs& a, cudaStream_t s) {
+  if (tq::tc_decode_supported(a, book->walsh_ok)) return tq::launch_decode_partials_tc(a, s, false);
+  return tq::launch_decode_partials(a, s);
 }
 
 }  // namespace
@@ -702,13 +751,16 @@ tq_status tq_decode_prepare(const tq_codebook* book, const void* q, tq_dtype dty
 
 tq_status tq_decode_partials(const tq_codebook* book, int batch, int n_q_heads, int n_kv_heads,
                              const tq_cache_view* cache, const int32_t* block_table, int max_blocks,
-                             const int32_t* context_lens, int max_context, float scale, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+                             const int32_t* context_lens, int max_context, float scale, float* out,
+                             void* workspace, size_t workspace_bytes, void* stream) {
   tq::DecodeArgs a;
-  tq_status st = decode_args(book, kPartials, nullptr, TQ_FP32, batch, n_q_heads, n_kv_heads, cache, block_table,
-                             max_blocks, context_lens, max_context, scale, nullptr, workspace, workspace_bytes, &a);
+  const int stages = out != nullptr ? kPartials | kFinish : kPartials;
+  tq_status st = decode_args(book, stages, nullptr, TQ_FP32, batch, n_q_heads, n_kv_heads, cache, block_table,
+                             max_blocks, context_lens, max_context, scale, out, workspace, workspace_bytes, &a);
   if (st != TQ_OK || batch == 0) return st;
-  return launched(launch_partials(book, a, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (out != nullptr) return launched(launch_partials_and_merge(book, a, s));
+  return launched(launch_partials(book, a, s));
 }
 
 tq_status tq_decode_finish(const tq_codebook* book, int batch, int n_q_heads, const int32_t* context_lens,

@@ -61,6 +61,9 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(DecodeArgs a) {
   const int warp = tid >> 5;
   const bool qjl = a.k_qjl != nullptr;
   const int qbase = b * a.n_q + kvh * G;
+  // one partial entry per chunk: entry (query head, chunk) of a [.][max_chunks] array
+  if (chunk == 0 && tid < G)
+    a.ws_seg[qbase + tid] = SegInfo{(qbase + tid) * a.max_chunks, (ctx + kChunk - 1) / kChunk, 1, 0};
 
   for (int idx = tid; idx < G * kDim; idx += kThreads) {
     const int g = idx / kDim, j = idx % kDim;

@@ -55,18 +55,23 @@ constexpr int kTile = 128;                  // tokens per tile = tensor-memory l
 constexpr int kTiles = kChunk / kTile;      // tiles per chunk
 constexpr int kBuilders = 256;              // warps 0-7: two threads per tensor-memory lane
 constexpr int kThreads = kBuilders + 32;     // warp 8: copies and MMA issue
-constexpr int kVPieces = 4;                 // e4m3 pieces of a softmax weight
+constexpr int kVPieces = 3;                 // e4m3 pieces of a softmax weight
+constexpr int kMaxPending = 8;              // group merges a CTA may defer
 
 __host__ __device__ constexpr int round16(int x) { return (x + 15) / 16 * 16; }
 // Score accumulator columns: the query heads of a group are split into two
 // halves (threads t < 128 read the first, t >= 128 the second); head h's
-// pieces sit at column score_half(g) * (h / half_heads(g)) + kQPieces * (h %
+// pieces sit at column score_half(g) * (h / half_heads(g)) + q_pieces(g) * (h %
 // half_heads(g)), so each thread reads 16-column groups of its own heads only.
+// Eight heads use the first four of the prepared pieces (relative precision
+// 2^-17 per query coefficient), which keeps a CTA within 256 tensor-memory
+// columns and lets two CTAs share an SM; fewer heads use all kQPieces.
+__host__ __device__ constexpr int q_pieces(int g) { return g >= 8 ? 4 : kQPieces; }
 __host__ __device__ constexpr int half_heads(int g) { return g >= 2 ? g / 2 : 1; }
-__host__ __device__ constexpr int score_half(int g) { return round16(kQPieces * half_heads(g)); }
+__host__ __device__ constexpr int score_half(int g) { return round16(q_pieces(g) * half_heads(g)); }
 __host__ __device__ constexpr int score_cols(int g) { return g >= 2 ? 2 * score_half(g) : score_half(g); }
 __host__ __device__ constexpr int score_row(int g, int h, int piece) {
-  return score_half(g) * (h / half_heads(g)) + kQPieces * (h % half_heads(g)) + piece;
+  return score_half(g) * (h / half_heads(g)) + q_pieces(g) * (h % half_heads(g)) + piece;
 }
 __host__ __device__ constexpr int value_cols(int g) { return round16(kVPieces * g); }   // per value plane
 
@@ -184,17 +189,55 @@ __device__ __forceinline__ void write_pieces2(uint8_t* b, int row_a, int row_b, 
 // Barrier of the 256 builder threads only (named barrier 1).
 __device__ __forceinline__ void builder_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// Reduce N values per thread over the eight builder warps at once (one pair
-// of barriers for all N); on return lane j < N of every warp holds the total
-// of value j (the other lanes the identity).  Within a warp the value set
-// halves at every shuffle step (lanes with bit `off` set keep the upper half
-// and send the lower): P = N rounded up to a power of two takes
-// P - 1 + log2(32 / P) shuffles instead of 5 N.  Across warps lane j sums
-// warp 0's partial first, then warps 1..7 in order.
+// Builder barrier that also ANDs a flag over the 256 builders, so that every
+// builder takes the same decision after it (a per-thread read of the abort
+// word could differ between warps when the control warp sets it meanwhile).
+__device__ __forceinline__ bool builder_all(bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(flag))
+      : "memory");
+  return r != 0;
+}
+
+// Inclusive-exclusive scan of v over the threads of the CTA in thread order
+// (every thread takes part): returns the CTA total, *excl the sum over the
+// threads before this one.  warp_s holds one int per warp.
+template <int THREADS>
+__device__ __forceinline__ int cta_scan(int v, int* excl, int* warp_s) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_s[warp] = x;
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < THREADS / 32; ++w) {
+    const int sw = warp_s[w];
+    before += w < warp ? sw : 0;
+    total += sw;
+  }
+  __syncthreads();
+  *excl = before + x - v;
+  return total;
+}
+
+// Per-warp totals of N values per thread over the eight builder warps (one
+// pair of barriers for all N): afterwards red[w * N + j] holds warp w's total
+// of value j.  Within a warp the value set halves at every shuffle step (lanes
+// with bit `off` set keep the upper half and send the lower): P = N rounded
+// up to a power of two takes P - 1 + log2(32 / P) shuffles instead of 5 N.
+// Warps 0-3 and 4-7 are the two builder halves, which own different query
+// heads, so callers combine the four totals of one half in warp order.
 template <int N, typename Op>
-__device__ __forceinline__ float block_reduce(const float (&v)[N], float* red, Op op) {
+__device__ __forceinline__ void warp_totals(const float (&v)[N], float* red, Op op) {
   constexpr int P = N <= 1 ? 1 : N <= 2 ? 2 : N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : 32;
-  constexpr int kWarps = kBuilders / 32;
   static_assert(N <= 32, "at most 32 values");
   const int lane = threadIdx.x & 31;
   float cur[P];
@@ -214,15 +257,17 @@ __device__ __forceinline__ float block_reduce(const float (&v)[N], float* red, O
   }
 #pragma unroll
   for (int off = 16 / P; off > 0; off >>= 1) cur[0] = op(cur[0], __shfl_xor_sync(0xffffffffu, cur[0], off));
-  builder_sync();
+  builder_sync();                               // the previous reduction's totals were read
   if ((lane & (32 / P - 1)) == 0 && idx < N) red[(threadIdx.x >> 5) * N + idx] = cur[0];
   builder_sync();
-  float r = op.identity();
-  if (lane < N) {
-    r = red[lane];
+}
+
+// Total of value j over the four warps of builder half `hf`, in warp order.
+template <int N, typename Op>
+__device__ __forceinline__ float half_total(const float* red, int hf, int j, Op op) {
+  float r = red[(4 * hf) * N + j];
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) r = op(r, red[w * N + lane]);
-  }
+  for (int w = 1; w < 4; ++w) r = op(r, red[(4 * hf + w) * N + j]);
   return r;
 }
 struct MaxOp {
@@ -261,7 +306,7 @@ struct TcLayout {
   int v_slots;              // value slots of kValueSlot columns (2 to kMaxValueSlots)
   int col_s, col_o, cols, tmem;
   int kbytes, vblock;       // key code bytes per token; value code bytes per (block, head)
-  int off_bmse, off_bqjl, off_bv, off_s0, off_s1, off_kc, off_kq, off_kn, off_kr, off_vn, off_vc, smem_bytes;
+  int off_bmse, off_bqjl, off_bv, off_s0, off_s1, off_sacc, off_kc, off_kq, off_kn, off_kr, off_vn, off_vc, smem_bytes;
 };
 
 constexpr int kValueSlot = 64;              // columns of one value slot (two sign planes)
@@ -300,7 +345,8 @@ TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size) 
   l.off_bqjl = o; o += l.n2 * 128;
   l.off_bv = o; o += kTiles * l.no * 128;
   l.off_s0 = o; o += group * kChunk * 4;
-  l.off_s1 = o; o += group * kChunk * 4;
+  l.off_s1 = o; o += group * kTile * 4;
+  l.off_sacc = o; o += group * kTile * 4;
   l.off_kc = o; o += kChunk * l.kbytes;
   l.off_kq = o; o += kChunk * 16;
   l.off_kn = o; o += kChunk * 4;
@@ -326,52 +372,132 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
 
 }  // namespace
 
-// One work item: (sequence b, KV head kvh, chunk) in the order of the item
-// index ((b * n_kv) + kvh) * max_chunks + chunk.  Items whose chunk starts at
-// or beyond the sequence's context are empty and skipped by every role.
+// Merge the n_seg segments of one group (its G heads' entries at ent0 + s G +
+// h), divide by the softmax sum and back-rotate into out (seo-farm page §2:
+// out = R^T o_rot).  Called by every builder thread (lane, half); half h
+// merges the heads it owns, then each half sums 64 of the 128 terms of every
+// head's back-rotation.  Not inlined: it runs about twice per CTA, and its
+// loads in flight must not take registers from the per-tile loop.
+template <int G>
+__device__ __noinline__ void merge_segments(const float* ws_part, const float* R, float* out, int ent0,
+                                            int n_seg, int qbase, float* orot, float* s1, int half, int lane) {
+  constexpr int HG = half_heads(G);
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    if (h / HG != half) continue;
+    float m = -INFINITY, l = 0.f, acc = 0.f;
+    for (int sg0 = 0; sg0 < n_seg; sg0 += 4) {
+      // (four segments' loads in flight at once)
+      float pm[4], pl[4], pa[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float* part = ws_part + (ent0 + static_cast<long long>(sg0 + k) * G + h) * kPartStride;
+        const bool in = sg0 + k < n_seg;
+        pm[k] = in ? __ldcg(part) : -INFINITY;
+        pl[k] = in ? __ldcg(part + 1) : 0.f;
+        pa[k] = in ? __ldcg(part + 4 + lane) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float mn = fmaxf(m, pm[k]);
+        const float so = m == -INFINITY ? 0.f : __expf(m - mn);
+        const float sn = pm[k] == -INFINITY ? 0.f : __expf(pm[k] - mn);
+        l = fmaf(l, so, pl[k] * sn);
+        acc = fmaf(acc, so, pa[k] * sn);
+        m = mn;
+      }
+    }
+    orot[h * kTile + lane] = l > 0.f ? acc / l : 0.f;
+  }
+  builder_sync();
+  // out[h][o] = sum_i R[i][o] o_rot[h][i]: thread (o = lane, half) sums i in
+  // [64 half, 64 half + 64), 32 loads of R in flight at a time
+  float r[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) r[h] = 0.f;
+  const float* rp = R + (64 * half) * kDim + lane;
+#pragma unroll 1
+  for (int i0 = 0; i0 < 64; i0 += 32) {
+    float w[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) w[k] = __ldg(rp + (i0 + k) * kDim);
+#pragma unroll
+    for (int k = 0; k < 32; k += 4)
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float4 v = *reinterpret_cast<const float4*>(orot + h * kTile + 64 * half + i0 + k);
+        r[h] = fmaf(w[k], v.x, fmaf(w[k + 1], v.y, fmaf(w[k + 2], v.z, fmaf(w[k + 3], v.w, r[h]))));
+      }
+  }
+  if (half == 1)
+#pragma unroll
+    for (int h = 0; h < G; ++h) s1[h * kTile + lane] = r[h];
+  builder_sync();
+  if (half == 0)
+#pragma unroll
+    for (int h = 0; h < G; ++h) out[static_cast<long long>(qbase + h) * kDim + lane] = r[h] + s1[h * kTile + lane];
+  builder_sync();
+}
+
+// One work item: (sequence b, KV head kvh, chunk) of a non-empty chunk.  The
+// items of a launch are the real chunks in the order (b, kvh, chunk), numbered
+// 0 .. T - 1; CTA c takes the run [c per_cta, (c + 1) per_cta), so every CTA
+// gets the same number of chunks whatever the spread of context lengths.  A
+// (sequence, KV head) group's consecutive items in one CTA form a segment whose
+// partials are merged in the CTA; group g has one segment per CTA in
+// [first_cta, last_cta], stored as entry slot g + c (unique: a CTA's groups
+// increase with c, and a group's CTAs with g).
 struct Item {
-  int b, kvh, chunk, ctx, start, n_local, n_tiles, n_blk;
+  int b, kvh, chunk, ctx, start, n_local, n_tiles, n_blk, group;
+  int g0, nch;                                  // the group's first item index and item count
+  // CTAs whose runs hold the group's first and last item
+  __device__ __forceinline__ int first_cta(int per_cta) const { return g0 / per_cta; }
+  __device__ __forceinline__ int last_cta(int per_cta) const { return (g0 + nch - 1) / per_cta; }
 };
 
-// Walks the item indices [first, last) of a CTA: the index is split into
-// (b, kvh, chunk) once, then carried forward one item at a time, and a
-// sequence's context length is read when the walk enters the sequence.
+// Walks the items [first, last) of a CTA from the (b, kvh, chunk) of `first`;
+// a sequence's context length is read when the walk enters the sequence, and
+// sequences without tokens are stepped over.
 struct ItemCursor {
-  int it, last, chunk, kvh, b, ctx;
-  __device__ ItemCursor(const DecodeArgs& a, int first, int last_) : it(first), last(last_) {
-    const int g = first / a.max_chunks;
-    chunk = first - g * a.max_chunks;
-    b = g / a.n_kv;
-    kvh = g - b * a.n_kv;
+  int it, last, b, kvh, chunk, ctx, nch;
+  __device__ ItemCursor(const DecodeArgs& a, int first, int last_, int b0, int kvh0, int chunk0)
+      : it(first), last(last_), b(b0), kvh(kvh0), chunk(chunk0) {
     ctx = first < last ? context_of(a, b) : 0;
+    nch = (ctx + kChunk - 1) / kChunk;
   }
   __device__ __forceinline__ void advance(const DecodeArgs& a) {
     ++it;
-    if (++chunk == a.max_chunks) {
-      chunk = 0;
-      if (++kvh == a.n_kv) {
-        kvh = 0;
-        ++b;
-        ctx = it < last ? context_of(a, b) : 0;
+    if (++chunk < nch) return;
+    chunk = 0;
+    if (++kvh < a.n_kv) return;
+    kvh = 0;
+    if (it >= last) return;
+    do {
+      if (b + 1 >= a.batch) {             // (only if the lengths changed under the launch)
+        it = last;
+        return;
       }
-    }
+      ++b;
+      ctx = context_of(a, b);
+      nch = (ctx + kChunk - 1) / kChunk;
+    } while (nch == 0);
   }
-  // the next non-empty item, if any
+  // the next item, if any
   __device__ __forceinline__ bool next(const DecodeArgs& a, int bs_shift, Item& x) {
-    for (; it < last; advance(a)) {
-      if (chunk * kChunk >= ctx) continue;
-      x.b = b;
-      x.kvh = kvh;
-      x.chunk = chunk;
-      x.ctx = ctx;
-      x.start = chunk * kChunk;
-      x.n_local = min(kChunk, ctx - x.start);
-      x.n_tiles = (x.n_local + kTile - 1) / kTile;
-      x.n_blk = (x.n_local + (1 << bs_shift) - 1) >> bs_shift;
-      advance(a);
-      return true;
-    }
-    return false;
+    if (it >= last) return false;
+    x.b = b;
+    x.kvh = kvh;
+    x.chunk = chunk;
+    x.ctx = ctx;
+    x.start = chunk * kChunk;
+    x.n_local = min(kChunk, ctx - x.start);
+    x.n_tiles = (x.n_local + kTile - 1) / kTile;
+    x.n_blk = (x.n_local + (1 << bs_shift) - 1) >> bs_shift;
+    x.group = b * a.n_kv + kvh;
+    x.g0 = it - chunk;
+    x.nch = nch;
+    advance(a);
+    return true;
   }
 };
 
@@ -380,11 +506,71 @@ struct ItemCursor {
 // thread at 96 registers (the register file is split over four sub-partitions
 // of 16384, and one of them holds five of the two CTAs' eighteen warps).
 template <int G, int KB, int VB, int QJ>
-__global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a, TcLayout L, int items_per_cta) {
+__global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a, TcLayout L) {
   constexpr int N1 = score_cols(G), NO = value_cols(G);
-  const int total = a.batch * a.n_kv * a.max_chunks;
-  const int first = blockIdx.x * items_per_cta;
-  const int last = min(total, first + items_per_cta);
+  const int t = threadIdx.x;
+
+  // ---- work split: the real chunks of every sequence, an equal run per CTA ----
+  __shared__ int scan_s[kThreads / 32];
+  __shared__ int split_s[3];                    // (b, kvh, chunk) of this CTA's first item
+  __shared__ int empty_s[kThreads];             // sequences without context (CTA 0, merging launch)
+  __shared__ int n_empty_s;
+  int n_chunks_total = 0;
+  int ch0 = 0, excl0 = 0;                       // pass 0: this thread's sequence (b = t)
+  for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
+    const int b = b0 + t;
+    const int ctx = b < a.batch ? context_of(a, b) : -1;
+    const int ch = ctx > 0 ? (ctx + kChunk - 1) / kChunk : 0;
+    if (a.merge_in_partials && blockIdx.x == 0) {
+      // a sequence without context has a zero output, which no item writes
+      if (t == 0) n_empty_s = 0;
+      __syncthreads();
+      if (ctx == 0) empty_s[atomicAdd(&n_empty_s, 1)] = b;
+      __syncthreads();
+      const int n_empty = n_empty_s;
+      for (int e = 0; e < n_empty; ++e) {
+        float4* row = reinterpret_cast<float4*>(a.out + static_cast<long long>(empty_s[e]) * a.n_q * kDim);
+        for (int i = t; i < a.n_q * (kDim / 4); i += kThreads) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      __syncthreads();
+    }
+    int excl;
+    n_chunks_total += cta_scan<kThreads>(ch, &excl, scan_s);
+    if (b0 == 0) {
+      ch0 = ch;
+      excl0 = excl;
+    }
+  }
+  const int n_items = n_chunks_total * a.n_kv;
+  const int per_cta = max(1, (n_items + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x));
+  const int first = static_cast<int>(blockIdx.x) * per_cta;
+  const int last = min(n_items, first + per_cta);
+  if (first >= last) return;                    // (uniform: no tensor memory or barrier is set up yet)
+  // the sequence holding item `first`: items of sequence b are [lo, lo + ch n_kv)
+  auto locate = [&](int b, int ch, int before) {
+    const int lo = before * a.n_kv;
+    if (ch > 0 && first >= lo && first < lo + ch * a.n_kv) {
+      split_s[0] = b;
+      split_s[1] = (first - lo) / ch;
+      split_s[2] = (first - lo) % ch;
+    }
+  };
+  if (a.batch <= kThreads) {
+    locate(t, ch0, excl0);                      // (one pass held the whole batch)
+  } else {
+    int base = 0;                               // chunks of the sequences before this pass
+    for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
+      const int b = b0 + t;
+      const int ctx = b < a.batch ? context_of(a, b) : 0;
+      const int ch = (ctx + kChunk - 1) / kChunk;
+      int excl;
+      const int tot = cta_scan<kThreads>(ch, &excl, scan_s);
+      locate(b, ch, base + excl);
+      base += tot;
+    }
+  }
+  __syncthreads();
+
   const int bs = a.block_size;                        // a power of two that divides kChunk
   const int bs_shift = 31 - __clz(bs);
 
@@ -405,7 +591,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   uint8_t* b_qjl = smem + L.off_bqjl;
   uint8_t* b_v = smem + L.off_bv;
   float* s0 = reinterpret_cast<float*>(smem + L.off_s0);           // [G][kChunk] scores, then weights
-  float* s1 = reinterpret_cast<float*>(smem + L.off_s1);           // output halves
+  float* s1 = reinterpret_cast<float*>(smem + L.off_s1);           // [G][kTile]: output halves
+  float* seg_acc = reinterpret_cast<float*>(smem + L.off_sacc);    // [G][kTile]: the segment's running acc
   uint8_t* kc_s = smem + L.off_kc;                                  // [kChunk][kbytes]
   uint8_t* kq_s = smem + L.off_kq;                                  // [kChunk][16]
   float* kn_s = reinterpret_cast<float*>(smem + L.off_kn);
@@ -421,15 +608,17 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       vdone[kMaxValueSlots], bar_d;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
-  __shared__ float red_s[(kBuilders / 32) * (2 * G + 1)];   // block_reduce of up to 2 G + 1 values
+  __shared__ float red_s[(kBuilders / 32) * (2 * half_heads(G) + 1)];   // warp totals of up to 2 HG + 1 values
   __shared__ float stat_s[2][G];                // chunk max, chunk sum per head
   __shared__ int blk_ok_s[2][kChunk / 32];      // per item parity: physical block of each block slot is valid
   __shared__ float sv_s;                        // piece scale of the softmax weights
   __shared__ float wsum_s[G];                   // sum over the chunk of e n_v per head
   __shared__ float cst_s[4][G];                 // per head: 1/sigma_mse, 1/sigma_qjl, ones_mse, ones_qjl
   __shared__ float vw_s[8];                     // odd Walsh coefficients of the value codebook
+  __shared__ int4 pend_s[kMaxPending];          // groups whose merge this CTA owes: (entry base, n_seg, qbase)
+  __shared__ int n_pend_s;
+  __shared__ float seg_ml_s[2][2][G];           // [item parity][max, sum][head] of the running segment
 
-  const int t = threadIdx.x;
   const bool builder = t < kBuilders;
   const int lane = t & (kTile - 1);             // tensor-memory lane (token or coordinate)
   const int half = (t >> 7) & 1;                // which of the two threads of the lane
@@ -526,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     const uint64_t desc_v = ptx::desc_k_sw128(ptx::smem_u32(b_v));
     const uint32_t mse_plane_step = (L.n1 * 128) >> 4, v_tile_step = (L.no * 128) >> 4;
     const uint32_t d_mse = tmem + L.col_s;
-    ItemCursor cursor(a, first, last);
+    ItemCursor cursor(a, first, last, split_s[0], split_s[1], split_s[2]);
     int seq = 0, ktile = 0;
     int vslot = 0, vwrap = 0;                   // value unit counter as (slot, times round the slots)
     Item cur, nxt;
@@ -609,13 +798,39 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   } else {
     // =================== builders ===================
     constexpr int HG = half_heads(G), HC = score_half(G);
-    ItemCursor cursor(a, first, last);
+    ItemCursor cursor(a, first, last, split_s[0], split_s[1], split_s[2]);
     int seq = 0, ktile = 0, cur_group = -1;
     int vslot = 0, vwrap = 0;                     // value unit counter as (slot, times round the slots)
-    Item x;
     const int wpd_shift = bs_shift - 5;         // log2 of the words per coordinate in a block
-    while (ok && cursor.next(a, bs_shift, x)) {
-      const int group = x.b * a.n_kv + x.kvh;
+    // The CTA's segment of the current group is merged chunk by chunk: the
+    // running max and sum of every head in seg_ml_s (item seq reads parity
+    // seq & 1 and writes the other), acc[coordinate lane] of head h in
+    // seg_acc, read and written only by the thread that owns (h, lane).
+    const bool ml_writer = (t & 127) == 0;        // one thread per half writes the heads it owns
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      if (h / HG != half) continue;
+      seg_acc[h * kTile + lane] = 0.f;
+      if (ml_writer) {
+        seg_ml_s[0][0][h] = -INFINITY;
+        seg_ml_s[0][1][h] = 0.f;
+      }
+    }
+
+    if (t == 0) n_pend_s = 0;
+    // the merges this CTA owes, by every builder (uniform: the count is read after a barrier)
+    auto run_pending = [&]() {
+      const int np = n_pend_s;
+      for (int p = 0; p < np; ++p) {
+        const int4 e = pend_s[p];
+        merge_segments<G>(a.ws_part, a.R, a.out, e.x, e.y, e.z, s0, s1, half, lane);
+      }
+    };
+
+    Item x;
+    bool have = cursor.next(a, bs_shift, x);
+    while (ok && have) {
+      const int group = x.group;
       const int qbase = x.b * a.n_q + x.kvh * G;
       const int* blk_ok = blk_ok_s[seq & 1];
       // B_K: the group's prepared score operand pieces into the swizzled layout
@@ -625,11 +840,13 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       if (group != cur_group) {
         asm volatile("griddepcontrol.wait;" ::: "memory");   // the query operands come from the previous grid
         const int nk = pk + pq;
-        const int per_head = nk * kQPieces * 8;     // 16-byte chunks per head
+        constexpr int QP = q_pieces(G);
+        const int per_head = nk * QP * 8;           // 16-byte chunks per head taken
         for (int idx = t; idx < G * per_head; idx += kBuilders) {
           const int h = idx / per_head, r = idx - h * per_head;
-          const int s = r / (kQPieces * 8), i = (r / 8) % kQPieces, c = r % 8;
-          const uint4 v = reinterpret_cast<const uint4*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride)[r];
+          const int s = r / (QP * 8), i = (r / 8) % QP, c = r % 8;
+          const uint4 v = reinterpret_cast<const uint4*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride)
+              [(s * kQPieces + i) * 8 + c];
           const int n = score_row(G, h, i);
           uint8_t* dst = s < pk ? b_mse + s * L.n1 * 128 : b_qjl;
           *reinterpret_cast<uint4*>(dst + n * 128 + ((c ^ (n & 7)) << 4)) = v;
@@ -658,9 +875,9 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       // s = scale (n_k <q_rot, k_mse> + gamma coef <q_s, signs>), into s0, and
       // keeps their running max (an accumulator holds sigma times the 0/1-bit
       // sum, so the +-1 sum is acc / sigma - ones)
-      float mx[G + 1];                            // owned heads' score max, then the value-norm max
+      float mx[HG + 1];                           // owned heads' score max, then the value-norm max
 #pragma unroll
-      for (int h = 0; h <= G; ++h) mx[h] = h < G ? -INFINITY : 0.f;
+      for (int j = 0; j <= HG; ++j) mx[j] = j < HG ? -INFINITY : 0.f;
       // (templated on the half, so that the owned heads are compile-time indices)
       auto read_scores_half = [&](int i, auto half_c) {
         constexpr int H0 = decltype(half_c)::value * HG;
@@ -676,14 +893,14 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             ptx::tmem_ld16(tmem + row_addr + L.col_s + (H0 / HG) * HC + c0, v);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const int hj = (c0 + j) / kQPieces, piece = (c0 + j) % kQPieces;
+              const int hj = (c0 + j) / q_pieces(G), piece = (c0 + j) % q_pieces(G);
               if (hj < HG) am[hj] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), am[hj]);
             }
             if (qjl) {
               ptx::tmem_ld16(tmem + row_addr + L.col_s + N1 + (H0 / HG) * HC + c0, v);
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                const int hj = (c0 + j) / kQPieces, piece = (c0 + j) % kQPieces;
+                const int hj = (c0 + j) / q_pieces(G), piece = (c0 + j) % q_pieces(G);
                 if (hj < HG) aq[hj] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), aq[hj]);
               }
             }
@@ -699,7 +916,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             const float qv = qjl ? fmaf(aq[j], cst_r[1][j], -cst_r[3][j]) : 0.f;
             const float sc = valid ? a.scale * fmaf(nk, mse, gk * qv) : -INFINITY;
             s0[h * kChunk + tl] = sc;
-            mx[h] = fmaxf(mx[h], sc);
+            mx[j] = fmaxf(mx[j], sc);
           }
         }
       };
@@ -758,24 +975,30 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       if (ok) take_scores(x.n_tiles - 1, k0 + x.n_tiles - 1);
       ptx::mbar_arrive(&kfree);                   // this item's key fields are no longer read
       ok = ok && wait_phase(&vin, seq & 1, abort, a.error);
-      builder_sync();
-      ok = ok && *abort == 0;
+      ok = builder_all(ok && *abort == 0);
       if (!ok) break;
 
       // ---- softmax max over the chunk; B_V pieces of exp(s - m) n_v ----
       for (int i = t; i < x.n_tiles * kTile; i += kBuilders)
-        mx[G] = fmaxf(mx[G], i < x.n_local && blk_ok[i >> bs_shift] ? vn_s[i] : 0.f);
-      float lw[2 * G];                            // owned heads: sum of e, then sum of e n_v
+        mx[HG] = fmaxf(mx[HG], i < x.n_local && blk_ok[i >> bs_shift] ? vn_s[i] : 0.f);
+      float lw[2 * HG];                           // owned heads: sum of e, then sum of e n_v
 #pragma unroll
-      for (int h = 0; h < 2 * G; ++h) lw[h] = 0.f;
+      for (int j = 0; j < 2 * HG; ++j) lw[j] = 0.f;
       {
-        const float tot = block_reduce(mx, red_s, MaxOp());
-        if (t < G) stat_s[0][t] = tot;
+        // chunk max of the owned heads over this half's warps; value-norm max over all
+        warp_totals(mx, red_s, MaxOp());
+        float vmax = 0.f;
 #pragma unroll
-        for (int h = 0; h <= G; ++h) mx[h] = __shfl_sync(0xffffffffu, tot, h);
+        for (int w = 0; w < kBuilders / 32; ++w) vmax = fmaxf(vmax, red_s[w * (HG + 1) + HG]);
+#pragma unroll
+        for (int j = 0; j < HG; ++j) {
+          mx[j] = half_total<HG + 1>(red_s, half, j, MaxOp());
+          if ((t & 127) == 0 && half * HG + j < G) stat_s[0][half * HG + j] = mx[j];
+        }
+        mx[HG] = vmax;
       }
       // the pieces carry 2 e n_v sv / beta_t, below 2 * 64 * max n_v * sv
-      const float sv = piece_scale(2.f * kMaxBitInvScale * mx[G]);
+      const float sv = piece_scale(2.f * kMaxBitInvScale * mx[HG]);
       {
         // thread (lane, half): token slot `lane` of every tile, its own heads
         // (templated on the half, so that the owned heads are compile-time indices)
@@ -797,10 +1020,10 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
                 e[j] = 0.f;
                 if (h >= G) continue;
                 // (a select, not a branch: the exponent of an invalid slot may be nan)
-                const float ex = __expf(s0[h * kChunk + tl] - mx[h]);
-                e[j] = valid && mx[h] != -INFINITY ? ex : 0.f;
-                lw[h] += e[j];
-                lw[G + h] = fmaf(e[j], nv, lw[G + h]);
+                const float ex = __expf(s0[h * kChunk + tl] - mx[j]);
+                e[j] = valid && mx[j] != -INFINITY ? ex : 0.f;
+                lw[j] += e[j];
+                lw[HG + j] = fmaf(e[j], nv, lw[HG + j]);
               }
               // the owned heads two at a time (one when the half owns one head)
 #pragma unroll
@@ -876,11 +1099,15 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       ptx::tc_fence_after();
 
       {
-        // (only thread 0's warp keeps the sums: lanes 0..G-1 the sums of e,
-        // lanes G..2G-1 those of e n_v)
-        const float tot = block_reduce(lw, red_s, SumOp());
-        if (t < G) stat_s[1][t] = tot;
-        else if (t < 2 * G) wsum_s[t - G] = tot;
+        // sums of e and of e n_v of the owned heads over this half's warps
+        warp_totals(lw, red_s, SumOp());
+        if ((t & 127) == 0)
+#pragma unroll
+          for (int j = 0; j < HG; ++j)
+            if (half * HG + j < G) {
+              stat_s[1][half * HG + j] = half_total<2 * HG>(red_s, half, j, SumOp());
+              wsum_s[half * HG + j] = half_total<2 * HG>(red_s, half, HG + j, SumOp());
+            }
       }
 
       // ---- partial output of this chunk: half h reads the planes s with s % 2 == h ----
@@ -903,32 +1130,91 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         }
       }
       ptx::tc_fence_before();
-      if (half == 1)
+      // each half keeps the heads it owns; the other half's sums for them come through s1
 #pragma unroll
-        for (int h = 0; h < G; ++h) s1[h * kTile + lane] = o[h];
-      builder_sync();
-      ok = ok && *abort == 0;
-      if (ok && half == 0) {
+      for (int h = 0; h < G; ++h)
+        if (h / HG != half) s1[h * kTile + lane] = o[h];
+      ok = builder_all(ok && *abort == 0);
+      if (ok) {
         const float inv_sv = 1.f / sv_s;          // exact: sv is a power of two
         float a_sum = 0.f;                        // sum_S a_S: the -1 half of every sign product
         for (int s = 0; s < pv; ++s) a_sum += vw_s[s];
+        // this chunk's (m, l, acc) into the segment's running values
+        const int par = seq & 1;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          float* part = a.ws_part + (static_cast<long long>(qbase + h) * a.max_chunks + x.chunk) * kPartStride;
-          part[4 + lane] = fmaf(o[h] + s1[h * kTile + lane], inv_sv, -a_sum * wsum_s[h]);
-          if (lane == 0) {
-            part[0] = stat_s[0][h];
-            part[1] = stat_s[1][h];
+          if (h / HG != half) continue;
+          const float mr = seg_ml_s[par][0][h], lr = seg_ml_s[par][1][h];
+          const float mi = stat_s[0][h], li = stat_s[1][h];
+          const float ai = fmaf(o[h] + s1[h * kTile + lane], inv_sv, -a_sum * wsum_s[h]);
+          const float mn = fmaxf(mr, mi);
+          const float so = mr == -INFINITY ? 0.f : __expf(mr - mn);
+          const float si = mi == -INFINITY ? 0.f : __expf(mi - mn);
+          seg_acc[h * kTile + lane] = fmaf(seg_acc[h * kTile + lane], so, ai * si);
+          if (ml_writer) {
+            seg_ml_s[par ^ 1][0][h] = mn;
+            seg_ml_s[par ^ 1][1][h] = fmaf(lr, so, li * si);
           }
         }
       }
       builder_sync();                             // s1, stat_s and wsum_s are free for the next item
+      Item y;
+      const bool more = cursor.next(a, bs_shift, y);
+      if (ok && (!more || y.group != x.group)) {
+        // ---- the segment ends: its partials go to entry slot group + CTA ----
+        const long long ent0 = (static_cast<long long>(x.group) + blockIdx.x) * G;
+        const int par = (seq & 1) ^ 1;            // where this item left the running max and sum
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          if (h / HG != half) continue;
+          float* part = a.ws_part + (ent0 + h) * kPartStride;
+          part[4 + lane] = seg_acc[h * kTile + lane];
+          seg_acc[h * kTile + lane] = 0.f;
+          if (ml_writer) {
+            part[0] = seg_ml_s[par][0][h];
+            part[1] = seg_ml_s[par][1][h];
+            seg_ml_s[par][0][h] = -INFINITY;
+            seg_ml_s[par][1][h] = 0.f;
+          }
+        }
+        const int f_cta = x.first_cta(per_cta);
+        const int n_seg = x.last_cta(per_cta) - f_cta + 1;
+        if (f_cta == static_cast<int>(blockIdx.x) && t < G)
+          a.ws_seg[qbase + t] = SegInfo{(x.group + f_cta) * G + t, n_seg, G, 0};
+        if (a.merge_in_partials) {
+          // The CTA that ends a group's last segment owes its merge; it runs
+          // the merges it owes after its last item (a merge here would stall
+          // the copy and MMA pipeline), or now when the list is full.
+          // (the count is read before the barrier: thread 0 changes it only after it)
+          const bool full = n_pend_s == kMaxPending;
+          builder_sync();                         // every builder's partial stores precede the ticket
+          if (full) {
+            run_pending();
+            if (t == 0) n_pend_s = 0;
+          }
+          if (t == 0) {
+            bool owe = true;                      // (a group inside this run has no other contributor)
+            if (n_seg > 1) {
+              __threadfence();
+              owe = atomicAdd(a.ws_ticket + x.group, 1) == n_seg - 1;
+              if (owe) __threadfence();           // the other CTAs' partials are visible from here on
+            }
+            if (owe) pend_s[n_pend_s++] = make_int4((x.group + f_cta) * G, n_seg, qbase, 0);
+          }
+        }
+      }
+      x = y;
+      have = more;
       ++seq;
+    }
+    if (ok && a.merge_in_partials) {
+      builder_sync();
+      run_pending();
     }
   }
 
-  // the merge kernel that follows may launch once every CTA got here (it
-  // waits for this grid to finish before it reads the partials)
+  // a grid launched as a programmatic dependent of this one may start once
+  // every CTA got here (and waits for this grid before it reads anything)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   ptx::tc_fence_before();
   __syncthreads();
@@ -967,14 +1253,15 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, bool early) {
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem_bytes);
   if (err != cudaSuccess) return err;
   // a persistent grid: two CTAs per SM (one when the tensor memory or shared
-  // memory of a CTA leaves room for one), each taking a contiguous run of
-  // (sequence, KV head, chunk) items so that consecutive items share the query
-  // operands and the next item's fields load while the current one computes
-  const long long total = static_cast<long long>(a.batch) * a.n_kv * a.max_chunks;
+  // memory of a CTA leaves room for one); the kernel splits the real chunks
+  // of the batch into equal runs, one per CTA, so that consecutive items share
+  // the query operands and the next item's fields load while the current one
+  // computes.  No more CTAs than the batch could have chunks.
+  const long long bound = static_cast<long long>(a.batch) * a.n_kv * a.max_chunks;
   const int per_sm = (l.tmem <= 256 && l.smem_bytes <= 113 * 1024) ? 2 : 1;
   const long long slots = static_cast<long long>(per_sm) * (a.num_sms > 0 ? a.num_sms : 148);
-  const int per_cta = static_cast<int>((total + slots - 1) / slots);
-  const int n_ctas = static_cast<int>((total + per_cta - 1) / per_cta);
+  // (at least one CTA: with no chunk at all it still writes the zero outputs)
+  const int n_ctas = static_cast<int>(bound < 1 ? 1 : bound < slots ? bound : slots);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);
   cfg.blockDim = dim3(kThreads);
@@ -985,11 +1272,11 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, bool early) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = early ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, a, l, per_cta);
+  return cudaLaunchKernelEx(&cfg, kernel, a, l);
 }
 
 cudaError_t launch_decode_partials_tc(const DecodeArgs& a, cudaStream_t stream, bool early) {
-  if (a.batch <= 0 || a.max_chunks <= 0) return cudaSuccess;
+  if (a.batch <= 0) return cudaSuccess;
   switch (a.group) {
     case 1: return launch_g<1>(a, stream, early);
     case 2: return launch_g<2>(a, stream, early);

@@ -65,6 +65,16 @@ cudaError_t launch_quantize_small(const QuantizeArgs* first, const QuantizeArgs*
 cudaError_t launch_quantize_tc(const QuantizeArgs& args, const CUtensorMap& x_map, const CUtensorMap& w_map,
                                int num_sms, cudaStream_t stream);
 
+// Where the split-K partials of one query head are: entries base,
+// base + stride, ..., base + (count - 1) stride of the partials array, each
+// (m, l, 2 pad, acc[128]).  The SIMT kernel writes one entry per 512-token
+// chunk (stride 1); the tensor-core kernel one per run of consecutive chunks
+// that a CTA processed (stride G, the entries of a group's G query heads
+// side by side).
+struct SegInfo {
+  int base, count, stride, pad;
+};
+
 struct DecodeArgs {
   const void* q;            // [batch][n_q][128]
   int batch, n_q, n_kv, group;
@@ -84,10 +94,13 @@ struct DecodeArgs {
   float qjl_coef;           // sqrt(pi/2) / m
   float* out;               // [batch][n_q][128]
   float* ws_q;              // [batch*n_q][256]: rotated query, projected query
-  float* ws_part;           // [batch*n_q][max_chunks][kPartStride]
+  float* ws_part;           // partial entries of kPartStride floats (see SegInfo)
   uint8_t* ws_bk;           // [batch*n_q][bk_stride]: tensor-core score operand pieces (null: not built)
+  int* ws_ticket;           // [batch*n_q]: per (sequence, KV head) count of finished segments
+  SegInfo* ws_seg;          // [batch*n_q]: where each query head's partials are
   int bk_stride;
   int max_chunks;
+  int merge_in_partials;    // the tensor-core kernel merges and writes `out` itself
   const float* R;           // [128][128] row-major
   const float* Rt;
   const float* Spt;
@@ -105,7 +118,7 @@ __host__ __device__ inline long long transposed_word(long long blk, int head, in
 }
 
 constexpr int kChunk = 512;       // context tokens per split-K work item
-constexpr int kQPieces = 6;       // e4m3 pieces of a query coefficient (tensor-core decode)
+constexpr int kQPieces = 5;       // e4m3 pieces of a query coefficient (tensor-core decode)
 
 // Bytes of one query head's tensor-core score operand in the decode
 // workspace: for each key sign plane and the QJL plane, kQPieces rows of 128
@@ -117,6 +130,15 @@ __host__ __device__ constexpr int bk_head_bytes(int k_mse_bits, bool qjl) {
   return ((k_mse_bits >= 1 ? (1 << (k_mse_bits - 1)) : 0) + (qjl ? 1 : 0)) * kQPieces * 128 + kBkHeader;
 }
 constexpr int kPartStride = 132;  // m, l, 2 pad, acc[128]
+
+// Partial entries a decode workspace holds: one per (query head, chunk) for
+// the SIMT kernel, and for the tensor-core kernel one per (query head,
+// segment), where a (sequence, KV head) group has one segment per CTA whose
+// run of chunks touches it, i.e. at most n_groups + n_ctas segments of G
+// entries, n_ctas <= 2 num_sms.
+__host__ __device__ constexpr long long partial_entries(long long n_vec, int max_chunks, int num_sms) {
+  return n_vec * max_chunks > n_vec + 16ll * num_sms ? n_vec * max_chunks : n_vec + 16ll * num_sms;
+}
 
 cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_t stream);
 

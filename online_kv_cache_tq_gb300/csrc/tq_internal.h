@@ -48,6 +48,13 @@ struct HostTables {
 // Build R, S, S' and the codebooks on the host (host_builder.cpp).
 void build_host_tables(int d, int qjl_m, uint64_t seed, int k_mse_bits, int v_bits, HostTables* out);
 
+// Every host-side check of tq_decode_attention for a workspace of
+// workspace_bytes (api.cu); launches nothing.
+tq_status check_decode_call(const tq_codebook* book, const void* q, tq_dtype dtype, int batch, int n_q_heads,
+                            int n_kv_heads, const tq_cache_view* cache, const int32_t* block_table, int max_blocks,
+                            const int32_t* context_lens, int max_context, float scale, float* out,
+                            size_t workspace_bytes);
+
 }  // namespace tq
 
 struct tq_codebook {

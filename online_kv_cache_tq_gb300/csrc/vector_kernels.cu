@@ -1,5 +1,5 @@
 // Per-vector kernels of a decode step: quantize-append of the step's new keys
-// and values (one vector per 256-thread CTA), the query preparation of decode
+// and values (one or four vectors per 256-thread CTA), the query preparation of decode
 // attention (two query heads per 256-thread CTA; a fused launch runs both for
 // a step), and the merge of the split-K partials with the back-rotation (two
 // query heads per 512-thread CTA).
@@ -19,7 +19,13 @@
 namespace tq {
 namespace {
 
-constexpr int kQueriesPerCta = 2;   // query heads prepared by one block
+// Query heads prepared by one block: two for a decode step's few hundred
+// (more blocks in flight, the launch is latency-bound), eight beyond
+// kManyQueries, where the matrix loads (128 KB of R^T and S^T from L2 per
+// block) dominate.
+constexpr int kQueriesPerCta = 2;
+constexpr int kQueriesPerCtaMany = 8;
+constexpr int kManyQueries = 1024;
 
 __device__ __forceinline__ float load_elem(const void* base, long long idx, bool bf16) {
   if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
@@ -27,71 +33,138 @@ __device__ __forceinline__ float load_elem(const void* base, long long idx, bool
 }
 
 
-// Quantize head vector v of `a` (n = ||x||, y = R x / n, nearest level, and
-// for keys the rotated residual r' = R x - n c[code], its norm and the signs
-// of S' r').  Thread (o, q) of the 256 works on rotated coordinate o; the
-// two copies of o split the matrix-vector products and threads q == 0
-// (warps 0-3) write the results.
-__device__ __forceinline__ void quantize_vector(const QuantizeArgs& a, int v, bool bf16) {
-  __shared__ float x_s[kDim];
-  __shared__ float r_s[kDim];
-  __shared__ float red_s[4 * kDim];
-  __shared__ float part_s[4];
+// out[j] = sum_i w[i * 128 + o] * x_s[j][i] for the NV vectors x_s[j] and
+// o = threadIdx.x % 128: thread (o, hf) sums the 64 terms i in [64 hf, 64 hf
+// + 64) with 32 loads of w in flight, every load serving all NV vectors; the
+// halves meet in red_s.  Every thread returns out[j] for its o; x_s must be
+// visible to all threads before the call, and red_s is free again on return.
+template <int NV>
+__device__ __forceinline__ void matvec_batch(const float* __restrict__ w, const float (*x_s)[kDim],
+                                             float (*red_s)[NV][kDim], float (&out)[NV]) {
+  const int o = threadIdx.x & 127, hf = threadIdx.x >> 7;
+  float acc[NV];
+#pragma unroll
+  for (int j = 0; j < NV; ++j) acc[j] = 0.f;
+#pragma unroll
+  for (int i0 = 0; i0 < 64; i0 += 32) {
+    const float* wp = w + (64 * hf + i0) * kDim + o;
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = __ldg(wp + k * kDim);
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+#pragma unroll
+      for (int j = 0; j < NV; ++j) acc[j] = fmaf(v[k], x_s[j][64 * hf + i0 + k], acc[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < NV; ++j) red_s[hf][j][o] = acc[j];
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < NV; ++j) out[j] = red_s[0][j][o] + red_s[1][j][o];
+  __syncthreads();
+}
+
+// Quantize head vectors v0 .. v0 + nv - 1 of `a` (nv <= NV): n = ||x||,
+// y = R x / n, nearest level, and for keys the rotated residual
+// r' = R x - n c[code], its norm and the signs of S' r'.  Thread (o, hf) of
+// the 256 works on rotated coordinate o of every vector; the two halves split
+// each matrix-vector product (every matrix load serves the NV vectors), and
+// the threads of half 0 write the results.
+template <int NV>
+__device__ __forceinline__ void quantize_vectors(const QuantizeArgs& a, int v0, int nv, bool bf16) {
+  __shared__ __align__(16) float x_s[NV][kDim];   // inputs, then residuals
+  __shared__ float red_s[2][NV][kDim];
+  __shared__ float nrm_s[NV][4], rnrm_s[NV][4];   // per-warp partial sums of squares
   const int o = threadIdx.x & 127;
   const bool lead = threadIdx.x < 128;
   const int lane = o & 31;
   const int warp = o >> 5;
-  const int token = v / a.n_kv;
-  const int head = v - token * a.n_kv;
-
-  const long long idx = static_cast<long long>(v) * kDim + o;
-  const float x = bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.x)[idx])
-                       : reinterpret_cast<const float*>(a.x)[idx];
-  if (lead) x_s[o] = x;
-  const float n = sqrtf(sum128(x * x, part_s));          // its barriers also publish x_s
-  const float yv = gemv<kVecThreads>(a.Rt, x_s, red_s);           // (R x)_o
-  const float y = n > 0.f ? yv / n : 0.f;
-  int code = 0;
-  for (int t = 0; t + 1 < (1 << a.bits); ++t) code += (y > a.bounds[t]) ? 1 : 0;
-
-  const long long cache_rows = static_cast<long long>(a.num_blocks) * a.block_size;
-  const long long slot = slot_of(a, token);
-  const bool ok = slot >= 0 && slot < cache_rows;
-  if (slot >= cache_rows && threadIdx.x == 0) atomicCAS(a.error, 0, kErrSlot);
-  const long long blk = ok ? slot / a.block_size : 0;
-  const int off = ok ? static_cast<int>(slot - blk * a.block_size) : 0;
-  const long long row = (blk * a.n_kv + head) * a.block_size + off;
-
-  if (a.transposed) {
-    if (ok && lead) {
-      unsigned* words = reinterpret_cast<unsigned*>(a.codes);
-      const unsigned mask = 1u << (off & 31);
-      for (int p = 0; p < a.bits; ++p) {
-        unsigned* w = words + transposed_word(blk, head, a.n_kv, a.bits, p, o, a.block_size, off);
-        if ((code >> p) & 1) atomicOr(w, mask); else atomicAnd(w, ~mask);
-      }
-    }
-  } else {
-    for (int p = 0; p < a.bits; ++p) {
-      const unsigned word = __ballot_sync(0xffffffffu, (code >> p) & 1);
-      if (ok && lead && lane == 0) reinterpret_cast<unsigned*>(a.codes + row * (a.bits * 16))[p * 4 + warp] = word;
+  for (int i = threadIdx.x; i < NV * kDim; i += kVecThreads) {
+    const int j = i >> 7;
+    x_s[j][i & 127] = j < nv ? load_elem(a.x, static_cast<long long>(v0) * kDim + i, bf16) : 0.f;
+  }
+  __syncthreads();
+  if (lead) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      float sq = x_s[j][o] * x_s[j][o];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+      if (lane == 0) nrm_s[j][warp] = sq;
     }
   }
-  if (ok && threadIdx.x == 0) a.norm[row] = n;
+  float yv[NV];
+  matvec_batch<NV>(a.Rt, x_s, red_s, yv);          // (R x_j)_o; its barriers also publish nrm_s
+  const long long cache_rows = static_cast<long long>(a.num_blocks) * a.block_size;
+  float n[NV];
+  int code[NV];
+  long long row[NV], blk[NV];
+  int off[NV];
+  bool ok[NV];
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    n[j] = sqrtf((nrm_s[j][0] + nrm_s[j][1]) + (nrm_s[j][2] + nrm_s[j][3]));
+    const float y = n[j] > 0.f ? yv[j] / n[j] : 0.f;
+    code[j] = 0;
+    for (int t = 0; t + 1 < (1 << a.bits); ++t) code[j] += (y > a.bounds[t]) ? 1 : 0;
+    const int v = v0 + j;
+    const int token = v / a.n_kv;
+    const int head = v - token * a.n_kv;
+    const long long slot = j < nv ? slot_of(a, token) : -1;
+    ok[j] = slot >= 0 && slot < cache_rows;
+    if (j < nv && slot >= cache_rows && threadIdx.x == 0) atomicCAS(a.error, 0, kErrSlot);
+    blk[j] = ok[j] ? slot / a.block_size : 0;
+    off[j] = ok[j] ? static_cast<int>(slot - blk[j] * a.block_size) : 0;
+    row[j] = (blk[j] * a.n_kv + head) * a.block_size + off[j];
+    if (a.transposed) {
+      if (ok[j] && lead) {
+        unsigned* words = reinterpret_cast<unsigned*>(a.codes);
+        const unsigned mask = 1u << (off[j] & 31);
+        for (int p = 0; p < a.bits; ++p) {
+          unsigned* w = words + transposed_word(blk[j], head, a.n_kv, a.bits, p, o, a.block_size, off[j]);
+          if ((code[j] >> p) & 1) atomicOr(w, mask); else atomicAnd(w, ~mask);
+        }
+      }
+    } else {
+      for (int p = 0; p < a.bits; ++p) {
+        const unsigned word = __ballot_sync(0xffffffffu, (code[j] >> p) & 1);
+        if (ok[j] && lead && lane == 0) reinterpret_cast<unsigned*>(a.codes + row[j] * (a.bits * 16))[p * 4 + warp] = word;
+      }
+    }
+    if (ok[j] && threadIdx.x == 0) a.norm[row[j]] = n[j];
+  }
 
   if (a.qjl != nullptr) {
-    const float r = fmaf(-n, a.levels[code], yv);
-    if (lead) r_s[o] = r;
-    const float gamma = sqrtf(sum128(r * r, part_s));    // its barriers also publish r_s
-    const float z = gemv<kVecThreads>(a.Spt, r_s, red_s);
-    const unsigned word = __ballot_sync(0xffffffffu, z > 0.f);
-    if (ok && lead && lane == 0) reinterpret_cast<unsigned*>(a.qjl + row * 16)[warp] = word;
-    if (ok && threadIdx.x == 0) a.rnorm[row] = gamma;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const float r = fmaf(-n[j], a.levels[code[j]], yv[j]);
+      if (lead) {
+        x_s[j][o] = r;                            // (x_s is no longer read: the last barrier passed)
+        float sq = r * r;
+#pragma unroll
+        for (int off2 = 16; off2 > 0; off2 >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off2);
+        if (lane == 0) rnrm_s[j][warp] = sq;
+      }
+    }
+    __syncthreads();
+    float z[NV];
+    matvec_batch<NV>(a.Spt, x_s, red_s, z);
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const float gamma = sqrtf((rnrm_s[j][0] + rnrm_s[j][1]) + (rnrm_s[j][2] + rnrm_s[j][3]));
+      const unsigned word = __ballot_sync(0xffffffffu, z[j] > 0.f);
+      if (ok[j] && lead && lane == 0) reinterpret_cast<unsigned*>(a.qjl + row[j] * 16)[warp] = word;
+      if (ok[j] && threadIdx.x == 0) a.rnorm[row[j]] = gamma;
+    }
   }
 }
 
+// Appended vectors per block of a decode step: one for a few hundred (more
+// blocks in flight: the launch is latency-bound), four beyond
+// kManyAppends per tensor, where the matrix loads dominate.
+constexpr int kManyAppends = 256;
 
-// Query heads v0 .. v0 + nv - 1 (nv <= kQueriesPerCta; consecutive heads
+// Query heads v0 .. v0 + nv - 1 (nv <= QN; consecutive heads
 // share every matrix load): ws_q[v] = (R q, S' R q), the projection taken as
 // S q since S' = S R^T; with ws_bk, also each head's tensor-core score
 // operand: e4m3 pieces of 2 sigma_0 a_S (R q)_j / beta_j per key sign plane S
@@ -100,12 +173,15 @@ __device__ __forceinline__ void quantize_vector(const QuantizeArgs& a, int v, bo
 // the 0/1 bit products into +-1 sign products.  256 threads: thread (o, m)
 // computes coordinate o of R q (m = 0) or of S q (m = 1) for every head, so
 // the two products run side by side.
+template <int QN>
 __device__ __forceinline__ void prepare_queries(const DecodeArgs& a, int v0, int nv, bool bf16) {
-  constexpr int QN = kQueriesPerCta;
   __shared__ __align__(16) float q_s[QN][kDim];
   __shared__ float stat_s[2][4][2 * QN];        // [m][warp]: max, then sum, per head
   const int o = threadIdx.x & 127, m = threadIdx.x >> 7;
   const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) & 3;
+  // the partials kernel that follows counts finished segments per (sequence,
+  // KV head) from zero (at most batch * n_q groups)
+  if (a.ws_ticket != nullptr && threadIdx.x < nv) a.ws_ticket[v0 + threadIdx.x] = 0;
   for (int i = threadIdx.x; i < QN * kDim; i += kVecThreads) {
     const int j = i >> 7;
     q_s[j][i & 127] = j < nv ? load_elem(a.q, static_cast<long long>(v0) * kDim + i, bf16) : 0.f;
@@ -206,11 +282,12 @@ __device__ __forceinline__ int context_of(const DecodeArgs& a, int b) {
 
 // out[v] = R^T (merged acc / merged l) for the query heads v = 2 blockIdx.x
 // and 2 blockIdx.x + 1 (one head when the count is odd).  kGemvThreads = 512:
-// thread (o, q) merges coordinate o of head q / 2 over the chunks c with
-// c % 2 == q % 2 as a running (m, l, acc); the two copies of a head merge
-// theirs; then thread (o, q) sums the terms [32 q, 32 q + 32) of both heads'
-// back-rotations from one set of loads of R.  Every thread's chunk loads are
-// independent, so a launch is a few memory round trips long.
+// thread (o, q) merges coordinate o of head q / 2 over the partial entries c
+// (listed by the head's SegInfo) with c % 2 == q % 2 as a running (m, l, acc);
+// the two copies of a head merge theirs; then thread (o, q) sums the terms
+// [32 q, 32 q + 32) of both heads' back-rotations from one set of loads of R.
+// Every thread's entry loads are independent, so a launch is a few memory
+// round trips long.
 __global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
   constexpr int kHeads = 2;
   __shared__ float o_s[kHeads][kDim];
@@ -226,16 +303,18 @@ __global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
   float m = -INFINITY, l = 0.f, acc = 0.f;
   if (live) {
     const int ctx = context_of(a, vec / a.n_q);
-    const int n_chunks = (ctx + kChunk - 1) / kChunk;
-    const float* part = a.ws_part + static_cast<long long>(vec) * a.max_chunks * kPartStride;
-    for (int c0 = q & 1; c0 < n_chunks; c0 += 2 * 4) {
+    // (a sequence without context has no entries, and its segment record is stale)
+    const SegInfo seg = ctx > 0 ? a.ws_seg[vec] : SegInfo{0, 0, 0, 0};
+    const int n_entries = seg.count;
+    for (int c0 = q & 1; c0 < n_entries; c0 += 2 * 4) {
       float mc[4], lc[4], ac[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int c = c0 + 2 * j;
-        mc[j] = c < n_chunks ? part[c * kPartStride] : -INFINITY;
-        lc[j] = c < n_chunks ? part[c * kPartStride + 1] : 0.f;
-        ac[j] = c < n_chunks ? part[c * kPartStride + 4 + o] : 0.f;
+        const float* part = a.ws_part + (static_cast<long long>(seg.base) + static_cast<long long>(c) * seg.stride) * kPartStride;
+        mc[j] = c < n_entries ? part[0] : -INFINITY;
+        lc[j] = c < n_entries ? part[1] : 0.f;
+        ac[j] = c < n_entries ? part[4 + o] : 0.f;
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -295,28 +374,33 @@ __global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
 __global__ void __launch_bounds__(kVecThreads) quantize_small_kernel(QuantizeArgs first, QuantizeArgs second,
                                                                       bool bf16) {
   const bool in_first = static_cast<int>(blockIdx.x) < first.n_vec;
-  quantize_vector(in_first ? first : second, in_first ? blockIdx.x : blockIdx.x - first.n_vec, bf16);
+  quantize_vectors<1>(in_first ? first : second, in_first ? blockIdx.x : blockIdx.x - first.n_vec, 1, bf16);
 }
 
+template <int QN>
 __global__ void __launch_bounds__(kVecThreads) qprep_kernel(DecodeArgs a, bool bf16) {
-  const int v0 = blockIdx.x * kQueriesPerCta;
-  prepare_queries(a, v0, min(kQueriesPerCta, a.batch * a.n_q - v0), bf16);
+  const int v0 = blockIdx.x * QN;
+  prepare_queries<QN>(a, v0, min(QN, a.batch * a.n_q - v0), bf16);
 }
 
 // One decode step's per-vector work: blocks [0, n_k) quantize the new keys,
-// [n_k, 2 n_k) the new values, the rest prepare the queries, kQueriesPerCta
+// [n_k, 2 n_k) the new values, the rest prepare the queries, QN
 // heads per block.  The decode
 // partials kernel that follows may start as soon as these blocks run (it
 // waits for their results where it reads them).
+template <int NV, int QN>
 __global__ void __launch_bounds__(kVecThreads) step_prep_kernel(QuantizeArgs ka, QuantizeArgs va, bool kv_bf16,
                                                                  DecodeArgs da, bool q_bf16) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int blk = blockIdx.x;
-  if (blk < ka.n_vec) quantize_vector(ka, blk, kv_bf16);
-  else if (blk < 2 * ka.n_vec) quantize_vector(va, blk - ka.n_vec, kv_bf16);
-  else {
-    const int v0 = (blk - 2 * ka.n_vec) * kQueriesPerCta;
-    prepare_queries(da, v0, min(kQueriesPerCta, da.batch * da.n_q - v0), q_bf16);
+  const int nb = (ka.n_vec + NV - 1) / NV;        // blocks per tensor
+  if (blk < 2 * nb) {
+    const QuantizeArgs& x = blk < nb ? ka : va;
+    const int v0 = (blk < nb ? blk : blk - nb) * NV;
+    quantize_vectors<NV>(x, v0, min(NV, x.n_vec - v0), kv_bf16);
+  } else {
+    const int v0 = (blk - 2 * nb) * QN;
+    prepare_queries<QN>(da, v0, min(QN, da.batch * da.n_q - v0), q_bf16);
   }
 }
 
@@ -334,7 +418,13 @@ cudaError_t launch_quantize_small(const QuantizeArgs* first, const QuantizeArgs*
 cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_t stream) {
   const int n_vec = args.batch * args.n_q;
   if (n_vec <= 0) return cudaSuccess;
-  qprep_kernel<<<(n_vec + kQueriesPerCta - 1) / kQueriesPerCta, kVecThreads, 0, stream>>>(args, bf16);
+  if (n_vec > kManyQueries) {
+    constexpr int QN = kQueriesPerCtaMany;
+    qprep_kernel<QN><<<(n_vec + QN - 1) / QN, kVecThreads, 0, stream>>>(args, bf16);
+  } else {
+    constexpr int QN = kQueriesPerCta;
+    qprep_kernel<QN><<<(n_vec + QN - 1) / QN, kVecThreads, 0, stream>>>(args, bf16);
+  }
   return cudaGetLastError();
 }
 
@@ -355,10 +445,18 @@ cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream, bo
 
 cudaError_t launch_step_prep(const QuantizeArgs& ka, const QuantizeArgs& va, bool kv_bf16, const DecodeArgs& da,
                              bool q_bf16, cudaStream_t stream) {
-  const int n = 2 * ka.n_vec + (da.batch * da.n_q + kQueriesPerCta - 1) / kQueriesPerCta;
-  if (n <= 0) return cudaSuccess;
-  step_prep_kernel<<<n, kVecThreads, 0, stream>>>(ka, va, kv_bf16, da, q_bf16);
-  return cudaGetLastError();
+  const int n_vec = da.batch * da.n_q;
+  const bool many_q = n_vec > kManyQueries, many_kv = ka.n_vec > kManyAppends;
+  auto launch = [&](auto kernel, int nv, int qn) {
+    const int n = 2 * ((ka.n_vec + nv - 1) / nv) + (n_vec + qn - 1) / qn;
+    if (n <= 0) return cudaSuccess;
+    kernel<<<n, kVecThreads, 0, stream>>>(ka, va, kv_bf16, da, q_bf16);
+    return cudaGetLastError();
+  };
+  if (many_kv && many_q) return launch(step_prep_kernel<4, kQueriesPerCtaMany>, 4, kQueriesPerCtaMany);
+  if (many_kv) return launch(step_prep_kernel<4, kQueriesPerCta>, 4, kQueriesPerCta);
+  if (many_q) return launch(step_prep_kernel<1, kQueriesPerCtaMany>, 1, kQueriesPerCtaMany);
+  return launch(step_prep_kernel<1, kQueriesPerCta>, 1, kQueriesPerCta);
 }
 
 }  // namespace tq

@@ -62,6 +62,28 @@ def read_sequence(cache, table_row, length, head, block_size):
     return out
 
 
+def decode_attention_heads(queries, cache, table_row, length, kv_head, book, scale=None):
+    """Outputs [H][d] of several query heads that read the same sequence and
+    KV head (a GQA group), and the normaliser max_t ||v_hat_t||: the same
+    arithmetic as ``decode_attention`` per head, with the cached keys and
+    values reconstructed once for the group."""
+    d = book["rot"].shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    block_size = cache["k_norm"].shape[2]
+    rows = read_sequence(cache, table_row, length, kv_head, block_size)
+    k_codes = packing.unpack_planes(rows["k_codes"], book["k_bits"], d)
+    khat = reconstruct_mse(rows["k_norm"].reshape(-1), k_codes, book["rot"], book["k_levels"])
+    vhat = reconstruct_mse(rows["v_norm"].reshape(-1), rows["v_code_values"], book["rot"], book["v_levels"])
+    qjl = "k_qjl" in rows and book["proj"].shape[0] > 0
+    signs = packing.unpack_signs(rows["k_qjl"], book["proj"].shape[0]) if qjl else None
+    outs = []
+    for query in np.asarray(queries, dtype=np.float64):
+        corr = qjl_estimate(query, rows["k_rnorm"].reshape(-1), signs, book["proj"]) if qjl else np.zeros(length)
+        outs.append(attend(query, khat, corr, vhat, scale))
+    return np.stack(outs), float(np.max(np.linalg.norm(vhat, axis=1)))
+
+
 def decode_attention(query, cache, table_row, length, kv_head, book, scale=None):
     """Output of one query head of one sequence, from the packed cache.
 

@@ -96,9 +96,14 @@ def test_host_only_handle_rejected_by_kernels(lib):
 
 
 def test_workspace_size_grows_with_context(lib):
+    # room for one partial entry per (query head, 512-token chunk) -- what the
+    # CUDA-core kernel writes -- and never less than the tensor-core kernel's
+    # per-segment entries, which do not grow with the context
     book = B.Codebook(device=-1)
-    small = B.tq_decode_workspace_bytes(book, 2, 8, 512)
-    large = B.tq_decode_workspace_bytes(book, 2, 8, 513)
+    small = B.tq_decode_workspace_bytes(book, 64, 64, 4096)
+    large = B.tq_decode_workspace_bytes(book, 64, 64, 4097)
     assert small % 256 == 0 and large > small
+    short = B.tq_decode_workspace_bytes(book, 2, 8, 512)
+    assert short == B.tq_decode_workspace_bytes(book, 2, 8, 513) > 0
     assert B.tq_decode_workspace_bytes(book, 0, 8, 512) == 0
     book.close()

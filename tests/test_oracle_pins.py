@@ -369,3 +369,20 @@ def test_cache_decode_uses_block_table_and_gqa_grouping():
     corr = attention.qjl_estimate(q[0, 3], keys["k_rnorm"], keys["signs"], book["proj"])
     expect = attention.attend(q[0, 3], khat, corr, vhat, 1 / math.sqrt(128))
     assert np.max(np.abs(out[0, 3] - expect)) < 1e-12
+
+
+def test_group_decode_equals_per_head_decode():
+    # decoding a GQA group's heads together reuses one reconstruction: same outputs
+    from oracle import attention
+    book = engine.build(k_bits=3, v_bits=2, qjl_m=128, seed=4)
+    rng = np.random.default_rng(12)
+    cache = engine.empty_cache(book, 2, 2, 64)
+    k = rng.standard_normal((90, 2, 128))
+    v = rng.standard_normal((90, 2, 128))
+    engine.append(cache, book, k, v, np.arange(90))
+    q = rng.standard_normal((3, 128))
+    table = np.array([1, 0])
+    outs, vmax = attention.decode_attention_heads(q, cache, table, 77, 1, book)
+    for h in range(3):
+        one, vm = attention.decode_attention(q[h], cache, table, 77, 1, book)
+        assert np.array_equal(outs[h], one) and vm == vmax

@@ -25,6 +25,7 @@ def test_single_head_fp32_outliers_every_vector():
     slots = np.arange(4096)
     quantize_into(book, cache, k, v, slots)
     rep = check_append(book, ref, cache, k, v, slots)
+    print("c1 fp32 append", rep)
     assert rep["vectors"] == 4096
     assert B.tq_get_last_device_error(book) == 0
 
