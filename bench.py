@@ -43,7 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 METRIC = "decode attn tokens/s & HBM GB/s (% of peak) over 3-bit KV; quantize vectors/s"
 HEADLINE = "c5_llama3_70b_paged"
-SECONDARY_DECODE = ("c2_llama3_8b_decode", "c4_long_context")
+SECONDARY_DECODE = ("c2_llama3_8b_decode", "c4_long_context", "c5_llama3_70b_paged_fp16_norms")
 CODE_EXEMPT = 1e-5          # codes within this distance of a boundary (unit-vector units) may differ
 ATTN_TOL = 1e-3             # max |o_gpu - o_oracle| / max_t ||v_hat_t||
 
@@ -222,7 +222,7 @@ class DecodeWorkload:
         self.seed = seed
         self.batch, self.n_q, self.n_kv = cfg["batch"], cfg["n_q"], cfg["n_kv"]
         self.book = B.Codebook(k_bits=cfg["k_bits"], v_bits=cfg["v_bits"], qjl_m=cfg["qjl_m"], seed=cfg["seed"],
-                               block_size=cfg["block_size"], device=device)
+                               block_size=cfg["block_size"], device=device, norm_bits=cfg.get("norm_bits", 32))
         self.ctx = W.context_lengths(cfg, seed)
         self.max_ctx = int(self.ctx.max())
         self.table, num_blocks = W.block_layout(self.ctx, cfg["block_size"], cfg.get("shuffled_table", False), seed)
@@ -259,10 +259,12 @@ class DecodeWorkload:
         self.ws, self.ws_bytes = C.allocate_workspace(self.book, self.batch, self.n_q, self.max_ctx)
         torch.cuda.synchronize()
         # tq_decode_step: append + query preparation (one launch up to 1024 head vectors, else
-        # quantize K, quantize V, prepare), then the partials kernel that also merges (tensor
-        # cores) or partials + merge (CUDA cores)
-        self.tc = B.tq_decode_kernel_kind(self.book, self.n_q, self.n_kv) == 1
-        self.launches_per_step = (1 if self.batch * self.n_kv <= 1024 else 3) + (1 if self.tc else 2)
+        # quantize K, quantize V, prepare), then the partials kernel, which merges in place or
+        # is followed by a merge launch
+        self.plan = B.tq_decode_plan(self.book, self.batch, self.n_q, self.n_kv, self.max_ctx)
+        self.tc = self.plan["tensor_cores"] == 1
+        self.launches_per_step = (1 if self.batch * self.n_kv <= 1024 else 3) + (1 if self.plan["merge_in_partials"]
+                                                                                  else 2)
 
     def step(self, i):
         """One decode step: tq_decode_step (append the new K/V token of every
@@ -274,16 +276,21 @@ class DecodeWorkload:
     def staged_step(self, i, ev):
         """The same step through the staged calls: the append + query
         preparation, then (between the events) the partials kernel exactly as
-        the step runs it -- it merges and writes the output itself."""
+        the step runs it (merging in place when the step's plan says so),
+        then the merge launch when the plan has one."""
         B = self.B
         view = self.views[i % len(self.views)]
         B.tq_decode_step_prepare(self.book, self.k_new, self.v_new, self.dtype_code, self.q, self.dtype_code,
                                  self.batch, self.n_q, self.n_kv, view, self.table_d, self.max_blocks, self.ctx_d,
                                  self.max_ctx, self.ws, self.ws_bytes)
+        fused = self.plan["merge_in_partials"] == 1
         ev[0].record()
         B.tq_decode_partials(self.book, self.batch, self.n_q, self.n_kv, view, self.table_d, self.max_blocks,
-                             self.ctx_d, self.max_ctx, 0.0, self.ws, self.ws_bytes, out=self.out)
+                             self.ctx_d, self.max_ctx, 0.0, self.ws, self.ws_bytes, out=self.out if fused else None)
         ev[1].record()
+        if not fused:
+            B.tq_decode_finish(self.book, self.batch, self.n_q, self.ctx_d, self.max_ctx, self.max_blocks, self.out,
+                               self.ws, self.ws_bytes)
 
     def e2e(self, steps, warmup):
         """Same step through the one-call C entry point for host buffers
@@ -393,10 +400,12 @@ def decode_summary(res, world, dev):
         "hbm_gbs_step": wl.cache_bytes / (step_ms * 1e-3) / 1e9,
         "bytes_per_token_head": wl.bytes_per_token_head,
         "compression_vs_bf16": 4.0 * 128 / wl.bytes_per_token_head,
+        "plan": wl.plan,
         "partials": {"kernel": wl.kernel_name(), "launch_ms": part_ms, "achieved_gbs": achieved,
                      "frac": achieved / peak, "peak_source": src + " hbm_gbs",
                      "algorithmic_bytes_per_launch": wl.cache_bytes},
         "context_tokens": int(wl.ctx.sum()), "l2": l2_note(len(wl.caches)),
+        "norm_bits": wl.book.norm_bits,
     }
 
 
@@ -526,6 +535,67 @@ def measure_single_head_fp32(steps, warmup):
             "note": "latency-bound sizes: one head, 4096 tokens"}
 
 
+BIAS_CASES = ((1, 0), (2, 128), (2, 0), (3, 128))   # (key bits, QJL rows): MSE-only and with the QJL bit
+
+
+def bias_sample(n=4096, n_queries=16, seed=5):
+    """Keys ~ N(0, I) (bf16) quantized by the GPU for each of BIAS_CASES, with
+    host copies of the inputs and of the cache rows the GPU wrote, and
+    queries ~ N(0, I): the material of the inner-product bias figures."""
+    import numpy as np
+    import torch
+
+    from online_kv_cache_tq_gb300 import binding as B
+    from online_kv_cache_tq_gb300 import cache as C
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    k = torch.randn((n, 1, 128), generator=g, device="cuda").to(torch.bfloat16)
+    slots = torch.arange(n, device="cuda", dtype=torch.int64)
+    cases = []
+    for k_bits, qjl in BIAS_CASES:
+        book = B.Codebook(k_bits=k_bits, v_bits=2, qjl_m=qjl, seed=0, block_size=64,
+                          device=torch.cuda.current_device())
+        cache = C.allocate_cache(book, n // 64, 1)
+        B.tq_quantize_append(book, k, None, B.TQ_BF16, n, 1, slots, C.cache_view(book, cache))
+        torch.cuda.synchronize()
+        cases.append({"k_bits": k_bits, "qjl_m": qjl,
+                      "cache": {f: t.cpu().numpy() for f, t in cache.items() if f.startswith("k_")}})
+    q = np.random.default_rng(seed).standard_normal((n_queries, 128))
+    return {"x": k.double().cpu().numpy().reshape(n, 128), "q": q, "cases": cases}
+
+
+def _bias_figures(sample):
+    """Slope of the estimated inner products on the true ones, sum e t / sum t^2
+    over (key, query) pairs, for keys decoded from the GPU's codes: stage 1
+    alone shrinks inner products by E||c||^2 = 1 - D_mse (d c_1^2, near 2/pi,
+    at 1 bit; 甲子光年 article §2 第二階段), the QJL bit removes the shrinkage.
+    The standard error treats keys as independent."""
+    import numpy as np
+
+    from oracle import attention, codebook, engine, packing, quantize
+    x, q = sample["x"], sample["q"]
+    true = x @ q.T
+    out = []
+    for case in sample["cases"]:
+        ref = engine.build(k_bits=case["k_bits"], v_bits=2, qjl_m=case["qjl_m"], seed=0)
+        c = case["cache"]
+        rows = c["k_codes"].reshape(-1, c["k_codes"].shape[-1])[:len(x)]
+        codes = packing.unpack_planes(rows, ref["k_bits"], 128)
+        xhat = quantize.reconstruct_mse(c["k_norm"].reshape(-1)[:len(x)], codes, ref["rot"], ref["k_levels"])
+        est = xhat @ q.T
+        if case["qjl_m"]:
+            signs = packing.unpack_signs(c["k_qjl"].reshape(-1, 16)[:len(x)], ref["proj"].shape[0])
+            gamma = c["k_rnorm"].reshape(-1)[:len(x)]
+            est = est + np.stack([attention.qjl_estimate(qq, gamma, signs, ref["proj"]) for qq in q], axis=1)
+        s_i, w_i = np.sum(est * true, axis=1), np.sum(true * true, axis=1)
+        slope = float(s_i.sum() / w_i.sum())
+        stderr = float(np.sqrt(np.sum((s_i - slope * w_i) ** 2)) / w_i.sum())
+        expect = 1.0 if case["qjl_m"] else 1.0 - codebook.mse_distortion(128, ref["k_levels"], ref["k_bounds"])
+        out.append({"k_bits": case["k_bits"], "qjl_m": case["qjl_m"], "mse_bits": ref["k_bits"],
+                    "slope": slope, "stderr": stderr, "expected": float(expect)})
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     torch.cuda.set_device(local_rank)
@@ -554,6 +624,8 @@ def run_ours(args, rank, world, local_rank):
             if sample is not None:
                 out["quant_samples"].append(sample)
         out["secondary"]["c1_single_head_parity"] = measure_single_head_fp32(20, 3)
+    if want_parity:
+        out["bias_sample"] = bias_sample()
     return out
 
 
@@ -678,7 +750,7 @@ def _quant_parity(sample):
     return rep
 
 
-def cpu_leg(name, n_groups, pool, procs, decode_samples, quant_samples):
+def cpu_leg(name, n_groups, pool, procs, decode_samples, quant_samples, bias=None):
     """The oracle on the host cores: its timed decode throughput on a bounded
     sample of the workload (cpu_baseline), then the parity figures of the GPU
     outputs and codes sampled by the GPU runs."""
@@ -695,6 +767,8 @@ def cpu_leg(name, n_groups, pool, procs, decode_samples, quant_samples):
             "worst_normalised_error": max(worst), "within_tolerance": max(worst) <= ATTN_TOL}
     for rep in pool.map(_quant_parity, quant_samples):
         parity["quantize"]["c3_prefill_quantize_b%d" % rep["bits"]] = rep
+    if bias is not None:
+        parity["inner_product_bias"] = _bias_figures(bias)
     return base, parity
 
 
@@ -782,13 +856,14 @@ def main(argv=None):
                      "peak_source": peak_src + " hbm_gbs", "algorithmic_bytes_per_launch": wl.cache_bytes,
                      "launch_ms": part_ms},
         "gpu_launches": wl.launches_per_step * args.steps,
+        "plan": wl.plan,
         "clocks": head["clocks"],
         "e2e": e2e,
         "secondary": res["secondary"],
     }
     if pool is not None:
         base, parity = cpu_leg(args.workload, args.cpu_groups, pool, procs, res["decode_samples"],
-                               res["quant_samples"])
+                               res["quant_samples"], res.get("bias_sample"))
         pool.close()
         line["cpu_baseline"] = base
         line["parity"] = parity

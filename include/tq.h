@@ -57,7 +57,11 @@ typedef enum { TQ_BF16 = 0, TQ_FP32 = 1 } tq_dtype;
  * v_bits: value MSE bits (1..4).  qjl_m: QJL projection rows (0 = off, or
  * 128).  seed: seeds the SplitMix64 stream that draws R (Haar, via QR of a
  * Gaussian matrix) and S.  block_size: tokens per cache block, a multiple of
- * 32 for device handles. */
+ * 32 for device handles.  norm_bits: width of the stored norms (the vector
+ * norm and, for keys, the residual norm): 32 (or 0) for float32, 16 for
+ * float16, which saves 6 of the 108 bytes of a (token, head) at 3/3 bits;
+ * the key residual is then taken against the float16 norm, the value the
+ * decoder reconstructs. */
 typedef struct {
   int d;
   int k_bits;
@@ -65,6 +69,7 @@ typedef struct {
   int qjl_m;
   uint64_t seed;
   int block_size;
+  int norm_bits;
 } tq_config;
 
 typedef struct tq_codebook tq_codebook; /* opaque, library-owned */
@@ -78,15 +83,16 @@ typedef struct tq_codebook tq_codebook; /* opaque, library-owned */
  * [v_bits][d][block_size/8] bytes, and for plane p and coordinate j, bit t%8
  * of byte t/8 holds bit p of the code of the token at offset t (the same
  * bytes per token as the key layout).  QJL bit k is bit k%8 of byte k/8, set
- * when the k-th projected residual is > 0.  Norms are float32.  Every pointer
- * must be 16-byte aligned; k_qjl/k_rnorm may be NULL when qjl_m == 0. */
+ * when the k-th projected residual is > 0.  Norms are float32, or float16
+ * when the handle was built with norm_bits 16.  Every pointer must be 16-byte
+ * aligned; k_qjl/k_rnorm may be NULL when qjl_m == 0. */
 typedef struct {
   void* k_codes;
   void* k_qjl;
-  float* k_norm;
-  float* k_rnorm;
+  void* k_norm;
+  void* k_rnorm;
   void* v_codes;
-  float* v_norm;
+  void* v_norm;
   int num_blocks;
   int n_kv_heads;
   int block_size;
@@ -127,6 +133,24 @@ tq_status tq_cache_field_bytes(const tq_codebook* book, size_t bytes_per_item[6]
 tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void* v, tq_dtype dtype,
                              int n_tokens, int n_kv_heads, const int64_t* slot_mapping,
                              const tq_cache_view* cache, void* stream);
+
+/* Reconstruction-error monitor (intelliparadigm.com §3.3 tracks the running
+ * mean of ||original - quantized||_2 in a deployment; the reconstruction is
+ * the stage-1 one of 甲子光年 article §2 第一階段, x_hat = n R^T c[code]).
+ * For the vectors x: device [n_tokens][n_kv_heads][d] in `dtype` that an
+ * earlier tq_quantize_append wrote at slot_mapping (same slots, same cache),
+ * which = 0 for keys, 1 for values, the call ADDS into stats (device, four
+ * doubles, 8-byte aligned): sum over vectors of ||x - x_hat||, of
+ * ||x - x_hat||^2, of ||x||^2, and the number of vectors (negative or
+ * out-of-range slots are skipped).  A caller keeps a running mean by zeroing
+ * stats once and calling this after each append; stats[0] / stats[3] is the
+ * mean error, stats[1] / stats[2] the relative squared error.  For keys with
+ * QJL, ||x - x_hat|| is also the stored residual norm.  Reads the cache only;
+ * asynchronous on `stream`; calls that overlap on the GPU may add into the
+ * same stats. */
+tq_status tq_reconstruction_error(const tq_codebook* book, const void* x, tq_dtype dtype, int which, int n_tokens,
+                                  int n_kv_heads, const int64_t* slot_mapping, const tq_cache_view* cache,
+                                  double* stats, void* stream);
 
 /* Workspace bytes tq_decode_attention needs for this batch shape (the
  * split-K partials and the rotated/projected queries).  max_context bounds
@@ -282,12 +306,41 @@ tq_status tq_decode_attention_static(const tq_codebook* book, const void* q, tq_
  * in tensor memory), 0 for the CUDA-core kernel.  Host only; launches nothing. */
 tq_status tq_decode_kernel_kind(const tq_codebook* book, int n_q_heads, int n_kv_heads, int* tensor_cores);
 
+/* How tq_decode_attention / tq_decode_step run this shape (host only; launches
+ * nothing): tensor_cores 1 for the tensor-core partials kernel (else the
+ * CUDA-core one); merge_in_partials 1 when that kernel merges each (sequence,
+ * KV head) group and writes the output itself (at most as many groups as
+ * CTAs), 0 when a merge launch follows it; partials_ctas the CTAs of its
+ * persistent grid (0 for the CUDA-core kernel); chunk_tokens the context
+ * tokens of one work item. */
+typedef struct {
+  int tensor_cores;
+  int merge_in_partials;
+  int partials_ctas;
+  int chunk_tokens;
+} tq_decode_plan_info;
+tq_status tq_decode_plan(const tq_codebook* book, int batch, int n_q_heads, int n_kv_heads, int max_context,
+                         tq_decode_plan_info* info);
+
 /* Synchronise `stream`, then return (and clear) the first device-side error
  * code recorded since the last call: 0 none, 1 slot out of range in
  * quantize-append, 2 block id out of range in decode, 3 context length out of
  * range in decode, 4 a kernel's internal wait timed out (the kernel stopped
- * early; its outputs are incomplete).  Returns TQ_ERR_DEVICE when *code != 0. */
+ * early; its outputs are incomplete), 5 a merge found the partials of a
+ * (sequence, KV head) missing or out of range (after a code 4 in the same
+ * call, or tq_decode_finish without tq_decode_partials; those outputs are
+ * zero).  Returns TQ_ERR_DEVICE when *code != 0. */
 tq_status tq_get_last_device_error(const tq_codebook* book, void* stream, int* code);
+
+/* A test aid for the bounded waits, off by default: while enabled on a
+ * handle, the first CTA of the tensor-core decode kernel withholds the commit
+ * of its first score MMAs, so its builders' wait for them runs out after the
+ * kernels' one-second limit.  The call then ends normally with that CTA
+ * stopped early (its in-flight copies and MMAs drained, its tensor memory
+ * freed): tq_get_last_device_error reports code 4 and the outputs are
+ * incomplete; later calls with it disabled are unaffected.  Not for use in
+ * production. */
+tq_status tq_debug_withhold_commit(tq_codebook* book, int enable);
 
 /* Static description of a status code. */
 const char* tq_status_string(tq_status status);

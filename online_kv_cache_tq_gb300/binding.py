@@ -21,10 +21,11 @@ FIELDS = ("k_codes", "k_qjl", "k_norm", "k_rnorm", "v_codes", "v_norm")
 
 # Entry points declared in include/tq.h, checked by the ABI test.
 EXPORTED = ("tq_codebook_build", "tq_codebook_destroy", "tq_codebook_levels", "tq_codebook_matrices",
-            "tq_cache_field_bytes", "tq_quantize_append", "tq_decode_workspace_bytes",
+            "tq_cache_field_bytes", "tq_quantize_append", "tq_reconstruction_error", "tq_decode_workspace_bytes",
             "tq_decode_attention", "tq_decode_step", "tq_decode_step_host", "tq_decode_step_host_workspace_bytes",
             "tq_decode_step_prepare", "tq_decode_prepare", "tq_decode_partials", "tq_decode_finish",
-            "tq_decode_attention_static", "tq_decode_kernel_kind", "tq_get_last_device_error",
+            "tq_decode_attention_static", "tq_decode_kernel_kind", "tq_decode_plan", "tq_debug_withhold_commit",
+            "tq_get_last_device_error",
             "tq_status_string")
 
 
@@ -36,13 +37,19 @@ class TQError(RuntimeError):
 
 class tq_config(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("k_bits", ctypes.c_int), ("v_bits", ctypes.c_int),
-                ("qjl_m", ctypes.c_int), ("seed", ctypes.c_uint64), ("block_size", ctypes.c_int)]
+                ("qjl_m", ctypes.c_int), ("seed", ctypes.c_uint64), ("block_size", ctypes.c_int),
+                ("norm_bits", ctypes.c_int)]
 
 
 class tq_cache_view(ctypes.Structure):
     _fields_ = [("k_codes", ctypes.c_void_p), ("k_qjl", ctypes.c_void_p), ("k_norm", ctypes.c_void_p),
                 ("k_rnorm", ctypes.c_void_p), ("v_codes", ctypes.c_void_p), ("v_norm", ctypes.c_void_p),
                 ("num_blocks", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("block_size", ctypes.c_int)]
+
+
+class tq_decode_plan_info(ctypes.Structure):
+    _fields_ = [("tensor_cores", ctypes.c_int), ("merge_in_partials", ctypes.c_int),
+                ("partials_ctas", ctypes.c_int), ("chunk_tokens", ctypes.c_int)]
 
 
 _LIB = None
@@ -68,6 +75,7 @@ def load():
     lib.tq_codebook_matrices.argtypes = [vp, vp, vp]
     lib.tq_cache_field_bytes.argtypes = [vp, ctypes.POINTER(sz * 6)]
     lib.tq_quantize_append.argtypes = [vp, vp, vp, i32, i32, i32, vp, ctypes.POINTER(tq_cache_view), vp]
+    lib.tq_reconstruction_error.argtypes = [vp, vp, i32, i32, i32, i32, vp, ctypes.POINTER(tq_cache_view), vp, vp]
     lib.tq_decode_workspace_bytes.argtypes = [vp, i32, i32, i32]
     lib.tq_decode_workspace_bytes.restype = sz
     lib.tq_decode_attention.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.POINTER(tq_cache_view), vp, i32,
@@ -87,6 +95,8 @@ def load():
     lib.tq_decode_attention_static.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.POINTER(tq_cache_view), vp,
                                                i32, vp, i32, ctypes.c_float, vp, vp]
     lib.tq_decode_kernel_kind.argtypes = [vp, i32, i32, ctypes.POINTER(i32)]
+    lib.tq_decode_plan.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(tq_decode_plan_info)]
+    lib.tq_debug_withhold_commit.argtypes = [vp, i32]
     lib.tq_get_last_device_error.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.tq_status_string.argtypes = [i32]
     lib.tq_status_string.restype = ctypes.c_char_p
@@ -123,8 +133,8 @@ def _stream(stream):
 class Codebook:
     """Owner of a tq_codebook handle."""
 
-    def __init__(self, d=128, k_bits=3, v_bits=3, qjl_m=128, seed=0, block_size=64, device=0):
-        self.config = tq_config(d, k_bits, v_bits, qjl_m, seed, block_size)
+    def __init__(self, d=128, k_bits=3, v_bits=3, qjl_m=128, seed=0, block_size=64, device=0, norm_bits=32):
+        self.config = tq_config(d, k_bits, v_bits, qjl_m, seed, block_size, norm_bits)
         self.device = device
         self.handle = tq_codebook_build(self.config, device)
 
@@ -146,6 +156,10 @@ class Codebook:
     @property
     def block_size(self):
         return self.config.block_size
+
+    @property
+    def norm_bits(self):
+        return 16 if self.config.norm_bits == 16 else 32
 
 
 def tq_codebook_build(config, device=0):
@@ -247,6 +261,15 @@ def tq_decode_step_prepare(book, k_new, v_new, kv_dtype, q, q_dtype, batch, n_q_
            "tq_decode_step_prepare")
 
 
+def tq_reconstruction_error(book, x, dtype, which, n_tokens, n_kv_heads, slot_mapping, view, stats, stream=None):
+    """Add reconstruction-error sums of appended vectors into ``stats`` (a
+    device float64 tensor of 4): sum ||x - x_hat||, sum ||x - x_hat||^2,
+    sum ||x||^2, count.  which: 0 keys, 1 values."""
+    _check(load().tq_reconstruction_error(book.handle, _ptr(x), dtype, which, n_tokens, n_kv_heads,
+                                          _ptr(slot_mapping), ctypes.byref(view), _ptr(stats), _stream(stream)),
+           "tq_reconstruction_error")
+
+
 def tq_decode_prepare(book, q, dtype, batch, n_q_heads, max_context, workspace, workspace_bytes, stream=None):
     _check(load().tq_decode_prepare(book.handle, _ptr(q), dtype, batch, n_q_heads, max_context, _ptr(workspace),
                                     workspace_bytes, _stream(stream)), "tq_decode_prepare")
@@ -297,3 +320,16 @@ def tq_get_last_device_error(book, stream=None):
 
 def tq_status_string(status):
     return load().tq_status_string(status).decode()
+
+
+def tq_decode_plan(book, batch, n_q_heads, n_kv_heads, max_context):
+    """dict(tensor_cores, merge_in_partials, partials_ctas, chunk_tokens) for a decode shape."""
+    info = tq_decode_plan_info()
+    _check(load().tq_decode_plan(book.handle, batch, n_q_heads, n_kv_heads, max_context, ctypes.byref(info)),
+           "tq_decode_plan")
+    return {name: getattr(info, name) for name, _ in info._fields_}
+
+
+def tq_debug_withhold_commit(book, enable):
+    """Test aid for the bounded waits (see include/tq.h)."""
+    _check(load().tq_debug_withhold_commit(book.handle, 1 if enable else 0), "tq_debug_withhold_commit")

@@ -21,7 +21,8 @@ def allocate_cache(book, num_blocks, n_kv_heads, device="cuda"):
             bits = nbytes * 8 // 128
             cache[name] = torch.zeros((num_blocks, n_kv_heads, bits, 128, bs // 8), dtype=torch.uint8, device=device)
         elif name.endswith("norm"):
-            cache[name] = torch.zeros((num_blocks, n_kv_heads, bs), dtype=torch.float32, device=device)
+            dt = torch.float16 if nbytes == 2 else torch.float32
+            cache[name] = torch.zeros((num_blocks, n_kv_heads, bs), dtype=dt, device=device)
         else:
             cache[name] = torch.zeros((num_blocks, n_kv_heads, bs, nbytes), dtype=torch.uint8, device=device)
     return cache

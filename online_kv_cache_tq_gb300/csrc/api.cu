@@ -242,6 +242,7 @@ tq_status tq_codebook_build(const tq_config* cfg, int device, tq_codebook** out)
   const bool host_only = device < 0;
   if (cfg->d <= 0 || cfg->d % 8 != 0 || cfg->d > 1024 || cfg->block_size <= 0) return TQ_ERR_INVALID_ARG;
   if (cfg->qjl_m < 0 || cfg->qjl_m % 8 != 0 || cfg->qjl_m > 1024) return TQ_ERR_INVALID_ARG;
+  if (cfg->norm_bits != 0 && cfg->norm_bits != 16 && cfg->norm_bits != 32) return TQ_ERR_INVALID_ARG;
   const int k_mse = cfg->qjl_m > 0 ? cfg->k_bits - 1 : cfg->k_bits;
   if (k_mse < 1 || k_mse > 4 || cfg->v_bits < 1 || cfg->v_bits > 4) return TQ_ERR_UNSUPPORTED;
   if (!host_only && (cfg->d != tq::kDim || (cfg->qjl_m != 0 && cfg->qjl_m != tq::kDim))) return TQ_ERR_UNSUPPORTED;
@@ -252,6 +253,7 @@ tq_status tq_codebook_build(const tq_config* cfg, int device, tq_codebook** out)
   b->device = host_only ? -1 : device;
   b->k_mse_bits = k_mse;
   b->v_bits = cfg->v_bits;
+  b->norm16 = cfg->norm_bits == 16;
   try {
     tq::build_host_tables(cfg->d, cfg->qjl_m, cfg->seed, k_mse, cfg->v_bits, &b->host);
   } catch (const std::bad_alloc&) {
@@ -309,10 +311,11 @@ tq_status tq_cache_field_bytes(const tq_codebook* book, size_t bytes_per_item[6]
   const bool qjl = book->cfg.qjl_m > 0;
   bytes_per_item[0] = book->k_mse_bits * d / 8;
   bytes_per_item[1] = qjl ? static_cast<size_t>(book->cfg.qjl_m) / 8 : 0;
-  bytes_per_item[2] = 4;
-  bytes_per_item[3] = qjl ? 4 : 0;
+  const size_t nb = book->norm16 ? 2 : 4;
+  bytes_per_item[2] = nb;
+  bytes_per_item[3] = qjl ? nb : 0;
   bytes_per_item[4] = book->v_bits * d / 8;
-  bytes_per_item[5] = 4;
+  bytes_per_item[5] = nb;
   return TQ_OK;
 }
 
@@ -343,6 +346,7 @@ tq_status append_args(const tq_codebook* book, const void* k, const void* v, tq_
   base.Rt = book->d_Rt;
   base.Spt = book->d_Spt;
   base.error = book->d_error;
+  base.norm16 = book->norm16;
   *ka = base;
   *va = base;
   ka->x = k;
@@ -391,6 +395,22 @@ tq_status tq_quantize_append(const tq_codebook* book, const void* k, const void*
   const tq_status st = append_args(book, k, v, dtype, n_tokens, n_kv_heads, slot_mapping, cache, &ka, &va);
   if (st != TQ_OK || n_tokens == 0) return st;
   return run_append(book, k, v, ka, va, dtype == TQ_BF16, static_cast<cudaStream_t>(stream));
+}
+
+tq_status tq_reconstruction_error(const tq_codebook* book, const void* x, tq_dtype dtype, int which, int n_tokens,
+                                  int n_kv_heads, const int64_t* slot_mapping, const tq_cache_view* cache,
+                                  double* stats, void* stream) {
+  if (which != 0 && which != 1) return TQ_ERR_INVALID_ARG;
+  if (n_tokens > 0 && (slot_mapping == nullptr || x == nullptr || stats == nullptr)) return TQ_ERR_INVALID_ARG;
+  if (stats != nullptr && (reinterpret_cast<uintptr_t>(stats) & 7u) != 0) return TQ_ERR_INVALID_ARG;
+  tq::QuantizeArgs ka{}, va{};
+  const tq_status st = append_args(book, which == 0 ? x : nullptr, which == 1 ? x : nullptr, dtype, n_tokens,
+                                   n_kv_heads, slot_mapping, cache, &ka, &va);
+  if (st != TQ_OK || n_tokens == 0) return st;
+  return tq::launch_monitor(which == 0 ? ka : va, dtype == TQ_BF16, stats, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? TQ_OK
+             : TQ_ERR_CUDA;
 }
 
 }  // extern "C"
@@ -489,6 +509,7 @@ tq_status decode_args(const tq_codebook* book, int stages, const void* q, tq_dty
     a->k_rnorm = book->cfg.qjl_m > 0 ? cache->k_rnorm : nullptr;
     a->v_codes = static_cast<const uint8_t*>(cache->v_codes);
     a->v_norm = cache->v_norm;
+    a->norm16 = book->norm16;
     a->num_blocks = cache->num_blocks;
   }
   a->block_size = book->cfg.block_size;
@@ -511,6 +532,8 @@ tq_status decode_args(const tq_codebook* book, int stages, const void* q, tq_dty
   a->ws_bk = bk == 0 ? nullptr : reinterpret_cast<uint8_t*>(ws + l.bk);
   a->ws_ticket = reinterpret_cast<int*>(ws + l.ticket);
   a->ws_seg = reinterpret_cast<tq::SegInfo*>(ws + l.seg);
+  a->part_cap = static_cast<long long>((l.bk - l.part) / (tq::kPartStride * sizeof(float)));
+  a->debug_withhold = book->debug_withhold;
   a->bk_stride = static_cast<int>(bk);
   a->R = book->d_R;
   a->Rt = book->d_Rt;
@@ -519,9 +542,10 @@ tq_status decode_args(const tq_codebook* book, int stages, const void* q, tq_dty
   a->tables = book->d_tables;
   a->error = book->d_error;
   a->num_sms = book->num_sms;
-  // the tensor-core partials kernel merges a group's segments and writes `out`
-  // itself when the call goes all the way to the output
-  a->merge_in_partials = (stages & kPartials) && out != nullptr && tq::tc_decode_supported(*a, book->walsh_ok);
+  // with an output, the tensor-core path either merges in the partials kernel
+  // (few groups per CTA) or in a dependent merge launch (see launch_partials_and_merge)
+  a->merge_in_partials = (stages & kPartials) && out != nullptr && tq::tc_decode_supported(*a, book->walsh_ok) &&
+                         tq::tc_merge_in_partials(*a);
   return TQ_OK;
 }
 
@@ -555,8 +579,11 @@ namespace {
 cudaError_t launch_partials_and_merge(const tq_codebook* book, const tq::DecodeArgs& a, cudaStream_t s,
                                       bool early = false) {
   if (a.merge_in_partials) return tq::launch_decode_partials_tc(a, s, early);
-  const bool tc = tq::tc_decode_supported(a, book->walsh_ok);
-  const cudaError_t err = tc ? tq::launch_decode_partials_tc(a, s, early) : tq::launch_decode_partials(a, s);
+  if (tq::tc_decode_supported(a, book->walsh_ok)) {
+    const cudaError_t err = tq::launch_decode_partials_tc(a, s, early);
+    return err == cudaSuccess ? tq::launch_merge_groups_tc(a, s) : err;
+  }
+  const cudaError_t err = tq::launch_decode_partials(a, s);
   return err == cudaSuccess ? tq::launch_decode_finish(a, s) : err;
 }
 
@@ -786,6 +813,38 @@ tq_status tq_decode_kernel_kind(const tq_codebook* book, int n_q_heads, int n_kv
   a.k_qjl = book->cfg.qjl_m > 0 ? reinterpret_cast<const uint8_t*>(1) : nullptr;
   a.ws_bk = bk_bytes(book) > 0 ? reinterpret_cast<uint8_t*>(1) : nullptr;   // null checks only
   *tensor_cores = tq::tc_decode_supported(a, book->walsh_ok) ? 1 : 0;
+  return TQ_OK;
+}
+
+tq_status tq_decode_plan(const tq_codebook* book, int batch, int n_q_heads, int n_kv_heads, int max_context,
+                         tq_decode_plan_info* info) {
+  if (!valid_device_handle(book) || info == nullptr || batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 ||
+      n_q_heads % n_kv_heads != 0 || max_context < 0) {
+    return TQ_ERR_INVALID_ARG;
+  }
+  tq::DecodeArgs a{};
+  a.batch = batch;
+  a.n_q = n_q_heads;
+  a.n_kv = n_kv_heads;
+  a.group = n_q_heads / n_kv_heads;
+  a.block_size = book->cfg.block_size;
+  a.k_bits = book->k_mse_bits;
+  a.v_bits = book->v_bits;
+  a.max_context = max_context;
+  a.num_sms = book->num_sms;
+  a.k_qjl = book->cfg.qjl_m > 0 ? reinterpret_cast<const uint8_t*>(1) : nullptr;
+  a.ws_bk = bk_bytes(book) > 0 ? reinterpret_cast<uint8_t*>(1) : nullptr;   // null checks only
+  const bool tc = tq::tc_decode_supported(a, book->walsh_ok);
+  info->tensor_cores = tc ? 1 : 0;
+  info->merge_in_partials = tc && tq::tc_merge_in_partials(a) ? 1 : 0;
+  info->partials_ctas = tc ? tq::tc_grid(a) : 0;
+  info->chunk_tokens = tc ? tq::tc_chunk(a) : tq::kChunk;
+  return TQ_OK;
+}
+
+tq_status tq_debug_withhold_commit(tq_codebook* book, int enable) {
+  if (!valid_device_handle(book)) return TQ_ERR_INVALID_ARG;
+  book->debug_withhold = enable ? 1 : 0;
   return TQ_OK;
 }
 

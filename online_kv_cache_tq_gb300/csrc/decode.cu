@@ -104,8 +104,8 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(DecodeArgs a) {
       kw[p] = p < a.k_bits ? reinterpret_cast<const uint4*>(a.k_codes + row * kbytes)[p] : make_uint4(0, 0, 0, 0);
     }
     const uint4 sw = qjl ? reinterpret_cast<const uint4*>(a.k_qjl + row * 16)[0] : make_uint4(0, 0, 0, 0);
-    const float nk = a.k_norm[row];
-    const float gk = qjl ? a.k_rnorm[row] : 0.f;
+    const float nk = load_norm(a.k_norm, row, a.norm16);
+    const float gk = qjl ? load_norm(a.k_rnorm, row, a.norm16) : 0.f;
     float mse[G], qj[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) { mse[g] = 0.f; qj[g] = 0.f; }
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(DecodeArgs a) {
     const int off = static_cast<int>(row - bh * a.block_size);
     const unsigned* words = reinterpret_cast<const unsigned*>(a.v_codes);
     const long long base = (bh * a.v_bits * 128) * (a.block_size / 32) + off / 32;
-    const float nv = a.v_norm[row];
+    const float nv = load_norm(a.v_norm, row, a.norm16);
     float val[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {

@@ -52,7 +52,6 @@ namespace tq {
 namespace {
 
 constexpr int kTile = 128;                  // tokens per tile = tensor-memory lanes
-constexpr int kTiles = kChunk / kTile;      // tiles per chunk
 constexpr int kBuilders = 256;              // warps 0-7: two threads per tensor-memory lane
 constexpr int kThreads = kBuilders + 32;     // warp 8: copies and MMA issue
 constexpr int kVPieces = 3;                 // e4m3 pieces of a softmax weight
@@ -306,14 +305,16 @@ struct TcLayout {
   int v_slots;              // value slots of kValueSlot columns (2 to kMaxValueSlots)
   int col_s, col_o, cols, tmem;
   int kbytes, vblock;       // key code bytes per token; value code bytes per (block, head)
+  int chunk;                // tokens per work item (512, or 256 when 512 would not fit two CTAs per SM)
   int off_bmse, off_bqjl, off_bv, off_s0, off_s1, off_sacc, off_kc, off_kq, off_kn, off_kr, off_vn, off_vc, smem_bytes;
 };
 
 constexpr int kValueSlot = 64;              // columns of one value slot (two sign planes)
 constexpr int kMaxValueSlots = 4;
 
-TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size) {
+TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size, int chunk) {
   TcLayout l{};
+  l.chunk = chunk;
   l.pk = 1 << (k_bits - 1);
   l.pq = qjl ? 1 : 0;
   l.pv = 1 << (v_bits - 1);
@@ -343,16 +344,16 @@ TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size) 
   int o = 0;
   l.off_bmse = o; o += l.n1 * l.pk * 128;
   l.off_bqjl = o; o += l.n2 * 128;
-  l.off_bv = o; o += kTiles * l.no * 128;
-  l.off_s0 = o; o += group * kChunk * 4;
+  l.off_bv = o; o += (chunk / kTile) * l.no * 128;
+  l.off_s0 = o; o += group * chunk * 4;
   l.off_s1 = o; o += group * kTile * 4;
   l.off_sacc = o; o += group * kTile * 4;
-  l.off_kc = o; o += kChunk * l.kbytes;
-  l.off_kq = o; o += kChunk * 16;
-  l.off_kn = o; o += kChunk * 4;
-  l.off_kr = o; o += kChunk * 4;
-  l.off_vn = o; o += kChunk * 4;
-  l.off_vc = o; o += (kChunk / block_size) * l.vblock;
+  l.off_kc = o; o += chunk * l.kbytes;
+  l.off_kq = o; o += chunk * 16;
+  l.off_kn = o; o += chunk * 4;
+  l.off_kr = o; o += chunk * 4;
+  l.off_vn = o; o += chunk * 4;
+  l.off_vc = o; o += (chunk / block_size) * l.vblock;
   l.smem_bytes = o + 1024;
   // more than half of tensor memory: keep a second CTA off the SM instead of
   // letting it wait in the allocator
@@ -376,59 +377,63 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
 // h), divide by the softmax sum and back-rotate into out (seo-farm page §2:
 // out = R^T o_rot).  Called by every builder thread (lane, half); half h
 // merges the heads it owns, then each half sums 64 of the 128 terms of every
-// head's back-rotation.  Not inlined: it runs about twice per CTA, and its
-// loads in flight must not take registers from the per-tile loop.
+// head's back-rotation.  Latency-bound: the loads of up to eight segments, and
+// all 64 loads of R a thread needs, are in flight at once.  Not inlined: it
+// runs about twice per CTA, and those loads must not take registers from the
+// per-tile loop.
 template <int G>
 __device__ __noinline__ void merge_segments(const float* ws_part, const float* R, float* out, int ent0,
                                             int n_seg, int qbase, float* orot, float* s1, int half, int lane) {
   constexpr int HG = half_heads(G);
+  constexpr int kBatch = 8;
+  float w[64];                                  // R[64 half + i][lane], loaded while the segments merge
+  const float* rp = R + (64 * half) * kDim + lane;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) w[i] = __ldg(rp + i * kDim);
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     if (h / HG != half) continue;
     float m = -INFINITY, l = 0.f, acc = 0.f;
-    for (int sg0 = 0; sg0 < n_seg; sg0 += 4) {
-      // (four segments' loads in flight at once)
-      float pm[4], pl[4], pa[4];
+    for (int sg0 = 0; sg0 < n_seg; sg0 += kBatch) {
+      float pm[kBatch], pl[kBatch], pa[kBatch];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float* part = ws_part + (ent0 + static_cast<long long>(sg0 + k) * G + h) * kPartStride;
+      for (int k = 0; k < kBatch; ++k) {
+        const float* part = ws_part + (static_cast<long long>(ent0) + static_cast<long long>(sg0 + k) * G + h) *
+                                          kPartStride;
         const bool in = sg0 + k < n_seg;
         pm[k] = in ? __ldcg(part) : -INFINITY;
         pl[k] = in ? __ldcg(part + 1) : 0.f;
         pa[k] = in ? __ldcg(part + 4 + lane) : 0.f;
       }
+      float mn = m;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float mn = fmaxf(m, pm[k]);
-        const float so = m == -INFINITY ? 0.f : __expf(m - mn);
+      for (int k = 0; k < kBatch; ++k) mn = fmaxf(mn, pm[k]);
+      if (mn == -INFINITY) continue;
+      const float so = m == -INFINITY ? 0.f : __expf(m - mn);
+      l *= so;
+      acc *= so;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
         const float sn = pm[k] == -INFINITY ? 0.f : __expf(pm[k] - mn);
-        l = fmaf(l, so, pl[k] * sn);
-        acc = fmaf(acc, so, pa[k] * sn);
-        m = mn;
+        l = fmaf(pl[k], sn, l);
+        acc = fmaf(pa[k], sn, acc);
       }
+      m = mn;
     }
     orot[h * kTile + lane] = l > 0.f ? acc / l : 0.f;
   }
   builder_sync();
-  // out[h][o] = sum_i R[i][o] o_rot[h][i]: thread (o = lane, half) sums i in
-  // [64 half, 64 half + 64), 32 loads of R in flight at a time
+  // out[h][o] = sum_i R[i][o] o_rot[h][i]: thread (o = lane, half) sums i in [64 half, 64 half + 64)
   float r[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) r[h] = 0.f;
-  const float* rp = R + (64 * half) * kDim + lane;
-#pragma unroll 1
-  for (int i0 = 0; i0 < 64; i0 += 32) {
-    float w[32];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) w[k] = __ldg(rp + (i0 + k) * kDim);
+  for (int k = 0; k < 64; k += 4)
 #pragma unroll
-    for (int k = 0; k < 32; k += 4)
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float4 v = *reinterpret_cast<const float4*>(orot + h * kTile + 64 * half + i0 + k);
-        r[h] = fmaf(w[k], v.x, fmaf(w[k + 1], v.y, fmaf(w[k + 2], v.z, fmaf(w[k + 3], v.w, r[h]))));
-      }
-  }
+    for (int h = 0; h < G; ++h) {
+      const float4 v = *reinterpret_cast<const float4*>(orot + h * kTile + 64 * half + k);
+      r[h] = fmaf(w[k], v.x, fmaf(w[k + 1], v.y, fmaf(w[k + 2], v.z, fmaf(w[k + 3], v.w, r[h]))));
+    }
   if (half == 1)
 #pragma unroll
     for (int h = 0; h < G; ++h) s1[h * kTile + lane] = r[h];
@@ -459,11 +464,11 @@ struct Item {
 // a sequence's context length is read when the walk enters the sequence, and
 // sequences without tokens are stepped over.
 struct ItemCursor {
-  int it, last, b, kvh, chunk, ctx, nch;
-  __device__ ItemCursor(const DecodeArgs& a, int first, int last_, int b0, int kvh0, int chunk0)
-      : it(first), last(last_), b(b0), kvh(kvh0), chunk(chunk0) {
+  int it, last, b, kvh, chunk, ctx, nch, csz;
+  __device__ ItemCursor(const DecodeArgs& a, int csz_, int first, int last_, int b0, int kvh0, int chunk0)
+      : it(first), last(last_), b(b0), kvh(kvh0), chunk(chunk0), csz(csz_) {
     ctx = first < last ? context_of(a, b) : 0;
-    nch = (ctx + kChunk - 1) / kChunk;
+    nch = (ctx + csz - 1) / csz;
   }
   __device__ __forceinline__ void advance(const DecodeArgs& a) {
     ++it;
@@ -479,7 +484,7 @@ struct ItemCursor {
       }
       ++b;
       ctx = context_of(a, b);
-      nch = (ctx + kChunk - 1) / kChunk;
+      nch = (ctx + csz - 1) / csz;
     } while (nch == 0);
   }
   // the next item, if any
@@ -489,8 +494,8 @@ struct ItemCursor {
     x.kvh = kvh;
     x.chunk = chunk;
     x.ctx = ctx;
-    x.start = chunk * kChunk;
-    x.n_local = min(kChunk, ctx - x.start);
+    x.start = chunk * csz;
+    x.n_local = min(csz, ctx - x.start);
     x.n_tiles = (x.n_local + kTile - 1) / kTile;
     x.n_blk = (x.n_local + (1 << bs_shift) - 1) >> bs_shift;
     x.group = b * a.n_kv + kvh;
@@ -505,7 +510,7 @@ struct ItemCursor {
 // time, or 0, 0, -1 to take them from the arguments.  Two CTAs per SM cap a
 // thread at 96 registers (the register file is split over four sub-partitions
 // of 16384, and one of them holds five of the two CTAs' eighteen warps).
-template <int G, int KB, int VB, int QJ>
+template <int G, int KB, int VB, int QJ, int CH>
 __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a, TcLayout L) {
   constexpr int N1 = score_cols(G), NO = value_cols(G);
   const int t = threadIdx.x;
@@ -520,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
     const int b = b0 + t;
     const int ctx = b < a.batch ? context_of(a, b) : -1;
-    const int ch = ctx > 0 ? (ctx + kChunk - 1) / kChunk : 0;
+    const int ch = ctx > 0 ? (ctx + CH - 1) / CH : 0;
     if (a.merge_in_partials && blockIdx.x == 0) {
       // a sequence without context has a zero output, which no item writes
       if (t == 0) n_empty_s = 0;
@@ -562,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
       const int b = b0 + t;
       const int ctx = b < a.batch ? context_of(a, b) : 0;
-      const int ch = (ctx + kChunk - 1) / kChunk;
+      const int ch = (ctx + CH - 1) / CH;
       int excl;
       const int tot = cta_scan<kThreads>(ch, &excl, scan_s);
       locate(b, ch, base + excl);
@@ -571,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   }
   __syncthreads();
 
-  const int bs = a.block_size;                        // a power of two that divides kChunk
+  const int bs = a.block_size;                        // a power of two that divides CH
   const int bs_shift = 31 - __clz(bs);
 
   const int k_bits = KB > 0 ? KB : a.k_bits;
@@ -590,14 +595,18 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   uint8_t* b_mse = smem + L.off_bmse;
   uint8_t* b_qjl = smem + L.off_bqjl;
   uint8_t* b_v = smem + L.off_bv;
-  float* s0 = reinterpret_cast<float*>(smem + L.off_s0);           // [G][kChunk] scores, then weights
+  float* s0 = reinterpret_cast<float*>(smem + L.off_s0);           // [G][CH] scores
   float* s1 = reinterpret_cast<float*>(smem + L.off_s1);           // [G][kTile]: output halves
   float* seg_acc = reinterpret_cast<float*>(smem + L.off_sacc);    // [G][kTile]: the segment's running acc
-  uint8_t* kc_s = smem + L.off_kc;                                  // [kChunk][kbytes]
-  uint8_t* kq_s = smem + L.off_kq;                                  // [kChunk][16]
-  float* kn_s = reinterpret_cast<float*>(smem + L.off_kn);
-  float* kr_s = reinterpret_cast<float*>(smem + L.off_kr);
-  float* vn_s = reinterpret_cast<float*>(smem + L.off_vn);
+  uint8_t* kc_s = smem + L.off_kc;                                  // [CH][kbytes]
+  uint8_t* kq_s = smem + L.off_kq;                                  // [CH][16]
+  uint8_t* kn_s = smem + L.off_kn;                                  // [CH] norms, float32 or float16
+  uint8_t* kr_s = smem + L.off_kr;
+  uint8_t* vn_s = smem + L.off_vn;
+  const int nb = a.norm16 ? 2 : 4;                                  // bytes of a stored norm
+  auto norm_at = [&](const uint8_t* f, int i) {
+    return a.norm16 ? __half2float(reinterpret_cast<const __half*>(f)[i]) : reinterpret_cast<const float*>(f)[i];
+  };
   uint32_t* vc_s = reinterpret_cast<uint32_t*>(smem + L.off_vc);   // [blk][plane][dim][bs/32]
   // kin / vin: an item's key / value fields landed (one phase per item);
   // kfree / vfree: the builders are done with the key / value fields of an
@@ -610,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   __shared__ int abort_s;
   __shared__ float red_s[(kBuilders / 32) * (2 * half_heads(G) + 1)];   // warp totals of up to 2 HG + 1 values
   __shared__ float stat_s[2][G];                // chunk max, chunk sum per head
-  __shared__ int blk_ok_s[2][kChunk / 32];      // per item parity: physical block of each block slot is valid
+  __shared__ int blk_ok_s[2][CH / 32];          // per item parity: physical block of each block slot is valid
   __shared__ float sv_s;                        // piece scale of the softmax weights
   __shared__ float wsum_s[G];                   // sum over the chunk of e n_v per head
   __shared__ float cst_s[4][G];                 // per head: 1/sigma_mse, 1/sigma_qjl, ones_mse, ones_qjl
@@ -680,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           if (!valid) atomicCAS(a.error, 0, kErrBlock);
         }
         rows = min(bs, (x.n_local - ln * bs + 31) / 32 * 32);
-        if (valid) bytes = keys ? rows * (kbytes + 4 + (qjl ? 16 + 4 : 0)) : rows * 4 + vblock;
+        if (valid) bytes = keys ? rows * (kbytes + nb + (qjl ? 16 + nb : 0)) : rows * nb + vblock;
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, off);
@@ -697,11 +706,11 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           ptx::bulk_load(kc_s + tl0 * kbytes, a.k_codes + r0 * kbytes, rows * kbytes, &kin);
           if (qjl) {
             ptx::bulk_load(kq_s + tl0 * 16, a.k_qjl + r0 * 16, rows * 16, &kin);
-            ptx::bulk_load(kr_s + tl0, a.k_rnorm + r0, rows * 4, &kin);
+            ptx::bulk_load(kr_s + tl0 * nb, static_cast<const uint8_t*>(a.k_rnorm) + r0 * nb, rows * nb, &kin);
           }
-          ptx::bulk_load(kn_s + tl0, a.k_norm + r0, rows * 4, &kin);
+          ptx::bulk_load(kn_s + tl0 * nb, static_cast<const uint8_t*>(a.k_norm) + r0 * nb, rows * nb, &kin);
         } else {
-          ptx::bulk_load(vn_s + tl0, a.v_norm + r0, rows * 4, &vin);
+          ptx::bulk_load(vn_s + tl0 * nb, static_cast<const uint8_t*>(a.v_norm) + r0 * nb, rows * nb, &vin);
           ptx::bulk_load(vc_s + ln * (vblock / 4), a.v_codes + (phys * a.n_kv + x.kvh) * vblock, vblock,
                          &vin);
         }
@@ -715,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     const uint64_t desc_v = ptx::desc_k_sw128(ptx::smem_u32(b_v));
     const uint32_t mse_plane_step = (L.n1 * 128) >> 4, v_tile_step = (L.no * 128) >> 4;
     const uint32_t d_mse = tmem + L.col_s;
-    ItemCursor cursor(a, first, last, split_s[0], split_s[1], split_s[2]);
+    ItemCursor cursor(a, CH, first, last, split_s[0], split_s[1], split_s[2]);
     int seq = 0, ktile = 0;
     int vslot = 0, vwrap = 0;                   // value unit counter as (slot, times round the slots)
     Item cur, nxt;
@@ -746,7 +755,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               ptx::mma_e4m3_tmem_a(d_mse + N1, a_col + 8 * kk, desc_qjl + 2 * kk, idesc_s, kk != 0);
-          ptx::mma_commit(&kdone);
+          // (a test of the bounded waits withholds the first commit of CTA 0)
+          if (!(a.debug_withhold && blockIdx.x == 0 && ktile == 0)) ptx::mma_commit(&kdone);
         }
         __syncwarp();
       }
@@ -798,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   } else {
     // =================== builders ===================
     constexpr int HG = half_heads(G), HC = score_half(G);
-    ItemCursor cursor(a, first, last, split_s[0], split_s[1], split_s[2]);
+    ItemCursor cursor(a, CH, first, last, split_s[0], split_s[1], split_s[2]);
     int seq = 0, ktile = 0, cur_group = -1;
     int vslot = 0, vwrap = 0;                     // value unit counter as (slot, times round the slots)
     const int wpd_shift = bs_shift - 5;         // log2 of the words per coordinate in a block
@@ -818,14 +828,6 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     }
 
     if (t == 0) n_pend_s = 0;
-    // the merges this CTA owes, by every builder (uniform: the count is read after a barrier)
-    auto run_pending = [&]() {
-      const int np = n_pend_s;
-      for (int p = 0; p < np; ++p) {
-        const int4 e = pend_s[p];
-        merge_segments<G>(a.ws_part, a.R, a.out, e.x, e.y, e.z, s0, s1, half, lane);
-      }
-    };
 
     Item x;
     bool have = cursor.next(a, bs_shift, x);
@@ -905,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
               }
             }
           }
-          const float kn = kn_s[tl], kr = kr_s[tl];     // (tl < kChunk: in bounds; selected below)
+          const float kn = norm_at(kn_s, tl), kr = norm_at(kr_s, tl);   // (tl < CH: in bounds; selected below)
           const float nk = valid ? kn : 0.f;
           const float gk = valid && qjl ? kr * a.qjl_coef : 0.f;
 #pragma unroll
@@ -915,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             const float mse = fmaf(am[j], cst_r[0][j], -cst_r[2][j]);
             const float qv = qjl ? fmaf(aq[j], cst_r[1][j], -cst_r[3][j]) : 0.f;
             const float sc = valid ? a.scale * fmaf(nk, mse, gk * qv) : -INFINITY;
-            s0[h * kChunk + tl] = sc;
+            s0[h * CH + tl] = sc;
             mx[j] = fmaxf(mx[j], sc);
           }
         }
@@ -940,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         if (k_slots == 1 && i > 0) take_scores(i - 1, ktile - 1);
         if (!ok) break;
         const int tl = i * kTile + lane;
-        // loaded for every token slot of the tile (tl < kChunk, inside the
+        // loaded for every token slot of the tile (tl < CH, inside the
         // copied fields): a slot past the context or in a skipped block holds
         // stale but finite operand bytes, and its score is set to -inf
         uint32_t bw[4][2] = {};
@@ -980,7 +982,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
 
       // ---- softmax max over the chunk; B_V pieces of exp(s - m) n_v ----
       for (int i = t; i < x.n_tiles * kTile; i += kBuilders)
-        mx[HG] = fmaxf(mx[HG], i < x.n_local && blk_ok[i >> bs_shift] ? vn_s[i] : 0.f);
+        mx[HG] = fmaxf(mx[HG], i < x.n_local && blk_ok[i >> bs_shift] ? norm_at(vn_s, i) : 0.f);
       float lw[2 * HG];                           // owned heads: sum of e, then sum of e n_v
 #pragma unroll
       for (int j = 0; j < 2 * HG; ++j) lw[j] = 0.f;
@@ -1010,7 +1012,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             for (int tile = 0; tile < x.n_tiles; ++tile) {
               const int tl = tile * kTile + lane;
               const bool valid = tl < x.n_local && blk_ok[tl >> bs_shift];
-              const float vn = vn_s[tl];                // (tl < kChunk: in bounds; selected below)
+              const float vn = norm_at(vn_s, tl);       // (tl < CH: in bounds; selected below)
               const float nv = valid ? vn : 0.f;
               uint8_t* dst = b_v + tile * L.no * 128;
               float e[HG];
@@ -1020,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
                 e[j] = 0.f;
                 if (h >= G) continue;
                 // (a select, not a branch: the exponent of an invalid slot may be nan)
-                const float ex = __expf(s0[h * kChunk + tl] - mx[j]);
+                const float ex = __expf(s0[h * CH + tl] - mx[j]);
                 e[j] = valid && mx[j] != -INFINITY ? ex : 0.f;
                 lw[j] += e[j];
                 lw[HG + j] = fmaf(e[j], nv, lw[HG + j]);
@@ -1182,16 +1184,12 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         if (f_cta == static_cast<int>(blockIdx.x) && t < G)
           a.ws_seg[qbase + t] = SegInfo{(x.group + f_cta) * G + t, n_seg, G, 0};
         if (a.merge_in_partials) {
-          // The CTA that ends a group's last segment owes its merge; it runs
+          // The CTA that ends a group's last segment owes its merge.  It runs
           // the merges it owes after its last item (a merge here would stall
-          // the copy and MMA pipeline), or now when the list is full.
-          // (the count is read before the barrier: thread 0 changes it only after it)
-          const bool full = n_pend_s == kMaxPending;
+          // the copy and MMA pipeline): listed in shared memory, or, when the
+          // list is full, marked in the group's ticket word (-1 - CTA) and
+          // found again by walking the run once more.
           builder_sync();                         // every builder's partial stores precede the ticket
-          if (full) {
-            run_pending();
-            if (t == 0) n_pend_s = 0;
-          }
           if (t == 0) {
             bool owe = true;                      // (a group inside this run has no other contributor)
             if (n_seg > 1) {
@@ -1199,7 +1197,14 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
               owe = atomicAdd(a.ws_ticket + x.group, 1) == n_seg - 1;
               if (owe) __threadfence();           // the other CTAs' partials are visible from here on
             }
-            if (owe) pend_s[n_pend_s++] = make_int4((x.group + f_cta) * G, n_seg, qbase, 0);
+            if (owe) {
+              if (n_pend_s < kMaxPending) {
+                pend_s[n_pend_s++] = make_int4((x.group + f_cta) * G, n_seg, qbase, 0);
+              } else {
+                a.ws_ticket[x.group] = -1 - static_cast<int>(blockIdx.x);
+                n_pend_s = kMaxPending + 1;       // (overflow)
+              }
+            }
           }
         }
       }
@@ -1208,8 +1213,27 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       ++seq;
     }
     if (ok && a.merge_in_partials) {
+      // the merges this CTA owes, by every builder (uniform: read after a barrier)
       builder_sync();
-      run_pending();
+      const int np = n_pend_s;
+      for (int p = 0; p < min(np, kMaxPending); ++p) {
+        const int4 e = pend_s[p];
+        merge_segments<G>(a.ws_part, a.R, a.out, e.x, e.y, e.z, s0, s1, half, lane);
+      }
+      if (np > kMaxPending) {
+        // the overflow: the run's groups once more, those whose ticket word names this CTA
+        ItemCursor again(a, CH, first, last, split_s[0], split_s[1], split_s[2]);
+        Item y;
+        int prev = -1;
+        while (again.next(a, bs_shift, y)) {
+          if (y.group == prev) continue;
+          prev = y.group;
+          if (__ldcg(a.ws_ticket + y.group) != -1 - static_cast<int>(blockIdx.x)) continue;
+          const int f_cta = y.first_cta(per_cta);
+          merge_segments<G>(a.ws_part, a.R, a.out, (y.group + f_cta) * G, y.last_cta(per_cta) - f_cta + 1,
+                            y.b * a.n_q + y.kvh * G, s0, s1, half, lane);
+        }
+      }
     }
   }
 
@@ -1235,33 +1259,54 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   }
 }
 
+// Chunk length of the tensor-core kernel for this shape: 512 tokens, or 256
+// when a 512-token layout would not leave room for two CTAs per SM and the
+// blocks divide 256 (the partials are per segment, so the chunk length is the
+// kernel's own choice).
+int tc_chunk(const DecodeArgs& a) {
+  const TcLayout l = tc_layout(a.group, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size, 512);
+  const bool two = l.tmem <= 256 && l.smem_bytes <= 108 * 1024;
+  return !two && 256 % a.block_size == 0 ? 256 : 512;
+}
+
 bool tc_decode_supported(const DecodeArgs& a, bool walsh_ok) {
-  if (!walsh_ok || a.ws_bk == nullptr || a.block_size % 32 != 0 || kChunk % a.block_size != 0) return false;
+  if (!walsh_ok || a.ws_bk == nullptr || a.block_size % 32 != 0 || 512 % a.block_size != 0) return false;
   if (a.k_bits < 1 || a.k_bits > 4 || a.v_bits < 1 || a.v_bits > 4) return false;
   if (a.group != 1 && a.group != 2 && a.group != 4 && a.group != 8) return false;
-  const TcLayout l = tc_layout(a.group, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size);
+  const TcLayout l = tc_layout(a.group, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size, tc_chunk(a));
   return l.cols <= 512 && l.smem_bytes <= 200 * 1024;
+}
+
+// CTAs of the persistent tensor-core grid: two per SM when a CTA's tensor
+// memory and shared memory leave room for a second, else one; no more than
+// the batch could have chunks, and at least one (with no chunk at all it still
+// writes the zero outputs).
+int tc_grid(const DecodeArgs& a) {
+  const int chunk = tc_chunk(a);
+  const TcLayout l = tc_layout(a.group, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size, chunk);
+  const int per_sm = (l.tmem <= 256 && l.smem_bytes <= 108 * 1024) ? 2 : 1;
+  const int max_items = (a.max_context + chunk - 1) / chunk;
+  const long long bound = static_cast<long long>(a.batch) * a.n_kv * max_items;
+  const long long slots = static_cast<long long>(per_sm) * (a.num_sms > 0 ? a.num_sms : 148);
+  return static_cast<int>(bound < 1 ? 1 : bound < slots ? bound : slots);
 }
 
 template <int G>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, bool early) {
-  const TcLayout l = tc_layout(G, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size);
+  const int chunk = tc_chunk(a);
+  const TcLayout l = tc_layout(G, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size, chunk);
   // 3-bit keys (2 MSE bits + the QJL bit) with 3-bit values have their own
   // build with the widths folded in; other widths are read at run time
-  const bool fixed = a.k_bits == 2 && a.v_bits == 3 && a.k_qjl != nullptr && l.k_slots == 2;
-  auto kernel = fixed ? attention_tc_kernel<G, 2, 3, 1> : attention_tc_kernel<G, 0, 0, -1>;
+  const bool fixed = a.k_bits == 2 && a.v_bits == 3 && a.k_qjl != nullptr && l.k_slots == 2 && chunk == 512;
+  auto kernel = fixed ? attention_tc_kernel<G, 2, 3, 1, 512>
+                      : chunk == 512 ? attention_tc_kernel<G, 0, 0, -1, 512> : attention_tc_kernel<G, 0, 0, -1, 256>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem_bytes);
   if (err != cudaSuccess) return err;
-  // a persistent grid: two CTAs per SM (one when the tensor memory or shared
-  // memory of a CTA leaves room for one); the kernel splits the real chunks
-  // of the batch into equal runs, one per CTA, so that consecutive items share
-  // the query operands and the next item's fields load while the current one
-  // computes.  No more CTAs than the batch could have chunks.
-  const long long bound = static_cast<long long>(a.batch) * a.n_kv * a.max_chunks;
-  const int per_sm = (l.tmem <= 256 && l.smem_bytes <= 113 * 1024) ? 2 : 1;
-  const long long slots = static_cast<long long>(per_sm) * (a.num_sms > 0 ? a.num_sms : 148);
-  // (at least one CTA: with no chunk at all it still writes the zero outputs)
-  const int n_ctas = static_cast<int>(bound < 1 ? 1 : bound < slots ? bound : slots);
+  // a persistent grid (tc_grid); the kernel splits the real chunks of the
+  // batch into equal runs, one per CTA, so that consecutive items share the
+  // query operands and the next item's fields load while the current one
+  // computes
+  const int n_ctas = tc_grid(a);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);
   cfg.blockDim = dim3(kThreads);
@@ -1273,6 +1318,68 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, bool early) {
   cfg.attrs = attr;
   cfg.numAttrs = early ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, a, l);
+}
+
+// The merge as its own launch, one 256-thread CTA per (sequence, KV head)
+// group: merge_segments over the entries the partials kernel listed for the
+// group (slot group + CTA, G heads side by side), so that R is loaded once
+// per G heads.  A programmatic dependent of the partials kernel: it waits for
+// that grid before it reads any entry.
+template <int G>
+__global__ void __launch_bounds__(kBuilders) merge_groups_kernel(DecodeArgs a) {
+  __shared__ __align__(16) float orot_s[G * kTile];
+  __shared__ __align__(16) float half_s[G * kTile];
+  const int g = blockIdx.x;
+  const int b = g / a.n_kv, kvh = g - b * a.n_kv;
+  const int qbase = b * a.n_q + kvh * G;
+  const int ctx = context_of(a, b);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (ctx == 0) {
+    for (int i = threadIdx.x; i < G * kDim; i += kBuilders) a.out[static_cast<long long>(qbase) * kDim + i] = 0.f;
+    return;
+  }
+  const SegInfo seg = a.ws_seg[qbase];            // head 0: entries base + s G, the others follow it
+  // (a partials CTA that stopped early leaves a stale record: check it)
+  if (seg.count < 1 || seg.base < 0 || seg.stride != G ||
+      static_cast<long long>(seg.base) + static_cast<long long>(seg.count) * G > a.part_cap) {
+    if (threadIdx.x == 0) atomicCAS(a.error, 0, kErrPartials);
+    for (int i = threadIdx.x; i < G * kDim; i += kBuilders) a.out[static_cast<long long>(qbase) * kDim + i] = 0.f;
+    return;
+  }
+  merge_segments<G>(a.ws_part, a.R, a.out, seg.base, seg.count, qbase, orot_s, half_s, (threadIdx.x >> 7) & 1,
+                    threadIdx.x & 127);
+}
+
+template <int G>
+cudaError_t launch_merge_g(const DecodeArgs& a, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.batch * a.n_kv);
+  cfg.blockDim = dim3(kBuilders);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_groups_kernel<G>, a);
+}
+
+cudaError_t launch_merge_groups_tc(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.batch <= 0) return cudaSuccess;
+  switch (a.group) {
+    case 1: return launch_merge_g<1>(a, stream);
+    case 2: return launch_merge_g<2>(a, stream);
+    case 4: return launch_merge_g<4>(a, stream);
+    case 8: return launch_merge_g<8>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+bool tc_merge_in_partials(const DecodeArgs& a) {
+  // a CTA owes the merges of the groups that end in its run: with more groups
+  // than CTAs (short, ragged contexts) some runs hold many, and the CTAs that
+  // owe most set the launch's end; a merge launch spreads them over the GPU
+  return static_cast<long long>(a.batch) * a.n_kv <= tc_grid(a);
 }
 
 cudaError_t launch_decode_partials_tc(const DecodeArgs& a, cudaStream_t stream, bool early) {

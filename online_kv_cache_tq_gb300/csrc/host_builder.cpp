@@ -199,6 +199,12 @@ void lloyd_max(int d, int bits, std::vector<double>* levels, std::vector<double>
     }
     if (moved < 1e-13) break;
   }
+  // The coordinate law is even, so the exact codebook is odd-symmetric with a
+  // middle boundary of exactly 0 (a coordinate at 0 then takes the lower level
+  // by the tie rule); the iteration's rounding leaves a ~1e-16 residue there.
+  std::vector<double> sym(count);
+  for (int i = 0; i < count; ++i) sym[i] = 0.5 * (c[i] - c[count - 1 - i]);
+  c = sym;
   for (int i = 0; i + 1 < count; ++i) t[i] = 0.5 * (c[i] + c[i + 1]);
   *levels = c;
   *bounds = t;

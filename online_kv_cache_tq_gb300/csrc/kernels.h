@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "tq_internal.h"
@@ -9,7 +10,7 @@
 namespace tq {
 
 // Error codes a kernel records in the handle's error word.
-enum DeviceError : int { kErrSlot = 1, kErrBlock = 2, kErrContext = 3, kErrTimeout = 4 };
+enum DeviceError : int { kErrSlot = 1, kErrBlock = 2, kErrContext = 3, kErrTimeout = 4, kErrPartials = 5 };
 
 struct QuantizeArgs {
   const void* x;          // [n_tokens][n_kv][128], bf16 or fp32
@@ -23,8 +24,9 @@ struct QuantizeArgs {
   int step_max_blocks;
   uint8_t* codes;         // field base, bits * 16 bytes per item
   uint8_t* qjl;           // field base, 16 bytes per item (null: no QJL)
-  float* norm;
-  float* rnorm;           // null when no QJL
+  void* norm;             // float32, or float16 with norm16
+  void* rnorm;            // null when no QJL
+  bool norm16;
   int num_blocks;
   int block_size;
   int bits;               // MSE bits of this tensor
@@ -34,6 +36,17 @@ struct QuantizeArgs {
   const float* Spt;       // [128][128], Spt[j][k] = S'[k][j]
   int* error;
 };
+
+// Norm fields hold float32, or float16 (rounded to nearest) with norm16.
+__device__ __forceinline__ float load_norm(const void* p, long long i, bool n16) {
+  return n16 ? __half2float(reinterpret_cast<const __half*>(p)[i]) : reinterpret_cast<const float*>(p)[i];
+}
+__device__ __forceinline__ void store_norm(void* p, long long i, float v, bool n16) {
+  if (n16) reinterpret_cast<__half*>(p)[i] = __float2half_rn(v);
+  else reinterpret_cast<float*>(p)[i] = v;
+}
+// The value a norm field will hold for v (what the decoder reconstructs with).
+__device__ __forceinline__ float stored_norm(float v, bool n16) { return n16 ? __half2float(__float2half_rn(v)) : v; }
 
 // Cache slot of token `token` of an append: slot_mapping[token], or for a
 // decode step (one token per sequence, slots == null) the slot of position
@@ -80,10 +93,11 @@ struct DecodeArgs {
   int batch, n_q, n_kv, group;
   const uint8_t* k_codes;
   const uint8_t* k_qjl;     // null: no QJL
-  const float* k_norm;
-  const float* k_rnorm;
+  const void* k_norm;       // float32, or float16 with norm16
+  const void* k_rnorm;
   const uint8_t* v_codes;
-  const float* v_norm;
+  const void* v_norm;
+  bool norm16;
   int num_blocks, block_size;
   int k_bits, v_bits, qjl_m;
   const int32_t* block_table;  // null: identity
@@ -101,6 +115,8 @@ struct DecodeArgs {
   int bk_stride;
   int max_chunks;
   int merge_in_partials;    // the tensor-core kernel merges and writes `out` itself
+  long long part_cap;       // partial entries the workspace holds (merges check records against it)
+  int debug_withhold;       // tests of the bounded waits: CTA 0 withholds its first score commit
   const float* R;           // [128][128] row-major
   const float* Rt;
   const float* Spt;
@@ -142,6 +158,11 @@ __host__ __device__ constexpr long long partial_entries(long long n_vec, int max
 
 cudaError_t launch_decode_prepare(const DecodeArgs& args, bool bf16, cudaStream_t stream);
 
+// Reconstruction-error statistics of appended vectors (monitor.cu): adds
+// sum ||x - x_hat||, sum ||x - x_hat||^2, sum ||x||^2 and the vector count
+// into stats[0..3] (x_hat: the stage-1 reconstruction the cache holds).
+cudaError_t launch_monitor(const QuantizeArgs& args, bool bf16, double* stats, cudaStream_t stream);
+
 // Quantize-append of one new key and value per sequence (ka and va share the
 // shape, at most kSmallQuantize vectors each) and the query preparation of
 // the same decode step, in one launch.
@@ -157,6 +178,13 @@ bool tc_decode_supported(const DecodeArgs& args, bool walsh_ok);
 // append + query preparation; the kernel waits for that grid only before it
 // reads the query operands and the chunk that holds the appended token.
 cudaError_t launch_decode_partials_tc(const DecodeArgs& args, cudaStream_t stream, bool early);
+// Whether the tensor-core kernel should merge in place (few groups per CTA)
+// rather than leave the merge to launch_merge_groups_tc, a programmatic
+// dependent launch with one CTA per (sequence, KV head) group.
+bool tc_merge_in_partials(const DecodeArgs& args);
+int tc_grid(const DecodeArgs& args);   // CTAs of the persistent tensor-core grid
+int tc_chunk(const DecodeArgs& args);  // tokens per work item of the tensor-core kernel
+cudaError_t launch_merge_groups_tc(const DecodeArgs& args, cudaStream_t stream);
 // early: launched as a programmatic dependent of the tensor-core partials
 // kernel (the merge waits for it before reading the partials).
 cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream, bool early = false);

@@ -157,17 +157,19 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QuantizeArgs a,
           }
         }
       }
-      if (row >= 0 && lane == 0) a.norm[row] = n;
+      if (row >= 0 && lane == 0) store_norm(a.norm, row, n, a.norm16);
       if (qjl) {
+        // the residual against the norm as stored (what the decoder reconstructs with)
+        const float ns = stored_norm(n, a.norm16);
         float rs = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float r = yv[i] - n * lev_s[code[i]];
+          const float r = yv[i] - ns * lev_s[code[i]];
           x_s[v * kDim + lane + 32 * i] = r;
           rs = fmaf(r, r, rs);
         }
         const float gamma = sqrtf(warp_sum(rs));
-        if (row >= 0 && lane == 0) a.rnorm[row] = gamma;
+        if (row >= 0 && lane == 0) store_norm(a.rnorm, row, gamma, a.norm16);
       }
     }
     if (qjl) {

@@ -382,7 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (dstp >= 0) {
         reinterpret_cast<uint32_t*>(a.qjl + dstp * 16)[g] = word;
         const float* r4 = rs_s + (j & 1) * 4 * kTileRows + row;
-        if (g == 0) a.rnorm[dstp] = sqrtf((r4[0] + r4[kTileRows]) + (r4[2 * kTileRows] + r4[3 * kTileRows]));
+        if (g == 0)
+          store_norm(a.rnorm, dstp, sqrtf((r4[0] + r4[kTileRows]) + (r4[2 * kTileRows] + r4[3 * kTileRows])),
+                     a.norm16);
       }
     };
 
@@ -453,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // y = Y / n against t is taken as Y against n t (a zero vector compares
       // y = 0 against t): one product per boundary instead of one per coordinate
       const float n_eff = n > 0.f ? n : 1.f;
+      const float ns = stored_norm(n, a.norm16);  // the residual is against the norm as stored
       float tn[kLevels - 1];
 #pragma unroll
       for (int i = 0; i < kLevels - 1; ++i) tn[i] = bnd[i] * n_eff;
@@ -473,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float yv = __uint_as_float(yr[j]);
                 const float lv = decide<BITS, QJL, j>(yv, tn, lev, planes);
                 if (QJL) {
-                  r[j] = fmaf(-n, lv, yv);
+                  r[j] = fmaf(-ns, lv, yv);
                   rs = fmaf(r[j], r[j], rs);
                 }
               },
@@ -487,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int p = 0; p < BITS; ++p) planes[p] |= bits[p] ? (1u << j) : 0u;
             if (QJL) {
-              r[j] = fmaf(-n, level_of<BITS>(lev, bits), yv);
+              r[j] = fmaf(-ns, level_of<BITS>(lev, bits), yv);
               rs = fmaf(r[j], r[j], rs);
             }
           }
@@ -538,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int p = 0; p < BITS; ++p) out[p * 4 + g] = planes[p];
       }
-      if (dst >= 0 && g == 0) a.norm[dst] = n;
+      if (dst >= 0 && g == 0) store_norm(a.norm, dst, n, a.norm16);
       if (QJL) {
         // rs_s[it & 1] is read after the next tile's first barrier and written
         // again two tiles later, after every thread has passed that barrier

@@ -74,4 +74,6 @@ struct tq_codebook {
   int num_sms;
   CUtensorMap w_map;  // TMA map of d_rot_tc as [512][128] bf16
   bool walsh_ok;      // both codebooks are exactly odd-symmetric (sign-plane decode usable)
+  bool norm16;        // norms stored as float16 (norm_bits 16)
+  int debug_withhold; // tq_debug_withhold_commit (tests of the bounded waits only)
 };

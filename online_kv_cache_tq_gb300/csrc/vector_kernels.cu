@@ -131,13 +131,14 @@ __device__ __forceinline__ void quantize_vectors(const QuantizeArgs& a, int v0, 
         if (ok[j] && lead && lane == 0) reinterpret_cast<unsigned*>(a.codes + row[j] * (a.bits * 16))[p * 4 + warp] = word;
       }
     }
-    if (ok[j] && threadIdx.x == 0) a.norm[row[j]] = n[j];
+    if (ok[j] && threadIdx.x == 0) store_norm(a.norm, row[j], n[j], a.norm16);
   }
 
   if (a.qjl != nullptr) {
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      const float r = fmaf(-n[j], a.levels[code[j]], yv[j]);
+      // the residual against the norm as stored (what the decoder reconstructs with)
+      const float r = fmaf(-stored_norm(n[j], a.norm16), a.levels[code[j]], yv[j]);
       if (lead) {
         x_s[j][o] = r;                            // (x_s is no longer read: the last barrier passed)
         float sq = r * r;
@@ -154,7 +155,7 @@ __device__ __forceinline__ void quantize_vectors(const QuantizeArgs& a, int v0, 
       const float gamma = sqrtf((rnrm_s[j][0] + rnrm_s[j][1]) + (rnrm_s[j][2] + rnrm_s[j][3]));
       const unsigned word = __ballot_sync(0xffffffffu, z[j] > 0.f);
       if (ok[j] && lead && lane == 0) reinterpret_cast<unsigned*>(a.qjl + row[j] * 16)[warp] = word;
-      if (ok[j] && threadIdx.x == 0) a.rnorm[row[j]] = gamma;
+      if (ok[j] && threadIdx.x == 0) store_norm(a.rnorm, row[j], gamma, a.norm16);
     }
   }
 }
@@ -304,7 +305,14 @@ __global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
   if (live) {
     const int ctx = context_of(a, vec / a.n_q);
     // (a sequence without context has no entries, and its segment record is stale)
-    const SegInfo seg = ctx > 0 ? a.ws_seg[vec] : SegInfo{0, 0, 0, 0};
+    SegInfo seg = ctx > 0 ? a.ws_seg[vec] : SegInfo{0, 0, 0, 0};
+    // (a partials CTA that stopped early leaves a stale record: check it)
+    if (ctx > 0 && (seg.count < 0 || seg.base < 0 || seg.stride < 1 ||
+                    static_cast<long long>(seg.base) +
+                            static_cast<long long>(seg.count > 0 ? seg.count - 1 : 0) * seg.stride >= a.part_cap)) {
+      if (o == 0) atomicCAS(a.error, 0, kErrPartials);
+      seg = SegInfo{0, 0, 0, 0};
+    }
     const int n_entries = seg.count;
     for (int c0 = q & 1; c0 < n_entries; c0 += 2 * 4) {
       float mc[4], lc[4], ac[4];

@@ -36,6 +36,8 @@ CONFIGS = {
         batch=64, n_q=64, n_kv=8, context=(1024, 32768), dtype="bf16", k_bits=3, v_bits=3, qjl_m=128,
         block_size=64, log_uniform=(0.1, 10.0), outliers=0, outlier_scale=1.0, shuffled_table=True, seed=0),
 }
+# the same paged decode with 16-bit stored norms (102 bytes per token-head)
+CONFIGS["c5_llama3_70b_paged_fp16_norms"] = dict(CONFIGS["c5_llama3_70b_paged"], norm_bits=16)
 
 
 def torch_dtype(name):

@@ -90,6 +90,11 @@ def lloyd_max(d, bits, tol=1e-13, max_iter=100000):
         levels = new
         if moved < tol:
             break
+    # f_d is even, so the exact fixed point is odd-symmetric (c_i = -c_{K-1-i})
+    # and its middle boundary is exactly 0; rounding in the iteration leaves a
+    # residue near 1e-16 there, which would decide the tie at y = 0 (reading:
+    # a tie goes to the lower level) by noise.  Restore the symmetry.
+    levels = 0.5 * (levels - levels[::-1])
     bounds = 0.5 * (levels[:-1] + levels[1:])
     return levels, bounds
 

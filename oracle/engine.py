@@ -23,8 +23,9 @@ def _matrices(d, m, seed):
     return rotation.rotation_and_projection(d, m, seed)
 
 
-def build(d=128, k_bits=3, v_bits=3, qjl_m=128, seed=0):
-    """The oracle's own R, S and codebooks for one configuration."""
+def build(d=128, k_bits=3, v_bits=3, qjl_m=128, seed=0, norm_bits=32):
+    """The oracle's own R, S and codebooks for one configuration; norm_bits 16
+    stores the norms (and the residual norm) as float16, 32 as float32."""
     k_mse_bits = k_bits - 1 if qjl_m else k_bits
     rot, proj = _matrices(d, qjl_m, seed)
     k_levels, k_bounds = _levels(d, k_mse_bits)
@@ -34,24 +35,26 @@ def build(d=128, k_bits=3, v_bits=3, qjl_m=128, seed=0):
         "k_bits": k_mse_bits, "v_bits": v_bits,
         "k_levels": k_levels, "k_bounds": k_bounds,
         "v_levels": v_levels, "v_bounds": v_bounds,
+        "norm_dtype": np.float16 if norm_bits == 16 else np.float32,
     }
 
 
 def encode_keys(x, book):
     """Key rows: dict of packed codes, sign bits, norm, residual norm, plus the
     fp64 intermediates (unit rotated y, projected residual z) for acceptance."""
-    norm, y, codes = quantize.encode_mse(x, book["rot"], book["k_bounds"])
+    nd = book.get("norm_dtype", np.float32)
+    norm, y, codes = quantize.encode_mse(x, book["rot"], book["k_bounds"], nd)
     out = {"k_codes": packing.pack_planes(codes, book["k_bits"]), "k_norm": norm,
            "codes": codes, "y": y}
     if book["qjl_m"]:
-        gamma, signs, z = quantize.encode_qjl(x, norm, codes, book["rot"], book["k_levels"], book["proj"])
+        gamma, signs, z = quantize.encode_qjl(x, norm, codes, book["rot"], book["k_levels"], book["proj"], nd)
         out.update({"k_qjl": packing.pack_signs(signs), "k_rnorm": gamma, "signs": signs, "z": z})
     return out
 
 
 def encode_values(x, book):
     """Value rows: packed codes and norm (plus fp64 intermediates)."""
-    norm, y, codes = quantize.encode_mse(x, book["rot"], book["v_bounds"])
+    norm, y, codes = quantize.encode_mse(x, book["rot"], book["v_bounds"], book.get("norm_dtype", np.float32))
     return {"v_codes": packing.pack_planes(codes, book["v_bits"]), "v_norm": norm,
             "codes": codes, "y": y}
 
@@ -59,11 +62,12 @@ def encode_values(x, book):
 def field_bytes(book):
     """Bytes per (token, head) of each cache field."""
     d = book["d"]
-    out = {"k_codes": book["k_bits"] * d // 8, "k_norm": 4,
-           "v_codes": book["v_bits"] * d // 8, "v_norm": 4}
+    nb = np.dtype(book.get("norm_dtype", np.float32)).itemsize
+    out = {"k_codes": book["k_bits"] * d // 8, "k_norm": nb,
+           "v_codes": book["v_bits"] * d // 8, "v_norm": nb}
     if book["qjl_m"]:
         out["k_qjl"] = book["qjl_m"] // 8
-        out["k_rnorm"] = 4
+        out["k_rnorm"] = nb
     return out
 
 
@@ -74,7 +78,7 @@ def empty_cache(book, num_blocks, n_kv_heads, block_size):
             cache[name] = np.zeros((num_blocks, n_kv_heads, book["v_bits"], book["d"], block_size // 8),
                                    dtype=np.uint8)
         elif name.endswith("norm"):
-            cache[name] = np.zeros((num_blocks, n_kv_heads, block_size), dtype=np.float32)
+            cache[name] = np.zeros((num_blocks, n_kv_heads, block_size), dtype=book.get("norm_dtype", np.float32))
         else:
             cache[name] = np.zeros((num_blocks, n_kv_heads, block_size, nbytes), dtype=np.uint8)
     return cache

@@ -22,14 +22,15 @@ def nearest_level_codes(y, bounds):
     return np.searchsorted(np.asarray(bounds, dtype=np.float64), y, side="left")
 
 
-def encode_mse(x, rot, bounds):
-    """x [N, d] -> (norm32 [N] float32, y [N, d] fp64 unit rotated vectors, codes [N, d])."""
+def encode_mse(x, rot, bounds, norm_dtype=np.float32):
+    """x [N, d] -> (stored norm [N] in norm_dtype -- float32, or float16 for a
+    cache with 16-bit norms --, y [N, d] fp64 unit rotated vectors, codes [N, d])."""
     x = np.asarray(x, dtype=np.float64)
     norm = np.sqrt(np.sum(x * x, axis=1))
     safe = np.where(norm > 0.0, norm, 1.0)
     y = (x @ rot.T) / safe[:, None]
     y[norm == 0.0] = 0.0
-    return norm.astype(np.float32), y, nearest_level_codes(y, bounds)
+    return norm.astype(norm_dtype), y, nearest_level_codes(y, bounds)
 
 
 def reconstruct_mse(norm32, codes, rot, levels):
@@ -38,13 +39,14 @@ def reconstruct_mse(norm32, codes, rot, levels):
     return norm32.astype(np.float64)[:, None] * (lv @ rot)
 
 
-def encode_qjl(x, norm32, codes, rot, levels, proj):
-    """Residual sketch: (gamma32 [N] float32, signs [N, m] 0/1, z = S r [N, m] fp64)."""
+def encode_qjl(x, norm32, codes, rot, levels, proj, norm_dtype=np.float32):
+    """Residual sketch against the stored norm ``norm32`` (float32 or float16):
+    (gamma [N] in norm_dtype, signs [N, m] 0/1, z = S r [N, m] fp64)."""
     x = np.asarray(x, dtype=np.float64)
     resid = x - reconstruct_mse(norm32, codes, rot, levels)
     gamma = np.sqrt(np.sum(resid * resid, axis=1))
     z = resid @ np.asarray(proj, dtype=np.float64).T
-    return gamma.astype(np.float32), (z > 0.0).astype(np.int64), z
+    return gamma.astype(norm_dtype), (z > 0.0).astype(np.int64), z
 
 
 def boundary_distance(y, bounds):

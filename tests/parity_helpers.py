@@ -23,10 +23,19 @@ CODE_EXEMPT = 1e-5
 ATTN_TOL = 1e-3
 
 
-def books(k_bits=3, v_bits=3, qjl_m=128, seed=0, block_size=64):
-    gpu = B.Codebook(k_bits=k_bits, v_bits=v_bits, qjl_m=qjl_m, seed=seed, block_size=block_size, device=0)
-    ref = engine.build(k_bits=k_bits, v_bits=v_bits, qjl_m=qjl_m, seed=seed)
+def books(k_bits=3, v_bits=3, qjl_m=128, seed=0, block_size=64, norm_bits=32):
+    gpu = B.Codebook(k_bits=k_bits, v_bits=v_bits, qjl_m=qjl_m, seed=seed, block_size=block_size, device=0,
+                     norm_bits=norm_bits)
+    ref = engine.build(k_bits=k_bits, v_bits=v_bits, qjl_m=qjl_m, seed=seed, norm_bits=norm_bits)
     return gpu, ref
+
+
+def norm_tolerance(stored, reference):
+    """|stored - reference| allowed for a norm held in ``stored``'s dtype: the
+    fp32 rounding of a 128-term sum of squares (relative 2e-6), plus half an
+    ulp of float16 (2^-11 relative) when the field is 16-bit."""
+    rel = 2e-6 + (2.0 ** -11 if stored.dtype == np.float16 else 0.0)
+    return rel * reference + 1e-30
 
 
 def dtype_code(t):
@@ -71,20 +80,20 @@ def check_mse_codes(x, got, norm_gpu, ref, which):
     bad = diff & ~exempt
     assert not bad.any(), "%d non-exempt code mismatches (first at %s)" % (bad.sum(), np.argwhere(bad)[:3])
     xn = np.linalg.norm(x, axis=1)
-    assert np.all(np.abs(norm_gpu.astype(np.float64) - xn) <= 2e-6 * xn + 1e-30)
+    assert np.all(np.abs(norm_gpu.astype(np.float64) - xn) <= norm_tolerance(norm_gpu, xn))
     return int((diff & exempt).sum()), int(exempt.sum()), got
 
 
 def check_qjl(x, codes_gpu, norm_gpu, packed_signs, gamma_gpu, ref):
     proj = ref["proj"]
-    gamma, signs, z = quantize.encode_qjl(x, norm_gpu, codes_gpu, ref["rot"], ref["k_levels"], proj)
+    gamma, signs, z = quantize.encode_qjl(x, norm_gpu, codes_gpu, ref["rot"], ref["k_levels"], proj, np.float64)
     got = packing.unpack_signs(packed_signs, proj.shape[0])
     xn = np.linalg.norm(x, axis=1)
     exempt = np.abs(z) < CODE_EXEMPT * xn[:, None] * np.linalg.norm(proj, axis=1)[None, :]
     diff = got != signs
     bad = diff & ~exempt
     assert not bad.any(), "%d non-exempt QJL bit mismatches" % bad.sum()
-    assert np.all(np.abs(gamma_gpu.astype(np.float64) - gamma.astype(np.float64)) <= 1e-5 * xn + 1e-30)
+    assert np.all(np.abs(gamma_gpu.astype(np.float64) - gamma) <= norm_tolerance(gamma_gpu, gamma) + 1e-5 * xn)
     return int((diff & exempt).sum())
 
 

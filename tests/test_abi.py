@@ -54,6 +54,8 @@ def test_host_builder_agrees_with_oracle(lib, k_bits, v_bits, qjl):
         levels, bounds, bits = B.tq_codebook_levels(book, which)
         assert bits == ref[name + "_bits"]
         assert np.max(np.abs(levels - ref[name + "_levels"])) < 1e-12
+        # both builders restore the exact symmetry: the tie at 0 is decided alike
+        assert np.array_equal(levels, -levels[::-1]) and bounds[len(bounds) // 2] == 0.0
         assert np.max(np.abs(bounds - ref[name + "_bounds"])) < 1e-12
     sizes = B.tq_cache_field_bytes(book)
     expect = engine.field_bytes(ref)
@@ -107,3 +109,15 @@ def test_workspace_size_grows_with_context(lib):
     assert short == B.tq_decode_workspace_bytes(book, 2, 8, 513) > 0
     assert B.tq_decode_workspace_bytes(book, 0, 8, 512) == 0
     book.close()
+
+
+def test_sixteen_bit_norms_field_sizes_and_checks(lib):
+    # norm_bits 16: every stored norm is 2 bytes, 102 bytes per (token, head) at 3/3 bits
+    book = B.Codebook(k_bits=3, v_bits=3, qjl_m=128, device=-1, norm_bits=16)
+    sizes = B.tq_cache_field_bytes(book)
+    assert [sizes[n] for n in B.FIELDS] == [32, 16, 2, 2, 48, 2]
+    assert sum(sizes.values()) == 102
+    book.close()
+    with pytest.raises(B.TQError) as err:
+        B.Codebook(device=-1, norm_bits=8)
+    assert err.value.status == 1

@@ -130,7 +130,11 @@ def test_lloyd_max_fixed_point_by_independent_quadrature(bits):
         den, _ = integrate.quad(lambda x: float(codebook.density(x, d)), edges[i], edges[i + 1],
                                 points=pts, epsabs=1e-18, epsrel=1e-13, limit=400)
         assert abs(num / den - level) < 1e-12
-    assert np.max(np.abs(levels + levels[::-1])) < 1e-12
+    # the coordinate law is even: the codebook is exactly odd-symmetric and the
+    # middle boundary is exactly 0 (a coordinate at 0 takes the lower level)
+    assert np.array_equal(levels, -levels[::-1])
+    assert bounds[len(bounds) // 2] == 0.0
+    assert np.searchsorted(bounds, 0.0, side="left") == len(levels) // 2 - 1
 
 
 def test_one_bit_levels_closed_form():

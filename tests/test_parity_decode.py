@@ -186,14 +186,14 @@ def test_long_context_full_size_every_head():
 
 def test_llama3_70b_paged_full_size_run_boundaries():
     # every group that holds the first or the last chunk of a CTA's run in the
-    # persistent tensor-core grid (two CTAs per SM for this shape), where the
-    # item cursor enters and leaves sequences and segments are merged across CTAs
-    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
-
+    # persistent tensor-core grid, where the item cursor enters and leaves
+    # sequences and segments are merged across CTAs
     def pick(cfg, ctx):
-        max_chunks = (int(ctx.max()) + 511) // 512
-        n_ctas = min(2 * n_sms, cfg["batch"] * cfg["n_kv"] * max_chunks)
-        groups = run_boundary_groups(ctx, cfg["n_kv"], n_ctas)
+        book = B.Codebook(k_bits=cfg["k_bits"], v_bits=cfg["v_bits"], qjl_m=cfg["qjl_m"], seed=cfg["seed"],
+                          block_size=cfg["block_size"], device=0)
+        plan = B.tq_decode_plan(book, cfg["batch"], cfg["n_q"], cfg["n_kv"], int(ctx.max()))
+        assert plan["tensor_cores"] == 1 and plan["chunk_tokens"] == 512
+        groups = run_boundary_groups(ctx, cfg["n_kv"], plan["partials_ctas"])
         assert len(groups) * cfg["n_q"] // cfg["n_kv"] >= 256
         return groups
 
@@ -273,3 +273,70 @@ def test_every_context_empty_gives_zero_rows():
         out = decode(book, cache, q, None, np.zeros(3, dtype=np.int32), max_context)
         assert np.all(out == 0.0)
     assert B.tq_get_last_device_error(book) == 0
+
+
+@pytest.mark.parametrize("group", [4, 8])
+def test_sixteen_bit_norms_decode(group):
+    # a cache with float16 norms (102 bytes per token-head at 3/3 bits), ragged
+    # contexts over shuffled blocks; the oracle decodes the GPU's cache
+    n_kv = 2
+    cfg = dict(n_kv=n_kv, block_size=64, dtype="bf16", seed=group + 40, log_uniform=(0.1, 10.0), outliers=3,
+               outlier_scale=30.0)
+    book, ref = books(3, 3, 128, seed=3, norm_bits=16)
+    assert B.tq_decode_kernel_kind(book, n_kv * group, n_kv) == 1
+    ctx = np.array([1, 300, 512, 1700, 2600], dtype=np.int32)
+    table, _ = W.block_layout(ctx, 64, True, seed=group)
+    g = generator(group + 40)
+    cache = fill_cache(book, cfg, ctx, table, g, chunk_tokens=1000)
+    q = W.queries(len(ctx), n_kv * group, torch.bfloat16, "cuda", g)
+    out = decode(book, cache, q, table, ctx, 2600)
+    worst = check_decode(out, host_cache(cache), q, table, ctx, ref,
+                         [(b, h) for b in range(len(ctx)) for h in range(n_kv * group)])
+    print("fp16 norms, G=%d: worst normalised error %.3g" % (group, worst))
+    assert B.tq_get_last_device_error(book) == 0
+
+
+def test_decode_plan_for_the_workloads():
+    # the launch plan: the 8B layer merges in the partials kernel (128 groups,
+    # fewer than CTAs), the 70B paged batch (512 groups) takes a merge launch,
+    # and the 4-bit-key long-context layout runs 256-token items (a 512-token
+    # one would not fit two CTAs per SM)
+    expect = {"c2_llama3_8b_decode": (1, 512), "c5_llama3_70b_paged": (0, 512), "c4_long_context": (1, 256)}
+    for name, (fused, chunk) in expect.items():
+        cfg = W.CONFIGS[name]
+        book = B.Codebook(k_bits=cfg["k_bits"], v_bits=cfg["v_bits"], qjl_m=cfg["qjl_m"], seed=cfg["seed"],
+                          block_size=cfg["block_size"], device=0)
+        ctx = W.context_lengths(cfg, cfg["seed"])
+        plan = B.tq_decode_plan(book, cfg["batch"], cfg["n_q"], cfg["n_kv"], int(ctx.max()))
+        assert plan["tensor_cores"] == 1
+        assert (plan["merge_in_partials"], plan["chunk_tokens"]) == (fused, chunk), (name, plan)
+        assert 0 < plan["partials_ctas"] <= 2 * torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("batch", [2, 400])
+def test_a_wait_that_runs_out_is_reported_and_the_next_call_is_correct(batch):
+    # the test aid withholds one MMA commit in the first CTA of the tensor-core
+    # kernel: that CTA's builders wait the one-second limit, the CTA drains its
+    # copies and MMAs and stops, the call ends with device error 4; with the
+    # aid off the same handle decodes correctly again.  batch 2 merges in the
+    # partials kernel, batch 400 (more groups than CTAs) in a merge launch,
+    # which must reject the stale segment records the stopped CTA left.
+    cfg = dict(n_kv=1, block_size=64, dtype="bf16", seed=batch, log_uniform=(0.1, 10.0), outliers=3,
+               outlier_scale=30.0)
+    book, ref = books(3, 3, 128, seed=14)
+    rng = np.random.default_rng(batch)
+    ctx = rng.integers(600, 1400, size=batch).astype(np.int32)
+    table, _ = W.block_layout(ctx, 64, True, seed=batch)
+    g = generator(batch + 1)
+    cache = fill_cache(book, cfg, ctx, table, g, chunk_tokens=2000)
+    q = W.queries(batch, 4, torch.bfloat16, "cuda", g)
+    plan = B.tq_decode_plan(book, batch, 4, 1, int(ctx.max()))
+    assert plan["merge_in_partials"] == (1 if batch == 2 else 0)
+    B.tq_debug_withhold_commit(book, True)
+    decode(book, cache, q, table, ctx, int(ctx.max()))
+    assert B.tq_get_last_device_error(book) == 4
+    B.tq_debug_withhold_commit(book, False)
+    out = decode(book, cache, q, table, ctx, int(ctx.max()))
+    assert B.tq_get_last_device_error(book) == 0
+    pairs = [(b, h) for b in range(batch) for h in range(4)] if batch <= 8 else attn_pairs(batch, 4, 24, seed=3)
+    check_decode(out, host_cache(cache), q, table, ctx, ref, pairs)

@@ -9,7 +9,7 @@ from online_kv_cache_tq_gb300 import binding as B
 from online_kv_cache_tq_gb300 import cache as C
 from online_kv_cache_tq_gb300 import workloads as W
 
-from parity_helpers import books, check_append, generator, quantize_into
+from parity_helpers import books, check_append, generator, host_cache, quantize_into
 
 pytestmark = pytest.mark.gpu
 
@@ -133,4 +133,65 @@ def test_prefill_full_size_sampled(bits):
     sample = np.concatenate([sample, [0, cfg["tokens"] - 1]])
     rep = check_append(book, ref, cache, k, v, slots, sample=sample)
     print("prefill bits=%d" % bits, rep)
+    assert B.tq_get_last_device_error(book) == 0
+
+
+@pytest.mark.parametrize("dtype,n_tok", [(torch.bfloat16, 1001), (torch.float32, 300), (torch.bfloat16, 40)])
+def test_sixteen_bit_norms(dtype, n_tok):
+    # float16 norms on every append path (tile quantizers and the per-vector
+    # one): norms within half an ulp, the residual taken against the stored
+    # float16 norm (the oracle recomputes it from the GPU's codes and norm)
+    book, ref = books(3, 3, 128, seed=8, norm_bits=16)
+    n_kv = 3
+    g = generator(n_tok)
+    scales = W.channel_scales(6, n_kv, (0.1, 10.0), 3, 30.0)
+    k = W.gaussian_tokens(n_tok, scales, dtype, "cuda", g)
+    v = W.gaussian_tokens(n_tok, scales, dtype, "cuda", g)
+    num_blocks = (n_tok + 63) // 64 + 1
+    cache = C.allocate_cache(book, num_blocks, n_kv)
+    assert cache["k_norm"].dtype == torch.float16
+    slots = np.random.default_rng(n_tok).permutation(num_blocks * 64)[:n_tok]
+    quantize_into(book, cache, k, v, slots)
+    print(check_append(book, ref, cache, k, v, slots))
+    assert B.tq_get_last_device_error(book) == 0
+
+
+@pytest.mark.parametrize("norm_bits,dtype", [(32, torch.bfloat16), (16, torch.float32)])
+def test_reconstruction_error_monitor(norm_bits, dtype):
+    # the monitor's sums against the oracle's fp64 reconstruction n R^T c[code]
+    # of the GPU's own codes and stored norms, for keys and values; a second
+    # call adds to the first; a skipped slot is not counted
+    from oracle import packing, quantize
+    book, ref = books(3, 3, 128, seed=12, norm_bits=norm_bits)
+    n_tok, n_kv = 700, 2
+    g = generator(70 + norm_bits)
+    scales = W.channel_scales(3, n_kv, (0.1, 10.0), 3, 30.0)
+    k = W.gaussian_tokens(n_tok, scales, dtype, "cuda", g)
+    v = W.gaussian_tokens(n_tok, scales, dtype, "cuda", g)
+    cache = C.allocate_cache(book, 12, n_kv)
+    slots = np.arange(n_tok)
+    slots[5] = -1
+    slot_t = quantize_into(book, cache, k, v, slots)
+    view = C.cache_view(book, cache)
+    hc = host_cache(cache)
+    live = slots >= 0
+    for which, x_t, name in ((0, k, "k"), (1, v, "v")):
+        stats = torch.zeros(4, dtype=torch.float64, device="cuda")
+        code = B.TQ_BF16 if dtype == torch.bfloat16 else B.TQ_FP32
+        B.tq_reconstruction_error(book, x_t, code, which, n_tok, n_kv, slot_t, view, stats)
+        B.tq_reconstruction_error(book, x_t, code, which, n_tok, n_kv, slot_t, view, stats)
+        got = stats.cpu().numpy() / 2.0
+        x = x_t.double().cpu().numpy()[live].reshape(-1, 128)
+        rows = np.stack([packing.slot_index(slots[live], h, n_kv, 64) for h in range(n_kv)], axis=1).reshape(-1)
+        if name == "k":
+            codes = packing.unpack_planes(hc["k_codes"].reshape(-1, hc["k_codes"].shape[-1])[rows], ref["k_bits"], 128)
+        else:
+            codes = np.stack([packing.read_value_codes(hc["v_codes"], slots[live], h) for h in range(n_kv)],
+                             axis=1).reshape(-1, 128)
+        norm = hc[name + "_norm"].reshape(-1)[rows]
+        err = np.linalg.norm(x - quantize.reconstruct_mse(norm, codes, ref["rot"], ref[name + "_levels"]), axis=1)
+        expect = np.array([err.sum(), (err ** 2).sum(), (x * x).sum(), len(x)])
+        assert got[3] == expect[3] == (n_tok - 1) * n_kv
+        assert np.allclose(got[:3], expect[:3], rtol=1e-5), (name, got, expect)
+        print(name, "mean error %.4g, relative squared error %.4g" % (got[0] / got[3], got[1] / got[2]))
     assert B.tq_get_last_device_error(book) == 0
