@@ -306,6 +306,34 @@ tq_status tq_decode_attention_static(const tq_codebook* book, const void* q, tq_
  * in tensor memory), 0 for the CUDA-core kernel.  Host only; launches nothing. */
 tq_status tq_decode_kernel_kind(const tq_codebook* book, int n_q_heads, int n_kv_heads, int* tensor_cores);
 
+/* Decode attention over a context held in two caches of different bit
+ * widths (the yfxerp.com page, §2.3 "dynamic bit-width scheduling": the
+ * prompt's keys and values kept at 4 bits from prefill, the generated ones at
+ * 3 bits): for every sequence b, the first context_lens[b] tokens of the
+ * first part and the second part's context_lens[b] tokens form one context
+ * under one softmax (the order within a context does not matter to decode
+ * attention).  Each part has its own handle, cache, block table and lengths
+ * (fields as in tq_decode_attention); the two handles must share d, qjl_m
+ * and the seed, i.e. R and S (else TQ_ERR_INVALID_ARG), so that one query
+ * rotation and one back-rotation serve both; their bit widths and norm
+ * widths may differ.  Either part of a sequence may be empty; a sequence with
+ * both empty yields a zero output row.  workspace: device scratch of
+ * tq_decode_parts_workspace_bytes bytes, 256-byte aligned.  Asynchronous on
+ * `stream`. */
+typedef struct {
+  const tq_codebook* book;
+  const tq_cache_view* cache;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* context_lens;
+  int max_context;
+} tq_context_part;
+size_t tq_decode_parts_workspace_bytes(const tq_context_part* first, const tq_context_part* second, int batch,
+                                       int n_q_heads);
+tq_status tq_decode_attention_parts(const tq_context_part* first, const tq_context_part* second, const void* q,
+                                    tq_dtype dtype, int batch, int n_q_heads, int n_kv_heads, float scale, float* out,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* How tq_decode_attention / tq_decode_step run this shape (host only; launches
  * nothing): tensor_cores 1 for the tensor-core partials kernel (else the
  * CUDA-core one); merge_in_partials 1 when that kernel merges each (sequence,

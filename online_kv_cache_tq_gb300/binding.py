@@ -25,6 +25,7 @@ EXPORTED = ("tq_codebook_build", "tq_codebook_destroy", "tq_codebook_levels", "t
             "tq_decode_attention", "tq_decode_step", "tq_decode_step_host", "tq_decode_step_host_workspace_bytes",
             "tq_decode_step_prepare", "tq_decode_prepare", "tq_decode_partials", "tq_decode_finish",
             "tq_decode_attention_static", "tq_decode_kernel_kind", "tq_decode_plan", "tq_debug_withhold_commit",
+            "tq_decode_parts_workspace_bytes", "tq_decode_attention_parts",
             "tq_get_last_device_error",
             "tq_status_string")
 
@@ -50,6 +51,11 @@ class tq_cache_view(ctypes.Structure):
 class tq_decode_plan_info(ctypes.Structure):
     _fields_ = [("tensor_cores", ctypes.c_int), ("merge_in_partials", ctypes.c_int),
                 ("partials_ctas", ctypes.c_int), ("chunk_tokens", ctypes.c_int)]
+
+
+class tq_context_part(ctypes.Structure):
+    _fields_ = [("book", ctypes.c_void_p), ("cache", ctypes.POINTER(tq_cache_view)), ("block_table", ctypes.c_void_p),
+                ("max_blocks", ctypes.c_int), ("context_lens", ctypes.c_void_p), ("max_context", ctypes.c_int)]
 
 
 _LIB = None
@@ -97,6 +103,11 @@ def load():
     lib.tq_decode_kernel_kind.argtypes = [vp, i32, i32, ctypes.POINTER(i32)]
     lib.tq_decode_plan.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(tq_decode_plan_info)]
     lib.tq_debug_withhold_commit.argtypes = [vp, i32]
+    lib.tq_decode_parts_workspace_bytes.argtypes = [ctypes.POINTER(tq_context_part), ctypes.POINTER(tq_context_part),
+                                                    i32, i32]
+    lib.tq_decode_parts_workspace_bytes.restype = sz
+    lib.tq_decode_attention_parts.argtypes = [ctypes.POINTER(tq_context_part), ctypes.POINTER(tq_context_part), vp,
+                                              i32, i32, i32, i32, ctypes.c_float, vp, vp, sz, vp]
     lib.tq_get_last_device_error.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.tq_status_string.argtypes = [i32]
     lib.tq_status_string.restype = ctypes.c_char_p
@@ -333,3 +344,22 @@ def tq_decode_plan(book, batch, n_q_heads, n_kv_heads, max_context):
 def tq_debug_withhold_commit(book, enable):
     """Test aid for the bounded waits (see include/tq.h)."""
     _check(load().tq_debug_withhold_commit(book.handle, 1 if enable else 0), "tq_debug_withhold_commit")
+
+
+def context_part(book, view, block_table, max_blocks, context_lens, max_context):
+    """A tq_context_part (keeps the cache view alive with it)."""
+    part = tq_context_part(book.handle, ctypes.pointer(view), _ptr(block_table), max_blocks, _ptr(context_lens),
+                           max_context)
+    part._keep = (view, block_table, context_lens)
+    return part
+
+
+def tq_decode_parts_workspace_bytes(first, second, batch, n_q_heads):
+    return load().tq_decode_parts_workspace_bytes(ctypes.byref(first), ctypes.byref(second), batch, n_q_heads)
+
+
+def tq_decode_attention_parts(first, second, q, dtype, batch, n_q_heads, n_kv_heads, scale, out, workspace,
+                              workspace_bytes, stream=None):
+    _check(load().tq_decode_attention_parts(ctypes.byref(first), ctypes.byref(second), _ptr(q), dtype, batch,
+                                            n_q_heads, n_kv_heads, scale, _ptr(out), _ptr(workspace),
+                                            workspace_bytes, _stream(stream)), "tq_decode_attention_parts")

@@ -816,6 +816,54 @@ tq_status tq_decode_kernel_kind(const tq_codebook* book, int n_q_heads, int n_kv
   return TQ_OK;
 }
 
+size_t tq_decode_parts_workspace_bytes(const tq_context_part* first, const tq_context_part* second, int batch,
+                                       int n_q_heads) {
+  if (first == nullptr || second == nullptr || first->book == nullptr || second->book == nullptr) return 0;
+  const size_t w1 = tq_decode_workspace_bytes(first->book, batch, n_q_heads, first->max_context);
+  const size_t w2 = tq_decode_workspace_bytes(second->book, batch, n_q_heads, second->max_context);
+  return w1 == 0 || w2 == 0 ? 0 : round_up(w1) + w2;
+}
+
+tq_status tq_decode_attention_parts(const tq_context_part* first, const tq_context_part* second, const void* q,
+                                    tq_dtype dtype, int batch, int n_q_heads, int n_kv_heads, float scale, float* out,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (first == nullptr || second == nullptr || !valid_device_handle(first->book) ||
+      !valid_device_handle(second->book)) {
+    return TQ_ERR_INVALID_ARG;
+  }
+  const tq_codebook* b1 = first->book;
+  const tq_codebook* b2 = second->book;
+  // one rotation and one projection for both parts: the parts' rotated-space
+  // partials merge, and one back-rotation serves both
+  if (b1->device != b2->device || b1->cfg.d != b2->cfg.d || b1->cfg.qjl_m != b2->cfg.qjl_m ||
+      b1->host.R != b2->host.R || b1->host.S != b2->host.S) {
+    return TQ_ERR_INVALID_ARG;
+  }
+  if (batch > 0 && (out == nullptr || !aligned16(out))) return TQ_ERR_INVALID_ARG;
+  const size_t w1 = tq_decode_workspace_bytes(b1, batch, n_q_heads, first->max_context);
+  const size_t w2 = tq_decode_workspace_bytes(b2, batch, n_q_heads, second->max_context);
+  if (batch > 0 && (workspace == nullptr || workspace_bytes < round_up(w1) + w2)) return TQ_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  tq::DecodeArgs a1, a2;
+  tq_status st = decode_args(b1, kPrepare | kPartials, q, dtype, batch, n_q_heads, n_kv_heads, first->cache,
+                             first->block_table, first->max_blocks, first->context_lens, first->max_context, scale,
+                             out, ws, w1, &a1);
+  if (st == TQ_OK)
+    st = decode_args(b2, kPrepare | kPartials, q, dtype, batch, n_q_heads, n_kv_heads, second->cache,
+                     second->block_table, second->max_blocks, second->context_lens, second->max_context, scale, out,
+                     batch > 0 ? ws + round_up(w1) : nullptr, w2, &a2);
+  if (st != TQ_OK || batch == 0) return st;
+  a1.merge_in_partials = a2.merge_in_partials = 0;   // the parts merge together below
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool bf16 = dtype == TQ_BF16;
+  st = launched(tq::launch_decode_prepare(a1, bf16, s));
+  if (st == TQ_OK) st = launched(launch_partials(b1, a1, s));
+  if (st == TQ_OK) st = launched(tq::launch_decode_prepare(a2, bf16, s));
+  if (st == TQ_OK) st = launched(launch_partials(b2, a2, s));
+  if (st == TQ_OK) st = launched(tq::launch_decode_finish_parts(a1, a2, s));
+  return st;
+}
+
 tq_status tq_decode_plan(const tq_codebook* book, int batch, int n_q_heads, int n_kv_heads, int max_context,
                          tq_decode_plan_info* info) {
   if (!valid_device_handle(book) || info == nullptr || batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 ||

@@ -188,5 +188,8 @@ cudaError_t launch_merge_groups_tc(const DecodeArgs& args, cudaStream_t stream);
 // early: launched as a programmatic dependent of the tensor-core partials
 // kernel (the merge waits for it before reading the partials).
 cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream, bool early = false);
+// The merge over the partials of two parts of every sequence's context (two
+// caches, each with its own handle and workspace; the same R), into first.out.
+cudaError_t launch_decode_finish_parts(const DecodeArgs& first, const DecodeArgs& second, cudaStream_t stream);
 
 }  // namespace tq

@@ -289,7 +289,7 @@ __device__ __forceinline__ int context_of(const DecodeArgs& a, int b) {
 // [32 q, 32 q + 32) of both heads' back-rotations from one set of loads of R.
 // Every thread's entry loads are independent, so a launch is a few memory
 // round trips long.
-__global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a, DecodeArgs second, int n_src) {
   constexpr int kHeads = 2;
   __shared__ float o_s[kHeads][kDim];
   __shared__ float red_s[4][kHeads][kDim];
@@ -302,15 +302,18 @@ __global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
   const bool live = vec < n_vec;
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the partials (no-op unless launched early)
   float m = -INFINITY, l = 0.f, acc = 0.f;
-  if (live) {
-    const int ctx = context_of(a, vec / a.n_q);
+  // the entries of every source (one cache, or the two parts of a split
+  // context), merged as one running (m, l, acc)
+  for (int src = 0; src < n_src && live; ++src) {
+    const DecodeArgs& s = src == 0 ? a : second;
+    const int ctx = context_of(s, vec / s.n_q);
     // (a sequence without context has no entries, and its segment record is stale)
-    SegInfo seg = ctx > 0 ? a.ws_seg[vec] : SegInfo{0, 0, 0, 0};
+    SegInfo seg = ctx > 0 ? s.ws_seg[vec] : SegInfo{0, 0, 0, 0};
     // (a partials CTA that stopped early leaves a stale record: check it)
     if (ctx > 0 && (seg.count < 0 || seg.base < 0 || seg.stride < 1 ||
                     static_cast<long long>(seg.base) +
-                            static_cast<long long>(seg.count > 0 ? seg.count - 1 : 0) * seg.stride >= a.part_cap)) {
-      if (o == 0) atomicCAS(a.error, 0, kErrPartials);
+                            static_cast<long long>(seg.count > 0 ? seg.count - 1 : 0) * seg.stride >= s.part_cap)) {
+      if (o == 0) atomicCAS(s.error, 0, kErrPartials);
       seg = SegInfo{0, 0, 0, 0};
     }
     const int n_entries = seg.count;
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(kGemvThreads) combine_kernel(DecodeArgs a) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int c = c0 + 2 * j;
-        const float* part = a.ws_part + (static_cast<long long>(seg.base) + static_cast<long long>(c) * seg.stride) * kPartStride;
+        const float* part = s.ws_part + (static_cast<long long>(seg.base) + static_cast<long long>(c) * seg.stride) * kPartStride;
         mc[j] = c < n_entries ? part[0] : -INFINITY;
         lc[j] = c < n_entries ? part[1] : 0.f;
         ac[j] = c < n_entries ? part[4 + o] : 0.f;
@@ -448,7 +451,14 @@ cudaError_t launch_decode_finish(const DecodeArgs& args, cudaStream_t stream, bo
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = early ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, combine_kernel, args);
+  return cudaLaunchKernelEx(&cfg, combine_kernel, args, args, 1);
+}
+
+cudaError_t launch_decode_finish_parts(const DecodeArgs& first, const DecodeArgs& second, cudaStream_t stream) {
+  const int n_vec = first.batch * first.n_q;
+  if (n_vec <= 0) return cudaSuccess;
+  combine_kernel<<<(n_vec + 1) / 2, kGemvThreads, 0, stream>>>(first, second, 2);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_step_prep(const QuantizeArgs& ka, const QuantizeArgs& va, bool kv_bf16, const DecodeArgs& da,

@@ -108,3 +108,33 @@ def decode_attention(query, cache, table_row, length, kv_head, book, scale=None)
     v_codes = rows["v_code_values"]
     vhat = reconstruct_mse(rows["v_norm"].reshape(-1), v_codes, book["rot"], book["v_levels"])
     return attend(query, khat, corr, vhat, scale), float(np.max(np.linalg.norm(vhat, axis=1)))
+
+
+def decode_attention_parts(query, parts, scale=None):
+    """Output of one query head over a context split into parts, each read
+    from its own cache with its own codebook (the yfxerp.com page, §2.3:
+    prompt tokens kept at a higher bit width than generated ones): one
+    softmax over the concatenation.  ``parts``: list of (cache, table_row,
+    length, kv_head, book); the books share R and S.  Returns the output and
+    max_t ||v_hat_t|| over every part."""
+    khats, corrs, vhats = [], [], []
+    d = parts[0][4]["rot"].shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    for cache, table_row, length, kv_head, book in parts:
+        if length == 0:
+            continue
+        rows = read_sequence(cache, table_row, length, kv_head, cache["k_norm"].shape[2])
+        codes = packing.unpack_planes(rows["k_codes"], book["k_bits"], d)
+        khats.append(reconstruct_mse(rows["k_norm"].reshape(-1), codes, book["rot"], book["k_levels"]))
+        if "k_qjl" in rows and book["proj"].shape[0] > 0:
+            signs = packing.unpack_signs(rows["k_qjl"], book["proj"].shape[0])
+            corrs.append(qjl_estimate(query, rows["k_rnorm"].reshape(-1), signs, book["proj"]))
+        else:
+            corrs.append(np.zeros(length))
+        vhats.append(reconstruct_mse(rows["v_norm"].reshape(-1), rows["v_code_values"], book["rot"],
+                                     book["v_levels"]))
+    if not khats:
+        return np.zeros(d), 1.0
+    khat, corr, vhat = np.concatenate(khats), np.concatenate(corrs), np.concatenate(vhats)
+    return attend(query, khat, corr, vhat, scale), float(np.max(np.linalg.norm(vhat, axis=1)))

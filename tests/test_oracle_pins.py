@@ -390,3 +390,24 @@ def test_group_decode_equals_per_head_decode():
     for h in range(3):
         one, vm = attention.decode_attention(q[h], cache, table, 77, 1, book)
         assert np.array_equal(outs[h], one) and vm == vmax
+
+
+def test_split_context_equals_one_cache():
+    # a context split over two caches of one codebook attends exactly like the
+    # same tokens in one cache (one softmax over the concatenation)
+    from oracle import attention
+    book = engine.build(k_bits=3, v_bits=3, qjl_m=128, seed=2)
+    rng = np.random.default_rng(21)
+    k = rng.standard_normal((150, 1, 128))
+    v = rng.standard_normal((150, 1, 128))
+    whole = engine.empty_cache(book, 3, 1, 64)
+    engine.append(whole, book, k, v, np.arange(150))
+    first = engine.empty_cache(book, 2, 1, 64)
+    engine.append(first, book, k[:100], v[:100], np.arange(100))
+    second = engine.empty_cache(book, 1, 1, 64)
+    engine.append(second, book, k[100:], v[100:], np.arange(50))
+    q = rng.standard_normal(128)
+    ref, vmax = attention.decode_attention(q, whole, np.arange(3), 150, 0, book)
+    got, vmax2 = attention.decode_attention_parts(q, [(first, np.arange(2), 100, 0, book),
+                                                      (second, np.arange(1), 50, 0, book)])
+    assert np.allclose(got, ref, rtol=0, atol=1e-12) and vmax == vmax2

@@ -340,3 +340,55 @@ def test_a_wait_that_runs_out_is_reported_and_the_next_call_is_correct(batch):
     assert B.tq_get_last_device_error(book) == 0
     pairs = [(b, h) for b in range(batch) for h in range(4)] if batch <= 8 else attn_pairs(batch, 4, 24, seed=3)
     check_decode(out, host_cache(cache), q, table, ctx, ref, pairs)
+
+
+def test_prefill_at_four_bits_decode_at_three_bits():
+    # the prompt's tokens in a 4-bit cache (3 MSE bits + QJL for keys, 4-bit
+    # values), the generated ones in a 3-bit cache, one softmax over both; the
+    # handles share the seed (one R, one S).  Sequences with an empty part, and
+    # one with both parts empty.
+    n_kv, g4 = 2, 4
+    cfg = dict(n_kv=n_kv, block_size=64, dtype="bf16", seed=31, log_uniform=(0.1, 10.0), outliers=3,
+               outlier_scale=30.0)
+    book_p, ref_p = books(4, 4, 128, seed=6)
+    book_d, ref_d = books(3, 3, 128, seed=6, norm_bits=16)
+    pre = np.array([700, 0, 1500, 300, 0], dtype=np.int32)
+    gen = np.array([5, 40, 0, 130, 0], dtype=np.int32)
+    table_p, _ = W.block_layout(pre, 64, True, seed=1)
+    table_d, _ = W.block_layout(gen, 64, True, seed=2)
+    g = generator(31)
+    cache_p = fill_cache(book_p, cfg, pre, table_p, g, chunk_tokens=1000)
+    cache_d = fill_cache(book_d, cfg, gen, table_d, g, chunk_tokens=1000)
+    batch, n_q = len(pre), n_kv * g4
+    q = W.queries(batch, n_q, torch.bfloat16, "cuda", g)
+    tp, td = (torch.as_tensor(t, device="cuda") for t in (table_p, table_d))
+    lp, ld = (torch.as_tensor(c, device="cuda") for c in (pre, gen))
+    first = B.context_part(book_p, C.cache_view(book_p, cache_p), tp, table_p.shape[1], lp, int(pre.max()))
+    second = B.context_part(book_d, C.cache_view(book_d, cache_d), td, table_d.shape[1], ld, int(gen.max()))
+    nbytes = B.tq_decode_parts_workspace_bytes(first, second, batch, n_q)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = torch.full((batch, n_q, 128), float("nan"), device="cuda")
+    B.tq_decode_attention_parts(first, second, q, B.TQ_BF16, batch, n_q, n_kv, 0.0, out, ws, nbytes)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    hp, hd = host_cache(cache_p), host_cache(cache_d)
+    qn = q.double().cpu().numpy()
+    from oracle import attention
+    worst = 0.0
+    for b in range(batch):
+        for h in range(n_q):
+            if pre[b] + gen[b] == 0:
+                assert np.all(got[b, h] == 0.0)
+                continue
+            expect, vmax = attention.decode_attention_parts(
+                qn[b, h], [(hp, table_p[b], int(pre[b]), h // g4, ref_p), (hd, table_d[b], int(gen[b]), h // g4, ref_d)])
+            err = np.max(np.abs(got[b, h] - expect)) / vmax
+            assert err <= 1e-3, (b, h, err)
+            worst = max(worst, err)
+    print("two-part decode: worst normalised error %.3g" % worst)
+    assert B.tq_get_last_device_error(book_p) == 0
+    # handles with different seeds (different R) are rejected
+    other, _ = books(3, 3, 128, seed=7)
+    bad = B.context_part(other, C.cache_view(book_d, cache_d), td, table_d.shape[1], ld, int(gen.max()))
+    with pytest.raises(B.TQError):
+        B.tq_decode_attention_parts(first, bad, q, B.TQ_BF16, batch, n_q, n_kv, 0.0, out, ws, nbytes)
