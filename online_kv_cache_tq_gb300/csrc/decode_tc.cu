@@ -158,33 +158,6 @@ __device__ __forceinline__ void value_pair(uint32_t base, const uint32_t (&bw)[4
   }
 }
 
-// Write the e4m3 pieces of y (row `row0 + i` for piece i): each piece is the
-// e4m3 rounding of what the previous pieces left, times 16.
-template <int N>
-__device__ __forceinline__ void write_pieces(uint8_t* b, int row0, int kpos, float y) {
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-    const uint8_t p = to_e4m3(y);
-    b[sw128(row0 + i, kpos)] = p;
-    y = (y - from_e4m3(p)) * 16.f;
-  }
-}
-
-// Two values at once (one paired conversion each way): pieces of ya go to rows
-// row_a + i, of yb to rows row_b + i.
-template <int N>
-__device__ __forceinline__ void write_pieces2(uint8_t* b, int row_a, int row_b, int kpos, float ya, float yb) {
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-    const __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(make_float2(ya, yb), __NV_SATFINITE, __NV_E4M3);
-    b[sw128(row_a + i, kpos)] = static_cast<uint8_t>(p & 0xFFu);
-    b[sw128(row_b + i, kpos)] = static_cast<uint8_t>(p >> 8);
-    const float2 back = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(p, __NV_E4M3)));
-    ya = (ya - back.x) * 16.f;
-    yb = (yb - back.y) * 16.f;
-  }
-}
-
 // Barrier of the 256 builder threads only (named barrier 1).
 __device__ __forceinline__ void builder_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
@@ -812,6 +785,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     int seq = 0, ktile = 0, cur_group = -1;
     int vslot = 0, vwrap = 0;                     // value unit counter as (slot, times round the slots)
     const int wpd_shift = bs_shift - 5;         // log2 of the words per coordinate in a block
+    const int kpos_lane = k_position(lane);     // K position of this lane's token in a tile
     // The CTA's segment of the current group is merged chunk by chunk: the
     // running max and sum of every head in seg_ml_s (item seq reads parity
     // seq & 1 and writes the other), acc[coordinate lane] of head h in
@@ -917,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             const float mse = fmaf(am[j], cst_r[0][j], -cst_r[2][j]);
             const float qv = qjl ? fmaf(aq[j], cst_r[1][j], -cst_r[3][j]) : 0.f;
             const float sc = valid ? a.scale * fmaf(nk, mse, gk * qv) : -INFINITY;
-            s0[h * CH + tl] = sc;
+            s0[h * CH + i * kTile + kpos_lane] = sc;   // (in K order: the weights read four at once)
             mx[j] = fmaxf(mx[j], sc);
           }
         }
@@ -983,9 +957,6 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       // ---- softmax max over the chunk; B_V pieces of exp(s - m) n_v ----
       for (int i = t; i < x.n_tiles * kTile; i += kBuilders)
         mx[HG] = fmaxf(mx[HG], i < x.n_local && blk_ok[i >> bs_shift] ? norm_at(vn_s, i) : 0.f);
-      float lw[2 * HG];                           // owned heads: sum of e, then sum of e n_v
-#pragma unroll
-      for (int j = 0; j < 2 * HG; ++j) lw[j] = 0.f;
       {
         // chunk max of the owned heads over this half's warps; value-norm max over all
         warp_totals(mx, red_s, MaxOp());
@@ -1001,48 +972,56 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       }
       // the pieces carry 2 e n_v sv / beta_t, below 2 * 64 * max n_v * sv
       const float sv = piece_scale(2.f * kMaxBitInvScale * mx[HG]);
+      // Thread t takes head hq = warp % G and, per pass, one quad of a tile:
+      // tokens 32 g + i + 8 k (k = 0..3) sit at the consecutive K positions
+      // 32 g + 4 i + k, so their scores (stored in K order) are one float4 and
+      // every piece of their four weights is one 32-bit word of its B_V row.
+      // (kBuilders is a multiple of 32 G, so every pass of a thread has the same head.)
+      const int hq = (t >> 5) % G;
+      const float mq = half_total<HG + 1>(red_s, hq / HG, hq % HG, MaxOp());   // head hq's chunk max
+      float lw0 = 0.f, lw1 = 0.f;                 // head hq: sum of e, sum of e n_v
       {
-        // thread (lane, half): token slot `lane` of every tile, its own heads
-        // (templated on the half, so that the owned heads are compile-time indices)
-        const int kpos = k_position(lane);
-        const float ib = 2.f * bit_inv_scale(lane) * sv;
-        auto weights_half = [&](auto half_c) {
-          constexpr int H0 = decltype(half_c)::value * HG;
-          if constexpr (H0 < G) {
-            for (int tile = 0; tile < x.n_tiles; ++tile) {
-              const int tl = tile * kTile + lane;
-              const bool valid = tl < x.n_local && blk_ok[tl >> bs_shift];
-              const float vn = norm_at(vn_s, tl);       // (tl < CH: in bounds; selected below)
-              const float nv = valid ? vn : 0.f;
-              uint8_t* dst = b_v + tile * L.no * 128;
-              float e[HG];
+        const int q = t & 31, gq = q >> 3, i = q & 7;
+        const int kp0 = 32 * gq + 4 * i;
+        const float ib = 2.f * bit_inv_scale(i) * sv;
+        const int units = x.n_tiles * 32 * G;
+        for (int u = t; u < units; u += kBuilders) {
+          const int tile = u / (32 * G);
+          const int tl0 = tile * kTile + 32 * gq + i;           // tokens tl0 + 8 k
+          const float4 sc = *reinterpret_cast<const float4*>(s0 + hq * CH + tile * kTile + kp0);
+          const bool blk_valid = blk_ok[tl0 >> bs_shift] != 0;   // (the four share a 32-token group)
+          const float sk[4] = {sc.x, sc.y, sc.z, sc.w};
+          float w[4];
 #pragma unroll
-              for (int j = 0; j < HG; ++j) {
-                const int h = H0 + j;
-                e[j] = 0.f;
-                if (h >= G) continue;
-                // (a select, not a branch: the exponent of an invalid slot may be nan)
-                const float ex = __expf(s0[h * CH + tl] - mx[j]);
-                e[j] = valid && mx[j] != -INFINITY ? ex : 0.f;
-                lw[j] += e[j];
-                lw[HG + j] = fmaf(e[j], nv, lw[HG + j]);
-              }
-              // the owned heads two at a time (one when the half owns one head)
+          for (int k = 0; k < 4; ++k) {
+            const int tl = tl0 + 8 * k;
+            const bool valid = blk_valid && tl < x.n_local;
+            const float vn = norm_at(vn_s, tl);                  // (tl < CH: in bounds; selected below)
+            // (selects, not branches: the exponent of an invalid slot may be nan)
+            const float ex = __expf(sk[k] - mq);
+            const float e = valid && mq != -INFINITY ? ex : 0.f;
+            const float nv = valid ? vn : 0.f;
+            lw0 += e;
+            lw1 = fmaf(e, nv, lw1);
+            w[k] = e * nv * ib;
+          }
+          uint8_t* rows = b_v + tile * L.no * 128;
 #pragma unroll
-              for (int j = 0; j < HG; j += 2) {
-                const int h = H0 + j;
-                if (h >= G) continue;
-                if (j + 1 < HG && h + 1 < G)
-                  write_pieces2<kVPieces>(dst, h * kVPieces, (h + 1) * kVPieces, kpos, e[j] * nv * ib,
-                                          e[j + 1] * nv * ib);
-                else
-                  write_pieces<kVPieces>(dst, h * kVPieces, kpos, e[j] * nv * ib);
-              }
+          for (int p = 0; p < kVPieces; ++p) {
+            const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(w[0], w[1]), __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(w[2], w[3]), __NV_SATFINITE, __NV_E4M3);
+            *reinterpret_cast<uint32_t*>(rows + sw128(hq * kVPieces + p, kp0)) =
+                static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+            if (p + 1 < kVPieces) {               // each piece is the e4m3 rounding of what is left, times 16
+              const float2 bl = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3)));
+              const float2 bh = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
+              w[0] = (w[0] - bl.x) * 16.f;
+              w[1] = (w[1] - bl.y) * 16.f;
+              w[2] = (w[2] - bh.x) * 16.f;
+              w[3] = (w[3] - bh.y) * 16.f;
             }
           }
-        };
-        if (half == 0) weights_half(std::integral_constant<int, 0>{});
-        else weights_half(std::integral_constant<int, 1>{});
+        }
       }
       if (t == 0) sv_s = sv;
       ptx::fence_async_shared();
@@ -1101,15 +1080,18 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       ptx::tc_fence_after();
 
       {
-        // sums of e and of e n_v of the owned heads over this half's warps
+        // sums of e and of e n_v per head: warp w holds head w % G's, added in warp order
+        const float lw[2] = {lw0, lw1};
         warp_totals(lw, red_s, SumOp());
-        if ((t & 127) == 0)
-#pragma unroll
-          for (int j = 0; j < HG; ++j)
-            if (half * HG + j < G) {
-              stat_s[1][half * HG + j] = half_total<2 * HG>(red_s, half, j, SumOp());
-              wsum_s[half * HG + j] = half_total<2 * HG>(red_s, half, HG + j, SumOp());
-            }
+        if (t < G) {
+          float se = 0.f, sw = 0.f;
+          for (int w = t; w < kBuilders / 32; w += G) {
+            se += red_s[2 * w];
+            sw += red_s[2 * w + 1];
+          }
+          stat_s[1][t] = se;
+          wsum_s[t] = sw;
+        }
       }
 
       // ---- partial output of this chunk: half h reads the planes s with s % 2 == h ----
