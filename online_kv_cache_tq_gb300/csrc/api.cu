@@ -216,15 +216,16 @@ const float* table_field(const tq_codebook* b, size_t offset) {
   return reinterpret_cast<const float*>(reinterpret_cast<const char*>(b->d_tables) + offset);
 }
 
-// Larger bf16 batches go to the tensor-core quantizer, larger fp32 batches to
-// the SIMT one (small batches are handled by tq_quantize_append directly).
+// Larger batches go to the tensor-core tile quantizer (bf16 x through TMA;
+// fp32 x split into bf16 hi/lo by converter warps); small batches are handled
+// by tq_quantize_append directly.
 cudaError_t launch_quantize(const tq_codebook* b, const tq::QuantizeArgs& a, bool bf16, cudaStream_t s) {
-  if (!bf16) return tq::launch_quantize_simt(a, false, b->num_sms, s);
+  if (!bf16) return tq::launch_quantize_tc(a, b->w_map, b->w_map, b->num_sms, true, s);   // (x_map unused)
   CUtensorMap x_map;
   if (!encode_tokens_bf16(&x_map, a.x, static_cast<uint64_t>(a.n_tokens), static_cast<uint64_t>(a.n_kv))) {
     return cudaErrorInvalidValue;
   }
-  return tq::launch_quantize_tc(a, x_map, b->w_map, b->num_sms, s);
+  return tq::launch_quantize_tc(a, x_map, b->w_map, b->num_sms, false, s);
 }
 
 constexpr size_t kWsAlign = 256;

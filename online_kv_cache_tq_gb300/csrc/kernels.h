@@ -64,7 +64,6 @@ __device__ __forceinline__ long long slot_of(const QuantizeArgs& a, int token) {
   return phys * a.block_size + pos % a.block_size;
 }
 
-cudaError_t launch_quantize_simt(const QuantizeArgs& args, bool bf16, int num_sms, cudaStream_t stream);
 
 // Small batches (up to kSmallQuantize vectors per tensor): one CTA per
 // vector; K and V (either may be null) share one launch.
@@ -72,11 +71,12 @@ constexpr int kSmallQuantize = 1024;
 cudaError_t launch_quantize_small(const QuantizeArgs* first, const QuantizeArgs* second, bool bf16,
                                   cudaStream_t stream);
 
-// bf16 inputs on the tensor cores; x_map tiles x as [n_tokens][n_kv][128]
-// bf16 in boxes of 64 columns x 1 head x 128 tokens (128-byte swizzle), w_map
-// tiles the handle's bf16 hi/lo images of R and S' as [512][128].
+// Tile quantizer on the tensor cores; x_map tiles bf16 x as [n_tokens][n_kv][128]
+// in boxes of 64 columns x 1 head x 128 tokens (128-byte swizzle), w_map tiles
+// the handle's bf16 hi/lo images of R and S' as [512][128].  f32: x is fp32,
+// read by converter warps into bf16 hi/lo operands (x_map unused).
 cudaError_t launch_quantize_tc(const QuantizeArgs& args, const CUtensorMap& x_map, const CUtensorMap& w_map,
-                               int num_sms, cudaStream_t stream);
+                               int num_sms, bool f32, cudaStream_t stream);
 
 // Where the split-K partials of one query head are: entries base,
 // base + stride, ..., base + (count - 1) stride of the partials array, each

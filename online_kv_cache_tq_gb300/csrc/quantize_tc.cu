@@ -52,6 +52,8 @@ constexpr int kMatBytes = 2 * kHalfBytes;         // one 128 x 128 bf16 operand:
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kCvtWarps = 4;                      // fp32 inputs: warps that split X into bf16 hi/lo
+constexpr int kThreadsF32 = kThreads + 32 * kCvtWarps;
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, 128);
 
 // Shared memory: the bf16 hi/lo images of R (and S'), X stages and, with the
@@ -59,14 +61,19 @@ constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, 128);
 // of 128 columns (with the QJL bit each turns into the residual, hi and lo
 // bf16, once its Y is read, and serves as the A operand of the second
 // product) and, with the QJL bit, one Z buffer.
-template <bool QJL>
+// fp32 inputs (F32) hold each X stage as two bf16 operands, X_hi and X_lo
+// (X_hi = bf16(X), X_lo = bf16(X - X_hi)), and the exact fp32 squared norms
+// of the stage's 128 rows.
+template <bool QJL, bool F32 = false>
 struct Layout {
   static constexpr int kW = QJL ? 4 : 2;          // R_hi, R_lo (, S'_hi, S'_lo)
-  static constexpr int kStages = QJL ? 2 : 3;     // X tiles in flight
+  static constexpr int kStageBytes = F32 ? 2 * kMatBytes : kMatBytes;
+  static constexpr int kStages = F32 ? (QJL ? 1 : 2) : (QJL ? 2 : 3);   // X tiles in flight
   static constexpr int kW0 = 0;
   static constexpr int kX0 = kW * kMatBytes;
-  static constexpr int kRs0 = kX0 + kStages * kMatBytes;   // [2][4][128] floats
-  static constexpr int kBytes = kRs0 + (QJL ? 2 * 4 * kTileRows * 4 : 0);
+  static constexpr int kRs0 = kX0 + kStages * kStageBytes;   // [2][4][128] floats
+  static constexpr int kNrm0 = kRs0 + (QJL ? 2 * 4 * kTileRows * 4 : 0);   // F32: [kStages][128] floats
+  static constexpr int kBytes = kNrm0 + (F32 ? kStages * kTileRows * 4 : 0);
   static constexpr int kYBufs = QJL ? 3 : 2;
   static constexpr uint32_t kZCol = 3 * 128;
   static constexpr uint32_t kTmemCols = QJL ? 512 : 256;
@@ -194,11 +201,11 @@ __device__ __forceinline__ int x_partial_offset(int g, int row) {
   return (g >> 1) * kHalfBytes + row * 128 + ((((g & 1) * 4) ^ (row & 7)) << 4);
 }
 
-template <int BITS, bool QJL, bool TRANS>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BITS, bool QJL, bool TRANS, bool F32>
+__global__ void __launch_bounds__(F32 ? kThreadsF32 : kThreads, 1)
     quantize_tc_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map,
                        QuantizeArgs a) {
-  using L = Layout<QJL>;
+  using L = Layout<QJL, F32>;
   constexpr int kLevels = 1 << BITS;
   extern __shared__ uint8_t smem_raw[];
   // y_full[b]: the first products of Y buffer b are in tensor memory;
@@ -224,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_s = 0;
     ptx::mbar_init(&w_full, 1);
     for (int s = 0; s < L::kStages; ++s) {
-      ptx::mbar_init(&x_full[s], 1);
+      ptx::mbar_init(&x_full[s], F32 ? 32 * kCvtWarps : 1);   // the TMA copy, or every converter thread
       ptx::mbar_init(&x_empty[s], kEpiThreads);
     }
     for (int b = 0; b < 3; ++b) {
@@ -257,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            m * kTileRows);
       int it = 0, last_stage = -1;
       uint32_t last_phase = 0;
-      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+      for (int tile = blockIdx.x; !F32 && tile < n_tiles; tile += gridDim.x, ++it) {
         const int s = it % L::kStages;
         const uint32_t ph = (it / L::kStages) & 1;
         if (!ptx::wait_bar(&x_empty[s], ph ^ 1, abort, a.error, kErrTimeout)) break;
@@ -318,17 +325,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = ok && ptx::wait_bar(&y_empty[b], ((it / L::kYBufs) & 1) ^ 1, abort, a.error, kErrTimeout);
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint32_t x_base = ptx::smem_u32(smem + L::kX0 + s * kMatBytes);
+        const uint32_t x_base = ptx::smem_u32(smem + L::kX0 + s * L::kStageBytes);
         uint32_t acc = 0;
+        // X R_hi, X R_lo (bf16 X exact); fp32 X: X_hi R_hi, X_hi R_lo, X_lo R_hi
 #pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {          // R_hi, then R_lo
+        for (int pass = 0; pass < (F32 ? 3 : 2); ++pass) {
+          const uint32_t a_off = pass == 2 ? kMatBytes : 0;
+          const int b_sel = pass == 1 ? 1 : 0;
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               const uint32_t off = kb * kHalfBytes + ks * 32;
-              ptx::mma_bf16(yb, ptx::desc_k_sw128(x_base + off),
-                            ptx::desc_k_sw128(w_base + pass * kMatBytes + off), kIdesc, acc);
+              ptx::mma_bf16(yb, ptx::desc_k_sw128(x_base + a_off + off),
+                            ptx::desc_k_sw128(w_base + b_sel * kMatBytes + off), kIdesc, acc);
               acc = 1;
             }
           }
@@ -341,6 +351,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit(&drain);
         ptx::drain_bar(&drain, 0);
       }
+    }
+  } else if (F32 && warp >= 2 + kEpiWarps) {
+    // ---------------- converters (fp32 X): bf16 hi/lo operands and exact norms ----------------
+    // warp cw takes rows 32 cw .. 32 cw + 31 of a tile, one row at a time: lane
+    // l reads coordinates 4 l .. 4 l + 3 (the row's 512 bytes in one coalesced
+    // load) and stores them as bf16 hi and lo into the 128-byte swizzled
+    // K-major stage the MMA reads (K block l / 16, 16-byte chunk (l % 16) / 2)
+    const int cw = warp - (2 + kEpiWarps);
+    float* const nrm_s = reinterpret_cast<float*>(smem + L::kNrm0);
+    const float* x = static_cast<const float*>(a.x);
+    const int kb = lane >> 4, chunk = (lane & 15) >> 1;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+      const int s = it % L::kStages;
+      const uint32_t ph = (it / L::kStages) & 1;
+      if (!__all_sync(0xffffffffu, ptx::wait_bar(&x_empty[s], ph ^ 1, abort, a.error, kErrTimeout))) break;
+      uint8_t* const st = smem + L::kX0 + s * L::kStageBytes;
+      const int head = tile / n_tt, tok0 = (tile % n_tt) * kTileRows;
+#pragma unroll 4
+      for (int r = 0; r < 32; ++r) {
+        const int row = 32 * cw + r, token = tok0 + row;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (token < a.n_tokens)
+          v = *reinterpret_cast<const float4*>(x + (static_cast<long long>(token) * a.n_kv + head) * kDim + 4 * lane);
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y), h23 = __floats2bfloat162_rn(v.z, v.w);
+        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+        const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
+        const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
+        const int off = kb * kHalfBytes + row * 128 + ((chunk ^ (row & 7)) << 4) + (lane & 1) * 8;
+        *reinterpret_cast<uint2*>(st + off) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+        *reinterpret_cast<uint2*>(st + kMatBytes + off) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
+        float ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, v.w * v.w)));
+#pragma unroll
+        for (int off2 = 16; off2 > 0; off2 >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off2);
+        if (lane == 0) nrm_s[s * kTileRows + row] = ss;
+      }
+      ptx::fence_async_shared();                  // the generic stores, before the MMA reads the stage
+      ptx::mbar_arrive(&x_full[s]);
     }
   } else {
     // ---------------- epilogue: four threads per vector, 32 coordinates each ----------------
@@ -417,10 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = ptx::wait_bar(&x_full[s], ph, abort, a.error, kErrTimeout);
       // the partial norm from this group's 32 bf16 coordinates of the X row
       // (K block g / 2, 16-byte chunks (g % 2) * 4 .. + 3, chunk c of a row at c ^ (row % 8))
-      uint8_t* const x_tile = smem + L::kX0 + s * kMatBytes;
+      uint8_t* const x_tile = smem + L::kX0 + s * L::kStageBytes;
       const uint8_t* xrow = x_tile + (g >> 1) * kHalfBytes + row * 128;
       float ss = 0.f;
-      if (ok) {
+      if (ok && !F32) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int c = (g & 1) * 4 + q;
@@ -438,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Once the products have read X, the first 4 bytes this thread read carry
       // its partial sum to the other three threads of the row (no other thread
       // reads those bytes, and the stage is refilled only after all have read).
-      if (ok) *reinterpret_cast<float*>(x_tile + x_partial_offset(g, row)) = ss;
+      if (ok && !F32) *reinterpret_cast<float*>(x_tile + x_partial_offset(g, row)) = ss;
       // a failed wait anywhere ends every epilogue warp (the tcgen05.ld below
       // needs whole warps, the barriers below all 16); this barrier also
       // publishes the previous tile's partial residual norms
@@ -446,10 +496,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         alive = false;
         break;
       }
-      const float n = sqrtf((*reinterpret_cast<const float*>(x_tile + x_partial_offset(0, row)) +
-                             *reinterpret_cast<const float*>(x_tile + x_partial_offset(1, row))) +
-                            (*reinterpret_cast<const float*>(x_tile + x_partial_offset(2, row)) +
-                             *reinterpret_cast<const float*>(x_tile + x_partial_offset(3, row))));
+      // (fp32 X: the exact norm the converters left with the stage)
+      const float n =
+          F32 ? sqrtf(reinterpret_cast<const float*>(smem + L::kNrm0)[s * kTileRows + row])
+              : sqrtf((*reinterpret_cast<const float*>(x_tile + x_partial_offset(0, row)) +
+                       *reinterpret_cast<const float*>(x_tile + x_partial_offset(1, row))) +
+                      (*reinterpret_cast<const float*>(x_tile + x_partial_offset(2, row)) +
+                       *reinterpret_cast<const float*>(x_tile + x_partial_offset(3, row))));
       ptx::fence_async_shared();                  // the generic write above, before TMA refills the stage
       ptx::mbar_arrive(&x_empty[s]);
       // y = Y / n against t is taken as Y against n t (a zero vector compares
@@ -561,38 +614,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BITS, bool QJL, bool TRANS>
+template <int BITS, bool QJL, bool TRANS, bool F32>
 cudaError_t launch_bits(const CUtensorMap& x_map, const CUtensorMap& w_map, const QuantizeArgs& a, int grid,
                         cudaStream_t stream) {
-  const int smem = Layout<QJL>::kBytes + 1024;
-  cudaError_t err = cudaFuncSetAttribute(quantize_tc_kernel<BITS, QJL, TRANS>,
+  const int smem = Layout<QJL, F32>::kBytes + 1024;
+  cudaError_t err = cudaFuncSetAttribute(quantize_tc_kernel<BITS, QJL, TRANS, F32>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  quantize_tc_kernel<BITS, QJL, TRANS><<<grid, kThreads, smem, stream>>>(x_map, w_map, a);
+  quantize_tc_kernel<BITS, QJL, TRANS, F32><<<grid, F32 ? kThreadsF32 : kThreads, smem, stream>>>(x_map, w_map, a);
   return cudaGetLastError();
 }
 
-template <int BITS>
+template <int BITS, bool F32>
 cudaError_t launch_kind(const CUtensorMap& x_map, const CUtensorMap& w_map, const QuantizeArgs& a, int grid,
                         cudaStream_t stream) {
-  if (a.qjl != nullptr) return launch_bits<BITS, true, false>(x_map, w_map, a, grid, stream);
-  if (a.transposed) return launch_bits<BITS, false, true>(x_map, w_map, a, grid, stream);
-  return launch_bits<BITS, false, false>(x_map, w_map, a, grid, stream);
+  if (a.qjl != nullptr) return launch_bits<BITS, true, false, F32>(x_map, w_map, a, grid, stream);
+  if (a.transposed) return launch_bits<BITS, false, true, F32>(x_map, w_map, a, grid, stream);
+  return launch_bits<BITS, false, false, F32>(x_map, w_map, a, grid, stream);
+}
+
+template <int BITS>
+cudaError_t launch_dtype(const CUtensorMap& x_map, const CUtensorMap& w_map, const QuantizeArgs& a, int grid,
+                         bool f32, cudaStream_t stream) {
+  return f32 ? launch_kind<BITS, true>(x_map, w_map, a, grid, stream)
+             : launch_kind<BITS, false>(x_map, w_map, a, grid, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_quantize_tc(const QuantizeArgs& a, const CUtensorMap& x_map, const CUtensorMap& w_map,
-                               int num_sms, cudaStream_t stream) {
+                               int num_sms, bool f32, cudaStream_t stream) {
   if (a.n_vec <= 0) return cudaSuccess;
   if (a.qjl != nullptr && a.transposed) return cudaErrorInvalidValue;
   const int n_tiles = ((a.n_tokens + kTileRows - 1) / kTileRows) * a.n_kv;
   const int grid = n_tiles < num_sms ? n_tiles : num_sms;
   switch (a.bits) {
-    case 1: return launch_kind<1>(x_map, w_map, a, grid, stream);
-    case 2: return launch_kind<2>(x_map, w_map, a, grid, stream);
-    case 3: return launch_kind<3>(x_map, w_map, a, grid, stream);
-    case 4: return launch_kind<4>(x_map, w_map, a, grid, stream);
+    case 1: return launch_dtype<1>(x_map, w_map, a, grid, f32, stream);
+    case 2: return launch_dtype<2>(x_map, w_map, a, grid, f32, stream);
+    case 3: return launch_dtype<3>(x_map, w_map, a, grid, f32, stream);
+    case 4: return launch_dtype<4>(x_map, w_map, a, grid, f32, stream);
     default: return cudaErrorInvalidValue;
   }
 }

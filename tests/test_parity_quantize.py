@@ -1,6 +1,8 @@
 """GPU quantize-append vs the fp64 oracle, through the C ABI.
 
-fp32 inputs run the SIMT quantizer, bf16 inputs the tcgen05 one."""
+Up to 1024 vectors per tensor take the per-vector kernel; larger appends the
+tcgen05 tile quantizer (bf16 inputs through TMA, fp32 inputs split into bf16
+hi/lo operands by converter warps)."""
 import numpy as np
 import pytest
 import torch
@@ -30,15 +32,17 @@ def test_single_head_fp32_outliers_every_vector():
     assert B.tq_get_last_device_error(book) == 0
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("k_bits,v_bits", [(2, 2), (3, 3), (4, 4), (5, 1), (4, 2)])
-def test_bf16_gqa_ragged_shuffled_slots(k_bits, v_bits):
-    # shuffled slots: value codes take the bit-by-bit path
+def test_tile_quantizer_gqa_ragged_shuffled_slots(k_bits, v_bits, dtype):
+    # shuffled slots: value codes take the bit-by-bit path; fp32 inputs are
+    # split into bf16 hi/lo operands on the tensor cores (three products)
     book, ref = books(k_bits, v_bits, 128, seed=3)
     n_tok, n_kv = 1001, 3                 # 3003 vectors: 24 tiles of 128 and a ragged tail
     g = generator(k_bits * 10 + v_bits)
     scales = W.channel_scales(5, n_kv, (0.1, 10.0), 3, 30.0)
-    k = W.gaussian_tokens(n_tok, scales, torch.bfloat16, "cuda", g)
-    v = W.gaussian_tokens(n_tok, scales[::-1].copy(), torch.bfloat16, "cuda", g)
+    k = W.gaussian_tokens(n_tok, scales, dtype, "cuda", g)
+    v = W.gaussian_tokens(n_tok, scales[::-1].copy(), dtype, "cuda", g)
     num_blocks = 20
     slots = np.random.default_rng(1).permutation(num_blocks * 64)[:n_tok]
     cache = C.allocate_cache(book, num_blocks, n_kv)
