@@ -338,14 +338,17 @@ tq_status tq_decode_attention_parts(const tq_context_part* first, const tq_conte
  * nothing): tensor_cores 1 for the tensor-core partials kernel (else the
  * CUDA-core one); merge_in_partials 1 when that kernel merges each (sequence,
  * KV head) group and writes the output itself (at most as many groups as
- * CTAs), 0 when a merge launch follows it; partials_ctas the CTAs of its
- * persistent grid (0 for the CUDA-core kernel); chunk_tokens the context
- * tokens of one work item. */
+ * CTAs, and few segments per group at max_context), 0 when a merge launch
+ * follows it; partials_ctas the CTAs of its persistent grid (0 for the
+ * CUDA-core kernel); chunk_tokens the context tokens of one work item;
+ * merge_ctas the CTAs of the merge launch (0 when there is none): one per
+ * group, or one per query head when there are fewer groups than SMs. */
 typedef struct {
   int tensor_cores;
   int merge_in_partials;
   int partials_ctas;
   int chunk_tokens;
+  int merge_ctas;
 } tq_decode_plan_info;
 tq_status tq_decode_plan(const tq_codebook* book, int batch, int n_q_heads, int n_kv_heads, int max_context,
                          tq_decode_plan_info* info);

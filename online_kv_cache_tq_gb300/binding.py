@@ -50,7 +50,7 @@ class tq_cache_view(ctypes.Structure):
 
 class tq_decode_plan_info(ctypes.Structure):
     _fields_ = [("tensor_cores", ctypes.c_int), ("merge_in_partials", ctypes.c_int),
-                ("partials_ctas", ctypes.c_int), ("chunk_tokens", ctypes.c_int)]
+                ("partials_ctas", ctypes.c_int), ("chunk_tokens", ctypes.c_int), ("merge_ctas", ctypes.c_int)]
 
 
 class tq_context_part(ctypes.Structure):
@@ -334,7 +334,7 @@ def tq_status_string(status):
 
 
 def tq_decode_plan(book, batch, n_q_heads, n_kv_heads, max_context):
-    """dict(tensor_cores, merge_in_partials, partials_ctas, chunk_tokens) for a decode shape."""
+    """dict(tensor_cores, merge_in_partials, partials_ctas, chunk_tokens, merge_ctas) for a decode shape."""
     info = tq_decode_plan_info()
     _check(load().tq_decode_plan(book.handle, batch, n_q_heads, n_kv_heads, max_context, ctypes.byref(info)),
            "tq_decode_plan")

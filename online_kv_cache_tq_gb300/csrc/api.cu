@@ -888,6 +888,9 @@ tq_status tq_decode_plan(const tq_codebook* book, int batch, int n_q_heads, int 
   info->merge_in_partials = tc && tq::tc_merge_in_partials(a) ? 1 : 0;
   info->partials_ctas = tc ? tq::tc_grid(a) : 0;
   info->chunk_tokens = tc ? tq::tc_chunk(a) : tq::kChunk;
+  const int n_vec = batch * n_q_heads;
+  info->merge_ctas = !tc ? (n_vec + 1) / 2
+                         : info->merge_in_partials ? 0 : tq::tc_merge_per_head(a) ? n_vec : batch * n_kv_heads;
   return TQ_OK;
 }
 

@@ -1332,10 +1332,106 @@ __global__ void __launch_bounds__(kBuilders) merge_groups_kernel(DecodeArgs a) {
                     threadIdx.x & 127);
 }
 
+// The merge as its own launch for a few (sequence, KV head) groups with many
+// segments each (long contexts over a small batch): one 256-thread CTA per
+// query head, whose two halves merge alternate segments side by side, so that
+// a head's merge is a few memory round trips long and the heads run on
+// different SMs.  Thread (lane, half) holds coordinate lane; then thread
+// (o = lane, half) sums 64 of the 128 terms of the back-rotation.
+template <int G>
+__global__ void __launch_bounds__(kBuilders) merge_heads_kernel(DecodeArgs a) {
+  constexpr int kBatch = 8;
+  __shared__ float ml_s[2];
+  __shared__ float acc_s[kTile];
+  __shared__ __align__(16) float orot_s[kTile];
+  const int v = blockIdx.x;                       // query head b n_q + hq
+  const int b = v / a.n_q;
+  const int h = (v - b * a.n_q) % G;              // head within its group
+  const int qbase = v - h;
+  const int t = threadIdx.x, half = t >> 7, lane = t & (kTile - 1);
+  const int ctx = context_of(a, b);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  float* const out = a.out + static_cast<long long>(v) * kDim;
+  if (ctx == 0) {
+    if (t < kDim) out[t] = 0.f;
+    return;
+  }
+  const SegInfo seg = a.ws_seg[qbase];            // head 0: entries base + s G, head h at + h
+  // (a partials CTA that stopped early leaves a stale record: check it)
+  if (seg.count < 1 || seg.base < 0 || seg.stride != G ||
+      static_cast<long long>(seg.base) + static_cast<long long>(seg.count) * G > a.part_cap) {
+    if (t == 0) atomicCAS(a.error, 0, kErrPartials);
+    if (t < kDim) out[t] = 0.f;
+    return;
+  }
+  float w[64];                                    // R[64 half + i][lane], loaded while the segments merge
+  const float* rp = a.R + (64 * half) * kDim + lane;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) w[i] = __ldg(rp + i * kDim);
+  // this half's segments s = half, half + 2, ... as a running (m, l, acc)
+  float m = -INFINITY, l = 0.f, acc = 0.f;
+  for (int s0 = half; s0 < seg.count; s0 += 2 * kBatch) {
+    float pm[kBatch], pl[kBatch], pa[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int sg = s0 + 2 * k;
+      const float* part = a.ws_part + (static_cast<long long>(seg.base) + static_cast<long long>(sg) * G + h) *
+                                          kPartStride;
+      const bool in = sg < seg.count;
+      pm[k] = in ? __ldcg(part) : -INFINITY;
+      pl[k] = in ? __ldcg(part + 1) : 0.f;
+      pa[k] = in ? __ldcg(part + 4 + lane) : 0.f;
+    }
+    float mn = m;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) mn = fmaxf(mn, pm[k]);
+    if (mn == -INFINITY) continue;
+    const float so = m == -INFINITY ? 0.f : __expf(m - mn);
+    l *= so;
+    acc *= so;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const float sn = pm[k] == -INFINITY ? 0.f : __expf(pm[k] - mn);
+      l = fmaf(pl[k], sn, l);
+      acc = fmaf(pa[k], sn, acc);
+    }
+    m = mn;
+  }
+  // the two halves' sums, then o_rot = acc / l
+  if (half == 1) {
+    if (lane == 0) {
+      ml_s[0] = m;
+      ml_s[1] = l;
+    }
+    acc_s[lane] = acc;
+  }
+  __syncthreads();
+  if (half == 0) {
+    const float m1 = ml_s[0], l1 = ml_s[1];
+    const float mn = fmaxf(m, m1);
+    const float sa = m == -INFINITY ? 0.f : __expf(m - mn);
+    const float sb = m1 == -INFINITY ? 0.f : __expf(m1 - mn);
+    const float lt = fmaf(l, sa, l1 * sb);
+    orot_s[lane] = lt > 0.f ? fmaf(acc, sa, acc_s[lane] * sb) / lt : 0.f;
+  }
+  __syncthreads();
+  // out[o] = sum_i R[i][o] o_rot[i] (seo-farm page §2: out = R^T o_rot)
+  float r = 0.f;
+#pragma unroll
+  for (int k = 0; k < 64; k += 4) {
+    const float4 o4 = *reinterpret_cast<const float4*>(orot_s + 64 * half + k);
+    r = fmaf(w[k], o4.x, fmaf(w[k + 1], o4.y, fmaf(w[k + 2], o4.z, fmaf(w[k + 3], o4.w, r))));
+  }
+  if (half == 1) acc_s[lane] = r;                 // (half 0 read acc_s before the last barrier)
+  __syncthreads();
+  if (half == 0) out[lane] = r + acc_s[lane];
+}
+
 template <int G>
 cudaError_t launch_merge_g(const DecodeArgs& a, cudaStream_t stream) {
+  const bool per_head = tc_merge_per_head(a);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.batch * a.n_kv);
+  cfg.gridDim = dim3(per_head ? a.batch * a.n_q : a.batch * a.n_kv);
   cfg.blockDim = dim3(kBuilders);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1343,7 +1439,8 @@ cudaError_t launch_merge_g(const DecodeArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_groups_kernel<G>, a);
+  return per_head ? cudaLaunchKernelEx(&cfg, merge_heads_kernel<G>, a)
+                  : cudaLaunchKernelEx(&cfg, merge_groups_kernel<G>, a);
 }
 
 cudaError_t launch_merge_groups_tc(const DecodeArgs& a, cudaStream_t stream) {
@@ -1357,11 +1454,30 @@ cudaError_t launch_merge_groups_tc(const DecodeArgs& a, cudaStream_t stream) {
   }
 }
 
+// Segments of a (sequence, KV head) group at full context: the group's chunks
+// over the run length a CTA takes when every sequence is max_context long,
+// plus one for a run boundary inside the group.
+long long tc_segments_estimate(const DecodeArgs& a) {
+  const int chunk = tc_chunk(a);
+  const long long chunks = (a.max_context + chunk - 1) / chunk;
+  const long long items = static_cast<long long>(a.batch) * a.n_kv * chunks;
+  const long long ctas = tc_grid(a);
+  const long long per_cta = items / ctas > 0 ? items / ctas : 1;
+  return (chunks + per_cta - 1) / per_cta + 1;
+}
+
 bool tc_merge_in_partials(const DecodeArgs& a) {
   // a CTA owes the merges of the groups that end in its run: with more groups
   // than CTAs (short, ragged contexts) some runs hold many, and the CTAs that
-  // owe most set the launch's end; a merge launch spreads them over the GPU
-  return static_cast<long long>(a.batch) * a.n_kv <= tc_grid(a);
+  // owe most set the launch's end; with many segments per group (long
+  // contexts over a small batch) one CTA would merge them all at the end.  A
+  // merge launch spreads either over the GPU.
+  return static_cast<long long>(a.batch) * a.n_kv <= tc_grid(a) && tc_segments_estimate(a) <= 8;
+}
+
+bool tc_merge_per_head(const DecodeArgs& a) {
+  // fewer groups than SMs: a CTA per query head keeps more SMs merging
+  return static_cast<long long>(a.batch) * a.n_kv < (a.num_sms > 0 ? a.num_sms : 148);
 }
 
 cudaError_t launch_decode_partials_tc(const DecodeArgs& a, cudaStream_t stream, bool early) {

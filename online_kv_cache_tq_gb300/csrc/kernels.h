@@ -180,8 +180,11 @@ bool tc_decode_supported(const DecodeArgs& args, bool walsh_ok);
 cudaError_t launch_decode_partials_tc(const DecodeArgs& args, cudaStream_t stream, bool early);
 // Whether the tensor-core kernel should merge in place (few groups per CTA)
 // rather than leave the merge to launch_merge_groups_tc, a programmatic
-// dependent launch with one CTA per (sequence, KV head) group.
+// dependent launch.
 bool tc_merge_in_partials(const DecodeArgs& args);
+// Whether that merge launch takes one CTA per query head (few groups: long
+// contexts over a small batch) rather than one per group.
+bool tc_merge_per_head(const DecodeArgs& args);
 int tc_grid(const DecodeArgs& args);   // CTAs of the persistent tensor-core grid
 int tc_chunk(const DecodeArgs& args);  // tokens per work item of the tensor-core kernel
 cudaError_t launch_merge_groups_tc(const DecodeArgs& args, cudaStream_t stream);

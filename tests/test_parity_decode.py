@@ -52,6 +52,29 @@ def test_gqa_ragged_contexts_shuffled_blocks(group):
     assert B.tq_get_last_device_error(book) == 0
 
 
+@pytest.mark.parametrize("group", [4, 8])
+def test_long_contexts_over_few_groups_merge_per_query_head(group):
+    # two sequences x two KV heads with contexts of 30 and 9 chunks: more
+    # segments per group than the in-kernel merge takes and fewer groups than
+    # SMs, so a merge launch with one CTA per query head follows the partials
+    n_kv = 2
+    cfg = dict(n_kv=n_kv, block_size=64, dtype="bf16", seed=20 + group, log_uniform=(0.1, 10.0), outliers=3,
+               outlier_scale=30.0)
+    book, ref = books(3, 3, 128, seed=6)
+    ctx = np.array([15000, 4500], dtype=np.int32)
+    table, _ = W.block_layout(ctx, 64, True, seed=group)
+    plan = B.tq_decode_plan(book, 2, n_kv * group, n_kv, int(ctx.max()))
+    assert plan["merge_in_partials"] == 0 and plan["merge_ctas"] == 2 * n_kv * group, plan
+    g = generator(30 + group)
+    cache = fill_cache(book, cfg, ctx, table, g, chunk_tokens=4000)
+    q = W.queries(2, n_kv * group, torch.bfloat16, "cuda", g)
+    out = decode(book, cache, q, table, ctx, int(ctx.max()))
+    pairs = [(b, h) for b in range(2) for h in range(n_kv * group)]
+    worst = check_decode(out, host_cache(cache), q, table, ctx, ref, pairs)
+    print("per-head merge, G=%d: worst normalised error %.3g" % (group, worst))
+    assert B.tq_get_last_device_error(book) == 0
+
+
 @pytest.mark.parametrize("k_bits,v_bits,qjl", [(2, 1, 128), (5, 4, 128), (4, 2, 128), (2, 3, 0)])
 def test_bit_width_variants(k_bits, v_bits, qjl):
     cfg = dict(n_kv=1, block_size=64, dtype="bf16", seed=5, log_uniform=None, outliers=2, outlier_scale=20.0)
@@ -298,18 +321,22 @@ def test_sixteen_bit_norms_decode(group):
 
 def test_decode_plan_for_the_workloads():
     # the launch plan: the 8B layer merges in the partials kernel (128 groups,
-    # fewer than CTAs), the 70B paged batch (512 groups) takes a merge launch,
-    # and the 4-bit-key long-context layout runs 256-token items (a 512-token
-    # one would not fit two CTAs per SM)
-    expect = {"c2_llama3_8b_decode": (1, 512), "c5_llama3_70b_paged": (0, 512), "c4_long_context": (1, 256)}
-    for name, (fused, chunk) in expect.items():
+    # fewer than CTAs, about four segments each), the 70B paged batch (512
+    # groups) takes a merge launch with a CTA per group, and the long-context
+    # layer (8 groups of about 40 segments) a merge launch with a CTA per
+    # query head; its 4-bit-key layout runs 256-token items (a 512-token one
+    # would not fit two CTAs per SM)
+    expect = {"c2_llama3_8b_decode": (1, 512, 0), "c5_llama3_70b_paged": (0, 512, 512),
+              "c4_long_context": (0, 256, 64)}
+    for name, (fused, chunk, merge_ctas) in expect.items():
         cfg = W.CONFIGS[name]
         book = B.Codebook(k_bits=cfg["k_bits"], v_bits=cfg["v_bits"], qjl_m=cfg["qjl_m"], seed=cfg["seed"],
                           block_size=cfg["block_size"], device=0)
         ctx = W.context_lengths(cfg, cfg["seed"])
         plan = B.tq_decode_plan(book, cfg["batch"], cfg["n_q"], cfg["n_kv"], int(ctx.max()))
         assert plan["tensor_cores"] == 1
-        assert (plan["merge_in_partials"], plan["chunk_tokens"]) == (fused, chunk), (name, plan)
+        assert (plan["merge_in_partials"], plan["chunk_tokens"], plan["merge_ctas"]) == (fused, chunk, merge_ctas), \
+            (name, plan)
         assert 0 < plan["partials_ctas"] <= 2 * torch.cuda.get_device_properties(0).multi_processor_count
 
 
