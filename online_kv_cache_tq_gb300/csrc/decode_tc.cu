@@ -839,12 +839,6 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         cur_group = group;
       }
       ok = wait_phase(&kin, seq & 1, abort, a.error);
-      // this thread's heads: 1/sigma_mse, 1/sigma_qjl, ones_mse, ones_qjl
-      float cst_r[4][HG];
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-#pragma unroll
-        for (int j = 0; j < HG; ++j) cst_r[k][j] = half * HG + j < G ? cst_s[k][half * HG + j] : 0.f;
 
       // thread (lane, half) owns the query heads h with h / HG == half: it turns
       // their accumulators of a key tile into the scaled scores of token lane,
@@ -888,8 +882,10 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           for (int j = 0; j < HG; ++j) {
             const int h = H0 + j;
             if (h >= G) break;
-            const float mse = fmaf(am[j], cst_r[0][j], -cst_r[2][j]);
-            const float qv = qjl ? fmaf(aq[j], cst_r[1][j], -cst_r[3][j]) : 0.f;
+            // (the head's 1/sigma_mse, 1/sigma_qjl, ones_mse, ones_qjl from shared memory: kept in registers
+            // across the key phase they would take sixteen)
+            const float mse = fmaf(am[j], cst_s[0][h], -cst_s[2][h]);
+            const float qv = qjl ? fmaf(aq[j], cst_s[1][h], -cst_s[3][h]) : 0.f;
             const float sc = valid ? a.scale * fmaf(nk, mse, gk * qv) : -INFINITY;
             s0[h * CH + i * kTile + kpos_lane] = sc;   // (in K order: the weights read four at once)
             mx[j] = fmaxf(mx[j], sc);
