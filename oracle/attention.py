@@ -18,12 +18,14 @@
   is not compressed (seo-farm page §4).  This oracle works in the original
   space; rotation invariance (seo-farm §2, R^T R = I) is what lets a kernel
   work in the rotated space instead.
+* A PolarQuant cache (``polar``) holds reconstructible keys and values with no
+  QJL term: the same softmax over <q, x_hat_k> applied to x_hat_v.
 """
 import math
 
 import numpy as np
 
-from . import packing
+from . import packing, polar
 from .quantize import reconstruct_mse
 
 
@@ -45,21 +47,30 @@ def attend(query, khat, qjl_term, vhat, scale):
     return weights @ np.asarray(vhat)
 
 
-def read_sequence(cache, table_row, length, head, block_size):
+def read_sequence(cache, table_row, length, head, block_size, polar_codec=False):
     """Rows of every token-major cache field, and the value codes, for tokens
-    0..length-1 of one sequence/head (value codes as ``v_code_values``)."""
+    0..length-1 of one sequence/head (value codes as ``v_code_values``; a
+    PolarQuant cache keeps its value records token-major)."""
     n_kv = cache["k_norm"].shape[1]
     pos = np.arange(length, dtype=np.int64)
     blocks = np.asarray(table_row, dtype=np.int64)[pos // block_size]
     rows = (blocks * n_kv + head) * block_size + pos % block_size
     out = {}
     for name, arr in cache.items():
-        if name == "v_codes":
+        if name == "v_codes" and not polar_codec:
             out["v_code_values"] = packing.read_value_codes(arr, blocks * block_size + pos % block_size, head)
             continue
         flat = arr.reshape(arr.shape[0] * arr.shape[1] * arr.shape[2], -1)
         out[name] = flat[rows]
     return out
+
+
+def _polar_rows(cache, table_row, length, kv_head, book):
+    """Reconstructed keys and values [length][d] of a PolarQuant cache."""
+    rows = read_sequence(cache, table_row, length, kv_head, cache["k_norm"].shape[2], polar_codec=True)
+    khat = polar.reconstruct(polar.unpack(rows["k_codes"]), rows["k_norm"].reshape(-1), book["rot"])
+    vhat = polar.reconstruct(polar.unpack(rows["v_codes"]), rows["v_norm"].reshape(-1), book["rot"])
+    return khat, vhat
 
 
 def decode_attention_heads(queries, cache, table_row, length, kv_head, book, scale=None):
@@ -70,6 +81,10 @@ def decode_attention_heads(queries, cache, table_row, length, kv_head, book, sca
     d = book["rot"].shape[0]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    if book.get("codec") == "polar":
+        khat, vhat = _polar_rows(cache, table_row, length, kv_head, book)
+        outs = [attend(q, khat, np.zeros(length), vhat, scale) for q in np.asarray(queries, dtype=np.float64)]
+        return np.stack(outs), float(np.max(np.linalg.norm(vhat, axis=1)))
     block_size = cache["k_norm"].shape[2]
     rows = read_sequence(cache, table_row, length, kv_head, block_size)
     k_codes = packing.unpack_planes(rows["k_codes"], book["k_bits"], d)
@@ -96,6 +111,9 @@ def decode_attention(query, cache, table_row, length, kv_head, book, scale=None)
     d = book["rot"].shape[0]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    if book.get("codec") == "polar":
+        khat, vhat = _polar_rows(cache, table_row, length, kv_head, book)
+        return attend(query, khat, np.zeros(length), vhat, scale), float(np.max(np.linalg.norm(vhat, axis=1)))
     block_size = cache["k_norm"].shape[2]
     rows = read_sequence(cache, table_row, length, kv_head, block_size)
     k_codes = packing.unpack_planes(rows["k_codes"], book["k_bits"], d)

@@ -10,7 +10,7 @@ import functools
 
 import numpy as np
 
-from . import attention, codebook, packing, quantize, rotation
+from . import attention, codebook, packing, polar, quantize, rotation
 
 
 @functools.lru_cache(maxsize=None)
@@ -23,9 +23,14 @@ def _matrices(d, m, seed):
     return rotation.rotation_and_projection(d, m, seed)
 
 
-def build(d=128, k_bits=3, v_bits=3, qjl_m=128, seed=0, norm_bits=32):
+def build(d=128, k_bits=3, v_bits=3, qjl_m=128, seed=0, norm_bits=32, codec="turboquant"):
     """The oracle's own R, S and codebooks for one configuration; norm_bits 16
-    stores the norms (and the residual norm) as float16, 32 as float32."""
+    stores the norms (and the residual norm) as float16, 32 as float32.
+    codec "polar": keys and values coded by PolarQuant (``polar``), no
+    codebooks and no QJL; R is the same seeded draw."""
+    if codec == "polar":
+        rot, proj = _matrices(d, 0, seed)
+        return {"codec": "polar", "d": d, "qjl_m": 0, "rot": rot, "proj": proj, "norm_dtype": np.float32}
     k_mse_bits = k_bits - 1 if qjl_m else k_bits
     rot, proj = _matrices(d, qjl_m, seed)
     k_levels, k_bounds = _levels(d, k_mse_bits)
@@ -39,9 +44,17 @@ def build(d=128, k_bits=3, v_bits=3, qjl_m=128, seed=0, norm_bits=32):
     }
 
 
+def _encode_polar(x, book, prefix):
+    codes, radius, margins, y = polar.encode_vectors(x, book["rot"])
+    return {prefix + "_codes": polar.pack(codes), prefix + "_norm": radius, "codes": codes, "margins": margins,
+            "y": y}
+
+
 def encode_keys(x, book):
     """Key rows: dict of packed codes, sign bits, norm, residual norm, plus the
     fp64 intermediates (unit rotated y, projected residual z) for acceptance."""
+    if book.get("codec") == "polar":
+        return _encode_polar(x, book, "k")
     nd = book.get("norm_dtype", np.float32)
     norm, y, codes = quantize.encode_mse(x, book["rot"], book["k_bounds"], nd)
     out = {"k_codes": packing.pack_planes(codes, book["k_bits"]), "k_norm": norm,
@@ -54,6 +67,8 @@ def encode_keys(x, book):
 
 def encode_values(x, book):
     """Value rows: packed codes and norm (plus fp64 intermediates)."""
+    if book.get("codec") == "polar":
+        return _encode_polar(x, book, "v")
     norm, y, codes = quantize.encode_mse(x, book["rot"], book["v_bounds"], book.get("norm_dtype", np.float32))
     return {"v_codes": packing.pack_planes(codes, book["v_bits"]), "v_norm": norm,
             "codes": codes, "y": y}
@@ -62,6 +77,8 @@ def encode_values(x, book):
 def field_bytes(book):
     """Bytes per (token, head) of each cache field."""
     d = book["d"]
+    if book.get("codec") == "polar":
+        return {"k_codes": polar.RECORD_BYTES, "k_norm": 4, "v_codes": polar.RECORD_BYTES, "v_norm": 4}
     nb = np.dtype(book.get("norm_dtype", np.float32)).itemsize
     out = {"k_codes": book["k_bits"] * d // 8, "k_norm": nb,
            "v_codes": book["v_bits"] * d // 8, "v_norm": nb}
@@ -74,7 +91,7 @@ def field_bytes(book):
 def empty_cache(book, num_blocks, n_kv_heads, block_size):
     cache = {}
     for name, nbytes in field_bytes(book).items():
-        if name == "v_codes":
+        if name == "v_codes" and book.get("codec") != "polar":
             cache[name] = np.zeros((num_blocks, n_kv_heads, book["v_bits"], book["d"], block_size // 8),
                                    dtype=np.uint8)
         elif name.endswith("norm"):
@@ -93,12 +110,14 @@ def append(cache, book, k, v, slots):
     n_tok = k.shape[0]
     keys = encode_keys(k.reshape(n_tok * n_kv, -1), book)
     vals = encode_values(v.reshape(n_tok * n_kv, -1), book)
+    polar_codec = book.get("codec") == "polar"
     live = [t for t in range(n_tok) if slots[t] >= 0]
-    for h in range(n_kv):
-        codes = vals["codes"].reshape(n_tok, n_kv, -1)[live, h]
-        packing.write_value_codes(cache["v_codes"], codes, np.asarray(slots)[live], h)
+    if not polar_codec:
+        for h in range(n_kv):
+            codes = vals["codes"].reshape(n_tok, n_kv, -1)[live, h]
+            packing.write_value_codes(cache["v_codes"], codes, np.asarray(slots)[live], h)
     for name in field_bytes(book):
-        if name == "v_codes":
+        if name == "v_codes" and not polar_codec:
             continue
         src = (keys if name.startswith("k_") else vals)[name]
         src = src.reshape(n_tok, n_kv, *src.shape[1:])
