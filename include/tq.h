@@ -61,7 +61,17 @@ typedef enum { TQ_BF16 = 0, TQ_FP32 = 1 } tq_dtype;
  * norm and, for keys, the residual norm): 32 (or 0) for float32, 16 for
  * float16, which saves 6 of the 108 bytes of a (token, head) at 3/3 bits;
  * the key residual is then taken against the float16 norm, the value the
- * decoder reconstructs. */
+ * decoder reconstructs.  codec: TQ_CODEC_TURBOQUANT (0) for the stage above,
+ * or TQ_CODEC_POLAR (1) for PolarQuant, the alternative stage 1 of the
+ * intelliparadigm.com page (§2.1.1 step 2): after the same rotation,
+ * coordinates are paired into (radius, angle) level after level, every angle
+ * rounded to a multiple of pi/12, the final radius kept; keys and values are
+ * both coded so (k_bits and v_bits are ignored), qjl_m must be 0 and norms
+ * are float32.  A PolarQuant record is 64 bytes (64 level-1 codes 0..23 x 5
+ * bits, then the 63 codes of levels 2..7, 0..6, x 3 bits, one little-endian
+ * bit stream), token-major for values too. */
+typedef enum { TQ_CODEC_TURBOQUANT = 0, TQ_CODEC_POLAR = 1 } tq_codec;
+
 typedef struct {
   int d;
   int k_bits;
@@ -70,6 +80,7 @@ typedef struct {
   uint64_t seed;
   int block_size;
   int norm_bits;
+  int codec;
 } tq_config;
 
 typedef struct tq_codebook tq_codebook; /* opaque, library-owned */

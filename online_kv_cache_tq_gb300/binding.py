@@ -15,6 +15,8 @@ from . import build as _build
 TQ_OK = 0
 TQ_BF16 = 0
 TQ_FP32 = 1
+TQ_CODEC_TURBOQUANT = 0
+TQ_CODEC_POLAR = 1
 STATUS_NAMES = {0: "TQ_OK", 1: "TQ_ERR_INVALID_ARG", 2: "TQ_ERR_UNSUPPORTED", 3: "TQ_ERR_CUDA",
                 4: "TQ_ERR_OOM", 5: "TQ_ERR_WORKSPACE", 6: "TQ_ERR_DEVICE"}
 FIELDS = ("k_codes", "k_qjl", "k_norm", "k_rnorm", "v_codes", "v_norm")
@@ -39,7 +41,7 @@ class TQError(RuntimeError):
 class tq_config(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("k_bits", ctypes.c_int), ("v_bits", ctypes.c_int),
                 ("qjl_m", ctypes.c_int), ("seed", ctypes.c_uint64), ("block_size", ctypes.c_int),
-                ("norm_bits", ctypes.c_int)]
+                ("norm_bits", ctypes.c_int), ("codec", ctypes.c_int)]
 
 
 class tq_cache_view(ctypes.Structure):
@@ -144,8 +146,9 @@ def _stream(stream):
 class Codebook:
     """Owner of a tq_codebook handle."""
 
-    def __init__(self, d=128, k_bits=3, v_bits=3, qjl_m=128, seed=0, block_size=64, device=0, norm_bits=32):
-        self.config = tq_config(d, k_bits, v_bits, qjl_m, seed, block_size, norm_bits)
+    def __init__(self, d=128, k_bits=3, v_bits=3, qjl_m=128, seed=0, block_size=64, device=0, norm_bits=32,
+                 codec=0):
+        self.config = tq_config(d, k_bits, v_bits, qjl_m, seed, block_size, norm_bits, codec)
         self.device = device
         self.handle = tq_codebook_build(self.config, device)
 
@@ -171,6 +174,10 @@ class Codebook:
     @property
     def norm_bits(self):
         return 16 if self.config.norm_bits == 16 else 32
+
+    @property
+    def codec(self):
+        return self.config.codec
 
 
 def tq_codebook_build(config, device=0):

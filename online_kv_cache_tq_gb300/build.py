@@ -18,7 +18,7 @@ LIB_DIR = os.path.join(PKG_DIR, "_lib")
 OBJ_DIR = os.path.join(LIB_DIR, "obj")
 LIB_PATH = os.path.join(LIB_DIR, "libtq.so")
 
-SOURCES = ["api.cu", "quantize_tc.cu", "vector_kernels.cu", "decode.cu", "decode_tc.cu", "decode_static.cu", "monitor.cu", "host_builder.cpp"]
+SOURCES = ["api.cu", "quantize_tc.cu", "vector_kernels.cu", "decode.cu", "decode_tc.cu", "decode_static.cu", "monitor.cu", "polar.cu", "host_builder.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

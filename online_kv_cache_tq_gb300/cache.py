@@ -16,7 +16,10 @@ def allocate_cache(book, num_blocks, n_kv_heads, device="cuda"):
     for name, nbytes in sizes.items():
         if nbytes == 0:
             continue
-        if name == "v_codes":
+        if name == "v_codes" and getattr(book, "codec", 0) == binding.TQ_CODEC_POLAR:
+            # PolarQuant records are token-major for values too
+            cache[name] = torch.zeros((num_blocks, n_kv_heads, bs, nbytes), dtype=torch.uint8, device=device)
+        elif name == "v_codes":
             # token-transposed inside a block: [block][head][plane][coordinate][block_size / 8]
             bits = nbytes * 8 // 128
             cache[name] = torch.zeros((num_blocks, n_kv_heads, bits, 128, bs // 8), dtype=torch.uint8, device=device)

@@ -178,7 +178,7 @@ tq_status upload_tables(tq_codebook* b) {
     t.v_bounds[i] = i < static_cast<int>(h.v_bounds.size()) ? static_cast<float>(h.v_bounds[i]) : INFINITY;
   }
   b->walsh_ok = walsh_coefficients(h.k_levels, b->k_mse_bits, t.k_walsh) &&
-                walsh_coefficients(h.v_levels, b->v_bits, t.v_walsh);
+                walsh_coefficients(h.v_levels, b->v_bits, t.v_walsh) && !b->polar;
   std::vector<tq::DeviceTables> tv(1, t);
   std::vector<int> zero(1, 0);
   cudaError_t err = upload(&b->d_R, R);
@@ -244,8 +244,14 @@ tq_status tq_codebook_build(const tq_config* cfg, int device, tq_codebook** out)
   if (cfg->d <= 0 || cfg->d % 8 != 0 || cfg->d > 1024 || cfg->block_size <= 0) return TQ_ERR_INVALID_ARG;
   if (cfg->qjl_m < 0 || cfg->qjl_m % 8 != 0 || cfg->qjl_m > 1024) return TQ_ERR_INVALID_ARG;
   if (cfg->norm_bits != 0 && cfg->norm_bits != 16 && cfg->norm_bits != 32) return TQ_ERR_INVALID_ARG;
-  const int k_mse = cfg->qjl_m > 0 ? cfg->k_bits - 1 : cfg->k_bits;
-  if (k_mse < 1 || k_mse > 4 || cfg->v_bits < 1 || cfg->v_bits > 4) return TQ_ERR_UNSUPPORTED;
+  if (cfg->codec != TQ_CODEC_TURBOQUANT && cfg->codec != TQ_CODEC_POLAR) return TQ_ERR_INVALID_ARG;
+  const bool polar = cfg->codec == TQ_CODEC_POLAR;
+  // PolarQuant: no codebooks and no QJL bits, float32 radii, a power-of-two
+  // head dimension (the pairing levels); the handle still draws R
+  if (polar && (cfg->qjl_m != 0 || cfg->norm_bits == 16 || (cfg->d & (cfg->d - 1)) != 0)) return TQ_ERR_UNSUPPORTED;
+  const int k_mse = polar ? 1 : cfg->qjl_m > 0 ? cfg->k_bits - 1 : cfg->k_bits;
+  const int v_mse = polar ? 1 : cfg->v_bits;
+  if (k_mse < 1 || k_mse > 4 || v_mse < 1 || v_mse > 4) return TQ_ERR_UNSUPPORTED;
   if (!host_only && (cfg->d != tq::kDim || (cfg->qjl_m != 0 && cfg->qjl_m != tq::kDim))) return TQ_ERR_UNSUPPORTED;
   if (!host_only && cfg->block_size % 32 != 0) return TQ_ERR_UNSUPPORTED;
   tq_codebook* b = new (std::nothrow) tq_codebook();
@@ -253,10 +259,11 @@ tq_status tq_codebook_build(const tq_config* cfg, int device, tq_codebook** out)
   b->cfg = *cfg;
   b->device = host_only ? -1 : device;
   b->k_mse_bits = k_mse;
-  b->v_bits = cfg->v_bits;
+  b->v_bits = v_mse;
   b->norm16 = cfg->norm_bits == 16;
+  b->polar = polar;
   try {
-    tq::build_host_tables(cfg->d, cfg->qjl_m, cfg->seed, k_mse, cfg->v_bits, &b->host);
+    tq::build_host_tables(cfg->d, cfg->qjl_m, cfg->seed, k_mse, v_mse, &b->host);
   } catch (const std::bad_alloc&) {
     delete b;
     return TQ_ERR_OOM;
@@ -291,6 +298,7 @@ tq_status tq_codebook_destroy(tq_codebook* book) {
 
 tq_status tq_codebook_levels(const tq_codebook* book, int which, double* levels, double* bounds, int* bits) {
   if (book == nullptr || (which != 0 && which != 1)) return TQ_ERR_INVALID_ARG;
+  if (book->polar) return TQ_ERR_UNSUPPORTED;     // (PolarQuant has no codebook)
   const std::vector<double>& lv = which == 0 ? book->host.k_levels : book->host.v_levels;
   const std::vector<double>& bd = which == 0 ? book->host.k_bounds : book->host.v_bounds;
   if (levels) std::memcpy(levels, lv.data(), lv.size() * sizeof(double));
@@ -310,6 +318,13 @@ tq_status tq_cache_field_bytes(const tq_codebook* book, size_t bytes_per_item[6]
   if (book == nullptr || bytes_per_item == nullptr) return TQ_ERR_INVALID_ARG;
   const size_t d = static_cast<size_t>(book->cfg.d);
   const bool qjl = book->cfg.qjl_m > 0;
+  if (book->polar) {
+    // a 64-byte record at d = 128 (d/2 angles x 5 bits + d/2 - 1 angles x 3 bits, rounded up to 16 bytes)
+    const size_t rec = ((d / 2 * 5 + (d / 2 - 1) * 3 + 127) / 128) * 16;
+    const size_t items[6] = {rec, 0, 4, 0, rec, 4};
+    std::memcpy(bytes_per_item, items, sizeof(items));
+    return TQ_OK;
+  }
   bytes_per_item[0] = book->k_mse_bits * d / 8;
   bytes_per_item[1] = qjl ? static_cast<size_t>(book->cfg.qjl_m) / 8 : 0;
   const size_t nb = book->norm16 ? 2 : 4;
@@ -374,6 +389,11 @@ tq_status append_args(const tq_codebook* book, const void* k, const void* v, tq_
 // Launch a validated append (either tensor may be absent).
 tq_status run_append(const tq_codebook* book, const void* k, const void* v, const tq::QuantizeArgs& ka,
                      const tq::QuantizeArgs& va, bool bf16, cudaStream_t s) {
+  if (book->polar) {
+    if (k && tq::launch_polar_quantize(ka, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;
+    if (v && tq::launch_polar_quantize(va, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;
+    return TQ_OK;
+  }
   if (ka.n_vec <= tq::kSmallQuantize) {
     // a decode step: keys and values in one launch, one CTA per vector
     return tq::launch_quantize_small(k ? &ka : nullptr, v ? &va : nullptr, bf16, s) == cudaSuccess ? TQ_OK
@@ -402,6 +422,7 @@ tq_status tq_reconstruction_error(const tq_codebook* book, const void* x, tq_dty
                                   int n_kv_heads, const int64_t* slot_mapping, const tq_cache_view* cache,
                                   double* stats, void* stream) {
   if (which != 0 && which != 1) return TQ_ERR_INVALID_ARG;
+  if (book != nullptr && book->polar) return TQ_ERR_UNSUPPORTED;   // (stage-1 reconstructions of Lloyd-Max codes)
   if (n_tokens > 0 && (slot_mapping == nullptr || x == nullptr || stats == nullptr)) return TQ_ERR_INVALID_ARG;
   if (stats != nullptr && (reinterpret_cast<uintptr_t>(stats) & 7u) != 0) return TQ_ERR_INVALID_ARG;
   tq::QuantizeArgs ka{}, va{};
@@ -543,6 +564,7 @@ tq_status decode_args(const tq_codebook* book, int stages, const void* q, tq_dty
   a->tables = book->d_tables;
   a->error = book->d_error;
   a->num_sms = book->num_sms;
+  a->polar = book->polar;
   // with an output, the tensor-core path either merges in the partials kernel
   // (few groups per CTA) or in a dependent merge launch (see launch_partials_and_merge)
   a->merge_in_partials = (stages & kPartials) && out != nullptr && tq::tc_decode_supported(*a, book->walsh_ok) &&
@@ -646,7 +668,7 @@ tq_status step_args(const tq_codebook* book, const void* k_new, const void* v_ne
 tq_status run_step_prepare(const tq_codebook* book, const void* k_new, const void* v_new, bool kv_bf16,
                            const tq::QuantizeArgs& ka, const tq::QuantizeArgs& va, const tq::DecodeArgs& a,
                            bool q_bf16, cudaStream_t s, bool* fused) {
-  *fused = ka.n_vec <= tq::kSmallQuantize;
+  *fused = ka.n_vec <= tq::kSmallQuantize && !book->polar;
   if (*fused) return launched(tq::launch_step_prep(ka, va, kv_bf16, a, q_bf16, s));
   tq_status st = run_append(book, k_new, v_new, ka, va, kv_bf16, s);
   if (st == TQ_OK) st = launched(tq::launch_decode_prepare(a, q_bf16, s));

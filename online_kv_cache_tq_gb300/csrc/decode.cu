@@ -238,6 +238,7 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(DecodeArgs a) {
 }  // namespace
 
 cudaError_t launch_decode_partials(const DecodeArgs& args, cudaStream_t stream) {
+  if (args.polar) return launch_polar_partials(args, stream);
   if (args.batch <= 0 || args.max_chunks <= 0) return cudaSuccess;
   dim3 grid(args.max_chunks, args.n_kv, args.batch);
   switch (args.group) {

@@ -124,6 +124,7 @@ struct DecodeArgs {
   const DeviceTables* tables;
   int* error;
   int num_sms;              // of the handle's device
+  bool polar;               // PolarQuant records (polar.cu) instead of Lloyd-Max codes
 };
 
 // Word (uint32 units) of a token-transposed codes field holding plane p,
@@ -169,6 +170,12 @@ cudaError_t launch_monitor(const QuantizeArgs& args, bool bf16, double* stats, c
 cudaError_t launch_step_prep(const QuantizeArgs& ka, const QuantizeArgs& va, bool kv_bf16, const DecodeArgs& da,
                              bool q_bf16, cudaStream_t stream);
 cudaError_t launch_decode_partials(const DecodeArgs& args, cudaStream_t stream);
+
+// PolarQuant codec (polar.cu): records of keys or values (args.codes: 64 bytes
+// per item, args.norm: the float32 final radius), and the split-K partials of
+// a PolarQuant cache in the CUDA-core kernel's entry layout.
+cudaError_t launch_polar_quantize(const QuantizeArgs& args, bool bf16, cudaStream_t stream);
+cudaError_t launch_polar_partials(const DecodeArgs& args, cudaStream_t stream);
 
 // Tensor-core partials (fp8 sign planes, decode_tc.cu) for the shapes it
 // supports: G in {1, 2, 4, 8}, tensor-memory columns within 512, and

@@ -1,0 +1,383 @@
+// PolarQuant (the intelliparadigm.com page, §2.1.1 step 2) as an alternative
+// stage-1 codec.  After the rotation y = R x, adjacent coordinates are paired,
+// each pair becomes a radius and an angle, the angle is rounded to the nearest
+// multiple of pi/12 (24 sectors), and the radii are paired again, level after
+// level, until the vector's norm is left.
+//
+// Record of a head vector (64 bytes, one little-endian bit stream): the 64
+// level-1 codes (0..23) x 5 bits, then the 63 codes of levels 2..7 (0..6,
+// both members of a pair are radii) x 3 bits; the final radius is the norm
+// field (float32).  Keys and values are coded alike and carry no QJL bits.
+//
+// Quantize: 256 threads take four vectors; thread (o, h) forms y_o of
+// vectors 2h and 2h + 1 from column o of R^T (every load serves both), then
+// pairs coordinates with warp shuffles (levels 1..5) and through shared
+// memory (levels 6 and 7), and 16 threads per vector pack the record.
+// Decode: one CTA per (512-token chunk, KV head, sequence), like the CUDA-core
+// decode; per 32-token tile, eight threads per token expand its record
+// top-down into the 128 rotated coordinates (16 each), the G scores
+// <q_rot, y_hat> follow from shared memory, then the values the same way with
+// the softmax weights; the partial (m, l, acc) goes to the merge that
+// back-rotates (seo-farm page §2: out = R^T o_rot).
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+
+namespace tq {
+namespace {
+
+constexpr int kPThreads = 256;
+constexpr int kPVecs = 4;               // vectors per quantize block
+constexpr int kRecordWords = 16;        // 64-byte record
+constexpr int kUpperBit = 320;          // first bit of the level-2..7 codes
+constexpr int kPTile = 32;              // tokens per decode tile
+constexpr float kSectorsPerRadian = 3.8197186342054881f;   // 12 / pi
+
+// Index of the first level-L code (L = 2..7) among the 63 upper codes.
+__device__ __forceinline__ int upper_offset(int level) { return 64 - (128 >> (level - 1)); }
+
+// Rounded multiple of pi/12 of the angle of (first, second); level 1 angles
+// span (-pi, pi] and are taken modulo 24, upper levels lie in [0, pi/2].
+__device__ __forceinline__ int angle_code(float second, float first, bool level1) {
+  const int k = __float2int_rn(atan2f(second, first) * kSectorsPerRadian);   // (half to even)
+  return level1 ? (k + 24) % 24 : k;
+}
+
+__device__ __forceinline__ float load_x(const void* base, long long idx, bool bf16) {
+  if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
+  return reinterpret_cast<const float*>(base)[idx];
+}
+
+__global__ void __launch_bounds__(kPThreads) polar_quantize_kernel(QuantizeArgs a, bool bf16) {
+  __shared__ __align__(16) float x_s[kPVecs][kDim];
+  __shared__ float r5_s[kPVecs][4];             // level-5 radii, one per 32 coordinates
+  __shared__ float rad_s[kPVecs];
+  __shared__ uint8_t c1_s[kPVecs][64];          // level-1 codes
+  __shared__ uint8_t cu_s[kPVecs][64];          // levels 2..7 (63 codes)
+  const int t = threadIdx.x, o = t & (kDim - 1), hv = t >> 7;
+  const int lane = t & 31, quarter = o >> 5;
+  const int v0 = blockIdx.x * kPVecs;
+  for (int i = t; i < kPVecs * kDim; i += kPThreads) {
+    const int j = i >> 7;
+    x_s[j][i & 127] = v0 + j < a.n_vec ? load_x(a.x, static_cast<long long>(v0) * kDim + i, bf16) : 0.f;
+  }
+  __syncthreads();
+  // y_o = sum_i R[o][i] x_i of vectors 2 hv and 2 hv + 1, 32 loads of R^T in flight
+  float y[2] = {0.f, 0.f};
+  const float* w = a.Rt + o;
+#pragma unroll
+  for (int i0 = 0; i0 < kDim; i0 += 32) {
+    float r[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) r[k] = __ldg(w + (i0 + k) * kDim);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      y[0] = fmaf(r[k], x_s[2 * hv][i0 + k], y[0]);
+      y[1] = fmaf(r[k], x_s[2 * hv + 1][i0 + k], y[1]);
+    }
+  }
+  // levels 1..5 in the warp: before level L the radius of node o >> (L - 1)
+  // sits at lanes o with o % 2^(L-1) == 0; the lane of the first member pairs it
+  // with the second, 2^(L-1) lanes up
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int vi = 2 * hv + e;
+    float rho = y[e];
+#pragma unroll
+    for (int lvl = 1; lvl <= 5; ++lvl) {
+      const int step = 1 << (lvl - 1);
+      const float second = __shfl_xor_sync(0xffffffffu, rho, step);
+      if ((o & (2 * step - 1)) == 0) {
+        const int code = angle_code(second, rho, lvl == 1);
+        if (lvl == 1) c1_s[vi][o >> 1] = static_cast<uint8_t>(code);
+        else cu_s[vi][upper_offset(lvl) + (o >> lvl)] = static_cast<uint8_t>(code);
+      }
+      rho = sqrtf(fmaf(rho, rho, second * second));
+    }
+    if (lane == 0) r5_s[vi][quarter] = rho;
+  }
+  __syncthreads();
+  // levels 6 and 7 of this half's two vectors
+  if (o == 0) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int vi = 2 * hv + e;
+      const float a0 = r5_s[vi][0], a1 = r5_s[vi][1], a2 = r5_s[vi][2], a3 = r5_s[vi][3];
+      cu_s[vi][60] = static_cast<uint8_t>(angle_code(a1, a0, false));
+      cu_s[vi][61] = static_cast<uint8_t>(angle_code(a3, a2, false));
+      const float r60 = sqrtf(fmaf(a0, a0, a1 * a1)), r61 = sqrtf(fmaf(a2, a2, a3 * a3));
+      cu_s[vi][62] = static_cast<uint8_t>(angle_code(r61, r60, false));
+      rad_s[vi] = sqrtf(fmaf(r60, r60, r61 * r61));
+    }
+  }
+  __syncthreads();
+  // pack: thread (vector vi, word wd) builds bits 32 wd .. 32 wd + 31 of the record
+  if (t < kPVecs * kRecordWords) {
+    const int vi = t >> 4, wd = t & 15;
+    const int v = v0 + vi;
+    if (v < a.n_vec) {
+      uint32_t word = 0;
+#pragma unroll 4
+      for (int bit = 0; bit < 32; ++bit) {
+        const int pos = 32 * wd + bit;
+        int val = 0;
+        if (pos < kUpperBit) {
+          val = (c1_s[vi][pos / 5] >> (pos % 5)) & 1;
+        } else if (pos < kUpperBit + 3 * 63) {
+          const int k = pos - kUpperBit;
+          val = (cu_s[vi][k / 3] >> (k % 3)) & 1;
+        }
+        word |= static_cast<uint32_t>(val) << bit;
+      }
+      const int token = v / a.n_kv, head = v - token * a.n_kv;
+      const long long slot = slot_of(a, token);
+      const long long cache_rows = static_cast<long long>(a.num_blocks) * a.block_size;
+      if (slot >= cache_rows) {
+        if (wd == 0) atomicCAS(a.error, 0, kErrSlot);
+      } else if (slot >= 0) {
+        const long long blk = slot / a.block_size;
+        const long long row = (blk * a.n_kv + head) * a.block_size + (slot - blk * a.block_size);
+        reinterpret_cast<uint32_t*>(a.codes + row * (4 * kRecordWords))[wd] = word;
+        if (wd == 0) reinterpret_cast<float*>(a.norm)[row] = rad_s[vi];
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ int chunk_context(const DecodeArgs& a, int b) {
+  int ctx = a.context_lens[b];
+  const int cap = min(a.max_context, a.max_blocks * a.block_size);
+  if (ctx < 0 || ctx > cap) {
+    atomicCAS(a.error, 0, kErrContext);
+    ctx = ctx < 0 ? 0 : cap;
+  }
+  return ctx;
+}
+
+// The `width` bits of a record row (kRecordWords + 1 words, the last 0) at bit `pos`.
+__device__ __forceinline__ int record_bits(const uint32_t* rec, int pos, int width) {
+  return static_cast<int>(__funnelshift_r(rec[pos >> 5], rec[(pos >> 5) + 1], pos & 31) & ((1u << width) - 1u));
+}
+
+// Level L (4..1) of the expansion of a part's subtree: its 2^(4-L) node radii
+// in v[0 ..] become the 2^(5-L) radii of level L - 1 (cos for the first member
+// of a pair, sin for the second), highest node first so that no radius is
+// overwritten before it is read.
+template <int L>
+__device__ __forceinline__ void expand_level(const uint32_t* rec, int part, const float* cos_s, const float* sin_s,
+                                             float (&v)[16]) {
+  constexpr int nodes = 1 << (4 - L);
+#pragma unroll
+  for (int k = nodes - 1; k >= 0; --k) {
+    const int node = part * nodes + k;
+    const int c = L == 1 ? record_bits(rec, 5 * node, 5) : record_bits(rec, kUpperBit + 3 * (upper_offset(L) + node), 3);
+    const float parent = v[k];
+    v[2 * k] = parent * cos_s[c];
+    v[2 * k + 1] = parent * sin_s[c];
+  }
+}
+
+// Rotated coordinates 16 part .. 16 part + 15 of one record: the three
+// ancestors above the part's subtree (levels 7, 6, 5), then its subtree
+// expanded level by level down to the coordinates.
+__device__ __forceinline__ void expand_part(const uint32_t* rec, float radius, int part, const float* cos_s,
+                                            const float* sin_s, float (&v)[16]) {
+  float r = radius;
+#pragma unroll
+  for (int lvl = 7; lvl >= 5; --lvl) {
+    const int node = part >> (lvl - 4);                 // pair index at this level
+    const int c = record_bits(rec, kUpperBit + 3 * (upper_offset(lvl) + node), 3);
+    r *= ((part >> (lvl - 5)) & 1) ? sin_s[c] : cos_s[c];
+  }
+  v[0] = r;
+  expand_level<4>(rec, part, cos_s, sin_s, v);
+  expand_level<3>(rec, part, cos_s, sin_s, v);
+  expand_level<2>(rec, part, cos_s, sin_s, v);
+  expand_level<1>(rec, part, cos_s, sin_s, v);
+}
+
+template <int G>
+__global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a) {
+  const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int t = threadIdx.x;
+  const int ctx = chunk_context(a, b);
+  const int qbase = b * a.n_q + kvh * G;
+  // one partial entry per chunk: entry (query head, chunk) of a [.][max_chunks] array
+  if (chunk == 0 && t < G) a.ws_seg[qbase + t] = SegInfo{(qbase + t) * a.max_chunks, (ctx + kChunk - 1) / kChunk, 1, 0};
+  const int start = chunk * kChunk;
+  if (start >= ctx) return;
+  const int n_local = min(kChunk, ctx - start);
+
+  __shared__ __align__(16) float q_s[G][kDim];
+  __shared__ float y_s[kDim][kPTile + 1];      // one tile's decoded vectors, coordinate-major
+  __shared__ float p_s[G][kChunk];             // scores, then softmax weights
+  __shared__ uint32_t rec_s[kPTile][kRecordWords + 1];
+  __shared__ float rad_s[kPTile];
+  __shared__ long long row_s[kChunk];
+  __shared__ float cos_s[24], sin_s[24];
+  __shared__ float red_s[kPThreads / 32][G];
+  __shared__ float stat_s[2][G];
+
+  for (int i = t; i < G * kDim; i += kPThreads) q_s[i / kDim][i % kDim] = a.ws_q[static_cast<long long>(qbase + i / kDim) * 2 * kDim + i % kDim];
+  if (t < 24) {
+    cos_s[t] = cospif(t / 12.f);
+    sin_s[t] = sinpif(t / 12.f);
+  }
+  for (int tl = t; tl < kChunk; tl += kPThreads) {
+    long long row = -1;
+    if (tl < n_local) {
+      const int tok = start + tl;
+      const int lblk = tok / a.block_size;
+      const long long phys = a.block_table ? a.block_table[static_cast<long long>(b) * a.max_blocks + lblk]
+                                           : static_cast<long long>(b) * a.max_blocks + lblk;
+      if (phys >= 0 && phys < a.num_blocks) {
+        row = (phys * a.n_kv + kvh) * a.block_size + (tok - lblk * a.block_size);
+      } else {
+        atomicCAS(a.error, 0, kErrBlock);
+      }
+    }
+    row_s[tl] = row;
+  }
+  __syncthreads();
+
+  const int tok_i = t >> 3, part = t & 7;      // expansion: token of the tile, 16-coordinate part
+  const int n_tiles = (n_local + kPTile - 1) / kPTile;
+  // one tile's records into rec_s and radii into rad_s (invalid tokens: radius 0)
+  auto load_tile = [&](const uint8_t* codes, const void* norms, int tile) {
+    const long long row = row_s[tile * kPTile + tok_i];
+    uint2 wv = make_uint2(0u, 0u);
+    if (row >= 0) wv = reinterpret_cast<const uint2*>(codes + row * (4 * kRecordWords))[part];
+    rec_s[tok_i][2 * part] = wv.x;
+    rec_s[tok_i][2 * part + 1] = wv.y;
+    if (part == 0) {
+      rec_s[tok_i][kRecordWords] = 0u;
+      rad_s[tok_i] = row >= 0 ? reinterpret_cast<const float*>(norms)[row] : 0.f;
+    }
+  };
+  auto expand_tile = [&]() {
+    float v[16];
+    expand_part(rec_s[tok_i], rad_s[tok_i], part, cos_s, sin_s, v);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) y_s[16 * part + k][tok_i] = v[k];
+  };
+
+  // ---- scores: s = scale <q_rot, y_hat_k> per (token, head) ----
+  for (int tile = 0; tile < n_tiles; ++tile) {
+    load_tile(a.k_codes, a.k_norm, tile);
+    __syncthreads();
+    expand_tile();
+    __syncthreads();
+    const int i = t & (kPTile - 1);
+    for (int h = t / kPTile; h < G; h += kPThreads / kPTile) {
+      float s = 0.f;
+#pragma unroll 8
+      for (int j = 0; j < kDim; ++j) s = fmaf(q_s[h][j], y_s[j][i], s);
+      const int tl = tile * kPTile + i;
+      if (tl < kChunk) p_s[h][tl] = tl < n_local && row_s[tl] >= 0 ? a.scale * s : -INFINITY;
+    }
+    __syncthreads();
+  }
+
+  // ---- softmax over the chunk: per-head max, weights e^(s - m), their sum ----
+  const int lane = t & 31, warp = t >> 5;
+  float part_v[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float m = -INFINITY;
+    for (int tl = t; tl < n_local; tl += kPThreads) m = fmaxf(m, p_s[h][tl]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    part_v[h] = m;
+  }
+  if (lane == 0)
+#pragma unroll
+    for (int h = 0; h < G; ++h) red_s[warp][h] = part_v[h];
+  __syncthreads();
+  if (t < G) {
+    float m = -INFINITY;
+    for (int w = 0; w < kPThreads / 32; ++w) m = fmaxf(m, red_s[w][t]);
+    stat_s[0][t] = m;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const float m = stat_s[0][h];
+    float l = 0.f;
+    for (int tl = t; tl < n_local; tl += kPThreads) {
+      const float s = p_s[h][tl];
+      const float e = s == -INFINITY || m == -INFINITY ? 0.f : __expf(s - m);
+      p_s[h][tl] = e;
+      l += e;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    part_v[h] = l;
+  }
+  __syncthreads();                              // red_s was read above
+  if (lane == 0)
+#pragma unroll
+    for (int h = 0; h < G; ++h) red_s[warp][h] = part_v[h];
+  __syncthreads();
+  if (t < G) {
+    float l = 0.f;
+    for (int w = 0; w < kPThreads / 32; ++w) l += red_s[w][t];
+    stat_s[1][t] = l;
+  }
+
+  // ---- values: acc[h][j] = sum_t w[h][t] y_hat_v[t][j]; thread (j, half) takes heads h % 2 == half ----
+  const int j = t & (kDim - 1), hf = t >> 7;
+  constexpr int HH = (G + 1) / 2;
+  float acc[HH];
+#pragma unroll
+  for (int k = 0; k < HH; ++k) acc[k] = 0.f;
+  for (int tile = 0; tile < n_tiles; ++tile) {
+    load_tile(a.v_codes, a.v_norm, tile);
+    __syncthreads();
+    expand_tile();
+    __syncthreads();
+    const int n_in = min(kPTile, n_local - tile * kPTile);
+    for (int i = 0; i < n_in; ++i) {
+      const float yv = y_s[j][i];
+#pragma unroll
+      for (int k = 0; k < HH; ++k) {
+        const int h = 2 * k + hf;
+        if (h < G) acc[k] = fmaf(p_s[h][tile * kPTile + i], yv, acc[k]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int k = 0; k < HH; ++k) {
+    const int h = 2 * k + hf;
+    if (h >= G) continue;
+    float* part_p = a.ws_part + (static_cast<long long>(qbase + h) * a.max_chunks + chunk) * kPartStride;
+    part_p[4 + j] = acc[k];
+    if (j == 0) {
+      part_p[0] = stat_s[0][h];
+      part_p[1] = stat_s[1][h];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_polar_quantize(const QuantizeArgs& a, bool bf16, cudaStream_t stream) {
+  if (a.n_vec <= 0) return cudaSuccess;
+  polar_quantize_kernel<<<(a.n_vec + kPVecs - 1) / kPVecs, kPThreads, 0, stream>>>(a, bf16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_polar_partials(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.batch <= 0 || a.max_chunks <= 0) return cudaSuccess;
+  dim3 grid(a.max_chunks, a.n_kv, a.batch);
+  switch (a.group) {
+    case 1: polar_attention_kernel<1><<<grid, kPThreads, 0, stream>>>(a); break;
+    case 2: polar_attention_kernel<2><<<grid, kPThreads, 0, stream>>>(a); break;
+    case 4: polar_attention_kernel<4><<<grid, kPThreads, 0, stream>>>(a); break;
+    case 8: polar_attention_kernel<8><<<grid, kPThreads, 0, stream>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace tq

@@ -75,5 +75,6 @@ struct tq_codebook {
   CUtensorMap w_map;  // TMA map of d_rot_tc as [512][128] bf16
   bool walsh_ok;      // both codebooks are exactly odd-symmetric (sign-plane decode usable)
   bool norm16;        // norms stored as float16 (norm_bits 16)
+  bool polar;         // PolarQuant records instead of Lloyd-Max codes (codec TQ_CODEC_POLAR)
   int debug_withhold; // tq_debug_withhold_commit (tests of the bounded waits only)
 };

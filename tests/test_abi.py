@@ -121,3 +121,26 @@ def test_sixteen_bit_norms_field_sizes_and_checks(lib):
     with pytest.raises(B.TQError) as err:
         B.Codebook(device=-1, norm_bits=8)
     assert err.value.status == 1
+
+
+def test_polar_codec_handle_fields_and_checks(lib):
+    # PolarQuant: 64-byte records for keys and values (token-major), float32
+    # radii, no QJL fields: 136 bytes per (token, head); no codebook to read
+    book = B.Codebook(k_bits=0, v_bits=0, qjl_m=0, device=-1, codec=B.TQ_CODEC_POLAR)
+    sizes = B.tq_cache_field_bytes(book)
+    assert [sizes[n] for n in B.FIELDS] == [64, 0, 4, 0, 64, 4]
+    assert sizes == engine.field_bytes(engine.build(codec="polar")) | {"k_qjl": 0, "k_rnorm": 0}
+    with pytest.raises(B.TQError) as err:
+        B.tq_codebook_levels(book, 0)
+    assert err.value.status == 2
+    # the rotation is the same seeded draw as a TurboQuant handle's
+    other = B.Codebook(k_bits=3, v_bits=3, qjl_m=0, device=-1)
+    assert np.array_equal(B.tq_codebook_matrices(book)[0], B.tq_codebook_matrices(other)[0])
+    other.close()
+    book.close()
+    for kw, status in ((dict(qjl_m=128), 2), (dict(norm_bits=16), 2), (dict(codec=2), 1)):
+        args = dict(k_bits=0, v_bits=0, qjl_m=0, norm_bits=32, codec=B.TQ_CODEC_POLAR)
+        args.update(kw)
+        with pytest.raises(B.TQError) as err:
+            B.Codebook(device=-1, **args)
+        assert err.value.status == status, kw
