@@ -43,7 +43,8 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 METRIC = "decode attn tokens/s & HBM GB/s (% of peak) over 3-bit KV; quantize vectors/s"
 HEADLINE = "c5_llama3_70b_paged"
-SECONDARY_DECODE = ("c2_llama3_8b_decode", "c4_long_context", "c5_llama3_70b_paged_fp16_norms")
+SECONDARY_DECODE = ("c2_llama3_8b_decode", "c4_long_context", "c5_llama3_70b_paged_fp16_norms",
+                    "c2_llama3_8b_decode_polar")
 CODE_EXEMPT = 1e-5          # codes within this distance of a boundary (unit-vector units) may differ
 ATTN_TOL = 1e-3             # max |o_gpu - o_oracle| / max_t ||v_hat_t||
 
@@ -222,7 +223,8 @@ class DecodeWorkload:
         self.seed = seed
         self.batch, self.n_q, self.n_kv = cfg["batch"], cfg["n_q"], cfg["n_kv"]
         self.book = B.Codebook(k_bits=cfg["k_bits"], v_bits=cfg["v_bits"], qjl_m=cfg["qjl_m"], seed=cfg["seed"],
-                               block_size=cfg["block_size"], device=device, norm_bits=cfg.get("norm_bits", 32))
+                               block_size=cfg["block_size"], device=device, norm_bits=cfg.get("norm_bits", 32),
+                               codec=cfg.get("codec", 0))
         self.ctx = W.context_lengths(cfg, seed)
         self.max_ctx = int(self.ctx.max())
         self.table, num_blocks = W.block_layout(self.ctx, cfg["block_size"], cfg.get("shuffled_table", False), seed)
@@ -263,8 +265,9 @@ class DecodeWorkload:
         # is followed by a merge launch
         self.plan = B.tq_decode_plan(self.book, self.batch, self.n_q, self.n_kv, self.max_ctx)
         self.tc = self.plan["tensor_cores"] == 1
-        self.launches_per_step = (1 if self.batch * self.n_kv <= 1024 else 3) + (1 if self.plan["merge_in_partials"]
-                                                                                  else 2)
+        # (a PolarQuant step appends keys and values in two launches before the preparation)
+        prep = 3 if self.book.codec == 1 or self.batch * self.n_kv > 1024 else 1
+        self.launches_per_step = prep + (1 if self.plan["merge_in_partials"] else 2)
 
     def step(self, i):
         """One decode step: tq_decode_step (append the new K/V token of every
@@ -323,6 +326,8 @@ class DecodeWorkload:
         return time.perf_counter() - t0, h2d, d2h
 
     def kernel_name(self):
+        if self.book.codec == 1:
+            return "polar_attention_kernel<%d>" % (self.n_q // self.n_kv)
         return ("attention_tc_kernel<%d>" if self.tc else "attention_kernel<%d>") % (self.n_q // self.n_kv)
 
     def parity_sample(self, n_groups, seed):
@@ -344,7 +349,7 @@ class DecodeWorkload:
             items.append({"b": b, "kvh": kvh, "ctx": int(self.ctx[b]), "cache": fields,
                           "q": q_h[b, kvh * g:(kvh + 1) * g], "out": out_h[b, kvh * g:(kvh + 1) * g]})
         return {"workload": self.name, "k_bits": self.cfg["k_bits"], "v_bits": self.cfg["v_bits"],
-                "qjl_m": self.cfg["qjl_m"], "seed": self.cfg["seed"], "groups": items}
+                "qjl_m": self.cfg["qjl_m"], "seed": self.cfg["seed"], "codec": self.book.codec, "groups": items}
 
 
 def measure_decode(name, steps, warmup, seed, clocks=None, with_e2e=False, parity_groups=0):
@@ -416,9 +421,10 @@ def l2_note(copies):
 
 # ------------------------------------------------------ quantize (ours) --
 
-def measure_quantize(bits, steps, warmup, sample_tokens=0):
+def measure_quantize(bits, steps, warmup, sample_tokens=0, polar=False):
     """Prefill quantize-append of 32768 tokens x 8 KV heads (bf16, Student-t
-    outlier channels) at ``bits`` per K (bits - 1 MSE + QJL) and V; two input
+    outlier channels) at ``bits`` per K (bits - 1 MSE + QJL) and V, or with
+    the PolarQuant codec (polar: bits unused, no parity sample); two input
     copies rotated so the 128 MB of inputs are read from HBM."""
     import numpy as np
     import torch
@@ -428,8 +434,12 @@ def measure_quantize(bits, steps, warmup, sample_tokens=0):
     from online_kv_cache_tq_gb300 import workloads as W
     cfg = W.CONFIGS["c3_prefill_quantize"]
     n_tok, n_kv = cfg["tokens"], cfg["n_kv"]
-    book = B.Codebook(k_bits=bits, v_bits=bits, qjl_m=cfg["qjl_m"], seed=cfg["seed"], block_size=cfg["block_size"],
-                      device=torch.cuda.current_device())
+    if polar:
+        book = B.Codebook(k_bits=0, v_bits=0, qjl_m=0, seed=cfg["seed"], block_size=cfg["block_size"],
+                          device=torch.cuda.current_device(), codec=B.TQ_CODEC_POLAR)
+    else:
+        book = B.Codebook(k_bits=bits, v_bits=bits, qjl_m=cfg["qjl_m"], seed=cfg["seed"],
+                          block_size=cfg["block_size"], device=torch.cuda.current_device())
     g = torch.Generator(device="cuda")
     g.manual_seed(cfg["seed"] + bits)
     inputs = [(W.student_t_tokens(n_tok, n_kv, cfg["student_t_channels"], torch.bfloat16, "cuda", g, 2 * i),
@@ -461,6 +471,14 @@ def measure_quantize(bits, steps, warmup, sample_tokens=0):
     flops = n_tok * n_kv * (2 * 32768) + n_tok * n_kv * 32768  # K: rotation + QJL, V: rotation
     hbm, _ = hbm_peak()
     tensor, tensor_src = bf16_peak()
+    if polar:
+        res = {"workload": "c3_prefill_quantize", "codec": "polar", "tokens": n_tok, "n_kv_heads": n_kv,
+               "ms_per_append": secs * 1e3, "vectors_per_s": vectors / secs,
+               "hbm_gbs": nbytes / secs / 1e9, "hbm_frac": nbytes / secs / 1e9 / hbm,
+               "algorithmic_bytes_per_append": nbytes,
+               "note": "PolarQuant records (64 B + float32 radius per vector); the rotation and the polar "
+                       "levels run on the CUDA cores"}
+        return res, None
     kb = bits - 1
     rec = [recorded_traffic(k, "c3_prefill_quantize") for k in
            ("quantize_tc_kernel<%d,1,0>" % kb, "quantize_tc_kernel<%d,0,1>" % bits)]
@@ -623,6 +641,7 @@ def run_ours(args, rank, world, local_rank):
             out["secondary"]["c3_prefill_quantize_b%d" % bits] = res
             if sample is not None:
                 out["quant_samples"].append(sample)
+        out["secondary"]["c3_prefill_quantize_polar"] = measure_quantize(0, 20, 3, polar=True)[0]
         out["secondary"]["c1_single_head_parity"] = measure_single_head_fp32(20, 3)
     if want_parity:
         out["bias_sample"] = bias_sample()
@@ -698,7 +717,10 @@ def _decode_parity_group(task):
 
     from oracle import attention, engine
     cfg, item = task
-    book = engine.build(k_bits=cfg["k_bits"], v_bits=cfg["v_bits"], qjl_m=cfg["qjl_m"], seed=cfg["seed"])
+    if cfg.get("codec", 0) == 1:
+        book = engine.build(codec="polar", seed=cfg["seed"])
+    else:
+        book = engine.build(k_bits=cfg["k_bits"], v_bits=cfg["v_bits"], qjl_m=cfg["qjl_m"], seed=cfg["seed"])
     table = np.arange(item["cache"]["k_norm"].shape[0])
     worst = 0.0
     for h in range(item["q"].shape[0]):
@@ -760,7 +782,7 @@ def cpu_leg(name, n_groups, pool, procs, decode_samples, quant_samples, bias=Non
                       "query heads over its context, scaled to the batch" % groups}
     parity = {"attention_tolerance": ATTN_TOL, "code_exempt_band": CODE_EXEMPT, "decode": {}, "quantize": {}}
     for s in decode_samples:
-        cfg = {k: s[k] for k in ("k_bits", "v_bits", "qjl_m", "seed")}
+        cfg = {k: s[k] for k in ("k_bits", "v_bits", "qjl_m", "seed", "codec")}
         worst = pool.map(_decode_parity_group, [(cfg, it) for it in s["groups"]])
         parity["decode"][s["workload"]] = {
             "groups": len(worst), "heads": int(sum(it["q"].shape[0] for it in s["groups"])),

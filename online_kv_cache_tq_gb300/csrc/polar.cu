@@ -9,10 +9,11 @@
 // both members of a pair are radii) x 3 bits; the final radius is the norm
 // field (float32).  Keys and values are coded alike and carry no QJL bits.
 //
-// Quantize: 256 threads take four vectors; thread (o, h) forms y_o of
-// vectors 2h and 2h + 1 from column o of R^T (every load serves both), then
-// pairs coordinates with warp shuffles (levels 1..5) and through shared
-// memory (levels 6 and 7), and 16 threads per vector pack the record.
+// Quantize: 256 threads take 32 vectors; thread (o, h) forms y_o of vectors
+// 16 h .. 16 h + 15 from column o of R^T (every load of R serves sixteen
+// vectors, so R is read from L2 once per 32 vectors), then pairs coordinates
+// with warp shuffles (levels 1..5) and through shared memory (levels 6 and
+// 7), and 16 threads per vector pack the record.
 // Decode: one CTA per (512-token chunk, KV head, sequence), like the CUDA-core
 // decode; per 32-token tile, eight threads per token expand its record
 // top-down into the 128 rotated coordinates (16 each), the G scores
@@ -27,7 +28,8 @@ namespace tq {
 namespace {
 
 constexpr int kPThreads = 256;
-constexpr int kPVecs = 4;               // vectors per quantize block
+constexpr int kPVecs = 32;              // vectors per quantize block (16 per 128-thread half)
+constexpr int kPHalf = kPVecs / 2;
 constexpr int kRecordWords = 16;        // 64-byte record
 constexpr int kUpperBit = 320;          // first bit of the level-2..7 codes
 constexpr int kPTile = 32;              // tokens per decode tile
@@ -62,26 +64,30 @@ __global__ void __launch_bounds__(kPThreads) polar_quantize_kernel(QuantizeArgs 
     x_s[j][i & 127] = v0 + j < a.n_vec ? load_x(a.x, static_cast<long long>(v0) * kDim + i, bf16) : 0.f;
   }
   __syncthreads();
-  // y_o = sum_i R[o][i] x_i of vectors 2 hv and 2 hv + 1, 32 loads of R^T in flight
-  float y[2] = {0.f, 0.f};
+  // y_o = sum_i R[o][i] x_i of vectors 16 hv .. 16 hv + 15, 16 loads of R^T in flight
+  float y[kPHalf];
+#pragma unroll
+  for (int e = 0; e < kPHalf; ++e) y[e] = 0.f;
   const float* w = a.Rt + o;
+#pragma unroll 1
+  for (int i0 = 0; i0 < kDim; i0 += 16) {
+    float r[16];
 #pragma unroll
-  for (int i0 = 0; i0 < kDim; i0 += 32) {
-    float r[32];
+    for (int k = 0; k < 16; ++k) r[k] = __ldg(w + (i0 + k) * kDim);
 #pragma unroll
-    for (int k = 0; k < 32; ++k) r[k] = __ldg(w + (i0 + k) * kDim);
+    for (int k = 0; k < 16; k += 4)
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      y[0] = fmaf(r[k], x_s[2 * hv][i0 + k], y[0]);
-      y[1] = fmaf(r[k], x_s[2 * hv + 1][i0 + k], y[1]);
-    }
+      for (int e = 0; e < kPHalf; ++e) {
+        const float4 xv = *reinterpret_cast<const float4*>(&x_s[kPHalf * hv + e][i0 + k]);
+        y[e] = fmaf(r[k], xv.x, fmaf(r[k + 1], xv.y, fmaf(r[k + 2], xv.z, fmaf(r[k + 3], xv.w, y[e]))));
+      }
   }
   // levels 1..5 in the warp: before level L the radius of node o >> (L - 1)
   // sits at lanes o with o % 2^(L-1) == 0; the lane of the first member pairs it
   // with the second, 2^(L-1) lanes up
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int vi = 2 * hv + e;
+  for (int e = 0; e < kPHalf; ++e) {
+    const int vi = kPHalf * hv + e;
     float rho = y[e];
 #pragma unroll
     for (int lvl = 1; lvl <= 5; ++lvl) {
@@ -97,23 +103,20 @@ __global__ void __launch_bounds__(kPThreads) polar_quantize_kernel(QuantizeArgs 
     if (lane == 0) r5_s[vi][quarter] = rho;
   }
   __syncthreads();
-  // levels 6 and 7 of this half's two vectors
-  if (o == 0) {
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int vi = 2 * hv + e;
-      const float a0 = r5_s[vi][0], a1 = r5_s[vi][1], a2 = r5_s[vi][2], a3 = r5_s[vi][3];
-      cu_s[vi][60] = static_cast<uint8_t>(angle_code(a1, a0, false));
-      cu_s[vi][61] = static_cast<uint8_t>(angle_code(a3, a2, false));
-      const float r60 = sqrtf(fmaf(a0, a0, a1 * a1)), r61 = sqrtf(fmaf(a2, a2, a3 * a3));
-      cu_s[vi][62] = static_cast<uint8_t>(angle_code(r61, r60, false));
-      rad_s[vi] = sqrtf(fmaf(r60, r60, r61 * r61));
-    }
+  // levels 6 and 7: thread o < 16 of each half takes vector 16 hv + o
+  if (o < kPHalf) {
+    const int vi = kPHalf * hv + o;
+    const float a0 = r5_s[vi][0], a1 = r5_s[vi][1], a2 = r5_s[vi][2], a3 = r5_s[vi][3];
+    cu_s[vi][60] = static_cast<uint8_t>(angle_code(a1, a0, false));
+    cu_s[vi][61] = static_cast<uint8_t>(angle_code(a3, a2, false));
+    const float r60 = sqrtf(fmaf(a0, a0, a1 * a1)), r61 = sqrtf(fmaf(a2, a2, a3 * a3));
+    cu_s[vi][62] = static_cast<uint8_t>(angle_code(r61, r60, false));
+    rad_s[vi] = sqrtf(fmaf(r60, r60, r61 * r61));
   }
   __syncthreads();
   // pack: thread (vector vi, word wd) builds bits 32 wd .. 32 wd + 31 of the record
-  if (t < kPVecs * kRecordWords) {
-    const int vi = t >> 4, wd = t & 15;
+  for (int idx = t; idx < kPVecs * kRecordWords; idx += kPThreads) {
+    const int vi = idx >> 4, wd = idx & 15;
     const int v = v0 + vi;
     if (v < a.n_vec) {
       uint32_t word = 0;

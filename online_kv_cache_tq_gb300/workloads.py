@@ -38,6 +38,8 @@ CONFIGS = {
 }
 # the same paged decode with 16-bit stored norms (102 bytes per token-head)
 CONFIGS["c5_llama3_70b_paged_fp16_norms"] = dict(CONFIGS["c5_llama3_70b_paged"], norm_bits=16)
+# the 8B-shaped decode over a PolarQuant cache (codec 1: 64-byte records, float32 radii, no QJL)
+CONFIGS["c2_llama3_8b_decode_polar"] = dict(CONFIGS["c2_llama3_8b_decode"], codec=1, k_bits=0, v_bits=0, qjl_m=0)
 
 
 def torch_dtype(name):
