@@ -11,9 +11,9 @@
 //
 // Quantize: 256 threads take 32 vectors; thread (o, h) forms y_o of vectors
 // 16 h .. 16 h + 15 from column o of R^T (every load of R serves sixteen
-// vectors, so R is read from L2 once per 32 vectors), then pairs coordinates
-// with warp shuffles (levels 1..5) and through shared memory (levels 6 and
-// 7), and 16 threads per vector pack the record.
+// vectors, so R is read from L2 once per 32 vectors); the levels then run
+// through two shared buffers, one pair of every vector per thread and pass,
+// and 16 threads per vector pack the record.
 // Decode: one CTA per (512-token chunk, KV head, sequence), like the CUDA-core
 // decode; per 32-token tile, eight threads per token expand its record
 // top-down into the 128 rotated coordinates (16 each), the G scores
@@ -52,12 +52,11 @@ __device__ __forceinline__ float load_x(const void* base, long long idx, bool bf
 
 __global__ void __launch_bounds__(kPThreads) polar_quantize_kernel(QuantizeArgs a, bool bf16) {
   __shared__ __align__(16) float x_s[kPVecs][kDim];
-  __shared__ float r5_s[kPVecs][4];             // level-5 radii, one per 32 coordinates
+  __shared__ __align__(16) float h_s[kPVecs][kDim];   // radii of odd levels (rows of kDim, the first half used)
   __shared__ float rad_s[kPVecs];
   __shared__ uint8_t c1_s[kPVecs][64];          // level-1 codes
   __shared__ uint8_t cu_s[kPVecs][64];          // levels 2..7 (63 codes)
   const int t = threadIdx.x, o = t & (kDim - 1), hv = t >> 7;
-  const int lane = t & 31, quarter = o >> 5;
   const int v0 = blockIdx.x * kPVecs;
   for (int i = t; i < kPVecs * kDim; i += kPThreads) {
     const int j = i >> 7;
@@ -82,55 +81,48 @@ __global__ void __launch_bounds__(kPThreads) polar_quantize_kernel(QuantizeArgs 
         y[e] = fmaf(r[k], xv.x, fmaf(r[k + 1], xv.y, fmaf(r[k + 2], xv.z, fmaf(r[k + 3], xv.w, y[e]))));
       }
   }
-  // levels 1..5 in the warp: before level L the radius of node o >> (L - 1)
-  // sits at lanes o with o % 2^(L-1) == 0; the lane of the first member pairs it
-  // with the second, 2^(L-1) lanes up
+  // y into x_s (every thread has read x_s), then the levels: level L pairs
+  // the 2^(8-L) values of every vector in one buffer into radii in the other
+  // (x_s and h_s alternate), one pair per thread and pass, all lanes busy
+  __syncthreads();
 #pragma unroll
-  for (int e = 0; e < kPHalf; ++e) {
-    const int vi = kPHalf * hv + e;
-    float rho = y[e];
+  for (int e = 0; e < kPHalf; ++e) x_s[kPHalf * hv + e][o] = y[e];
+  __syncthreads();
 #pragma unroll
-    for (int lvl = 1; lvl <= 5; ++lvl) {
-      const int step = 1 << (lvl - 1);
-      const float second = __shfl_xor_sync(0xffffffffu, rho, step);
-      if ((o & (2 * step - 1)) == 0) {
-        const int code = angle_code(second, rho, lvl == 1);
-        if (lvl == 1) c1_s[vi][o >> 1] = static_cast<uint8_t>(code);
-        else cu_s[vi][upper_offset(lvl) + (o >> lvl)] = static_cast<uint8_t>(code);
-      }
-      rho = sqrtf(fmaf(rho, rho, second * second));
+  for (int lvl = 1; lvl <= 7; ++lvl) {
+    const int pairs = kDim >> lvl;                       // pairs per vector at this level
+    const float* src = (lvl & 1) ? &x_s[0][0] : &h_s[0][0];
+    float* dst = (lvl & 1) ? &h_s[0][0] : &x_s[0][0];
+    for (int idx = t; idx < kPVecs * pairs; idx += kPThreads) {
+      const int vi = idx / pairs, p = idx - vi * pairs;
+      const float2 fs = *reinterpret_cast<const float2*>(src + vi * kDim + 2 * p);   // (first, second)
+      const int code = angle_code(fs.y, fs.x, lvl == 1);
+      if (lvl == 1) c1_s[vi][p] = static_cast<uint8_t>(code);
+      else cu_s[vi][upper_offset(lvl) + p] = static_cast<uint8_t>(code);
+      const float rho = sqrtf(fmaf(fs.x, fs.x, fs.y * fs.y));
+      if (lvl == 7) rad_s[vi] = rho;
+      else dst[vi * kDim + p] = rho;
     }
-    if (lane == 0) r5_s[vi][quarter] = rho;
+    __syncthreads();
   }
-  __syncthreads();
-  // levels 6 and 7: thread o < 16 of each half takes vector 16 hv + o
-  if (o < kPHalf) {
-    const int vi = kPHalf * hv + o;
-    const float a0 = r5_s[vi][0], a1 = r5_s[vi][1], a2 = r5_s[vi][2], a3 = r5_s[vi][3];
-    cu_s[vi][60] = static_cast<uint8_t>(angle_code(a1, a0, false));
-    cu_s[vi][61] = static_cast<uint8_t>(angle_code(a3, a2, false));
-    const float r60 = sqrtf(fmaf(a0, a0, a1 * a1)), r61 = sqrtf(fmaf(a2, a2, a3 * a3));
-    cu_s[vi][62] = static_cast<uint8_t>(angle_code(r61, r60, false));
-    rad_s[vi] = sqrtf(fmaf(r60, r60, r61 * r61));
-  }
-  __syncthreads();
   // pack: thread (vector vi, word wd) builds bits 32 wd .. 32 wd + 31 of the record
   for (int idx = t; idx < kPVecs * kRecordWords; idx += kPThreads) {
     const int vi = idx >> 4, wd = idx & 15;
     const int v = v0 + vi;
     if (v < a.n_vec) {
+      // OR in every code whose bits overlap [lo, lo + 32): level-1 codes at 5 c,
+      // upper codes at kUpperBit + 3 k (a code cut by lo contributes its top bits)
+      const int lo = 32 * wd;
       uint32_t word = 0;
-#pragma unroll 4
-      for (int bit = 0; bit < 32; ++bit) {
-        const int pos = 32 * wd + bit;
-        int val = 0;
-        if (pos < kUpperBit) {
-          val = (c1_s[vi][pos / 5] >> (pos % 5)) & 1;
-        } else if (pos < kUpperBit + 3 * 63) {
-          const int k = pos - kUpperBit;
-          val = (cu_s[vi][k / 3] >> (k % 3)) & 1;
-        }
-        word |= static_cast<uint32_t>(val) << bit;
+      for (int c = lo / 5; c < 64 && 5 * c < lo + 32; ++c) {
+        const int sh = 5 * c - lo;
+        const uint32_t code = c1_s[vi][c];
+        word |= sh >= 0 ? code << sh : code >> -sh;
+      }
+      for (int k = lo > kUpperBit ? (lo - kUpperBit) / 3 : 0; k < 63 && kUpperBit + 3 * k < lo + 32; ++k) {
+        const int sh = kUpperBit + 3 * k - lo;
+        const uint32_t code = cu_s[vi][k];
+        word |= sh >= 0 ? code << sh : code >> -sh;
       }
       const int token = v / a.n_kv, head = v - token * a.n_kv;
       const long long slot = slot_of(a, token);
