@@ -16,10 +16,11 @@
 // and 16 threads per vector pack the record.
 // Decode: one CTA per (512-token chunk, KV head, sequence), like the CUDA-core
 // decode; per 32-token tile, eight threads per token expand its record
-// top-down into the 128 rotated coordinates (16 each), the G scores
-// <q_rot, y_hat> follow from shared memory, then the values the same way with
-// the softmax weights; the partial (m, l, acc) goes to the merge that
-// back-rotates (seo-farm page §2: out = R^T o_rot).
+// top-down into the 128 rotated coordinates (16 each, a padded token-major
+// row in shared memory), the G scores <q_rot, y_hat> follow from float4
+// reads, then the values the same way with the softmax weights; the partial
+// (m, l, acc) goes to the merge that back-rotates (seo-farm page §2:
+// out = R^T o_rot).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -33,6 +34,7 @@ constexpr int kPHalf = kPVecs / 2;
 constexpr int kRecordWords = 16;        // 64-byte record
 constexpr int kUpperBit = 320;          // first bit of the level-2..7 codes
 constexpr int kPTile = 32;              // tokens per decode tile
+constexpr int kYRow = kDim + 4;         // padded row of a decoded vector (float4 reads by 8 lanes hit distinct banks)
 constexpr float kSectorsPerRadian = 3.8197186342054881f;   // 12 / pi
 
 // Index of the first level-L code (L = 2..7) among the 63 upper codes.
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
   const int n_local = min(kChunk, ctx - start);
 
   __shared__ __align__(16) float q_s[G][kDim];
-  __shared__ float y_s[kDim][kPTile + 1];      // one tile's decoded vectors, coordinate-major
+  __shared__ __align__(16) float y_s[kPTile][kYRow];   // one tile's decoded vectors, token-major
   __shared__ float p_s[G][kChunk];             // scores, then softmax weights
   __shared__ uint32_t rec_s[kPTile][kRecordWords + 1];
   __shared__ float rad_s[kPTile];
@@ -238,35 +240,50 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
   const int tok_i = t >> 3, part = t & 7;      // expansion: token of the tile, 16-coordinate part
   const int n_tiles = (n_local + kPTile - 1) / kPTile;
   // one tile's records into rec_s and radii into rad_s (invalid tokens: radius 0)
-  auto load_tile = [&](const uint8_t* codes, const void* norms, int tile) {
+  // one tile's records and radii: fetched into registers one tile ahead
+  // (the loads fly while the current tile is expanded and used), then
+  // stashed into rec_s / rad_s (invalid tokens: zero record, radius 0)
+  uint2 wv = make_uint2(0u, 0u);
+  float rd = 0.f;
+  auto fetch_tile = [&](const uint8_t* codes, const void* norms, int tile) {
     const long long row = row_s[tile * kPTile + tok_i];
-    uint2 wv = make_uint2(0u, 0u);
-    if (row >= 0) wv = reinterpret_cast<const uint2*>(codes + row * (4 * kRecordWords))[part];
+    wv = row >= 0 ? reinterpret_cast<const uint2*>(codes + row * (4 * kRecordWords))[part] : make_uint2(0u, 0u);
+    rd = part == 0 && row >= 0 ? reinterpret_cast<const float*>(norms)[row] : 0.f;
+  };
+  auto stash_tile = [&]() {
     rec_s[tok_i][2 * part] = wv.x;
     rec_s[tok_i][2 * part + 1] = wv.y;
     if (part == 0) {
       rec_s[tok_i][kRecordWords] = 0u;
-      rad_s[tok_i] = row >= 0 ? reinterpret_cast<const float*>(norms)[row] : 0.f;
+      rad_s[tok_i] = rd;
     }
   };
   auto expand_tile = [&]() {
     float v[16];
     expand_part(rec_s[tok_i], rad_s[tok_i], part, cos_s, sin_s, v);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) y_s[16 * part + k][tok_i] = v[k];
+    for (int k = 0; k < 16; k += 4)
+      *reinterpret_cast<float4*>(&y_s[tok_i][16 * part + k]) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
   };
 
   // ---- scores: s = scale <q_rot, y_hat_k> per (token, head) ----
+  fetch_tile(a.k_codes, a.k_norm, 0);
   for (int tile = 0; tile < n_tiles; ++tile) {
-    load_tile(a.k_codes, a.k_norm, tile);
+    stash_tile();
     __syncthreads();
+    if (tile + 1 < n_tiles) fetch_tile(a.k_codes, a.k_norm, tile + 1);
+    else fetch_tile(a.v_codes, a.v_norm, 0);     // (the first value tile, while the softmax runs)
     expand_tile();
     __syncthreads();
     const int i = t & (kPTile - 1);
     for (int h = t / kPTile; h < G; h += kPThreads / kPTile) {
       float s = 0.f;
 #pragma unroll 8
-      for (int j = 0; j < kDim; ++j) s = fmaf(q_s[h][j], y_s[j][i], s);
+      for (int j = 0; j < kDim; j += 4) {
+        const float4 qv = *reinterpret_cast<const float4*>(&q_s[h][j]);
+        const float4 yv = *reinterpret_cast<const float4*>(&y_s[i][j]);
+        s = fmaf(qv.x, yv.x, fmaf(qv.y, yv.y, fmaf(qv.z, yv.z, fmaf(qv.w, yv.w, s))));
+      }
       const int tl = tile * kPTile + i;
       if (tl < kChunk) p_s[h][tl] = tl < n_local && row_s[tl] >= 0 ? a.scale * s : -INFINITY;
     }
@@ -326,13 +343,14 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
 #pragma unroll
   for (int k = 0; k < HH; ++k) acc[k] = 0.f;
   for (int tile = 0; tile < n_tiles; ++tile) {
-    load_tile(a.v_codes, a.v_norm, tile);
+    stash_tile();
     __syncthreads();
+    if (tile + 1 < n_tiles) fetch_tile(a.v_codes, a.v_norm, tile + 1);
     expand_tile();
     __syncthreads();
     const int n_in = min(kPTile, n_local - tile * kPTile);
     for (int i = 0; i < n_in; ++i) {
-      const float yv = y_s[j][i];
+      const float yv = y_s[i][j];
 #pragma unroll
       for (int k = 0; k < HH; ++k) {
         const int h = 2 * k + hf;
