@@ -83,18 +83,36 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Lane i holds row i of a 32 x 32 bit matrix (bit j = column j); afterwards
-// lane j holds column j (bit i = row i).  Five butterfly stages.
-__device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
-  const uint32_t masks[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+// lane j holds column j (bit i = row i).  Five butterfly stages; in stage k
+// (distance sh = 16 >> k) a lane keeps the bits of its half of every 2 sh
+// block and takes the other half from its partner lane, rotated into place
+// (left by sh for the lower lane of a pair, right by sh for the upper: the
+// bits a rotation wraps around fall in the half the lane keeps), so a stage
+// is a shuffle, a funnel shift and one select-by-mask.  The per-lane masks
+// and rotations are set once.
+struct LaneTranspose {
+  uint32_t keep[5];
+  uint32_t rot[5];
+  __device__ __forceinline__ explicit LaneTranspose(int lane) {
+    const uint32_t masks[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
 #pragma unroll
-  for (int k = 0; k < 5; ++k) {
-    const int sh = 16 >> k;
-    const uint32_t m = masks[k];
-    const uint32_t o = __shfl_xor_sync(0xffffffffu, x, sh);
-    x = (lane & sh) ? ((x & ~m) | ((o & ~m) >> sh)) : ((x & m) | ((o & m) << sh));
+    for (int k = 0; k < 5; ++k) {
+      const int sh = 16 >> k;
+      const bool upper = (lane & sh) != 0;
+      keep[k] = upper ? ~masks[k] : masks[k];
+      rot[k] = upper ? 32 - sh : sh;
+    }
   }
-  return x;
-}
+  __device__ __forceinline__ uint32_t operator()(uint32_t x) const {
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+      const uint32_t o = __shfl_xor_sync(0xffffffffu, x, 16 >> k);
+      const uint32_t z = __funnelshift_l(o, o, rot[k]);
+      x = (x & keep[k]) | (z & ~keep[k]);
+    }
+    return x;
+  }
+};
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -398,6 +416,7 @@ __global__ void __launch_bounds__(F32 ? kThreadsF32 : kThreads, 1)
     const int g = (warp - 2) >> 2;                // its coordinate group: 32 g .. 32 g + 31
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const LaneTranspose transpose(lane);          // (used by the token-transposed value codes)
     float bnd[kLevels - 1];
 #pragma unroll
     for (int i = 0; i < kLevels - 1; ++i) bnd[i] = a.bounds[i];
@@ -579,7 +598,7 @@ __global__ void __launch_bounds__(F32 ? kThreadsF32 : kThreads, 1)
 #pragma unroll
           for (int p = 0; p < BITS; ++p)
             words[transposed_word(blk0, head, a.n_kv, BITS, p, 32 * g + lane, a.block_size, off0)] =
-                transpose32(planes[p], lane);
+                transpose(planes[p]);
         } else if (dst >= 0) {
           const int off = static_cast<int>(slot - blk * a.block_size);
           const unsigned mask = 1u << (off & 31);
