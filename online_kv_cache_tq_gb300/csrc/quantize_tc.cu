@@ -164,16 +164,33 @@ __device__ __forceinline__ float level_of(const float (&levels)[1 << BITS], cons
   return cand[0];
 }
 
-// The same search for 2- and 3-bit codes in one block of predicated PTX:
+// The same search for 2-, 3- and 4-bit codes in one block of predicated PTX:
 // each compare feeds the next level's boundary select and a predicated OR of
 // bit j into its plane word (one logic instruction per plane bit where a
-// select and an OR would be two).  With LEV it also returns levels[code].
+// select and an OR would be two).  With LEV it also returns levels[code]
+// (2 and 3 bits).
 template <int BITS, bool LEV, int J>
 __device__ __forceinline__ float decide(float y, const float (&t)[(1 << BITS) - 1], const float (&l)[1 << BITS],
                                         uint32_t (&pl)[BITS]) {
-  static_assert(BITS == 2 || BITS == 3, "2- or 3-bit codes");
+  static_assert(BITS >= 2 && BITS <= 4 && !(BITS == 4 && LEV), "2- to 4-bit codes, levels up to 3 bits");
   float lev = 0.f;
-  if constexpr (BITS == 3) {
+  if constexpr (BITS == 4) {
+    // boundaries by (q3 q2 q1): level 2 from t3 / t11, level 1 from t1 t5 t9
+    // t13, level 0 from the even ones
+    asm("{\n\t.reg .pred q3, q2, q1, q0;\n\t.reg .f32 ta, tb, tc, td, e0, e1, e2, e3, f0, f1, g;\n\t"
+        "setp.gt.f32 q3, %4, %5;\n\t@q3 or.b32 %0, %0, %20;\n\t"
+        "selp.f32 ta, %7, %6, q3;\n\t"
+        "setp.gt.f32 q2, %4, ta;\n\t@q2 or.b32 %1, %1, %20;\n\t"
+        "selp.f32 tb, %9, %8, q2;\n\tselp.f32 tc, %11, %10, q2;\n\tselp.f32 td, tc, tb, q3;\n\t"
+        "setp.gt.f32 q1, %4, td;\n\t@q1 or.b32 %2, %2, %20;\n\t"
+        "selp.f32 e0, %13, %12, q1;\n\tselp.f32 e1, %15, %14, q1;\n\t"
+        "selp.f32 e2, %17, %16, q1;\n\tselp.f32 e3, %19, %18, q1;\n\t"
+        "selp.f32 f0, e1, e0, q2;\n\tselp.f32 f1, e3, e2, q2;\n\tselp.f32 g, f1, f0, q3;\n\t"
+        "setp.gt.f32 q0, %4, g;\n\t@q0 or.b32 %3, %3, %20;\n\t}"
+        : "+r"(pl[3]), "+r"(pl[2]), "+r"(pl[1]), "+r"(pl[0])
+        : "f"(y), "f"(t[7]), "f"(t[3]), "f"(t[11]), "f"(t[1]), "f"(t[5]), "f"(t[9]), "f"(t[13]), "f"(t[0]),
+          "f"(t[2]), "f"(t[4]), "f"(t[6]), "f"(t[8]), "f"(t[10]), "f"(t[12]), "f"(t[14]), "n"(1u << J));
+  } else if constexpr (BITS == 3) {
     asm("{\n\t.reg .pred q2, q1, q0;\n\t.reg .f32 ta, tb, tc, td;\n\t"
         "setp.gt.f32 q2, %3, %4;\n\t@q2 or.b32 %0, %0, %11;\n\t"
         "selp.f32 ta, %6, %5, q2;\n\t"
@@ -541,7 +558,7 @@ __global__ void __launch_bounds__(F32 ? kThreadsF32 : kThreads, 1)
 #pragma unroll
         for (int p = 0; p < BITS; ++p) planes[p] = 0;
         float r[32];
-        if constexpr (BITS == 2 || BITS == 3) {
+        if constexpr (BITS == 2 || BITS == 3 || (BITS == 4 && !QJL)) {
           for_each_index(
               [&](auto jc) {
                 constexpr int j = decltype(jc)::value;
