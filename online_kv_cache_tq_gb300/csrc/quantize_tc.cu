@@ -190,7 +190,7 @@ __device__ __forceinline__ float decide(float y, const float (&t)[(1 << BITS) - 
         : "+r"(pl[3]), "+r"(pl[2]), "+r"(pl[1]), "+r"(pl[0])
         : "f"(y), "f"(t[7]), "f"(t[3]), "f"(t[11]), "f"(t[1]), "f"(t[5]), "f"(t[9]), "f"(t[13]), "f"(t[0]),
           "f"(t[2]), "f"(t[4]), "f"(t[6]), "f"(t[8]), "f"(t[10]), "f"(t[12]), "f"(t[14]), "n"(1u << J));
-  } else if constexpr (BITS == 3) {
+  } else if constexpr (BITS == 3 && !LEV) {
     asm("{\n\t.reg .pred q2, q1, q0;\n\t.reg .f32 ta, tb, tc, td;\n\t"
         "setp.gt.f32 q2, %3, %4;\n\t@q2 or.b32 %0, %0, %11;\n\t"
         "selp.f32 ta, %6, %5, q2;\n\t"
@@ -199,11 +199,20 @@ __device__ __forceinline__ float decide(float y, const float (&t)[(1 << BITS) - 
         "setp.gt.f32 q0, %3, td;\n\t@q0 or.b32 %2, %2, %11;\n\t}"
         : "+r"(pl[2]), "+r"(pl[1]), "+r"(pl[0])
         : "f"(y), "f"(t[3]), "f"(t[1]), "f"(t[5]), "f"(t[0]), "f"(t[2]), "f"(t[4]), "f"(t[6]), "n"(1u << J));
-    if constexpr (LEV) {
-      // (only with 3 MSE bits and the QJL bit: the level by the generic selects)
-      const bool b[3] = {((pl[0] >> J) & 1u) != 0, ((pl[1] >> J) & 1u) != 0, ((pl[2] >> J) & 1u) != 0};
-      lev = level_of<3>(l, b);
-    }
+  } else if constexpr (BITS == 3) {
+    // with the level: levels[code] selected by q0, then q1, then q2
+    asm("{\n\t.reg .pred q2, q1, q0;\n\t.reg .f32 ta, tb, tc, td, la, lb, lc, ld, lf, lg;\n\t"
+        "setp.gt.f32 q2, %4, %5;\n\t@q2 or.b32 %0, %0, %20;\n\t"
+        "selp.f32 ta, %7, %6, q2;\n\t"
+        "setp.gt.f32 q1, %4, ta;\n\t@q1 or.b32 %1, %1, %20;\n\t"
+        "selp.f32 tb, %11, %10, q1;\n\tselp.f32 tc, %9, %8, q1;\n\tselp.f32 td, tb, tc, q2;\n\t"
+        "setp.gt.f32 q0, %4, td;\n\t@q0 or.b32 %2, %2, %20;\n\t"
+        "selp.f32 la, %13, %12, q0;\n\tselp.f32 lb, %15, %14, q0;\n\t"
+        "selp.f32 lc, %17, %16, q0;\n\tselp.f32 ld, %19, %18, q0;\n\t"
+        "selp.f32 lf, lb, la, q1;\n\tselp.f32 lg, ld, lc, q1;\n\tselp.f32 %3, lg, lf, q2;\n\t}"
+        : "+r"(pl[2]), "+r"(pl[1]), "+r"(pl[0]), "=f"(lev)
+        : "f"(y), "f"(t[3]), "f"(t[1]), "f"(t[5]), "f"(t[0]), "f"(t[2]), "f"(t[4]), "f"(t[6]), "f"(l[0]),
+          "f"(l[1]), "f"(l[2]), "f"(l[3]), "f"(l[4]), "f"(l[5]), "f"(l[6]), "f"(l[7]), "n"(1u << J));
   } else if constexpr (LEV) {
     asm("{\n\t.reg .pred q1, q0;\n\t.reg .f32 ta, la, lb;\n\t"
         "setp.gt.f32 q1, %3, %4;\n\t@q1 or.b32 %0, %0, %11;\n\t"
