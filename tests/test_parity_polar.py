@@ -127,3 +127,46 @@ def test_polar_decode_step_appends_then_attends():
     worst = check_decode(out.cpu().numpy(), hc, q, table, ctx, ref, pairs)
     print("polar decode step: worst normalised error %.3g" % worst)
     assert B.tq_get_last_device_error(book) == 0
+
+
+def test_polar_cache_through_the_static_and_host_buffer_entry_points():
+    # the allocation-free decode and the host-buffer step take a PolarQuant
+    # handle like any other: their outputs equal the workspace decode's
+    n_kv, group, bs = 2, 4, 64
+    cfg = dict(n_kv=n_kv, block_size=bs, dtype="bf16", seed=12, log_uniform=(0.1, 10.0), outliers=3,
+               outlier_scale=30.0)
+    book, ref = polar_books(seed=12)
+    ctx = np.array([300, 1100], dtype=np.int32)
+    table, _ = W.block_layout(ctx, bs, True, seed=5)
+    g = generator(90)
+    cache = fill_cache(book, cfg, ctx, table, g, chunk_tokens=500)
+    q = W.queries(2, n_kv * group, torch.bfloat16, "cuda", g)
+    expect = decode(book, cache, q, table, ctx, int(ctx.max()))
+    out = torch.full((2, n_kv * group, 128), float("nan"), device="cuda")
+    table_t = torch.as_tensor(table, device="cuda")
+    ctx_t = torch.as_tensor(ctx, device="cuda")
+    B.tq_decode_attention_static(book, q, B.TQ_BF16, 2, n_kv * group, n_kv, C.cache_view(book, cache), table_t,
+                                 table.shape[1], ctx_t, int(ctx.max()), 0.0, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), expect)
+    # one host-buffer step appends a token per sequence and decodes; the same
+    # step through device buffers on a copy of the cache gives the same output
+    k_new = W.gaussian_tokens(2, W.channel_scales(3, n_kv, (0.1, 10.0), 3, 30.0), torch.bfloat16, "cuda", g)
+    v_new = W.gaussian_tokens(2, W.channel_scales(4, n_kv, (0.1, 10.0), 3, 30.0), torch.bfloat16, "cuda", g)
+    ctx2 = ctx + 1
+    copy = {name: t.clone() for name, t in cache.items()}
+    ws, nbytes = C.allocate_workspace(book, 2, n_kv * group, int(ctx2.max()))
+    dev_out = torch.empty((2, n_kv * group, 128), device="cuda")
+    ctx2_t = torch.as_tensor(ctx2, device="cuda")
+    B.tq_decode_step(book, k_new, v_new, B.TQ_BF16, q, B.TQ_BF16, 2, n_kv * group, n_kv, C.cache_view(book, copy),
+                     table_t, table.shape[1], ctx2_t, int(ctx2.max()), 0.0, dev_out, ws, nbytes)
+    host_out = torch.empty((2, n_kv * group, 128)).pin_memory()
+    hws = B.tq_decode_step_host_workspace_bytes(book, 2, n_kv * group, n_kv, int(ctx2.max()), B.TQ_BF16, B.TQ_BF16)
+    hws_t = torch.empty(hws, dtype=torch.uint8, device="cuda")
+    B.tq_decode_step_host(book, k_new.cpu().pin_memory(), v_new.cpu().pin_memory(), B.TQ_BF16,
+                          q.cpu().pin_memory(), B.TQ_BF16, 2, n_kv * group, n_kv, C.cache_view(book, cache), table_t,
+                          table.shape[1], torch.as_tensor(ctx2).pin_memory(), int(ctx2.max()), 0.0, host_out, hws_t,
+                          hws, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert np.array_equal(host_out.numpy(), dev_out.cpu().numpy())
+    assert B.tq_get_last_device_error(book) == 0
