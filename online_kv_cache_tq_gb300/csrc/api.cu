@@ -370,7 +370,7 @@ tq_status append_args(const tq_codebook* book, const void* k, const void* v, tq_
   ka->qjl = book->cfg.qjl_m > 0 ? static_cast<uint8_t*>(cache->k_qjl) : nullptr;
   ka->norm = cache->k_norm;
   ka->rnorm = book->cfg.qjl_m > 0 ? cache->k_rnorm : nullptr;
-  ka->bits = book->k_mse_bits;
+  ka->bits = book->polar ? 0 : book->k_mse_bits;   // (0: PolarQuant records)
   ka->transposed = false;
   ka->levels = table_field(book, offsetof(tq::DeviceTables, k_levels));
   ka->bounds = table_field(book, offsetof(tq::DeviceTables, k_bounds));
@@ -379,8 +379,8 @@ tq_status append_args(const tq_codebook* book, const void* k, const void* v, tq_
   va->qjl = nullptr;
   va->norm = cache->v_norm;
   va->rnorm = nullptr;
-  va->bits = book->v_bits;
-  va->transposed = true;
+  va->bits = book->polar ? 0 : book->v_bits;
+  va->transposed = !book->polar;                  // (PolarQuant value records are token-major)
   va->levels = table_field(book, offsetof(tq::DeviceTables, v_levels));
   va->bounds = table_field(book, offsetof(tq::DeviceTables, v_bounds));
   return TQ_OK;
@@ -389,7 +389,9 @@ tq_status append_args(const tq_codebook* book, const void* k, const void* v, tq_
 // Launch a validated append (either tensor may be absent).
 tq_status run_append(const tq_codebook* book, const void* k, const void* v, const tq::QuantizeArgs& ka,
                      const tq::QuantizeArgs& va, bool bf16, cudaStream_t s) {
-  if (book->polar) {
+  if (book->polar && ka.n_vec <= tq::kSmallQuantize) {
+    // a decode step's few vectors: the CUDA-core PolarQuant kernel (the tile
+    // quantizer's PolarQuant epilogue takes larger appends)
     if (k && tq::launch_polar_quantize(ka, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;
     if (v && tq::launch_polar_quantize(va, bf16, s) != cudaSuccess) return TQ_ERR_CUDA;
     return TQ_OK;

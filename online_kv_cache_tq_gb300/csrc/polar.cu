@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "polar_codes.cuh"
 
 namespace tq {
 namespace {
@@ -31,20 +32,14 @@ namespace {
 constexpr int kPThreads = 256;
 constexpr int kPVecs = 32;              // vectors per quantize block (16 per 128-thread half)
 constexpr int kPHalf = kPVecs / 2;
-constexpr int kRecordWords = 16;        // 64-byte record
-constexpr int kUpperBit = 320;          // first bit of the level-2..7 codes
+constexpr int kRecordWords = kPolarRecordWords;
+constexpr int kUpperBit = kPolarUpperBit;
 constexpr int kPTile = 32;              // tokens per decode tile
 constexpr int kYRow = kDim + 4;         // padded row of a decoded vector (float4 reads by 8 lanes hit distinct banks)
-constexpr float kSectorsPerRadian = 3.8197186342054881f;   // 12 / pi
 
-// Index of the first level-L code (L = 2..7) among the 63 upper codes.
-__device__ __forceinline__ int upper_offset(int level) { return 64 - (128 >> (level - 1)); }
-
-// Rounded multiple of pi/12 of the angle of (first, second); level 1 angles
-// span (-pi, pi] and are taken modulo 24, upper levels lie in [0, pi/2].
+__device__ __forceinline__ int upper_offset(int level) { return polar_upper_offset(level); }
 __device__ __forceinline__ int angle_code(float second, float first, bool level1) {
-  const int k = __float2int_rn(atan2f(second, first) * kSectorsPerRadian);   // (half to even)
-  return level1 ? (k + 24) % 24 : k;
+  return polar_angle_code(second, first, level1);
 }
 
 __device__ __forceinline__ float load_x(const void* base, long long idx, bool bf16) {
@@ -112,20 +107,7 @@ __global__ void __launch_bounds__(kPThreads) polar_quantize_kernel(QuantizeArgs 
     const int vi = idx >> 4, wd = idx & 15;
     const int v = v0 + vi;
     if (v < a.n_vec) {
-      // OR in every code whose bits overlap [lo, lo + 32): level-1 codes at 5 c,
-      // upper codes at kUpperBit + 3 k (a code cut by lo contributes its top bits)
-      const int lo = 32 * wd;
-      uint32_t word = 0;
-      for (int c = lo / 5; c < 64 && 5 * c < lo + 32; ++c) {
-        const int sh = 5 * c - lo;
-        const uint32_t code = c1_s[vi][c];
-        word |= sh >= 0 ? code << sh : code >> -sh;
-      }
-      for (int k = lo > kUpperBit ? (lo - kUpperBit) / 3 : 0; k < 63 && kUpperBit + 3 * k < lo + 32; ++k) {
-        const int sh = kUpperBit + 3 * k - lo;
-        const uint32_t code = cu_s[vi][k];
-        word |= sh >= 0 ? code << sh : code >> -sh;
-      }
+      const uint32_t word = polar_record_word(c1_s[vi], cu_s[vi], wd);
       const int token = v / a.n_kv, head = v - token * a.n_kv;
       const long long slot = slot_of(a, token);
       const long long cache_rows = static_cast<long long>(a.num_blocks) * a.block_size;

@@ -18,6 +18,12 @@
 // with warp shuffles and stored as whole words when the 32 slots are
 // contiguous and aligned (prefill), or set bit by bit with atomics otherwise.
 //
+// BITS = 0 is the PolarQuant epilogue (the intelliparadigm.com page, §2.1.1
+// step 2) on the same rotation: each thread pairs its 32 coordinates through
+// levels 1..5 in registers, the four threads of a vector meet in shared
+// memory for levels 6 and 7, and the 64-byte records are packed from the
+// codes staged there; the radius stored is the exact norm.
+//
 // One persistent CTA per SM, 18 warps:
 //   warp 0      TMA producer: R/S' hi/lo once, then 128-token tiles of X;
 //   warp 1      tcgen05.mma issuer (and owner of the tensor-memory columns);
@@ -40,6 +46,7 @@
 #include <utility>
 
 #include "kernels.h"
+#include "polar_codes.cuh"
 #include "tc_ptx.cuh"
 
 namespace tq {
@@ -74,6 +81,11 @@ struct Layout {
   static constexpr int kRs0 = kX0 + kStages * kStageBytes;   // [2][4][128] floats
   static constexpr int kNrm0 = kRs0 + (QJL ? 2 * 4 * kTileRows * 4 : 0);   // F32: [kStages][128] floats
   static constexpr int kBytes = kNrm0 + (F32 ? kStages * kTileRows * 4 : 0);
+  // PolarQuant epilogue (BITS = 0): one tile's codes, [128 rows][64 level-1 |
+  // 63 upper + 1] bytes, then the level-5 radii [128 rows][4] floats
+  static constexpr int kPolar0 = kBytes;
+  static constexpr int kPolarBytes = kBytes + kTileRows * 128 + kTileRows * 4 * 4;
+  static_assert(kPolarBytes > kPolar0, "the PolarQuant region follows the rest");
   static constexpr int kYBufs = QJL ? 3 : 2;
   static constexpr uint32_t kZCol = 3 * 128;
   static constexpr uint32_t kTmemCols = QJL ? 512 : 256;
@@ -250,7 +262,10 @@ __global__ void __launch_bounds__(F32 ? kThreadsF32 : kThreads, 1)
     quantize_tc_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map,
                        QuantizeArgs a) {
   using L = Layout<QJL, F32>;
+  constexpr bool POLAR = BITS == 0;
   constexpr int kLevels = 1 << BITS;
+  constexpr int kBounds = POLAR ? 1 : kLevels - 1;   // (array sizes: no codebook with PolarQuant)
+  constexpr int kPlanes = POLAR ? 1 : BITS;
   extern __shared__ uint8_t smem_raw[];
   // y_full[b]: the first products of Y buffer b are in tensor memory;
   // y_empty[b]: the epilogue is done with buffer b (Y read, and with the QJL
@@ -443,7 +458,7 @@ __global__ void __launch_bounds__(F32 ? kThreadsF32 : kThreads, 1)
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const LaneTranspose transpose(lane);          // (used by the token-transposed value codes)
-    float bnd[kLevels - 1];
+    float bnd[kBounds];
 #pragma unroll
     for (int i = 0; i < kLevels - 1; ++i) bnd[i] = a.bounds[i];
     float lev[kLevels];                           // read only by the QJL residual
@@ -554,12 +569,57 @@ __global__ void __launch_bounds__(F32 ? kThreadsF32 : kThreads, 1)
       // y = 0 against t): one product per boundary instead of one per coordinate
       const float n_eff = n > 0.f ? n : 1.f;
       const float ns = stored_norm(n, a.norm16);  // the residual is against the norm as stored
-      float tn[kLevels - 1];
+      float tn[kBounds];
 #pragma unroll
       for (int i = 0; i < kLevels - 1; ++i) tn[i] = bnd[i] * n_eff;
 
       ptx::tc_fence_after();
-      uint32_t planes[BITS];
+      if constexpr (POLAR) {
+        uint32_t yr[32];
+        ptx::tmem_ld32(yb + 32 * g, yr);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&y_empty[b]);            // this buffer may take the tile after next
+        uint8_t* const pc = smem + L::kPolar0 + row * 128;   // [0, 64) level 1, [64, 127) levels 2..7
+        float* const r5 = reinterpret_cast<float*>(smem + L::kPolar0 + kTileRows * 128) + row * 4;
+        // levels 1..5 over coordinates 32 g .. 32 g + 31: at level L this
+        // thread's pairs are g 2^(5-L) + i; radii overwrite the front of v
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(yr[j]);
+#pragma unroll
+        for (int lvl = 1; lvl <= 5; ++lvl) {
+#pragma unroll
+          for (int i = 0; i < (32 >> lvl); ++i) {
+            const float first = v[2 * i], second = v[2 * i + 1];
+            const int p = (g << (5 - lvl)) + i;
+            const int code = polar_angle_code(second, first, lvl == 1);
+            if (lvl == 1) pc[p] = static_cast<uint8_t>(code);
+            else pc[64 + polar_upper_offset(lvl) + p] = static_cast<uint8_t>(code);
+            v[i] = sqrtf(fmaf(first, first, second * second));
+          }
+        }
+        r5[g] = v[0];
+        epi_sync_any(false);                      // every thread's codes and level-5 radius are staged
+        if (g == 0) {
+          pc[64 + 60] = static_cast<uint8_t>(polar_angle_code(r5[1], r5[0], false));
+          pc[64 + 61] = static_cast<uint8_t>(polar_angle_code(r5[3], r5[2], false));
+          const float r60 = sqrtf(fmaf(r5[0], r5[0], r5[1] * r5[1]));
+          const float r61 = sqrtf(fmaf(r5[2], r5[2], r5[3] * r5[3]));
+          pc[64 + 62] = static_cast<uint8_t>(polar_angle_code(r61, r60, false));
+        }
+        epi_sync_any(false);
+        if (dst >= 0) {
+          uint4 wv;
+          wv.x = polar_record_word(pc, pc + 64, 4 * g);
+          wv.y = polar_record_word(pc, pc + 64, 4 * g + 1);
+          wv.z = polar_record_word(pc, pc + 64, 4 * g + 2);
+          wv.w = polar_record_word(pc, pc + 64, 4 * g + 3);
+          reinterpret_cast<uint4*>(a.codes + dst * (4 * kPolarRecordWords))[g] = wv;
+          if (g == 0) reinterpret_cast<float*>(a.norm)[dst] = n;
+        }
+        continue;                                 // (the next tile's first barrier frees the staged codes)
+      }
+      uint32_t planes[kPlanes];
       float rs = 0.f;
       {
         uint32_t yr[32];
@@ -567,7 +627,9 @@ __global__ void __launch_bounds__(F32 ? kThreadsF32 : kThreads, 1)
 #pragma unroll
         for (int p = 0; p < BITS; ++p) planes[p] = 0;
         float r[32];
-        if constexpr (BITS == 2 || BITS == 3 || (BITS == 4 && !QJL)) {
+        if constexpr (POLAR) {
+          // (handled above)
+        } else if constexpr (BITS == 2 || BITS == 3 || (BITS == 4 && !QJL)) {
           for_each_index(
               [&](auto jc) {
                 constexpr int j = decltype(jc)::value;
@@ -662,7 +724,7 @@ __global__ void __launch_bounds__(F32 ? kThreadsF32 : kThreads, 1)
 template <int BITS, bool QJL, bool TRANS, bool F32>
 cudaError_t launch_bits(const CUtensorMap& x_map, const CUtensorMap& w_map, const QuantizeArgs& a, int grid,
                         cudaStream_t stream) {
-  const int smem = Layout<QJL, F32>::kBytes + 1024;
+  const int smem = (BITS == 0 ? Layout<QJL, F32>::kPolarBytes : Layout<QJL, F32>::kBytes) + 1024;
   cudaError_t err = cudaFuncSetAttribute(quantize_tc_kernel<BITS, QJL, TRANS, F32>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
@@ -694,6 +756,9 @@ cudaError_t launch_quantize_tc(const QuantizeArgs& a, const CUtensorMap& x_map, 
   const int n_tiles = ((a.n_tokens + kTileRows - 1) / kTileRows) * a.n_kv;
   const int grid = n_tiles < num_sms ? n_tiles : num_sms;
   switch (a.bits) {
+    case 0:   // PolarQuant records
+      return f32 ? launch_bits<0, false, false, true>(x_map, w_map, a, grid, stream)
+                 : launch_bits<0, false, false, false>(x_map, w_map, a, grid, stream);
     case 1: return launch_dtype<1>(x_map, w_map, a, grid, f32, stream);
     case 2: return launch_dtype<2>(x_map, w_map, a, grid, f32, stream);
     case 3: return launch_dtype<3>(x_map, w_map, a, grid, f32, stream);
