@@ -14,9 +14,9 @@
 // * The other operand (a_S q_rot, the projected query q_s, and the softmax
 //   weights) is split into e4m3 pieces x = sum_i p_i 16^-i / sigma (sigma a
 //   power of two), one piece per GEMM column; each piece holds about four more
-//   bits: 6 pieces for query coefficients (fp32-level scores), 3 for softmax
-//   weights (relative 2^-13).  Products are exact and accumulate in fp32 in
-//   tensor memory.
+//   bits: 5 pieces for query coefficients (4 with eight query heads per KV
+//   head, relative 2^-17), 3 for softmax weights (relative 2^-13).  Products
+//   are exact and accumulate in fp32 in tensor memory.
 //
 // Scores:  D_S[token][head, piece] = sum_k A_K[token][k] B_K[head, piece][k]
 //          (A_K: the token's key sign planes, written into tensor memory by the
@@ -25,16 +25,18 @@
 //          (A_V: the sign planes of one coordinate across 128 tokens, read
 //          directly from the token-transposed value field by the thread that
 //          owns the coordinate; B_V: pieces of exp(s - m) n_v).
-// The output of a CTA is the same split-K partial (m, l, acc[128]) the SIMT
-// kernel writes, merged by the same finish kernel.
-//
-// One CTA of 288 threads per (512-token chunk, KV head, sequence).  Warps 0-7
+// A persistent grid of 288-thread CTAs (two per SM) takes the real chunks of
+// the batch -- items (sequence, KV head, 512- or 256-token chunk) numbered in
+// that order -- in equal contiguous runs; a CTA merges the consecutive items
+// of one (sequence, KV head) as it goes and writes one split-K partial
+// (m, l, acc[128]) per such segment, which the CTA that completes a group
+// merges (atomic ticket) or a merge launch does.  Warps 0-7
 // build operands: threads t and t + 128 share tensor-memory lane t and split
 // its work (two of the four 32-bit words of every sign plane, half of the
 // accumulator columns, half of the operand pieces).  Warp 8 is the control
-// warp: lane k copies block k of the chunk's packed fields (contiguous per
-// block and head) into shared memory with bulk asynchronous copies, then an
-// elected lane issues every MMA.  The two sides meet only on mbarriers: the
+// warp: lane k copies block k of an item's packed fields (contiguous per
+// block and head) into shared memory with bulk asynchronous copies, one item
+// ahead, and an elected lane issues every MMA.  The two sides meet only on mbarriers: the
 // builders store a tile's sign planes into one of two tensor-memory slots and
 // arrive; the control warp issues that tile's MMAs and commits; the builders
 // build the next tile meanwhile and wait on the commit only to read the
