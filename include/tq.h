@@ -260,9 +260,11 @@ tq_status tq_decode_step_prepare(const tq_codebook* book, const void* k_new, con
  *                         (device float32 [batch][n_q_heads][d]) it leaves the
  *                         final output there instead, as tq_decode_attention's
  *                         last two stages do (the tensor-core kernel merges
- *                         each (sequence, KV head) in place; after the CUDA-core
- *                         kernel the merge runs as a second launch); calling
- *                         tq_decode_finish afterwards is allowed and redundant;
+ *                         each (sequence, KV head) in place or is followed by
+ *                         a merge launch, as tq_decode_plan reports; after the
+ *                         CUDA-core kernel the merge runs as a second launch);
+ *                         calling tq_decode_finish afterwards is allowed and
+ *                         redundant;
  *   tq_decode_finish   -- merge the partials, divide by the softmax sum and
  *                         back-rotate by R^T into `out`.
  * Argument meaning, checks and errors are those of tq_decode_attention. */
