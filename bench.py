@@ -408,7 +408,8 @@ def decode_summary(res, world, dev):
         "plan": wl.plan,
         "partials": {"kernel": wl.kernel_name(), "launch_ms": part_ms, "achieved_gbs": achieved,
                      "frac": achieved / peak, "peak_source": src + " hbm_gbs",
-                     "algorithmic_bytes_per_launch": wl.cache_bytes},
+                     "algorithmic_bytes_per_launch": wl.cache_bytes,
+                     "traffic": recorded_traffic(wl.kernel_name(), wl.name)},
         "context_tokens": int(wl.ctx.sum()), "l2": l2_note(len(wl.caches)),
         "norm_bits": wl.book.norm_bits,
     }
