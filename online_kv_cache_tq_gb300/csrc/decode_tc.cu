@@ -320,8 +320,11 @@ TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size, 
   l.off_bmse = o; o += l.n1 * l.pk * 128;
   l.off_bqjl = o; o += l.n2 * 128;
   l.off_bv = o; o += (chunk / kTile) * l.no * 128;
+  // s1 (the other half's output sums, and scratch of the final merges) lies
+  // inside s0 past its first G x kTile floats: the scores are dead by the time
+  // s1 is written, and the merges use s0's first part and s1 together
   l.off_s0 = o; o += group * chunk * 4;
-  l.off_s1 = o; o += group * kTile * 4;
+  l.off_s1 = l.off_s0 + group * kTile * 4;
   l.off_sacc = o; o += group * kTile * 4;
   l.off_kc = o; o += chunk * l.kbytes;
   l.off_kq = o; o += chunk * 16;
@@ -490,10 +493,16 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   constexpr int N1 = score_cols(G), NO = value_cols(G);
   const int t = threadIdx.x;
 
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte aligned, as an offset from smem_raw so that accesses stay shared-space
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
+
   // ---- work split: the real chunks of every sequence, an equal run per CTA ----
   __shared__ int scan_s[kThreads / 32];
   __shared__ int split_s[3];                    // (b, kvh, chunk) of this CTA's first item
-  __shared__ int empty_s[kThreads];             // sequences without context (CTA 0, merging launch)
+  // sequences without context (CTA 0 of a merging launch), in the B operand
+  // region, which is zeroed after this prologue (at least 2 KB at any shape)
+  int* const empty_s = reinterpret_cast<int*>(smem);
   __shared__ int n_empty_s;
   int n_chunks_total = 0;
   int ch0 = 0, excl0 = 0;                       // pass 0: this thread's sequence (b = t)
@@ -564,14 +573,11 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   const int vblock = v_bits * 16 * bs;               // value code bytes per (block, head)
   const int k_slots = KB > 0 ? 2 : L.k_slots;        // the fixed build is launched with two key slots
 
-  extern __shared__ uint8_t smem_raw[];
-  // 1024-byte aligned, as an offset from smem_raw so that accesses stay shared-space
-  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* b_mse = smem + L.off_bmse;
   uint8_t* b_qjl = smem + L.off_bqjl;
   uint8_t* b_v = smem + L.off_bv;
   float* s0 = reinterpret_cast<float*>(smem + L.off_s0);           // [G][CH] scores
-  float* s1 = reinterpret_cast<float*>(smem + L.off_s1);           // [G][kTile]: output halves
+  float* s1 = reinterpret_cast<float*>(smem + L.off_s1);           // [G][kTile]: output halves (inside s0)
   float* seg_acc = reinterpret_cast<float*>(smem + L.off_sacc);    // [G][kTile]: the segment's running acc
   uint8_t* kc_s = smem + L.off_kc;                                  // [CH][kbytes]
   uint8_t* kq_s = smem + L.off_kq;                                  // [CH][16]
@@ -1239,13 +1245,32 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   }
 }
 
+// Whether two CTAs of this layout fit an SM: half of tensor memory each, and
+// dynamic plus static shared memory (under kStaticSmemBound for every build)
+// plus the driver's per-CTA reservation within half of the SM's shared memory
+// (queried once from the current device; 228 KB and 1 KB if the query fails).
+constexpr int kStaticSmemBound = 1536;
+bool two_ctas_fit(const TcLayout& l) {
+  static const int per_sm_half = [] {
+    int dev = 0, per_sm = 0, reserved = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
+      per_sm = 228 * 1024;
+      reserved = 1024;
+    }
+    return per_sm / 2 - reserved;
+  }();
+  return l.tmem <= 256 && l.smem_bytes + kStaticSmemBound <= per_sm_half;
+}
+
 // Chunk length of the tensor-core kernel for this shape: 512 tokens, or 256
 // when a 512-token layout would not leave room for two CTAs per SM and the
 // blocks divide 256 (the partials are per segment, so the chunk length is the
 // kernel's own choice).
 int tc_chunk(const DecodeArgs& a) {
   const TcLayout l = tc_layout(a.group, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size, 512);
-  const bool two = l.tmem <= 256 && l.smem_bytes <= 108 * 1024;
+  const bool two = two_ctas_fit(l);
   return !two && 256 % a.block_size == 0 ? 256 : 512;
 }
 
@@ -1264,7 +1289,7 @@ bool tc_decode_supported(const DecodeArgs& a, bool walsh_ok) {
 int tc_grid(const DecodeArgs& a) {
   const int chunk = tc_chunk(a);
   const TcLayout l = tc_layout(a.group, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size, chunk);
-  const int per_sm = (l.tmem <= 256 && l.smem_bytes <= 108 * 1024) ? 2 : 1;
+  const int per_sm = two_ctas_fit(l) ? 2 : 1;
   const int max_items = (a.max_context + chunk - 1) / chunk;
   const long long bound = static_cast<long long>(a.batch) * a.n_kv * max_items;
   const long long slots = static_cast<long long>(per_sm) * (a.num_sms > 0 ? a.num_sms : 148);

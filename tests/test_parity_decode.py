@@ -324,10 +324,10 @@ def test_decode_plan_for_the_workloads():
     # fewer than CTAs, about four segments each), the 70B paged batch (512
     # groups) takes a merge launch with a CTA per group, and the long-context
     # layer (8 groups of about 40 segments) a merge launch with a CTA per
-    # query head; its 4-bit-key layout runs 256-token items (a 512-token one
-    # would not fit two CTAs per SM)
+    # query head; its 4-bit-key layout also fits two CTAs per SM with 512-token
+    # items (the output-exchange buffer lies inside the score buffer)
     expect = {"c2_llama3_8b_decode": (1, 512, 0), "c5_llama3_70b_paged": (0, 512, 512),
-              "c4_long_context": (0, 256, 64)}
+              "c4_long_context": (0, 512, 64)}
     for name, (fused, chunk, merge_ctas) in expect.items():
         cfg = W.CONFIGS[name]
         book = B.Codebook(k_bits=cfg["k_bits"], v_bits=cfg["v_bits"], qjl_m=cfg["qjl_m"], seed=cfg["seed"],
