@@ -209,8 +209,10 @@ __device__ __forceinline__ int cta_scan(int v, int* excl, int* warp_s) {
 // up to a power of two takes P - 1 + log2(32 / P) shuffles instead of 5 N.
 // Warps 0-3 and 4-7 are the two builder halves, which own different query
 // heads, so callers combine the four totals of one half in warp order.
+// With `all`, the first barrier also ANDs *all over the builders (as
+// builder_all).
 template <int N, typename Op>
-__device__ __forceinline__ void warp_totals(const float (&v)[N], float* red, Op op) {
+__device__ __forceinline__ void warp_totals(const float (&v)[N], float* red, Op op, bool* all = nullptr) {
   constexpr int P = N <= 1 ? 1 : N <= 2 ? 2 : N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : 32;
   static_assert(N <= 32, "at most 32 values");
   const int lane = threadIdx.x & 31;
@@ -231,7 +233,8 @@ __device__ __forceinline__ void warp_totals(const float (&v)[N], float* red, Op 
   }
 #pragma unroll
   for (int off = 16 / P; off > 0; off >>= 1) cur[0] = op(cur[0], __shfl_xor_sync(0xffffffffu, cur[0], off));
-  builder_sync();                               // the previous reduction's totals were read
+  if (all != nullptr) *all = builder_all(*all);  // the previous reduction's totals were read
+  else builder_sync();
   if ((lane & (32 / P - 1)) == 0 && idx < N) red[(threadIdx.x >> 5) * N + idx] = cur[0];
   builder_sync();
 }
@@ -856,36 +859,47 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       float mx[HG + 1];                           // owned heads' score max, then the value-norm max
 #pragma unroll
       for (int j = 0; j <= HG; ++j) mx[j] = j < HG ? -INFINITY : 0.f;
-      // (templated on the half, so that the owned heads are compile-time indices)
-      auto read_scores_half = [&](int i, auto half_c) {
+      // (templated on the half, so that the owned heads are compile-time indices;
+      // `release` runs once the last accumulator column is in registers, so the
+      // next tile's MMAs may start while the scores are being formed)
+      auto read_scores_half = [&](int i, auto half_c, auto release) {
         constexpr int H0 = decltype(half_c)::value * HG;
         if constexpr (H0 < G) {
           const int tl = i * kTile + lane;
           const bool valid = tl < x.n_local && blk_ok[tl >> bs_shift];
+          // a head's pieces p_0 .. p_{Q-1} sum as p_0 + (p_1 + (p_2 + ...) / 16) / 16 (Horner: Q - 1 FMAs)
+          constexpr int QP = q_pieces(G);
           float am[HG], aq[HG];
 #pragma unroll
           for (int j = 0; j < HG; ++j) am[j] = aq[j] = 0.f;
-#pragma unroll
-          for (int c0 = 0; c0 < HC; c0 += 16) {
+          static_assert(HC == 16, "one 16-column load per half and kind");
+          {
             uint32_t v[16];
-            ptx::tmem_ld16(tmem + row_addr + L.col_s + (H0 / HG) * HC + c0, v);
+            ptx::tmem_ld16(tmem + row_addr + L.col_s + (H0 / HG) * HC, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int hj = (c0 + j) / q_pieces(G), piece = (c0 + j) % q_pieces(G);
-              if (hj < HG) am[hj] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), am[hj]);
+            for (int j = 0; j < HG; ++j) {
+              float r = __uint_as_float(v[j * QP + QP - 1]);
+#pragma unroll
+              for (int i = QP - 2; i >= 0; --i) r = fmaf(r, 0.0625f, __uint_as_float(v[j * QP + i]));
+              am[j] = r;
             }
             if (qjl) {
-              ptx::tmem_ld16(tmem + row_addr + L.col_s + N1 + (H0 / HG) * HC + c0, v);
+              ptx::tmem_ld16(tmem + row_addr + L.col_s + N1 + (H0 / HG) * HC, v);
+              release();
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int hj = (c0 + j) / q_pieces(G), piece = (c0 + j) % q_pieces(G);
-                if (hj < HG) aq[hj] = fmaf(__uint_as_float(v[j]), inv16_pow(piece), aq[hj]);
+              for (int j = 0; j < HG; ++j) {
+                float r = __uint_as_float(v[j * QP + QP - 1]);
+#pragma unroll
+                for (int i = QP - 2; i >= 0; --i) r = fmaf(r, 0.0625f, __uint_as_float(v[j * QP + i]));
+                aq[j] = r;
               }
+            } else {
+              release();
             }
           }
           const float kn = norm_at(kn_s, tl), kr = norm_at(kr_s, tl);   // (tl < CH: in bounds; selected below)
-          const float nk = valid ? kn : 0.f;
-          const float gk = valid && qjl ? kr * a.qjl_coef : 0.f;
+          const float nk = valid ? a.scale * kn : 0.f;
+          const float gk = valid && qjl ? a.scale * kr * a.qjl_coef : 0.f;
 #pragma unroll
           for (int j = 0; j < HG; ++j) {
             const int h = H0 + j;
@@ -894,23 +908,25 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             // across the key phase they would take sixteen)
             const float mse = fmaf(am[j], cst_s[0][h], -cst_s[2][h]);
             const float qv = qjl ? fmaf(aq[j], cst_s[1][h], -cst_s[3][h]) : 0.f;
-            const float sc = valid ? a.scale * fmaf(nk, mse, gk * qv) : -INFINITY;
+            const float sc = valid ? fmaf(nk, mse, gk * qv) : -INFINITY;
             s0[h * CH + i * kTile + kpos_lane] = sc;   // (in K order: the weights read four at once)
             mx[j] = fmaxf(mx[j], sc);
           }
+        } else {
+          release();                              // (G = 1: the second half owns no head)
         }
-      };
-      auto read_scores = [&](int i) {
-        if (half == 0) read_scores_half(i, std::integral_constant<int, 0>{});
-        else read_scores_half(i, std::integral_constant<int, 1>{});
       };
       // wait for the MMAs of key tile i (global index g), read its accumulators, release them
       auto take_scores = [&](int i, int g) {
         ok = ok && wait_phase(&kdone, g & 1, abort, a.error);
         ptx::tc_fence_after();
-        if (ok) read_scores(i);
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&sfree);
+        auto release = [&]() {
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&sfree);
+        };
+        if (!ok) release();
+        else if (half == 0) read_scores_half(i, std::integral_constant<int, 0>{}, release);
+        else read_scores_half(i, std::integral_constant<int, 1>{}, release);
       };
 
       // ---- scores: the planes of tile i are built while the MMAs of tile i - 1 run ----
@@ -955,15 +971,17 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       if (ok) take_scores(x.n_tiles - 1, k0 + x.n_tiles - 1);
       ptx::mbar_arrive(&kfree);                   // this item's key fields are no longer read
       ok = ok && wait_phase(&vin, seq & 1, abort, a.error);
-      ok = builder_all(ok && *abort == 0);
-      if (!ok) break;
 
       // ---- softmax max over the chunk; B_V pieces of exp(s - m) n_v ----
+      // (after a failed wait the loop reads stale but in-bounds norms, and every
+      // builder leaves at the barrier that ANDs the flags)
       for (int i = t; i < x.n_tiles * kTile; i += kBuilders)
         mx[HG] = fmaxf(mx[HG], i < x.n_local && blk_ok[i >> bs_shift] ? norm_at(vn_s, i) : 0.f);
       {
         // chunk max of the owned heads over this half's warps; value-norm max over all
-        warp_totals(mx, red_s, MaxOp());
+        ok = ok && *abort == 0;
+        warp_totals(mx, red_s, MaxOp(), &ok);
+        if (!ok) break;
         float vmax = 0.f;
 #pragma unroll
         for (int w = 0; w < kBuilders / 32; ++w) vmax = fmaxf(vmax, red_s[w * (HG + 1) + HG]);
@@ -1028,8 +1046,9 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         }
       }
       if (t == 0) sv_s = sv;
+      // (no barrier: every builder's B_V pieces precede its first vfull arrival,
+      // and the control warp issues a value MMA only after all 256 arrived)
       ptx::fence_async_shared();
-      builder_sync();                             // every B_V piece is in place before the first value MMA
 
       // ---- values: lane d owns coordinate d; units of two sign planes rotate through the slots ----
       int last_slot = 0, last_wrap = 0;
@@ -1079,12 +1098,9 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           ptx::mbar_arrive(&vfull[slot]);
         }
       }
-      // the item's last commit (a commit covers every earlier MMA)
-      if (ok) ok = wait_phase(&vdone[last_slot], last_wrap & 1, abort, a.error);
-      ptx::tc_fence_after();
-
       {
-        // sums of e and of e n_v per head: warp w holds head w % G's, added in warp order
+        // sums of e and of e n_v per head (while the last value MMAs run): warp w holds head w % G's,
+        // added in warp order
         const float lw[2] = {lw0, lw1};
         warp_totals(lw, red_s, SumOp());
         if (t < G) {
@@ -1097,6 +1113,10 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           wsum_s[t] = sw;
         }
       }
+
+      // the item's last commit (a commit covers every earlier MMA)
+      if (ok) ok = wait_phase(&vdone[last_slot], last_wrap & 1, abort, a.error);
+      ptx::tc_fence_after();
 
       // ---- partial output of this chunk: half h reads the planes s with s % 2 == h ----
       float o[G];
@@ -1145,7 +1165,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           }
         }
       }
-      builder_sync();                             // s1, stat_s and wsum_s are free for the next item
+      // (no barrier before the next item: the ones in its key and softmax phases
+      // come before anything there writes s1, stat_s, wsum_s or seg_ml_s)
       Item y;
       const bool more = cursor.next(a, bs_shift, y);
       if (ok && (!more || y.group != x.group)) {
