@@ -344,6 +344,14 @@ TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size, 
 
 namespace {
 
+// 2^x on the special-function unit (ex2.approx.ftz); the softmax takes
+// exp(y) as 2^(y log2 e).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // Time-bounded wait on an mbarrier phase by the calling thread (suspending
 // between polls); false after a timeout anywhere in the CTA.
 // The result is made warp-uniform, since tensor-memory loads and stores that
@@ -867,8 +875,22 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         if constexpr (H0 < G) {
           const int tl = i * kTile + lane;
           const bool valid = tl < x.n_local && blk_ok[tl >> bs_shift];
-          // a head's pieces p_0 .. p_{Q-1} sum as p_0 + (p_1 + (p_2 + ...) / 16) / 16 (Horner: Q - 1 FMAs)
+          // a head's pieces p_0 .. p_{Q-1} sum as p_0 + (p_1 + (p_2 + ...) / 16) / 16 (Horner: Q - 1 FMAs);
+          // four pieces as (p_0 + p_2 / 256) + (p_1 + p_3 / 256) / 16, the first step on both pairs at once
           constexpr int QP = q_pieces(G);
+          auto piece_sum = [](const uint32_t* v) {
+            if constexpr (QP == 4) {
+              const float2 h = __ffma2_rn(make_float2(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                                          make_float2(0.00390625f, 0.00390625f),
+                                          make_float2(__uint_as_float(v[0]), __uint_as_float(v[1])));
+              return fmaf(h.y, 0.0625f, h.x);
+            } else {
+              float r = __uint_as_float(v[QP - 1]);
+#pragma unroll
+              for (int i = QP - 2; i >= 0; --i) r = fmaf(r, 0.0625f, __uint_as_float(v[i]));
+              return r;
+            }
+          };
           float am[HG], aq[HG];
 #pragma unroll
           for (int j = 0; j < HG; ++j) am[j] = aq[j] = 0.f;
@@ -877,22 +899,12 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             uint32_t v[16];
             ptx::tmem_ld16(tmem + row_addr + L.col_s + (H0 / HG) * HC, v);
 #pragma unroll
-            for (int j = 0; j < HG; ++j) {
-              float r = __uint_as_float(v[j * QP + QP - 1]);
-#pragma unroll
-              for (int i = QP - 2; i >= 0; --i) r = fmaf(r, 0.0625f, __uint_as_float(v[j * QP + i]));
-              am[j] = r;
-            }
+            for (int j = 0; j < HG; ++j) am[j] = piece_sum(v + j * QP);
             if (qjl) {
               ptx::tmem_ld16(tmem + row_addr + L.col_s + N1 + (H0 / HG) * HC, v);
               release();
 #pragma unroll
-              for (int j = 0; j < HG; ++j) {
-                float r = __uint_as_float(v[j * QP + QP - 1]);
-#pragma unroll
-                for (int i = QP - 2; i >= 0; --i) r = fmaf(r, 0.0625f, __uint_as_float(v[j * QP + i]));
-                aq[j] = r;
-              }
+              for (int j = 0; j < HG; ++j) aq[j] = piece_sum(v + j * QP);
             } else {
               release();
             }
@@ -1005,14 +1017,21 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       {
         const int q = t & 31, gq = q >> 3, i = q & 7;
         const int kp0 = 32 * gq + 4 * i;
+        // ib: a power of two, so lw1 is summed ib-scaled and rescaled exactly after the loop
         const float ib = 2.f * bit_inv_scale(i) * sv;
+        constexpr float kLog2e = 1.4426950408889634f;
+        const float2 l2e = make_float2(kLog2e, kLog2e);
+        const float2 nml = make_float2(-mq * kLog2e, -mq * kLog2e);   // (the same rounding for every token)
         const int units = x.n_tiles * 32 * G;
         for (int u = t; u < units; u += kBuilders) {
           const int tile = u / (32 * G);
           const int tl0 = tile * kTile + 32 * gq + i;           // tokens tl0 + 8 k
           const float4 sc = *reinterpret_cast<const float4*>(s0 + hq * CH + tile * kTile + kp0);
           const bool blk_valid = blk_ok[tl0 >> bs_shift] != 0;   // (the four share a 32-token group)
-          const float sk[4] = {sc.x, sc.y, sc.z, sc.w};
+          // exp(s - m) = 2^(s log2 e - m log2 e), two tokens per fused multiply-add
+          const float2 a01 = __ffma2_rn(make_float2(sc.x, sc.y), l2e, nml);
+          const float2 a23 = __ffma2_rn(make_float2(sc.z, sc.w), l2e, nml);
+          const float ak[4] = {a01.x, a01.y, a23.x, a23.y};
           float w[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -1020,12 +1039,12 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             const bool valid = blk_valid && tl < x.n_local;
             const float vn = norm_at(vn_s, tl);                  // (tl < CH: in bounds; selected below)
             // (selects, not branches: the exponent of an invalid slot may be nan)
-            const float ex = __expf(sk[k] - mq);
+            const float ex = ex2_approx(ak[k]);
             const float e = valid && mq != -INFINITY ? ex : 0.f;
-            const float nv = valid ? vn : 0.f;
+            const float nvb = valid ? vn * ib : 0.f;
             lw0 += e;
-            lw1 = fmaf(e, nv, lw1);
-            w[k] = e * nv * ib;
+            lw1 = fmaf(e, nvb, lw1);
+            w[k] = e * nvb;
           }
           uint8_t* rows = b_v + tile * L.no * 128;
 #pragma unroll
@@ -1037,13 +1056,18 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             if (p + 1 < kVPieces) {               // each piece is the e4m3 rounding of what is left, times 16
               const float2 bl = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3)));
               const float2 bh = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
-              w[0] = (w[0] - bl.x) * 16.f;
-              w[1] = (w[1] - bl.y) * 16.f;
-              w[2] = (w[2] - bh.x) * 16.f;
-              w[3] = (w[3] - bh.y) * 16.f;
+              // (w - b) exactly (b is w's nearest e4m3 value), then times 16; two tokens per instruction
+              const float2 m1 = make_float2(-1.f, -1.f), x16 = make_float2(16.f, 16.f);
+              const float2 d01 = __fmul2_rn(__ffma2_rn(bl, m1, make_float2(w[0], w[1])), x16);
+              const float2 d23 = __fmul2_rn(__ffma2_rn(bh, m1, make_float2(w[2], w[3])), x16);
+              w[0] = d01.x;
+              w[1] = d01.y;
+              w[2] = d23.x;
+              w[3] = d23.y;
             }
           }
         }
+        lw1 *= 1.f / ib;                          // exact: ib is a power of two
       }
       if (t == 0) sv_s = sv;
       // (no barrier: every builder's B_V pieces precede its first vfull arrival,
