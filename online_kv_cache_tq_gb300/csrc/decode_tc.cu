@@ -610,15 +610,14 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
   __shared__ float red_s[(kBuilders / 32) * (2 * half_heads(G) + 1)];   // warp totals of up to 2 HG + 1 values
-  __shared__ float stat_s[2][G];                // chunk max, chunk sum per head
+  __shared__ float stat_s[G];                   // chunk max per head
+  __shared__ float4 mrg_s[G];                   // per head: the factors of the segment merge (so, si / sv, -a_sum wsum si)
   __shared__ int blk_ok_s[2][CH / 32];          // per item parity: physical block of each block slot is valid
   __shared__ float sv_s;                        // piece scale of the softmax weights
-  __shared__ float wsum_s[G];                   // sum over the chunk of e n_v per head
-  __shared__ float cst_s[4][G];                 // per head: 1/sigma_mse, 1/sigma_qjl, ones_mse, ones_qjl
+  __shared__ float4 cst_s[G];                   // per head: 1/sigma_mse, 1/sigma_qjl, -ones_mse, -ones_qjl
   __shared__ float vw_s[8];                     // odd Walsh coefficients of the value codebook
   __shared__ int4 pend_s[kMaxPending];          // groups whose merge this CTA owes: (entry base, n_seg, qbase)
   __shared__ int n_pend_s;
-  __shared__ float seg_ml_s[2][2][G];           // [item parity][max, sum][head] of the running segment
 
   const bool builder = t < kBuilders;
   const int lane = t & (kTile - 1);             // tensor-memory lane (token or coordinate)
@@ -805,20 +804,14 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     int vslot = 0, vwrap = 0;                     // value unit counter as (slot, times round the slots)
     const int wpd_shift = bs_shift - 5;         // log2 of the words per coordinate in a block
     const int kpos_lane = k_position(lane);     // K position of this lane's token in a tile
-    // The CTA's segment of the current group is merged chunk by chunk: the
-    // running max and sum of every head in seg_ml_s (item seq reads parity
-    // seq & 1 and writes the other), acc[coordinate lane] of head h in
-    // seg_acc, read and written only by the thread that owns (h, lane).
-    const bool ml_writer = (t & 127) == 0;        // one thread per half writes the heads it owns
+    // The CTA's segment of the current group is merged chunk by chunk: thread
+    // t < G keeps head t's running max and sum in registers (seg_m, seg_l),
+    // acc[coordinate lane] of head h is in seg_acc, read and written only by
+    // the thread that owns (h, lane).
+    float seg_m = -INFINITY, seg_l = 0.f;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      if (h / HG != half) continue;
-      seg_acc[h * kTile + lane] = 0.f;
-      if (ml_writer) {
-        seg_ml_s[0][0][h] = -INFINITY;
-        seg_ml_s[0][1][h] = 0.f;
-      }
-    }
+    for (int h = 0; h < G; ++h)
+      if (h / HG == half) seg_acc[h * kTile + lane] = 0.f;
 
     if (t == 0) n_pend_s = 0;
 
@@ -851,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           const int h = t >> 2, k = t & 3;
           const float* hdr = reinterpret_cast<const float*>(a.ws_bk + static_cast<long long>(qbase + h) * a.bk_stride +
                                                             nk * kQPieces * 128);
-          cst_s[k][h] = hdr[k < 2 ? 2 + k : 4 + (k - 2)];
+          reinterpret_cast<float*>(cst_s + h)[k] = k < 2 ? hdr[2 + k] : -hdr[4 + (k - 2)];
         }
         ptx::fence_async_shared();
         builder_sync();
@@ -916,10 +909,12 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           for (int j = 0; j < HG; ++j) {
             const int h = H0 + j;
             if (h >= G) break;
-            // (the head's 1/sigma_mse, 1/sigma_qjl, ones_mse, ones_qjl from shared memory: kept in registers
-            // across the key phase they would take sixteen)
-            const float mse = fmaf(am[j], cst_s[0][h], -cst_s[2][h]);
-            const float qv = qjl ? fmaf(aq[j], cst_s[1][h], -cst_s[3][h]) : 0.f;
+            // (mse, qv) = (am / sigma_mse - ones_mse, aq / sigma_qjl - ones_qjl) in one paired FMA, the
+            // head's constants in one 16-byte shared-memory load (kept in registers across the key phase
+            // they would take sixteen); without QJL aq = 0 and gk = 0, so the second half drops out
+            const float4 c = cst_s[h];
+            const float2 mq2 = __ffma2_rn(make_float2(am[j], aq[j]), make_float2(c.x, c.y), make_float2(c.z, c.w));
+            const float mse = mq2.x, qv = mq2.y;
             const float sc = valid ? fmaf(nk, mse, gk * qv) : -INFINITY;
             s0[h * CH + i * kTile + kpos_lane] = sc;   // (in K order: the weights read four at once)
             mx[j] = fmaxf(mx[j], sc);
@@ -1000,7 +995,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
 #pragma unroll
         for (int j = 0; j < HG; ++j) {
           mx[j] = half_total<HG + 1>(red_s, half, j, MaxOp());
-          if ((t & 127) == 0 && half * HG + j < G) stat_s[0][half * HG + j] = mx[j];
+          if ((t & 127) == 0 && half * HG + j < G) stat_s[half * HG + j] = mx[j];
         }
         mx[HG] = vmax;
       }
@@ -1133,8 +1128,18 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             se += red_s[2 * w];
             sw += red_s[2 * w + 1];
           }
-          stat_s[1][t] = se;
-          wsum_s[t] = sw;
+          // head t: this chunk's (max, sum) into the segment's, and the factors every lane applies to its
+          // acc: acc so + (o / sv - a_sum wsum) si
+          const float mi = stat_s[t];
+          const float mn = fmaxf(seg_m, mi);
+          const float so = seg_m == -INFINITY ? 0.f : __expf(seg_m - mn);
+          const float si = mi == -INFINITY ? 0.f : __expf(mi - mn);
+          float a_sum = 0.f;                      // sum_S a_S: the -1 half of every sign product
+          for (int s = 0; s < pv; ++s) a_sum += vw_s[s];
+          const float sis = si / sv_s;            // exact: sv is a power of two
+          mrg_s[t] = make_float4(so, sis, -a_sum * sw * si, 0.f);
+          seg_m = mn;
+          seg_l = fmaf(seg_l, so, se * si);
         }
       }
 
@@ -1168,47 +1173,33 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         if (h / HG != half) s1[h * kTile + lane] = o[h];
       ok = builder_all(ok && *abort == 0);
       if (ok) {
-        const float inv_sv = 1.f / sv_s;          // exact: sv is a power of two
-        float a_sum = 0.f;                        // sum_S a_S: the -1 half of every sign product
-        for (int s = 0; s < pv; ++s) a_sum += vw_s[s];
-        // this chunk's (m, l, acc) into the segment's running values
-        const int par = seq & 1;
+        // this chunk's acc into the segment's running acc
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           if (h / HG != half) continue;
-          const float mr = seg_ml_s[par][0][h], lr = seg_ml_s[par][1][h];
-          const float mi = stat_s[0][h], li = stat_s[1][h];
-          const float ai = fmaf(o[h] + s1[h * kTile + lane], inv_sv, -a_sum * wsum_s[h]);
-          const float mn = fmaxf(mr, mi);
-          const float so = mr == -INFINITY ? 0.f : __expf(mr - mn);
-          const float si = mi == -INFINITY ? 0.f : __expf(mi - mn);
-          seg_acc[h * kTile + lane] = fmaf(seg_acc[h * kTile + lane], so, ai * si);
-          if (ml_writer) {
-            seg_ml_s[par ^ 1][0][h] = mn;
-            seg_ml_s[par ^ 1][1][h] = fmaf(lr, so, li * si);
-          }
+          const float4 c = mrg_s[h];
+          seg_acc[h * kTile + lane] = fmaf(seg_acc[h * kTile + lane], c.x, fmaf(o[h] + s1[h * kTile + lane], c.y, c.z));
         }
       }
       // (no barrier before the next item: the ones in its key and softmax phases
-      // come before anything there writes s1, stat_s, wsum_s or seg_ml_s)
+      // come before anything there writes s1, stat_s or mrg_s)
       Item y;
       const bool more = cursor.next(a, bs_shift, y);
       if (ok && (!more || y.group != x.group)) {
         // ---- the segment ends: its partials go to entry slot group + CTA ----
         const long long ent0 = (static_cast<long long>(x.group) + blockIdx.x) * G;
-        const int par = (seq & 1) ^ 1;            // where this item left the running max and sum
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           if (h / HG != half) continue;
-          float* part = a.ws_part + (ent0 + h) * kPartStride;
-          part[4 + lane] = seg_acc[h * kTile + lane];
+          a.ws_part[(ent0 + h) * kPartStride + 4 + lane] = seg_acc[h * kTile + lane];
           seg_acc[h * kTile + lane] = 0.f;
-          if (ml_writer) {
-            part[0] = seg_ml_s[par][0][h];
-            part[1] = seg_ml_s[par][1][h];
-            seg_ml_s[par][0][h] = -INFINITY;
-            seg_ml_s[par][1][h] = 0.f;
-          }
+        }
+        if (t < G) {
+          float* part = a.ws_part + (ent0 + t) * kPartStride;
+          part[0] = seg_m;
+          part[1] = seg_l;
+          seg_m = -INFINITY;
+          seg_l = 0.f;
         }
         const int f_cta = x.first_cta(per_cta);
         const int n_seg = x.last_cta(per_cta) - f_cta + 1;

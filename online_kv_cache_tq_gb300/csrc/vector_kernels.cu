@@ -195,6 +195,10 @@ __device__ __forceinline__ void prepare_queries(const DecodeArgs& a, int v0, int
   for (int j = 0; j < QN; ++j) acc[j] = 0.f;
   if (active) {
     const float* w = (proj ? a.St : a.Rt) + o;
+    // even and odd terms in the two halves of a paired FMA, added at the end
+    float2 acc2[QN];
+#pragma unroll
+    for (int j = 0; j < QN; ++j) acc2[j] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k0 = 0; k0 < kDim; k0 += 32) {
       float v[32];
@@ -205,12 +209,12 @@ __device__ __forceinline__ void prepare_queries(const DecodeArgs& a, int v0, int
 #pragma unroll
         for (int j = 0; j < QN; ++j) {
           const float4 x = *reinterpret_cast<const float4*>(&q_s[j][k0 + k]);
-          acc[j] = fmaf(v[k], x.x, acc[j]);
-          acc[j] = fmaf(v[k + 1], x.y, acc[j]);
-          acc[j] = fmaf(v[k + 2], x.z, acc[j]);
-          acc[j] = fmaf(v[k + 3], x.w, acc[j]);
+          acc2[j] = __ffma2_rn(make_float2(v[k], v[k + 1]), make_float2(x.x, x.y), acc2[j]);
+          acc2[j] = __ffma2_rn(make_float2(v[k + 2], v[k + 3]), make_float2(x.z, x.w), acc2[j]);
         }
     }
+#pragma unroll
+    for (int j = 0; j < QN; ++j) acc[j] = acc2[j].x + acc2[j].y;
 #pragma unroll
     for (int j = 0; j < QN; ++j)
       if (j < nv) a.ws_q[static_cast<long long>(v0 + j) * 2 * kDim + m * kDim + o] = acc[j];
