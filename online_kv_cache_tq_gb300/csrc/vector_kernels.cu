@@ -165,6 +165,34 @@ __device__ __forceinline__ void quantize_vectors(const QuantizeArgs& a, int v0, 
 // kManyAppends per tensor, where the matrix loads dominate.
 constexpr int kManyAppends = 256;
 
+// Totals of N values (a power of two, at most 32) over the 32 lanes of a warp:
+// at every shuffle step the value set halves (lanes with bit `off` set keep
+// the upper half and send the lower), N - 1 + log2(32 / N) shuffles in all.
+// Returns the total of value *idx, which every lane of its 32 / N lanes holds.
+template <int N, typename Op>
+__device__ __forceinline__ float halving_reduce(const float (&v)[N], int lane, int* idx, Op op) {
+  static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "a power of two up to 32");
+  float cur[N];
+#pragma unroll
+  for (int j = 0; j < N; ++j) cur[j] = v[j];
+  int base = 0;
+#pragma unroll
+  for (int n = N, off = 16; n > 1; n >>= 1, off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? cur[i] : cur[i + n / 2];
+      const float keep = upper ? cur[i + n / 2] : cur[i];
+      cur[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, off));
+    }
+    if (upper) base += n / 2;
+  }
+#pragma unroll
+  for (int off = 16 / N; off > 0; off >>= 1) cur[0] = op(cur[0], __shfl_xor_sync(0xffffffffu, cur[0], off));
+  *idx = base;
+  return cur[0];
+}
+
 // Query heads v0 .. v0 + nv - 1 (nv <= QN; consecutive heads
 // share every matrix load): ws_q[v] = (R q, S' R q), the projection taken as
 // S q since S' = S R^T; with ws_bk, also each head's tensor-core score
@@ -227,51 +255,58 @@ __device__ __forceinline__ void prepare_queries(const DecodeArgs& a, int v0, int
     asum += a.tables->k_walsh[s];
   }
   const float ib = 2.f * bit_inv_scale(o);
-  // per head: max of the scaled magnitudes (sigma) and sum of the coordinates
-  float red[2 * QN];
+  // per head: max of the scaled magnitudes (sigma) and sum of the coordinates,
+  // each a halving reduction over the warp
+  float mx[QN], sm[QN];
 #pragma unroll
   for (int j = 0; j < QN; ++j) {
-    red[j] = fabsf(acc[j]) * (proj ? ib : amax * ib);
-    red[QN + j] = acc[j];
+    mx[j] = fabsf(acc[j]) * (proj ? ib : amax * ib);
+    sm[j] = acc[j];
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-    for (int j = 0; j < 2 * QN; ++j) {
-      const float u = __shfl_xor_sync(0xffffffffu, red[j], off);
-      red[j] = j < QN ? fmaxf(red[j], u) : red[j] + u;
-    }
-  if (lane == 0)
-#pragma unroll
-    for (int j = 0; j < 2 * QN; ++j) stat_s[m][warp][j] = red[j];
+  int jm, js;
+  const float wmax = halving_reduce<QN>(mx, lane, &jm, [](float x, float y) { return fmaxf(x, y); });
+  const float wsum = halving_reduce<QN>(sm, lane, &js, [](float x, float y) { return x + y; });
+  constexpr int kLanesPer = 32 / QN;              // lanes that hold the same head's total
+  if ((lane & (kLanesPer - 1)) == 0) {
+    stat_s[m][warp][jm] = wmax;
+    stat_s[m][warp][QN + js] = wsum;
+  }
+  __syncthreads();
+  // once per (product, head): the piece scale sigma, a power of two
+  __shared__ float sig_s[2][QN];
+  if (threadIdx.x < 2 * QN) {
+    const int mm = threadIdx.x / QN, j = threadIdx.x % QN;
+    sig_s[mm][j] = piece_scale(fmaxf(fmaxf(stat_s[mm][0][j], stat_s[mm][1][j]), fmaxf(stat_s[mm][2][j], stat_s[mm][3][j])));
+  }
   __syncthreads();
   const int kpos = k_position(o);
   const int items = planes + (a.qjl_m > 0 ? 1 : 0);
 #pragma unroll
   for (int j = 0; j < QN; ++j) {
     if (j >= nv) break;
-    const float sig0 = piece_scale(fmaxf(fmaxf(stat_s[0][0][j], stat_s[0][1][j]), fmaxf(stat_s[0][2][j], stat_s[0][3][j])));
-    const float sig1 = piece_scale(fmaxf(fmaxf(stat_s[1][0][j], stat_s[1][1][j]), fmaxf(stat_s[1][2][j], stat_s[1][3][j])));
     uint8_t* dst = a.ws_bk + static_cast<long long>(v0 + j) * a.bk_stride;
     if (!proj) {
+      const float y = acc[j] * ib * sig_s[0][j];
       for (int s = 0; s < planes; ++s)
-        write_pieces_rows<kQPieces>(dst + s * kQPieces * 128, kpos, a.tables->k_walsh[s] * acc[j] * ib * sig0);
+        write_pieces_rows<kQPieces>(dst + s * kQPieces * 128, kpos, a.tables->k_walsh[s] * y);
     } else if (a.qjl_m > 0) {
-      write_pieces_rows<kQPieces>(dst + planes * kQPieces * 128, kpos, acc[j] * ib * sig1);
+      write_pieces_rows<kQPieces>(dst + planes * kQPieces * 128, kpos, acc[j] * ib * sig_s[1][j]);
     }
-    if (threadIdx.x == 0) {
-      const float sum_qr = (stat_s[0][0][QN + j] + stat_s[0][1][QN + j]) + (stat_s[0][2][QN + j] + stat_s[0][3][QN + j]);
-      const float sum_qs = (stat_s[1][0][QN + j] + stat_s[1][1][QN + j]) + (stat_s[1][2][QN + j] + stat_s[1][3][QN + j]);
-      float* hdr = reinterpret_cast<float*>(dst + items * kQPieces * 128);
-      hdr[0] = sig0;
-      hdr[1] = sig1;
-      hdr[2] = 1.f / sig0;      // exact: powers of two
-      hdr[3] = 1.f / sig1;
-      hdr[4] = asum * sum_qr;   // sum_S a_S <q_rot, 1>: the -1 half of every sign
-      hdr[5] = sum_qs;
-      hdr[6] = 0.f;
-      hdr[7] = 0.f;
-    }
+  }
+  if (threadIdx.x < nv) {
+    const int j = threadIdx.x;
+    const float sig0 = sig_s[0][j], sig1 = sig_s[1][j];
+    const float sum_qr = (stat_s[0][0][QN + j] + stat_s[0][1][QN + j]) + (stat_s[0][2][QN + j] + stat_s[0][3][QN + j]);
+    const float sum_qs = (stat_s[1][0][QN + j] + stat_s[1][1][QN + j]) + (stat_s[1][2][QN + j] + stat_s[1][3][QN + j]);
+    float* hdr = reinterpret_cast<float*>(a.ws_bk + static_cast<long long>(v0 + j) * a.bk_stride + items * kQPieces * 128);
+    hdr[0] = sig0;
+    hdr[1] = sig1;
+    hdr[2] = 1.f / sig0;      // exact: powers of two
+    hdr[3] = 1.f / sig1;
+    hdr[4] = asum * sum_qr;   // sum_S a_S <q_rot, 1>: the -1 half of every sign
+    hdr[5] = sum_qs;
+    hdr[6] = 0.f;
+    hdr[7] = 0.f;
   }
 }
 
