@@ -60,4 +60,20 @@ __device__ __forceinline__ void write_pieces_rows(uint8_t* rows, int kpos, float
   }
 }
 
+// As write_pieces_rows for two values at once (rows_a gets ya's pieces,
+// rows_b yb's): one paired conversion, and the residual of both in one paired
+// FMA and multiply (the same pieces, bit for bit).
+template <int N>
+__device__ __forceinline__ void write_pieces_rows2(uint8_t* rows_a, uint8_t* rows_b, int kpos, float ya, float yb) {
+  float2 y = make_float2(ya, yb);
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);   // (x in the low byte)
+    rows_a[i * 128 + kpos] = static_cast<uint8_t>(p & 0xff);
+    rows_b[i * 128 + kpos] = static_cast<uint8_t>(p >> 8);
+    const float2 b = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(p, __NV_E4M3)));
+    y = __fmul2_rn(__ffma2_rn(b, make_float2(-1.f, -1.f), y), make_float2(16.f, 16.f));
+  }
+}
+
 }  // namespace tq

@@ -287,8 +287,12 @@ __device__ __forceinline__ void prepare_queries(const DecodeArgs& a, int v0, int
     uint8_t* dst = a.ws_bk + static_cast<long long>(v0 + j) * a.bk_stride;
     if (!proj) {
       const float y = acc[j] * ib * sig_s[0][j];
-      for (int s = 0; s < planes; ++s)
-        write_pieces_rows<kQPieces>(dst + s * kQPieces * 128, kpos, a.tables->k_walsh[s] * y);
+      for (int s = 0; s < planes; s += 2)           // (planes: 1, or an even count)
+        if (s + 1 < planes)
+          write_pieces_rows2<kQPieces>(dst + s * kQPieces * 128, dst + (s + 1) * kQPieces * 128, kpos,
+                                       a.tables->k_walsh[s] * y, a.tables->k_walsh[s + 1] * y);
+        else
+          write_pieces_rows<kQPieces>(dst + s * kQPieces * 128, kpos, a.tables->k_walsh[s] * y);
     } else if (a.qjl_m > 0) {
       write_pieces_rows<kQPieces>(dst + planes * kQPieces * 128, kpos, acc[j] * ib * sig_s[1][j]);
     }
