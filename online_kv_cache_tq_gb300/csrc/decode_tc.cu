@@ -82,23 +82,23 @@ __device__ __forceinline__ int sw128(int n, int k) { return n * 128 + ((((k >> 4
 
 // Store the 0/beta_j e4m3 image of one 32-bit word of bits as eight columns:
 // column j holds bits j, j+8, j+16, j+24 of the word, each as 0 or the power
-// of two beta_j of bit_inv_scale: bits 0-6 stay where they are (the three
-// mantissa bits, then the four exponent bits of a byte), bit 7 moves to bit 6
-// (nine integer operations per word).  The arithmetic sits inside the asm
-// block so that the compiler keeps only the word, not eight operand registers
-// per plane, live across planes.
+// of two beta_j of bit_inv_scale: bits 0-2 stay in place, bits 3-7 move down
+// by three (one shift and eight masks per word), so every byte has one bit
+// among its three mantissa bits and lowest two exponent bits (2^-9 .. 2^-5).
+// The arithmetic sits inside the asm block so that the compiler keeps only
+// the word, not eight operand registers per plane, live across planes.
 __device__ __forceinline__ void store_bits(uint32_t taddr, uint32_t w) {
   asm volatile(
       "{\n\t.reg .b32 h, c0, c1, c2, c3, c4, c5, c6, c7;\n\t"
-      "shr.b32 h, %1, 1;\n\t"
+      "shr.b32 h, %1, 3;\n\t"
       "and.b32 c0, %1, 0x01010101;\n\t"
       "and.b32 c1, %1, 0x02020202;\n\t"
       "and.b32 c2, %1, 0x04040404;\n\t"
-      "and.b32 c3, %1, 0x08080808;\n\t"
-      "and.b32 c4, %1, 0x10101010;\n\t"
-      "and.b32 c5, %1, 0x20202020;\n\t"
-      "and.b32 c6, %1, 0x40404040;\n\t"
-      "and.b32 c7, h, 0x40404040;\n\t"
+      "and.b32 c3, h, 0x01010101;\n\t"
+      "and.b32 c4, h, 0x02020202;\n\t"
+      "and.b32 c5, h, 0x04040404;\n\t"
+      "and.b32 c6, h, 0x08080808;\n\t"
+      "and.b32 c7, h, 0x10101010;\n\t"
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {c0, c1, c2, c3, c4, c5, c6, c7};\n\t}\n"
       ::"r"(taddr), "r"(w)
       : "memory");

@@ -29,12 +29,13 @@ __device__ __forceinline__ float from_e4m3(uint8_t b) {
 
 // The bit-plane operand stores bit i of a 32-bit word (coordinate or token i
 // of a 32-element group) as an e4m3 byte that is 0 or a power of two beta_j,
-// j = i % 8: bits 0-2 are the mantissa bits of a subnormal (2^-9, 2^-8,
-// 2^-7), bits 3-6 the exponent bits (2^-6, 2^-5, 2^-3, 2^1), and bit 7 moves
-// to bit 6 (2^1).  The other operand carries 1 / beta_j.
+// j = i % 8: bits 0-2 as the mantissa bits of a subnormal (2^-9, 2^-8, 2^-7),
+// bits 3-7 moved down by three (2^-9, 2^-8, 2^-7, then the lowest two
+// exponent bits: 2^-6, 2^-5).  The other operand carries 1 / beta_j; the
+// classes span a factor of 16, so the pieces of every class keep their bits.
 __host__ __device__ constexpr float bit_inv_scale(int j) {
-  return (j & 7) == 0 ? 512.f : (j & 7) == 1 ? 256.f : (j & 7) == 2 ? 128.f : (j & 7) == 3 ? 64.f
-       : (j & 7) == 4 ? 32.f : (j & 7) == 5 ? 8.f : 0.5f;
+  return (j & 7) == 0 || (j & 7) == 3 ? 512.f : (j & 7) == 1 || (j & 7) == 4 ? 256.f
+       : (j & 7) == 2 || (j & 7) == 5 ? 128.f : (j & 7) == 6 ? 64.f : 32.f;
 }
 constexpr float kMaxBitInvScale = 512.f;
 
