@@ -497,10 +497,11 @@ struct ItemCursor {
 };
 
 // KB, VB, QJ: key MSE bits, value bits and QJL plane (0/1) fixed at compile
-// time, or 0, 0, -1 to take them from the arguments.  Two CTAs per SM cap a
+// time, or 0, 0, -1 to take them from the arguments; NB: the stored norms'
+// width (16 or 32 bits), or 0 to take it from the arguments.  Two CTAs per SM cap a
 // thread at 96 registers (the register file is split over four sub-partitions
 // of 16384, and one of them holds five of the two CTAs' eighteen warps).
-template <int G, int KB, int VB, int QJ, int CH>
+template <int G, int KB, int VB, int QJ, int CH, int NB>
 __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a, TcLayout L) {
   constexpr int N1 = score_cols(G), NO = value_cols(G);
   const int t = threadIdx.x;
@@ -596,9 +597,10 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   uint8_t* kn_s = smem + L.off_kn;                                  // [CH] norms, float32 or float16
   uint8_t* kr_s = smem + L.off_kr;
   uint8_t* vn_s = smem + L.off_vn;
-  const int nb = a.norm16 ? 2 : 4;                                  // bytes of a stored norm
+  const bool n16 = NB == 0 ? a.norm16 : NB == 16;                   // norms stored as float16
+  const int nb = n16 ? 2 : 4;                                       // bytes of a stored norm
   auto norm_at = [&](const uint8_t* f, int i) {
-    return a.norm16 ? __half2float(reinterpret_cast<const __half*>(f)[i]) : reinterpret_cast<const float*>(f)[i];
+    return n16 ? __half2float(reinterpret_cast<const __half*>(f)[i]) : reinterpret_cast<const float*>(f)[i];
   };
   uint32_t* vc_s = reinterpret_cast<uint32_t*>(smem + L.off_vc);   // [blk][plane][dim][bs/32]
   // kin / vin: an item's key / value fields landed (one phase per item);
@@ -1340,8 +1342,8 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, bool early) {
   // 3-bit keys (2 MSE bits + the QJL bit) with 3-bit values have their own
   // build with the widths folded in; other widths are read at run time
   const bool fixed = a.k_bits == 2 && a.v_bits == 3 && a.k_qjl != nullptr && l.k_slots == 2 && chunk == 512;
-  auto kernel = fixed ? attention_tc_kernel<G, 2, 3, 1, 512>
-                      : chunk == 512 ? attention_tc_kernel<G, 0, 0, -1, 512> : attention_tc_kernel<G, 0, 0, -1, 256>;
+  auto kernel = fixed ? (a.norm16 ? attention_tc_kernel<G, 2, 3, 1, 512, 16> : attention_tc_kernel<G, 2, 3, 1, 512, 32>)
+                      : chunk == 512 ? attention_tc_kernel<G, 0, 0, -1, 512, 0> : attention_tc_kernel<G, 0, 0, -1, 256, 0>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem_bytes);
   if (err != cudaSuccess) return err;
   // a persistent grid (tc_grid); the kernel splits the real chunks of the
