@@ -498,10 +498,11 @@ struct ItemCursor {
 
 // KB, VB, QJ: key MSE bits, value bits and QJL plane (0/1) fixed at compile
 // time, or 0, 0, -1 to take them from the arguments; NB: the stored norms'
-// width (16 or 32 bits), or 0 to take it from the arguments.  Two CTAs per SM cap a
+// width (16 or 32 bits), or 0 to take it from the arguments; BS: the block
+// size, or 0 to take it from the arguments.  Two CTAs per SM cap a
 // thread at 96 registers (the register file is split over four sub-partitions
 // of 16384, and one of them holds five of the two CTAs' eighteen warps).
-template <int G, int KB, int VB, int QJ, int CH, int NB>
+template <int G, int KB, int VB, int QJ, int CH, int NB, int BS>
 __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a, TcLayout L) {
   constexpr int N1 = score_cols(G), NO = value_cols(G);
   const int t = threadIdx.x;
@@ -573,8 +574,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   }
   __syncthreads();
 
-  const int bs = a.block_size;                        // a power of two that divides CH
-  const int bs_shift = 31 - __clz(bs);
+  const int bs = BS > 0 ? BS : a.block_size;          // a power of two that divides CH
+  const int bs_shift = BS > 0 ? 31 - __clz(BS) : 31 - __clz(bs);
 
   const int k_bits = KB > 0 ? KB : a.k_bits;
   const int v_bits = VB > 0 ? VB : a.v_bits;
@@ -1339,11 +1340,15 @@ template <int G>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, bool early) {
   const int chunk = tc_chunk(a);
   const TcLayout l = tc_layout(G, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size, chunk);
-  // 3-bit keys (2 MSE bits + the QJL bit) with 3-bit values have their own
-  // build with the widths folded in; other widths are read at run time
-  const bool fixed = a.k_bits == 2 && a.v_bits == 3 && a.k_qjl != nullptr && l.k_slots == 2 && chunk == 512;
-  auto kernel = fixed ? (a.norm16 ? attention_tc_kernel<G, 2, 3, 1, 512, 16> : attention_tc_kernel<G, 2, 3, 1, 512, 32>)
-                      : chunk == 512 ? attention_tc_kernel<G, 0, 0, -1, 512, 0> : attention_tc_kernel<G, 0, 0, -1, 256, 0>;
+  // 3-bit keys (2 MSE bits + the QJL bit) with 3-bit values in 64-token
+  // blocks have their own build with the widths, the norm width and the block
+  // size folded in; other shapes are read at run time
+  const bool fixed = a.k_bits == 2 && a.v_bits == 3 && a.k_qjl != nullptr && l.k_slots == 2 && chunk == 512 &&
+                     a.block_size == 64;
+  auto kernel = fixed ? (a.norm16 ? attention_tc_kernel<G, 2, 3, 1, 512, 16, 64>
+                                  : attention_tc_kernel<G, 2, 3, 1, 512, 32, 64>)
+                      : chunk == 512 ? attention_tc_kernel<G, 0, 0, -1, 512, 0, 0>
+                                     : attention_tc_kernel<G, 0, 0, -1, 256, 0, 0>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem_bytes);
   if (err != cudaSuccess) return err;
   // a persistent grid (tc_grid); the kernel splits the real chunks of the
