@@ -291,7 +291,8 @@ struct TcLayout {
 constexpr int kValueSlot = 64;              // columns of one value slot (two sign planes)
 constexpr int kMaxValueSlots = 4;
 
-TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size, int chunk) {
+__host__ __device__ constexpr TcLayout tc_layout(int group, int k_bits, bool qjl, int v_bits, int block_size,
+                                                 int chunk) {
   TcLayout l{};
   l.chunk = chunk;
   l.pk = 1 << (k_bits - 1);
@@ -503,7 +504,12 @@ struct ItemCursor {
 // thread at 96 registers (the register file is split over four sub-partitions
 // of 16384, and one of them holds five of the two CTAs' eighteen warps).
 template <int G, int KB, int VB, int QJ, int CH, int NB, int BS>
-__global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a, TcLayout L) {
+__global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a, TcLayout layout) {
+  // (with the widths and the block size fixed, the layout -- the one the host
+  // computed for the launch -- folds to constants)
+  constexpr bool kFixedLayout = KB > 0 && VB > 0 && QJ >= 0 && BS > 0;
+  constexpr TcLayout kLayout = kFixedLayout ? tc_layout(G, KB, QJ == 1, VB, BS, CH) : TcLayout{};
+  const TcLayout L = kFixedLayout ? kLayout : layout;
   constexpr int N1 = score_cols(G), NO = value_cols(G);
   const int t = threadIdx.x;
 
