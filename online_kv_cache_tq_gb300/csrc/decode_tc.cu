@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   const int kp = 32 * (pk + pq);                     // columns per key slot
   const int kbytes = 16 * k_bits;                    // key code bytes per token
   const int vblock = v_bits * 16 * bs;               // value code bytes per (block, head)
-  const int k_slots = KB > 0 ? 2 : L.k_slots;        // the fixed build is launched with two key slots
+  const int k_slots = L.k_slots;
 
   uint8_t* b_mse = smem + L.off_bmse;
   uint8_t* b_qjl = smem + L.off_bqjl;
@@ -1346,15 +1346,20 @@ template <int G>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, bool early) {
   const int chunk = tc_chunk(a);
   const TcLayout l = tc_layout(G, a.k_bits, a.k_qjl != nullptr, a.v_bits, a.block_size, chunk);
-  // 3-bit keys (2 MSE bits + the QJL bit) with 3-bit values in 64-token
-  // blocks have their own build with the widths, the norm width and the block
-  // size folded in; other shapes are read at run time
-  const bool fixed = a.k_bits == 2 && a.v_bits == 3 && a.k_qjl != nullptr && l.k_slots == 2 && chunk == 512 &&
-                     a.block_size == 64;
-  auto kernel = fixed ? (a.norm16 ? attention_tc_kernel<G, 2, 3, 1, 512, 16, 64>
-                                  : attention_tc_kernel<G, 2, 3, 1, 512, 32, 64>)
-                      : chunk == 512 ? attention_tc_kernel<G, 0, 0, -1, 512, 0, 0>
-                                     : attention_tc_kernel<G, 0, 0, -1, 256, 0, 0>;
+  // 3-bit keys (2 MSE bits + the QJL bit) with 3-bit values, and (eight
+  // query heads per KV head) 4-bit keys with 2-bit values, in 64-token blocks
+  // and 512-token items, have their own builds with the widths, the norm
+  // width, the block size and so the layout folded in; other shapes are read
+  // at run time
+  const bool common = a.k_qjl != nullptr && chunk == 512 && a.block_size == 64;
+  const bool k3v3 = common && a.k_bits == 2 && a.v_bits == 3;
+  const bool k4v2 = common && G == 8 && a.k_bits == 3 && a.v_bits == 2;
+  auto kernel = chunk == 512 ? attention_tc_kernel<G, 0, 0, -1, 512, 0, 0> : attention_tc_kernel<G, 0, 0, -1, 256, 0, 0>;
+  if (k3v3)
+    kernel = a.norm16 ? attention_tc_kernel<G, 2, 3, 1, 512, 16, 64> : attention_tc_kernel<G, 2, 3, 1, 512, 32, 64>;
+  if constexpr (G == 8)
+    if (k4v2)
+      kernel = a.norm16 ? attention_tc_kernel<G, 3, 2, 1, 512, 16, 64> : attention_tc_kernel<G, 3, 2, 1, 512, 32, 64>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem_bytes);
   if (err != cudaSuccess) return err;
   // a persistent grid (tc_grid); the kernel splits the real chunks of the
