@@ -298,6 +298,35 @@ def test_every_context_empty_gives_zero_rows():
     assert B.tq_get_last_device_error(book) == 0
 
 
+@pytest.mark.parametrize("k_bits,v_bits,norm_bits,block_size,group", [
+    (4, 2, 16, 64, 8),      # the 4-bit-key build with float16 norms
+    (4, 2, 32, 64, 8),      # ... with float32 norms
+    (3, 3, 32, 32, 8),      # 3/3 bits in 32-token blocks: the build that reads the shape from the arguments
+    (3, 3, 16, 128, 4),     # ... 128-token blocks, float16 norms
+    (4, 2, 32, 256, 8),     # ... 256-token blocks
+])
+def test_fixed_and_run_time_shape_builds(k_bits, v_bits, norm_bits, block_size, group):
+    # every tensor-core build the launcher picks (widths, norm width and block
+    # size folded in, or read from the arguments) against the oracle, over
+    # ragged contexts and shuffled blocks
+    n_kv = 2
+    cfg = dict(n_kv=n_kv, block_size=block_size, dtype="bf16", seed=60 + block_size, log_uniform=(0.1, 10.0),
+               outliers=3, outlier_scale=30.0)
+    book, ref = books(k_bits, v_bits, 128, seed=9, block_size=block_size, norm_bits=norm_bits)
+    assert B.tq_decode_kernel_kind(book, n_kv * group, n_kv) == 1
+    ctx = np.array([0, 1, 77, 513, 1500], dtype=np.int32)
+    table, _ = W.block_layout(ctx, block_size, True, seed=block_size)
+    g = generator(70 + block_size)
+    cache = fill_cache(book, cfg, ctx, table, g, chunk_tokens=1000)
+    q = W.queries(len(ctx), n_kv * group, torch.bfloat16, "cuda", g)
+    out = decode(book, cache, q, table, ctx, 1500)
+    worst = check_decode(out, host_cache(cache), q, table, ctx, ref,
+                         [(b, h) for b in range(len(ctx)) for h in range(n_kv * group)])
+    print("K%d V%d, %d-bit norms, %d-token blocks, G=%d: worst normalised error %.3g"
+          % (k_bits, v_bits, norm_bits, block_size, group, worst))
+    assert B.tq_get_last_device_error(book) == 0
+
+
 @pytest.mark.parametrize("group", [4, 8])
 def test_sixteen_bit_norms_decode(group):
     # a cache with float16 norms (102 bytes per token-head at 3/3 bits), ragged
