@@ -138,6 +138,26 @@ __device__ __forceinline__ void key_planes(uint32_t base, const uint32_t (&bw)[4
     for (int c = 0; c < 2; ++c) store_bits(base + 32 * P + 8 * (w0 + c), sg[c]);
 }
 
+// Unit u of a key tile built in two units (3-bit MSE codes: four sign
+// planes): unit 0 holds sign planes 0-2, unit 1 sign plane 3 and then the QJL
+// plane; words w0 and w0 + 1 of each.
+__device__ __forceinline__ void key_unit3(uint32_t base, const uint32_t (&bw)[4][2], const uint32_t (&sg)[2], bool qjl,
+                                          int w0, int unit) {
+  if (unit == 0) {
+#pragma unroll
+    for (int s = 0; s < 3; ++s)
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        store_bits(base + 32 * s + 8 * (w0 + c), plane_word(bw[0][c], bw[1][c], bw[2][c], bw[3][c], walsh_set(3, s)));
+  } else {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) store_bits(base + 8 * (w0 + c), plane_word(bw[0][c], bw[1][c], bw[2][c], bw[3][c], walsh_set(3, 3)));
+    if (qjl)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) store_bits(base + 32 + 8 * (w0 + c), sg[c]);
+  }
+}
+
 // Value sign plane S of BITS-bit codes (compile-time Walsh set) at `col`.
 template <int BITS, int S>
 __device__ __forceinline__ void value_plane(uint32_t col, const uint32_t (&bw)[4][2], int w0) {
@@ -272,15 +292,20 @@ __device__ __forceinline__ int context_of(const DecodeArgs& a, int b) {
 // Tensor-memory columns and dynamic shared memory the kernel needs.
 //
 // Key phase: k_slots slots of kp = 32 (pk + pq) columns (the sign planes of
-// one tile), then the score accumulators (n1 mse + n2 qjl columns).  Value
-// phase (after every score has been read, so it reuses the same columns): two
-// slots of 64 columns (two value sign planes each), then pv accumulator blocks
-// of no columns.  Two key slots are used when they fit beside the rest; the
-// allocation is a power of two of at least 32 columns.
+// one tile), then the score accumulators (n1 mse + n2 qjl columns); with four
+// MSE planes (3-bit MSE keys) two slots of a whole tile do not fit, and a tile
+// is built as two units instead -- MSE planes 0-2 in slot 0, plane 3 and the
+// QJL plane in slot 1 (k_units = 2, kp = 96) -- so that one unit is built while
+// the other's MMAs run.  Value phase (after every score has been read, so it
+// reuses the same columns): two slots of 64 columns (two value sign planes
+// each), then pv accumulator blocks of no columns.  Two key slots are used when
+// they fit beside the rest; the allocation is a power of two of at least 32
+// columns.
 struct TcLayout {
   int pk, pq, pv;           // key sign planes, QJL plane (0/1), value sign planes
   int n1, n2, no;           // score columns (mse, qjl), value columns per plane
   int kp, k_slots;          // columns per key slot, key slots (1 or 2)
+  int k_units;              // units a key tile is built in (1, or 2 with four MSE planes)
   int v_slots;              // value slots of kValueSlot columns (2 to kMaxValueSlots)
   int col_s, col_o, cols, tmem;
   int kbytes, vblock;       // key code bytes per token; value code bytes per (block, head)
@@ -308,10 +333,20 @@ __host__ __device__ constexpr TcLayout tc_layout(int group, int k_bits, bool qjl
   const int vcols = 2 * kValueSlot + vacc;
   auto kcols = [&](int slots) { return slots * l.kp + l.n1 + l.n2; };
   auto mx = [](int x, int y) { return x > y ? x : y; };
-  if (mx(kcols(2), vcols) <= 256) l.k_slots = 2;
-  else if (mx(kcols(1), vcols) <= 256) l.k_slots = 1;
-  else if (mx(kcols(2), vcols) <= 512) l.k_slots = 2;
-  else l.k_slots = 1;
+  l.k_units = 1;
+  if (mx(kcols(2), vcols) <= 256) {
+    l.k_slots = 2;
+  } else if (l.pk == 4 && mx(2 * 96 + l.n1 + l.n2, vcols) <= 256) {
+    l.k_units = 2;                          // a tile as two units of at most three planes
+    l.kp = 96;
+    l.k_slots = 2;
+  } else if (mx(kcols(1), vcols) <= 256) {
+    l.k_slots = 1;
+  } else if (mx(kcols(2), vcols) <= 512) {
+    l.k_slots = 2;
+  } else {
+    l.k_slots = 1;
+  }
   l.col_s = l.k_slots * l.kp;
   l.cols = mx(kcols(l.k_slots), vcols);
   l.tmem = 32;
@@ -588,10 +623,11 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   const int pk = KB > 0 ? 1 << (KB - 1) : L.pk;     // key sign planes
   const int pq = QJ >= 0 ? QJ : L.pq;                // QJL plane
   const int pv = VB > 0 ? 1 << (VB - 1) : L.pv;     // value sign planes
-  const int kp = 32 * (pk + pq);                     // columns per key slot
+  const int kp = L.kp;                               // columns per key slot
   const int kbytes = 16 * k_bits;                    // key code bytes per token
   const int vblock = v_bits * 16 * bs;               // value code bytes per (block, head)
   const int k_slots = L.k_slots;
+  const bool k_two = L.k_units == 2;                 // a key tile in two units (slot 0: planes 0-2; slot 1: 3 + QJL)
 
   uint8_t* b_mse = smem + L.off_bmse;
   uint8_t* b_qjl = smem + L.off_bqjl;
@@ -615,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   // item (256 arrivals); kfull / vfull: the builders stored a slot's planes
   // (256 arrivals); kdone / vdone: the slot's MMAs completed (commit); sfree:
   // the builders read the score accumulators (256 arrivals); bar_d: drain
-  __shared__ __align__(8) uint64_t kin, vin, kfree, vfree, kfull[2], kdone, sfree, vfull[kMaxValueSlots],
+  __shared__ __align__(8) uint64_t kin, vin, kfree, vfree, kfull[2], kdone, kudone, sfree, vfull[kMaxValueSlots],
       vdone[kMaxValueSlots], bar_d;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
@@ -651,6 +687,7 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
     ptx::mbar_init(&kfull[0], kBuilders);
     ptx::mbar_init(&kfull[1], kBuilders);
     ptx::mbar_init(&kdone, 1);
+    ptx::mbar_init(&kudone, 1);
     ptx::mbar_init(&sfree, kBuilders);
     for (int i = 0; i < kMaxValueSlots; ++i) {
       ptx::mbar_init(&vfull[i], kBuilders);
@@ -738,6 +775,37 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       const bool more = cursor.next(a, bs_shift, nxt);
       // scores: tile i once its planes are stored and the previous tile's accumulators were read
       for (int i = 0; i < cur.n_tiles && ok; ++i, ++ktile) {
+        if (k_two) {
+          // unit 0 (MSE planes 0-2, slot 0) once stored and the previous tile's scores were read
+          ok = wait_phase(&kfull[0], ktile & 1, abort, a.error);
+          if (ok && ktile > 0) ok = wait_phase(&sfree, (ktile - 1) & 1, abort, a.error);
+          if (ok && ptx::elect_one()) {
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < 3; ++s)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                ptx::mma_e4m3_tmem_a(d_mse, tmem + 32 * s + 8 * kk, desc_mse + s * mse_plane_step + 2 * kk, idesc_s,
+                                     (s | kk) != 0);
+            ptx::mma_commit(&kudone);
+          }
+          __syncwarp();
+          // unit 1 (MSE plane 3 and the QJL plane, slot 1)
+          if (ok) ok = wait_phase(&kfull[1], ktile & 1, abort, a.error);
+          if (ok && ptx::elect_one()) {
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::mma_e4m3_tmem_a(d_mse, tmem + kp + 8 * kk, desc_mse + 3 * mse_plane_step + 2 * kk, idesc_s, true);
+            if (qjl)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                ptx::mma_e4m3_tmem_a(d_mse + N1, tmem + kp + 32 + 8 * kk, desc_qjl + 2 * kk, idesc_s, kk != 0);
+            if (!(a.debug_withhold && blockIdx.x == 0 && ktile == 0)) ptx::mma_commit(&kdone);
+          }
+          __syncwarp();
+          continue;
+        }
         const int slot = k_slots == 2 ? (ktile & 1) : 0;
         ok = wait_phase(&kfull[slot], (k_slots == 2 ? ktile >> 1 : ktile) & 1, abort, a.error);
         if (ok && ktile > 0) ok = wait_phase(&sfree, (ktile - 1) & 1, abort, a.error);
@@ -950,7 +1018,15 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       const int k0 = ktile;
       for (int i = 0; i < x.n_tiles && ok; ++i, ++ktile) {
         const int slot = k_slots == 2 ? (ktile & 1) : 0;
-        if (k_slots == 1 && i > 0) take_scores(i - 1, ktile - 1);
+        if (k_two) {
+          // slot 0 once the previous tile's unit-0 MMAs completed
+          if (ktile > 0) {
+            ok = wait_phase(&kudone, (ktile - 1) & 1, abort, a.error);
+            ptx::tc_fence_after();
+          }
+        } else if (k_slots == 1 && i > 0) {
+          take_scores(i - 1, ktile - 1);
+        }
         if (!ok) break;
         const int tl = i * kTile + lane;
         // loaded for every token slot of the tile (tl < CH, inside the
@@ -972,6 +1048,20 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             sg[0] = w.x;
             sg[1] = w.y;
           }
+        }
+        if (k_two) {
+          // unit 0 into slot 0; the previous tile's scores (which frees slot 1); unit 1 into slot 1
+          key_unit3(tmem + row_addr, bw, sg, qjl, w0, 0);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&kfull[0]);
+          if (i > 0) take_scores(i - 1, ktile - 1);
+          if (!ok) break;
+          key_unit3(tmem + row_addr + kp, bw, sg, qjl, w0, 1);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&kfull[1]);
+          continue;
         }
         const uint32_t base = tmem + row_addr + slot * kp;
         switch (k_bits) {
