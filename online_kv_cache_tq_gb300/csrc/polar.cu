@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
   if (start >= ctx) return;
   const int n_local = min(kChunk, ctx - start);
 
-  __shared__ __align__(16) float q_s[G][kDim];
+  __shared__ __align__(16) float q_s[G][8][20];   // q_rot in 16-coordinate parts, rows padded to 20 (no bank conflicts)
   __shared__ __align__(16) float y_s[kPTile][kYRow];   // one tile's decoded vectors, token-major
   __shared__ float p_s[G][kChunk];             // scores, then softmax weights
   __shared__ uint32_t rec_s[kPTile][kRecordWords + 1];
@@ -197,7 +197,8 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
   __shared__ float red_s[kPThreads / 32][G];
   __shared__ float stat_s[2][G];
 
-  for (int i = t; i < G * kDim; i += kPThreads) q_s[i / kDim][i % kDim] = a.ws_q[static_cast<long long>(qbase + i / kDim) * 2 * kDim + i % kDim];
+  for (int i = t; i < G * kDim; i += kPThreads)
+    q_s[i / kDim][(i % kDim) >> 4][i & 15] = a.ws_q[static_cast<long long>(qbase + i / kDim) * 2 * kDim + i % kDim];
   if (t < 24) {
     cos_s[t] = cospif(t / 12.f);
     sin_s[t] = sinpif(t / 12.f);
@@ -248,28 +249,40 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
       *reinterpret_cast<float4*>(&y_s[tok_i][16 * part + k]) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
   };
 
-  // ---- scores: s = scale <q_rot, y_hat_k> per (token, head) ----
+  // ---- scores: s = scale <q_rot, y_hat_k> per (token, head): each thread takes
+  // the share of its expanded 16 coordinates in every head's score, and the
+  // eight lanes of a token add their shares ----
   fetch_tile(a.k_codes, a.k_norm, 0);
   for (int tile = 0; tile < n_tiles; ++tile) {
     stash_tile();
     __syncthreads();
     if (tile + 1 < n_tiles) fetch_tile(a.k_codes, a.k_norm, tile + 1);
     else fetch_tile(a.v_codes, a.v_norm, 0);     // (the first value tile, while the softmax runs)
-    expand_tile();
-    __syncthreads();
-    const int i = t & (kPTile - 1);
-    for (int h = t / kPTile; h < G; h += kPThreads / kPTile) {
-      float s = 0.f;
-#pragma unroll 8
-      for (int j = 0; j < kDim; j += 4) {
-        const float4 qv = *reinterpret_cast<const float4*>(&q_s[h][j]);
-        const float4 yv = *reinterpret_cast<const float4*>(&y_s[i][j]);
-        s = fmaf(qv.x, yv.x, fmaf(qv.y, yv.y, fmaf(qv.z, yv.z, fmaf(qv.w, yv.w, s))));
+    float v[16];
+    expand_part(rec_s[tok_i], rad_s[tok_i], part, cos_s, sin_s, v);
+    float sc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 16; k += 4) {
+        const float4 qv = *reinterpret_cast<const float4*>(&q_s[h][part][k]);
+        acc = __ffma2_rn(make_float2(v[k], v[k + 1]), make_float2(qv.x, qv.y), acc);
+        acc = __ffma2_rn(make_float2(v[k + 2], v[k + 3]), make_float2(qv.z, qv.w), acc);
       }
-      const int tl = tile * kPTile + i;
-      if (tl < kChunk) p_s[h][tl] = tl < n_local && row_s[tl] >= 0 ? a.scale * s : -INFINITY;
+      sc[h] = acc.x + acc.y;
     }
-    __syncthreads();
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1)          // (the token's eight lanes are consecutive)
+#pragma unroll
+      for (int h = 0; h < G; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], off);
+    // lane `part` of the token writes head `part`'s score (G <= 8)
+    float mine = sc[0];
+#pragma unroll
+    for (int h = 1; h < G; ++h) mine = part == h ? sc[h] : mine;
+    const int tl = tile * kPTile + tok_i;
+    if (part < G && tl < kChunk) p_s[part][tl] = tl < n_local && row_s[tl] >= 0 ? a.scale * mine : -INFINITY;
+    __syncthreads();                              // (rec_s is rewritten by the next stash)
   }
 
   // ---- softmax over the chunk: per-head max, weights e^(s - m), their sum ----
