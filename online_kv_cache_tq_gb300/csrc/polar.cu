@@ -133,46 +133,66 @@ __device__ __forceinline__ int chunk_context(const DecodeArgs& a, int b) {
   return ctx;
 }
 
-// The `width` bits of a record row (kRecordWords + 1 words, the last 0) at bit `pos`.
-__device__ __forceinline__ int record_bits(const uint32_t* rec, int pos, int width) {
-  return static_cast<int>(__funnelshift_r(rec[pos >> 5], rec[(pos >> 5) + 1], pos & 31) & ((1u << width) - 1u));
+// 64 bits of a record row (kRecordWords + 1 words, the last 0) from bit
+// `pos` on, the bits past the row's end zero.
+__device__ __forceinline__ uint64_t record_window(const uint32_t* rec, int pos) {
+  const int w = pos >> 5;
+  return ((static_cast<uint64_t>(rec[w + 1]) << 32) | rec[w]) >> (pos & 31);
 }
 
-// Level L (4..1) of the expansion of a part's subtree: its 2^(4-L) node radii
-// in v[0 ..] become the 2^(5-L) radii of level L - 1 (cos for the first member
-// of a pair, sin for the second), highest node first so that no radius is
-// overwritten before it is read.
-template <int L>
-__device__ __forceinline__ void expand_level(const uint32_t* rec, int part, const float* cos_s, const float* sin_s,
-                                             float (&v)[16]) {
-  constexpr int nodes = 1 << (4 - L);
-#pragma unroll
-  for (int k = nodes - 1; k >= 0; --k) {
-    const int node = part * nodes + k;
-    const int c = L == 1 ? record_bits(rec, 5 * node, 5) : record_bits(rec, kUpperBit + 3 * (upper_offset(L) + node), 3);
-    const float parent = v[k];
-    v[2 * k] = parent * cos_s[c];
-    v[2 * k + 1] = parent * sin_s[c];
-  }
-}
-
-// Rotated coordinates 16 part .. 16 part + 15 of one record: the three
-// ancestors above the part's subtree (levels 7, 6, 5), then its subtree
-// expanded level by level down to the coordinates.
-__device__ __forceinline__ void expand_part(const uint32_t* rec, float radius, int part, const float* cos_s,
-                                            const float* sin_s, float (&v)[16]) {
+// Rotated coordinates 16 part .. 16 part + 15 of one record, from the top:
+// the three ancestors above the part's subtree (levels 7, 6, 5), then its
+// subtree level by level (4 .. 1), a node's radius r becoming r cos(theta)
+// and r sin(theta) for its pair (cs_s: cos and sin of the 24 sector angles).
+// The part's codes come from four 64-bit windows of the record held in
+// registers: its level-1 codes (40 bits from bit 40 part), its level-2 codes
+// (12 bits), the level-3 codes (48 bits from bit 416) and the level 4-7 codes
+// (45 bits from bit 464).
+__device__ __forceinline__ void expand_part(const uint32_t* rec, float radius, int part, const float2* cs_s,
+                                            float (&v)[16]) {
+  const uint64_t w1 = record_window(rec, 40 * part);
+  const uint64_t w2 = record_window(rec, kUpperBit + 3 * (polar_upper_offset(2) + 4 * part));
+  const uint64_t w3 = record_window(rec, kUpperBit + 3 * polar_upper_offset(3));
+  const uint64_t w4 = record_window(rec, kUpperBit + 3 * polar_upper_offset(4));
+  // code of node `node` at upper level L (3 .. 7)
+  auto upper = [&](int level, int node) {
+    const int bit = 3 * (polar_upper_offset(level) + node);
+    return level >= 4 ? static_cast<int>((w4 >> (bit - 3 * polar_upper_offset(4))) & 7u)
+                      : static_cast<int>((w3 >> (bit - 3 * polar_upper_offset(3))) & 7u);
+  };
   float r = radius;
 #pragma unroll
   for (int lvl = 7; lvl >= 5; --lvl) {
-    const int node = part >> (lvl - 4);                 // pair index at this level
-    const int c = record_bits(rec, kUpperBit + 3 * (upper_offset(lvl) + node), 3);
-    r *= ((part >> (lvl - 5)) & 1) ? sin_s[c] : cos_s[c];
+    const float2 cs = cs_s[upper(lvl, part >> (lvl - 4))];
+    r *= ((part >> (lvl - 5)) & 1) ? cs.y : cs.x;
   }
   v[0] = r;
-  expand_level<4>(rec, part, cos_s, sin_s, v);
-  expand_level<3>(rec, part, cos_s, sin_s, v);
-  expand_level<2>(rec, part, cos_s, sin_s, v);
-  expand_level<1>(rec, part, cos_s, sin_s, v);
+  {
+    const float2 cs = cs_s[upper(4, part)];                          // level 4: one node
+    v[1] = v[0] * cs.y;
+    v[0] = v[0] * cs.x;
+  }
+#pragma unroll
+  for (int k = 1; k >= 0; --k) {                                    // level 3: two nodes
+    const float2 cs = cs_s[upper(3, 2 * part + k)];
+    const float parent = v[k];
+    v[2 * k] = parent * cs.x;
+    v[2 * k + 1] = parent * cs.y;
+  }
+#pragma unroll
+  for (int k = 3; k >= 0; --k) {                                    // level 2: four nodes
+    const float2 cs = cs_s[static_cast<int>((w2 >> (3 * k)) & 7u)];
+    const float parent = v[k];
+    v[2 * k] = parent * cs.x;
+    v[2 * k + 1] = parent * cs.y;
+  }
+#pragma unroll
+  for (int k = 7; k >= 0; --k) {                                    // level 1: eight nodes, codes 0 .. 23
+    const float2 cs = cs_s[static_cast<int>((w1 >> (5 * k)) & 31u)];
+    const float parent = v[k];
+    v[2 * k] = parent * cs.x;
+    v[2 * k + 1] = parent * cs.y;
+  }
 }
 
 template <int G>
@@ -193,15 +213,14 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
   __shared__ uint32_t rec_s[kPTile][kRecordWords + 1];
   __shared__ float rad_s[kPTile];
   __shared__ long long row_s[kChunk];
-  __shared__ float cos_s[24], sin_s[24];
+  __shared__ float2 cs_s[24];                  // cos, sin of the sector angles k pi / 12
   __shared__ float red_s[kPThreads / 32][G];
   __shared__ float stat_s[2][G];
 
   for (int i = t; i < G * kDim; i += kPThreads)
     q_s[i / kDim][(i % kDim) >> 4][i & 15] = a.ws_q[static_cast<long long>(qbase + i / kDim) * 2 * kDim + i % kDim];
   if (t < 24) {
-    cos_s[t] = cospif(t / 12.f);
-    sin_s[t] = sinpif(t / 12.f);
+    cs_s[t] = make_float2(cospif(t / 12.f), sinpif(t / 12.f));
   }
   for (int tl = t; tl < kChunk; tl += kPThreads) {
     long long row = -1;
@@ -243,7 +262,7 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
   };
   auto expand_tile = [&]() {
     float v[16];
-    expand_part(rec_s[tok_i], rad_s[tok_i], part, cos_s, sin_s, v);
+    expand_part(rec_s[tok_i], rad_s[tok_i], part, cs_s, v);
 #pragma unroll
     for (int k = 0; k < 16; k += 4)
       *reinterpret_cast<float4*>(&y_s[tok_i][16 * part + k]) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
@@ -259,7 +278,7 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
     if (tile + 1 < n_tiles) fetch_tile(a.k_codes, a.k_norm, tile + 1);
     else fetch_tile(a.v_codes, a.v_norm, 0);     // (the first value tile, while the softmax runs)
     float v[16];
-    expand_part(rec_s[tok_i], rad_s[tok_i], part, cos_s, sin_s, v);
+    expand_part(rec_s[tok_i], rad_s[tok_i], part, cs_s, v);
     float sc[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
