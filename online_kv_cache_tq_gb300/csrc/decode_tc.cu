@@ -37,11 +37,12 @@
 // warp: lane k copies block k of an item's packed fields (contiguous per
 // block and head) into shared memory with bulk asynchronous copies, one item
 // ahead, and an elected lane issues every MMA.  The two sides meet only on mbarriers: the
-// builders store a tile's sign planes into one of two tensor-memory slots and
-// arrive; the control warp issues that tile's MMAs and commits; the builders
-// build the next tile meanwhile and wait on the commit only to read the
-// accumulators or to reuse the slot.  Every wait is time-bounded (error
-// code 4) and a failed wait makes every other wait give up.
+// builders store a tile's sign planes into one of two tensor-memory slots (or,
+// with four MSE planes, the tile's two units into the two slots) and arrive;
+// the control warp issues that tile's MMAs and commits; the builders build the
+// next tile meanwhile and wait on the commit only to read the accumulators or
+// to reuse the slot.  Every wait is time-bounded (error code 4) and a failed
+// wait makes every other wait give up.
 #include <cuda_fp8.h>
 
 #include <type_traits>
@@ -649,8 +650,10 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
   // kin / vin: an item's key / value fields landed (one phase per item);
   // kfree / vfree: the builders are done with the key / value fields of an
   // item (256 arrivals); kfull / vfull: the builders stored a slot's planes
-  // (256 arrivals); kdone / vdone: the slot's MMAs completed (commit); sfree:
-  // the builders read the score accumulators (256 arrivals); bar_d: drain
+  // (256 arrivals); kdone / vdone: the slot's MMAs completed (commit; kdone
+  // once per key tile); kudone: the first unit's MMAs of a key tile built in
+  // two units completed; sfree: the builders read the score accumulators
+  // (256 arrivals); bar_d: drain
   __shared__ __align__(8) uint64_t kin, vin, kfree, vfree, kfull[2], kdone, kudone, sfree, vfull[kMaxValueSlots],
       vdone[kMaxValueSlots], bar_d;
   __shared__ uint32_t tmem_base_s;
