@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
 
   __shared__ __align__(16) float q_s[G][8][20];   // q_rot in 16-coordinate parts, rows padded to 20 (no bank conflicts)
   __shared__ __align__(16) float y_s[kPTile][kYRow];   // one tile's decoded vectors, token-major
-  __shared__ float p_s[G][kChunk];             // scores, then softmax weights
+  __shared__ __align__(16) float p_s[kChunk][G];   // scores, then softmax weights (a token's heads side by side)
   __shared__ uint32_t rec_s[kPTile][kRecordWords + 1];
   __shared__ float rad_s[kPTile];
   __shared__ long long row_s[kChunk];
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
 #pragma unroll
     for (int h = 1; h < G; ++h) mine = part == h ? sc[h] : mine;
     const int tl = tile * kPTile + tok_i;
-    if (part < G && tl < kChunk) p_s[part][tl] = tl < n_local && row_s[tl] >= 0 ? a.scale * mine : -INFINITY;
+    if (part < G && tl < kChunk) p_s[tl][part] = tl < n_local && row_s[tl] >= 0 ? a.scale * mine : -INFINITY;
     __syncthreads();                              // (rec_s is rewritten by the next stash)
   }
 
@@ -308,13 +308,14 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
   const int lane = t & 31, warp = t >> 5;
   float part_v[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float m = -INFINITY;
-    for (int tl = t; tl < n_local; tl += kPThreads) m = fmaxf(m, p_s[h][tl]);
+  for (int h = 0; h < G; ++h) part_v[h] = -INFINITY;
+  for (int tl = t; tl < n_local; tl += kPThreads)
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    part_v[h] = m;
-  }
+    for (int h = 0; h < G; ++h) part_v[h] = fmaxf(part_v[h], p_s[tl][h]);
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part_v[h] = fmaxf(part_v[h], __shfl_xor_sync(0xffffffffu, part_v[h], off));
   if (lane == 0)
 #pragma unroll
     for (int h = 0; h < G; ++h) red_s[warp][h] = part_v[h];
@@ -325,20 +326,24 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
     stat_s[0][t] = m;
   }
   __syncthreads();
+  float mh[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    const float m = stat_s[0][h];
-    float l = 0.f;
-    for (int tl = t; tl < n_local; tl += kPThreads) {
-      const float s = p_s[h][tl];
-      const float e = s == -INFINITY || m == -INFINITY ? 0.f : __expf(s - m);
-      p_s[h][tl] = e;
-      l += e;
+    mh[h] = stat_s[0][h];
+    part_v[h] = 0.f;
+  }
+  for (int tl = t; tl < kChunk; tl += kPThreads)   // (weight 0 past the context, for the value loop)
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float s = p_s[tl][h];
+      const float e = tl >= n_local || s == -INFINITY || mh[h] == -INFINITY ? 0.f : __expf(s - mh[h]);
+      p_s[tl][h] = e;
+      part_v[h] += e;
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-    part_v[h] = l;
-  }
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part_v[h] += __shfl_xor_sync(0xffffffffu, part_v[h], off);
   __syncthreads();                              // red_s was read above
   if (lane == 0)
 #pragma unroll
@@ -350,40 +355,55 @@ __global__ void __launch_bounds__(kPThreads) polar_attention_kernel(DecodeArgs a
     stat_s[1][t] = l;
   }
 
-  // ---- values: acc[h][j] = sum_t w[h][t] y_hat_v[t][j]; thread (j, half) takes heads h % 2 == half ----
-  const int j = t & (kDim - 1), hf = t >> 7;
-  constexpr int HH = (G + 1) / 2;
-  float acc[HH];
+  // ---- values: acc[h][j] = sum_t w[h][t] y_hat_v[t][j]; thread (j, th) takes every head over the
+  // tile's tokens 16 th .. 16 th + 15 (past the context: weight 0 and a zero record) ----
+  const int j = t & (kDim - 1), th = t >> 7;
+  float acc[G];
 #pragma unroll
-  for (int k = 0; k < HH; ++k) acc[k] = 0.f;
+  for (int h = 0; h < G; ++h) acc[h] = 0.f;
   for (int tile = 0; tile < n_tiles; ++tile) {
     stash_tile();
     __syncthreads();
     if (tile + 1 < n_tiles) fetch_tile(a.v_codes, a.v_norm, tile + 1);
     expand_tile();
     __syncthreads();
-    const int n_in = min(kPTile, n_local - tile * kPTile);
-    for (int i = 0; i < n_in; ++i) {
-      const float yv = y_s[i][j];
+#pragma unroll 4
+    for (int i = 0; i < kPTile / 2; ++i) {
+      const int tok = (kPTile / 2) * th + i;
+      const float yv = y_s[tok][j];
+      const float* w = p_s[tile * kPTile + tok];
+      if constexpr (G % 4 == 0) {
 #pragma unroll
-      for (int k = 0; k < HH; ++k) {
-        const int h = 2 * k + hf;
-        if (h < G) acc[k] = fmaf(p_s[h][tile * kPTile + i], yv, acc[k]);
+        for (int h = 0; h < G; h += 4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(w + h);
+          acc[h] = fmaf(w4.x, yv, acc[h]);
+          acc[h + 1] = fmaf(w4.y, yv, acc[h + 1]);
+          acc[h + 2] = fmaf(w4.z, yv, acc[h + 2]);
+          acc[h + 3] = fmaf(w4.w, yv, acc[h + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc[h] = fmaf(w[h], yv, acc[h]);
       }
     }
     __syncthreads();
   }
+  // the two token halves meet in the decoded tile's buffer (free after the last barrier)
+  float* const half_s = &y_s[0][0];             // [G][kDim]
+  if (th == 1)
 #pragma unroll
-  for (int k = 0; k < HH; ++k) {
-    const int h = 2 * k + hf;
-    if (h >= G) continue;
-    float* part_p = a.ws_part + (static_cast<long long>(qbase + h) * a.max_chunks + chunk) * kPartStride;
-    part_p[4 + j] = acc[k];
-    if (j == 0) {
-      part_p[0] = stat_s[0][h];
-      part_p[1] = stat_s[1][h];
+    for (int h = 0; h < G; ++h) half_s[h * kDim + j] = acc[h];
+  __syncthreads();
+  if (th == 0)
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float* part_p = a.ws_part + (static_cast<long long>(qbase + h) * a.max_chunks + chunk) * kPartStride;
+      part_p[4 + j] = acc[h] + half_s[h * kDim + j];
+      if (j == 0) {
+        part_p[0] = stat_s[0][h];
+        part_p[1] = stat_s[1][h];
+      }
     }
-  }
 }
 
 }  // namespace
