@@ -75,8 +75,10 @@ def test_long_contexts_over_few_groups_merge_per_query_head(group):
     assert B.tq_get_last_device_error(book) == 0
 
 
-@pytest.mark.parametrize("k_bits,v_bits,qjl", [(2, 1, 128), (5, 4, 128), (4, 2, 128), (2, 3, 0)])
+@pytest.mark.parametrize("k_bits,v_bits,qjl", [(2, 1, 128), (5, 4, 128), (4, 2, 128), (2, 3, 0), (3, 2, 0)])
 def test_bit_width_variants(k_bits, v_bits, qjl):
+    # (4, 2, 128) and (3, 2, 0) have four MSE sign planes: key tiles built in two units, with and without the
+    # QJL plane in the second
     cfg = dict(n_kv=1, block_size=64, dtype="bf16", seed=5, log_uniform=None, outliers=2, outlier_scale=20.0)
     book, ref = books(k_bits, v_bits, qjl, seed=2)
     ctx = np.array([1100, 300], dtype=np.int32)
