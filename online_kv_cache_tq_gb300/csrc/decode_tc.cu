@@ -1318,9 +1318,12 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
           if (t == 0) {
             bool owe = true;                      // (a group inside this run has no other contributor)
             if (n_seg > 1) {
-              __threadfence();
-              owe = atomicAdd(a.ws_ticket + x.group, 1) == n_seg - 1;
-              if (owe) __threadfence();           // the other CTAs' partials are visible from here on
+              // one acquire-release add at GPU scope: it publishes this CTA's partials (every builder's
+              // stores precede it through the barrier above), and the CTA that completes the count sees
+              // every other contributor's
+              int prev;
+              asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(a.ws_ticket + x.group) : "memory");
+              owe = prev == n_seg - 1;
             }
             if (owe) {
               if (n_pend_s < kMaxPending) {
