@@ -14,7 +14,7 @@ from online_kv_cache_tq_gb300 import cache as C
 from online_kv_cache_tq_gb300 import workloads as W
 
 from parity_helpers import (attn_pairs, books, check_decode, check_decode_groups, decode, fill_cache, generator,
-                            host_cache, identity_table, run_boundary_groups)
+                            host_cache, identity_table, run_boundary_groups, quantize_into)
 
 pytestmark = pytest.mark.gpu
 
@@ -326,6 +326,36 @@ def test_fixed_and_run_time_shape_builds(k_bits, v_bits, norm_bits, block_size, 
                          [(b, h) for b in range(len(ctx)) for h in range(n_kv * group)])
     print("K%d V%d, %d-bit norms, %d-token blocks, G=%d: worst normalised error %.3g"
           % (k_bits, v_bits, norm_bits, block_size, group, worst))
+    assert B.tq_get_last_device_error(book) == 0
+
+
+@pytest.mark.parametrize("norm_bits", [32, 16])
+def test_extreme_magnitudes_and_sharp_softmax(norm_bits):
+    # tokens scaled log-uniformly over 1e-3 .. 1e3 (and a few zero vectors), queries 20x larger than the rest
+    # of the tests (scores in the hundreds: a sharp softmax): the piece scales of the query and weight operands
+    # and the running max of the merge against the oracle
+    n_kv, group, bs = 2, 8, 64
+    book, ref = books(3, 3, 128, seed=13, norm_bits=norm_bits)
+    ctx = np.array([700, 1500], dtype=np.int32)
+    table, _ = W.block_layout(ctx, bs, True, seed=13)
+    num_blocks = int(table.max()) + 1
+    cache = C.allocate_cache(book, num_blocks, n_kv)
+    g = generator(131)
+    rng = np.random.default_rng(131)
+    ones = np.ones((n_kv, 128))
+    for b, length in enumerate(ctx):
+        n = int(length)
+        factors = np.exp(rng.uniform(np.log(1e-3), np.log(1e3), size=(n, n_kv, 1)))
+        factors[rng.choice(n, size=3, replace=False)] = 0.0          # zero vectors
+        f = torch.as_tensor(factors, dtype=torch.float32, device="cuda")
+        k = (W.gaussian_tokens(n, ones, torch.float32, "cuda", g) * f).to(torch.bfloat16)
+        v = (W.gaussian_tokens(n, ones, torch.float32, "cuda", g) * f).to(torch.bfloat16)
+        quantize_into(book, cache, k, v, W.slots_for(table[b], np.arange(n), bs))
+    q = (W.queries(2, n_kv * group, torch.float32, "cuda", g) * 20.0).to(torch.bfloat16)
+    out = decode(book, cache, q, table, ctx, int(ctx.max()))
+    worst = check_decode(out, host_cache(cache), q, table, ctx, ref,
+                         [(b, h) for b in range(2) for h in range(n_kv * group)])
+    print("extreme magnitudes, %d-bit norms: worst normalised error %.3g" % (norm_bits, worst))
     assert B.tq_get_last_device_error(book) == 0
 
 
