@@ -224,6 +224,14 @@ __device__ __forceinline__ int cta_scan(int v, int* excl, int* warp_s) {
   return total;
 }
 
+struct MaxOp {
+  __device__ float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+struct SumOp {
+  __device__ float operator()(float a, float b) const { return a + b; }
+  __device__ float identity() const { return 0.f; }
+};
+
 // Per-warp totals of N values per thread over the eight builder warps (one
 // pair of barriers for all N): afterwards red[w * N + j] holds warp w's total
 // of value j.  Within a warp the value set halves at every shuffle step (lanes
@@ -261,6 +269,24 @@ __device__ __forceinline__ void warp_totals(const float (&v)[N], float* red, Op 
   builder_sync();
 }
 
+// The same for maxima: one warp-wide float max reduction per value
+// (redux.sync.max.f32), lane j then stores value j's total.
+template <int N>
+__device__ __forceinline__ void warp_totals(const float (&v)[N], float* red, MaxOp, bool* all = nullptr) {
+  static_assert(N <= 32, "at most 32 values");
+  const int lane = threadIdx.x & 31;
+  float r[N];
+#pragma unroll
+  for (int j = 0; j < N; ++j) asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r[j]) : "f"(v[j]));
+  if (all != nullptr) *all = builder_all(*all);  // the previous reduction's totals were read
+  else builder_sync();
+  float mine = r[0];
+#pragma unroll
+  for (int j = 1; j < N; ++j) mine = lane == j ? r[j] : mine;
+  if (lane < N) red[(threadIdx.x >> 5) * N + lane] = mine;
+  builder_sync();
+}
+
 // Total of value j over the four warps of builder half `hf`, in warp order.
 template <int N, typename Op>
 __device__ __forceinline__ float half_total(const float* red, int hf, int j, Op op) {
@@ -269,14 +295,6 @@ __device__ __forceinline__ float half_total(const float* red, int hf, int j, Op 
   for (int w = 1; w < 4; ++w) r = op(r, red[(4 * hf + w) * N + j]);
   return r;
 }
-struct MaxOp {
-  __device__ float operator()(float a, float b) const { return fmaxf(a, b); }
-  __device__ float identity() const { return -INFINITY; }
-};
-struct SumOp {
-  __device__ float operator()(float a, float b) const { return a + b; }
-  __device__ float identity() const { return 0.f; }
-};
 
 __device__ __forceinline__ int context_of(const DecodeArgs& a, int b) {
   int ctx = a.context_lens[b];
@@ -1085,8 +1103,19 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       // ---- softmax max over the chunk; B_V pieces of exp(s - m) n_v ----
       // (after a failed wait the loop reads stale but in-bounds norms, and every
       // builder leaves at the barrier that ANDs the flags)
-      for (int i = t; i < x.n_tiles * kTile; i += kBuilders)
-        mx[HG] = fmaxf(mx[HG], i < x.n_local && blk_ok[i >> bs_shift] ? norm_at(vn_s, i) : 0.f);
+      // The norm of a slot past the context or in a skipped block -- stale or
+      // uncopied bytes -- is set to 0 in place, so the weight loop below needs
+      // no validity test: such a slot's score is -inf, its exponential 0, and
+      // its weight 0 * 0.
+      for (int i = t; i < x.n_tiles * kTile; i += kBuilders) {
+        if (i < x.n_local && blk_ok[i >> bs_shift]) {
+          mx[HG] = fmaxf(mx[HG], norm_at(vn_s, i));
+        } else if (n16) {
+          reinterpret_cast<uint16_t*>(vn_s)[i] = 0;
+        } else {
+          reinterpret_cast<float*>(vn_s)[i] = 0.f;
+        }
+      }
       {
         // chunk max of the owned heads over this half's warps; value-norm max over all
         ok = ok && *abort == 0;
@@ -1119,31 +1148,28 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
         const float ib = 2.f * bit_inv_scale(i) * sv;
         constexpr float kLog2e = 1.4426950408889634f;
         const float2 l2e = make_float2(kLog2e, kLog2e);
-        const float2 nml = make_float2(-mq * kLog2e, -mq * kLog2e);   // (the same rounding for every token)
+        // (the same rounding for every token; a head without a valid token in
+        // the chunk has m = -inf and every score -inf: 2^(-inf) = 0, not nan)
+        const float nm = mq == -INFINITY ? 0.f : -mq * kLog2e;
+        const float2 nml = make_float2(nm, nm);
+        const float2 ib2 = make_float2(ib, ib);
+        float2 se2 = make_float2(0.f, 0.f), sw2 = make_float2(0.f, 0.f);   // sums of e and of e n_v ib
         const int units = x.n_tiles * 32 * G;
         for (int u = t; u < units; u += kBuilders) {
           const int tile = u / (32 * G);
           const int tl0 = tile * kTile + 32 * gq + i;           // tokens tl0 + 8 k
           const float4 sc = *reinterpret_cast<const float4*>(s0 + hq * CH + tile * kTile + kp0);
-          const bool blk_valid = blk_ok[tl0 >> bs_shift] != 0;   // (the four share a 32-token group)
           // exp(s - m) = 2^(s log2 e - m log2 e), two tokens per fused multiply-add
           const float2 a01 = __ffma2_rn(make_float2(sc.x, sc.y), l2e, nml);
           const float2 a23 = __ffma2_rn(make_float2(sc.z, sc.w), l2e, nml);
-          const float ak[4] = {a01.x, a01.y, a23.x, a23.y};
-          float w[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int tl = tl0 + 8 * k;
-            const bool valid = blk_valid && tl < x.n_local;
-            const float vn = norm_at(vn_s, tl);                  // (tl < CH: in bounds; selected below)
-            // (selects, not branches: the exponent of an invalid slot may be nan)
-            const float ex = ex2_approx(ak[k]);
-            const float e = valid && mq != -INFINITY ? ex : 0.f;
-            const float nvb = valid ? vn * ib : 0.f;
-            lw0 += e;
-            lw1 = fmaf(e, nvb, lw1);
-            w[k] = e * nvb;
-          }
+          const float2 e01 = make_float2(ex2_approx(a01.x), ex2_approx(a01.y));
+          const float2 e23 = make_float2(ex2_approx(a23.x), ex2_approx(a23.y));
+          const float2 n01 = __fmul2_rn(make_float2(norm_at(vn_s, tl0), norm_at(vn_s, tl0 + 8)), ib2);
+          const float2 n23 = __fmul2_rn(make_float2(norm_at(vn_s, tl0 + 16), norm_at(vn_s, tl0 + 24)), ib2);
+          const float2 w01 = __fmul2_rn(e01, n01), w23 = __fmul2_rn(e23, n23);
+          se2 = __fadd2_rn(se2, __fadd2_rn(e01, e23));
+          sw2 = __fadd2_rn(sw2, __fadd2_rn(w01, w23));
+          float w[4] = {w01.x, w01.y, w23.x, w23.y};
           uint8_t* rows = b_v + tile * L.no * 128;
 #pragma unroll
           for (int p = 0; p < kVPieces; ++p) {
@@ -1165,7 +1191,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
             }
           }
         }
-        lw1 *= 1.f / ib;                          // exact: ib is a power of two
+        lw0 = se2.x + se2.y;
+        lw1 = (sw2.x + sw2.y) * (1.f / ib);       // exact scaling: ib is a power of two
       }
       if (t == 0) sv_s = sv;
       // (no barrier: every builder's B_V pieces precede its first vfull arrival,
