@@ -159,6 +159,37 @@ def test_custom_scale_and_device_errors():
     assert B.tq_get_last_device_error(book) == 0
 
 
+@pytest.mark.parametrize("group", [1, 4, 8])
+def test_skipped_blocks_and_a_chunk_without_a_valid_slot(group):
+    # Table entries outside the cache are skipped (and recorded): the output is
+    # the attention over the remaining tokens, which the oracle gets from a table
+    # with those entries taken out.  Sequence 1 loses every block of its second
+    # 512-token chunk, so that chunk's item has no valid slot in any head.
+    n_kv = 2
+    cfg = dict(n_kv=n_kv, block_size=64, dtype="bf16", seed=20 + group, log_uniform=(0.1, 10.0), outliers=2,
+               outlier_scale=20.0)
+    book, ref = books(3, 3, 128, seed=7)
+    assert B.tq_decode_kernel_kind(book, n_kv * group, n_kv) == 1      # tensor-core partials
+    ctx = np.array([1300, 1100], dtype=np.int32)
+    table, num_blocks = W.block_layout(ctx, 64, True, seed=group)
+    g = generator(30 + group)
+    cache = fill_cache(book, cfg, ctx, table, g, chunk_tokens=1000)
+    q = W.queries(len(ctx), n_kv * group, torch.bfloat16, "cuda", g)
+    bad = table.copy()
+    bad[0, 3] = num_blocks + 5                   # one block past the cache
+    bad[1, 8:16] = -1                            # tokens 512 .. 1023: the whole second chunk
+    out = decode(book, cache, q, bad, ctx, 1300)
+    assert B.tq_get_last_device_error(book) == 2
+    assert np.all(np.isfinite(out))
+    kept = np.full_like(table, -1)
+    rows = [np.concatenate([table[0, :3], table[0, 4:21]]), np.concatenate([table[1, :8], table[1, 16:18]])]
+    for b, r in enumerate(rows):
+        kept[b, :len(r)] = r
+    kept_ctx = np.array([1300 - 64, 1100 - 512], dtype=np.int32)
+    pairs = [(b, h) for b in range(len(ctx)) for h in range(n_kv * group)]
+    check_decode(out, host_cache(cache), q, kept, kept_ctx, ref, pairs)
+
+
 def test_workspace_and_argument_checks():
     book, _ = books()
     cache = C.allocate_cache(book, 4, 1)
