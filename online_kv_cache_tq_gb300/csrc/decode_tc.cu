@@ -332,6 +332,7 @@ struct TcLayout {
   int off_bmse, off_bqjl, off_bv, off_s0, off_s1, off_sacc, off_kc, off_kq, off_kn, off_kr, off_vn, off_vc, smem_bytes;
 };
 
+constexpr int kHeadMergeThreads = 512;      // per-query-head merge: four quarters of 128 lanes
 constexpr int kValueSlot = 64;              // columns of one value slot (two sign planes)
 constexpr int kMaxValueSlots = 4;
 
@@ -418,23 +419,20 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
 
 }  // namespace
 
-// Merge the n_seg segments of one group (its G heads' entries at ent0 + s G +
-// h), divide by the softmax sum and back-rotate into out (seo-farm page §2:
-// out = R^T o_rot).  Called by every builder thread (lane, half); half h
-// merges the heads it owns, then each half sums 64 of the 128 terms of every
-// head's back-rotation.  Latency-bound: the loads of up to eight segments, and
-// all 64 loads of R a thread needs, are in flight at once.  Not inlined: it
-// runs about twice per CTA, and those loads must not take registers from the
-// per-tile loop.
-template <int G>
-__device__ __noinline__ void merge_segments(const float* ws_part, const float* R, float* out, int ent0,
-                                            int n_seg, int qbase, float* orot, float* s1, int half, int lane) {
-  constexpr int HG = half_heads(G);
-  constexpr int kBatch = 8;
-  float w[64];                                  // R[64 half + i][lane], loaded while the segments merge
+// R[64 half + i][lane], i < 64: the rows of R that thread (lane, half) needs for
+// the back-rotation (a handle constant: no launch writes it).
+__device__ __forceinline__ void load_r_half(const float* R, int half, int lane, float (&w)[64]) {
   const float* rp = R + (64 * half) * kDim + lane;
 #pragma unroll
   for (int i = 0; i < 64; ++i) w[i] = __ldg(rp + i * kDim);
+}
+
+// merge_segments (below) with the rows of R already in registers (load_r_half).
+template <int G>
+__device__ __forceinline__ void merge_segments_r(const float (&w)[64], const float* ws_part, float* out, int ent0,
+                                                 int n_seg, int qbase, float* orot, float* s1, int half, int lane) {
+  constexpr int HG = half_heads(G);
+  constexpr int kBatch = 8;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     if (h / HG != half) continue;
@@ -487,6 +485,22 @@ __device__ __noinline__ void merge_segments(const float* ws_part, const float* R
 #pragma unroll
     for (int h = 0; h < G; ++h) out[static_cast<long long>(qbase + h) * kDim + lane] = r[h] + s1[h * kTile + lane];
   builder_sync();
+}
+
+// Merge the n_seg segments of one group (its G heads' entries at ent0 + s G +
+// h), divide by the softmax sum and back-rotate into out (seo-farm page §2:
+// out = R^T o_rot).  Called by every builder thread (lane, half); half h
+// merges the heads it owns, then each half sums 64 of the 128 terms of every
+// head's back-rotation.  Latency-bound: the loads of up to eight segments, and
+// all 64 loads of R a thread needs, are in flight at once.  Not inlined: it
+// runs about twice per CTA, and those loads must not take registers from the
+// per-tile loop.
+template <int G>
+__device__ __noinline__ void merge_segments(const float* ws_part, const float* R, float* out, int ent0,
+                                            int n_seg, int qbase, float* orot, float* s1, int half, int lane) {
+  float w[64];                                  // loaded while the segments merge
+  load_r_half(R, half, lane, w);
+  merge_segments_r<G>(w, ws_part, out, ent0, n_seg, qbase, orot, s1, half, lane);
 }
 
 // One work item: (sequence b, KV head kvh, chunk) of a non-empty chunk.  The
@@ -1515,7 +1529,10 @@ __global__ void __launch_bounds__(kBuilders) merge_groups_kernel(DecodeArgs a) {
   const int g = blockIdx.x;
   const int b = g / a.n_kv, kvh = g - b * a.n_kv;
   const int qbase = b * a.n_q + kvh * G;
+  const int half = (threadIdx.x >> 7) & 1, lane = threadIdx.x & 127;
   const int ctx = context_of(a, b);
+  float w[64];                                    // (R is no output of the partials launch: loaded before the wait)
+  load_r_half(a.R, half, lane, w);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (ctx == 0) {
     for (int i = threadIdx.x; i < G * kDim; i += kBuilders) a.out[static_cast<long long>(qbase) * kDim + i] = 0.f;
@@ -1529,27 +1546,33 @@ __global__ void __launch_bounds__(kBuilders) merge_groups_kernel(DecodeArgs a) {
     for (int i = threadIdx.x; i < G * kDim; i += kBuilders) a.out[static_cast<long long>(qbase) * kDim + i] = 0.f;
     return;
   }
-  merge_segments<G>(a.ws_part, a.R, a.out, seg.base, seg.count, qbase, orot_s, half_s, (threadIdx.x >> 7) & 1,
-                    threadIdx.x & 127);
+  merge_segments_r<G>(w, a.ws_part, a.out, seg.base, seg.count, qbase, orot_s, half_s, half, lane);
 }
 
 // The merge as its own launch for a few (sequence, KV head) groups with many
-// segments each (long contexts over a small batch): one 256-thread CTA per
-// query head, whose two halves merge alternate segments side by side, so that
-// a head's merge is a few memory round trips long and the heads run on
-// different SMs.  Thread (lane, half) holds coordinate lane; then thread
-// (o = lane, half) sums 64 of the 128 terms of the back-rotation.
+// segments each (long contexts over a small batch): one 512-thread CTA per
+// query head, whose four quarters merge every fourth segment side by side with
+// sixteen segments' loads in flight each, so that a head's merge is about one
+// memory round trip long and the heads run on different SMs.  Thread
+// (lane, quarter) holds coordinate lane; then thread (o = lane, quarter) sums
+// 32 of the 128 terms of the back-rotation.
 template <int G>
-__global__ void __launch_bounds__(kBuilders) merge_heads_kernel(DecodeArgs a) {
-  constexpr int kBatch = 8;
-  __shared__ float ml_s[2];
-  __shared__ float acc_s[kTile];
+__global__ void __launch_bounds__(kHeadMergeThreads) merge_heads_kernel(DecodeArgs a) {
+  constexpr int kQ = kHeadMergeThreads / kTile;   // quarters of 128 lanes
+  constexpr int kBatch = 16;                      // a quarter's segment loads in flight at once
+  __shared__ float ml_s[kQ][2];
+  __shared__ float acc_s[kQ][kTile];
   __shared__ __align__(16) float orot_s[kTile];
   const int v = blockIdx.x;                       // query head b n_q + hq
   const int b = v / a.n_q;
   const int h = (v - b * a.n_q) % G;              // head within its group
   const int qbase = v - h;
-  const int t = threadIdx.x, half = t >> 7, lane = t & (kTile - 1);
+  const int t = threadIdx.x, qt = t / kTile, lane = t & (kTile - 1);
+  constexpr int kRows = kDim / kQ;                // rows of R per quarter
+  float w[kRows];                                 // R[kRows qt + i][lane] (no output of the partials launch:
+  const float* rp = a.R + (kRows * qt) * kDim + lane;   // loaded before the wait)
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) w[i] = __ldg(rp + i * kDim);
   const int ctx = context_of(a, b);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   float* const out = a.out + static_cast<long long>(v) * kDim;
@@ -1565,17 +1588,13 @@ __global__ void __launch_bounds__(kBuilders) merge_heads_kernel(DecodeArgs a) {
     if (t < kDim) out[t] = 0.f;
     return;
   }
-  float w[64];                                    // R[64 half + i][lane], loaded while the segments merge
-  const float* rp = a.R + (64 * half) * kDim + lane;
-#pragma unroll
-  for (int i = 0; i < 64; ++i) w[i] = __ldg(rp + i * kDim);
-  // this half's segments s = half, half + 2, ... as a running (m, l, acc)
+  // this quarter's segments s = qt, qt + kQ, ... as a running (m, l, acc)
   float m = -INFINITY, l = 0.f, acc = 0.f;
-  for (int s0 = half; s0 < seg.count; s0 += 2 * kBatch) {
+  for (int s0 = qt; s0 < seg.count; s0 += kQ * kBatch) {
     float pm[kBatch], pl[kBatch], pa[kBatch];
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
-      const int sg = s0 + 2 * k;
+      const int sg = s0 + kQ * k;
       const float* part = a.ws_part + (static_cast<long long>(seg.base) + static_cast<long long>(sg) * G + h) *
                                           kPartStride;
       const bool in = sg < seg.count;
@@ -1598,34 +1617,38 @@ __global__ void __launch_bounds__(kBuilders) merge_heads_kernel(DecodeArgs a) {
     }
     m = mn;
   }
-  // the two halves' sums, then o_rot = acc / l
-  if (half == 1) {
-    if (lane == 0) {
-      ml_s[0] = m;
-      ml_s[1] = l;
+  // the quarters' sums, then o_rot = acc / l
+  if (lane == 0) {
+    ml_s[qt][0] = m;
+    ml_s[qt][1] = l;
+  }
+  acc_s[qt][lane] = acc;
+  __syncthreads();
+  if (qt == 0) {
+    float mn = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) mn = fmaxf(mn, ml_s[q][0]);
+    float lt = 0.f, at = 0.f;
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      const float mq = ml_s[q][0];
+      const float sq = mq == -INFINITY ? 0.f : __expf(mq - mn);
+      lt = fmaf(ml_s[q][1], sq, lt);
+      at = fmaf(acc_s[q][lane], sq, at);
     }
-    acc_s[lane] = acc;
+    orot_s[lane] = lt > 0.f ? at / lt : 0.f;
   }
   __syncthreads();
-  if (half == 0) {
-    const float m1 = ml_s[0], l1 = ml_s[1];
-    const float mn = fmaxf(m, m1);
-    const float sa = m == -INFINITY ? 0.f : __expf(m - mn);
-    const float sb = m1 == -INFINITY ? 0.f : __expf(m1 - mn);
-    const float lt = fmaf(l, sa, l1 * sb);
-    orot_s[lane] = lt > 0.f ? fmaf(acc, sa, acc_s[lane] * sb) / lt : 0.f;
-  }
-  __syncthreads();
-  // out[o] = sum_i R[i][o] o_rot[i] (seo-farm page §2: out = R^T o_rot)
+  // out[o] = sum_i R[i][o] o_rot[i] (seo-farm page §2: out = R^T o_rot): quarter qt sums kRows of the terms
   float r = 0.f;
 #pragma unroll
-  for (int k = 0; k < 64; k += 4) {
-    const float4 o4 = *reinterpret_cast<const float4*>(orot_s + 64 * half + k);
+  for (int k = 0; k < kRows; k += 4) {
+    const float4 o4 = *reinterpret_cast<const float4*>(orot_s + kRows * qt + k);
     r = fmaf(w[k], o4.x, fmaf(w[k + 1], o4.y, fmaf(w[k + 2], o4.z, fmaf(w[k + 3], o4.w, r))));
   }
-  if (half == 1) acc_s[lane] = r;                 // (half 0 read acc_s before the last barrier)
+  acc_s[qt][lane] = r;                            // (quarter 0 read acc_s before the last barrier)
   __syncthreads();
-  if (half == 0) out[lane] = r + acc_s[lane];
+  if (qt == 0) out[lane] = (acc_s[0][lane] + acc_s[1][lane]) + (acc_s[2][lane] + acc_s[3][lane]);
 }
 
 template <int G>
@@ -1633,7 +1656,7 @@ cudaError_t launch_merge_g(const DecodeArgs& a, cudaStream_t stream) {
   const bool per_head = tc_merge_per_head(a);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(per_head ? a.batch * a.n_q : a.batch * a.n_kv);
-  cfg.blockDim = dim3(kBuilders);
+  cfg.blockDim = dim3(per_head ? kHeadMergeThreads : kBuilders);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
