@@ -1217,12 +1217,23 @@ __global__ void __launch_bounds__(kThreads, 2) attention_tc_kernel(DecodeArgs a,
       int last_slot = 0, last_wrap = 0;
       for (int tile = 0; tile < x.n_tiles && ok; ++tile) {
         uint32_t bw[4][2] = {};                   // [bit-plane][this thread's 32-token groups]
+        // (every 32-token group of the tile, inside the copied fields: a group
+        // past the context or in a skipped block gets weight 0)
+        if constexpr (BS > 0 && BS % 64 == 0) {
+          // the thread's two groups are consecutive words of one block's rows, at an even word: one 8-byte load
+          const int tl = tile * kTile + 32 * w0;
+          const uint32_t* src = vc_s + (tl >> bs_shift) * (vblock / 4) + ((tl & (bs - 1)) >> 5) + (lane << wpd_shift);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          // every 32-token group of the tile (inside the copied fields): a group
-          // past the context or in a skipped block gets weight 0
-          const int tl = tile * kTile + 32 * (w0 + c);
-          {
+          for (int p = 0; p < 4; ++p)
+            if (p < v_bits) {
+              const uint2 pw = *reinterpret_cast<const uint2*>(src + ((p * 128) << wpd_shift));
+              bw[p][0] = pw.x;
+              bw[p][1] = pw.y;
+            }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int tl = tile * kTile + 32 * (w0 + c);
             const uint32_t* src =
                 vc_s + (tl >> bs_shift) * (vblock / 4) + ((tl & (bs - 1)) >> 5) + (lane << wpd_shift);
 #pragma unroll
